@@ -1,0 +1,518 @@
+"""ORACLE -- test infrastructure only.
+
+A plain, slow CPU implementation of the tree-verification step, written from
+the SpecPilot pages' description and the synthetic model definitions, in
+fp64 with bf16 rounding at every kernel boundary of the model definition.
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import it.  It shares no code with the CUDA library and the
+product path never calls it.
+
+Sources followed (page title, section):
+  * "SpecPilot: AI Agent Framework Boosts Speculative Decoding 10.87x ...",
+    "(1) W12: Lossless 12-bit Weight Format" -- 12-bit code, exponent table,
+    sparse escape list, bit-exact restoration (``w12_*``; C in oracle.c).
+  * same page, "(2) Best-first Tree Verification for Hybrid Architectures" --
+    the target scores every node of a draft tree in one pass, each node seeing
+    its root path (``tree_info``, ``tree_attention``), and a recurrent state
+    that follows each root path (``linrec_literal``).
+  * same page, "(3) Two-Level Verification" and "SpecPilot Uses Agentic
+    Discovery ...", "Core Idea" (token forcing) -- only exact greedy target
+    verification accepts tokens (``accept``).
+  * "SpecPilot Uses Agentic Discovery ...", "Technical Mechanisms" -- a
+    drafter proposes candidates, the target verifies them in parallel.
+The dense decoder itself (RMSNorm, RoPE, GQA, SwiGLU) is the synthetic
+architecture the workloads name; the pages do not define it.
+
+Readings where the pages are silent are listed in the design doc; the ones that
+change arithmetic are restated in the docstrings below.
+
+Parity pins for every function live in ``tests/test_oracle_*.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass, field
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "_liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    src = os.path.join(_HERE, "oracle.c")
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(src):
+        tmp = _SO + ".tmp"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+                               "-o", tmp, src, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_SO)
+            vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+            L.or_bf16_to_double.restype = ctypes.c_double
+            L.or_bf16_to_double.argtypes = [ctypes.c_uint16]
+            L.or_double_to_bf16.restype = ctypes.c_uint16
+            L.or_double_to_bf16.argtypes = [ctypes.c_double]
+            L.or_round_bf16.restype = None
+            L.or_round_bf16.argtypes = [vp, i64, vp]
+            L.or_bf16_to_f64.restype = None
+            L.or_bf16_to_f64.argtypes = [vp, i64, vp]
+            L.or_w12_histogram.restype = None
+            L.or_w12_histogram.argtypes = [vp, i64, vp]
+            L.or_w12_table.restype = ctypes.c_int
+            L.or_w12_table.argtypes = [vp, vp]
+            L.or_w12_count_escapes.restype = i64
+            L.or_w12_count_escapes.argtypes = [vp, i64, vp, ctypes.c_int]
+            L.or_w12_pack.restype = i64
+            L.or_w12_pack.argtypes = [vp, i64, i64, vp, ctypes.c_int, vp, vp, vp, i64, vp]
+            L.or_w12_unpack.restype = ctypes.c_int
+            L.or_w12_unpack.argtypes = [vp, i64, i64, vp, ctypes.c_int, vp, vp, i64, vp]
+            L.or_w12_field.restype = ctypes.c_uint32
+            L.or_w12_field.argtypes = [vp, i64, i64, i64]
+            L.or_linear.restype = None
+            L.or_linear.argtypes = [vp, i64, i64, vp, i64, vp]
+            _lib = L
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ------------------------------------------------------------------ bf16 --
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact value of bf16 bit patterns."""
+    b = _c(bits, np.uint16)
+    out = np.empty(b.shape, dtype=np.float64)
+    lib().or_bf16_to_f64(b.ctypes.data, b.size, out.ctypes.data)
+    return out
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round fp64 values to bf16 (nearest, ties to even); returns bit patterns."""
+    a = _c(x, np.float64)
+    out = np.empty(a.shape, dtype=np.uint16)
+    lib().or_round_bf16(a.ctypes.data, a.size, out.ctypes.data)
+    return out
+
+
+# ------------------------------------------------------------------- W12 --
+
+@dataclass
+class W12:
+    """A packed tensor in the W12 layout described in oracle.c."""
+    N: int
+    K: int
+    table: np.ndarray      # uint8 [n_table] ascending exponents
+    words: np.ndarray      # uint32 [N*K*3/8]
+    esc_idx: np.ndarray    # uint32 [n_esc], increasing flat index
+    esc_val: np.ndarray    # uint16 [n_esc], bf16 bits
+    row_ptr: np.ndarray    # uint32 [N+1]
+
+    @property
+    def n_table(self) -> int:
+        return int(self.table.size)
+
+    @property
+    def n_esc(self) -> int:
+        return int(self.esc_idx.size)
+
+
+def w12_histogram(w: np.ndarray) -> np.ndarray:
+    a = _c(w, np.uint16)
+    h = np.zeros(256, dtype=np.uint64)
+    lib().or_w12_histogram(a.ctypes.data, a.size, h.ctypes.data)
+    return h
+
+
+def w12_table(hist: np.ndarray) -> np.ndarray:
+    """The 15 most frequent exponents (ties -> smaller exponent), ascending."""
+    h = _c(hist, np.uint64)
+    t = np.zeros(16, dtype=np.uint8)
+    n = lib().or_w12_table(h.ctypes.data, t.ctypes.data)
+    return t[:n].copy()
+
+
+def w12_pack(W: np.ndarray, table: np.ndarray | None = None) -> W12:
+    W = _c(W, np.uint16)
+    N, K = W.shape
+    if table is None:
+        table = w12_table(w12_histogram(W))
+    t16 = np.zeros(16, dtype=np.uint8)
+    t16[: table.size] = table
+    n_esc = int(lib().or_w12_count_escapes(W.ctypes.data, W.size, t16.ctypes.data, int(table.size)))
+    words = np.empty(N * K * 3 // 8, dtype=np.uint32)
+    esc_idx = np.empty(max(n_esc, 1), dtype=np.uint32)
+    esc_val = np.empty(max(n_esc, 1), dtype=np.uint16)
+    row_ptr = np.empty(N + 1, dtype=np.uint32)
+    got = lib().or_w12_pack(W.ctypes.data, N, K, t16.ctypes.data, int(table.size), words.ctypes.data,
+                            esc_idx.ctypes.data, esc_val.ctypes.data, max(n_esc, 1), row_ptr.ctypes.data)
+    if got < 0:
+        raise ValueError(f"w12_pack failed ({got}) for shape {W.shape}")
+    assert got == n_esc
+    return W12(N, K, table.astype(np.uint8).copy(), words, esc_idx[:n_esc].copy(), esc_val[:n_esc].copy(), row_ptr)
+
+
+def w12_unpack(p: W12) -> np.ndarray:
+    W = np.empty((p.N, p.K), dtype=np.uint16)
+    t16 = np.zeros(16, dtype=np.uint8)
+    t16[: p.n_table] = p.table
+    ei = _c(p.esc_idx if p.n_esc else np.zeros(1, np.uint32), np.uint32)
+    ev = _c(p.esc_val if p.n_esc else np.zeros(1, np.uint16), np.uint16)
+    rc = lib().or_w12_unpack(_c(p.words, np.uint32).ctypes.data, p.N, p.K, t16.ctypes.data, p.n_table,
+                             ei.ctypes.data, ev.ctypes.data, p.n_esc, W.ctypes.data)
+    if rc != 0:
+        raise ValueError("w12_unpack: bad shape")
+    return W
+
+
+def w12_field(p: W12, n: int, k: int) -> int:
+    """The stored 12-bit field (sign<<11 | code<<7 | mantissa) of weight (n, k)."""
+    w = _c(p.words, np.uint32)
+    return int(lib().or_w12_field(w.ctypes.data, n, k, p.K))
+
+
+# ---------------------------------------------------------------- linear --
+
+def linear(x: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """y = x W^T in fp64, each output summed in k order.  x: fp64 [M][K]
+    (or bf16 bits, converted exactly), W: bf16 bits [N][K]."""
+    if x.dtype == np.uint16:
+        x = bf16_to_f64(x)
+    x = _c(x, np.float64)
+    W = _c(W, np.uint16)
+    M, K = x.shape
+    N, K2 = W.shape
+    assert K == K2
+    y = np.empty((M, N), dtype=np.float64)
+    if M and N:
+        lib().or_linear(x.ctypes.data, M, K, W.ctypes.data, N, y.ctypes.data)
+    return y
+
+
+def linear_bf16(x: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """A GEMM kernel boundary: bf16(x W^T)."""
+    return round_bf16(linear(x, W))
+
+
+# -------------------------------------------------------------- layers ----
+
+def rmsnorm(x_bits: np.ndarray, gamma_bits: np.ndarray, eps: float) -> np.ndarray:
+    """bf16( (x / sqrt(mean(x^2) + eps)) * gamma ), row-wise."""
+    x = bf16_to_f64(x_bits)
+    g = bf16_to_f64(gamma_bits)
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return round_bf16((x * r) * g)
+
+
+def rope_angles(positions: np.ndarray, hd: int, base: float) -> np.ndarray:
+    """theta[m][d] = pos[m] * base^(-2d/hd), d < hd/2 (rotate-half pairing d, d+hd/2)."""
+    d = np.arange(hd // 2, dtype=np.float64)
+    inv = base ** (-2.0 * d / hd)
+    return np.asarray(positions, dtype=np.float64)[:, None] * inv[None, :]
+
+
+def rope(x_bits: np.ndarray, positions: np.ndarray, base: float) -> np.ndarray:
+    """Rotate-half RoPE of x [M][nh][hd] at per-row positions; bf16 out."""
+    x = bf16_to_f64(x_bits)
+    hd = x.shape[-1]
+    th = rope_angles(positions, hd, base)[:, None, :]
+    c, s = np.cos(th), np.sin(th)
+    a, b = x[..., : hd // 2], x[..., hd // 2:]
+    return round_bf16(np.concatenate([a * c - b * s, b * c + a * s], axis=-1))
+
+
+def silu_mul(g_bits: np.ndarray, u_bits: np.ndarray) -> np.ndarray:
+    g = bf16_to_f64(g_bits)
+    u = bf16_to_f64(u_bits)
+    return round_bf16(g / (1.0 + np.exp(-g)) * u)
+
+
+def residual(x_bits: np.ndarray, y_bits: np.ndarray) -> np.ndarray:
+    return round_bf16(bf16_to_f64(x_bits) + bf16_to_f64(y_bits))
+
+
+# ------------------------------------------------------------------ tree --
+
+@dataclass
+class TreeInfo:
+    valid: bool
+    depth: np.ndarray   # int32 [M]
+    anc: np.ndarray     # bool [M][M]; anc[i][j] = j is i or an ancestor of i
+
+
+def tree_info(parents: np.ndarray) -> TreeInfo:
+    """Validate a parent array (root at 0 with parent -1, parent[i] < i) and
+    derive depths and ancestor sets."""
+    p = np.asarray(parents, dtype=np.int64)
+    M = p.size
+    valid = M >= 1 and p[0] == -1 and all(0 <= p[i] < i for i in range(1, M))
+    depth = np.zeros(M, dtype=np.int32)
+    anc = np.zeros((M, M), dtype=bool)
+    if valid:
+        for i in range(M):
+            j = i
+            while j >= 0:
+                anc[i, j] = True
+                j = p[j]
+            depth[i] = anc[i].sum() - 1
+    return TreeInfo(bool(valid), depth, anc)
+
+
+def tree_attention(q_bits, k_prefix_bits, v_prefix_bits, k_new_bits, v_new_bits, anc, ctx):
+    """Tree-masked GQA attention, softmax in fp64, bf16 out.
+
+    q: [M][Hq][hd]; k/v prefix: [Hkv][>=ctx][hd] (first ctx used);
+    k/v new: [M][Hkv][hd] (node j's key/value); anc: [M][M] bool.
+    Node i attends to every prefix position and to the nodes j with
+    anc[i][j] (its root path, itself included).  q head h reads kv head
+    h // (Hq/Hkv).  Scores are q.k / sqrt(hd)."""
+    q = bf16_to_f64(q_bits)
+    M, Hq, hd = q.shape
+    Hkv = k_new_bits.shape[1]
+    G = Hq // Hkv
+    kp = bf16_to_f64(k_prefix_bits[:, :ctx])
+    vp = bf16_to_f64(v_prefix_bits[:, :ctx])
+    kn = bf16_to_f64(k_new_bits)
+    vn = bf16_to_f64(v_new_bits)
+    out = np.empty((M, Hq, hd), dtype=np.float64)
+    scale = 1.0 / np.sqrt(hd)
+    for h in range(Hq):
+        g = h // G
+        keys = np.concatenate([kp[g], kn[:, g, :]], axis=0)      # [ctx+M][hd]
+        vals = np.concatenate([vp[g], vn[:, g, :]], axis=0)
+        s = (q[:, h, :] @ keys.T) * scale                          # [M][ctx+M]
+        mask = np.concatenate([np.ones((M, ctx), dtype=bool), anc], axis=1)
+        s = np.where(mask, s, -np.inf)
+        s = s - s.max(axis=1, keepdims=True)
+        e = np.exp(s)
+        pr = e / e.sum(axis=1, keepdims=True)
+        out[:, h, :] = pr @ vals
+    return round_bf16(out)
+
+
+def phi(x: np.ndarray) -> np.ndarray:
+    """Feature map of the linear-recurrent layer: elu(x) + 1."""
+    return np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+
+
+def linrec_literal(q_bits, k_bits, v_bits, S0, z0, parents, eps):
+    """Tree linear recurrence, literal per-node state.
+
+    Per head: S_i = S_parent(i) + phi(k_i) v_i^T, z_i = z_parent(i) + phi(k_i),
+    with (S0, z0) the state before the root; output
+    o_i = S_i^T phi(q_i) / (z_i . phi(q_i) + eps), rounded to bf16.
+    q/k/v: bf16 [M][nh][hd]; S0: [nh][hd][hd] (row = key dim, column = value
+    dim); z0: [nh][hd].  Returns (o bits [M][nh][hd], S nodes [M][nh][hd][hd],
+    z nodes [M][nh][hd])."""
+    q = phi(bf16_to_f64(q_bits))
+    k = phi(bf16_to_f64(k_bits))
+    v = bf16_to_f64(v_bits)
+    S0 = np.asarray(S0, dtype=np.float64)
+    z0 = np.asarray(z0, dtype=np.float64)
+    M, nh, hd = q.shape
+    S = np.empty((M, nh, hd, hd))
+    z = np.empty((M, nh, hd))
+    o = np.empty((M, nh, hd))
+    for i in range(M):
+        Sp = S0 if parents[i] < 0 else S[parents[i]]
+        zp = z0 if parents[i] < 0 else z[parents[i]]
+        S[i] = Sp + k[i][:, :, None] * v[i][:, None, :]
+        z[i] = zp + k[i]
+        num = np.einsum("hab,ha->hb", S[i], q[i])
+        den = np.einsum("ha,ha->h", z[i], q[i]) + eps
+        o[i] = num / den[:, None]
+    return round_bf16(o), S, z
+
+
+# -------------------------------------------------------- argmax / accept --
+
+def argmax_margin(logits: np.ndarray):
+    """Per row: index of the largest logit (smallest index on ties) and the
+    gap between the largest and the second largest value."""
+    idx = np.argmax(logits, axis=1).astype(np.int32)
+    part = np.partition(logits, -2, axis=1)
+    margin = part[:, -1] - part[:, -2]
+    return idx, margin
+
+
+@dataclass
+class Accept:
+    accepted_len: int
+    accepted_tokens: list
+    bonus: int
+    path: list          # node ids root .. deepest accepted node
+    last: int           # deepest accepted node
+
+
+def accept(tokens, parents, argmax) -> Accept:
+    """Greedy longest accepted path.  Node i >= 1 matches when its token equals
+    the target's argmax at its parent; a node is accepted when it and all its
+    ancestors match (the root always is).  The deepest accepted node wins,
+    the smallest index among equally deep ones.  The accepted tokens are the
+    path's tokens below the root; the bonus is the target's argmax there."""
+    M = len(parents)
+    ti = tree_info(parents)
+    ok = [False] * M
+    ok[0] = True
+    for i in range(1, M):
+        ok[i] = ok[parents[i]] and int(tokens[i]) == int(argmax[parents[i]])
+    best = 0
+    for i in range(M):
+        if ok[i] and ti.depth[i] > ti.depth[best]:
+            best = i
+    path = []
+    j = best
+    while j >= 0:
+        path.append(j)
+        j = parents[j]
+    path.reverse()
+    return Accept(int(ti.depth[best]), [int(tokens[j]) for j in path[1:]], int(argmax[best]), path, best)
+
+
+# ----------------------------------------------------------------- model --
+
+@dataclass
+class LayerState:
+    """Per-layer cache of one request: KV prefix (attention layers) or the
+    recurrent state (linear-recurrent layers)."""
+    k: np.ndarray | None = None    # bf16 bits [Hkv][cap][hd]
+    v: np.ndarray | None = None
+    S: np.ndarray | None = None    # fp64 [nh][hd][hd]
+    z: np.ndarray | None = None    # fp64 [nh][hd]
+
+
+@dataclass
+class Request:
+    tokens: np.ndarray             # int32 [M]
+    parents: np.ndarray            # int32 [M]
+    ctx: int
+    layers: list = field(default_factory=list)   # list[LayerState]
+
+
+@dataclass
+class ForwardOut:
+    logits: np.ndarray             # fp64 [sum M][V]
+    argmax: np.ndarray
+    margin: np.ndarray
+    new_kv: list                   # per layer: (k bits [M][Hkv][hd], v bits) or (phi k, v) rows
+    infos: list                    # TreeInfo per request
+
+
+def forward(shape, weights, requests: list) -> ForwardOut:
+    """One verify forward over the draft trees of all requests.
+
+    Every GEMM sees the rows of all requests together (rows never interact);
+    attention and recurrence act per request.  Layer order (pre-norm):
+      h = x + O(mix(RMSNorm(x)));  x' = h + down(silu(gate(n)) * up(n)), n = RMSNorm(h)
+    with mix = tree attention (RoPE on q,k at position ctx + depth) or the
+    tree linear recurrence.  Final RMSNorm then lm_head."""
+    hd, Hq, Hkv, eps = shape.hd, shape.Hq, shape.Hkv, shape.eps
+    infos = [tree_info(r.parents) for r in requests]
+    for inf in infos:
+        if not inf.valid:
+            raise ValueError("invalid parent array")
+    seg = np.cumsum([0] + [len(r.tokens) for r in requests])
+    tokens = np.concatenate([np.asarray(r.tokens, dtype=np.int64) for r in requests])
+    Mt = tokens.size
+    x = weights.embed_rows(tokens)                                      # bf16 [Mt][H]
+    pos = np.concatenate([r.ctx + inf.depth for r, inf in zip(requests, infos)])
+    new_kv = []
+    for l, kind in enumerate(shape.layer_kinds):
+        xn = rmsnorm(x, weights.norm(l, "attn"), eps)
+        if kind == "attn":
+            q = linear_bf16(xn, weights.layer(l, "wq")).reshape(Mt, Hq, hd)
+            k = linear_bf16(xn, weights.layer(l, "wk")).reshape(Mt, Hkv, hd)
+            v = linear_bf16(xn, weights.layer(l, "wv")).reshape(Mt, Hkv, hd)
+            q = rope(q, pos, shape.rope_base)
+            k = rope(k, pos, shape.rope_base)
+            att = np.empty((Mt, Hq, hd), dtype=np.uint16)
+            for r, req in enumerate(requests):
+                a, b = seg[r], seg[r + 1]
+                st = req.layers[l]
+                att[a:b] = tree_attention(q[a:b], st.k, st.v, k[a:b], v[a:b], infos[r].anc, req.ctx)
+            new_kv.append((k, v))
+        else:
+            nh = shape.H // hd
+            q = linear_bf16(xn, weights.layer(l, "wq")).reshape(Mt, nh, hd)
+            k = linear_bf16(xn, weights.layer(l, "wk")).reshape(Mt, nh, hd)
+            v = linear_bf16(xn, weights.layer(l, "wv")).reshape(Mt, nh, hd)
+            att = np.empty((Mt, nh, hd), dtype=np.uint16)
+            for r, req in enumerate(requests):
+                a, b = seg[r], seg[r + 1]
+                st = req.layers[l]
+                att[a:b], _, _ = linrec_literal(q[a:b], k[a:b], v[a:b], st.S, st.z, req.parents, shape.rec_eps)
+            new_kv.append((k, v))
+        o = linear_bf16(att.reshape(Mt, -1), weights.layer(l, "wo"))
+        h = residual(x, o)
+        hn = rmsnorm(h, weights.norm(l, "mlp"), eps)
+        g = linear_bf16(hn, weights.layer(l, "w_gate"))
+        u = linear_bf16(hn, weights.layer(l, "w_up"))
+        a_ = silu_mul(g, u)
+        d = linear_bf16(a_, weights.layer(l, "w_down"))
+        x = residual(h, d)
+    xf = rmsnorm(x, weights.final_norm(), eps)
+    logits = linear(xf, weights.lm_head())
+    idx, margin = argmax_margin(logits)
+    return ForwardOut(logits, idx, margin, new_kv, infos)
+
+
+def commit(shape, requests: list, out: ForwardOut, accepts: list) -> list:
+    """State after acceptance, per request: for attention layers the K/V of
+    the root and the accepted path nodes land at positions ctx + depth (the
+    prefix grows by accepted_len + 1); for recurrent layers the state becomes
+    the accepted node's state (root path included).  Returns new Requests
+    with ctx advanced (tokens/parents left empty)."""
+    seg = np.cumsum([0] + [len(r.tokens) for r in requests])
+    res = []
+    for r, (req, acc) in enumerate(zip(requests, accepts)):
+        a = seg[r]
+        layers = []
+        for l, kind in enumerate(shape.layer_kinds):
+            st = req.layers[l]
+            kk, vv = out.new_kv[l]
+            if kind == "attn":
+                K = st.k.copy()
+                V = st.v.copy()
+                for d, node in enumerate(acc.path):
+                    K[:, req.ctx + d, :] = kk[a + node]
+                    V[:, req.ctx + d, :] = vv[a + node]
+                layers.append(LayerState(k=K, v=V))
+            else:
+                S = np.asarray(st.S, dtype=np.float64).copy()
+                z = np.asarray(st.z, dtype=np.float64).copy()
+                kf = phi(bf16_to_f64(kk))
+                vf = bf16_to_f64(vv)
+                for node in acc.path:
+                    S += kf[a + node][:, :, None] * vf[a + node][:, None, :]
+                    z += kf[a + node]
+                layers.append(LayerState(S=S, z=z))
+        res.append(Request(np.zeros(0, np.int32), np.zeros(0, np.int32), req.ctx + acc.accepted_len + 1, layers))
+    return res
+
+
+def verify(shape, weights, requests: list):
+    """forward + greedy acceptance per request + committed state."""
+    out = forward(shape, weights, requests)
+    seg = np.cumsum([0] + [len(r.tokens) for r in requests])
+    accepts = [accept(req.tokens, req.parents, out.argmax[seg[i]:seg[i + 1]]) for i, req in enumerate(requests)]
+    return out, accepts, commit(shape, requests, out, accepts)
+
+
+def tiny_forward(W1, Wlm, act_bits):
+    """Tiny verify model: y = bf16(a W1^T), logits = y Wlm^T (fp64)."""
+    y = linear_bf16(act_bits, W1)
+    return linear(y, Wlm)
