@@ -1,0 +1,281 @@
+/*
+ * sdv -- tree verification with lossless 12-bit weights on one GB300.
+ *
+ * C ABI of the library libsdv.so.  Every pointer is a DEVICE pointer unless
+ * its name ends in _host.  Streams are passed as `void*` holding a
+ * cudaStream_t (NULL = legacy default stream).  Every function returns an
+ * `int` status (SD_OK = 0); host-checkable argument errors are reported
+ * synchronously, data errors found on the device (a bad parent array, a token
+ * outside the vocabulary, a full cache, a wait that timed out) are recorded in
+ * a device status word and never trap.  The caller owns every buffer it
+ * passes; the library never frees caller memory.  sd_last_error() returns a
+ * text for the last failing call on this thread.
+ *
+ * The pages this library follows:
+ *   [W12]  "SpecPilot: AI Agent Framework Boosts Speculative Decoding 10.87x
+ *          for Qwen3.8-27B", section "(1) W12: Lossless 12-bit Weight Format".
+ *   [TREE] same page, "(2) Best-first Tree Verification for Hybrid
+ *          Architectures"; "SpecPilot Uses Agentic Discovery to Push
+ *          Speculative Decoding to 10.87x", "Core Idea" (the drafter proposes a
+ *          block, the target verifies it in one parallel pass).
+ *   [EXACT] first page, "(3) Two-Level Verification": only the exact target
+ *          verification accepts tokens; second page "Core Idea", item 4
+ *          (token forcing: outputs equal the stock greedy outputs).
+ */
+#ifndef SDV_H
+#define SDV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status -- */
+enum {
+  SD_OK = 0,
+  SD_ERR_INVALID_ARG = 1,  /* a host-side argument is wrong */
+  SD_ERR_UNSUPPORTED = 2,  /* shape outside what the kernels handle (N%16, K%64, M>64 per request ...) */
+  SD_ERR_CUDA = 3,         /* a CUDA runtime call failed (text in sd_last_error) */
+  SD_ERR_OOM = 4,          /* device allocation failed */
+  SD_ERR_BAD_TREE = 5,     /* device: parent array not a tree rooted at node 0 with parent[i] < i */
+  SD_ERR_TIMEOUT = 6,      /* device: a bounded wait gave up */
+  SD_ERR_CAPACITY = 7,     /* device: ctx + nodes exceeds the cache capacity / page table / RoPE table */
+  SD_ERR_BAD_TOKEN = 8,    /* device: a token outside [0, vocab) */
+  SD_ERR_WORKSPACE = 9     /* caller workspace smaller than the size query returned */
+};
+
+const char* sd_last_error(void);
+const char* sd_version(void);
+
+/* ---------------------------------------------------------------- W12 -- */
+/* [W12] Each bf16 weight is stored in 12 bits: sign, 7-bit mantissa and a
+ * 4-bit code into a per-tensor table of the 15 most frequent exponents
+ * (count descending, ties to the smaller exponent, stored in ascending
+ * exponent order).  Code 15 marks an escape; the escaped weight's exact bf16
+ * bits are kept in a side list sorted by flat index n*K+k, with a CSR row
+ * pointer.  Unpacking restores every bf16 bit pattern exactly (NaN payloads,
+ * infinities, zeros and subnormals included).
+ *
+ * Layout (requires N % 16 == 0 and K % 64 == 0): rows form strips of 16,
+ * columns super-tiles of 64 split into four 16-wide sub-tiles.  The words of
+ * strip s, super-tile t are the 384 u32 at offset (s*(K/64)+t)*384, ordered
+ * [plane p = 0..2][lane 0..31][sub-tile j = 0..3].  Lane 4g+q holds the
+ * tensor-core A fragment of its sub-tile: pair 0 = W[g][2q..2q+1], pair 1 =
+ * W[g+8][2q..2q+1], pair 2 = W[g][2q+8..2q+9], pair 3 = W[g+8][2q+8..2q+9]
+ * (rows and columns relative to the sub-tile).  With f = sign<<11 | code<<7 |
+ * mantissa, plane p (p < 3) stores pair p as f&0x7FF with the sign in bit 15
+ * of each 16-bit half; pair 3's three nibbles fill bits 11..14 / 27..30 of
+ * planes 0, 1, 2.  An escaped weight stores code 15, sign 0, mantissa 0. */
+
+typedef struct {
+  int64_t N, K;             /* rows (outputs), columns (inputs) */
+  uint8_t table[16];        /* exponents of codes 0..n_table-1, ascending; rest 0 */
+  int32_t n_table;          /* <= 15 */
+  int32_t affine;           /* 1 if table[c] == table[0] + c for all c < n_table
+                               and table[0] + 15 <= 254 (fast decode path) */
+  int64_t n_escapes;
+} w12_meta;
+
+typedef struct {
+  int64_t N, K;
+  const uint32_t* words;    /* device, w12_words_count(N,K) u32 */
+  const uint32_t* esc_idx;  /* device [n_escapes], increasing */
+  const uint16_t* esc_val;  /* device [n_escapes], bf16 bits */
+  const uint32_t* row_ptr;  /* device [N+1] */
+  int64_t n_escapes;
+  uint8_t table[16];
+  int32_t n_table;
+  int32_t affine;
+} w12_tensor;
+
+/* Number of u32 words of a packed N x K tensor (N*K*3/8). */
+int64_t w12_words_count(int64_t N, int64_t K);
+
+/* Histogram of the exponents of w[N][K] (bf16 bits, row-major, device) and
+ * the code table.  Fills meta (including n_escapes); synchronises `stream`.
+ * Errors: SD_ERR_UNSUPPORTED if N%16 or K%64 or N*K >= 2^32, SD_ERR_CUDA. */
+int w12_pack_analyze(const uint16_t* w, int64_t N, int64_t K, w12_meta* meta, void* stream);
+
+/* Encode w into the W12 layout using meta from w12_pack_analyze.
+ * row_src (optional, device int32[N]): packed row n is taken from row
+ * row_src[n] of w; it must be a permutation of 0..N-1 (the histogram is
+ * permutation-invariant).  Escape indices refer to packed rows.  Outputs are
+ * caller-allocated: words[w12_words_count], esc_idx/esc_val[meta->n_escapes],
+ * row_ptr[N+1].  Allocates and frees its own scratch (stream-ordered);
+ * asynchronous on `stream`. */
+int w12_pack_encode(const uint16_t* w, const int32_t* row_src, const w12_meta* meta, uint32_t* words,
+                    uint32_t* esc_idx, uint16_t* esc_val, uint32_t* row_ptr, void* stream);
+
+/* Restore the bf16 tensor [N][K] (bit-exact).  Asynchronous. */
+int w12_unpack(const w12_tensor* t, uint16_t* w_out, void* stream);
+
+/* ------------------------------------------------ fused W12 linear -- */
+/* [W12] y[m][n] = bf16( sum_k x[m][k] * W[n][k] ), fp32 accumulation, with
+ * the weights decoded in registers straight from the packed words (they
+ * cross HBM once, 1.5 bytes each) and the escapes added in the epilogue.
+ * x: bf16 [M][K] row-major, 16-byte aligned; y: bf16 [M][N] row-major.
+ * 1 <= M <= 256.  workspace: caller-owned device scratch of
+ * sd_w12_linear_workspace(N, K, M) bytes, 256-byte aligned; it needs no
+ * initialisation (the call clears what it must).  Errors: SD_ERR_UNSUPPORTED
+ * (shape), SD_ERR_WORKSPACE, SD_ERR_CUDA. */
+size_t sd_w12_linear_workspace(int64_t N, int64_t K, int32_t M);
+int sd_w12_linear(const w12_tensor* W, const uint16_t* x, int32_t M, uint16_t* y, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------ tree helpers -- */
+/* [TREE] Validate one draft tree (parents[0] == -1, 0 <= parents[i] < i,
+ * M <= 64) and derive per node the ancestor bitmask anc[i] = anc[parent[i]]
+ * | 1<<i, the depth and the position ctx + depth.  On a bad tree, *status is
+ * set to SD_ERR_BAD_TREE and anc[i] = 1<<i, depth = 0.  All device. */
+int sd_tree_info(const int32_t* parents, int32_t M, int32_t ctx, uint64_t* anc, int32_t* depth, int32_t* pos,
+                 int32_t* status, void* stream);
+
+/* [EXACT] Greedy acceptance.  Node i >= 1 matches when tokens[i] ==
+ * argmax[parents[i]]; a node is accepted when it and all its ancestors match
+ * (the root always is).  The deepest accepted node d* wins (smallest index on
+ * ties); accepted_len = depth(d*), accepted_tokens[0..len) = tokens on the
+ * path below the root, bonus = argmax[d*], path[0..len] = node ids root..d*.
+ * All device; path may be NULL.  A bad tree sets *status = SD_ERR_BAD_TREE,
+ * accepted_len = 0 and bonus = -1. */
+int sd_accept(const int32_t* tokens, const int32_t* parents, const int32_t* argmax, int32_t M,
+              int32_t* accepted_len, int32_t* accepted_tokens, int32_t* bonus, int32_t* path, int32_t* status,
+              void* stream);
+
+/* -------------------------------------------------------- tiny verify -- */
+/* One linear layer and an lm_head: logits = (bf16(act W1^T)) Wlm^T, argmax
+ * per node in fp32, then greedy acceptance over the tree.  act: bf16 [M][K];
+ * logits (optional): bf16 [M][V]; argmax (optional) int32 [M].  M <= 64.
+ * workspace: sd_tiny_workspace(W1->N, W1->K, Wlm->N, M) bytes. */
+size_t sd_tiny_workspace(int64_t N1, int64_t K, int64_t V, int32_t M);
+int sd_tiny_verify(const w12_tensor* W1, const w12_tensor* Wlm, const uint16_t* act, const int32_t* tokens,
+                   const int32_t* parents, int32_t M, int32_t* accepted_len, int32_t* accepted_tokens,
+                   int32_t* bonus, uint16_t* logits, int32_t* argmax, int32_t* status, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------- model -- */
+/* Decoder whose every linear weight is W12.  Per layer (pre-norm):
+ *   h = x + O(mix(RMSNorm(x))),  x' = h + down(silu(gate(n)) * up(n)), n = RMSNorm(h)
+ * mix = tree-masked GQA attention with rotate-half RoPE at position
+ * ctx + depth (layer_kind 0) or the tree linear recurrence (layer_kind 1):
+ *   S_i = S_parent + phi(k_i) v_i^T, z_i = z_parent + phi(k_i),
+ *   o_i = S_i^T phi(q_i) / (z_i . phi(q_i) + rec_eps), phi = elu + 1.
+ * Then a final RMSNorm and the lm_head.  bf16 activations between kernels,
+ * fp32 inside them. */
+
+typedef struct {
+  int32_t n_layers, hidden, inter, n_q_heads, n_kv_heads, head_dim, vocab;
+  float rms_eps, rope_base, rec_eps;
+  const int8_t* layer_kind_host; /* [n_layers]: 0 attention, 1 linear recurrent (copied) */
+  int32_t max_rows;              /* max tree nodes per call summed over requests (<= 256) */
+  int32_t max_requests;          /* max requests per sd_verify_batch call */
+  int32_t max_positions;         /* RoPE table length: > largest ctx + depth used */
+} sd_model_config;
+
+/* Weight row orders the kernels expect (build them with w12_pack_encode's
+ * row_src, see sd_model_row_map):
+ *   qkv     = [q heads; k heads; v heads] rows, hidden columns.  Within each
+ *             q or k head of 128 rows, strip i (16 rows) holds dims 8i..8i+7
+ *             then 64+8i..64+8i+7 (the two halves of each RoPE pair);
+ *             v heads in natural order.  Recurrent layers: [q; k; v], all
+ *             natural, no RoPE.
+ *   gate_up = 16-row strips j holding gate rows 8j..8j+7 then up rows
+ *             8j..8j+7.
+ *   o, down = natural. */
+typedef struct {
+  w12_tensor qkv, o, gate_up, down;
+  const uint16_t* attn_norm;  /* bf16 [hidden] */
+  const uint16_t* mlp_norm;   /* bf16 [hidden] */
+} sd_layer_weights;
+
+typedef struct {
+  const sd_layer_weights* layers_host; /* [n_layers], copied */
+  const uint16_t* embed;               /* bf16 [vocab][hidden], unpacked */
+  const uint16_t* final_norm;          /* bf16 [hidden] */
+  w12_tensor lm_head;                  /* [vocab][hidden] */
+} sd_model_weights;
+
+typedef struct sd_model sd_model;
+
+/* Source row of packed row n for the fused tensors above.  kind 0: qkv of an
+ * attention layer (rows = (Hq + 2 Hkv) * head_dim), kind 1: gate_up (rows =
+ * 2 * inter; source = [gate; up]), kind 2: identity.  out_host[N]. */
+int sd_model_row_map(int32_t kind, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t inter,
+                     int32_t* out_host, int64_t N);
+
+/* The model keeps the weight pointers (borrowed; they must outlive it) and
+ * owns its workspace, activations, RoPE table and status word. */
+int sd_model_create(const sd_model_config* cfg, const sd_model_weights* w, sd_model** out);
+int sd_model_destroy(sd_model* m);
+
+/* Contiguous per-request cache.  K/V: bf16 [n_attn_layers][n_kv_heads][cap][head_dim];
+ * the committed prefix occupies slots [0, *ctx_len).  S, z (hybrid only):
+ * fp32 [n_rec_layers][n_heads][head_dim][head_dim] (row = key dim) and
+ * [n_rec_layers][n_heads][head_dim]. */
+typedef struct {
+  uint16_t* k;
+  uint16_t* v;
+  int64_t cap;
+  float* S;
+  float* z;
+  int32_t* ctx_len;   /* device [1] */
+} sd_kv;
+
+/* Paged cache for batched verify.  K/V pools: bf16
+ * [n_attn_layers][n_pages][n_kv_heads][page_size][head_dim]; request r's
+ * logical slot t lives in page page_table[r*max_pages + t/page_size].
+ * S, z (hybrid): [R][n_rec_layers][...] as in sd_kv.  ctx_len: device [R]. */
+typedef struct {
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  int32_t n_pages, page_size;
+  const int32_t* page_table;  /* device [R][max_pages] */
+  int32_t max_pages;
+  float* S;
+  float* z;
+  int32_t* ctx_len;
+} sd_paged_kv;
+
+/* [TREE][EXACT] One verification step of a draft tree of M <= 64 nodes:
+ * node 0 is the last committed token (its K/V is not in the cache yet), the
+ * others are draft tokens with parents[i] < i.  Runs the target forward over
+ * all nodes at once (node i at position ctx + depth(i), seeing the prefix and
+ * its root path), takes the fp32 argmax per node, walks the greedy longest
+ * accepted path (see sd_accept), moves the K/V of the root and the accepted
+ * nodes to slots ctx + depth (recurrent layers: state += the path's updates)
+ * and advances *ctx_len by accepted_len + 1.  Outputs (device):
+ * accepted_len[1], accepted_tokens[M], bonus_token[1], logits (optional, bf16
+ * [M][vocab]), argmax (optional, int32 [M]).  Asynchronous on `stream`; the
+ * caller synchronises.  Requires ctx + M <= cap (else SD_ERR_CAPACITY on the
+ * device and nothing is committed). */
+int sd_verify_step(sd_model* m, const int32_t* tree_tokens, const int32_t* parents, int32_t M, const sd_kv* kv,
+                   int32_t* accepted_len, int32_t* accepted_tokens, int32_t* bonus_token, uint16_t* logits,
+                   int32_t* argmax, void* stream);
+
+/* The forward part of sd_verify_step only: argmax (and logits) per node; the
+ * new K/V are written to slots ctx + node but nothing is committed. */
+int sd_forward(sd_model* m, const int32_t* tree_tokens, const int32_t* parents, int32_t M, const sd_kv* kv,
+               uint16_t* logits, int32_t* argmax, void* stream);
+
+/* Batched verify of R requests over a paged cache: request r owns nodes
+ * [cu_nodes_host[r], cu_nodes_host[r+1]) of tokens/parents (parents local to
+ * the request, <= 64 nodes each).  Every GEMM processes all rows at once;
+ * attention, acceptance and compaction act per request.  Outputs per request
+ * r: accepted_len[r], bonus[r], accepted_tokens[cu_nodes_host[r] ...]. */
+int sd_verify_batch(sd_model* m, const int32_t* tokens, const int32_t* parents, const int32_t* cu_nodes_host,
+                    int32_t R, const sd_paged_kv* kv, int32_t* accepted_len, int32_t* accepted_tokens,
+                    int32_t* bonus, uint16_t* logits, int32_t* argmax, void* stream);
+
+/* Copy the device status word of the model's last calls (synchronises the
+ * device) and clear it. */
+int sd_status(sd_model* m, int32_t* status_host);
+
+/* Number of kernels the last sd_verify_step / sd_forward / sd_verify_batch
+ * call launched. */
+int sd_model_last_launches(sd_model* m);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SDV_H */

@@ -1,0 +1,608 @@
+// Fused W12-decode skinny GEMM for sm_103a.
+//
+// "SpecPilot: AI Agent Framework Boosts Speculative Decoding 10.87x for
+// Qwen3.8-27B", "(1) W12": a dedicated GEMM decodes the 12-bit weights
+// directly in registers, so the weights cross HBM once at 1.5 bytes each and
+// no bf16 copy is ever materialised.  "SpecPilot Uses Agentic Discovery ...",
+// "Technical Mechanisms": decode-time verification is bound by the bytes of
+// the target weights, so this kernel is built as a weight streamer:
+//
+//  * y[m][n] = sum_k x[m][k] W[n][k] with weights as the 16-row A operand of
+//    mma.m16n8k16 (tokens are the 8-wide N side, "swap-AB"): up to 128 tree
+//    rows per launch ride along while the step is bandwidth-bound.
+//  * One persistent CTA per SM: warp 8 is a producer that streams the packed
+//    words with cp.async.bulk and the activation slice with a 2-D TMA box
+//    (128-byte swizzle) into a multi-stage mbarrier ring; warps 0..7 each own
+//    one 16-row strip of the current 128-row block, decode their words
+//    (3 words -> 4 bf16x2 fragment registers, about two integer operations
+//    per weight when the exponent table is contiguous) and issue the MMAs.
+//  * Work = (row block, 64-column super-tile) units, split evenly over the
+//    CTAs in row-block-major order (stream-K), so every SM streams the same
+//    number of bytes.  A row block split between CTAs is finished by the last
+//    contributor (atomic ticket, no spinning), which sums the partials in CTA
+//    order (deterministic) and runs the epilogue.
+//  * Escaped weights decode to a fixed slot value; the epilogue adds
+//    (w - slot) * x for the few escapes of its rows from the CSR side list.
+//  * Fused epilogues: store, residual add, SiLU(gate)*up, RoPE + KV-cache
+//    write for q/k/v, bf16 logits + running argmax.
+//  * Programmatic dependent launch: the producer streams weights into the
+//    ring before waiting for the previous kernel's activations.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "gemm.cuh"
+
+namespace sdv {
+
+constexpr int kNCW = 8;            // consumer warps
+constexpr int kRB = kNCW;          // strips per row block
+constexpr int kThreads = (kNCW + 1) * 32;
+constexpr int kStripBytes = 1536;  // one strip x one super-tile (16 x 64 x 12 bit)
+
+template <int NT>
+struct Cfg {
+  static constexpr int MP = NT * 8;    // padded rows (tokens) per launch
+  static constexpr int XB = MP * 128;  // x tile bytes per stage (64 columns of bf16)
+  static constexpr int WB = kRB * kStripBytes;
+  static constexpr int S = NT <= 1 ? 8 : NT <= 2 ? 7 : NT <= 4 ? 6 : NT <= 8 ? 5 : 4;
+  static constexpr int SMEM = 1024 + S * (XB + WB) + 2 * S * 8 + kNCW * MP * 8 + 16;
+};
+
+struct GemmParams {
+  const uint32_t* words;
+  int64_t N, K;
+  int KT, NS, NB;
+  int64_t U;
+  uint32_t base2;
+  uint32_t tab[4];
+  float esc_slot;
+  const uint32_t* row_ptr;
+  const uint32_t* esc_idx;
+  const uint16_t* esc_val;
+  const uint16_t* x;
+  int M, m0;
+  float* partial;
+  int32_t* counters;
+  GemmEpilogue e;
+  int32_t* status;
+};
+
+__device__ __forceinline__ uint32_t lut_exp(uint32_t c, const uint32_t* tab) {
+  const uint32_t lo = __byte_perm(tab[0], tab[1], c & 7);
+  const uint32_t hi = __byte_perm(tab[2], tab[3], c & 7);
+  return ((c & 8) ? hi : lo) & 0xFF;
+}
+
+// Stored half (sign in bit 15, code in bits 7..10, mantissa 0..6) -> bf16.
+__device__ __forceinline__ uint32_t general_pair(uint32_t v, const uint32_t* tab) {
+  const uint32_t e0 = lut_exp((v >> 7) & 15, tab), e1 = lut_exp((v >> 23) & 15, tab);
+  return (v & 0x807F807Fu) | (e0 << 7) | (e1 << 23);
+}
+
+template <bool AFFINE>
+__device__ __forceinline__ void decode(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t base2, const uint32_t* tab,
+                                       uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+  const uint32_t X = ((w0 >> 11) & 0x000F000Fu) | ((w1 >> 7) & 0x00F000F0u) | ((w2 >> 3) & 0x0F000F00u);
+  if (AFFINE) {
+    a0 = (w0 & 0x87FF87FFu) + base2;
+    a1 = (w1 & 0x87FF87FFu) + base2;
+    a2 = (w2 & 0x87FF87FFu) + base2;
+    a3 = ((X & 0x07FF07FFu) + base2) | ((X << 4) & 0x80008000u);
+  } else {
+    a0 = general_pair(w0 & 0x87FF87FFu, tab);
+    a1 = general_pair(w1 & 0x87FF87FFu, tab);
+    a2 = general_pair(w2 & 0x87FF87FFu, tab);
+    a3 = general_pair((X & 0x07FF07FFu) | ((X << 4) & 0x80008000u), tab);
+  }
+}
+
+__device__ __forceinline__ uint32_t comp(const uint4& v, int j) {
+  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+template <int NT>
+__device__ __forceinline__ void epilogue(const GemmParams& p, int strip, int lane, float (&acc)[NT][4],
+                                         float (&bestv)[NT][2], int (&besti)[NT][2]) {
+  const int g = lane >> 2, q = lane & 3;
+  const int64_t n_lo = (int64_t)strip * 16 + g;
+  const int64_t K = p.K;
+  // escapes of rows n_lo and n_lo + 8
+#pragma unroll
+  for (int h = 0; h < 2; h++) {
+    const int64_t n = n_lo + 8 * h;
+    const uint32_t e0 = p.row_ptr[n], e1 = p.row_ptr[n + 1];
+    for (uint32_t e = e0; e < e1; e++) {
+      const int64_t k = (int64_t)p.esc_idx[e] - n * K;
+      const float w = bf2f(p.esc_val[e]);
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int cc = 0; cc < 2; cc++) {
+          const int m = p.m0 + nt * 8 + 2 * q + cc;
+          if (m < p.M) {
+            const float xv = bf2f(p.x[(int64_t)m * K + k]);
+            const float a = fmaf(w, xv, acc[nt][2 * h + cc]);
+            acc[nt][2 * h + cc] = fmaf(-p.esc_slot, xv, a);
+          }
+        }
+    }
+  }
+  const GemmEpilogue& E = p.e;
+#pragma unroll
+  for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+    for (int cc = 0; cc < 2; cc++) {
+      const int m = p.m0 + nt * 8 + 2 * q + cc;
+      if (m >= p.M) continue;
+      const float v_lo = acc[nt][cc], v_hi = acc[nt][2 + cc];
+      switch (E.epi) {
+        case EPI_STORE:
+          E.out[(int64_t)m * E.ldo + n_lo] = f2bf(v_lo);
+          E.out[(int64_t)m * E.ldo + n_lo + 8] = f2bf(v_hi);
+          break;
+        case EPI_RESID: {
+          const int64_t i0 = (int64_t)m * E.ldo + n_lo, i1 = i0 + 8;
+          const float r0 = bf2f(E.resid[i0]), r1 = bf2f(E.resid[i1]);
+          E.out[i0] = f2bf(r0 + rbf(v_lo));
+          E.out[i1] = f2bf(r1 + rbf(v_hi));
+          break;
+        }
+        case EPI_SILU: {
+          const float gt = rbf(v_lo), up = rbf(v_hi);
+          const float s = gt / (1.0f + expf(-gt));
+          E.out[(int64_t)m * E.ldo + (int64_t)strip * 8 + g] = f2bf(s * up);
+          break;
+        }
+        case EPI_QKV: {
+          const int64_t qrows = (int64_t)E.hq * 128, krows = (int64_t)E.hkv * 128;
+          const int64_t row0 = (int64_t)strip * 16;
+          if (row0 < qrows + krows) {
+            const bool is_q = row0 < qrows;
+            const int64_t rr = is_q ? row0 : row0 - qrows;
+            const int head = (int)(rr / 128);
+            const int d = (int)((rr % 128) / 16) * 8 + g;
+            const float x1 = rbf(v_lo), x2 = rbf(v_hi);
+            const int pos = E.rows.pos[m];
+            const float c = E.rope_cos[(int64_t)pos * 64 + d], sn = E.rope_sin[(int64_t)pos * 64 + d];
+            const uint16_t o1 = f2bf(x1 * c - x2 * sn), o2 = f2bf(x2 * c + x1 * sn);
+            if (is_q) {
+              uint16_t* dst = E.q_out + ((int64_t)m * E.hq + head) * 128;
+              dst[d] = o1;
+              dst[d + 64] = o2;
+            } else {
+              const int r = E.rows.req[m];
+              if (E.rows.req_ok[r]) {
+                const int slot = E.rows.slot[m];
+                const int page = E.cache.page_table[(int64_t)r * E.cache.max_pages + slot / E.cache.page_size];
+                uint16_t* dst = E.cache.k + (((int64_t)page * E.cache.hkv + head) * E.cache.page_size +
+                                             slot % E.cache.page_size) * 128;
+                dst[d] = o1;
+                dst[d + 64] = o2;
+              }
+            }
+          } else {
+            const int64_t vr = row0 - qrows - krows;
+            const int head = (int)(vr / 128);
+            const int d = (int)(vr % 128) + g;
+            const int r = E.rows.req[m];
+            if (E.rows.req_ok[r]) {
+              const int slot = E.rows.slot[m];
+              const int page = E.cache.page_table[(int64_t)r * E.cache.max_pages + slot / E.cache.page_size];
+              uint16_t* dst = E.cache.v + (((int64_t)page * E.cache.hkv + head) * E.cache.page_size +
+                                           slot % E.cache.page_size) * 128;
+              dst[d] = f2bf(v_lo);
+              dst[d + 8] = f2bf(v_hi);
+            }
+          }
+          break;
+        }
+        case EPI_LOGITS: {
+          if (E.out) {
+            E.out[(int64_t)m * E.ldo + n_lo] = f2bf(v_lo);
+            E.out[(int64_t)m * E.ldo + n_lo + 8] = f2bf(v_hi);
+          }
+          if (v_lo > bestv[nt][cc] || (v_lo == bestv[nt][cc] && (int)n_lo < besti[nt][cc])) {
+            bestv[nt][cc] = v_lo;
+            besti[nt][cc] = (int)n_lo;
+          }
+          if (v_hi > bestv[nt][cc] || (v_hi == bestv[nt][cc] && (int)n_lo + 8 < besti[nt][cc])) {
+            bestv[nt][cc] = v_hi;
+            besti[nt][cc] = (int)n_lo + 8;
+          }
+          break;
+        }
+      }
+    }
+}
+
+template <int NT, bool AFFINE>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_w12_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap xmap) {
+  using C = Cfg<NT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sx = smem;
+  uint8_t* sw = smem + C::S * C::XB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sw + C::S * C::WB);
+  uint64_t* empty = full + C::S;
+  float* red_v = reinterpret_cast<float*>(empty + C::S);
+  int* red_i = reinterpret_cast<int*>(red_v + kNCW * C::MP);
+  int* flag = red_i + kNCW * C::MP;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t G = gridDim.x;
+  const int64_t u0 = (int64_t)blockIdx.x * p.U / G, u1 = (int64_t)(blockIdx.x + 1) * p.U / G;
+  const int KT = p.KT;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::S; i++) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kNCW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch();
+
+  if (warp == kNCW) {
+    // ------------------------------------------------------- producer --
+    if (lane == 0) {
+      const int64_t n = u1 - u0;
+      const int pre = (int)(n < C::S ? n : C::S);
+      for (int i = 0; i < pre; i++) {
+        const int64_t u = u0 + i;
+        const int b = (int)(u / KT), t = (int)(u % KT);
+        const int ns = min(kRB, p.NS - b * kRB);
+        mbar_arrive_expect_tx(&full[i], ns * kStripBytes + C::XB);
+        for (int r = 0; r < ns; r++)
+          bulk_g2s(sw + i * C::WB + r * kStripBytes, p.words + ((int64_t)(b * kRB + r) * KT + t) * 384, kStripBytes,
+                   &full[i]);
+      }
+      pdl_wait();  // activations come from the previous kernel
+      for (int i = 0; i < pre; i++) tma2d_g2s(sx + i * C::XB, &xmap, (int)((u0 + i) % KT) * 64, p.m0, &full[i]);
+      for (int64_t i = pre; i < n; i++) {
+        const int slot = (int)(i % C::S);
+        if (!mbar_wait(&empty[slot], (uint32_t)(((i / C::S) & 1) ^ 1))) {
+          set_status(p.status, SD_ERR_TIMEOUT);
+          break;
+        }
+        const int64_t u = u0 + i;
+        const int b = (int)(u / KT), t = (int)(u % KT);
+        const int ns = min(kRB, p.NS - b * kRB);
+        mbar_arrive_expect_tx(&full[slot], ns * kStripBytes + C::XB);
+        for (int r = 0; r < ns; r++)
+          bulk_g2s(sw + slot * C::WB + r * kStripBytes, p.words + ((int64_t)(b * kRB + r) * KT + t) * 384,
+                   kStripBytes, &full[slot]);
+        tma2d_g2s(sx + slot * C::XB, &xmap, t * 64, p.m0, &full[slot]);
+      }
+    }
+    return;
+  }
+
+  // --------------------------------------------------------- consumers --
+  pdl_wait();
+  float acc[NT][4];
+  float bestv[NT][2];
+  int besti[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+    for (int c = 0; c < 2; c++) {
+      bestv[nt][c] = -INFINITY;
+      besti[nt][c] = 0x7FFFFFFF;
+    }
+  const int first_b = u1 > u0 ? (int)(u0 / KT) : -1;
+
+  auto zero = [&]() {
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int c = 0; c < 4; c++) acc[nt][c] = 0.f;
+  };
+  auto partial_ptr = [&](int64_t cta, int slot_id) {
+    return p.partial + (((cta * 2 + slot_id) * kRB + warp) * NT) * 128 + lane * 4;
+  };
+  // finish the segment [t0, t1) of row block b
+  auto finish = [&](int b, int t0, int t1) {
+    const int strip = b * kRB + warp;
+    if (!(t0 == 0 && t1 == KT)) {
+      const int slot_id = (b == first_b) ? 0 : 1;
+      float* dst = partial_ptr(blockIdx.x, slot_id);
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+        __stcg(reinterpret_cast<float4*>(dst + nt * 128), make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]));
+      __threadfence();
+      bar_sync(1, kNCW * 32);
+      if (threadIdx.x == 0) {
+        const int add = t1 - t0;
+        const int old = atomicAdd(&p.counters[b], add);
+        *flag = (old + add == KT) ? 1 : 0;
+      }
+      bar_sync(1, kNCW * 32);
+      if (!*flag) return;
+      __threadfence();
+      zero();
+      // contributors: the CTAs whose (non-empty) unit range meets row block b
+      const int64_t c_first = (((int64_t)b * KT + 1) * G - 1) / p.U;
+      const int64_t c_last = (((int64_t)(b + 1) * KT) * G - 1) / p.U;
+      for (int64_t c = c_first; c <= c_last; c++) {
+        const int64_t cs = c * p.U / G, ce = (c + 1) * p.U / G;
+        if (cs == ce) continue;  // empty range: never wrote a partial
+        const int sid = (b == (int)(cs / KT)) ? 0 : 1;
+        const float* src = partial_ptr(c, sid);
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(src + nt * 128));
+          acc[nt][0] += v.x;
+          acc[nt][1] += v.y;
+          acc[nt][2] += v.z;
+          acc[nt][3] += v.w;
+        }
+      }
+      if (threadIdx.x == 0) p.counters[b] = 0;
+    }
+    if (strip < p.NS) epilogue<NT>(p, strip, lane, acc, bestv, besti);
+  };
+
+  zero();
+  int cur_b = -1, seg_t0 = 0;
+  bool ok = true;
+  int64_t it = 0;
+  for (int64_t u = u0; u < u1; ++u, ++it) {
+    const int b = (int)(u / KT), t = (int)(u % KT);
+    if (b != cur_b) {
+      if (cur_b >= 0) finish(cur_b, seg_t0, KT);
+      cur_b = b;
+      seg_t0 = t;
+      zero();
+    }
+    const int slot = (int)(it % C::S);
+    if (!mbar_wait(&full[slot], (uint32_t)((it / C::S) & 1))) {
+      set_status(p.status, SD_ERR_TIMEOUT);
+      ok = false;
+      break;
+    }
+    const int strip = b * kRB + warp;
+    if (strip < p.NS) {
+      const uint8_t* wsm = sw + slot * C::WB + warp * kStripBytes;
+      const uint4 W0 = *reinterpret_cast<const uint4*>(wsm + lane * 16);
+      const uint4 W1 = *reinterpret_cast<const uint4*>(wsm + 512 + lane * 16);
+      const uint4 W2 = *reinterpret_cast<const uint4*>(wsm + 1024 + lane * 16);
+      const uint32_t xb = smem_u32(sx + slot * C::XB);
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        uint32_t a0, a1, a2, a3;
+        decode<AFFINE>(comp(W0, j), comp(W1, j), comp(W2, j), p.base2, p.tab, a0, a1, a2, a3);
+        const int kchunk = 2 * j + ((lane >> 3) & 1);
+        if (NT == 1) {
+          const int mrow = lane & 7;
+          uint32_t b0, b1;
+          ldsm_x2(xb + mrow * 128 + ((kchunk ^ mrow) << 4), b0, b1);
+          mma_bf16(acc[0], a0, a1, a2, a3, b0, b1);
+        } else {
+#pragma unroll
+          for (int np = 0; np < NT; np += 2) {
+            const int mrow = (np + (lane >> 4)) * 8 + (lane & 7);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(xb + mrow * 128 + ((kchunk ^ (lane & 7)) << 4), b0, b1, b2, b3);
+            mma_bf16(acc[np], a0, a1, a2, a3, b0, b1);
+            mma_bf16(acc[np + 1], a0, a1, a2, a3, b2, b3);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+  if (ok && cur_b >= 0) finish(cur_b, seg_t0, (int)((u1 - 1) % KT) + 1);
+
+  if (p.e.epi == EPI_LOGITS) {
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int c = 0; c < 2; c++) {
+        float v = bestv[nt][c];
+        int i = besti[nt][c];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+          const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+          if (ov > v || (ov == v && oi < i)) {
+            v = ov;
+            i = oi;
+          }
+        }
+        if (lane < 4) {
+          red_v[warp * C::MP + nt * 8 + 2 * lane + c] = v;
+          red_i[warp * C::MP + nt * 8 + 2 * lane + c] = i;
+        }
+      }
+    bar_sync(1, kNCW * 32);
+    if (threadIdx.x < C::MP) {
+      const int ml = threadIdx.x;
+      float v = -INFINITY;
+      int i = 0x7FFFFFFF;
+      for (int w = 0; w < kNCW; w++) {
+        const float ov = red_v[w * C::MP + ml];
+        const int oi = red_i[w * C::MP + ml];
+        if (ov > v || (ov == v && oi < i)) {
+          v = ov;
+          i = oi;
+        }
+      }
+      const int m = p.m0 + ml;
+      if (m < p.M) {
+        p.e.amax_val[(int64_t)blockIdx.x * p.e.ld_amax + m] = v;
+        p.e.amax_idx[(int64_t)blockIdx.x * p.e.ld_amax + m] = i;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host --
+
+int gemm_grid() { return num_sms(); }
+
+int pad_rows(int M) { return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+
+size_t gemm_partial_floats(int M) {
+  const int NT = pad_rows(std::min(M, 128)) / 8;
+  return (size_t)gemm_grid() * 2 * kRB * NT * 128;
+}
+
+int gemm_counters(int64_t N) { return (int)((N / 16 + kRB - 1) / kRB); }
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+int make_x_map(XMap* xm, const uint16_t* x, int rows_total, int64_t K, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled unavailable");
+    return SD_ERR_CUDA;
+  }
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || K % 64 || box_rows < 8 || box_rows > 128 || rows_total < 1) {
+    set_error("make_x_map: x must be 16-byte aligned, K % 64 == 0");
+    return SD_ERR_INVALID_ARG;
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows_total};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(&xm->map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
+    return SD_ERR_CUDA;
+  }
+  xm->rows_total = rows_total;
+  xm->box_rows = box_rows;
+  return SD_OK;
+}
+
+template <int NT, bool AFF>
+static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, cudaStream_t s, bool pdl) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k_w12_gemm<NT, AFF>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NT>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch(k_w12_gemm<NT, AFF>, dim3(gemm_grid()), dim3(kThreads), Cfg<NT>::SMEM, s, pdl, p, map);
+}
+
+int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
+                const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl) {
+  if (W.N % 16 || W.K % 64 || M < 1 || M > 256) {
+    set_error("gemm: unsupported shape");
+    return SD_ERR_UNSUPPORTED;
+  }
+  GemmParams p{};
+  p.words = W.words;
+  p.N = W.N;
+  p.K = W.K;
+  p.KT = (int)(W.K / 64);
+  p.NS = (int)(W.N / 16);
+  p.NB = gemm_counters(W.N);
+  p.U = (int64_t)p.NB * p.KT;
+  const uint32_t base = W.n_table > 0 ? W.table[0] : 0;
+  p.base2 = (base << 7) | (base << 23);
+  uint8_t t16[16] = {0};
+  for (int i = 0; i < W.n_table && i < 15; i++) t16[i] = W.table[i];
+  for (int i = 0; i < 4; i++)
+    p.tab[i] = t16[4 * i] | (t16[4 * i + 1] << 8) | (t16[4 * i + 2] << 16) | ((uint32_t)t16[4 * i + 3] << 24);
+  p.esc_slot = W.affine ? ldexpf(1.0f, (int)base + 15 - 127) : 0.0f;
+  p.row_ptr = W.row_ptr;
+  p.esc_idx = W.esc_idx;
+  p.esc_val = W.esc_val;
+  p.x = x;
+  p.M = M;
+  p.partial = ws.partial;
+  p.counters = ws.counters;
+  p.e = epi;
+  p.status = status;
+  if (ws.counters_len < p.NB) {
+    set_error("gemm: workspace counters too small");
+    return SD_ERR_WORKSPACE;
+  }
+  const int NT = M > 128 ? 16 : pad_rows(M) / 8;
+  if (xm.box_rows != NT * 8) {
+    set_error("gemm: tensor map box does not match the row count");
+    return SD_ERR_INVALID_ARG;
+  }
+  if (ws.partial_floats < (size_t)gemm_grid() * 2 * kRB * NT * 128) {
+    set_error("gemm: workspace too small");
+    return SD_ERR_WORKSPACE;
+  }
+  const bool aff = W.affine != 0;
+  for (int m0 = 0; m0 < M; m0 += 128) {
+    p.m0 = m0;
+    cudaError_t e;
+    switch (NT) {
+      case 1: e = aff ? launch_nt<1, true>(p, xm.map, s, pdl) : launch_nt<1, false>(p, xm.map, s, pdl); break;
+      case 2: e = aff ? launch_nt<2, true>(p, xm.map, s, pdl) : launch_nt<2, false>(p, xm.map, s, pdl); break;
+      case 4: e = aff ? launch_nt<4, true>(p, xm.map, s, pdl) : launch_nt<4, false>(p, xm.map, s, pdl); break;
+      case 8: e = aff ? launch_nt<8, true>(p, xm.map, s, pdl) : launch_nt<8, false>(p, xm.map, s, pdl); break;
+      default: e = aff ? launch_nt<16, true>(p, xm.map, s, pdl) : launch_nt<16, false>(p, xm.map, s, pdl); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "k_w12_gemm launch");
+  }
+  return SD_OK;
+}
+
+}  // namespace sdv
+
+using namespace sdv;
+
+extern "C" size_t sd_w12_linear_workspace(int64_t N, int64_t K, int32_t M) {
+  (void)K;
+  const size_t pf = gemm_partial_floats(std::max(1, std::min<int>(M, 128)));
+  const size_t pbytes = (pf * sizeof(float) + 255) & ~size_t(255);
+  return pbytes + (size_t)gemm_counters(N) * sizeof(int32_t) + 256;
+}
+
+extern "C" int sd_w12_linear(const w12_tensor* W, const uint16_t* x, int32_t M, uint16_t* y, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!W || !x || !y || !workspace || M < 1 || M > 256) {
+    set_error("sd_w12_linear: bad argument");
+    return SD_ERR_INVALID_ARG;
+  }
+  if (W->N % 16 || W->K % 64) {
+    set_error("sd_w12_linear: need N % 16 == 0 and K % 64 == 0");
+    return SD_ERR_UNSUPPORTED;
+  }
+  if (workspace_bytes < sd_w12_linear_workspace(W->N, W->K, M) || (reinterpret_cast<uintptr_t>(workspace) & 255)) {
+    set_error("sd_w12_linear: workspace too small or not 256-byte aligned");
+    return SD_ERR_WORKSPACE;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  GemmWorkspace ws;
+  ws.partial = reinterpret_cast<float*>(workspace);
+  ws.partial_floats = gemm_partial_floats(std::min<int>(M, 128));
+  const size_t pbytes = (ws.partial_floats * sizeof(float) + 255) & ~size_t(255);
+  ws.counters = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(workspace) + pbytes);
+  ws.counters_len = gemm_counters(W->N);
+  SD_CK(cudaMemsetAsync(ws.counters, 0, (size_t)ws.counters_len * sizeof(int32_t), s));
+  XMap xm;
+  const int rc = make_x_map(&xm, x, M, W->K, M > 128 ? 128 : pad_rows(M));
+  if (rc) return rc;
+  GemmEpilogue e;
+  e.epi = EPI_STORE;
+  e.out = y;
+  e.ldo = (int)W->N;
+  return gemm_launch(*W, x, xm, M, e, ws, nullptr, s, false);
+}

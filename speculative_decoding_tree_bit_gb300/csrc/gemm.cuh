@@ -1,0 +1,73 @@
+// Fused W12-decode skinny GEMM: launch interface.
+#pragma once
+
+#include "common.cuh"
+
+namespace sdv {
+
+enum Epi : int {
+  EPI_STORE = 0,   // out[m][n] = bf16(acc)
+  EPI_RESID = 1,   // out[m][n] = bf16(resid[m][n] + bf16(acc))       (out may alias resid)
+  EPI_SILU = 2,    // gate/up strips: out[m][8s+g] = bf16(silu(bf16(gate)) * bf16(up))
+  EPI_QKV = 3,     // rope-paired q/k strips + v: q -> q_out, k/v -> paged cache
+  EPI_LOGITS = 4,  // optional bf16 logits + per-CTA running fp32 argmax per row
+};
+
+// Per-row (token) bookkeeping written by the tree kernel each step.
+struct RowInfo {
+  const int32_t* pos;     // [rows] position ctx + depth (RoPE)
+  const int32_t* slot;    // [rows] cache slot ctx + local node index
+  const int32_t* req;     // [rows] request index
+  const int32_t* req_ok;  // [R] 1 if the request's tree is valid and fits
+};
+
+struct PagedCache {
+  uint16_t* k;  // this layer's pool: [n_pages][Hkv][page][hd]
+  uint16_t* v;
+  const int32_t* page_table;  // [R][max_pages]
+  int32_t max_pages, page_size, hkv;
+};
+
+struct GemmEpilogue {
+  int epi = EPI_STORE;
+  uint16_t* out = nullptr;
+  int ldo = 0;
+  const uint16_t* resid = nullptr;
+  // QKV
+  uint16_t* q_out = nullptr;  // [rows][Hq][hd]
+  int hq = 0, hkv = 0;
+  PagedCache cache{};
+  RowInfo rows{};
+  const float* rope_cos = nullptr;  // [positions][hd/2]
+  const float* rope_sin = nullptr;
+  // LOGITS
+  float* amax_val = nullptr;  // [grid][ld_amax]
+  int32_t* amax_idx = nullptr;
+  int ld_amax = 0;
+};
+
+struct GemmWorkspace {
+  float* partial = nullptr;  // partial sums of row blocks split between CTAs
+  int32_t* counters = nullptr;
+  size_t partial_floats = 0;
+  int counters_len = 0;
+};
+
+int gemm_grid();                    // CTAs per launch (persistent, one per SM)
+size_t gemm_partial_floats(int M);  // workspace floats for M rows
+int gemm_counters(int64_t N);       // counters for N rows
+int pad_rows(int M);                // rows of one launch's TMA box: 8, 16, 32, 64 or 128
+
+// TMA descriptor of an activation buffer bf16 [rows_total][K].
+struct XMap {
+  CUtensorMap map;
+  int rows_total;
+  int box_rows;
+};
+int make_x_map(XMap* xm, const uint16_t* x, int rows_total, int64_t K, int box_rows);
+
+// y = epilogue(x W^T) for rows [0, M); M > 128 runs in launches of 128 rows.
+int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
+                const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl);
+
+}  // namespace sdv

@@ -1,0 +1,619 @@
+// Tree-verify kernels other than the W12 GEMM.
+//
+// Tree bookkeeping, RMSNorm (+ embedding gather), tree-masked GQA attention
+// (split over the cached prefix, one more split for the tree's own keys, then
+// a combine), the tree linear recurrence, argmax reduction + greedy
+// acceptance, and the commit (K/V compaction, recurrent state update).
+//
+// "SpecPilot: AI Agent Framework Boosts Speculative Decoding 10.87x for
+// Qwen3.8-27B", "(2) Best-first Tree Verification for Hybrid Architectures":
+// the target scores all tree nodes in one pass; each node must see exactly
+// its root path, and a recurrent state has to follow each root path.
+// "(3) Two-Level Verification": only the exact verification accepts tokens.
+#include "layers.cuh"
+
+namespace sdv {
+
+// ------------------------------------------------------------------ tree --
+
+__global__ void k_tree(const int32_t* __restrict__ tokens, const int32_t* __restrict__ parents,
+                       const int32_t* __restrict__ cu, CacheView cv, int vocab, int max_positions, StepRows rows,
+                       int32_t* status) {
+  pdl_wait();
+  pdl_launch();
+  __shared__ uint64_t anc[64];
+  __shared__ int dep[64];
+  __shared__ int okflag, ctx_s;
+  const int r = blockIdx.x;
+  const int a = cu[r], M = cu[r + 1] - a;
+  if (threadIdx.x == 0) {
+    int code = 0;
+    const int ctx = cv.ctx_len[r];
+    if (M < 1 || M > 64) code = SD_ERR_BAD_TREE;
+    for (int i = 0; i < M && i < 64 && !code; i++) {
+      const int p = parents[a + i];
+      if (i == 0 ? p != -1 : (p < 0 || p >= i)) {
+        code = SD_ERR_BAD_TREE;
+        break;
+      }
+      anc[i] = (i ? anc[p] : 0ull) | (1ull << i);
+      dep[i] = i ? dep[p] + 1 : 0;
+    }
+    for (int i = 0; i < M && i < 64 && !code; i++) {
+      const int t = tokens[a + i];
+      if (t < 0 || t >= vocab) code = SD_ERR_BAD_TOKEN;
+    }
+    if (!code) {
+      const int64_t need = (int64_t)ctx + M;
+      if (ctx < 0 || need > (int64_t)cv.max_pages * cv.page_size || need > max_positions) code = SD_ERR_CAPACITY;
+      const int np = code ? 0 : (int)((need + cv.page_size - 1) / cv.page_size);
+      for (int pg = 0; pg < np && !code; pg++) {
+        const int id = cv.page_table[(int64_t)r * cv.max_pages + pg];
+        if (id < 0 || id >= cv.n_pages) code = SD_ERR_CAPACITY;
+      }
+    }
+    if (code) {
+      set_status(status, code);
+      for (int i = 0; i < 64; i++) {
+        anc[i] = 1ull << i;
+        dep[i] = 0;
+      }
+    }
+    okflag = code ? 0 : 1;
+    ctx_s = code ? 0 : ctx;
+  }
+  __syncthreads();
+  const int n = M < 64 ? M : 64;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    rows.pos[a + i] = ctx_s + dep[i];
+    rows.slot[a + i] = ctx_s + i;
+    rows.req[a + i] = r;
+    rows.depth[a + i] = dep[i];
+    rows.anc[a + i] = anc[i];
+  }
+  if (threadIdx.x == 0) {
+    rows.ctx_snap[r] = ctx_s;
+    rows.req_ok[r] = okflag;
+  }
+}
+
+cudaError_t launch_tree(const int32_t* tokens, const int32_t* parents, const int32_t* cu, int R, const CacheView& cv,
+                        int vocab, int max_positions, const StepRows& rows, int32_t* status, cudaStream_t s, bool pdl) {
+  return launch(k_tree, dim3(R), dim3(64), 0, s, pdl, tokens, parents, cu, cv, vocab, max_positions, rows, status);
+}
+
+// ------------------------------------------------------------- RMSNorm --
+// y = bf16((x * (1 / sqrt(mean(x^2) + eps))) * gamma), fp32 inside.
+
+__global__ void __launch_bounds__(256) k_rmsnorm(const uint16_t* __restrict__ src, const uint16_t* __restrict__ gamma,
+                                                 int H, float eps, uint16_t* __restrict__ xn,
+                                                 const int32_t* __restrict__ tokens,
+                                                 const uint16_t* __restrict__ embed, uint16_t* __restrict__ x_out,
+                                                 const int32_t* __restrict__ row_req,
+                                                 const int32_t* __restrict__ req_ok) {
+  pdl_wait();
+  pdl_launch();
+  const int m = blockIdx.x;
+  const uint16_t* row;
+  if (embed) {
+    int t = tokens[m];
+    if (!req_ok[row_req[m]]) t = 0;
+    row = embed + (int64_t)t * H;
+  } else {
+    row = src + (int64_t)m * H;
+  }
+  const int n8 = H / 8;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+    const uint4 v = reinterpret_cast<const uint4*>(row)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const float lo = bf2f(w[j] & 0xFFFF), hi = bf2f(w[j] >> 16);
+      ss = fmaf(lo, lo, ss);
+      ss = fmaf(hi, hi, ss);
+    }
+    if (x_out) reinterpret_cast<uint4*>(x_out + (int64_t)m * H)[i] = v;
+  }
+  __shared__ float red[8];
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); i++) tot += red[i];
+  const float rinv = 1.0f / sqrtf(tot / (float)H + eps);
+  for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+    const uint4 v = reinterpret_cast<const uint4*>(row)[i];
+    const uint4 gm = reinterpret_cast<const uint4*>(gamma)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t gg[4] = {gm.x, gm.y, gm.z, gm.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const float lo = (bf2f(w[j] & 0xFFFF) * rinv) * bf2f(gg[j] & 0xFFFF);
+      const float hi = (bf2f(w[j] >> 16) * rinv) * bf2f(gg[j] >> 16);
+      o[j] = pack_bf16x2(lo, hi);
+    }
+    reinterpret_cast<uint4*>(xn + (int64_t)m * H)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_rmsnorm(const uint16_t* src, const uint16_t* gamma, int rows, int H, float eps, uint16_t* xn,
+                           const int32_t* tokens, const uint16_t* embed, uint16_t* x_out, const int32_t* row_req,
+                           const int32_t* req_ok, cudaStream_t s, bool pdl) {
+  return launch(k_rmsnorm, dim3(rows), dim3(256), 0, s, pdl, src, gamma, H, eps, xn, tokens, embed, x_out, row_req,
+                req_ok);
+}
+
+// ------------------------------------------------------------ attention --
+// CTA = (split, kv head x row chunk, request).  Query rows of a (request,
+// kv head) are its G = Hq/Hkv heads x M nodes (head-major); a row chunk is 64
+// rows (4 warps x 16).  Keys of a prefix split are a contiguous range of the
+// committed prefix; the last split holds the tree's own keys (slots ctx ..
+// ctx+M-1) masked by the row's ancestor bits.  Keys stream through a
+// double-buffered 64-key tile (cp.async, 16-byte XOR swizzle); S = Q K^T and
+// O += P V run on mma.m16n8k16 with an online (base-2) softmax in fp32.
+
+constexpr int kAttnTile = 64;
+constexpr int kAttnSmem = 4 * kAttnTile * 128 * 2;  // K and V, double buffered
+
+int attn_rows_per_group(int hq, int hkv, int max_m) { return (hq / hkv) * max_m; }
+
+struct AttnKernelArgs {
+  AttnArgs a;
+  int rpg;  // row stride of one (request, kv head, split) group in the partial arrays
+};
+
+__global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
+  pdl_wait();
+  pdl_launch();
+  const AttnArgs& a = ka.a;
+  extern __shared__ __align__(128) uint8_t smem_attn[];
+  uint16_t* sK = reinterpret_cast<uint16_t*>(smem_attn);
+  uint16_t* sV = sK + 2 * kAttnTile * 128;
+  const int sp = blockIdx.x;
+  const int h = blockIdx.y % a.hkv, rc = blockIdx.y / a.hkv;
+  const int r = blockIdx.z;
+  const int G = a.hq / a.hkv;
+  const int node0 = a.cu[r], Mr = a.cu[r + 1] - node0;
+  const int rows = G * Mr;
+  if (rc * 64 >= rows) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const int rt = rc * 4 + warp;
+  const int ctx = a.ctx[r];
+  const bool tree = sp == a.splits;
+  int k0, k1;
+  if (!a.req_ok[r]) {
+    k0 = k1 = 0;
+  } else if (tree) {
+    k0 = ctx;
+    k1 = ctx + Mr;
+  } else {
+    k0 = (int)((int64_t)sp * ctx / a.splits);
+    k1 = (int)((int64_t)(sp + 1) * ctx / a.splits);
+  }
+  const bool has_rows = rt * 16 < rows;
+  // this lane's two query rows
+  const int rho0 = rt * 16 + g, rho1 = rho0 + 8;
+  const bool v0 = rho0 < rows, v1 = rho1 < rows;
+  const int n0 = v0 ? rho0 % Mr : 0, n1 = v1 ? rho1 % Mr : 0;
+  const int qh0 = h * G + (v0 ? rho0 / Mr : 0), qh1 = h * G + (v1 ? rho1 / Mr : 0);
+  const uint64_t anc0 = v0 ? a.anc[node0 + n0] : 0ull, anc1 = v1 ? a.anc[node0 + n1] : 0ull;
+  uint32_t qa[8][4];
+  {
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q + ((int64_t)(node0 + n0) * a.hq + qh0) * 128);
+    const uint32_t* q1 = reinterpret_cast<const uint32_t*>(a.q + ((int64_t)(node0 + n1) * a.hq + qh1) * 128);
+#pragma unroll
+    for (int kk = 0; kk < 8; kk++) {
+      qa[kk][0] = v0 ? q0[(16 * kk + 2 * q) / 2] : 0u;
+      qa[kk][1] = v1 ? q1[(16 * kk + 2 * q) / 2] : 0u;
+      qa[kk][2] = v0 ? q0[(16 * kk + 8 + 2 * q) / 2] : 0u;
+      qa[kk][3] = v1 ? q1[(16 * kk + 8 + 2 * q) / 2] : 0u;
+    }
+  }
+  float o[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+  const float sl2 = 0.08838834764831845f * 1.4426950408889634f;  // log2(e) / sqrt(128)
+
+  const int64_t head_stride = (int64_t)a.page_size * 128;
+  auto load_tile = [&](int tile, int buf) {
+    const int kb = k0 + tile * kAttnTile;
+    for (int c = threadIdx.x; c < kAttnTile * 16; c += 128) {
+      const int kr = c >> 4, ch = c & 15;
+      const int t = kb + kr;
+      const bool valid = t < k1;
+      int64_t off = 0;
+      if (valid) {
+        const int page = a.page_table[(int64_t)r * a.max_pages + t / a.page_size];
+        off = ((int64_t)page * a.hkv + h) * head_stride + (int64_t)(t % a.page_size) * 128 + ch * 8;
+      }
+      const int so = (buf * kAttnTile + kr) * 128 + ((ch ^ (kr & 7)) * 8);
+      cp_async16_zfill(sK + so, a.k_pool + off, valid);
+      cp_async16_zfill(sV + so, a.v_pool + off, valid);
+    }
+    cp_async_commit();
+  };
+  const int ntiles = (k1 - k0 + kAttnTile - 1) / kAttnTile;
+  if (ntiles > 0) load_tile(0, 0);
+  for (int tile = 0; tile < ntiles; tile++) {
+    const int buf = tile & 1;
+    if (tile + 1 < ntiles) {
+      load_tile(tile + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    if (has_rows) {
+      float s[8][4];
+#pragma unroll
+      for (int i = 0; i < 8; i++) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+      const uint32_t kb = smem_u32(sK + buf * kAttnTile * 128);
+#pragma unroll
+      for (int kk = 0; kk < 8; kk++) {
+#pragma unroll
+        for (int np = 0; np < 4; np++) {
+          const int key = np * 16 + (lane >> 4) * 8 + (lane & 7);
+          const int ch = 2 * kk + ((lane >> 3) & 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kb + key * 256 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+          mma_bf16(s[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+          mma_bf16(s[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+        }
+      }
+      const int tb = k0 + tile * kAttnTile;
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const int rr = e >> 1;
+          const int t = tb + nt * 8 + 2 * q + (e & 1);
+          bool ok = t < k1 && (rr ? v1 : v0);
+          if (tree && ok) ok = ((rr ? anc1 : anc0) >> (t - ctx)) & 1ull;
+          s[nt][e] = ok ? s[nt][e] * sl2 : -INFINITY;
+          mx[rr] = fmaxf(mx[rr], s[nt][e]);
+        }
+      float alpha[2], ms[2], sum[2] = {0.f, 0.f};
+#pragma unroll
+      for (int rr = 0; rr < 2; rr++) {
+        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+        const float mn = fmaxf(mrow[rr], mx[rr]);
+        ms[rr] = mn == -INFINITY ? 0.f : mn;
+        alpha[rr] = exp2f(mrow[rr] - ms[rr]);
+        mrow[rr] = mn;
+      }
+#pragma unroll
+      for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const int rr = e >> 1;
+          s[nt][e] = exp2f(s[nt][e] - ms[rr]);
+          sum[rr] += s[nt][e];
+        }
+#pragma unroll
+      for (int rr = 0; rr < 2; rr++) {
+        sum[rr] += __shfl_xor_sync(0xffffffffu, sum[rr], 1);
+        sum[rr] += __shfl_xor_sync(0xffffffffu, sum[rr], 2);
+        lrow[rr] = lrow[rr] * alpha[rr] + sum[rr];
+      }
+#pragma unroll
+      for (int dn = 0; dn < 16; dn++) {
+        o[dn][0] *= alpha[0];
+        o[dn][1] *= alpha[0];
+        o[dn][2] *= alpha[1];
+        o[dn][3] *= alpha[1];
+      }
+      const uint32_t vb = smem_u32(sV + buf * kAttnTile * 128);
+#pragma unroll
+      for (int k2 = 0; k2 < 4; k2++) {
+        const uint32_t pa0 = pack_bf16x2(s[2 * k2][0], s[2 * k2][1]);
+        const uint32_t pa1 = pack_bf16x2(s[2 * k2][2], s[2 * k2][3]);
+        const uint32_t pa2 = pack_bf16x2(s[2 * k2 + 1][0], s[2 * k2 + 1][1]);
+        const uint32_t pa3 = pack_bf16x2(s[2 * k2 + 1][2], s[2 * k2 + 1][3]);
+#pragma unroll
+        for (int dp = 0; dp < 8; dp++) {
+          const int key = k2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+          const int ch = 2 * dp + (lane >> 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vb + key * 256 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+          mma_bf16(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
+          mma_bf16(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (!has_rows) return;
+  const int64_t gbase = ((int64_t)(r * a.hkv + h) * (a.splits + 1) + sp) * ka.rpg;
+#pragma unroll
+  for (int rr = 0; rr < 2; rr++) {
+    const int rho = rr ? rho1 : rho0;
+    if (rho >= rows) continue;
+    const int64_t b = gbase + rho;
+    if (q == 0) {
+      a.part_ml[b * 2] = mrow[rr];
+      a.part_ml[b * 2 + 1] = lrow[rr];
+    }
+    float* dst = a.part_o + b * 128;
+#pragma unroll
+    for (int dn = 0; dn < 16; dn++)
+      *reinterpret_cast<float2*>(dst + dn * 8 + 2 * q) = make_float2(o[dn][2 * rr], o[dn][2 * rr + 1]);
+  }
+}
+
+// out[m][qh] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the splits.
+__global__ void __launch_bounds__(128) k_attn_combine(AttnKernelArgs ka) {
+  pdl_wait();
+  pdl_launch();
+  const AttnArgs& a = ka.a;
+  const int m = blockIdx.x, qh = blockIdx.y, d = threadIdx.x;
+  const int r = a.row_req[m];
+  const int node = m - a.cu[r], Mr = a.cu[r + 1] - a.cu[r];
+  const int G = a.hq / a.hkv, h = qh / G;
+  const int rho = (qh % G) * Mr + node;
+  const int64_t gbase = (int64_t)(r * a.hkv + h) * (a.splits + 1);
+  float mx = -INFINITY;
+  for (int sp = 0; sp <= a.splits; sp++) mx = fmaxf(mx, a.part_ml[((gbase + sp) * ka.rpg + rho) * 2]);
+  float L = 0.f, acc = 0.f;
+  for (int sp = 0; sp <= a.splits; sp++) {
+    const int64_t b = (gbase + sp) * ka.rpg + rho;
+    const float mm = a.part_ml[b * 2];
+    if (mm == -INFINITY) continue;
+    const float w = exp2f(mm - mx);
+    L += w * a.part_ml[b * 2 + 1];
+    acc += w * a.part_o[b * 128 + d];
+  }
+  a.out[(int64_t)m * a.hq * 128 + qh * 128 + d] = f2bf(L > 0.f ? acc / L : 0.f);
+}
+
+cudaError_t launch_attention(const AttnArgs& a, int rows_total, cudaStream_t s, bool pdl) {
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int rpg = attn_rows_per_group(a.hq, a.hkv, a.max_m);
+  const AttnKernelArgs ka{a, rpg};
+  const int chunks = (rpg + 63) / 64;
+  const cudaError_t e = launch(k_attn, dim3(a.splits + 1, a.hkv * chunks, a.R), dim3(128), kAttnSmem, s, pdl, ka);
+  if (e != cudaSuccess) return e;
+  return launch(k_attn_combine, dim3(rows_total, a.hq), dim3(128), 0, s, pdl, ka);
+}
+
+// ------------------------------------------------- linear recurrence -----
+// CTA = (value-dim chunk of 32, head, request).  Closed form of the tree
+// recurrence: S_i = S0 + sum_{j in path(i)} phi(k_j) v_j^T gives
+//   o_i = (S0^T phi(q_i) + sum_j (phi(k_j).phi(q_i)) v_j) / (z0.phi(q_i) + sum_j phi(k_j).phi(q_i) + eps)
+// so the per-node states are never materialised.
+
+__device__ __forceinline__ float phi(float x) { return x > 0.f ? x + 1.0f : expf(x); }
+
+constexpr int kRecSmem = (64 * 128 * 2 + 128 * 32 + 64 * 32 + 128 + 64 * 64 + 64) * 4;
+
+__global__ void __launch_bounds__(128) k_linrec(LinrecArgs a) {
+  pdl_wait();
+  pdl_launch();
+  extern __shared__ __align__(16) float smem_rec[];
+  float* fq = smem_rec;       // [64][128]
+  float* fk = fq + 64 * 128;  // [64][128]
+  float* sS = fk + 64 * 128;  // [128][32]
+  float* sv = sS + 128 * 32;  // [64][32]
+  float* sz = sv + 64 * 32;   // [128]
+  float* dots = sz + 128;     // [64][64]
+  float* zq = dots + 64 * 64; // [64]
+  const int cc = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
+  const int node0 = a.cu[r], Mr = min(a.cu[r + 1] - node0, 64);
+  const int64_t H3 = (int64_t)a.H * 3;
+  for (int idx = threadIdx.x; idx < Mr * 128; idx += blockDim.x) {
+    const int i = idx >> 7, d = idx & 127;
+    const uint16_t* row = a.qkv + (int64_t)(node0 + i) * H3;
+    fq[i * 128 + d] = phi(bf2f(row[h * 128 + d]));
+    fk[i * 128 + d] = phi(bf2f(row[a.H + h * 128 + d]));
+  }
+  for (int idx = threadIdx.x; idx < Mr * 32; idx += blockDim.x) {
+    const int i = idx >> 5, c = idx & 31;
+    sv[i * 32 + c] = bf2f(a.qkv[(int64_t)(node0 + i) * H3 + 2 * a.H + h * 128 + cc * 32 + c]);
+  }
+  const float* Sg = a.S + r * a.req_stride_S + (int64_t)h * 128 * 128;
+  const float* zg = a.z + r * a.req_stride_z + (int64_t)h * 128;
+  for (int idx = threadIdx.x; idx < 128 * 32; idx += blockDim.x) {
+    const int k = idx >> 5, c = idx & 31;
+    sS[k * 32 + c] = Sg[k * 128 + cc * 32 + c];
+  }
+  for (int k = threadIdx.x; k < 128; k += blockDim.x) sz[k] = zg[k];
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < Mr * Mr; idx += blockDim.x) {
+    const int i = idx / Mr, j = idx % Mr;
+    float dt = 0.f;
+    if ((a.anc[node0 + i] >> j) & 1ull) {
+      for (int d = 0; d < 128; d++) dt = fmaf(fk[j * 128 + d], fq[i * 128 + d], dt);
+    }
+    dots[i * 64 + j] = dt;
+  }
+  for (int i = threadIdx.x; i < Mr; i += blockDim.x) {
+    float t = 0.f;
+    for (int d = 0; d < 128; d++) t = fmaf(sz[d], fq[i * 128 + d], t);
+    zq[i] = t;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < Mr * 32; idx += blockDim.x) {
+    const int i = idx >> 5, c = idx & 31;
+    float num = 0.f;
+    for (int k = 0; k < 128; k++) num = fmaf(fq[i * 128 + k], sS[k * 32 + c], num);
+    float den = zq[i];
+    for (int j = 0; j < Mr; j++) {
+      const float w = dots[i * 64 + j];
+      num = fmaf(w, sv[j * 32 + c], num);
+      den += w;
+    }
+    a.out[(int64_t)(node0 + i) * a.H + h * 128 + cc * 32 + c] = f2bf(num / (den + a.eps));
+  }
+}
+
+cudaError_t launch_linrec(const LinrecArgs& a, cudaStream_t s, bool pdl) {
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(k_linrec, cudaFuncAttributeMaxDynamicSharedMemorySize, kRecSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch(k_linrec, dim3(4, a.nh, a.R), dim3(128), kRecSmem, s, pdl, a);
+}
+
+// --------------------------------------------------- argmax + accept -----
+
+__global__ void k_accept(AcceptArgs a) {
+  pdl_wait();
+  pdl_launch();
+  __shared__ int am[64], par[64], dep[64], okn[64], pth[65];
+  const int r = blockIdx.x;
+  const int node0 = a.cu ? a.cu[r] : 0, Mr = a.cu ? a.cu[r + 1] - node0 : a.single_M;
+  const int i = threadIdx.x;
+  if (i < Mr && i < 64) {
+    int best;
+    if (a.amax_val) {
+      float v = -INFINITY;
+      best = 0x7FFFFFFF;
+      for (int c = 0; c < a.n_part; c++) {
+        const float ov = a.amax_val[(int64_t)c * a.ld + node0 + i];
+        const int oi = a.amax_idx[(int64_t)c * a.ld + node0 + i];
+        if (ov > v || (ov == v && oi < best)) {
+          v = ov;
+          best = oi;
+        }
+      }
+    } else {
+      best = a.argmax_in[node0 + i];
+    }
+    am[i] = best;
+    if (a.argmax_out) a.argmax_out[node0 + i] = best;
+    par[i] = a.parents[node0 + i];
+  }
+  __syncthreads();
+  if (i != 0) return;
+  bool valid = Mr >= 1 && Mr <= 64 && (a.req_ok ? a.req_ok[r] != 0 : true);
+  for (int j = 0; j < Mr && j < 64 && valid; j++)
+    if (j == 0 ? par[0] != -1 : (par[j] < 0 || par[j] >= j)) valid = false;
+  if (!valid) {
+    if (!a.req_ok) set_status(a.status, SD_ERR_BAD_TREE);
+    a.accepted_len[r] = 0;
+    a.bonus[r] = -1;
+    if (a.path_len) a.path_len[r] = 0;
+    return;
+  }
+  dep[0] = 0;
+  okn[0] = 1;
+  int best = 0;
+  for (int j = 1; j < Mr; j++) {
+    dep[j] = dep[par[j]] + 1;
+    okn[j] = okn[par[j]] && a.tokens[node0 + j] == am[par[j]];
+    if (okn[j] && dep[j] > dep[best]) best = j;
+  }
+  const int L = dep[best];
+  for (int d = L, j = best; d >= 0; d--, j = par[j]) pth[d] = j;
+  a.accepted_len[r] = L;
+  a.bonus[r] = am[best];
+  for (int d = 1; d <= L; d++) a.accepted_tokens[node0 + d - 1] = a.tokens[node0 + pth[d]];
+  if (a.path)
+    for (int d = 0; d <= L; d++) a.path[r * 65 + d] = pth[d];
+  if (a.path_len) a.path_len[r] = L + 1;
+  if (a.ctx_len) a.ctx_len[r] = a.ctx_snap[r] + L + 1;
+}
+
+cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s, bool pdl) {
+  return launch(k_accept, dim3(a.R), dim3(64), 0, s, pdl, a);
+}
+
+// ------------------------------------------------------------- commit ----
+// K/V of the root and the accepted nodes move from slot ctx + node to slot
+// ctx + depth.  A destination can be another path node's source, so every
+// row is read into shared memory before any is written.
+
+__global__ void __launch_bounds__(128) k_compact(CacheView cv, int hkv, const int32_t* __restrict__ ctx_snap,
+                                                 const int32_t* __restrict__ path,
+                                                 const int32_t* __restrict__ path_len) {
+  pdl_wait();
+  pdl_launch();
+  __shared__ uint4 bk[65][16], bv[65][16];
+  const int r = blockIdx.x, la = blockIdx.y, h = blockIdx.z;
+  const int P = path_len[r];
+  if (P <= 0) return;
+  const int ctx = ctx_snap[r];
+  const int64_t layer = (int64_t)la * cv.n_pages * hkv * cv.page_size * 128;
+  auto at = [&](int t) -> int64_t {
+    const int page = cv.page_table[(int64_t)r * cv.max_pages + t / cv.page_size];
+    return layer + ((int64_t)page * hkv + h) * cv.page_size * 128 + (int64_t)(t % cv.page_size) * 128;
+  };
+  for (int idx = threadIdx.x; idx < P * 16; idx += blockDim.x) {
+    const int d = idx >> 4, ch = idx & 15;
+    const int64_t src = at(ctx + path[r * 65 + d]);
+    bk[d][ch] = reinterpret_cast<const uint4*>(cv.k_pool + src)[ch];
+    bv[d][ch] = reinterpret_cast<const uint4*>(cv.v_pool + src)[ch];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < P * 16; idx += blockDim.x) {
+    const int d = idx >> 4, ch = idx & 15;
+    const int64_t dst = at(ctx + d);
+    reinterpret_cast<uint4*>(cv.k_pool + dst)[ch] = bk[d][ch];
+    reinterpret_cast<uint4*>(cv.v_pool + dst)[ch] = bv[d][ch];
+  }
+}
+
+cudaError_t launch_compact(const CacheView& cv, int n_attn_layers, int hkv, int R, const int32_t* ctx_snap,
+                           const int32_t* path, const int32_t* path_len, cudaStream_t s, bool pdl) {
+  return launch(k_compact, dim3(R, n_attn_layers, hkv), dim3(128), 0, s, pdl, cv, hkv, ctx_snap, path, path_len);
+}
+
+// Recurrent state after acceptance: S0 += sum_{path} phi(k) v^T, z0 += sum phi(k).
+__global__ void __launch_bounds__(128) k_rec_commit(CacheView cv, int n_rec, int nh, int H, int max_rows,
+                                                    const uint16_t* __restrict__ qkv_rec,
+                                                    const int32_t* __restrict__ cu, const int32_t* __restrict__ path,
+                                                    const int32_t* __restrict__ path_len) {
+  pdl_wait();
+  pdl_launch();
+  __shared__ float fk[65][128];
+  __shared__ float vv[65][32];
+  const int r = blockIdx.x / n_rec, lr = blockIdx.x % n_rec, h = blockIdx.y, cc = blockIdx.z;
+  const int P = path_len[r];
+  if (P <= 0) return;
+  const int64_t H3 = (int64_t)H * 3;
+  const uint16_t* base = qkv_rec + (int64_t)lr * max_rows * H3;
+  for (int idx = threadIdx.x; idx < P * 128; idx += blockDim.x) {
+    const int p = idx >> 7, d = idx & 127;
+    const int row = cu[r] + path[r * 65 + p];
+    fk[p][d] = phi(bf2f(base[(int64_t)row * H3 + H + h * 128 + d]));
+  }
+  for (int idx = threadIdx.x; idx < P * 32; idx += blockDim.x) {
+    const int p = idx >> 5, c = idx & 31;
+    const int row = cu[r] + path[r * 65 + p];
+    vv[p][c] = bf2f(base[(int64_t)row * H3 + 2 * H + h * 128 + cc * 32 + c]);
+  }
+  __syncthreads();
+  float* S = cv.S + (((int64_t)r * n_rec + lr) * nh + h) * 128 * 128;
+  float* z = cv.z + (((int64_t)r * n_rec + lr) * nh + h) * 128;
+  const int k = threadIdx.x;
+  for (int c = 0; c < 32; c++) {
+    float add = 0.f;
+    for (int p = 0; p < P; p++) add = fmaf(fk[p][k], vv[p][c], add);
+    S[k * 128 + cc * 32 + c] += add;
+  }
+  if (cc == 0) {
+    float add = 0.f;
+    for (int p = 0; p < P; p++) add += fk[p][k];
+    z[k] += add;
+  }
+}
+
+cudaError_t launch_rec_commit(const CacheView& cv, int n_rec, int nh, int H, int R, int max_rows,
+                              const uint16_t* qkv_rec, const int32_t* cu, const int32_t* path,
+                              const int32_t* path_len, cudaStream_t s, bool pdl) {
+  return launch(k_rec_commit, dim3(R * n_rec, nh, 4), dim3(128), 0, s, pdl, cv, n_rec, nh, H, max_rows, qkv_rec, cu,
+                path, path_len);
+}
+
+}  // namespace sdv

@@ -1,0 +1,343 @@
+"""Device-side objects around libsdv: packed tensors, the model, the caches.
+
+Marshalling and memory only (PyTorch allocates, the library computes).
+Weights come from any provider with the methods of
+``synthetic.workloads.SyntheticWeights`` (natural PyTorch-Linear layout,
+bf16 bit patterns as uint16 numpy arrays).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import KV, LayerWeights, ModelConfig, ModelWeights, PagedKV, W12Meta, W12Tensor, check, lib, stream_ptr
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def to_device_u16(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """uint16 bit patterns -> int16 device tensor with the same bits."""
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device)
+
+
+def _i32(a, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(np.asarray(a, dtype=np.int32))).to(device)
+
+
+class Packed:
+    """A W12-packed tensor on the device (owns its buffers)."""
+
+    def __init__(self, meta: W12Meta, words, esc_idx, esc_val, row_ptr):
+        self.meta, self.words, self.esc_idx, self.esc_val, self.row_ptr = meta, words, esc_idx, esc_val, row_ptr
+
+    N = property(lambda self: int(self.meta.N))
+    K = property(lambda self: int(self.meta.K))
+    n_escapes = property(lambda self: int(self.meta.n_escapes))
+
+    @property
+    def table(self):
+        return np.array(self.meta.table[: self.meta.n_table], dtype=np.uint8)
+
+    def struct(self) -> W12Tensor:
+        t = W12Tensor()
+        t.N, t.K = self.meta.N, self.meta.K
+        t.words, t.esc_idx, t.esc_val, t.row_ptr = (_ptr(self.words), _ptr(self.esc_idx), _ptr(self.esc_val),
+                                                    _ptr(self.row_ptr))
+        t.n_escapes = self.meta.n_escapes
+        t.table = self.meta.table
+        t.n_table = self.meta.n_table
+        t.affine = self.meta.affine
+        return t
+
+    def nbytes(self) -> int:
+        """Bytes a GEMM streams: the packed words plus the escape side list."""
+        return (self.words.numel() * 4 + self.n_escapes * 6 + self.row_ptr.numel() * 4)
+
+
+def pack(w: torch.Tensor, row_src: np.ndarray | None = None, stream=None) -> Packed:
+    """Pack a bf16 device tensor [N][K] (int16/uint16/bfloat16 storage)."""
+    assert w.is_cuda and w.dim() == 2 and w.element_size() == 2 and w.is_contiguous()
+    N, K = w.shape
+    s = stream_ptr(stream)
+    meta = W12Meta()
+    check(lib().w12_pack_analyze(w.data_ptr(), N, K, ctypes.byref(meta), s))
+    dev = w.device
+    words = torch.empty(int(lib().w12_words_count(N, K)), dtype=torch.int32, device=dev)
+    ne = max(int(meta.n_escapes), 1)
+    esc_idx = torch.empty(ne, dtype=torch.int32, device=dev)
+    esc_val = torch.empty(ne, dtype=torch.int16, device=dev)
+    row_ptr = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    rs = None if row_src is None else _i32(row_src, dev)
+    check(lib().w12_pack_encode(w.data_ptr(), _ptr(rs), ctypes.byref(meta), words.data_ptr(), esc_idx.data_ptr(),
+                                esc_val.data_ptr(), row_ptr.data_ptr(), s))
+    torch.cuda.current_stream().synchronize()
+    return Packed(meta, words, esc_idx, esc_val, row_ptr)
+
+
+def unpack(p: Packed, stream=None) -> torch.Tensor:
+    out = torch.empty((p.N, p.K), dtype=torch.int16, device=p.words.device)
+    t = p.struct()
+    check(lib().w12_unpack(ctypes.byref(t), out.data_ptr(), stream_ptr(stream)))
+    return out
+
+
+class Workspace:
+    """Caller-owned device scratch for the stand-alone entry points."""
+
+    def __init__(self, nbytes: int, device="cuda"):
+        self.buf = torch.empty(max(int(nbytes), 256) + 256, dtype=torch.uint8, device=device)
+        self.ptr = (self.buf.data_ptr() + 255) & ~255
+        self.nbytes = int(nbytes)
+
+
+def linear(p: Packed, x: torch.Tensor, ws: Workspace | None = None, stream=None) -> torch.Tensor:
+    """y = bf16(x W^T) through the fused W12 GEMM; x int16 bits [M][K]."""
+    M = x.shape[0]
+    need = int(lib().sd_w12_linear_workspace(p.N, p.K, M))
+    if ws is None or ws.nbytes < need:
+        ws = Workspace(need, x.device)
+    y = torch.empty((M, p.N), dtype=torch.int16, device=x.device)
+    t = p.struct()
+    check(lib().sd_w12_linear(ctypes.byref(t), x.data_ptr(), M, y.data_ptr(), ws.ptr, ws.nbytes, stream_ptr(stream)))
+    return y
+
+
+def row_map(kind: int, Hq: int, Hkv: int, inter: int, N: int) -> np.ndarray:
+    out = np.empty(N, dtype=np.int32)
+    check(lib().sd_model_row_map(kind, Hq, Hkv, 128, inter, out.ctypes.data, N))
+    return out
+
+
+class Model:
+    """A decoder whose linear weights are W12-packed on the device."""
+
+    def __init__(self, shape, weights, max_rows: int = 64, max_requests: int = 1, max_positions: int = 4352,
+                 device: str = "cuda", progress=None):
+        self.shape = shape
+        self.device = device
+        keep = []
+        L = shape.n_layers
+        layers = (LayerWeights * L)()
+        H, I, Hq, Hkv = shape.H, shape.I, shape.Hq, shape.Hkv
+        self.packed_bytes = 0
+        self.layer_bytes = []
+        for l, kind in enumerate(shape.layer_kinds):
+            qkv = to_device_u16(np.concatenate([weights.layer(l, n) for n in ("wq", "wk", "wv")]), device)
+            p_qkv = pack(qkv, row_map(0, Hq, Hkv, I, qkv.shape[0]) if kind == "attn" else None)
+            del qkv
+            p_o = pack(to_device_u16(weights.layer(l, "wo"), device))
+            gu = to_device_u16(np.concatenate([weights.layer(l, "w_gate"), weights.layer(l, "w_up")]), device)
+            p_gu = pack(gu, row_map(1, Hq, Hkv, I, gu.shape[0]))
+            del gu
+            p_d = pack(to_device_u16(weights.layer(l, "w_down"), device))
+            an = to_device_u16(weights.norm(l, "attn"), device)
+            mn = to_device_u16(weights.norm(l, "mlp"), device)
+            keep += [p_qkv, p_o, p_gu, p_d, an, mn]
+            layers[l].qkv, layers[l].o, layers[l].gate_up, layers[l].down = (p.struct() for p in (p_qkv, p_o, p_gu, p_d))
+            layers[l].attn_norm, layers[l].mlp_norm = an.data_ptr(), mn.data_ptr()
+            self.layer_bytes.append({k: p.nbytes() for k, p in (("qkv", p_qkv), ("o", p_o), ("gate_up", p_gu),
+                                                                ("down", p_d))})
+            self.packed_bytes += sum(self.layer_bytes[-1].values())
+            if progress:
+                progress(l)
+        self.embed = to_device_u16(weights.embedding(), device)
+        self.final_norm = to_device_u16(weights.final_norm(), device)
+        self.lm_head = pack(to_device_u16(weights.lm_head(), device))
+        self.packed_bytes += self.lm_head.nbytes()
+        keep += [self.embed, self.final_norm, self.lm_head]
+        self._keep, self._layers = keep, layers
+        self._kinds = (ctypes.c_int8 * L)(*[0 if k == "attn" else 1 for k in shape.layer_kinds])
+        cfg = ModelConfig()
+        cfg.n_layers, cfg.hidden, cfg.inter, cfg.n_q_heads, cfg.n_kv_heads = L, H, I, Hq, Hkv
+        cfg.head_dim, cfg.vocab = 128, shape.V
+        cfg.rms_eps, cfg.rope_base, cfg.rec_eps = shape.eps, shape.rope_base, shape.rec_eps
+        cfg.layer_kind_host = ctypes.addressof(self._kinds)
+        cfg.max_rows, cfg.max_requests, cfg.max_positions = max_rows, max_requests, max_positions
+        mw = ModelWeights()
+        mw.layers_host = ctypes.addressof(layers)
+        mw.embed, mw.final_norm = self.embed.data_ptr(), self.final_norm.data_ptr()
+        mw.lm_head = self.lm_head.struct()
+        self._cfg, self._mw = cfg, mw
+        h = ctypes.c_void_p()
+        torch.cuda.synchronize()
+        check(lib().sd_model_create(ctypes.byref(cfg), ctypes.byref(mw), ctypes.byref(h)))
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().sd_model_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def status(self) -> int:
+        st = ctypes.c_int32()
+        check(lib().sd_status(self.handle, ctypes.byref(st)))
+        return int(st.value)
+
+    def last_launches(self) -> int:
+        return int(lib().sd_model_last_launches(self.handle))
+
+    def outputs(self, M: int, logits: bool = False, R: int = 1):
+        d = self.device
+        o = {"accepted_len": torch.zeros(R, dtype=torch.int32, device=d),
+             "accepted_tokens": torch.zeros(M, dtype=torch.int32, device=d),
+             "bonus": torch.zeros(R, dtype=torch.int32, device=d),
+             "argmax": torch.zeros(M, dtype=torch.int32, device=d)}
+        if logits:
+            o["logits"] = torch.empty((M, self.shape.V), dtype=torch.int16, device=d)
+        return o
+
+    def forward(self, tokens, parents, kv: "KVCache", logits: bool = True, stream=None):
+        tok, par = _i32(tokens, self.device), _i32(parents, self.device)
+        M = tok.numel()
+        lg = torch.empty((M, self.shape.V), dtype=torch.int16, device=self.device) if logits else None
+        am = torch.empty(M, dtype=torch.int32, device=self.device)
+        kvs = kv.struct()
+        check(lib().sd_forward(self.handle, tok.data_ptr(), par.data_ptr(), M, ctypes.byref(kvs), _ptr(lg),
+                               am.data_ptr(), stream_ptr(stream)))
+        return lg, am
+
+    def verify(self, tokens, parents, kv: "KVCache", logits: bool = False, out=None, stream=None):
+        tok = tokens if isinstance(tokens, torch.Tensor) else _i32(tokens, self.device)
+        par = parents if isinstance(parents, torch.Tensor) else _i32(parents, self.device)
+        M = tok.numel()
+        o = out or self.outputs(M, logits)
+        kvs = kv.struct()
+        check(lib().sd_verify_step(self.handle, tok.data_ptr(), par.data_ptr(), M, ctypes.byref(kvs),
+                                   o["accepted_len"].data_ptr(), o["accepted_tokens"].data_ptr(),
+                                   o["bonus"].data_ptr(), _ptr(o.get("logits")), o["argmax"].data_ptr(),
+                                   stream_ptr(stream)))
+        return o
+
+    def verify_batch(self, tokens, parents, cu_nodes, kv: "PagedKVCache", logits: bool = False, out=None,
+                     stream=None):
+        tok = tokens if isinstance(tokens, torch.Tensor) else _i32(tokens, self.device)
+        par = parents if isinstance(parents, torch.Tensor) else _i32(parents, self.device)
+        cu = np.ascontiguousarray(np.asarray(cu_nodes, dtype=np.int32))
+        R = cu.size - 1
+        o = out or self.outputs(tok.numel(), logits, R)
+        kvs = kv.struct()
+        check(lib().sd_verify_batch(self.handle, tok.data_ptr(), par.data_ptr(), cu.ctypes.data, R,
+                                    ctypes.byref(kvs), o["accepted_len"].data_ptr(), o["accepted_tokens"].data_ptr(),
+                                    o["bonus"].data_ptr(), _ptr(o.get("logits")), o["argmax"].data_ptr(),
+                                    stream_ptr(stream)))
+        return o
+
+
+class KVCache:
+    """Contiguous cache of one request: K/V [n_attn][Hkv][cap][128] bf16,
+    recurrent state S [n_rec][nh][128][128] fp32, z [n_rec][nh][128]."""
+
+    def __init__(self, shape, cap: int, device="cuda"):
+        self.shape, self.cap, self.device = shape, cap, device
+        na, nr, nh = max(shape.n_attn, 1), max(shape.n_rec, 1), shape.H // 128
+        self.k = torch.zeros((na, shape.Hkv, cap, 128), dtype=torch.int16, device=device)
+        self.v = torch.zeros_like(self.k)
+        self.S = torch.zeros((nr, nh, 128, 128), dtype=torch.float32, device=device)
+        self.z = torch.zeros((nr, nh, 128), dtype=torch.float32, device=device)
+        self.ctx_len = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def fill(self, seed: int, ctx: int, r: int = 0):
+        from synthetic import workloads as wl
+        la = lr = 0
+        for l, kind in enumerate(self.shape.layer_kinds):
+            if kind == "attn":
+                k, v = wl.kv_prefix(self.shape, seed, r, l, ctx, ctx)
+                self.k[la, :, :ctx] = to_device_u16(k, self.device)
+                self.v[la, :, :ctx] = to_device_u16(v, self.device)
+                la += 1
+            else:
+                S, z = wl.rec_state(self.shape, seed, r, l)
+                self.S[lr] = torch.from_numpy(S).to(self.device)
+                self.z[lr] = torch.from_numpy(z).to(self.device)
+                lr += 1
+        self.ctx_len.fill_(ctx)
+        return self
+
+    def struct(self) -> KV:
+        s = KV()
+        s.k, s.v, s.cap = self.k.data_ptr(), self.v.data_ptr(), self.cap
+        s.S, s.z = self.S.data_ptr(), self.z.data_ptr()
+        s.ctx_len = self.ctx_len.data_ptr()
+        return s
+
+
+class PagedKVCache:
+    """Paged cache of R requests: pools [n_attn][n_pages][Hkv][page][128]."""
+
+    def __init__(self, shape, page_table: np.ndarray, n_pages: int, page_size: int = 16, device="cuda"):
+        self.shape, self.device, self.page_size, self.n_pages = shape, device, page_size, n_pages
+        self.page_table_host = np.ascontiguousarray(page_table, dtype=np.int32)
+        self.R, self.max_pages = self.page_table_host.shape
+        na, nr, nh = max(shape.n_attn, 1), max(shape.n_rec, 1), shape.H // 128
+        self.k = torch.zeros((na, n_pages, shape.Hkv, page_size, 128), dtype=torch.int16, device=device)
+        self.v = torch.zeros_like(self.k)
+        self.S = torch.zeros((self.R, nr, nh, 128, 128), dtype=torch.float32, device=device)
+        self.z = torch.zeros((self.R, nr, nh, 128), dtype=torch.float32, device=device)
+        self.page_table = _i32(self.page_table_host, device)
+        self.ctx_len = torch.zeros(self.R, dtype=torch.int32, device=device)
+
+    def fill(self, seed: int, ctxs):
+        from synthetic import workloads as wl
+        ps = self.page_size
+        la = lr = 0
+        for l, kind in enumerate(self.shape.layer_kinds):
+            if kind == "attn":
+                kp = np.zeros((self.n_pages, self.shape.Hkv, ps, 128), dtype=np.uint16)
+                vp = np.zeros_like(kp)
+                for r, ctx in enumerate(ctxs):
+                    k, v = wl.kv_prefix(self.shape, seed, r, l, ctx, ctx)
+                    t = np.arange(ctx)
+                    pages = self.page_table_host[r, t // ps]
+                    kp[pages, :, t % ps, :] = k.transpose(1, 0, 2)
+                    vp[pages, :, t % ps, :] = v.transpose(1, 0, 2)
+                self.k[la] = to_device_u16(kp, self.device)
+                self.v[la] = to_device_u16(vp, self.device)
+                la += 1
+            else:
+                for r in range(len(ctxs)):
+                    S, z = wl.rec_state(self.shape, seed, r, l)
+                    self.S[r, lr] = torch.from_numpy(S).to(self.device)
+                    self.z[r, lr] = torch.from_numpy(z).to(self.device)
+                lr += 1
+        self.ctx_len.copy_(_i32(ctxs, self.device))
+        return self
+
+    def struct(self) -> PagedKV:
+        s = PagedKV()
+        s.k_pool, s.v_pool = self.k.data_ptr(), self.v.data_ptr()
+        s.n_pages, s.page_size = self.n_pages, self.page_size
+        s.page_table, s.max_pages = self.page_table.data_ptr(), self.max_pages
+        s.S, s.z, s.ctx_len = self.S.data_ptr(), self.z.data_ptr(), self.ctx_len.data_ptr()
+        return s
+
+
+def tiny_verify(W1: Packed, Wlm: Packed, act: torch.Tensor, tokens, parents, logits: bool = True, stream=None):
+    """The tiny verify model through the C ABI; returns a dict of device tensors."""
+    dev = act.device
+    tok, par = _i32(tokens, dev), _i32(parents, dev)
+    M = tok.numel()
+    ws = Workspace(int(lib().sd_tiny_workspace(W1.N, W1.K, Wlm.N, M)), dev)
+    o = {"accepted_len": torch.zeros(1, dtype=torch.int32, device=dev),
+         "accepted_tokens": torch.zeros(M, dtype=torch.int32, device=dev),
+         "bonus": torch.zeros(1, dtype=torch.int32, device=dev),
+         "argmax": torch.zeros(M, dtype=torch.int32, device=dev),
+         "status": torch.zeros(1, dtype=torch.int32, device=dev)}
+    if logits:
+        o["logits"] = torch.empty((M, Wlm.N), dtype=torch.int16, device=dev)
+    t1, t2 = W1.struct(), Wlm.struct()
+    check(lib().sd_tiny_verify(ctypes.byref(t1), ctypes.byref(t2), act.data_ptr(), tok.data_ptr(), par.data_ptr(), M,
+                               o["accepted_len"].data_ptr(), o["accepted_tokens"].data_ptr(), o["bonus"].data_ptr(),
+                               _ptr(o.get("logits")), o["argmax"].data_ptr(), o["status"].data_ptr(), ws.ptr,
+                               ws.nbytes, stream_ptr(stream)))
+    o["_ws"] = ws
+    return o

@@ -210,6 +210,17 @@ def copy_rule_tokens(td: TreeDraft, argmax_fn) -> np.ndarray:
     return tok
 
 
+def copy_rule_tokens_static(td: TreeDraft, argmax_all) -> np.ndarray:
+    """Copy rule when the target's argmax does not depend on the tokens
+    (the tiny model): one pass over the nodes."""
+    parents = np.asarray(td.parents)
+    tok = np.zeros(parents.size, dtype=np.int32)
+    tok[0] = td.root_token
+    for i in range(1, parents.size):
+        tok[i] = argmax_all[parents[i]] if td.copy[i] else td.rand_tok[i]
+    return tok
+
+
 # ------------------------------------------------------------------- tiny --
 
 @dataclass

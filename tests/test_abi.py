@@ -1,0 +1,75 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function include/*.h declares, and its host-side logic (row maps, argument
+checks) behaves."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import speculative_decoding_tree_bit_gb300 as sdv
+from speculative_decoding_tree_bit_gb300 import _build
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return sdv.lib()
+
+
+def test_every_declared_function_is_exported(L):
+    names = sdv.header_functions()
+    assert len(names) >= 20
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    assert set(names) == set(sdv._SIGS), "binding signatures and header differ"
+
+
+def test_words_count(L):
+    assert L.w12_words_count(16, 64) == 384
+    assert L.w12_words_count(151936, 4096) == 151936 * 4096 * 3 // 8
+
+
+def test_qkv_row_map_pairs_rope_halves(L):
+    Hq, Hkv = 4, 2
+    N = (Hq + 2 * Hkv) * 128
+    m = np.empty(N, np.int32)
+    assert L.sd_model_row_map(0, Hq, Hkv, 128, 0, m.ctypes.data, N) == 0
+    assert sorted(m.tolist()) == list(range(N))
+    for head in range(Hq + Hkv):
+        for strip in range(8):
+            rows = m[head * 128 + strip * 16: head * 128 + strip * 16 + 16] - head * 128
+            assert list(rows[:8]) == list(range(8 * strip, 8 * strip + 8))
+            assert list(rows[8:]) == [64 + d for d in range(8 * strip, 8 * strip + 8)]
+    assert list(m[(Hq + Hkv) * 128:]) == list(range((Hq + Hkv) * 128, N))
+
+
+def test_gate_up_row_map_interleaves(L):
+    I = 64
+    m = np.empty(2 * I, np.int32)
+    assert L.sd_model_row_map(1, 4, 2, 128, I, m.ctypes.data, 2 * I) == 0
+    assert sorted(m.tolist()) == list(range(2 * I))
+    for j in range(I // 8):
+        assert list(m[16 * j:16 * j + 8]) == list(range(8 * j, 8 * j + 8))
+        assert list(m[16 * j + 8:16 * j + 16]) == list(range(I + 8 * j, I + 8 * j + 8))
+
+
+def test_host_argument_checks(L):
+    meta = sdv.W12Meta()
+    # N % 16 != 0 is refused before any device call
+    assert L.w12_pack_analyze(ctypes.c_void_p(16), 10, 64, ctypes.byref(meta), None) == 2
+    assert b"N % 16" in L.sd_last_error()
+    assert L.w12_pack_analyze(None, 16, 64, ctypes.byref(meta), None) == 1
+    bad = np.empty(4, np.int32)
+    assert L.sd_model_row_map(7, 4, 2, 128, 64, bad.ctypes.data, 4) == 1
+    cfg = sdv.ModelConfig()
+    cfg.n_layers, cfg.head_dim = 1, 64
+    kinds = (ctypes.c_int8 * 1)(0)
+    cfg.layer_kind_host = ctypes.addressof(kinds)
+    w = sdv.ModelWeights()
+    lw = (sdv.LayerWeights * 1)()
+    w.layers_host, w.embed, w.final_norm = ctypes.addressof(lw), 16, 16
+    h = ctypes.c_void_p()
+    assert L.sd_model_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == 2
+    assert L.sd_accept(None, None, None, 4, None, None, None, None, None, None) == 1
+    assert L.sd_tree_info(ctypes.c_void_p(16), 65, 0, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                          ctypes.c_void_p(16), None, None) == 2
