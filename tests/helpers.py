@@ -1,0 +1,73 @@
+"""Shared test helpers: oracle requests and the parity rules."""
+import numpy as np
+
+import oracle
+from synthetic import workloads as wl
+
+# Parity rules for floating point (the workloads' rule for bf16 logits with
+# fp32 accumulation): |gpu - oracle| <= ATOL + RTOL * |oracle|; argmax must
+# agree except where the oracle's top-2 margin is below MARGIN.
+ATOL, RTOL, MARGIN = 2e-2, 1e-2, 1e-3
+
+
+def oracle_request(shape, seed, r, ctx, tokens, parents, cap=None):
+    cap = cap or ctx + 80
+    layers = []
+    for l, kind in enumerate(shape.layer_kinds):
+        if kind == "attn":
+            k, v = wl.kv_prefix(shape, seed, r, l, ctx, cap)
+            layers.append(oracle.LayerState(k=k, v=v))
+        else:
+            S, z = wl.rec_state(shape, seed, r, l)
+            layers.append(oracle.LayerState(S=S.astype(np.float64), z=z.astype(np.float64)))
+    return oracle.Request(np.asarray(tokens, np.int32), np.asarray(parents, np.int32), ctx, layers)
+
+
+def oracle_copy_tokens(shape, W, seed, r, ctx, td):
+    """Copy-rule draft tokens by depth waves, the target argmax from the oracle."""
+    def am(tok, par):
+        return oracle.forward(shape, W, [oracle_request(shape, seed, r, ctx, tok, par)]).argmax
+    return wl.copy_rule_tokens(td, am)
+
+
+def assert_close(gpu_bits, ref):
+    got = oracle.bf16_to_f64(np.asarray(gpu_bits).view(np.uint16))
+    err = np.abs(got - ref)
+    bad = err > ATOL + RTOL * np.abs(ref)
+    assert not bad.any(), f"{int(bad.sum())} elements out of tolerance, max err {float(err.max())}"
+    return float(err.max())
+
+
+def assert_argmax(gpu_am, ref_am, margin):
+    diff = np.asarray(gpu_am) != np.asarray(ref_am)
+    assert not np.any(diff & (np.asarray(margin) >= MARGIN)), (np.nonzero(diff)[0], np.asarray(margin)[diff])
+    return diff
+
+
+def brute_accept(tokens, parents, am):
+    """Deepest fully matching root path (smallest index on ties)."""
+    best = (0, 0, [0])
+    for node in range(len(parents)):
+        path = []
+        j = node
+        while j >= 0:
+            path.append(j)
+            j = parents[j]
+        path.reverse()
+        if all(tokens[path[i]] == am[path[i - 1]] for i in range(1, len(path))):
+            if len(path) - 1 > best[0]:
+                best = (len(path) - 1, node, path)
+    return best
+
+
+def assert_accept(tokens, parents, gpu_am, acc_len, acc_tokens, bonus, ref_am=None):
+    """The GPU's walk must be the correct walk over the GPU's own argmax, and
+    equal the oracle's walk when the two argmax vectors agree."""
+    d, node, path = brute_accept(tokens, parents, gpu_am)
+    assert acc_len == d
+    assert list(acc_tokens[:d]) == [int(tokens[j]) for j in path[1:]]
+    assert bonus == gpu_am[node]
+    if ref_am is not None and np.array_equal(gpu_am, ref_am):
+        a = oracle.accept(tokens, parents, ref_am)
+        assert (a.accepted_len, a.bonus) == (acc_len, bonus)
+    return path

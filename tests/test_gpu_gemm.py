@@ -1,0 +1,90 @@
+"""Fused W12-decode GEMM (sd_w12_linear) vs the oracle's fp64 linear.
+
+Tolerance: |gpu - oracle| <= 2e-2 + 1e-2 |oracle| per element (the rule for
+bf16 outputs with fp32 accumulation); in addition almost every element must
+equal the oracle's correctly rounded bf16 value, since a single GEMM differs
+from it only by the fp32 summation order."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from synthetic import workloads as wl
+from helpers import ATOL, RTOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def M():
+    from speculative_decoding_tree_bit_gb300 import model
+    return model
+
+
+def _x(Mrows, K, seed=0):
+    return synthetic.normal_bf16(synthetic.key(seed, 77 + Mrows), Mrows * K, 1.0).reshape(Mrows, K)
+
+
+def _check(M, W, x, rows=None, exact_frac=0.99, p=None):
+    p = p or M.pack(M.to_device_u16(W))
+    y = M.linear(p, M.to_device_u16(x)).cpu().numpy().view(np.uint16)
+    if rows is not None:
+        W, y = W[rows], y[:, rows]
+    ref = oracle.linear(x, W)
+    got = oracle.bf16_to_f64(y)
+    err = np.abs(got - ref)
+    assert np.all(err <= ATOL + RTOL * np.abs(ref)), float(err.max())
+    same = np.mean(oracle.round_bf16(ref) == y)
+    assert same >= exact_frac, same
+    return p
+
+
+@pytest.mark.parametrize("Mrows", [1, 5, 8, 13, 16, 17, 32, 48, 64, 100, 128, 129, 200, 256])
+def test_tiny_shape_all_row_counts(M, Mrows):
+    t = wl.tiny()
+    _check(M, t.W1, _x(Mrows, 1024))
+
+
+@pytest.mark.parametrize("N,K,Mrows", [(16, 64, 8), (48, 192, 16), (4000, 512, 8), (512, 512, 8), (1024, 4096, 16),
+                                       (144, 1088, 3), (4000, 512, 64)])
+def test_ragged_shapes(M, N, K, Mrows):
+    W = synthetic.normal_bf16(synthetic.key(2, N * 7 + K), N * K, 0.02).reshape(N, K)
+    _check(M, W, _x(Mrows, K, 1))
+
+
+def test_escapes_affine_path(M):
+    t = wl.tiny()
+    p = _check(M, t.Wlm, _x(8, 1024, 2))
+    assert p.meta.affine == 1 and p.n_escapes >= 4194
+
+
+def test_general_table_path(M):
+    rng = np.random.default_rng(5)
+    exps = np.array([110, 112, 114, 116, 118, 120, 121, 122, 123, 124, 100, 102, 104, 106, 108, 90], np.uint32)
+    e = exps[rng.integers(0, exps.size, size=256 * 512)]
+    W = ((rng.integers(0, 2, size=e.size).astype(np.uint32) << 15) | (e << 7)
+         | rng.integers(0, 128, size=e.size).astype(np.uint32)).astype(np.uint16).reshape(256, 512)
+    p = _check(M, W, _x(16, 512, 3))
+    assert p.meta.affine == 0 and p.n_escapes > 0
+
+
+@pytest.mark.parametrize("name,Mrows", [("wq", 16), ("w_down", 16), ("lm", 16), ("lm", 64)])
+def test_full_size_8b(M, name, Mrows):
+    sh = wl.SHAPES["8b"]
+    w = wl.SyntheticWeights(sh, 0)
+    W = w.lm_head() if name == "lm" else w.layer(0, name)
+    rows = np.sort(np.random.default_rng(0).choice(W.shape[0], 1024, replace=False))
+    _check(M, W, _x(Mrows, W.shape[1], 4), rows=rows)
+
+
+def test_repeat_calls_are_deterministic_with_dirty_workspace(M):
+    t = wl.tiny()
+    p = M.pack(M.to_device_u16(t.W1))
+    x = M.to_device_u16(_x(16, 1024, 9))
+    ws = M.Workspace(int(M.lib().sd_w12_linear_workspace(1024, 1024, 16)))
+    ws.buf.fill_(0x7F)  # garbage in the scratch must not leak into results
+    a = M.linear(p, x, ws)
+    ws.buf.fill_(0xFF)
+    b = M.linear(p, x, ws)
+    assert torch.equal(a, b)

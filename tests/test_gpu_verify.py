@@ -1,0 +1,162 @@
+"""End-to-end verify step on the GPU vs the oracle: the tiny model, small
+dense and hybrid decoders (several GEMM tiles, ragged row blocks), batched
+paged verify, and the device-side error paths."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import workloads as wl
+from helpers import assert_accept, assert_argmax, assert_close, oracle_copy_tokens, oracle_request
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def M():
+    from speculative_decoding_tree_bit_gb300 import model
+    return model
+
+
+def _np(t):
+    return t.cpu().numpy()
+
+
+# ------------------------------------------------------------------ tiny --
+
+def test_tiny_verify(M):
+    t = wl.tiny()
+    lo = oracle.tiny_forward(t.W1, t.Wlm, t.act)
+    am_o, margin = oracle.argmax_margin(lo)
+    tokens = wl.copy_rule_tokens_static(t.draft, am_o)
+    p1, p2 = M.pack(M.to_device_u16(t.W1)), M.pack(M.to_device_u16(t.Wlm))
+    o = M.tiny_verify(p1, p2, M.to_device_u16(t.act), tokens, t.draft.parents)
+    torch.cuda.synchronize()
+    assert int(o["status"][0]) == 0
+    assert_close(_np(o["logits"]), lo)
+    am = _np(o["argmax"])
+    assert_argmax(am, am_o, margin)
+    assert_accept(tokens, t.draft.parents, am, int(o["accepted_len"][0]), _np(o["accepted_tokens"]),
+                  int(o["bonus"][0]), am_o)
+    assert int(o["accepted_len"][0]) >= 1
+
+
+def test_tiny_rejects_bad_tree(M):
+    t = wl.tiny()
+    p1, p2 = M.pack(M.to_device_u16(t.W1)), M.pack(M.to_device_u16(t.Wlm))
+    parents = t.draft.parents.copy()
+    parents[3] = 5  # parent after child
+    o = M.tiny_verify(p1, p2, M.to_device_u16(t.act), np.zeros(8, np.int32), parents)
+    torch.cuda.synchronize()
+    assert int(o["status"][0]) == 5 and int(o["accepted_len"][0]) == 0
+
+
+# ------------------------------------------------------------ decoders --
+
+@pytest.fixture(scope="module", params=["mini", "mini_hybrid"])
+def dec(request, M):
+    shape = wl.SHAPES[request.param]
+    W = wl.SyntheticWeights(shape, seed=3, cache=True)
+    model = M.Model(shape, W, max_rows=64, max_requests=4, max_positions=512)
+    yield shape, W, model
+    model.close()
+
+
+def _verify_case(M, shape, W, model, td, ctx, seed=3):
+    tokens = oracle_copy_tokens(shape, W, seed, 0, ctx, td)
+    req = oracle_request(shape, seed, 0, ctx, tokens, td.parents, cap=ctx + 80)
+    out, (acc,), (st,) = oracle.verify(shape, W, [req])
+    kv = M.KVCache(shape, ctx + 80).fill(seed, ctx)
+    o = model.verify(tokens, td.parents, kv, logits=True)
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    assert_close(_np(o["logits"]), out.logits)
+    am = _np(o["argmax"])
+    diff = assert_argmax(am, out.argmax, out.margin)
+    assert_accept(tokens, td.parents, am, int(o["accepted_len"][0]), _np(o["accepted_tokens"]), int(o["bonus"][0]),
+                  out.argmax)
+    L = int(o["accepted_len"][0])
+    assert int(kv.ctx_len[0]) == ctx + L + 1
+    if not diff.any():
+        # the committed state equals the oracle's
+        la = lr = 0
+        for l, kind in enumerate(shape.layer_kinds):
+            if kind == "attn":
+                k, v = _np(kv.k[la]).view(np.uint16), _np(kv.v[la]).view(np.uint16)
+                n = ctx + L + 1
+                assert np.array_equal(k[:, :ctx], st.layers[l].k[:, :ctx])
+                assert_close(k[:, ctx:n], oracle.bf16_to_f64(st.layers[l].k[:, ctx:n]))
+                assert_close(v[:, ctx:n], oracle.bf16_to_f64(st.layers[l].v[:, ctx:n]))
+                la += 1
+            else:
+                assert np.allclose(_np(kv.S[lr]), st.layers[l].S, rtol=1e-2, atol=2e-3)
+                assert np.allclose(_np(kv.z[lr]), st.layers[l].z, rtol=1e-2, atol=2e-3)
+                lr += 1
+    return L
+
+
+def test_tree_verify_matches_oracle(M, dec):
+    shape, W, model = dec
+    _verify_case(M, shape, W, model, wl.draft(11, 0, 16, 8, 0.8, shape.V), 37)
+
+
+def test_wide_tree_64_nodes(M, dec):
+    shape, W, model = dec
+    _verify_case(M, shape, W, model, wl.draft(12, 0, 64, 10, 0.7, shape.V), 130)
+
+
+def test_single_node_and_long_context(M, dec):
+    shape, W, model = dec
+    assert _verify_case(M, shape, W, model, wl.draft(13, 0, 1, 1, 0.7, shape.V), 300) == 0
+
+
+def test_chain_equals_sequential_on_gpu(M, dec):
+    shape, W, model = dec
+    ctx, n = 40, 6
+    toks = np.random.default_rng(4).integers(0, shape.V, n).astype(np.int32)
+    kv = M.KVCache(shape, ctx + 80).fill(3, ctx)
+    lg_chain, _ = model.forward(toks, np.arange(-1, n - 1), kv)
+    kv2 = M.KVCache(shape, ctx + 80).fill(3, ctx)
+    for i in range(n):
+        # a one-node verify accepts nothing and commits that node (ctx += 1)
+        o = model.verify(toks[i:i + 1], [-1], kv2, logits=True)
+        torch.cuda.synchronize()
+        assert_close(_np(o["logits"][0]), oracle.bf16_to_f64(_np(lg_chain[i]).view(np.uint16)))
+    assert int(kv2.ctx_len[0]) == ctx + n
+
+
+def test_batched_paged_equals_oracle(M, dec):
+    shape, W, model = dec
+    ctxs = [23, 61, 40]
+    drafts = [wl.draft(20 + r, r, m, 5, 0.8, shape.V) for r, m in enumerate([5, 9, 1])]
+    toks = [oracle_copy_tokens(shape, W, 3, r, ctxs[r], td) for r, td in enumerate(drafts)]
+    reqs = [oracle_request(shape, 3, r, ctxs[r], toks[r], drafts[r].parents, cap=ctxs[r] + 32) for r in range(3)]
+    out, accs, sts = oracle.verify(shape, W, reqs)
+    table, n_pages = wl.page_tables(7, ctxs, 16, 16)
+    kv = M.PagedKVCache(shape, table, n_pages, 16).fill(3, ctxs)
+    cu = np.cumsum([0] + [len(t) for t in toks])
+    o = model.verify_batch(np.concatenate(toks), np.concatenate([d.parents for d in drafts]), cu, kv, logits=True)
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    assert_close(_np(o["logits"]), out.logits)
+    am = _np(o["argmax"])
+    assert_argmax(am, out.argmax, out.margin)
+    for r in range(3):
+        a, b = cu[r], cu[r + 1]
+        assert_accept(toks[r], drafts[r].parents, am[a:b], int(o["accepted_len"][r]), _np(o["accepted_tokens"][a:b]),
+                      int(o["bonus"][r]), out.argmax[a:b])
+        assert int(kv.ctx_len[r]) == ctxs[r] + int(o["accepted_len"][r]) + 1
+
+
+def test_bad_inputs_set_status_and_commit_nothing(M, dec):
+    shape, W, model = dec
+    ctx = 30
+    kv = M.KVCache(shape, ctx + 8).fill(3, ctx)
+    model.verify([1, 2, 3], [-1, 0, 2], kv)  # parent[2] == 2
+    assert model.status() == 5 and int(kv.ctx_len[0]) == ctx
+    model.verify([1, shape.V, 3], [-1, 0, 0], kv)  # token out of range
+    assert model.status() == 8 and int(kv.ctx_len[0]) == ctx
+    model.verify(list(range(9)), list(range(-1, 8)), kv)  # ctx + 9 > cap
+    assert model.status() == 7 and int(kv.ctx_len[0]) == ctx
+    o = model.verify([1, 2], [-1, 0], kv)  # still usable afterwards
+    assert model.status() == 0 and int(kv.ctx_len[0]) == ctx + int(o["accepted_len"][0]) + 1
