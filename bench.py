@@ -1,0 +1,368 @@
+#!/usr/bin/env python3
+"""Benchmark of the tree-verify step on GB300.
+
+Default workload: the 8B-class dense decoder (36 layers, hidden 4096, SwiGLU
+12288, 32/8 heads, vocab 151936, every linear weight W12-packed), one request,
+a draft tree of M = 16 nodes (depth <= 8, copy-rule tokens with p = 0.7),
+2048 cached positions.  A step is one sd_verify_step: tree bookkeeping,
+forward over all nodes, fp32 argmax, greedy acceptance and commit.  Each
+timed step starts from the same cache state (ctx_len is reset; the prefix is
+never written by a step), so all steps do identical work.  The weights
+(11.4 GB packed) are far larger than L2, so no flush is needed.
+
+Prints one JSON line (rank 0).  --impl reference times the oracle (the plain
+CPU implementation the tests compare against) on this machine's host cores
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_BW_GBS = 8000.0       # the metric's "fraction of 8 TB/s"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return PEAKS_FALLBACK, "fallback"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="sdv", choices=["sdv", "reference"])
+    ap.add_argument("--workload", default="8b_m16")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--timeline", action="store_true", help="print the per-kernel breakdown to stderr")
+    return ap.parse_args()
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.p:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except Exception:
+                self.p.kill()
+
+    def summary(self):
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sms.append(float(r[1]))
+                mx = float(r[2])
+                for nm, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(nm)
+            except Exception:
+                continue
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def oracle_sample(shape, seed, M, ctx, parents, tokens, n_layers=1, reps=1):
+    """Time the oracle on a bounded sample: the first n_layers layers plus the
+    final norm, lm_head and argmax; returns (per-layer s, lm_head s, threads)."""
+    import numpy as np
+    import oracle
+    from synthetic import workloads as wl
+    W = wl.SyntheticWeights(shape, seed, cache=True)
+    for l in range(n_layers):
+        for nm in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down"):
+            W.layer(l, nm)
+    W.lm_head()
+    layers = []
+    for l in range(n_layers):
+        k, v = wl.kv_prefix(shape, seed, 0, l, ctx, ctx + M)
+        layers.append(oracle.LayerState(k=k, v=v))
+    req = oracle.Request(np.asarray(tokens, np.int32), np.asarray(parents, np.int32), ctx, layers)
+    t_full = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.forward(shape, W, [req], n_layers=n_layers)
+        t_full.append(time.perf_counter() - t0)
+    x = oracle.bf16_to_f64(W.embed_rows(tokens))
+    t0 = time.perf_counter()
+    oracle.linear(x, W.lm_head())
+    t_lm = time.perf_counter() - t0
+    per_layer = max(1e-9, (statistics.median(t_full) - t_lm) / n_layers)
+    return per_layer, t_lm, os.cpu_count()
+
+
+def reference_arm(args):
+    """The oracle as it stands, timed on the host cores (the reference arm)."""
+    import numpy as np
+    from synthetic import workloads as wl
+    spec = wl.make(args.workload, args.seed)
+    shape, M, ctx = spec.shape, spec.M, spec.ctx[0]
+    td = spec.drafts[0]
+    tokens = np.where(td.copy, 0, td.rand_tok).astype(np.int32)
+    tokens[0] = td.root_token
+    for _ in range(args.warmup):
+        oracle_sample(shape, args.seed, M, ctx, td.parents, tokens, n_layers=1)
+    per_layer, t_lm = [], []
+    for _ in range(args.steps):
+        a, b, thr = oracle_sample(shape, args.seed, M, ctx, td.parents, tokens, n_layers=1)
+        per_layer.append(a)
+        t_lm.append(b)
+    step_s = statistics.median(per_layer) * shape.n_layers + statistics.median(t_lm)
+    value = M / step_s
+    sample = f"oracle forward of layer 0 + lm_head/argmax per step, M={M}, ctx={ctx}; step = layer x {shape.n_layers} + lm_head"
+    return {"metric": "tree_tokens_per_s", "value": value, "unit": "tree tokens/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "M": M, "ctx": ctx, "layers": shape.n_layers},
+            "cpu_baseline": {"value": value, "unit": "tree tokens/s", "cores": thr, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tree tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# --------------------------------------------------------------- GPU arm --
+
+def kv_bytes_per_step(shape, ctx, M):
+    """Algorithmic cache bytes of one step: every attention layer reads the
+    K/V prefix and writes the tree's K/V; every recurrent layer reads its
+    state and commits it."""
+    hd = 128
+    attn = shape.n_attn * shape.Hkv * (ctx + M) * hd * 2 * 2
+    nh = shape.H // hd
+    rec = shape.n_rec * nh * (hd * hd + hd) * 4 * 2
+    return attn + rec
+
+
+def gpu_arm(args, rank, world, dist):
+    import numpy as np
+    import torch
+    from speculative_decoding_tree_bit_gb300 import _build
+    from speculative_decoding_tree_bit_gb300 import model as Mdl
+    from synthetic import workloads as wl
+
+    _build.build()
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    spec = wl.make(args.workload, args.seed)
+    shape, M, ctx = spec.shape, spec.M, spec.ctx[0]
+    if spec.R != 1:
+        raise SystemExit("this bench drives single-request workloads")
+    t0 = time.time()
+    W = wl.SyntheticWeights(shape, args.seed)
+    model = Mdl.Model(shape, W, max_rows=M, max_requests=1, max_positions=ctx + M + 64)
+    kv = Mdl.KVCache(shape, ctx + M + 16).fill(args.seed, ctx)
+    log(f"[rank {rank}] model built in {time.time() - t0:.1f}s, packed {model.packed_bytes / 1e9:.2f} GB")
+    td = spec.drafts[0]
+
+    def am_fn(tok, par):
+        _, am = model.forward(tok, par, kv, logits=False)
+        return am.cpu().numpy()
+
+    tokens = wl.copy_rule_tokens(td, am_fn)
+    dev = torch.device("cuda", local)
+    tok_d = torch.from_numpy(tokens).to(dev)
+    par_d = torch.from_numpy(np.asarray(td.parents, np.int32)).to(dev)
+    out = model.outputs(M)
+    ctx0 = kv.ctx_len.clone()
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        kv.ctx_len.copy_(ctx0, non_blocking=True)
+        model.verify(tok_d, par_d, kv, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    st = model.status()
+    if st != 0:
+        raise SystemExit(f"device status {st} after warm-up")
+    acc_len = int(out["accepted_len"][0])
+    launches = model.last_launches()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-resident timed region
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                step()
+            e1.record(stream)
+        barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    clocks = clk.summary()
+
+    # ---- end to end through the public API with host buffers
+    tok_h = torch.from_numpy(tokens).pin_memory()
+    par_h = torch.from_numpy(np.asarray(td.parents, np.int32)).pin_memory()
+    res_h = {k: torch.empty_like(out[k], device="cpu").pin_memory() for k in ("accepted_len", "accepted_tokens",
+                                                                                 "bonus")}
+
+    def e2e_step():
+        tok_d.copy_(tok_h, non_blocking=True)
+        par_d.copy_(par_h, non_blocking=True)
+        step()
+        for k, h in res_h.items():
+            h.copy_(out[k], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+    barrier()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    h2d = tok_h.numel() * 4 + par_h.numel() * 4 + 4
+    d2h = sum(h.numel() * 4 for h in res_h.values())
+
+    # ---- per-kernel timing pass (events around each kernel group)
+    model.set_timing(True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    tl = model.timeline()
+    model.set_timing(False)
+
+    if dist is not None:
+        t = torch.tensor([ms, ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_e2e = float(t[0]), float(t[1])
+
+    pk, pk_src = peaks()
+    gemm = [(k, t, b) for k, t, b in tl if k.startswith("gemm")]
+    g_ms = sum(t for _, t, _ in gemm)
+    g_bytes = sum(b for _, _, b in gemm)
+    achieved = g_bytes / (g_ms * 1e-3) / 1e9 if g_ms > 0 else None
+    peak = pk["hbm_gbs"]
+    step_bytes = model.packed_bytes + kv_bytes_per_step(shape, ctx, M)
+    # the pages' per-kernel lower bound: max(FLOPs at 60% of dense peak, bytes at 90% of bandwidth)
+    flops = 2.0 * M * (shape.n_weights())
+    P = pk["bf16_tflops"] * 1e12
+    bound_s = sum(max(2.0 * M * (b / 1.5) / (0.6 * P), b / (0.9 * NOMINAL_BW_GBS * 1e9)) for _, _, b in gemm)
+    bound_s += kv_bytes_per_step(shape, ctx, M) / (0.9 * NOMINAL_BW_GBS * 1e9)
+    by_kind = {}
+    for k, t, b in tl:
+        a = by_kind.setdefault(k, [0, 0.0, 0.0])
+        a[0] += 1
+        a[1] += t
+        a[2] += b
+    if args.timeline:
+        log(json.dumps({k: {"launches": v[0], "ms": round(v[1], 4), "GB/s": round(v[2] / v[1] / 1e6, 1) if v[2] else None}
+                        for k, v in by_kind.items()}))
+    value = world * M / (ms * 1e-3)
+    res = {
+        "metric": "tree_tokens_per_s", "value": value, "unit": "tree tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "verify_step_us": ms * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "model": shape.name, "layers": shape.n_layers, "M": M,
+                   "max_depth": spec.max_depth, "ctx": ctx, "p_copy": spec.p, "accepted_len": acc_len,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (packed weights %.1f GB)" % (model.packed_bytes / 1e9)},
+        "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
+        "hbm_frac_of_8tbs": step_bytes / (ms * 1e-3) / 1e9 / NOMINAL_BW_GBS,
+        "step_bytes": step_bytes, "step_flops": flops,
+        "step_lower_bound_us": bound_s * 1e6,
+        "frac_of_step_lower_bound": bound_s / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak if achieved else None, "traffic": None,
+                     "kernel": "k_w12_gemm (all GEMM launches of a step, event-timed)",
+                     "peak_source": pk_src},
+        "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in by_kind.items()},
+        "e2e": {"value": world * M / (ms_e2e * 1e-3), "unit": "tree tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        per_layer, t_lm, thr = oracle_sample(shape, args.seed, M, ctx, td.parents, tokens, n_layers=1)
+        est = per_layer * shape.n_layers + t_lm
+        res["cpu_baseline"] = {"value": M / est, "unit": "tree tokens/s", "cores": thr, "kind": "oracle",
+                               "sample": f"oracle forward of layer 0 + lm_head/argmax (M={M}, ctx={ctx}); "
+                                         f"step estimated as layer x {shape.n_layers} + lm_head"}
+    model.close()
+    return res
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    dist = None
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist_mod
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    res = gpu_arm(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -275,6 +275,27 @@ int sd_status(sd_model* m, int32_t* status_host);
  * call launched. */
 int sd_model_last_launches(sd_model* m);
 
+/* Kernel kinds reported by sd_model_timeline. */
+enum {
+  SD_K_TREE = 0, SD_K_NORM = 1, SD_K_GEMM_QKV = 2, SD_K_ATTN = 3, SD_K_LINREC = 4, SD_K_GEMM_O = 5,
+  SD_K_GEMM_GATE_UP = 6, SD_K_GEMM_DOWN = 7, SD_K_GEMM_LM_HEAD = 8, SD_K_ACCEPT = 9, SD_K_COMMIT = 10
+};
+
+/* Per-kernel timing of the following model calls: with enable = 1 every
+ * kernel group of a step is bracketed by CUDA events on the call's stream.
+ * The events serialise kernels that would otherwise overlap through
+ * programmatic dependent launch, so timed steps are slower than untimed
+ * ones; use the numbers for the breakdown, not for the step time. */
+int sd_model_set_timing(sd_model* m, int32_t enable);
+
+/* Timeline of the last timed call: for entry i, kind_host[i] (SD_K_*),
+ * ms_host[i] (event-measured duration; SD_K_ATTN covers the split kernel and
+ * its combine) and bytes_host[i] (algorithmic bytes of a GEMM: packed words,
+ * escape list, row pointers, activations read and written; 0 for other
+ * kinds).  Synchronises the device.  Returns the number of entries written
+ * (<= max), or -1 with sd_last_error set. */
+int sd_model_timeline(sd_model* m, int32_t max, int32_t* kind_host, float* ms_host, double* bytes_host);
+
 #ifdef __cplusplus
 }
 #endif

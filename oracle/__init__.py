@@ -412,14 +412,15 @@ class ForwardOut:
     infos: list                    # TreeInfo per request
 
 
-def forward(shape, weights, requests: list) -> ForwardOut:
+def forward(shape, weights, requests: list, n_layers: int | None = None) -> ForwardOut:
     """One verify forward over the draft trees of all requests.
 
     Every GEMM sees the rows of all requests together (rows never interact);
     attention and recurrence act per request.  Layer order (pre-norm):
       h = x + O(mix(RMSNorm(x)));  x' = h + down(silu(gate(n)) * up(n)), n = RMSNorm(h)
     with mix = tree attention (RoPE on q,k at position ctx + depth) or the
-    tree linear recurrence.  Final RMSNorm then lm_head."""
+    tree linear recurrence.  Final RMSNorm then lm_head.  ``n_layers`` runs
+    only the first layers (a bounded sample for timing)."""
     hd, Hq, Hkv, eps = shape.hd, shape.Hq, shape.Hkv, shape.eps
     infos = [tree_info(r.parents) for r in requests]
     for inf in infos:
@@ -431,7 +432,8 @@ def forward(shape, weights, requests: list) -> ForwardOut:
     x = weights.embed_rows(tokens)                                      # bf16 [Mt][H]
     pos = np.concatenate([r.ctx + inf.depth for r, inf in zip(requests, infos)])
     new_kv = []
-    for l, kind in enumerate(shape.layer_kinds):
+    kinds = shape.layer_kinds if n_layers is None else shape.layer_kinds[:n_layers]
+    for l, kind in enumerate(kinds):
         xn = rmsnorm(x, weights.norm(l, "attn"), eps)
         if kind == "attn":
             q = linear_bf16(xn, weights.layer(l, "wq")).reshape(Mt, Hq, hd)

@@ -86,7 +86,12 @@ _SIGS = {
     "sd_verify_batch": (ctypes.c_int, [vp, vp, vp, vp, i32, P(PagedKV), vp, vp, vp, vp, vp, vp]),
     "sd_status": (ctypes.c_int, [vp, vp]),
     "sd_model_last_launches": (ctypes.c_int, [vp]),
+    "sd_model_set_timing": (ctypes.c_int, [vp, i32]),
+    "sd_model_timeline": (ctypes.c_int, [vp, i32, vp, vp, vp]),
 }
+
+KERNEL_KINDS = ["tree", "rmsnorm", "gemm_qkv", "attention", "linrec", "gemm_o", "gemm_gate_up", "gemm_down",
+                "gemm_lm_head", "accept", "commit"]
 
 _lib = None
 _lock = threading.Lock()

@@ -36,6 +36,11 @@ struct sd_model {
   std::map<int, sdv::XMap> map_xn, map_attn, map_act;
   std::vector<int32_t> cu_host;  // last uploaded cu
   int last_launches = 0;
+  // optional per-kernel timing
+  bool timing = false;
+  std::vector<cudaEvent_t> events;  // 2 per entry
+  std::vector<int32_t> t_kind;
+  std::vector<double> t_bytes;
 };
 
 namespace sdv {
@@ -79,17 +84,49 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   int launches = 0;
   const int rows = io.rows;
   int rc;
-#define LK(expr)                                        \
+  m->t_kind.clear();
+  m->t_bytes.clear();
+  // bracket one kernel group with events when timing is on
+  auto tbegin = [&](int kind, double bytes) -> int {
+    if (!m->timing) return SD_OK;
+    const size_t i = m->t_kind.size();
+    while (m->events.size() < 2 * (i + 1)) {
+      cudaEvent_t e;
+      SD_CK(cudaEventCreate(&e));
+      m->events.push_back(e);
+    }
+    m->t_kind.push_back(kind);
+    m->t_bytes.push_back(bytes);
+    SD_CK(cudaEventRecord(m->events[2 * i], s));
+    return SD_OK;
+  };
+  auto tend = [&]() -> int {
+    if (!m->timing) return SD_OK;
+    SD_CK(cudaEventRecord(m->events[2 * (m->t_kind.size() - 1) + 1], s));
+    return SD_OK;
+  };
+  auto gbytes = [&](const w12_tensor& W, int epi) -> double {
+    double b = (double)W.N * W.K * 1.5 + (double)W.n_escapes * 6.0 + (double)(W.N + 1) * 4.0;
+    b += (double)rows * W.K * 2.0;                                        // activations read
+    b += (double)rows * W.N * (epi == EPI_SILU ? 1.0 : 2.0);              // outputs written
+    if (epi == EPI_RESID) b += (double)rows * W.N * 2.0;                  // residual read
+    return b;
+  };
+#define LK(kind, expr)                                  \
   do {                                                  \
+    if ((rc = tbegin(kind, 0.0))) return rc;            \
     cudaError_t _e = (expr);                            \
     if (_e != cudaSuccess) return cuda_fail(_e, #expr); \
+    if ((rc = tend())) return rc;                       \
     launches++;                                         \
   } while (0)
-#define GK(expr)       \
-  do {                 \
-    rc = (expr);       \
-    if (rc) return rc; \
-    launches += rows > 128 ? 2 : 1; \
+#define GK(kind, W, EPI, expr)                           \
+  do {                                                   \
+    if ((rc = tbegin(kind, gbytes(W, EPI)))) return rc;  \
+    rc = (expr);                                         \
+    if (rc) return rc;                                   \
+    if ((rc = tend())) return rc;                        \
+    launches += rows > 128 ? 2 : 1;                      \
   } while (0)
 
   XMap *mx, *ma, *mc;
@@ -98,8 +135,8 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   if ((rc = get_map(m->map_act, m->act, m->max_rows, m->I, rows, &mc))) return rc;
 
   const StepRows sr{m->ctx_snap, m->req_ok, m->pos, m->slotv, m->req, m->depth, m->anc};
-  LK(launch_tree(io.tokens, io.parents, m->cu, io.R, io.cv, m->V, m->cfg.max_positions, sr, m->status, s, pdl));
-  LK(launch_rmsnorm(nullptr, m->layers[0].attn_norm, rows, m->H, m->cfg.rms_eps, m->xn, io.tokens, m->w.embed, m->x,
+  LK(SD_K_TREE, launch_tree(io.tokens, io.parents, m->cu, io.R, io.cv, m->V, m->cfg.max_positions, sr, m->status, s, pdl));
+  LK(SD_K_NORM, launch_rmsnorm(nullptr, m->layers[0].attn_norm, rows, m->H, m->cfg.rms_eps, m->xn, io.tokens, m->w.embed, m->x,
                     m->req, m->req_ok, s, pdl));
 
   const int rpg = attn_rows_per_group(m->Hq, m->Hkv, m->max_m);
@@ -132,7 +169,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
       eq.out = m->qkv_rec + (int64_t)ls * m->max_rows * 3 * m->H;
       eq.ldo = 3 * m->H;
     }
-    GK(gemm_launch(Lw.qkv, m->xn, *mx, rows, eq, m->gws, m->status, s, pdl));
+    GK(SD_K_GEMM_QKV, Lw.qkv, eq.epi, gemm_launch(Lw.qkv, m->xn, *mx, rows, eq, m->gws, m->status, s, pdl));
     if (is_attn) {
       AttnArgs aa{};
       aa.q = m->q;
@@ -154,8 +191,10 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
       aa.part_o = m->attn_o;
       aa.part_ml = m->attn_ml;
       aa.out = m->attn;
+      if ((rc = tbegin(SD_K_ATTN, 0.0))) return rc;
       const cudaError_t e = launch_attention(aa, rows, s, pdl);
       if (e != cudaSuccess) return cuda_fail(e, "attention");
+      if ((rc = tend())) return rc;
       launches += 2;
     } else {
       LinrecArgs la{};
@@ -172,29 +211,29 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
       la.H = m->H;
       la.eps = m->cfg.rec_eps;
       la.out = m->attn;
-      LK(launch_linrec(la, s, pdl));
+      LK(SD_K_LINREC, launch_linrec(la, s, pdl));
     }
     GemmEpilogue eo;  // h = x + O(attn)
     eo.epi = EPI_RESID;
     eo.out = m->h;
     eo.resid = m->x;
     eo.ldo = m->H;
-    GK(gemm_launch(Lw.o, m->attn, *ma, rows, eo, m->gws, m->status, s, pdl));
-    LK(launch_rmsnorm(m->h, Lw.mlp_norm, rows, m->H, m->cfg.rms_eps, m->xn, nullptr, nullptr, nullptr, nullptr,
+    GK(SD_K_GEMM_O, Lw.o, EPI_RESID, gemm_launch(Lw.o, m->attn, *ma, rows, eo, m->gws, m->status, s, pdl));
+    LK(SD_K_NORM, launch_rmsnorm(m->h, Lw.mlp_norm, rows, m->H, m->cfg.rms_eps, m->xn, nullptr, nullptr, nullptr, nullptr,
                       nullptr, s, pdl));
     GemmEpilogue eg;
     eg.epi = EPI_SILU;
     eg.out = m->act;
     eg.ldo = m->I;
-    GK(gemm_launch(Lw.gate_up, m->xn, *mx, rows, eg, m->gws, m->status, s, pdl));
+    GK(SD_K_GEMM_GATE_UP, Lw.gate_up, EPI_SILU, gemm_launch(Lw.gate_up, m->xn, *mx, rows, eg, m->gws, m->status, s, pdl));
     GemmEpilogue ed;  // x = h + down(act)
     ed.epi = EPI_RESID;
     ed.out = m->x;
     ed.resid = m->h;
     ed.ldo = m->H;
-    GK(gemm_launch(Lw.down, m->act, *mc, rows, ed, m->gws, m->status, s, pdl));
+    GK(SD_K_GEMM_DOWN, Lw.down, EPI_RESID, gemm_launch(Lw.down, m->act, *mc, rows, ed, m->gws, m->status, s, pdl));
     const uint16_t* gnext = l + 1 < m->cfg.n_layers ? m->layers[l + 1].attn_norm : m->w.final_norm;
-    LK(launch_rmsnorm(m->x, gnext, rows, m->H, m->cfg.rms_eps, m->xn, nullptr, nullptr, nullptr, nullptr, nullptr, s,
+    LK(SD_K_NORM, launch_rmsnorm(m->x, gnext, rows, m->H, m->cfg.rms_eps, m->xn, nullptr, nullptr, nullptr, nullptr, nullptr, s,
                       pdl));
   }
   GemmEpilogue el;
@@ -204,7 +243,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   el.amax_val = m->amax_val;
   el.amax_idx = m->amax_idx;
   el.ld_amax = m->max_rows;
-  GK(gemm_launch(m->w.lm_head, m->xn, *mx, rows, el, m->gws, m->status, s, pdl));
+  GK(SD_K_GEMM_LM_HEAD, m->w.lm_head, EPI_LOGITS, gemm_launch(m->w.lm_head, m->xn, *mx, rows, el, m->gws, m->status, s, pdl));
 
   AcceptArgs ac{};
   ac.tokens = io.tokens;
@@ -225,11 +264,11 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   ac.path = m->path;
   ac.path_len = m->path_len;
   ac.status = m->status;
-  LK(launch_accept(ac, s, pdl));
+  LK(SD_K_ACCEPT, launch_accept(ac, s, pdl));
   if (io.commit) {
-    if (m->n_attn) LK(launch_compact(io.cv, m->n_attn, m->Hkv, io.R, m->ctx_snap, m->path, m->path_len, s, pdl));
+    if (m->n_attn) LK(SD_K_COMMIT, launch_compact(io.cv, m->n_attn, m->Hkv, io.R, m->ctx_snap, m->path, m->path_len, s, pdl));
     if (m->n_rec)
-      LK(launch_rec_commit(io.cv, m->n_rec, m->nh_rec, m->H, io.R, m->max_rows, m->qkv_rec, m->cu, m->path,
+      LK(SD_K_COMMIT, launch_rec_commit(io.cv, m->n_rec, m->nh_rec, m->H, io.R, m->max_rows, m->qkv_rec, m->cu, m->path,
                            m->path_len, s, pdl));
   }
 #undef LK
@@ -426,6 +465,7 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
 
 extern "C" int sd_model_destroy(sd_model* m) {
   if (!m) return SD_OK;
+  for (cudaEvent_t e : m->events) cudaEventDestroy(e);
   cudaFree(m->arena);
   delete m;
   return SD_OK;
@@ -543,3 +583,32 @@ extern "C" int sd_status(sd_model* m, int32_t* status_host) {
 }
 
 extern "C" int sd_model_last_launches(sd_model* m) { return m ? m->last_launches : 0; }
+
+extern "C" int sd_model_set_timing(sd_model* m, int32_t enable) {
+  if (!m) {
+    set_error("sd_model_set_timing: null model");
+    return SD_ERR_INVALID_ARG;
+  }
+  m->timing = enable != 0;
+  return SD_OK;
+}
+
+extern "C" int sd_model_timeline(sd_model* m, int32_t max, int32_t* kind_host, float* ms_host, double* bytes_host) {
+  if (!m || max < 0 || (max > 0 && (!kind_host || !ms_host || !bytes_host))) {
+    set_error("sd_model_timeline: bad argument");
+    return -1;
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    set_error("sd_model_timeline: device error");
+    return -1;
+  }
+  const int n = std::min<int>(max, (int)m->t_kind.size());
+  for (int i = 0; i < n; i++) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, m->events[2 * i], m->events[2 * i + 1]) != cudaSuccess) ms = -1.f;
+    kind_host[i] = m->t_kind[i];
+    ms_host[i] = ms;
+    bytes_host[i] = m->t_bytes[i];
+  }
+  return n;
+}

@@ -186,6 +186,20 @@ class Model:
     def last_launches(self) -> int:
         return int(lib().sd_model_last_launches(self.handle))
 
+    def set_timing(self, on: bool):
+        check(lib().sd_model_set_timing(self.handle, 1 if on else 0))
+
+    def timeline(self, max_entries: int = 4096):
+        """[(kind name, ms, algorithmic bytes)] of the last timed call."""
+        from . import KERNEL_KINDS
+        k = np.zeros(max_entries, np.int32)
+        ms = np.zeros(max_entries, np.float32)
+        b = np.zeros(max_entries, np.float64)
+        n = lib().sd_model_timeline(self.handle, max_entries, k.ctypes.data, ms.ctypes.data, b.ctypes.data)
+        if n < 0:
+            check(3)
+        return [(KERNEL_KINDS[k[i]], float(ms[i]), float(b[i])) for i in range(n)]
+
     def outputs(self, M: int, logits: bool = False, R: int = 1):
         d = self.device
         o = {"accepted_len": torch.zeros(R, dtype=torch.int32, device=d),

@@ -35,7 +35,7 @@ def test_tiny_verify(M):
     assert int(o["status"][0]) == 0
     assert_close(_np(o["logits"]), lo)
     am = _np(o["argmax"])
-    assert_argmax(am, am_o, margin)
+    assert_argmax(am, am_o, margin, lo)
     assert_accept(tokens, t.draft.parents, am, int(o["accepted_len"][0]), _np(o["accepted_tokens"]),
                   int(o["bonus"][0]), am_o)
     assert int(o["accepted_len"][0]) >= 1
@@ -72,7 +72,7 @@ def _verify_case(M, shape, W, model, td, ctx, seed=3):
     assert model.status() == 0
     assert_close(_np(o["logits"]), out.logits)
     am = _np(o["argmax"])
-    diff = assert_argmax(am, out.argmax, out.margin)
+    diff = assert_argmax(am, out.argmax, out.margin, out.logits)
     assert_accept(tokens, td.parents, am, int(o["accepted_len"][0]), _np(o["accepted_tokens"]), int(o["bonus"][0]),
                   out.argmax)
     L = int(o["accepted_len"][0])
@@ -140,7 +140,7 @@ def test_batched_paged_equals_oracle(M, dec):
     assert model.status() == 0
     assert_close(_np(o["logits"]), out.logits)
     am = _np(o["argmax"])
-    assert_argmax(am, out.argmax, out.margin)
+    assert_argmax(am, out.argmax, out.margin, out.logits)
     for r in range(3):
         a, b = cu[r], cu[r + 1]
         assert_accept(toks[r], drafts[r].parents, am[a:b], int(o["accepted_len"][r]), _np(o["accepted_tokens"][a:b]),
