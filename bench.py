@@ -51,7 +51,43 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--timeline", action="store_true", help="print the per-kernel breakdown to stderr")
+    ap.add_argument("--nvtx", action="store_true", help="wrap the timed steps in the NVTX range 'sdv_step'")
+    ap.add_argument("--probe", default=None, metavar="N,K,M",
+                    help="time the fused W12 linear alone on an N x K tensor with M rows")
     return ap.parse_args()
+
+
+def probe_arm(args):
+    """The fused W12 GEMM alone (sd_w12_linear) on a seeded N x K tensor:
+    per-launch time with CUDA events, algorithmic GB/s."""
+    import numpy as np
+    import torch
+    import synthetic
+    from speculative_decoding_tree_bit_gb300 import _build
+    from speculative_decoding_tree_bit_gb300 import model as Mdl
+    _build.build()
+    N, K, M = (int(v) for v in args.probe.split(","))
+    w = synthetic.normal_bf16(synthetic.key(args.seed, 4242), N * K, 0.02).reshape(N, K)
+    p = Mdl.pack(Mdl.to_device_u16(w))
+    del w
+    x = Mdl.to_device_u16(synthetic.normal_bf16(synthetic.key(args.seed, 4243), M * K, 1.0).reshape(M, K))
+    import speculative_decoding_tree_bit_gb300 as sdv
+    ws = Mdl.Workspace(int(sdv.lib().sd_w12_linear_workspace(N, K, M)))
+    for _ in range(args.warmup):
+        Mdl.linear(p, x, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        Mdl.linear(p, x, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    nbytes = p.nbytes() + M * K * 2 + M * N * 2
+    pk, src = peaks()
+    return {"probe": "sd_w12_linear", "N": N, "K": K, "M": M, "us_per_launch": us,
+            "GBps": nbytes / (us * 1e-6) / 1e9, "frac_of_peak": nbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"],
+            "peak_source": src, "bytes": nbytes, "escapes": p.n_escapes}
 
 
 def log(*a):
@@ -237,11 +273,17 @@ def gpu_arm(args, rank, world, dist):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
+        if args.nvtx:
+            torch.cuda.nvtx.range_push("sdv_step")
+        t_host = time.perf_counter()
         with torch.cuda.stream(stream):
             e0.record(stream)
             for _ in range(args.steps):
                 step()
             e1.record(stream)
+        t_host = (time.perf_counter() - t_host) / args.steps
+        if args.nvtx:
+            torch.cuda.nvtx.range_pop()
         barrier()
     ms = e0.elapsed_time(e1) / args.steps
     clocks = clk.summary()
@@ -311,7 +353,7 @@ def gpu_arm(args, rank, world, dist):
     res = {
         "metric": "tree_tokens_per_s", "value": value, "unit": "tree tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "verify_step_us": ms * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "verify_step_us": ms * 1e3, "host_submit_us_per_step": t_host * 1e6, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "model": shape.name, "layers": shape.n_layers, "M": M,
                    "max_depth": spec.max_depth, "ctx": ctx, "p_copy": spec.p, "accepted_len": acc_len,
@@ -347,6 +389,9 @@ def main():
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     dist = None
+    if args.probe:
+        print(json.dumps(probe_arm(args)), flush=True)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(reference_arm(args)), flush=True)
