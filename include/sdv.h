@@ -124,6 +124,22 @@ size_t sd_w12_linear_workspace(int64_t N, int64_t K, int32_t M);
 int sd_w12_linear(const w12_tensor* W, const uint16_t* x, int32_t M, uint16_t* y, void* workspace,
                   size_t workspace_bytes, void* stream);
 
+/* The same linear for callers that cannot allocate device memory: a host
+ * framework that owns all device memory through its own pool, a real-time
+ * thread that must not take cudaMalloc's implicit synchronisation, a plug-in
+ * that may not grow the process's device footprint.  No counterpart in the
+ * SpecPilot pages; it is a packaging variant of sd_w12_linear.  The split-K
+ * scratch lives in a static device array inside the library (about 9.5 MiB
+ * that every GPU loading the library holds until the process exits), so the
+ * call allocates nothing; the caller passes only W, x and y.
+ * Limits: 1 <= M <= 64 and N <= 262144, else SD_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address (with that
+ * device current), so make that first call before any stream capture.
+ * Every call on a device shares the one array: calls that can overlap on the
+ * GPU (different streams without ordering between them) race and give wrong
+ * results; serialise them. */
+int sd_w12_linear_static(const w12_tensor* W, const uint16_t* x, int32_t M, uint16_t* y, void* stream);
+
 /* ------------------------------------------------------ tree helpers -- */
 /* [TREE] Validate one draft tree (parents[0] == -1, 0 <= parents[i] < i,
  * M <= 64) and derive per node the ancestor bitmask anc[i] = anc[parent[i]]

@@ -494,7 +494,7 @@ int make_x_map(XMap* xm, const uint16_t* x, int rows_total, int64_t K, int box_r
 }
 
 template <int NT, bool AFF>
-static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, cudaStream_t s, bool pdl) {
+static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, cudaStream_t s, bool pdl, int grid) {
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e =
@@ -502,11 +502,12 @@ static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, cudaSt
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch(k_w12_gemm<NT, AFF>, dim3(gemm_grid()), dim3(kThreads), Cfg<NT>::SMEM, s, pdl, p, map);
+  return launch(k_w12_gemm<NT, AFF>, dim3(grid), dim3(kThreads), Cfg<NT>::SMEM, s, pdl, p, map);
 }
 
 int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
-                const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl) {
+                const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid) {
+  if (grid <= 0) grid = gemm_grid();
   if (W.N % 16 || W.K % 64 || M < 1 || M > 256) {
     set_error("gemm: unsupported shape");
     return SD_ERR_UNSUPPORTED;
@@ -544,7 +545,7 @@ int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, c
     set_error("gemm: tensor map box does not match the row count");
     return SD_ERR_INVALID_ARG;
   }
-  if (ws.partial_floats < (size_t)gemm_grid() * 2 * kRB * NT * 128) {
+  if (ws.partial_floats < (size_t)grid * 2 * kRB * NT * 128) {
     set_error("gemm: workspace too small");
     return SD_ERR_WORKSPACE;
   }
@@ -553,11 +554,11 @@ int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, c
     p.m0 = m0;
     cudaError_t e;
     switch (NT) {
-      case 1: e = aff ? launch_nt<1, true>(p, xm.map, s, pdl) : launch_nt<1, false>(p, xm.map, s, pdl); break;
-      case 2: e = aff ? launch_nt<2, true>(p, xm.map, s, pdl) : launch_nt<2, false>(p, xm.map, s, pdl); break;
-      case 4: e = aff ? launch_nt<4, true>(p, xm.map, s, pdl) : launch_nt<4, false>(p, xm.map, s, pdl); break;
-      case 8: e = aff ? launch_nt<8, true>(p, xm.map, s, pdl) : launch_nt<8, false>(p, xm.map, s, pdl); break;
-      default: e = aff ? launch_nt<16, true>(p, xm.map, s, pdl) : launch_nt<16, false>(p, xm.map, s, pdl); break;
+      case 1: e = aff ? launch_nt<1, true>(p, xm.map, s, pdl, grid) : launch_nt<1, false>(p, xm.map, s, pdl, grid); break;
+      case 2: e = aff ? launch_nt<2, true>(p, xm.map, s, pdl, grid) : launch_nt<2, false>(p, xm.map, s, pdl, grid); break;
+      case 4: e = aff ? launch_nt<4, true>(p, xm.map, s, pdl, grid) : launch_nt<4, false>(p, xm.map, s, pdl, grid); break;
+      case 8: e = aff ? launch_nt<8, true>(p, xm.map, s, pdl, grid) : launch_nt<8, false>(p, xm.map, s, pdl, grid); break;
+      default: e = aff ? launch_nt<16, true>(p, xm.map, s, pdl, grid) : launch_nt<16, false>(p, xm.map, s, pdl, grid); break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "k_w12_gemm launch");
   }

@@ -67,7 +67,9 @@ struct XMap {
 int make_x_map(XMap* xm, const uint16_t* x, int rows_total, int64_t K, int box_rows);
 
 // y = epilogue(x W^T) for rows [0, M); M > 128 runs in launches of 128 rows.
+// grid: CTAs per launch, 0 = gemm_grid(); the partial-sum workspace must
+// hold grid * 2 * 8 * (padded rows / 8) * 128 floats.
 int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
-                const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl);
+                const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid = 0);
 
 }  // namespace sdv
