@@ -291,6 +291,15 @@ int sd_status(sd_model* m, int32_t* status_host);
  * call launched. */
 int sd_model_last_launches(sd_model* m);
 
+/* Step execution mode.  With enable = 1 (the default), a call on a
+ * non-default stream that is not itself being captured is recorded once per
+ * distinct argument set (every pointer and size) into a CUDA graph, which is
+ * replayed by later calls with the same arguments: no per-kernel launch cost
+ * on the host.  Up to 16 graphs are kept per model.  enable = 0 launches the
+ * kernels directly every call (also the behaviour on the legacy default
+ * stream and inside a caller's own stream capture). */
+int sd_model_set_graphs(sd_model* m, int32_t enable);
+
 /* Kernel kinds reported by sd_model_timeline. */
 enum {
   SD_K_TREE = 0, SD_K_NORM = 1, SD_K_GEMM_QKV = 2, SD_K_ATTN = 3, SD_K_LINREC = 4, SD_K_GEMM_O = 5,
@@ -298,10 +307,11 @@ enum {
 };
 
 /* Per-kernel timing of the following model calls: with enable = 1 every
- * kernel group of a step is bracketed by CUDA events on the call's stream.
- * The events serialise kernels that would otherwise overlap through
- * programmatic dependent launch, so timed steps are slower than untimed
- * ones; use the numbers for the breakdown, not for the step time. */
+ * kernel group of a step is bracketed by CUDA events on the call's stream
+ * (captured into the step's graph when graphs are on, so host launch gaps do
+ * not enter the times).  The events serialise kernels that would otherwise
+ * overlap through programmatic dependent launch, so timed steps are slower
+ * than untimed ones; use the numbers for the breakdown, not the step time. */
 int sd_model_set_timing(sd_model* m, int32_t enable);
 
 /* Timeline of the last timed call: for entry i, kind_host[i] (SD_K_*),

@@ -88,6 +88,7 @@ _SIGS = {
     "sd_status": (ctypes.c_int, [vp, vp]),
     "sd_model_last_launches": (ctypes.c_int, [vp]),
     "sd_model_set_timing": (ctypes.c_int, [vp, i32]),
+    "sd_model_set_graphs": (ctypes.c_int, [vp, i32]),
     "sd_model_timeline": (ctypes.c_int, [vp, i32, vp, vp, vp]),
 }
 

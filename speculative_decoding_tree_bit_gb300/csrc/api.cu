@@ -123,9 +123,9 @@ static TinyLayout tiny_layout(int64_t N1, int64_t V, int M) {
   L.counters = o;
   o = al256(o + (size_t)L.counters_len * 4);
   L.amax_val = o;
-  o = al256(o + (size_t)gemm_grid() * M * 4);
+  o = al256(o + (size_t)gemm_grid(M) * M * 4);
   L.amax_idx = o;
-  o = al256(o + (size_t)gemm_grid() * M * 4);
+  o = al256(o + (size_t)gemm_grid(M) * M * 4);
   L.total = o;
   return L;
 }
@@ -191,7 +191,7 @@ extern "C" int sd_tiny_verify(const w12_tensor* W1, const w12_tensor* Wlm, const
   a.single_M = M;
   a.amax_val = av;
   a.amax_idx = ai;
-  a.n_part = gemm_grid();
+  a.n_part = gemm_grid(M);
   a.ld = M;
   a.argmax_out = argmax;
   a.accepted_len = accepted_len;

@@ -217,8 +217,11 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int strip, int lan
     }
 }
 
+template <int NT>
+constexpr int ctas_per_sm() { return NT <= 4 ? 2 : 1; }
+
 template <int NT, bool AFFINE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
     k_w12_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap xmap) {
   using C = Cfg<NT>;
   extern __shared__ uint8_t smem_raw[];
@@ -250,32 +253,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------- producer --
     if (lane == 0) {
       const int64_t n = u1 - u0;
-      const int pre = (int)(n < C::S ? n : C::S);
-      for (int i = 0; i < pre; i++) {
-        const int64_t u = u0 + i;
-        const int b = (int)(u / KT), t = (int)(u % KT);
-        const int ns = min(kRB, p.NS - b * kRB);
-        mbar_arrive_expect_tx(&full[i], ns * kStripBytes + C::XB);
-        for (int r = 0; r < ns; r++)
-          bulk_g2s(sw + i * C::WB + r * kStripBytes, p.words + ((int64_t)(b * kRB + r) * KT + t) * 384, kStripBytes,
-                   &full[i]);
-      }
-      pdl_wait();  // activations come from the previous kernel
-      for (int i = 0; i < pre; i++) tma2d_g2s(sx + i * C::XB, &xmap, (int)((u0 + i) % KT) * 64, p.m0, &full[i]);
-      for (int64_t i = pre; i < n; i++) {
-        const int slot = (int)(i % C::S);
-        if (!mbar_wait(&empty[slot], (uint32_t)(((i / C::S) & 1) ^ 1))) {
-          set_status(p.status, SD_ERR_TIMEOUT);
-          break;
+      if (n > 0) {
+        const int pre = (int)(n < C::S ? n : C::S);
+        const int64_t strip_words = (int64_t)KT * 384;  // one strip's full K range
+        int b = (int)(u0 / KT), t = (int)(u0 % KT);
+        const int b_first = b, t_first = t;
+        auto issue_weights = [&](int slot, int bb, int tt) {
+          const int ns = min(kRB, p.NS - bb * kRB);
+          mbar_arrive_expect_tx(&full[slot], ns * kStripBytes + C::XB);
+          const uint32_t* src = p.words + (int64_t)bb * kRB * strip_words + (int64_t)tt * 384;
+          uint8_t* dst = sw + slot * C::WB;
+          for (int r = 0; r < ns; r++) bulk_g2s(dst + r * kStripBytes, src + r * strip_words, kStripBytes, &full[slot]);
+        };
+        for (int i = 0; i < pre; i++) {
+          issue_weights(i, b, t);
+          if (++t == KT) {
+            t = 0;
+            b++;
+          }
         }
-        const int64_t u = u0 + i;
-        const int b = (int)(u / KT), t = (int)(u % KT);
-        const int ns = min(kRB, p.NS - b * kRB);
-        mbar_arrive_expect_tx(&full[slot], ns * kStripBytes + C::XB);
-        for (int r = 0; r < ns; r++)
-          bulk_g2s(sw + slot * C::WB + r * kStripBytes, p.words + ((int64_t)(b * kRB + r) * KT + t) * 384,
-                   kStripBytes, &full[slot]);
-        tma2d_g2s(sx + slot * C::XB, &xmap, t * 64, p.m0, &full[slot]);
+        pdl_wait();  // activations come from the previous kernel
+        {
+          int tt = t_first;
+          for (int i = 0; i < pre; i++) {
+            tma2d_g2s(sx + i * C::XB, &xmap, tt * 64, p.m0, &full[i]);
+            if (++tt == KT) tt = 0;
+          }
+        }
+        (void)b_first;
+        // the loop below runs only when pre == S: stage S reuses slot 0,
+        // whose first use completed phase 0 of its empty barrier
+        int slot = 0;
+        uint32_t par = 0;
+        for (int64_t i = pre; i < n; i++) {
+          if (!mbar_wait(&empty[slot], par)) {
+            set_status(p.status, SD_ERR_TIMEOUT);
+            break;
+          }
+          issue_weights(slot, b, t);
+          tma2d_g2s(sx + slot * C::XB, &xmap, t * 64, p.m0, &full[slot]);
+          if (++t == KT) {
+            t = 0;
+            b++;
+          }
+          if (++slot == C::S) {
+            slot = 0;
+            par ^= 1u;
+          }
+        }
+      } else {
+        pdl_wait();
       }
     }
     return;
@@ -283,7 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // --------------------------------------------------------- consumers --
   pdl_wait();
-  float acc[NT][4];
+  // small tiles: even and odd sub-tiles feed separate accumulators so that
+  // consecutive MMAs do not wait on each other; larger tiles have NT
+  // independent MMAs per sub-tile already
+  constexpr bool kDual = NT <= 4;
+  float acc[NT][4], acc2[kDual ? NT : 1][4];
   float bestv[NT][2];
   int besti[NT][2];
 #pragma unroll
@@ -299,7 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int nt = 0; nt < NT; nt++)
 #pragma unroll
-      for (int c = 0; c < 4; c++) acc[nt][c] = 0.f;
+      for (int c = 0; c < 4; c++) {
+        acc[nt][c] = 0.f;
+        if constexpr (kDual) acc2[nt][c] = 0.f;
+      }
   };
   auto partial_ptr = [&](int64_t cta, int slot_id) {
     return p.partial + (((cta * 2 + slot_id) * kRB + warp) * NT) * 128 + lane * 4;
@@ -307,6 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // finish the segment [t0, t1) of row block b
   auto finish = [&](int b, int t0, int t1) {
     const int strip = b * kRB + warp;
+    if constexpr (kDual) {
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int c = 0; c < 4; c++) acc[nt][c] += acc2[nt][c];
+    }
     if (!(t0 == 0 && t1 == KT)) {
       const int slot_id = (b == first_b) ? 0 : 1;
       float* dst = partial_ptr(blockIdx.x, slot_id);
@@ -349,17 +389,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   zero();
   int cur_b = -1, seg_t0 = 0;
   bool ok = true;
-  int64_t it = 0;
-  for (int64_t u = u0; u < u1; ++u, ++it) {
-    const int b = (int)(u / KT), t = (int)(u % KT);
+  int b = u1 > u0 ? (int)(u0 / KT) : 0, t = u1 > u0 ? (int)(u0 % KT) : 0;
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int64_t n = u1 - u0; n > 0; --n) {
     if (b != cur_b) {
       if (cur_b >= 0) finish(cur_b, seg_t0, KT);
       cur_b = b;
       seg_t0 = t;
       zero();
     }
-    const int slot = (int)(it % C::S);
-    if (!mbar_wait(&full[slot], (uint32_t)((it / C::S) & 1))) {
+    if (!mbar_wait(&full[slot], phase)) {
       set_status(p.status, SD_ERR_TIMEOUT);
       ok = false;
       break;
@@ -376,25 +416,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t a0, a1, a2, a3;
         decode<AFFINE>(comp(W0, j), comp(W1, j), comp(W2, j), p.base2, p.tab, a0, a1, a2, a3);
         const int kchunk = 2 * j + ((lane >> 3) & 1);
+        // even and odd sub-tiles accumulate into separate sets (shorter MMA chains)
+        float(*A)[4] = (kDual && (j & 1)) ? acc2 : acc;
         if (NT == 1) {
           const int mrow = lane & 7;
           uint32_t b0, b1;
           ldsm_x2(xb + mrow * 128 + ((kchunk ^ mrow) << 4), b0, b1);
-          mma_bf16(acc[0], a0, a1, a2, a3, b0, b1);
+          mma_bf16(A[0], a0, a1, a2, a3, b0, b1);
         } else {
 #pragma unroll
           for (int np = 0; np < NT; np += 2) {
             const int mrow = (np + (lane >> 4)) * 8 + (lane & 7);
             uint32_t b0, b1, b2, b3;
             ldsm_x4(xb + mrow * 128 + ((kchunk ^ (lane & 7)) << 4), b0, b1, b2, b3);
-            mma_bf16(acc[np], a0, a1, a2, a3, b0, b1);
-            mma_bf16(acc[np + 1], a0, a1, a2, a3, b2, b3);
+            mma_bf16(A[np], a0, a1, a2, a3, b0, b1);
+            mma_bf16(A[np + 1], a0, a1, a2, a3, b2, b3);
           }
         }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
+    if (++slot == C::S) {
+      slot = 0;
+      phase ^= 1u;
+    }
+    if (++t == KT) {
+      t = 0;
+      b++;
+    }
   }
   if (ok && cur_b >= 0) finish(cur_b, seg_t0, (int)((u1 - 1) % KT) + 1);
 
@@ -443,14 +493,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host --
 
-int gemm_grid() { return num_sms(); }
-
 int pad_rows(int M) { return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
 
-size_t gemm_partial_floats(int M) {
-  const int NT = pad_rows(std::min(M, 128)) / 8;
-  return (size_t)gemm_grid() * 2 * kRB * NT * 128;
-}
+static int nt_of(int M) { return M > 128 ? 16 : pad_rows(M) / 8; }
+
+int gemm_grid(int M) { return (nt_of(M) <= 4 ? 2 : 1) * num_sms(); }
+
+size_t gemm_partial_floats(int M) { return (size_t)gemm_grid(M) * 2 * kRB * nt_of(M) * 128; }
 
 int gemm_counters(int64_t N) { return (int)((N / 16 + kRB - 1) / kRB); }
 
@@ -507,7 +556,7 @@ static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, cudaSt
 
 int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
                 const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid) {
-  if (grid <= 0) grid = gemm_grid();
+  if (grid <= 0) grid = gemm_grid(M);
   if (W.N % 16 || W.K % 64 || M < 1 || M > 256) {
     set_error("gemm: unsupported shape");
     return SD_ERR_UNSUPPORTED;
@@ -540,7 +589,7 @@ int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, c
     set_error("gemm: workspace counters too small");
     return SD_ERR_WORKSPACE;
   }
-  const int NT = M > 128 ? 16 : pad_rows(M) / 8;
+  const int NT = nt_of(M);
   if (xm.box_rows != NT * 8) {
     set_error("gemm: tensor map box does not match the row count");
     return SD_ERR_INVALID_ARG;

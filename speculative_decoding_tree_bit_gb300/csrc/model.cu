@@ -36,6 +36,16 @@ struct sd_model {
   std::map<int, sdv::XMap> map_xn, map_attn, map_act;
   std::vector<int32_t> cu_host;  // last uploaded cu
   int last_launches = 0;
+  // captured steps: one executable graph per distinct argument set
+  struct Graph {
+    std::vector<uintptr_t> key;
+    cudaGraphExec_t exec;
+    int launches;
+    std::vector<int32_t> t_kind;  // timeline entries captured with it
+    std::vector<double> t_bytes;
+  };
+  std::vector<Graph> graphs;
+  bool use_graphs = true;
   // optional per-kernel timing
   bool timing = false;
   std::vector<cudaEvent_t> events;  // 2 per entry
@@ -252,7 +262,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   ac.R = io.R;
   ac.amax_val = m->amax_val;
   ac.amax_idx = m->amax_idx;
-  ac.n_part = gemm_grid();
+  ac.n_part = gemm_grid(rows);
   ac.ld = m->max_rows;
   ac.req_ok = m->req_ok;
   ac.ctx_snap = m->ctx_snap;
@@ -275,6 +285,56 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
 #undef GK
   m->last_launches = launches;
   return SD_OK;
+}
+
+// Enqueue one step.  On a non-default stream that is not already capturing,
+// the step is captured once per distinct argument set into a CUDA graph and
+// replayed from then on (no per-kernel host launch cost); the captured
+// kernels keep their programmatic-dependent-launch edges.  The key holds
+// every pointer and size the kernels see, so a replay is the same launch
+// sequence; values behind the pointers are read at run time.
+static int launch_step(sd_model* m, const StepIO& io, cudaStream_t s, std::vector<uintptr_t> key) {
+  if (!m->use_graphs || s == nullptr) return run_step(m, io, s);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  SD_CK(cudaStreamIsCapturing(s, &cs));
+  if (cs != cudaStreamCaptureStatusNone) return run_step(m, io, s);
+  key.push_back(m->timing ? 1 : 0);
+  for (auto& g : m->graphs)
+    if (g.key == key) {
+      SD_CK(cudaGraphLaunch(g.exec, s));
+      m->last_launches = g.launches;
+      m->t_kind = g.t_kind;
+      m->t_bytes = g.t_bytes;
+      return SD_OK;
+    }
+  SD_CK(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+  const int rc = run_step(m, io, s);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(s, &graph);
+  if (rc) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  SD_CK(e);
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  SD_CK(ei);
+  if (m->graphs.size() >= 16) {
+    cudaGraphExecDestroy(m->graphs.front().exec);
+    m->graphs.erase(m->graphs.begin());
+  }
+  m->graphs.push_back({key, exec, m->last_launches, m->t_kind, m->t_bytes});
+  SD_CK(cudaGraphLaunch(exec, s));
+  return SD_OK;
+}
+
+static std::vector<uintptr_t> step_key(const StepIO& io, int M) {
+  auto u = [](const void* p) { return reinterpret_cast<uintptr_t>(p); };
+  return {(uintptr_t)M, (uintptr_t)io.R, (uintptr_t)io.rows, u(io.tokens), u(io.parents), u(io.cv.k_pool),
+          u(io.cv.v_pool), (uintptr_t)io.cv.n_pages, (uintptr_t)io.cv.page_size, u(io.cv.page_table),
+          (uintptr_t)io.cv.max_pages, u(io.cv.S), u(io.cv.z), u(io.cv.ctx_len), u(io.accepted_len),
+          u(io.accepted_tokens), u(io.bonus), u(io.logits), u(io.argmax), (uintptr_t)io.commit};
 }
 
 static int upload_cu(sd_model* m, const std::vector<int32_t>& cu, cudaStream_t s) {
@@ -421,8 +481,8 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
       {(void**)&m->anc, (size_t)MR * 8},
       {(void**)&m->attn_o, units * m->Hkv * rpg * 128 * 4},
       {(void**)&m->attn_ml, units * m->Hkv * rpg * 2 * 4},
-      {(void**)&m->amax_val, (size_t)gemm_grid() * MR * 4},
-      {(void**)&m->amax_idx, (size_t)gemm_grid() * MR * 4},
+      {(void**)&m->amax_val, (size_t)gemm_grid(1) * MR * 4},
+      {(void**)&m->amax_idx, (size_t)gemm_grid(1) * MR * 4},
       {(void**)&m->gws.partial, gemm_partial_floats(MR) * 4},
       {(void**)&m->gws.counters, (size_t)gemm_counters(max_n) * 4},
   };
@@ -465,6 +525,7 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
 
 extern "C" int sd_model_destroy(sd_model* m) {
   if (!m) return SD_OK;
+  for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);
   for (cudaEvent_t e : m->events) cudaEventDestroy(e);
   cudaFree(m->arena);
   delete m;
@@ -511,7 +572,7 @@ static int single_step(sd_model* m, const int32_t* tokens, const int32_t* parent
   io.logits = logits;
   io.argmax = argmax;
   io.commit = commit;
-  return run_step(m, io, s);
+  return launch_step(m, io, s, step_key(io, M));
 }
 
 extern "C" int sd_verify_step(sd_model* m, const int32_t* tree_tokens, const int32_t* parents, int32_t M,
@@ -568,7 +629,9 @@ extern "C" int sd_verify_batch(sd_model* m, const int32_t* tokens, const int32_t
   io.logits = logits;
   io.argmax = argmax;
   io.commit = true;
-  return run_step(m, io, s);
+  std::vector<uintptr_t> key = step_key(io, io.rows);
+  for (int32_t c : cu) key.push_back((uintptr_t)(uint32_t)c);
+  return launch_step(m, io, s, key);
 }
 
 extern "C" int sd_status(sd_model* m, int32_t* status_host) {
@@ -611,4 +674,13 @@ extern "C" int sd_model_timeline(sd_model* m, int32_t max, int32_t* kind_host, f
     bytes_host[i] = m->t_bytes[i];
   }
   return n;
+}
+
+extern "C" int sd_model_set_graphs(sd_model* m, int32_t enable) {
+  if (!m) {
+    set_error("sd_model_set_graphs: null model");
+    return SD_ERR_INVALID_ARG;
+  }
+  m->use_graphs = enable != 0;
+  return SD_OK;
 }

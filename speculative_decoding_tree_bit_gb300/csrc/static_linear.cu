@@ -94,6 +94,6 @@ extern "C" int sd_w12_linear_static(const w12_tensor* W, const uint16_t* x, int3
   e.epi = EPI_STORE;
   e.out = y;
   e.ldo = (int)W->N;
-  const int grid = gemm_grid() < kStaticMaxCtas ? gemm_grid() : kStaticMaxCtas;
+  const int grid = gemm_grid(M) < kStaticMaxCtas ? gemm_grid(M) : kStaticMaxCtas;
   return gemm_launch(*W, x, xm, M, e, ws, nullptr, s, false, grid);
 }

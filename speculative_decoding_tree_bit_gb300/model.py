@@ -186,6 +186,9 @@ class Model:
     def last_launches(self) -> int:
         return int(lib().sd_model_last_launches(self.handle))
 
+    def set_graphs(self, on: bool):
+        check(lib().sd_model_set_graphs(self.handle, 1 if on else 0))
+
     def set_timing(self, on: bool):
         check(lib().sd_model_set_timing(self.handle, 1 if on else 0))
 

@@ -160,3 +160,31 @@ def test_bad_inputs_set_status_and_commit_nothing(M, dec):
     assert model.status() == 7 and int(kv.ctx_len[0]) == ctx
     o = model.verify([1, 2], [-1, 0], kv)  # still usable afterwards
     assert model.status() == 0 and int(kv.ctx_len[0]) == ctx + int(o["accepted_len"][0]) + 1
+
+
+def test_graph_capture_and_replay_match_direct_launches(M, dec):
+    """A step captured into a CUDA graph (first call on a side stream) and its
+    replays give the same bits as direct kernel launches."""
+    shape, W, model = dec
+    ctx = 50
+    td = wl.draft(31, 0, 12, 5, 0.8, shape.V)
+    tok = torch.from_numpy(np.random.default_rng(5).integers(0, shape.V, 12).astype(np.int32)).cuda()
+    par = torch.from_numpy(td.parents.astype(np.int32)).cuda()
+    kv = M.KVCache(shape, ctx + 80).fill(3, ctx)
+    out = model.outputs(12, logits=True)
+    s = torch.cuda.Stream()
+    results = []
+    for graphs in (False, True, True, True):
+        model.set_graphs(graphs)
+        kv.ctx_len.fill_(ctx)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            model.verify(tok, par, kv, out=out, stream=s)
+        s.synchronize()
+        assert model.status() == 0
+        results.append({k: v.clone() for k, v in out.items()} | {"k": kv.k.clone(), "v": kv.v.clone(),
+                                                                 "ctx": kv.ctx_len.clone()})
+    model.set_graphs(True)
+    for r in results[1:]:
+        for k in r:
+            assert torch.equal(r[k], results[0][k]), k
