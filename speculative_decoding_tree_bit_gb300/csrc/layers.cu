@@ -616,4 +616,16 @@ cudaError_t launch_rec_commit(const CacheView& cv, int n_rec, int nh, int H, int
                 path, path_len);
 }
 
+// Busy-waits for `ns` nanoseconds of %globaltimer (bounded by construction).
+// The per-kernel timing mode puts it in front of a step so that the host can
+// enqueue the whole step while the GPU is still busy: the step's kernels then
+// run back to back and the events around them measure GPU time only.
+__global__ void k_delay(uint64_t ns) {
+  const uint64_t t0 = globaltimer();
+  while (globaltimer() - t0 < ns) {
+  }
+}
+
+cudaError_t launch_delay(uint64_t ns, cudaStream_t s) { return launch(k_delay, dim3(1), dim3(1), 0, s, false, ns); }
+
 }  // namespace sdv

@@ -99,4 +99,6 @@ cudaError_t launch_rec_commit(const CacheView& cv, int n_rec, int nh, int H, int
                               const uint16_t* qkv_rec, const int32_t* cu, const int32_t* path,
                               const int32_t* path_len, cudaStream_t s, bool pdl);
 
+cudaError_t launch_delay(uint64_t ns, cudaStream_t s);
+
 }  // namespace sdv

@@ -139,6 +139,11 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     launches += rows > 128 ? 2 : 1;                      \
   } while (0)
 
+  if (m->timing) {
+    // let the host enqueue the whole step before the GPU starts on it
+    const cudaError_t e = launch_delay(30000000ull, s);
+    if (e != cudaSuccess) return cuda_fail(e, "delay");
+  }
   XMap *mx, *ma, *mc;
   if ((rc = get_map(m->map_xn, m->xn, m->max_rows, m->H, rows, &mx))) return rc;
   if ((rc = get_map(m->map_attn, m->attn, m->max_rows, (int64_t)m->Hq * m->hd, rows, &ma))) return rc;
@@ -294,11 +299,10 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
 // every pointer and size the kernels see, so a replay is the same launch
 // sequence; values behind the pointers are read at run time.
 static int launch_step(sd_model* m, const StepIO& io, cudaStream_t s, std::vector<uintptr_t> key) {
-  if (!m->use_graphs || s == nullptr) return run_step(m, io, s);
+  if (!m->use_graphs || m->timing || s == nullptr) return run_step(m, io, s);
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   SD_CK(cudaStreamIsCapturing(s, &cs));
   if (cs != cudaStreamCaptureStatusNone) return run_step(m, io, s);
-  key.push_back(m->timing ? 1 : 0);
   for (auto& g : m->graphs)
     if (g.key == key) {
       SD_CK(cudaGraphLaunch(g.exec, s));

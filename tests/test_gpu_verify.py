@@ -173,10 +173,13 @@ def test_graph_capture_and_replay_match_direct_launches(M, dec):
     kv = M.KVCache(shape, ctx + 80).fill(3, ctx)
     out = model.outputs(12, logits=True)
     s = torch.cuda.Stream()
+    S0, z0 = kv.S.clone(), kv.z.clone()  # a step commits into the recurrent state
     results = []
     for graphs in (False, True, True, True):
         model.set_graphs(graphs)
         kv.ctx_len.fill_(ctx)
+        kv.S.copy_(S0)
+        kv.z.copy_(z0)
         torch.cuda.synchronize()
         with torch.cuda.stream(s):
             model.verify(tok, par, kv, out=out, stream=s)
