@@ -217,6 +217,10 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int strip, int lan
     }
 }
 
+// One CTA per SM is launched, but the register budget is that of two: a GEMM
+// CTA then uses under half of an SM's registers and shared memory, so the
+// next kernel's CTA can be resident at the same time and stream its weights
+// (programmatic dependent launch) while this one drains.
 template <int NT>
 constexpr int ctas_per_sm() { return NT <= 4 ? 2 : 1; }
 
@@ -367,19 +371,31 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
       // contributors: the CTAs whose (non-empty) unit range meets row block b
       const int64_t c_first = (((int64_t)b * KT + 1) * G - 1) / p.U;
       const int64_t c_last = (((int64_t)(b + 1) * KT) * G - 1) / p.U;
-      for (int64_t c = c_first; c <= c_last; c++) {
-        const int64_t cs = c * p.U / G, ce = (c + 1) * p.U / G;
-        if (cs == ce) continue;  // empty range: never wrote a partial
-        const int sid = (b == (int)(cs / KT)) ? 0 : 1;
-        const float* src = partial_ptr(c, sid);
+      // partial slots of the contributors, read kBatch at a time with all
+      // loads in flight before any is used (CTA order kept: deterministic)
+      constexpr int kBatch = NT <= 2 ? 4 : 2;
+      for (int64_t c0 = c_first; c0 <= c_last; c0 += kBatch) {
+        float4 v[kBatch][NT];
+        bool use[kBatch];
 #pragma unroll
-        for (int nt = 0; nt < NT; nt++) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(src + nt * 128));
-          acc[nt][0] += v.x;
-          acc[nt][1] += v.y;
-          acc[nt][2] += v.z;
-          acc[nt][3] += v.w;
+        for (int u = 0; u < kBatch; u++) {
+          const int64_t c = c0 + u;
+          const int64_t cs = c * p.U / G, ce = (c + 1) * p.U / G;
+          use[u] = c <= c_last && cs != ce;  // empty ranges never wrote a partial
+          const float* src = partial_ptr(use[u] ? c : blockIdx.x, (use[u] && b != (int)(cs / KT)) ? 1 : 0);
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++)
+            v[u][nt] = use[u] ? __ldcg(reinterpret_cast<const float4*>(src + nt * 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+#pragma unroll
+        for (int u = 0; u < kBatch; u++)
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++) {
+            acc[nt][0] += v[u][nt].x;
+            acc[nt][1] += v[u][nt].y;
+            acc[nt][2] += v[u][nt].z;
+            acc[nt][3] += v[u][nt].w;
+          }
       }
       if (threadIdx.x == 0) p.counters[b] = 0;
     }
@@ -497,7 +513,10 @@ int pad_rows(int M) { return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 
 
 static int nt_of(int M) { return M > 128 ? 16 : pad_rows(M) / 8; }
 
-int gemm_grid(int M) { return (nt_of(M) <= 4 ? 2 : 1) * num_sms(); }
+int gemm_grid(int M) {
+  (void)M;
+  return num_sms();
+}
 
 size_t gemm_partial_floats(int M) { return (size_t)gemm_grid(M) * 2 * kRB * nt_of(M) * 128; }
 
