@@ -217,16 +217,14 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int strip, int lan
     }
 }
 
-// One CTA per SM is launched, but the register budget is that of two: a GEMM
-// CTA then uses under half of an SM's registers and shared memory, so the
-// next kernel's CTA can be resident at the same time and stream its weights
-// (programmatic dependent launch) while this one drains.
+// Two CTAs per SM for small tiles (more warps to hide decode and MMA latency).
 template <int NT>
 constexpr int ctas_per_sm() { return NT <= 4 ? 2 : 1; }
 
 template <int NT, bool AFFINE>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
-    k_w12_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap xmap) {
+    k_w12_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap xmap,
+               const __grid_constant__ CUtensorMap wmap) {
   using C = Cfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -259,15 +257,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
       const int64_t n = u1 - u0;
       if (n > 0) {
         const int pre = (int)(n < C::S ? n : C::S);
-        const int64_t strip_words = (int64_t)KT * 384;  // one strip's full K range
         int b = (int)(u0 / KT), t = (int)(u0 % KT);
         const int b_first = b, t_first = t;
+        // one 2-D box per stage: 8 strips x 1536 bytes (ragged row blocks are
+        // zero-filled by the copy engine and never read)
         auto issue_weights = [&](int slot, int bb, int tt) {
-          const int ns = min(kRB, p.NS - bb * kRB);
-          mbar_arrive_expect_tx(&full[slot], ns * kStripBytes + C::XB);
-          const uint32_t* src = p.words + (int64_t)bb * kRB * strip_words + (int64_t)tt * 384;
-          uint8_t* dst = sw + slot * C::WB;
-          for (int r = 0; r < ns; r++) bulk_g2s(dst + r * kStripBytes, src + r * strip_words, kStripBytes, &full[slot]);
+          mbar_arrive_expect_tx(&full[slot], C::WB + C::XB);
+          tma2d_g2s(sw + slot * C::WB, &wmap, tt * 192, bb * kRB, &full[slot]);
         };
         for (int i = 0; i < pre; i++) {
           issue_weights(i, b, t);
@@ -513,10 +509,7 @@ int pad_rows(int M) { return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 
 
 static int nt_of(int M) { return M > 128 ? 16 : pad_rows(M) / 8; }
 
-int gemm_grid(int M) {
-  (void)M;
-  return num_sms();
-}
+int gemm_grid(int M) { return (nt_of(M) <= 4 ? 2 : 1) * num_sms(); }
 
 size_t gemm_partial_floats(int M) { return (size_t)gemm_grid(M) * 2 * kRB * nt_of(M) * 128; }
 
@@ -561,8 +554,36 @@ int make_x_map(XMap* xm, const uint16_t* x, int rows_total, int64_t K, int box_r
   return SD_OK;
 }
 
+// The packed words as a 2-D tensor of u64: [strips][K/64 * 192]; one box is
+// 192 u64 (one strip's 1536-byte super-tile) x 8 strips.
+static int make_w_map(CUtensorMap* map, const w12_tensor& W) {
+  auto fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled unavailable");
+    return SD_ERR_CUDA;
+  }
+  if (reinterpret_cast<uintptr_t>(W.words) & 15) {
+    set_error("gemm: packed words must be 16-byte aligned");
+    return SD_ERR_INVALID_ARG;
+  }
+  const int64_t KT = W.K / 64;
+  cuuint64_t dims[2] = {(cuuint64_t)KT * 192, (cuuint64_t)(W.N / 16)};
+  cuuint64_t strides[1] = {(cuuint64_t)KT * kStripBytes};
+  cuuint32_t box[2] = {192, (cuuint32_t)kRB};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint32_t*>(W.words), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (weights) failed: " + std::to_string((int)r));
+    return SD_ERR_CUDA;
+  }
+  return SD_OK;
+}
+
 template <int NT, bool AFF>
-static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, cudaStream_t s, bool pdl, int grid) {
+static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, const CUtensorMap& wmap, cudaStream_t s,
+                             bool pdl, int grid) {
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e =
@@ -570,7 +591,7 @@ static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, cudaSt
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch(k_w12_gemm<NT, AFF>, dim3(grid), dim3(kThreads), Cfg<NT>::SMEM, s, pdl, p, map);
+  return launch(k_w12_gemm<NT, AFF>, dim3(grid), dim3(kThreads), Cfg<NT>::SMEM, s, pdl, p, map, wmap);
 }
 
 int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
@@ -618,15 +639,18 @@ int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, c
     return SD_ERR_WORKSPACE;
   }
   const bool aff = W.affine != 0;
+  CUtensorMap wmap;
+  const int wrc = make_w_map(&wmap, W);
+  if (wrc) return wrc;
   for (int m0 = 0; m0 < M; m0 += 128) {
     p.m0 = m0;
     cudaError_t e;
     switch (NT) {
-      case 1: e = aff ? launch_nt<1, true>(p, xm.map, s, pdl, grid) : launch_nt<1, false>(p, xm.map, s, pdl, grid); break;
-      case 2: e = aff ? launch_nt<2, true>(p, xm.map, s, pdl, grid) : launch_nt<2, false>(p, xm.map, s, pdl, grid); break;
-      case 4: e = aff ? launch_nt<4, true>(p, xm.map, s, pdl, grid) : launch_nt<4, false>(p, xm.map, s, pdl, grid); break;
-      case 8: e = aff ? launch_nt<8, true>(p, xm.map, s, pdl, grid) : launch_nt<8, false>(p, xm.map, s, pdl, grid); break;
-      default: e = aff ? launch_nt<16, true>(p, xm.map, s, pdl, grid) : launch_nt<16, false>(p, xm.map, s, pdl, grid); break;
+      case 1: e = aff ? launch_nt<1, true>(p, xm.map, wmap, s, pdl, grid) : launch_nt<1, false>(p, xm.map, wmap, s, pdl, grid); break;
+      case 2: e = aff ? launch_nt<2, true>(p, xm.map, wmap, s, pdl, grid) : launch_nt<2, false>(p, xm.map, wmap, s, pdl, grid); break;
+      case 4: e = aff ? launch_nt<4, true>(p, xm.map, wmap, s, pdl, grid) : launch_nt<4, false>(p, xm.map, wmap, s, pdl, grid); break;
+      case 8: e = aff ? launch_nt<8, true>(p, xm.map, wmap, s, pdl, grid) : launch_nt<8, false>(p, xm.map, wmap, s, pdl, grid); break;
+      default: e = aff ? launch_nt<16, true>(p, xm.map, wmap, s, pdl, grid) : launch_nt<16, false>(p, xm.map, wmap, s, pdl, grid); break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "k_w12_gemm launch");
   }
