@@ -73,16 +73,27 @@ def probe_arm(args):
     x = Mdl.to_device_u16(synthetic.normal_bf16(synthetic.key(args.seed, 4243), M * K, 1.0).reshape(M, K))
     import speculative_decoding_tree_bit_gb300 as sdv
     ws = Mdl.Workspace(int(sdv.lib().sd_w12_linear_workspace(N, K, M)))
-    for _ in range(args.warmup):
-        Mdl.linear(p, x, ws)
+    y = Mdl.linear(p, x, ws)
+    stream = torch.cuda.Stream()
+    # the launches are replayed from a CUDA graph: no host time between them
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            Mdl.linear(p, x, ws, stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(args.steps):
+                Mdl.linear(p, x, ws, stream=stream)
+    torch.cuda.synchronize()
+    g.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(args.steps):
-        Mdl.linear(p, x, ws)
+    g.replay()
     e1.record()
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / args.steps
+    del y
     nbytes = p.nbytes() + M * K * 2 + M * N * 2
     pk, src = peaks()
     return {"probe": "sd_w12_linear", "N": N, "K": K, "M": M, "us_per_launch": us,

@@ -1,6 +1,7 @@
 // C ABI: errors, stand-alone tree helpers and the tiny verify model.
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "gemm.cuh"
 #include "layers.cuh"
@@ -14,6 +15,16 @@ void set_error(const std::string& s) { g_last_error = s; }
 int cuda_fail(cudaError_t e, const char* what) {
   g_last_error = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
   return e == cudaErrorMemoryAllocation ? SD_ERR_OOM : SD_ERR_CUDA;
+}
+
+void carveout_once(const void* kern) {
+  static std::mutex mu;
+  static std::vector<const void*> done;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const void* k : done)
+    if (k == kern) return;
+  cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  done.push_back(kern);
 }
 
 int num_sms() {

@@ -26,12 +26,18 @@ int cuda_fail(cudaError_t e, const char* what);
 
 int num_sms();
 
+// Every kernel asks for the same (maximum) shared-memory carveout, so that
+// consecutive kernels of a step never make an SM re-partition L1 / shared
+// memory between them.
+void carveout_once(const void* kern);
+
 // Launch with programmatic dependent launch allowed: the kernel may start
 // before the previous kernel on the stream ends, so it must call pdl_wait()
 // before touching anything that kernel (or an earlier one) writes.
 template <typename... KArgs, typename... Args>
 cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
                    Args&&... args) {
+  carveout_once(reinterpret_cast<const void*>(kern));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
