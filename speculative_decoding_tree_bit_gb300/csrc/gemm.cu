@@ -102,91 +102,32 @@ __device__ __forceinline__ uint32_t comp(const uint4& v, int j) {
   return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
 }
 
-// Escape entries of one strip held by a warp: lane i keeps entries i and
-// 32 + i of the strip's range in the side list (sorted by flat index, so a
-// strip's escapes are contiguous), as (row in strip << 16 | column) and the
-// weight's value.  Entries past the first 64 are applied in the epilogue.
-struct StripEscapes {
-  uint32_t key[2];  // 0xFFFFFFFF = none
-  float w[2];
-  uint32_t lo, hi;  // the strip's range in the side list
-};
-
-__device__ __forceinline__ void load_strip_escapes(const GemmParams& p, int strip, int lane, StripEscapes& se) {
-  se.lo = __ldg(p.row_ptr + (int64_t)strip * 16);
-  se.hi = __ldg(p.row_ptr + (int64_t)strip * 16 + 16);
-#pragma unroll
-  for (int c = 0; c < 2; c++) {
-    const uint32_t e = se.lo + c * 32 + lane;
-    se.key[c] = 0xFFFFFFFFu;
-    se.w[c] = 0.f;
-    if (e < se.hi) {
-      const uint32_t idx = __ldg(p.esc_idx + e);
-      const uint32_t row = idx / (uint32_t)p.K;
-      se.key[c] = ((row - (uint32_t)strip * 16) << 16) | (idx - row * (uint32_t)p.K);
-      se.w[c] = bf2f(__ldg(p.esc_val + e));
-    }
-  }
-}
-
-// acc += (w - slot) * x for the strip's escapes whose column lies in the
-// 64-column tile starting at k0; x comes from the staged (swizzled) tile.
-template <int NT>
-__device__ __forceinline__ void apply_tile_escapes(const GemmParams& p, const StripEscapes& se, int k0,
-                                                   const uint8_t* xtile, int lane, float (&acc)[NT][4]) {
-  const int g = lane >> 2, q = lane & 3;
-#pragma unroll
-  for (int c = 0; c < 2; c++) {
-    uint32_t mask = __ballot_sync(0xffffffffu, se.key[c] != 0xFFFFFFFFu && (se.key[c] & 0xFFFFu) - (uint32_t)k0 < 64u);
-    while (mask) {
-      const int src = __ffs(mask) - 1;
-      mask &= mask - 1;
-      const uint32_t key = __shfl_sync(0xffffffffu, se.key[c], src);
-      const float w = __shfl_sync(0xffffffffu, se.w[c], src);
-      const int row = (int)(key >> 16), kk = (int)(key & 0xFFFFu) - k0;
-      if ((row & 7) == g) {
-        const int half = row >> 3;
-#pragma unroll
-        for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-          for (int cc = 0; cc < 2; cc++) {
-            const int m = nt * 8 + 2 * q + cc;
-            const uint16_t xb = *reinterpret_cast<const uint16_t*>(xtile + m * 128 + ((((kk >> 3) ^ (m & 7))) << 4) +
-                                                                  (kk & 7) * 2);
-            const float xv = bf2f(xb);
-            const float a = fmaf(w, xv, acc[nt][2 * half + cc]);
-            acc[nt][2 * half + cc] = fmaf(-p.esc_slot, xv, a);
-          }
-      }
-    }
-  }
-}
-
 template <int NT>
 __device__ __forceinline__ void epilogue(const GemmParams& p, int strip, int lane, float (&acc)[NT][4],
-                                         float (&bestv)[NT][2], int (&besti)[NT][2], const StripEscapes& se) {
+                                         float (&bestv)[NT][2], int (&besti)[NT][2]) {
   const int g = lane >> 2, q = lane & 3;
   const int64_t n_lo = (int64_t)strip * 16 + g;
   const int64_t K = p.K;
-  // escapes beyond the 64 applied tile by tile (rare: very long rows)
-  for (uint32_t e = se.lo + 64; e < se.hi; e++) {
-    const uint32_t idx = __ldg(p.esc_idx + e);
-    const int64_t n = idx / K, k = idx - n * K;
-    const int row = (int)(n - (int64_t)strip * 16);
-    if ((row & 7) != g) continue;
-    const int half = row >> 3;
-    const float w = bf2f(__ldg(p.esc_val + e));
+  // escapes of rows n_lo and n_lo + 8
 #pragma unroll
-    for (int nt = 0; nt < NT; nt++)
+  for (int h = 0; h < 2; h++) {
+    const int64_t n = n_lo + 8 * h;
+    const uint32_t e0 = p.row_ptr[n], e1 = p.row_ptr[n + 1];
+    for (uint32_t e = e0; e < e1; e++) {
+      const int64_t k = (int64_t)p.esc_idx[e] - n * K;
+      const float w = bf2f(p.esc_val[e]);
 #pragma unroll
-      for (int cc = 0; cc < 2; cc++) {
-        const int m = p.m0 + nt * 8 + 2 * q + cc;
-        if (m < p.M) {
-          const float xv = bf2f(p.x[(int64_t)m * K + k]);
-          const float a = fmaf(w, xv, acc[nt][2 * half + cc]);
-          acc[nt][2 * half + cc] = fmaf(-p.esc_slot, xv, a);
+      for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int cc = 0; cc < 2; cc++) {
+          const int m = p.m0 + nt * 8 + 2 * q + cc;
+          if (m < p.M) {
+            const float xv = bf2f(p.x[(int64_t)m * K + k]);
+            const float a = fmaf(w, xv, acc[nt][2 * h + cc]);
+            acc[nt][2 * h + cc] = fmaf(-p.esc_slot, xv, a);
+          }
         }
-      }
+    }
   }
   const GemmEpilogue& E = p.e;
 #pragma unroll
@@ -280,11 +221,8 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int strip, int lan
 template <int NT>
 constexpr int ctas_per_sm() { return NT <= 4 ? 2 : 1; }
 
-template <int NT>
-constexpr int max_regs() { return ctas_per_sm<NT>() == 2 ? 112 : 168; }
-
 template <int NT, bool AFFINE>
-__global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NT>())
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
     k_w12_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap xmap,
                const __grid_constant__ CUtensorMap wmap) {
   using C = Cfg<NT>;
@@ -387,10 +325,6 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NT>())
       besti[nt][c] = 0x7FFFFFFF;
     }
   const int first_b = u1 > u0 ? (int)(u0 / KT) : -1;
-  StripEscapes se;
-  se.key[0] = se.key[1] = 0xFFFFFFFFu;
-  se.w[0] = se.w[1] = 0.f;
-  se.lo = se.hi = 0;
 
   auto zero = [&]() {
 #pragma unroll
@@ -461,7 +395,7 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NT>())
       }
       if (threadIdx.x == 0) p.counters[b] = 0;
     }
-    if (strip < p.NS) epilogue<NT>(p, strip, lane, acc, bestv, besti, se);
+    if (strip < p.NS) epilogue<NT>(p, strip, lane, acc, bestv, besti);
   };
 
   zero();
@@ -476,7 +410,6 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NT>())
       cur_b = b;
       seg_t0 = t;
       zero();
-      if (b * kRB + warp < p.NS) load_strip_escapes(p, b * kRB + warp, lane, se);
     }
     if (!mbar_wait(&full[slot], phase)) {
       set_status(p.status, SD_ERR_TIMEOUT);
@@ -513,7 +446,6 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NT>())
           }
         }
       }
-      if (se.hi > se.lo) apply_tile_escapes<NT>(p, se, t * 64, sx + slot * C::XB, lane, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
