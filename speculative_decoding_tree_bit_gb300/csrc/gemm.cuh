@@ -72,4 +72,12 @@ int make_x_map(XMap* xm, const uint16_t* x, int rows_total, int64_t K, int box_r
 int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
                 const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid = 0);
 
+// Descriptor of the packed words for the 2-D weight loads (one box = 8
+// strips x 1536 bytes).
+int make_w_map(CUtensorMap* map, const w12_tensor& W);
+
+struct GemmParams;
+int make_gemm_params(GemmParams* out, const w12_tensor& W, const uint16_t* x, int M, const GemmEpilogue& epi,
+                     const GemmWorkspace& ws, int32_t* status);
+
 }  // namespace sdv
