@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--timeline", action="store_true", help="print the per-kernel breakdown to stderr")
+    ap.add_argument("--chain", action="store_true",
+                    help="run each layer's GEMMs and RMSNorms as one persistent chain launch")
     ap.add_argument("--nvtx", action="store_true", help="wrap the timed steps in the NVTX range 'sdv_step'")
     ap.add_argument("--probe", default=None, metavar="N,K,M",
                     help="time the fused W12 linear alone on an N x K tensor with M rows")
@@ -228,6 +230,29 @@ def kv_bytes_per_step(shape, ctx, M):
     return attn + rec
 
 
+def chain_phase_summary(model, launch):
+    """Per phase of one chain launch: when the CTAs' first stage was ready,
+    their last stage consumed and the phase finished, in us after the previous
+    phase's last CTA finished (the first CTA's start for phase 0), as
+    [median, max] over the CTAs that had work."""
+    import numpy as np
+    try:
+        st = model.chain_trace(launch).astype(np.int64)
+    except Exception as e:  # no chain launch in the timed step
+        return {"error": str(e)}
+    n = (st.shape[0] - 1) // 3
+    prev = int(st[0].min())
+    out = []
+    for p in range(n):
+        row = {}
+        for name, r in (("first_ready", 1 + 3 * p), ("last_consumed", 2 + 3 * p), ("finished", 3 + 3 * p)):
+            v = st[r][st[r] > 0]
+            row[name] = [round(float(np.median(v) - prev) / 1e3, 2), round(float(v.max() - prev) / 1e3, 2)] if v.size else None
+        out.append(row)
+        prev = int(st[3 + 3 * p].max())
+    return {"chain_launch": launch, "phases_us_median_max": out}
+
+
 def gpu_arm(args, rank, world, dist):
     import numpy as np
     import torch
@@ -245,6 +270,7 @@ def gpu_arm(args, rank, world, dist):
     t0 = time.time()
     W = wl.SyntheticWeights(shape, args.seed)
     model = Mdl.Model(shape, W, max_rows=M, max_requests=1, max_positions=ctx + M + 64)
+    model.set_chain(args.chain)
     kv = Mdl.KVCache(shape, ctx + M + 16).fill(args.seed, ctx)
     log(f"[rank {rank}] model built in {time.time() - t0:.1f}s, packed {model.packed_bytes / 1e9:.2f} GB")
     td = spec.drafts[0]
@@ -332,6 +358,9 @@ def gpu_arm(args, rank, world, dist):
             step()
     torch.cuda.synchronize()
     tl = model.timeline()
+    chain_phases = None
+    if args.timeline and args.chain:
+        chain_phases = chain_phase_summary(model, shape.n_layers // 2)
     model.set_timing(False)
 
     if dist is not None:
@@ -340,7 +369,7 @@ def gpu_arm(args, rank, world, dist):
         ms, ms_e2e = float(t[0]), float(t[1])
 
     pk, pk_src = peaks()
-    gemm = [(k, t, b) for k, t, b in tl if k.startswith("gemm")]
+    gemm = [(k, t, b) for k, t, b in tl if k.startswith("gemm")]  # chain launches and lone GEMMs
     g_ms = sum(t for _, t, _ in gemm)
     g_bytes = sum(b for _, _, b in gemm)
     achieved = g_bytes / (g_ms * 1e-3) / 1e9 if g_ms > 0 else None
@@ -360,6 +389,8 @@ def gpu_arm(args, rank, world, dist):
     if args.timeline:
         log(json.dumps({k: {"launches": v[0], "ms": round(v[1], 4), "GB/s": round(v[2] / v[1] / 1e6, 1) if v[2] else None}
                         for k, v in by_kind.items()}))
+        if chain_phases:
+            log(json.dumps(chain_phases))
     value = world * M / (ms * 1e-3)
     res = {
         "metric": "tree_tokens_per_s", "value": value, "unit": "tree tokens/s",
@@ -367,6 +398,7 @@ def gpu_arm(args, rank, world, dist):
         "verify_step_us": ms * 1e3, "host_submit_us_per_step": t_host * 1e6, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "model": shape.name, "layers": shape.n_layers, "M": M,
+                   "gemm_chain": bool(args.chain),
                    "max_depth": spec.max_depth, "ctx": ctx, "p_copy": spec.p, "accepted_len": acc_len,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (packed weights %.1f GB)" % (model.packed_bytes / 1e9)},
@@ -377,7 +409,9 @@ def gpu_arm(args, rank, world, dist):
         "frac_of_step_lower_bound": bound_s / (ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak if achieved else None, "traffic": None,
-                     "kernel": "k_w12_gemm (all GEMM launches of a step, event-timed)",
+                     "kernel": ("k_w12_gemm (all GEMM launches of a step, event-timed)" if not args.chain else
+                                "k_w12_chain + k_w12_gemm (all GEMM chain / GEMM launches of a step, event-timed; "
+                                "a chain's time includes its two RMSNorm phases)"),
                      "peak_source": pk_src},
         "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in by_kind.items()},
         "e2e": {"value": world * M / (ms_e2e * 1e-3), "unit": "tree tokens/s", "h2d_bytes_per_step": h2d,

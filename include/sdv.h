@@ -84,6 +84,8 @@ typedef struct {
   const uint32_t* esc_idx;  /* device [n_escapes], increasing */
   const uint16_t* esc_val;  /* device [n_escapes], bf16 bits */
   const uint32_t* row_ptr;  /* device [N+1] */
+  const uint32_t* tile_ptr; /* device [w12_tile_ptr_count(N,K)]: escape tile index (w12_pack_tile_index) */
+  const uint32_t* tile_esc; /* device [n_escapes] */
   int64_t n_escapes;
   uint8_t table[16];
   int32_t n_table;
@@ -108,13 +110,34 @@ int w12_pack_analyze(const uint16_t* w, int64_t N, int64_t K, w12_meta* meta, vo
 int w12_pack_encode(const uint16_t* w, const int32_t* row_src, const w12_meta* meta, uint32_t* words,
                     uint32_t* esc_idx, uint16_t* esc_val, uint32_t* row_ptr, void* stream);
 
-/* Restore the bf16 tensor [N][K] (bit-exact).  Asynchronous. */
+/* Restore the bf16 tensor [N][K] (bit-exact).  Asynchronous.  Uses words,
+ * esc_idx, esc_val only. */
 int w12_unpack(const w12_tensor* t, uint16_t* w_out, void* stream);
+
+/* Escape tile index (no counterpart in the pages: an access structure of
+ * this library over the side list, which stays the format's record of the
+ * escapes).  The fused kernels stream a tensor by blocks of 128 rows and
+ * tiles of 64 columns and need each (block, tile)'s escapes as one
+ * contiguous run: with NB = ceil(N/128) and KT = K/64, the escapes of row
+ * block b and column tile t are tile_esc[tile_ptr[b*KT+t] ..
+ * tile_ptr[b*KT+t+1]), each encoded as (bf16 bits << 16) | (row - 128b) << 6
+ * | (column - 64t), in row-major order within the (block, tile);
+ * tile_ptr[NB*KT] = n_escapes.  The escapes of block b occupy the same index
+ * range as in the side list.  w12_tile_ptr_count(N, K) = NB*KT + 1. */
+int64_t w12_tile_ptr_count(int64_t N, int64_t K);
+
+/* Build the escape tile index of t from its side list (esc_idx, esc_val,
+ * row_ptr).  Outputs are caller-allocated device arrays:
+ * tile_ptr[w12_tile_ptr_count], tile_esc[n_escapes] (may be NULL when
+ * n_escapes == 0).  Asynchronous on `stream`.  Every fused kernel requires
+ * t->tile_ptr and, with escapes, t->tile_esc (SD_ERR_INVALID_ARG if missing). */
+int w12_pack_tile_index(const w12_tensor* t, uint32_t* tile_ptr, uint32_t* tile_esc, void* stream);
 
 /* ------------------------------------------------ fused W12 linear -- */
 /* [W12] y[m][n] = bf16( sum_k x[m][k] * W[n][k] ), fp32 accumulation, with
  * the weights decoded in registers straight from the packed words (they
- * cross HBM once, 1.5 bytes each) and the escapes added in the epilogue.
+ * cross HBM once, 1.5 bytes each) and the escapes added from the escape tile
+ * index (W->tile_ptr / tile_esc must be set).
  * x: bf16 [M][K] row-major, 16-byte aligned; y: bf16 [M][N] row-major.
  * 1 <= M <= 256.  workspace: caller-owned device scratch of
  * sd_w12_linear_workspace(N, K, M) bytes, 256-byte aligned; it needs no
@@ -284,7 +307,8 @@ int sd_verify_batch(sd_model* m, const int32_t* tokens, const int32_t* parents, 
                     int32_t* bonus, uint16_t* logits, int32_t* argmax, void* stream);
 
 /* Copy the device status word of the model's last calls (synchronises the
- * device) and clear it. */
+ * device) and clear it; after a non-zero status the GEMM chain's grid barrier
+ * is also reset. */
 int sd_status(sd_model* m, int32_t* status_host);
 
 /* Number of kernels the last sd_verify_step / sd_forward / sd_verify_batch
@@ -300,10 +324,38 @@ int sd_model_last_launches(sd_model* m);
  * stream and inside a caller's own stream capture). */
 int sd_model_set_graphs(sd_model* m, int32_t enable);
 
-/* Kernel kinds reported by sd_model_timeline. */
+/* GEMM chaining (no counterpart in the pages: an execution choice of this
+ * library).  With enable = 1 (default 0) and at most 128 rows per step,
+ * each run of GEMMs and RMSNorms between two attention / recurrence kernels
+ * (O + residual, RMSNorm, gate/up + SiLU, down + residual, RMSNorm, the next
+ * layer's q/k/v or the lm_head) is executed by one persistent kernel whose
+ * phases are separated by grid barriers, so weight streaming continues across
+ * phase boundaries.  enable = 0 launches every GEMM and RMSNorm as its own
+ * kernel, chained by programmatic dependent launch (faster on GB300 for the
+ * 8B-class step: a kernel's early CTAs start the next GEMM while its last
+ * CTAs finish, which a grid barrier forbids).  Results are identical up to the order of fp32 additions inside
+ * the GEMMs (none: both modes use the same partition and summation order).
+ * Returns SD_OK or SD_ERR_INVALID_ARG for a null model. */
+int sd_model_set_chain(sd_model* m, int32_t enable);
+
+/* Raw device-clock stamps (%globaltimer, ns) of chain launch `launch` (0 =
+ * the first chain launch) of the last timed step: *n_phases = n, *n_ctas = G
+ * and, when stamps_host is not NULL (room for max_stamps >= (1 + 3n) G
+ * values), stamps_host[r * G + c] for CTA c: r = 0 its start; for phase i,
+ * r = 1 + 3i when its first stage was ready (RMSNorm phase: input complete),
+ * r = 2 + 3i when its last stage was consumed (RMSNorm: rows written), r = 3 +
+ * 3i when it finished the phase (0 = not written: no work in that phase).
+ * Synchronises the device when copying.  SD_ERR_INVALID_ARG for a launch the
+ * last timed step does not have or a short buffer. */
+int sd_model_chain_trace(sd_model* m, int32_t launch, int32_t* n_phases, int32_t* n_ctas, uint64_t* stamps_host,
+                         int64_t max_stamps);
+
+/* Kernel kinds reported by sd_model_timeline (SD_K_GEMM_CHAIN: one chain
+ * launch; its bytes are those of the GEMMs it runs). */
 enum {
   SD_K_TREE = 0, SD_K_NORM = 1, SD_K_GEMM_QKV = 2, SD_K_ATTN = 3, SD_K_LINREC = 4, SD_K_GEMM_O = 5,
-  SD_K_GEMM_GATE_UP = 6, SD_K_GEMM_DOWN = 7, SD_K_GEMM_LM_HEAD = 8, SD_K_ACCEPT = 9, SD_K_COMMIT = 10
+  SD_K_GEMM_GATE_UP = 6, SD_K_GEMM_DOWN = 7, SD_K_GEMM_LM_HEAD = 8, SD_K_ACCEPT = 9, SD_K_COMMIT = 10,
+  SD_K_GEMM_CHAIN = 11
 };
 
 /* Per-kernel timing of the following model calls: with enable = 1 every
@@ -320,8 +372,13 @@ int sd_model_set_timing(sd_model* m, int32_t enable);
  * ms_host[i] (event-measured duration; SD_K_ATTN covers the split kernel and
  * its combine) and bytes_host[i] (algorithmic bytes of a GEMM: packed words,
  * escape list, row pointers, activations read and written; 0 for other
- * kinds).  Synchronises the device.  Returns the number of entries written
- * (<= max), or -1 with sd_last_error set. */
+ * kinds).  Each SD_K_GEMM_CHAIN entry is followed by one entry per phase of
+ * that launch with kind 100 + the phase's kind (SD_K_GEMM_O, SD_K_NORM, ...):
+ * its time runs from the last CTA finishing the previous phase (the first CTA
+ * starting, for the first phase) to the last CTA finishing this one, read from
+ * the device clock (%globaltimer); these entries overlap their chain entry.
+ * Synchronises the device.  Returns the number of entries written (<= max),
+ * or -1 with sd_last_error set. */
 int sd_model_timeline(sd_model* m, int32_t max, int32_t* kind_host, float* ms_host, double* bytes_host);
 
 #ifdef __cplusplus

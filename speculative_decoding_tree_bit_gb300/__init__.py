@@ -35,7 +35,8 @@ class W12Meta(ctypes.Structure):
 
 class W12Tensor(ctypes.Structure):
     _fields_ = [("N", i64), ("K", i64), ("words", vp), ("esc_idx", vp), ("esc_val", vp), ("row_ptr", vp),
-                ("n_escapes", i64), ("table", u8 * 16), ("n_table", i32), ("affine", i32)]
+                ("tile_ptr", vp), ("tile_esc", vp), ("n_escapes", i64), ("table", u8 * 16), ("n_table", i32),
+                ("affine", i32)]
 
 
 class ModelConfig(ctypes.Structure):
@@ -71,6 +72,8 @@ _SIGS = {
     "w12_pack_analyze": (ctypes.c_int, [vp, i64, i64, P(W12Meta), vp]),
     "w12_pack_encode": (ctypes.c_int, [vp, vp, P(W12Meta), vp, vp, vp, vp, vp]),
     "w12_unpack": (ctypes.c_int, [P(W12Tensor), vp, vp]),
+    "w12_tile_ptr_count": (i64, [i64, i64]),
+    "w12_pack_tile_index": (ctypes.c_int, [P(W12Tensor), vp, vp, vp]),
     "sd_w12_linear_workspace": (ctypes.c_size_t, [i64, i64, i32]),
     "sd_w12_linear": (ctypes.c_int, [P(W12Tensor), vp, i32, vp, vp, ctypes.c_size_t, vp]),
     "sd_w12_linear_static": (ctypes.c_int, [P(W12Tensor), vp, i32, vp, vp]),
@@ -89,11 +92,13 @@ _SIGS = {
     "sd_model_last_launches": (ctypes.c_int, [vp]),
     "sd_model_set_timing": (ctypes.c_int, [vp, i32]),
     "sd_model_set_graphs": (ctypes.c_int, [vp, i32]),
+    "sd_model_set_chain": (ctypes.c_int, [vp, i32]),
+    "sd_model_chain_trace": (ctypes.c_int, [vp, i32, vp, vp, vp, ctypes.c_int64]),
     "sd_model_timeline": (ctypes.c_int, [vp, i32, vp, vp, vp]),
 }
 
 KERNEL_KINDS = ["tree", "rmsnorm", "gemm_qkv", "attention", "linrec", "gemm_o", "gemm_gate_up", "gemm_down",
-                "gemm_lm_head", "accept", "commit"]
+                "gemm_lm_head", "accept", "commit", "gemm_chain"]
 
 _lib = None
 _lock = threading.Lock()

@@ -65,6 +65,14 @@ __device__ __forceinline__ void set_status(int* st, int code) {
   if (st) atomicCAS(st, 0, code);
 }
 
+// Status of a bounded wait that gave up.  Built with -DSDV_TIMEOUT_SITES the
+// code also names the wait (bits 8..15), for diagnosing a stuck pipeline.
+#ifdef SDV_TIMEOUT_SITES
+#define SD_TIMEOUT_AT(site) (SD_ERR_TIMEOUT | ((site) << 8))
+#else
+#define SD_TIMEOUT_AT(site) SD_ERR_TIMEOUT
+#endif
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -109,6 +117,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(addr, parity)) {
     if (globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// Bounded wait shared by the warps of a CTA: the first wait that times out
+// sets *abort, after which every wait of the CTA returns false at once.
+// Callers keep their control flow (and their named barriers) unchanged after
+// a failed wait, working on stale shared memory, so that no warp is left
+// waiting for another.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(addr, parity)) {
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      return false;
+    }
   }
   return true;
 }

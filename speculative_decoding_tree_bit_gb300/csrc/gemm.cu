@@ -48,12 +48,16 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sx = smem;
-  uint8_t* sw = smem + C::S * C::XB;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sw + C::S * C::WB);
-  uint64_t* empty = full + C::S;
-  float* red_v = reinterpret_cast<float*>(empty + C::S);
-  int* red_i = reinterpret_cast<int*>(red_v + kNCW * C::MP);
-  int* flag = red_i + kNCW * C::MP;
+  uint8_t* sw = smem + C::OFF_W;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_FULL);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + C::OFF_EMPTY);
+  float* red_v = reinterpret_cast<float*>(smem + C::OFF_RED_V);
+  int* red_i = reinterpret_cast<int*>(smem + C::OFF_RED_I);
+  int* flag = reinterpret_cast<int*>(smem + C::OFF_FLAG);
+  volatile int* abort = flag + 1;
+  uint64_t* corr_full = reinterpret_cast<uint64_t*>(smem + C::OFF_CBAR);
+  uint64_t* corr_empty = corr_full + 1;
+  float* corr = reinterpret_cast<float*>(smem + C::OFF_CORR);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
@@ -63,21 +67,25 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::S; i++) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kNCW);
+      mbar_init(&empty[i], kNCW + 1);  // consumer warps + escape warp
     }
+    mbar_init(corr_full, 1);
+    mbar_init(corr_empty, kNCW);
+    *abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
   pdl_launch();
 
-  if (warp == kNCW) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------- producer --
     if (lane == 0) {
       const int64_t n = u1 - u0;
+      int64_t issued = 0;
       if (n > 0) {
         const int pre = (int)(n < C::S ? n : C::S);
         int b = (int)(u0 / KT), t = (int)(u0 % KT);
-        const int b_first = b, t_first = t;
+        const int t_first = t;
         // one 2-D box per stage: 8 strips x 1536 bytes (ragged row blocks are
         // zero-filled by the copy engine and never read)
         auto issue_weights = [&](int slot, int bb, int tt) {
@@ -99,18 +107,19 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
             if (++tt == KT) tt = 0;
           }
         }
-        (void)b_first;
+        issued = pre;
         // the loop below runs only when pre == S: stage S reuses slot 0,
         // whose first use completed phase 0 of its empty barrier
         int slot = 0;
         uint32_t par = 0;
         for (int64_t i = pre; i < n; i++) {
-          if (!mbar_wait(&empty[slot], par)) {
-            set_status(p.status, SD_ERR_TIMEOUT);
+          if (!mbar_wait_or_abort(&empty[slot], par, abort)) {
+            set_status(p.status, SD_TIMEOUT_AT(1));
             break;
           }
           issue_weights(slot, b, t);
           tma2d_g2s(sx + slot * C::XB, &xmap, t * 64, p.m0, &full[slot]);
+          issued++;
           if (++t == KT) {
             t = 0;
             b++;
@@ -123,203 +132,29 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
       } else {
         pdl_wait();
       }
+      // every copy this CTA started has landed before it exits
+      for (int s = 0; s < C::S && s < issued; s++) {
+        const int64_t n_s = issued / C::S + (s < issued % C::S ? 1 : 0);
+        if (!mbar_wait(&full[s], (uint32_t)((n_s - 1) & 1))) set_status(p.status, SD_TIMEOUT_AT(2));
+      }
     }
+    return;
+  }
+
+  if (warp == kEscapeWarp) {
+    // -------------------------------------------------- escape warp --
+    int eseg = 0, eslot = 0;
+    uint32_t ephase = 0;
+    escape_segments<NT>(p, sx, full, empty, eslot, ephase, corr, corr_full, corr_empty, eseg, abort);
     return;
   }
 
   // --------------------------------------------------------- consumers --
   pdl_wait();
-  // small tiles: even and odd sub-tiles feed separate accumulators so that
-  // consecutive MMAs do not wait on each other; larger tiles have NT
-  // independent MMAs per sub-tile already
-  constexpr bool kDual = NT <= 4;
-  float acc[NT][4], acc2[kDual ? NT : 1][4];
-  float bestv[NT][2];
-  int besti[NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-    for (int c = 0; c < 2; c++) {
-      bestv[nt][c] = -INFINITY;
-      besti[nt][c] = 0x7FFFFFFF;
-    }
-  const int first_b = u1 > u0 ? (int)(u0 / KT) : -1;
-
-  auto zero = [&]() {
-#pragma unroll
-    for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-      for (int c = 0; c < 4; c++) {
-        acc[nt][c] = 0.f;
-        if constexpr (kDual) acc2[nt][c] = 0.f;
-      }
-  };
-  auto partial_ptr = [&](int64_t cta, int slot_id) {
-    return p.partial + (((cta * 2 + slot_id) * kRB + warp) * NT) * 128 + lane * 4;
-  };
-  // finish the segment [t0, t1) of row block b
-  auto finish = [&](int b, int t0, int t1) {
-    const int strip = b * kRB + warp;
-    if constexpr (kDual) {
-#pragma unroll
-      for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-        for (int c = 0; c < 4; c++) acc[nt][c] += acc2[nt][c];
-    }
-    if (!(t0 == 0 && t1 == KT)) {
-      const int slot_id = (b == first_b) ? 0 : 1;
-      float* dst = partial_ptr(blockIdx.x, slot_id);
-#pragma unroll
-      for (int nt = 0; nt < NT; nt++)
-        __stcg(reinterpret_cast<float4*>(dst + nt * 128), make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]));
-      __threadfence();
-      bar_sync(1, kNCW * 32);
-      if (threadIdx.x == 0) {
-        const int add = t1 - t0;
-        const int old = atomicAdd(&p.counters[b], add);
-        *flag = (old + add == KT) ? 1 : 0;
-      }
-      bar_sync(1, kNCW * 32);
-      if (!*flag) return;
-      __threadfence();
-      zero();
-      // contributors: the CTAs whose (non-empty) unit range meets row block b
-      const int64_t c_first = (((int64_t)b * KT + 1) * G - 1) / p.U;
-      const int64_t c_last = (((int64_t)(b + 1) * KT) * G - 1) / p.U;
-      // partial slots of the contributors, read kBatch at a time with all
-      // loads in flight before any is used (CTA order kept: deterministic)
-      constexpr int kBatch = NT <= 2 ? 4 : 2;
-      for (int64_t c0 = c_first; c0 <= c_last; c0 += kBatch) {
-        float4 v[kBatch][NT];
-        bool use[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; u++) {
-          const int64_t c = c0 + u;
-          const int64_t cs = c * p.U / G, ce = (c + 1) * p.U / G;
-          use[u] = c <= c_last && cs != ce;  // empty ranges never wrote a partial
-          const float* src = partial_ptr(use[u] ? c : blockIdx.x, (use[u] && b != (int)(cs / KT)) ? 1 : 0);
-#pragma unroll
-          for (int nt = 0; nt < NT; nt++)
-            v[u][nt] = use[u] ? __ldcg(reinterpret_cast<const float4*>(src + nt * 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; u++)
-#pragma unroll
-          for (int nt = 0; nt < NT; nt++) {
-            acc[nt][0] += v[u][nt].x;
-            acc[nt][1] += v[u][nt].y;
-            acc[nt][2] += v[u][nt].z;
-            acc[nt][3] += v[u][nt].w;
-          }
-      }
-      if (threadIdx.x == 0) p.counters[b] = 0;
-    }
-    if (strip < p.NS) epilogue<NT>(p, strip, lane, acc, bestv, besti);
-  };
-
-  zero();
-  int cur_b = -1, seg_t0 = 0;
-  bool ok = true;
-  int b = u1 > u0 ? (int)(u0 / KT) : 0, t = u1 > u0 ? (int)(u0 % KT) : 0;
-  int slot = 0;
+  int slot = 0, cseg = 0;
   uint32_t phase = 0;
-  for (int64_t n = u1 - u0; n > 0; --n) {
-    if (b != cur_b) {
-      if (cur_b >= 0) finish(cur_b, seg_t0, KT);
-      cur_b = b;
-      seg_t0 = t;
-      zero();
-    }
-    if (!mbar_wait(&full[slot], phase)) {
-      set_status(p.status, SD_ERR_TIMEOUT);
-      ok = false;
-      break;
-    }
-    const int strip = b * kRB + warp;
-    if (strip < p.NS) {
-      const uint8_t* wsm = sw + slot * C::WB + warp * kStripBytes;
-      const uint4 W0 = *reinterpret_cast<const uint4*>(wsm + lane * 16);
-      const uint4 W1 = *reinterpret_cast<const uint4*>(wsm + 512 + lane * 16);
-      const uint4 W2 = *reinterpret_cast<const uint4*>(wsm + 1024 + lane * 16);
-      const uint32_t xb = smem_u32(sx + slot * C::XB);
-#pragma unroll
-      for (int j = 0; j < 4; j++) {
-        uint32_t a0, a1, a2, a3;
-        decode<AFFINE>(comp(W0, j), comp(W1, j), comp(W2, j), p.base2, p.tab, a0, a1, a2, a3);
-        const int kchunk = 2 * j + ((lane >> 3) & 1);
-        // even and odd sub-tiles accumulate into separate sets (shorter MMA chains)
-        float(*A)[4] = (kDual && (j & 1)) ? acc2 : acc;
-        if (NT == 1) {
-          const int mrow = lane & 7;
-          uint32_t b0, b1;
-          ldsm_x2(xb + mrow * 128 + ((kchunk ^ mrow) << 4), b0, b1);
-          mma_bf16(A[0], a0, a1, a2, a3, b0, b1);
-        } else {
-#pragma unroll
-          for (int np = 0; np < NT; np += 2) {
-            const int mrow = (np + (lane >> 4)) * 8 + (lane & 7);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(xb + mrow * 128 + ((kchunk ^ (lane & 7)) << 4), b0, b1, b2, b3);
-            mma_bf16(A[np], a0, a1, a2, a3, b0, b1);
-            mma_bf16(A[np + 1], a0, a1, a2, a3, b2, b3);
-          }
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
-    if (++slot == C::S) {
-      slot = 0;
-      phase ^= 1u;
-    }
-    if (++t == KT) {
-      t = 0;
-      b++;
-    }
-  }
-  if (ok && cur_b >= 0) finish(cur_b, seg_t0, (int)((u1 - 1) % KT) + 1);
-
-  if (p.e.epi == EPI_LOGITS) {
-#pragma unroll
-    for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-      for (int c = 0; c < 2; c++) {
-        float v = bestv[nt][c];
-        int i = besti[nt][c];
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-          const int oi = __shfl_xor_sync(0xffffffffu, i, off);
-          if (ov > v || (ov == v && oi < i)) {
-            v = ov;
-            i = oi;
-          }
-        }
-        if (lane < 4) {
-          red_v[warp * C::MP + nt * 8 + 2 * lane + c] = v;
-          red_i[warp * C::MP + nt * 8 + 2 * lane + c] = i;
-        }
-      }
-    bar_sync(1, kNCW * 32);
-    if (threadIdx.x < C::MP) {
-      const int ml = threadIdx.x;
-      float v = -INFINITY;
-      int i = 0x7FFFFFFF;
-      for (int w = 0; w < kNCW; w++) {
-        const float ov = red_v[w * C::MP + ml];
-        const int oi = red_i[w * C::MP + ml];
-        if (ov > v || (ov == v && oi < i)) {
-          v = ov;
-          i = oi;
-        }
-      }
-      const int m = p.m0 + ml;
-      if (m < p.M) {
-        p.e.amax_val[(int64_t)blockIdx.x * p.e.ld_amax + m] = v;
-        p.e.amax_idx[(int64_t)blockIdx.x * p.e.ld_amax + m] = i;
-      }
-    }
-  }
+  consume_gemm<NT, AFFINE>(p, sx, sw, full, empty, red_v, red_i, flag, slot, phase, corr, corr_full, corr_empty,
+                           cseg, abort);
 }
 
 // ------------------------------------------------------------------ host --
@@ -435,9 +270,12 @@ int make_gemm_params(GemmParams* out, const w12_tensor& W, const uint16_t* x, in
   for (int i = 0; i < 4; i++)
     p.tab[i] = t16[4 * i] | (t16[4 * i + 1] << 8) | (t16[4 * i + 2] << 16) | ((uint32_t)t16[4 * i + 3] << 24);
   p.esc_slot = W.affine ? ldexpf(1.0f, (int)base + 15 - 127) : 0.0f;
-  p.row_ptr = W.row_ptr;
-  p.esc_idx = W.esc_idx;
-  p.esc_val = W.esc_val;
+  if (W.n_escapes > 0 && (!W.tile_ptr || !W.tile_esc)) {
+    set_error("gemm: the tensor has escapes but no escape tile index (w12_pack_tile_index)");
+    return SD_ERR_INVALID_ARG;
+  }
+  p.tile_ptr = W.n_escapes > 0 ? W.tile_ptr : nullptr;
+  p.tile_esc = W.tile_esc;
   p.x = x;
   p.M = M;
   p.m0 = 0;

@@ -6,18 +6,30 @@
 
 namespace sdv {
 
-constexpr int kNCW = 8;            // consumer warps
+constexpr int kNCW = 8;            // consumer warps 0..7
 constexpr int kRB = kNCW;          // strips per row block
-constexpr int kThreads = (kNCW + 1) * 32;
+constexpr int kProducerWarp = kNCW;     // streams weights and activations into the ring
+constexpr int kEscapeWarp = kNCW + 1;   // computes escape corrections ahead of the consumers
+constexpr int kThreads = (kNCW + 2) * 32;
 constexpr int kStripBytes = 1536;  // one strip x one super-tile (16 x 64 x 12 bit)
 
+// Shared-memory layout of the GEMM kernels (after 1024-byte alignment).
 template <int NT>
 struct Cfg {
   static constexpr int MP = NT * 8;    // padded rows (tokens) per launch
   static constexpr int XB = MP * 128;  // x tile bytes per stage (64 columns of bf16)
   static constexpr int WB = kRB * kStripBytes;
-  static constexpr int S = NT <= 1 ? 8 : NT <= 2 ? 7 : NT <= 4 ? 6 : NT <= 8 ? 5 : 4;
-  static constexpr int SMEM = 1024 + S * (XB + WB) + 2 * S * 8 + kNCW * MP * 8 + 16;
+  static constexpr int S = NT <= 1 ? 8 : NT <= 2 ? 7 : NT <= 8 ? 5 : 4;  // ring stages
+  static constexpr int OFF_W = S * XB;
+  static constexpr int OFF_FULL = OFF_W + S * WB;
+  static constexpr int OFF_EMPTY = OFF_FULL + S * 8;
+  static constexpr int OFF_RED_V = OFF_EMPTY + S * 8;          // argmax scratch [8][MP]
+  static constexpr int OFF_RED_I = OFF_RED_V + kNCW * MP * 4;
+  static constexpr int OFF_FLAG = OFF_RED_I + kNCW * MP * 4;    // finisher flag, abort flag
+  static constexpr int OFF_CBAR = OFF_FLAG + 16;                // escape tile full / empty barriers
+  static constexpr int OFF_CORR = (OFF_CBAR + 16 + 15) & ~15;   // escape corrections [128 rows][MP] fp32
+  static constexpr int END = OFF_CORR + 128 * MP * 4;
+  static constexpr int SMEM = 1024 + END;
 };
 
 struct GemmParams {
@@ -28,9 +40,8 @@ struct GemmParams {
   uint32_t base2;
   uint32_t tab[4];
   float esc_slot;
-  const uint32_t* row_ptr;
-  const uint32_t* esc_idx;
-  const uint16_t* esc_val;
+  const uint32_t* tile_ptr;  // escape tile index (null when there are no escapes)
+  const uint32_t* tile_esc;
   const uint16_t* x;
   int M, m0;
   float* partial;
@@ -72,33 +83,13 @@ __device__ __forceinline__ uint32_t comp(const uint4& v, int j) {
   return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
 }
 
+// Residuals may have been written earlier in the same launch by other CTAs
+// (chained phases): they are read with L1-bypassing loads.
 template <int NT>
 __device__ __forceinline__ void epilogue(const GemmParams& p, int strip, int lane, float (&acc)[NT][4],
                                          float (&bestv)[NT][2], int (&besti)[NT][2]) {
   const int g = lane >> 2, q = lane & 3;
   const int64_t n_lo = (int64_t)strip * 16 + g;
-  const int64_t K = p.K;
-  // escapes of rows n_lo and n_lo + 8
-#pragma unroll
-  for (int h = 0; h < 2; h++) {
-    const int64_t n = n_lo + 8 * h;
-    const uint32_t e0 = p.row_ptr[n], e1 = p.row_ptr[n + 1];
-    for (uint32_t e = e0; e < e1; e++) {
-      const int64_t k = (int64_t)p.esc_idx[e] - n * K;
-      const float w = bf2f(p.esc_val[e]);
-#pragma unroll
-      for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-        for (int cc = 0; cc < 2; cc++) {
-          const int m = p.m0 + nt * 8 + 2 * q + cc;
-          if (m < p.M) {
-            const float xv = bf2f(p.x[(int64_t)m * K + k]);
-            const float a = fmaf(w, xv, acc[nt][2 * h + cc]);
-            acc[nt][2 * h + cc] = fmaf(-p.esc_slot, xv, a);
-          }
-        }
-    }
-  }
   const GemmEpilogue& E = p.e;
 #pragma unroll
   for (int nt = 0; nt < NT; nt++)
@@ -114,7 +105,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int strip, int lan
           break;
         case EPI_RESID: {
           const int64_t i0 = (int64_t)m * E.ldo + n_lo, i1 = i0 + 8;
-          const float r0 = bf2f(E.resid[i0]), r1 = bf2f(E.resid[i1]);
+          const float r0 = bf2f(__ldcg(E.resid + i0)), r1 = bf2f(__ldcg(E.resid + i1));
           E.out[i0] = f2bf(r0 + rbf(v_lo));
           E.out[i1] = f2bf(r1 + rbf(v_hi));
           break;
@@ -185,6 +176,378 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int strip, int lan
         }
       }
     }
+}
+
+// ----------------------------------------------------------- escapes --
+// Escaped weights decode to the slot value in the main loop; the escape warp
+// supplies, for each row-block segment [t0, t1) of a CTA's unit range (in the
+// consumers' order), the correction sum (w - slot) x[m][k] over the escapes of
+// the segment's rows and columns in a shared tile corr[128 rows][MP].  It is
+// a ninth reader of the ring: each stage's escapes - one contiguous run of
+// the escape tile index - are applied from the activation tile already
+// staged in shared memory, one escape at a time with the lanes parallel over
+// the token rows m, in the index's fixed order (deterministic).  The index is
+// read in chunks of 32 tiles: lane i holds the tile pointers of tile tc + i
+// and tc + i + 1 and entries e_lo + i + 32 j; the next chunk's pointers and
+// entries are loaded while the current chunk's stages are processed.
+
+struct EscChunk {
+  uint32_t tpa, tpb;  // tile_ptr of tiles tc + lane, tc + lane + 1 (clamped to the segment end)
+  uint32_t ent[4];    // entries e_lo + lane + 32 j
+  uint32_t e_lo, e_hi;
+};
+
+__device__ __forceinline__ void esc_chunk_ptrs(const GemmParams& p, int b, int tc, int tend, EscChunk& c) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t* tp = p.tile_ptr + (int64_t)b * p.KT;
+  c.tpa = __ldg(tp + min(tc + lane, tend));
+  c.tpb = __ldg(tp + min(tc + lane + 1, tend));
+}
+
+__device__ __forceinline__ void esc_chunk_entries(const GemmParams& p, int tc, int tend, EscChunk& c) {
+  const int lane = threadIdx.x & 31;
+  c.e_lo = __shfl_sync(0xffffffffu, c.tpa, 0);
+  c.e_hi = __shfl_sync(0xffffffffu, c.tpb, min(31, tend - 1 - tc));
+#pragma unroll
+  for (int j = 0; j < 4; j++) {
+    const uint32_t e = c.e_lo + lane + 32 * j;
+    c.ent[j] = e < c.e_hi ? __ldg(p.tile_esc + e) : 0u;
+  }
+}
+
+// The escape warp's work for one GEMM; slot / phase follow the ring exactly
+// as the consumers do (it arrives on every stage's empty barrier).  eseg
+// counts the tiles produced.  Returns false on a failed wait (status set).
+template <int NT>
+__device__ __forceinline__ bool escape_segments(const GemmParams& p, const uint8_t* sx, uint64_t* full,
+                                                uint64_t* empty, int& slot, uint32_t& phase, float* corr,
+                                                uint64_t* corr_full, uint64_t* corr_empty, int& eseg,
+                                                volatile int* abort) {
+  using C = Cfg<NT>;
+  constexpr int MP = C::MP;
+  const int lane = threadIdx.x & 31;
+  const int64_t G = gridDim.x;
+  const int64_t u0 = (int64_t)blockIdx.x * p.U / G, u1 = (int64_t)(blockIdx.x + 1) * p.U / G;
+  if (u1 <= u0) return true;
+  const int KT = p.KT;
+  const int b_first = (int)(u0 / KT), b_last = (int)((u1 - 1) / KT);
+  const bool any = p.tile_ptr != nullptr;
+  const int mrows = min(MP, p.M - p.m0);
+  auto tbeg = [&](int b) { return b == b_first ? (int)(u0 % KT) : 0; };
+  auto tend = [&](int b) { return b == b_last ? (int)((u1 - 1) % KT) + 1 : KT; };
+  bool ok = true;
+  EscChunk cur{}, nxt{};
+  int cb = b_first, ctc = tbeg(b_first), seg_b = -1;
+  if (any) {
+    esc_chunk_ptrs(p, cb, ctc, tend(cb), cur);
+    esc_chunk_entries(p, ctc, tend(cb), cur);
+  }
+  for (;;) {
+    if (cb != seg_b) {
+      if (seg_b >= 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(corr_full);
+        eseg++;
+      }
+      if (!mbar_wait_or_abort(corr_empty, (uint32_t)(eseg & 1) ^ 1u, abort)) {
+        set_status(p.status, SD_TIMEOUT_AT(3));
+        ok = false;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        float* row = corr + (lane + 32 * i) * MP;
+#pragma unroll
+        for (int m = 0; m < MP; m += 4) *reinterpret_cast<float4*>(row + m) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      seg_b = cb;
+    }
+    const int ce = min(ctc + 32, tend(cb));
+    int nb = cb, ntc = ce;
+    if (ntc >= tend(cb)) {
+      nb = cb + 1;
+      ntc = nb <= b_last ? tbeg(nb) : 0;
+    }
+    const bool has_next = nb <= b_last;
+    if (any && has_next) esc_chunk_ptrs(p, nb, ntc, tend(nb), nxt);
+    for (int t = ctc; t < ce; t++) {
+      if (!mbar_wait_or_abort(&full[slot], phase, abort)) {
+        set_status(p.status, SD_TIMEOUT_AT(14));
+        ok = false;
+      }
+      if (any) {
+        const uint8_t* xs = sx + slot * C::XB;
+        const uint32_t lo = __shfl_sync(0xffffffffu, cur.tpa, t - ctc);
+        const uint32_t hi = __shfl_sync(0xffffffffu, cur.tpb, t - ctc);
+        for (uint32_t e = lo; e < hi; e++) {
+          const uint32_t idx = e - cur.e_lo;
+          uint32_t v;
+          if (idx < 128) {
+            const uint32_t r = idx < 32 ? cur.ent[0] : idx < 64 ? cur.ent[1] : idx < 96 ? cur.ent[2] : cur.ent[3];
+            v = __shfl_sync(0xffffffffu, r, idx & 31);
+          } else {
+            v = __ldg(p.tile_esc + e);  // a chunk with more than 128 escapes
+          }
+          const int row = (v >> 6) & 127, kk = v & 63;
+          const float w = bf2f(v >> 16);
+          float* cr = corr + row * MP;
+          for (int m = lane; m < mrows; m += 32) {
+            const float xv = bf2f(
+                *reinterpret_cast<const uint16_t*>(xs + m * 128 + (((kk >> 3) ^ (m & 7)) << 4) + (kk & 7) * 2));
+            const float a = fmaf(w, xv, cr[m]);
+            cr[m] = fmaf(-p.esc_slot, xv, a);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      if (++slot == C::S) {
+        slot = 0;
+        phase ^= 1u;
+      }
+      if (any && has_next && t == ctc) esc_chunk_entries(p, ntc, tend(nb), nxt);
+    }
+    if (!has_next) break;
+    cb = nb;
+    ctc = ntc;
+    cur = nxt;
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(corr_full);
+  eseg++;
+  return ok;
+}
+
+// Consumer warps (0..7) of one GEMM over this CTA's stream-K unit range:
+// wait for each ring stage, decode + MMA, finish row blocks (split ones by
+// the last contributor) and run the epilogue; for EPI_LOGITS also write this
+// CTA's per-row argmax partial.  slot / phase continue the ring position
+// across calls.  Returns false after a timed-out wait (status set).
+// stamps (optional): thread 0 records the device clock when its first stage
+// is ready (stamps[0]) and when its last stage is consumed (stamps[stride]).
+// Escape corrections of each segment come from the escape warp's tile (cseg
+// counts the tiles taken).  After a failed wait (status set) the warps run
+// on with stale data, so all of them keep meeting at the named barriers.
+template <int NT, bool AFFINE>
+__device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, uint8_t* sw, uint64_t* full,
+                                             uint64_t* empty, float* red_v, int* red_i, int* flag, int& slot,
+                                             uint32_t& phase, const float* corr, uint64_t* corr_full,
+                                             uint64_t* corr_empty, int& cseg, volatile int* abort,
+                                             uint64_t* stamps = nullptr, int64_t stride = 0) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t G = gridDim.x;
+  const int64_t u0 = (int64_t)blockIdx.x * p.U / G, u1 = (int64_t)(blockIdx.x + 1) * p.U / G;
+  const int KT = p.KT;
+  // small tiles: even and odd sub-tiles feed separate accumulators so that
+  // consecutive MMAs do not wait on each other; larger tiles have NT
+  // independent MMAs per sub-tile already
+  constexpr bool kDual = NT <= 4;
+  float acc[NT][4], acc2[kDual ? NT : 1][4];
+  float bestv[NT][2];
+  int besti[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+    for (int c = 0; c < 2; c++) {
+      bestv[nt][c] = -INFINITY;
+      besti[nt][c] = 0x7FFFFFFF;
+    }
+  const int first_b = u1 > u0 ? (int)(u0 / KT) : -1;
+
+  auto zero = [&]() {
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        acc[nt][c] = 0.f;
+        if constexpr (kDual) acc2[nt][c] = 0.f;
+      }
+  };
+  auto partial_ptr = [&](int64_t cta, int slot_id) {
+    return p.partial + (((cta * 2 + slot_id) * kRB + warp) * NT) * 128 + lane * 4;
+  };
+  // finish the segment [t0, t1) of row block b
+  auto finish = [&](int b, int t0, int t1) {
+    const int strip = b * kRB + warp;
+    if constexpr (kDual) {
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int c = 0; c < 4; c++) acc[nt][c] += acc2[nt][c];
+    }
+    // this segment's escape corrections
+    if (!mbar_wait_or_abort(corr_full, (uint32_t)(cseg & 1), abort)) set_status(p.status, SD_TIMEOUT_AT(4));
+    {
+      constexpr int MP = Cfg<NT>::MP;
+      const int g = lane >> 2, q = lane & 3;
+      const float* c0 = corr + (warp * 16 + g) * MP;
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int cc = 0; cc < 2; cc++) {
+          acc[nt][cc] += c0[nt * 8 + 2 * q + cc];
+          acc[nt][2 + cc] += c0[8 * MP + nt * 8 + 2 * q + cc];
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(corr_empty);
+    cseg++;
+    if (!(t0 == 0 && t1 == KT)) {
+      const int slot_id = (b == first_b) ? 0 : 1;
+      float* dst = partial_ptr(blockIdx.x, slot_id);
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+        __stcg(reinterpret_cast<float4*>(dst + nt * 128), make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]));
+      // the named barrier orders every thread's partial before thread 0's
+      // device-scope fence and ticket (and the ticket before the others'
+      // reads of the contributors' partials)
+      bar_sync(1, kNCW * 32);
+      if (threadIdx.x == 0) {
+        __threadfence();
+        const int add = t1 - t0;
+        const int old = atomicAdd(&p.counters[b], add);
+        *flag = (old + add == KT) ? 1 : 0;
+        __threadfence();
+      }
+      bar_sync(1, kNCW * 32);
+      if (!*flag) return;
+      zero();
+      // contributors: the CTAs whose (non-empty) unit range meets row block b
+      const int64_t c_first = (((int64_t)b * KT + 1) * G - 1) / p.U;
+      const int64_t c_last = (((int64_t)(b + 1) * KT) * G - 1) / p.U;
+      // partial slots of the contributors, read kBatch at a time with all
+      // loads in flight before any is used (CTA order kept: deterministic)
+      constexpr int kBatch = NT <= 2 ? 4 : 2;
+      for (int64_t c0 = c_first; c0 <= c_last; c0 += kBatch) {
+        float4 v[kBatch][NT];
+        bool use[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; u++) {
+          const int64_t c = c0 + u;
+          const int64_t cs = c * p.U / G, ce = (c + 1) * p.U / G;
+          use[u] = c <= c_last && cs != ce;  // empty ranges never wrote a partial
+          const float* src = partial_ptr(use[u] ? c : blockIdx.x, (use[u] && b != (int)(cs / KT)) ? 1 : 0);
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++)
+            v[u][nt] = use[u] ? __ldcg(reinterpret_cast<const float4*>(src + nt * 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; u++)
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++) {
+            acc[nt][0] += v[u][nt].x;
+            acc[nt][1] += v[u][nt].y;
+            acc[nt][2] += v[u][nt].z;
+            acc[nt][3] += v[u][nt].w;
+          }
+      }
+      if (threadIdx.x == 0) p.counters[b] = 0;
+    }
+    if (strip < p.NS) epilogue<NT>(p, strip, lane, acc, bestv, besti);
+  };
+
+  zero();
+  int cur_b = -1, seg_t0 = 0;
+  bool ok = true;
+  int b = u1 > u0 ? (int)(u0 / KT) : 0, t = u1 > u0 ? (int)(u0 % KT) : 0;
+  for (int64_t n = u1 - u0; n > 0; --n) {
+    if (b != cur_b) {
+      if (cur_b >= 0) finish(cur_b, seg_t0, KT);
+      cur_b = b;
+      seg_t0 = t;
+      zero();
+    }
+    if (!mbar_wait_or_abort(&full[slot], phase, abort)) {
+      set_status(p.status, SD_TIMEOUT_AT(5));
+      ok = false;
+    }
+    if (stamps && threadIdx.x == 0 && n == u1 - u0) stamps[0] = globaltimer();
+    const int strip = b * kRB + warp;
+    if (strip < p.NS) {
+      const uint8_t* wsm = sw + slot * Cfg<NT>::WB + warp * kStripBytes;
+      const uint4 W0 = *reinterpret_cast<const uint4*>(wsm + lane * 16);
+      const uint4 W1 = *reinterpret_cast<const uint4*>(wsm + 512 + lane * 16);
+      const uint4 W2 = *reinterpret_cast<const uint4*>(wsm + 1024 + lane * 16);
+      const uint32_t xb = smem_u32(sx + slot * Cfg<NT>::XB);
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        uint32_t a0, a1, a2, a3;
+        decode<AFFINE>(comp(W0, j), comp(W1, j), comp(W2, j), p.base2, p.tab, a0, a1, a2, a3);
+        const int kchunk = 2 * j + ((lane >> 3) & 1);
+        // even and odd sub-tiles accumulate into separate sets (shorter MMA chains)
+        float(*A)[4] = (kDual && (j & 1)) ? acc2 : acc;
+        if (NT == 1) {
+          const int mrow = lane & 7;
+          uint32_t b0, b1;
+          ldsm_x2(xb + mrow * 128 + ((kchunk ^ mrow) << 4), b0, b1);
+          mma_bf16(A[0], a0, a1, a2, a3, b0, b1);
+        } else {
+#pragma unroll
+          for (int np = 0; np < NT; np += 2) {
+            const int mrow = (np + (lane >> 4)) * 8 + (lane & 7);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(xb + mrow * 128 + ((kchunk ^ (lane & 7)) << 4), b0, b1, b2, b3);
+            mma_bf16(A[np], a0, a1, a2, a3, b0, b1);
+            mma_bf16(A[np + 1], a0, a1, a2, a3, b2, b3);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (++slot == Cfg<NT>::S) {
+      slot = 0;
+      phase ^= 1u;
+    }
+    if (++t == KT) {
+      t = 0;
+      b++;
+    }
+  }
+  if (stamps && threadIdx.x == 0) stamps[stride] = globaltimer();
+  if (cur_b >= 0) finish(cur_b, seg_t0, (int)((u1 - 1) % KT) + 1);
+
+  if (p.e.epi == EPI_LOGITS) {
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int c = 0; c < 2; c++) {
+        float v = bestv[nt][c];
+        int i = besti[nt][c];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+          const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+          if (ov > v || (ov == v && oi < i)) {
+            v = ov;
+            i = oi;
+          }
+        }
+        if (lane < 4) {
+          red_v[warp * Cfg<NT>::MP + nt * 8 + 2 * lane + c] = v;
+          red_i[warp * Cfg<NT>::MP + nt * 8 + 2 * lane + c] = i;
+        }
+      }
+    bar_sync(1, kNCW * 32);
+    if (threadIdx.x < Cfg<NT>::MP) {
+      const int ml = threadIdx.x;
+      float v = -INFINITY;
+      int i = 0x7FFFFFFF;
+      for (int w = 0; w < kNCW; w++) {
+        const float ov = red_v[w * Cfg<NT>::MP + ml];
+        const int oi = red_i[w * Cfg<NT>::MP + ml];
+        if (ov > v || (ov == v && oi < i)) {
+          v = ov;
+          i = oi;
+        }
+      }
+      const int m = p.m0 + ml;
+      if (m < p.M) {
+        p.e.amax_val[(int64_t)blockIdx.x * p.e.ld_amax + m] = v;
+        p.e.amax_idx[(int64_t)blockIdx.x * p.e.ld_amax + m] = i;
+      }
+    }
+  }
+  return ok;
 }
 
 }  // namespace sdv

@@ -7,11 +7,15 @@
 // -> greedy acceptance -> K/V compaction / state commit.
 // Every kernel is launched with programmatic dependent launch, so a GEMM's
 // producer streams its weights while the previous kernel is still finishing.
+// With the chain enabled (up to 128 rows; off by default), each run of GEMMs
+// and RMSNorms between two attention (or recurrence) kernels - O, RMSNorm,
+// gate/up, down, RMSNorm, next q/k/v or lm_head - is one persistent launch.
 #include <algorithm>
 #include <cmath>
 #include <map>
 #include <vector>
 
+#include "chain.cuh"
 #include "gemm.cuh"
 #include "layers.cuh"
 
@@ -46,11 +50,23 @@ struct sd_model {
   };
   std::vector<Graph> graphs;
   bool use_graphs = true;
+  bool use_chain = false;
+  unsigned long long* chain_bar;  // grid-barrier words of the chain kernel (counter, base)
   // optional per-kernel timing
   bool timing = false;
   std::vector<cudaEvent_t> events;  // 2 per entry
   std::vector<int32_t> t_kind;
   std::vector<double> t_bytes;
+  // per-phase stamps of the chain launches of a timed step
+  uint64_t* trace = nullptr;
+  size_t trace_cap = 0;  // u64 entries
+  struct ChainRec {
+    size_t entry, off;
+    int n, G;
+    std::vector<int32_t> kinds;
+    std::vector<double> bytes;
+  };
+  std::vector<ChainRec> t_chain;
 };
 
 namespace sdv {
@@ -96,6 +112,8 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   int rc;
   m->t_kind.clear();
   m->t_bytes.clear();
+  m->t_chain.clear();
+  size_t trace_off = 0;
   // bracket one kernel group with events when timing is on
   auto tbegin = [&](int kind, double bytes) -> int {
     if (!m->timing) return SD_OK;
@@ -116,7 +134,8 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     return SD_OK;
   };
   auto gbytes = [&](const w12_tensor& W, int epi) -> double {
-    double b = (double)W.N * W.K * 1.5 + (double)W.n_escapes * 6.0 + (double)(W.N + 1) * 4.0;
+    // packed words, escape tile index (entries and pointers)
+    double b = (double)W.N * W.K * 1.5 + (double)W.n_escapes * 4.0 + (double)w12_tile_ptr_count(W.N, W.K) * 4.0;
     b += (double)rows * W.K * 2.0;                                        // activations read
     b += (double)rows * W.N * (epi == EPI_SILU ? 1.0 : 2.0);              // outputs written
     if (epi == EPI_RESID) b += (double)rows * W.N * 2.0;                  // residual read
@@ -130,14 +149,91 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     if ((rc = tend())) return rc;                       \
     launches++;                                         \
   } while (0)
-#define GK(kind, W, EPI, expr)                           \
-  do {                                                   \
-    if ((rc = tbegin(kind, gbytes(W, EPI)))) return rc;  \
-    rc = (expr);                                         \
-    if (rc) return rc;                                   \
-    if ((rc = tend())) return rc;                        \
-    launches += rows > 128 ? 2 : 1;                      \
-  } while (0)
+
+  // GEMMs and RMSNorms are queued and launched at the next attention /
+  // recurrence / acceptance kernel: as chain launches, or one by one
+  struct PendingOp {
+    int kind;
+    ChainPhaseDesc d;
+  };
+  std::vector<PendingOp> pend;
+  const bool chain = m->use_chain && rows <= 128 && chain_grid(rows) > 0;
+  auto add_gemm = [&](int kind, const w12_tensor& W, const uint16_t* x, const XMap* xm, const GemmEpilogue& e) {
+    PendingOp op{};
+    op.kind = kind;
+    op.d.type = PH_GEMM;
+    op.d.W = &W;
+    op.d.x = x;
+    op.d.xm = xm;
+    op.d.epi = e;
+    pend.push_back(op);
+  };
+  auto add_norm = [&](const uint16_t* src, const uint16_t* gamma, uint16_t* dst) {
+    PendingOp op{};
+    op.kind = SD_K_NORM;
+    op.d.type = PH_NORM;
+    op.d.norm.src = src;
+    op.d.norm.gamma = gamma;
+    op.d.norm.dst = dst;
+    op.d.norm.H = m->H;
+    op.d.norm.eps = m->cfg.rms_eps;
+    pend.push_back(op);
+  };
+  auto flush = [&]() -> int {
+    size_t i = 0;
+    while (i < pend.size()) {
+      size_t n = 1;
+      if (chain)
+        while (i + n < pend.size() && n < (size_t)kChainMaxPhases) n++;
+      if (n >= 2) {
+        std::vector<ChainPhaseDesc> d;
+        double bytes = 0.0;
+        for (size_t j = i; j < i + n; j++) {
+          d.push_back(pend[j].d);
+          if (pend[j].d.type == PH_GEMM) bytes += gbytes(*pend[j].d.W, pend[j].d.epi.epi);
+        }
+        if ((rc = tbegin(SD_K_GEMM_CHAIN, bytes))) return rc;
+        uint64_t* trace = nullptr;
+        const int G = chain_grid(rows);
+        const size_t rows_tr = 1 + 3 * n;
+        if (m->timing && m->trace && trace_off + rows_tr * (size_t)G <= m->trace_cap) {
+          trace = m->trace + trace_off;
+          sd_model::ChainRec cr;
+          cr.entry = m->t_kind.size() - 1;
+          cr.off = trace_off;
+          cr.n = (int)n;
+          cr.G = G;
+          for (size_t j = i; j < i + n; j++) {
+            cr.kinds.push_back(pend[j].kind);
+            cr.bytes.push_back(pend[j].d.type == PH_GEMM ? gbytes(*pend[j].d.W, pend[j].d.epi.epi) : 0.0);
+          }
+          m->t_chain.push_back(cr);
+          trace_off += rows_tr * (size_t)G;
+        }
+        if ((rc = chain_launch(d.data(), (int)n, rows, m->gws, m->chain_bar, m->status, s, pdl, trace))) return rc;
+        if ((rc = tend())) return rc;
+        launches++;
+      } else {
+        const PendingOp& op = pend[i];
+        if (op.d.type == PH_GEMM) {
+          if ((rc = tbegin(op.kind, gbytes(*op.d.W, op.d.epi.epi)))) return rc;
+          if ((rc = gemm_launch(*op.d.W, op.d.x, *op.d.xm, rows, op.d.epi, m->gws, m->status, s, pdl))) return rc;
+          if ((rc = tend())) return rc;
+          launches += rows > 128 ? 2 : 1;
+        } else {
+          if ((rc = tbegin(SD_K_NORM, 0.0))) return rc;
+          const cudaError_t e = launch_rmsnorm(op.d.norm.src, op.d.norm.gamma, rows, op.d.norm.H, op.d.norm.eps,
+                                               op.d.norm.dst, nullptr, nullptr, nullptr, nullptr, nullptr, s, pdl);
+          if (e != cudaSuccess) return cuda_fail(e, "rmsnorm");
+          if ((rc = tend())) return rc;
+          launches++;
+        }
+      }
+      i += n;
+    }
+    pend.clear();
+    return SD_OK;
+  };
 
   if (m->timing) {
     // let the host enqueue the whole step before the GPU starts on it
@@ -184,7 +280,8 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
       eq.out = m->qkv_rec + (int64_t)ls * m->max_rows * 3 * m->H;
       eq.ldo = 3 * m->H;
     }
-    GK(SD_K_GEMM_QKV, Lw.qkv, eq.epi, gemm_launch(Lw.qkv, m->xn, *mx, rows, eq, m->gws, m->status, s, pdl));
+    add_gemm(SD_K_GEMM_QKV, Lw.qkv, m->xn, mx, eq);
+    if ((rc = flush())) return rc;
     if (is_attn) {
       AttnArgs aa{};
       aa.q = m->q;
@@ -233,23 +330,21 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     eo.out = m->h;
     eo.resid = m->x;
     eo.ldo = m->H;
-    GK(SD_K_GEMM_O, Lw.o, EPI_RESID, gemm_launch(Lw.o, m->attn, *ma, rows, eo, m->gws, m->status, s, pdl));
-    LK(SD_K_NORM, launch_rmsnorm(m->h, Lw.mlp_norm, rows, m->H, m->cfg.rms_eps, m->xn, nullptr, nullptr, nullptr, nullptr,
-                      nullptr, s, pdl));
+    add_gemm(SD_K_GEMM_O, Lw.o, m->attn, ma, eo);
+    add_norm(m->h, Lw.mlp_norm, m->xn);
     GemmEpilogue eg;
     eg.epi = EPI_SILU;
     eg.out = m->act;
     eg.ldo = m->I;
-    GK(SD_K_GEMM_GATE_UP, Lw.gate_up, EPI_SILU, gemm_launch(Lw.gate_up, m->xn, *mx, rows, eg, m->gws, m->status, s, pdl));
+    add_gemm(SD_K_GEMM_GATE_UP, Lw.gate_up, m->xn, mx, eg);
     GemmEpilogue ed;  // x = h + down(act)
     ed.epi = EPI_RESID;
     ed.out = m->x;
     ed.resid = m->h;
     ed.ldo = m->H;
-    GK(SD_K_GEMM_DOWN, Lw.down, EPI_RESID, gemm_launch(Lw.down, m->act, *mc, rows, ed, m->gws, m->status, s, pdl));
+    add_gemm(SD_K_GEMM_DOWN, Lw.down, m->act, mc, ed);
     const uint16_t* gnext = l + 1 < m->cfg.n_layers ? m->layers[l + 1].attn_norm : m->w.final_norm;
-    LK(SD_K_NORM, launch_rmsnorm(m->x, gnext, rows, m->H, m->cfg.rms_eps, m->xn, nullptr, nullptr, nullptr, nullptr, nullptr, s,
-                      pdl));
+    add_norm(m->x, gnext, m->xn);
   }
   GemmEpilogue el;
   el.epi = EPI_LOGITS;
@@ -258,7 +353,8 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   el.amax_val = m->amax_val;
   el.amax_idx = m->amax_idx;
   el.ld_amax = m->max_rows;
-  GK(SD_K_GEMM_LM_HEAD, m->w.lm_head, EPI_LOGITS, gemm_launch(m->w.lm_head, m->xn, *mx, rows, el, m->gws, m->status, s, pdl));
+  add_gemm(SD_K_GEMM_LM_HEAD, m->w.lm_head, m->xn, mx, el);
+  if ((rc = flush())) return rc;
 
   AcceptArgs ac{};
   ac.tokens = io.tokens;
@@ -287,7 +383,6 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
                            m->path_len, s, pdl));
   }
 #undef LK
-#undef GK
   m->last_launches = launches;
   return SD_OK;
 }
@@ -300,6 +395,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
 // sequence; values behind the pointers are read at run time.
 static int launch_step(sd_model* m, const StepIO& io, cudaStream_t s, std::vector<uintptr_t> key) {
   if (!m->use_graphs || m->timing || s == nullptr) return run_step(m, io, s);
+  key.push_back((uintptr_t)m->use_chain);
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   SD_CK(cudaStreamIsCapturing(s, &cs));
   if (cs != cudaStreamCaptureStatusNone) return run_step(m, io, s);
@@ -394,7 +490,7 @@ extern "C" int sd_model_row_map(int32_t kind, int32_t n_q_heads, int32_t n_kv_he
 }
 
 static bool tensor_ok(const w12_tensor& t, int64_t N, int64_t K) {
-  return t.words && t.row_ptr && t.N == N && t.K == K && (t.n_escapes == 0 || (t.esc_idx && t.esc_val));
+  return t.words && t.N == N && t.K == K && (t.n_escapes == 0 || (t.tile_ptr && t.tile_esc));
 }
 
 extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weights* w, sd_model** out) {
@@ -489,6 +585,7 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
       {(void**)&m->amax_idx, (size_t)gemm_grid(1) * MR * 4},
       {(void**)&m->gws.partial, gemm_partial_floats(MR) * 4},
       {(void**)&m->gws.counters, (size_t)gemm_counters(max_n) * 4},
+      {(void**)&m->chain_bar, 16},
   };
   size_t total = 0;
   for (auto& it : items) total = al256(total + it.bytes);
@@ -531,6 +628,7 @@ extern "C" int sd_model_destroy(sd_model* m) {
   if (!m) return SD_OK;
   for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);
   for (cudaEvent_t e : m->events) cudaEventDestroy(e);
+  if (m->trace) cudaFree(m->trace);
   cudaFree(m->arena);
   delete m;
   return SD_OK;
@@ -646,6 +744,9 @@ extern "C" int sd_status(sd_model* m, int32_t* status_host) {
   SD_CK(cudaDeviceSynchronize());
   SD_CK(cudaMemcpy(status_host, m->status, 4, cudaMemcpyDeviceToHost));
   SD_CK(cudaMemset(m->status, 0, 4));
+  // a chain that gave up on a barrier may have left its arrival counter
+  // short of a multiple of the grid: start the next one from zero
+  if (*status_host != SD_OK) SD_CK(cudaMemset(m->chain_bar, 0, 16));
   return SD_OK;
 }
 
@@ -657,6 +758,15 @@ extern "C" int sd_model_set_timing(sd_model* m, int32_t enable) {
     return SD_ERR_INVALID_ARG;
   }
   m->timing = enable != 0;
+  if (m->timing && !m->trace) {
+    // stamps of every chain launch of one step: (layers + 2) launches of at
+    // most 1 + 3 x 6 rows x the largest grid (filled with zeros: a CTA
+    // without work in a phase leaves two of its stamps unwritten)
+    const size_t cap = (size_t)(m->cfg.n_layers + 2) * (1 + 3 * kChainMaxPhases) * gemm_grid(1);
+    SD_CK(cudaMalloc(&m->trace, cap * sizeof(uint64_t)));
+    SD_CK(cudaMemset(m->trace, 0, cap * sizeof(uint64_t)));
+    m->trace_cap = cap;
+  }
   return SD_OK;
 }
 
@@ -669,15 +779,74 @@ extern "C" int sd_model_timeline(sd_model* m, int32_t max, int32_t* kind_host, f
     set_error("sd_model_timeline: device error");
     return -1;
   }
-  const int n = std::min<int>(max, (int)m->t_kind.size());
-  for (int i = 0; i < n; i++) {
+  int n = 0;
+  size_t ci = 0;
+  for (size_t i = 0; i < m->t_kind.size() && n < max; i++) {
     float ms = 0.f;
     if (cudaEventElapsedTime(&ms, m->events[2 * i], m->events[2 * i + 1]) != cudaSuccess) ms = -1.f;
-    kind_host[i] = m->t_kind[i];
-    ms_host[i] = ms;
-    bytes_host[i] = m->t_bytes[i];
+    kind_host[n] = m->t_kind[i];
+    ms_host[n] = ms;
+    bytes_host[n] = m->t_bytes[i];
+    n++;
+    if (ci < m->t_chain.size() && m->t_chain[ci].entry == i) {
+      // the chain's phases from the device stamps: phase p lasts from the
+      // last CTA finishing phase p - 1 (the first CTA starting, for p = 0)
+      // to the last CTA finishing phase p
+      const sd_model::ChainRec& cr = m->t_chain[ci++];
+      std::vector<uint64_t> st((size_t)(1 + 3 * cr.n) * cr.G);
+      if (cudaMemcpy(st.data(), m->trace + cr.off, st.size() * sizeof(uint64_t), cudaMemcpyDeviceToHost) !=
+          cudaSuccess) {
+        set_error("sd_model_timeline: trace copy failed");
+        return -1;
+      }
+      uint64_t prev = ~0ull;
+      for (int c = 0; c < cr.G; c++) prev = std::min(prev, st[c]);
+      for (int p = 0; p < cr.n && n < max; p++) {
+        uint64_t end = 0;
+        for (int c = 0; c < cr.G; c++) end = std::max(end, st[(size_t)(3 + 3 * p) * cr.G + c]);
+        kind_host[n] = 100 + cr.kinds[p];
+        ms_host[n] = (float)((double)(end - prev) * 1e-6);
+        bytes_host[n] = cr.bytes[p];
+        n++;
+        prev = end;
+      }
+    }
   }
   return n;
+}
+
+extern "C" int sd_model_chain_trace(sd_model* m, int32_t launch, int32_t* n_phases, int32_t* n_ctas,
+                                    uint64_t* stamps_host, int64_t max_stamps) {
+  if (!m || !n_phases || !n_ctas || launch < 0) {
+    set_error("sd_model_chain_trace: bad argument");
+    return SD_ERR_INVALID_ARG;
+  }
+  if (launch >= (int)m->t_chain.size()) {
+    set_error("sd_model_chain_trace: no such chain launch in the last timed step");
+    return SD_ERR_INVALID_ARG;
+  }
+  const sd_model::ChainRec& cr = m->t_chain[launch];
+  *n_phases = cr.n;
+  *n_ctas = cr.G;
+  const size_t cnt = (size_t)(1 + 3 * cr.n) * cr.G;
+  if (stamps_host) {
+    if (max_stamps < (int64_t)cnt) {
+      set_error("sd_model_chain_trace: buffer too small");
+      return SD_ERR_INVALID_ARG;
+    }
+    SD_CK(cudaDeviceSynchronize());
+    SD_CK(cudaMemcpy(stamps_host, m->trace + cr.off, cnt * sizeof(uint64_t), cudaMemcpyDeviceToHost));
+  }
+  return SD_OK;
+}
+
+extern "C" int sd_model_set_chain(sd_model* m, int32_t enable) {
+  if (!m) {
+    set_error("sd_model_set_chain: null model");
+    return SD_ERR_INVALID_ARG;
+  }
+  m->use_chain = enable != 0;
+  return SD_OK;
 }
 
 extern "C" int sd_model_set_graphs(sd_model* m, int32_t enable) {

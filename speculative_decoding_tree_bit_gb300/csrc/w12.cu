@@ -229,6 +229,40 @@ __global__ void k_row_ptr(const uint32_t* __restrict__ esc_idx, int64_t n_esc, i
   }
 }
 
+// Escape tile index of one 128-row block (one CTA): count the block's
+// escapes per 64-column tile, prefix-sum from the block's first side-list
+// index, then place them tile by tile keeping the side list's (row-major)
+// order within each tile.
+__global__ void k_tile_index(const uint32_t* __restrict__ esc_idx, const uint16_t* __restrict__ esc_val,
+                             const uint32_t* __restrict__ row_ptr, int64_t N, int64_t K,
+                             uint32_t* __restrict__ tile_ptr, uint32_t* __restrict__ tile_esc) {
+  extern __shared__ uint32_t cursor[];  // [KT]
+  const int KT = (int)(K / 64);
+  const int64_t b = blockIdx.x;
+  const int64_t n0 = b * 128, n1 = n0 + 128 < N ? n0 + 128 : N;
+  const uint32_t e0 = row_ptr[n0], e1 = row_ptr[n1];
+  for (int t = threadIdx.x; t < KT; t += blockDim.x) cursor[t] = 0;
+  __syncthreads();
+  for (uint32_t e = e0 + threadIdx.x; e < e1; e += blockDim.x)
+    atomicAdd(&cursor[(int)((esc_idx[e] % (uint64_t)K) / 64)], 1u);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t run = e0;
+    for (int t = 0; t < KT; t++) {
+      const uint32_t c = cursor[t];
+      tile_ptr[b * KT + t] = run;
+      cursor[t] = run;
+      run += c;
+    }
+    if (b == gridDim.x - 1) tile_ptr[(b + 1) * KT] = e1;
+    for (uint32_t e = e0; e < e1; e++) {
+      const uint64_t idx = esc_idx[e];
+      const uint32_t n = (uint32_t)(idx / (uint64_t)K), k = (uint32_t)(idx % (uint64_t)K);
+      tile_esc[cursor[k / 64]++] = ((uint32_t)esc_val[e] << 16) | ((n - (uint32_t)n0) << 6) | (k & 63u);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- unpack --
 
 struct TableArg {
@@ -357,6 +391,29 @@ extern "C" int w12_pack_encode(const uint16_t* w, const int32_t* row_src, const 
   k_row_ptr<<<grid_for(N + 1, 256), 256, 0, s>>>(esc_idx, meta->n_escapes, N, K, row_ptr);
   SD_CK(cudaGetLastError());
   SD_CK(cudaFreeAsync(scratch, s));
+  return SD_OK;
+}
+
+extern "C" int64_t w12_tile_ptr_count(int64_t N, int64_t K) { return ((N + 127) / 128) * (K / 64) + 1; }
+
+extern "C" int w12_pack_tile_index(const w12_tensor* t, uint32_t* tile_ptr, uint32_t* tile_esc, void* stream) {
+  if (!t || !tile_ptr || !t->row_ptr || (t->n_escapes > 0 && (!t->esc_idx || !t->esc_val || !tile_esc))) {
+    set_error("w12_pack_tile_index: null pointer");
+    return SD_ERR_INVALID_ARG;
+  }
+  if (t->N <= 0 || t->K <= 0 || t->N % 16 || t->K % 64 || t->N * t->K >= (int64_t)1 << 32) {
+    set_error("w12_pack_tile_index: bad shape");
+    return SD_ERR_UNSUPPORTED;
+  }
+  const int64_t NB = (t->N + 127) / 128, KT = t->K / 64;
+  const size_t smem = (size_t)KT * sizeof(uint32_t);
+  if (smem > 48 * 1024) {
+    set_error("w12_pack_tile_index: K too large (K/64 tiles must fit 48 KB of shared memory)");
+    return SD_ERR_UNSUPPORTED;
+  }
+  k_tile_index<<<(unsigned)NB, 256, smem, (cudaStream_t)stream>>>(t->esc_idx, t->esc_val, t->row_ptr, t->N, t->K,
+                                                                  tile_ptr, tile_esc);
+  SD_CK(cudaGetLastError());
   return SD_OK;
 }
 

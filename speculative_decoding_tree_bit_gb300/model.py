@@ -31,8 +31,9 @@ def _i32(a, device="cuda") -> torch.Tensor:
 class Packed:
     """A W12-packed tensor on the device (owns its buffers)."""
 
-    def __init__(self, meta: W12Meta, words, esc_idx, esc_val, row_ptr):
+    def __init__(self, meta: W12Meta, words, esc_idx, esc_val, row_ptr, tile_ptr=None, tile_esc=None):
         self.meta, self.words, self.esc_idx, self.esc_val, self.row_ptr = meta, words, esc_idx, esc_val, row_ptr
+        self.tile_ptr, self.tile_esc = tile_ptr, tile_esc
 
     N = property(lambda self: int(self.meta.N))
     K = property(lambda self: int(self.meta.K))
@@ -47,6 +48,7 @@ class Packed:
         t.N, t.K = self.meta.N, self.meta.K
         t.words, t.esc_idx, t.esc_val, t.row_ptr = (_ptr(self.words), _ptr(self.esc_idx), _ptr(self.esc_val),
                                                     _ptr(self.row_ptr))
+        t.tile_ptr, t.tile_esc = _ptr(self.tile_ptr), _ptr(self.tile_esc)
         t.n_escapes = self.meta.n_escapes
         t.table = self.meta.table
         t.n_table = self.meta.n_table
@@ -54,8 +56,8 @@ class Packed:
         return t
 
     def nbytes(self) -> int:
-        """Bytes a GEMM streams: the packed words plus the escape side list."""
-        return (self.words.numel() * 4 + self.n_escapes * 6 + self.row_ptr.numel() * 4)
+        """Bytes a GEMM streams: the packed words plus the escape tile index."""
+        return self.words.numel() * 4 + self.n_escapes * 4 + int(lib().w12_tile_ptr_count(self.N, self.K)) * 4
 
 
 def pack(w: torch.Tensor, row_src: np.ndarray | None = None, stream=None) -> Packed:
@@ -74,8 +76,13 @@ def pack(w: torch.Tensor, row_src: np.ndarray | None = None, stream=None) -> Pac
     rs = None if row_src is None else _i32(row_src, dev)
     check(lib().w12_pack_encode(w.data_ptr(), _ptr(rs), ctypes.byref(meta), words.data_ptr(), esc_idx.data_ptr(),
                                 esc_val.data_ptr(), row_ptr.data_ptr(), s))
-    torch.cuda.current_stream().synchronize()
-    return Packed(meta, words, esc_idx, esc_val, row_ptr)
+    p = Packed(meta, words, esc_idx, esc_val, row_ptr)
+    p.tile_ptr = torch.empty(int(lib().w12_tile_ptr_count(N, K)), dtype=torch.int32, device=dev)
+    p.tile_esc = torch.empty(ne, dtype=torch.int32, device=dev)
+    t = p.struct()
+    check(lib().w12_pack_tile_index(ctypes.byref(t), p.tile_ptr.data_ptr(), p.tile_esc.data_ptr(), s))
+    torch.cuda.synchronize()
+    return p
 
 
 def unpack(p: Packed, stream=None) -> torch.Tensor:
@@ -189,11 +196,16 @@ class Model:
     def set_graphs(self, on: bool):
         check(lib().sd_model_set_graphs(self.handle, 1 if on else 0))
 
+    def set_chain(self, on: bool):
+        """Chained GEMM/RMSNorm launches (default on) or one kernel per op."""
+        check(lib().sd_model_set_chain(self.handle, 1 if on else 0))
+
     def set_timing(self, on: bool):
         check(lib().sd_model_set_timing(self.handle, 1 if on else 0))
 
     def timeline(self, max_entries: int = 4096):
-        """[(kind name, ms, algorithmic bytes)] of the last timed call."""
+        """[(kind name, ms, algorithmic bytes)] of the last timed call; the
+        phases of a chain launch follow it as "chain.<kind>" entries."""
         from . import KERNEL_KINDS
         k = np.zeros(max_entries, np.int32)
         ms = np.zeros(max_entries, np.float32)
@@ -201,7 +213,19 @@ class Model:
         n = lib().sd_model_timeline(self.handle, max_entries, k.ctypes.data, ms.ctypes.data, b.ctypes.data)
         if n < 0:
             check(3)
-        return [(KERNEL_KINDS[k[i]], float(ms[i]), float(b[i])) for i in range(n)]
+        def name(x):
+            return "chain." + KERNEL_KINDS[x - 100] if x >= 100 else KERNEL_KINDS[x]
+        return [(name(int(k[i])), float(ms[i]), float(b[i])) for i in range(n)]
+
+    def chain_trace(self, launch: int):
+        """Device-clock stamps (ns) of chain launch `launch` of the last timed
+        step as an array [1 + 3 n_phases][n_ctas] (see sd_model_chain_trace)."""
+        n, g = ctypes.c_int32(), ctypes.c_int32()
+        check(lib().sd_model_chain_trace(self.handle, launch, ctypes.byref(n), ctypes.byref(g), None, 0))
+        buf = np.zeros((1 + 3 * n.value) * g.value, np.uint64)
+        check(lib().sd_model_chain_trace(self.handle, launch, ctypes.byref(n), ctypes.byref(g), buf.ctypes.data,
+                                         buf.size))
+        return buf.reshape(1 + 3 * n.value, g.value)
 
     def outputs(self, M: int, logits: bool = False, R: int = 1):
         d = self.device

@@ -191,3 +191,26 @@ def test_graph_capture_and_replay_match_direct_launches(M, dec):
     for r in results[1:]:
         for k in r:
             assert torch.equal(r[k], results[0][k]), k
+
+
+@pytest.mark.parametrize("n", [5, 16, 64])
+def test_chained_and_per_kernel_launches_give_identical_bits(M, dec, n):
+    """The persistent GEMM chain and one kernel per GEMM / RMSNorm (default)
+    share the partition and the summation order: same bits everywhere."""
+    shape, W, model = dec
+    ctx = 45
+    td = wl.draft(40 + n, 0, n, 6, 0.8, shape.V)
+    tok = np.random.default_rng(n).integers(0, shape.V, n).astype(np.int32)
+    results = []
+    for chain in (True, False, True):
+        model.set_chain(chain)
+        kv = M.KVCache(shape, ctx + 80).fill(3, ctx)
+        o = model.verify(tok, td.parents, kv, logits=True)
+        torch.cuda.synchronize()
+        assert model.status() == 0
+        results.append({k: v.clone() for k, v in o.items()} | {"k": kv.k.clone(), "v": kv.v.clone(),
+                                                               "S": kv.S.clone(), "ctx": kv.ctx_len.clone()})
+    model.set_chain(False)
+    for r in results[1:]:
+        for k in r:
+            assert torch.equal(r[k], results[0][k]), k

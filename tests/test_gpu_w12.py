@@ -28,7 +28,27 @@ def _cmp(M, W, row_src=None):
         assert np.array_equal(p.esc_val[: o.n_esc].cpu().numpy().view(np.uint16), o.esc_val)
     assert np.array_equal(p.row_ptr.cpu().numpy().view(np.uint32), o.row_ptr)
     assert np.array_equal(M.unpack(p).cpu().numpy().view(np.uint16), Wsrc)
+    _cmp_tile_index(p, o)
     return p
+
+
+def _cmp_tile_index(p, o):
+    """The escape tile index regroups the oracle's side list by (128-row
+    block, 64-column tile), row-major inside a group: bit-exact."""
+    N, K = p.N, p.K
+    NB, KT = (N + 127) // 128, K // 64
+    idx = o.esc_idx.astype(np.int64)
+    n, k = idx // K, idx % K
+    key = (n // 128) * KT + k // 64
+    order = np.argsort(key, kind="stable")  # side list is row-major: stable keeps it inside a group
+    want_ptr = np.zeros(NB * KT + 1, np.int64)
+    np.add.at(want_ptr, key + 1, 1)
+    want_ptr = np.cumsum(want_ptr)
+    want_esc = ((o.esc_val.astype(np.uint32) << 16) | ((n % 128).astype(np.uint32) << 6)
+                | (k % 64).astype(np.uint32))[order]
+    assert np.array_equal(p.tile_ptr.cpu().numpy().view(np.uint32).astype(np.int64), want_ptr)
+    if o.n_esc:
+        assert np.array_equal(p.tile_esc[: o.n_esc].cpu().numpy().view(np.uint32), want_esc)
 
 
 def test_every_bf16_pattern(M):
