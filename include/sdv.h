@@ -369,8 +369,7 @@ enum {
 int sd_model_set_timing(sd_model* m, int32_t enable);
 
 /* Timeline of the last timed call: for entry i, kind_host[i] (SD_K_*),
- * ms_host[i] (event-measured duration; SD_K_ATTN covers the split kernel and
- * its combine) and bytes_host[i] (algorithmic bytes of a GEMM: packed words,
+ * ms_host[i] (event-measured duration) and bytes_host[i] (algorithmic bytes of a GEMM: packed words,
  * escape list, row pointers, activations read and written; 0 for other
  * kinds).  Each SD_K_GEMM_CHAIN entry is followed by one entry per phase of
  * that launch with kind 100 + the phase's kind (SD_K_GEMM_O, SD_K_NORM, ...):

@@ -151,17 +151,27 @@ cudaError_t launch_rmsnorm(const uint16_t* src, const uint16_t* gamma, int rows,
 // rows (4 warps x 16).  Keys of a prefix split are a contiguous range of the
 // committed prefix; the last split holds the tree's own keys (slots ctx ..
 // ctx+M-1) masked by the row's ancestor bits.  Keys stream through a
-// double-buffered 64-key tile (cp.async, 16-byte XOR swizzle); S = Q K^T and
-// O += P V run on mma.m16n8k16 with an online (base-2) softmax in fp32.
+// 2-stage ring of 64-key K and V tiles (cp.async, 16-byte XOR swizzle); S =
+// Q K^T and O += P V run on mma.m16n8k16 with an online (base-2) softmax in
+// fp32.  Many short splits keep the tensor-core latency chains of one warp
+// short.  Each split writes its (max, sum, unnormalised O) partial, then the
+// splits of a (request, kv head, row chunk) merge them in split order
+// (deterministic) into the bf16 output: when the whole grid fits on the GPU
+// at once, every split waits (bounded) for its group's partials and merges a
+// 1/P share of the rows; otherwise the last split to finish merges them all.
+// The group counters return to zero for the next call.
 
 constexpr int kAttnTile = 64;
-constexpr int kAttnSmem = 4 * kAttnTile * 128 * 2;  // K and V, double buffered
+constexpr int kAttnStages = 2;
+constexpr int kAttnSmem = kAttnStages * 2 * kAttnTile * 128 * 2;  // K and V tiles
 
 int attn_rows_per_group(int hq, int hkv, int max_m) { return (hq / hkv) * max_m; }
 
 struct AttnKernelArgs {
   AttnArgs a;
-  int rpg;  // row stride of one (request, kv head, split) group in the partial arrays
+  int rpg;     // row stride of one (request, kv head, split) group in the partial arrays
+  int chunks;  // row chunks of 64 per (request, kv head)
+  int coop;    // 1: the whole grid is resident, splits merge together
 };
 
 __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
@@ -170,14 +180,15 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
   const AttnArgs& a = ka.a;
   extern __shared__ __align__(128) uint8_t smem_attn[];
   uint16_t* sK = reinterpret_cast<uint16_t*>(smem_attn);
-  uint16_t* sV = sK + 2 * kAttnTile * 128;
+  uint16_t* sV = sK + kAttnStages * kAttnTile * 128;
+  __shared__ int s_last;
   const int sp = blockIdx.x;
   const int h = blockIdx.y % a.hkv, rc = blockIdx.y / a.hkv;
   const int r = blockIdx.z;
   const int G = a.hq / a.hkv;
   const int node0 = a.cu[r], Mr = a.cu[r + 1] - node0;
   const int rows = G * Mr;
-  if (rc * 64 >= rows) return;
+  if (rc * 64 >= rows) return;  // no rows: no split of this chunk writes or merges anything
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
   const int rt = rc * 4 + warp;
   const int ctx = a.ctx[r];
@@ -199,6 +210,33 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
   const int n0 = v0 ? rho0 % Mr : 0, n1 = v1 ? rho1 % Mr : 0;
   const int qh0 = h * G + (v0 ? rho0 / Mr : 0), qh1 = h * G + (v1 ? rho1 / Mr : 0);
   const uint64_t anc0 = v0 ? a.anc[node0 + n0] : 0ull, anc1 = v1 ? a.anc[node0 + n1] : 0ull;
+
+  const int64_t head_stride = (int64_t)a.page_size * 128;
+  auto load_tile = [&](int tile, int buf) {
+    const int kb = k0 + tile * kAttnTile;
+    for (int c = threadIdx.x; c < kAttnTile * 16; c += 128) {
+      const int kr = c >> 4, ch = c & 15;
+      const int t = kb + kr;
+      const bool valid = t < k1;
+      int64_t off = 0;
+      if (valid) {
+        const int page = a.page_table[(int64_t)r * a.max_pages + t / a.page_size];
+        off = ((int64_t)page * a.hkv + h) * head_stride + (int64_t)(t % a.page_size) * 128 + ch * 8;
+      }
+      const int so = (buf * kAttnTile + kr) * 128 + ((ch ^ (kr & 7)) * 8);
+      cp_async16_zfill(sK + so, a.k_pool + off, valid);
+      cp_async16_zfill(sV + so, a.v_pool + off, valid);
+    }
+  };
+  const int ntiles = (k1 - k0 + kAttnTile - 1) / kAttnTile;
+  // exactly kAttnStages - 1 groups before the loop and one per iteration, so
+  // that waiting for all but the newest kAttnStages - 1 completes the tile
+#pragma unroll
+  for (int i = 0; i < kAttnStages - 1; i++) {
+    if (i < ntiles) load_tile(i, i);
+    cp_async_commit();
+  }
+
   uint32_t qa[8][4];
   {
     const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q + ((int64_t)(node0 + n0) * a.hq + qh0) * 128);
@@ -217,34 +255,11 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
   const float sl2 = 0.08838834764831845f * 1.4426950408889634f;  // log2(e) / sqrt(128)
 
-  const int64_t head_stride = (int64_t)a.page_size * 128;
-  auto load_tile = [&](int tile, int buf) {
-    const int kb = k0 + tile * kAttnTile;
-    for (int c = threadIdx.x; c < kAttnTile * 16; c += 128) {
-      const int kr = c >> 4, ch = c & 15;
-      const int t = kb + kr;
-      const bool valid = t < k1;
-      int64_t off = 0;
-      if (valid) {
-        const int page = a.page_table[(int64_t)r * a.max_pages + t / a.page_size];
-        off = ((int64_t)page * a.hkv + h) * head_stride + (int64_t)(t % a.page_size) * 128 + ch * 8;
-      }
-      const int so = (buf * kAttnTile + kr) * 128 + ((ch ^ (kr & 7)) * 8);
-      cp_async16_zfill(sK + so, a.k_pool + off, valid);
-      cp_async16_zfill(sV + so, a.v_pool + off, valid);
-    }
-    cp_async_commit();
-  };
-  const int ntiles = (k1 - k0 + kAttnTile - 1) / kAttnTile;
-  if (ntiles > 0) load_tile(0, 0);
   for (int tile = 0; tile < ntiles; tile++) {
-    const int buf = tile & 1;
-    if (tile + 1 < ntiles) {
-      load_tile(tile + 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    const int buf = tile % kAttnStages;
+    if (tile + kAttnStages - 1 < ntiles) load_tile(tile + kAttnStages - 1, (tile + kAttnStages - 1) % kAttnStages);
+    cp_async_commit();
+    cp_async_wait<kAttnStages - 1>();
     __syncthreads();
     if (has_rows) {
       float s[8][4];
@@ -327,62 +342,141 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
     }
     __syncthreads();
   }
-  if (!has_rows) return;
-  const int64_t gbase = ((int64_t)(r * a.hkv + h) * (a.splits + 1) + sp) * ka.rpg;
-#pragma unroll
-  for (int rr = 0; rr < 2; rr++) {
-    const int rho = rr ? rho1 : rho0;
-    if (rho >= rows) continue;
-    const int64_t b = gbase + rho;
-    if (q == 0) {
-      a.part_ml[b * 2] = mrow[rr];
-      a.part_ml[b * 2 + 1] = lrow[rr];
-    }
-    float* dst = a.part_o + b * 128;
-#pragma unroll
-    for (int dn = 0; dn < 16; dn++)
-      *reinterpret_cast<float2*>(dst + dn * 8 + 2 * q) = make_float2(o[dn][2 * rr], o[dn][2 * rr + 1]);
-  }
-}
+  cp_async_wait<0>();
 
-// out[m][qh] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the splits.
-__global__ void __launch_bounds__(128) k_attn_combine(AttnKernelArgs ka) {
-  pdl_wait();
-  pdl_launch();
-  const AttnArgs& a = ka.a;
-  const int m = blockIdx.x, qh = blockIdx.y, d = threadIdx.x;
-  const int r = a.row_req[m];
-  const int node = m - a.cu[r], Mr = a.cu[r + 1] - a.cu[r];
-  const int G = a.hq / a.hkv, h = qh / G;
-  const int rho = (qh % G) * Mr + node;
+  // this split's partial
   const int64_t gbase = (int64_t)(r * a.hkv + h) * (a.splits + 1);
-  float mx = -INFINITY;
-  for (int sp = 0; sp <= a.splits; sp++) mx = fmaxf(mx, a.part_ml[((gbase + sp) * ka.rpg + rho) * 2]);
-  float L = 0.f, acc = 0.f;
-  for (int sp = 0; sp <= a.splits; sp++) {
-    const int64_t b = (gbase + sp) * ka.rpg + rho;
-    const float mm = a.part_ml[b * 2];
-    if (mm == -INFINITY) continue;
-    const float w = exp2f(mm - mx);
-    L += w * a.part_ml[b * 2 + 1];
-    acc += w * a.part_o[b * 128 + d];
+  if (has_rows) {
+#pragma unroll
+    for (int rr = 0; rr < 2; rr++) {
+      const int rho = rr ? rho1 : rho0;
+      if (rho >= rows) continue;
+      const int64_t b = (gbase + sp) * ka.rpg + rho;
+      if (q == 0) {
+        __stcg(a.part_ml + b * 2, mrow[rr]);
+        __stcg(a.part_ml + b * 2 + 1, lrow[rr]);
+      }
+      float* dst = a.part_o + b * 128;
+#pragma unroll
+      for (int dn = 0; dn < 16; dn++)
+        __stcg(reinterpret_cast<float2*>(dst + dn * 8 + 2 * q), make_float2(o[dn][2 * rr], o[dn][2 * rr + 1]));
+    }
   }
-  a.out[(int64_t)m * a.hq * 128 + qh * 128 + d] = f2bf(L > 0.f ? acc / L : 0.f);
+  // group counters: [0] splits that wrote their partial, [1] splits done merging
+  const int P = a.splits + 1;
+  int32_t* gc = a.tickets + (((int64_t)r * a.hkv + h) * ka.chunks + rc) * 2;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int old = atomicAdd(gc, 1);
+    if (ka.coop) {
+      // wait (bounded) for the group's other splits
+      int v = old + 1;
+      const uint64_t t0 = globaltimer();
+      while (v < P) {
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          set_status(a.status, SD_TIMEOUT_AT(20));
+          break;
+        }
+        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(gc) : "memory");
+      }
+      s_last = 1;
+    } else {
+      s_last = old == P - 1;
+      if (s_last) *gc = 0;
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // rows merged by this CTA
+  const int rbeg0 = rc * 64, nrow0 = min(rows, rbeg0 + 64) - rbeg0;
+  const int rbeg = ka.coop ? rbeg0 + sp * nrow0 / P : rbeg0;
+  const int nrow = ka.coop ? rbeg0 + (sp + 1) * nrow0 / P - rbeg : nrow0;
+  // merge: split weights 2^(m_p - max) / L for every (row, split) into shared
+  // memory (one pass of independent loads), then each thread forms 4-wide
+  // slices of the output with its partial loads batched
+  float* wsm = reinterpret_cast<float*>(smem_attn);  // [64 rows][kMaxParts] (K/V ring no longer needed)
+  constexpr int kMaxParts = 33;
+  for (int i = threadIdx.x; i < nrow; i += 128) {
+    const int rho = rbeg + i;
+    // every split's (max, sum) in flight at once
+    float2 ml[kMaxParts];
+#pragma unroll
+    for (int p = 0; p < kMaxParts; p++)
+      ml[p] = p < P ? __ldcg(reinterpret_cast<const float2*>(a.part_ml + ((gbase + p) * ka.rpg + rho) * 2))
+                    : make_float2(-INFINITY, 0.f);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int p = 0; p < kMaxParts; p++) mx = fmaxf(mx, ml[p].x);
+    float L = 0.f;
+#pragma unroll
+    for (int p = 0; p < kMaxParts; p++) {
+      ml[p].x = ml[p].x == -INFINITY ? 0.f : exp2f(ml[p].x - mx);
+      L += ml[p].x * ml[p].y;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int p = 0; p < kMaxParts; p++)
+      if (p < P) wsm[i * kMaxParts + p] = ml[p].x * inv;
+  }
+  __syncthreads();
+  // slice = (row, 4 dims): 32 slices per row; a slice's partials are loaded
+  // 16 splits at a time, all in flight before they are used
+  for (int sl = threadIdx.x; sl < nrow * 32; sl += 128) {
+    const int i = sl >> 5, d4 = sl & 31;
+    const float4* src = reinterpret_cast<const float4*>(a.part_o + (gbase * ka.rpg + rbeg + i) * 128) + d4;
+    const int64_t pstride = (int64_t)ka.rpg * 32;  // float4 per split
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < P; p0 += 16) {
+      float4 v[16];
+#pragma unroll
+      for (int u = 0; u < 16; u++) v[u] = p0 + u < P ? __ldcg(src + (p0 + u) * pstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 16; u++) {
+        const float w = p0 + u < P ? wsm[i * kMaxParts + p0 + u] : 0.f;
+        acc.x = fmaf(w, v[u].x, acc.x);
+        acc.y = fmaf(w, v[u].y, acc.y);
+        acc.z = fmaf(w, v[u].z, acc.z);
+        acc.w = fmaf(w, v[u].w, acc.w);
+      }
+    }
+    const int rho = rbeg + i;
+    const int node = rho % Mr, qh = h * G + rho / Mr;
+    uint2 o2;
+    o2.x = pack_bf16x2(acc.x, acc.y);
+    o2.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(a.out + (int64_t)(node0 + node) * a.hq * 128 + qh * 128 + d4 * 4) = o2;
+  }
+  if (ka.coop) {
+    // the last split to finish merging resets the group's counters (every
+    // split has passed its wait by then)
+    __syncthreads();
+    if (threadIdx.x == 0 && atomicAdd(gc + 1, 1) == P - 1) {
+      gc[0] = 0;
+      gc[1] = 0;
+    }
+  }
 }
 
 cudaError_t launch_attention(const AttnArgs& a, int rows_total, cudaStream_t s, bool pdl) {
+  (void)rows_total;
   static bool attr = false;
   if (!attr) {
     const cudaError_t e = cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
+  static int per_sm = -1;
+  if (per_sm < 0) {
+    carveout_once(reinterpret_cast<const void*>(k_attn));
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_attn, 128, kAttnSmem) != cudaSuccess) per_sm = 0;
+  }
   const int rpg = attn_rows_per_group(a.hq, a.hkv, a.max_m);
-  const AttnKernelArgs ka{a, rpg};
   const int chunks = (rpg + 63) / 64;
-  const cudaError_t e = launch(k_attn, dim3(a.splits + 1, a.hkv * chunks, a.R), dim3(128), kAttnSmem, s, pdl, ka);
-  if (e != cudaSuccess) return e;
-  return launch(k_attn_combine, dim3(rows_total, a.hq), dim3(128), 0, s, pdl, ka);
+  const int64_t grid = (int64_t)(a.splits + 1) * a.hkv * chunks * a.R;
+  const AttnKernelArgs ka{a, rpg, chunks, grid <= (int64_t)per_sm * num_sms() ? 1 : 0};
+  return launch(k_attn, dim3(a.splits + 1, a.hkv * chunks, a.R), dim3(128), kAttnSmem, s, pdl, ka);
 }
 
 // ------------------------------------------------- linear recurrence -----

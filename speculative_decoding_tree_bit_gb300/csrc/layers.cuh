@@ -52,6 +52,8 @@ struct AttnArgs {
   int R, max_m, splits;    // splits = prefix splits (the tree segment is one more)
   float* part_o;           // [R][Hkv][splits+1][rows_per_group][hd]
   float* part_ml;          // [R][Hkv][splits+1][rows_per_group][2]
+  int32_t* tickets;        // [R][Hkv][row chunks][2]: zero between calls (each call resets its own)
+  int32_t* status;         // a bounded wait that gave up records SD_ERR_TIMEOUT
   uint16_t* out;           // [rows][Hq*hd]
 };
 int attn_rows_per_group(int hq, int hkv, int max_m);

@@ -33,6 +33,7 @@ struct sd_model {
   int32_t *ctx_snap, *req_ok, *pos, *slotv, *req, *depth, *path, *path_len, *status, *cu, *page0, *acc_scratch;
   uint64_t* anc;
   float *attn_o, *attn_ml;
+  int32_t* attn_tickets;
   size_t attn_units;  // capacity in (request x (splits+1)) units
   float* amax_val;
   int32_t* amax_idx;
@@ -73,6 +74,8 @@ namespace sdv {
 
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Prefix splits per (request, kv head, row chunk): about one CTA per SM, so
+// that each split's key range (and its tensor-core latency chain) is short.
 static int attn_splits(int R, int hkv, int chunks) {
   const int ctas = R * hkv * chunks;
   const int s = (num_sms() + ctas - 1) / ctas - 1;
@@ -302,12 +305,14 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
       aa.splits = splits;
       aa.part_o = m->attn_o;
       aa.part_ml = m->attn_ml;
+      aa.tickets = m->attn_tickets;
+      aa.status = m->status;
       aa.out = m->attn;
       if ((rc = tbegin(SD_K_ATTN, 0.0))) return rc;
       const cudaError_t e = launch_attention(aa, rows, s, pdl);
       if (e != cudaSuccess) return cuda_fail(e, "attention");
       if ((rc = tend())) return rc;
-      launches += 2;
+      launches += 1;
     } else {
       LinrecArgs la{};
       la.qkv = m->qkv_rec + (int64_t)ls * m->max_rows * 3 * m->H;
@@ -581,6 +586,7 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
       {(void**)&m->anc, (size_t)MR * 8},
       {(void**)&m->attn_o, units * m->Hkv * rpg * 128 * 4},
       {(void**)&m->attn_ml, units * m->Hkv * rpg * 2 * 4},
+      {(void**)&m->attn_tickets, (size_t)R * m->Hkv * chunks * 2 * 4},
       {(void**)&m->amax_val, (size_t)gemm_grid(1) * MR * 4},
       {(void**)&m->amax_idx, (size_t)gemm_grid(1) * MR * 4},
       {(void**)&m->gws.partial, gemm_partial_floats(MR) * 4},
