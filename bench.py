@@ -242,7 +242,7 @@ def chain_phase_summary(model, launch):
         return {"error": str(e)}
     n = (st.shape[0] - 1) // 3
     prev = int(st[0].min())
-    out = []
+    out = [{"start": [round(float(np.median(st[0]) - prev) / 1e3, 2), round(float(st[0].max() - prev) / 1e3, 2)]}]
     for p in range(n):
         row = {}
         for name, r in (("first_ready", 1 + 3 * p), ("last_consumed", 2 + 3 * p), ("finished", 3 + 3 * p)):
@@ -250,7 +250,14 @@ def chain_phase_summary(model, launch):
             row[name] = [round(float(np.median(v) - prev) / 1e3, 2), round(float(v.max() - prev) / 1e3, 2)] if v.size else None
         out.append(row)
         prev = int(st[3 + 3 * p].max())
-    return {"chain_launch": launch, "phases_us_median_max": out}
+    res = {"chain_launch": launch, "phases_us_median_max": out}
+    if n == 1:
+        # spread of the stream end over the CTAs, and the slowest CTAs
+        lc = (st[2] - st[0].min()) / 1e3
+        res["last_consumed_pct"] = [round(float(np.percentile(lc, q)), 2) for q in (10, 50, 90, 99)]
+        res["slowest_ctas"] = [int(i) for i in np.argsort(lc)[-12:]]
+        res["fastest_ctas"] = [int(i) for i in np.argsort(lc)[:12]]
+    return res
 
 
 def gpu_arm(args, rank, world, dist):
@@ -359,8 +366,11 @@ def gpu_arm(args, rank, world, dist):
     torch.cuda.synchronize()
     tl = model.timeline()
     chain_phases = None
-    if args.timeline and args.chain:
-        chain_phases = chain_phase_summary(model, shape.n_layers // 2)
+    if args.timeline:
+        # the middle layer's launches (a chain, or its four GEMMs)
+        per_layer = 1 if args.chain else 4
+        first = 1 + (shape.n_layers // 2) * per_layer if not args.chain else shape.n_layers // 2
+        chain_phases = [chain_phase_summary(model, first + i) for i in range(per_layer)]
     model.set_timing(False)
 
     if dist is not None:
@@ -369,7 +379,7 @@ def gpu_arm(args, rank, world, dist):
         ms, ms_e2e = float(t[0]), float(t[1])
 
     pk, pk_src = peaks()
-    gemm = [(k, t, b) for k, t, b in tl if k.startswith("gemm")]  # chain launches and lone GEMMs
+    gemm = [(k, t, b) for k, t, b in tl if k.startswith("gemm")]  # chain launches and lone GEMMs (not their traces)
     g_ms = sum(t for _, t, _ in gemm)
     g_bytes = sum(b for _, _, b in gemm)
     achieved = g_bytes / (g_ms * 1e-3) / 1e9 if g_ms > 0 else None

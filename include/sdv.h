@@ -338,8 +338,9 @@ int sd_model_set_graphs(sd_model* m, int32_t enable);
  * Returns SD_OK or SD_ERR_INVALID_ARG for a null model. */
 int sd_model_set_chain(sd_model* m, int32_t enable);
 
-/* Raw device-clock stamps (%globaltimer, ns) of chain launch `launch` (0 =
- * the first chain launch) of the last timed step: *n_phases = n, *n_ctas = G
+/* Raw device-clock stamps (%globaltimer, ns) of traced launch `launch` (0 =
+ * the first) of the last timed step - every chain launch, and every lone
+ * GEMM launch of at most 128 rows as a one-phase record: *n_phases = n, *n_ctas = G
  * and, when stamps_host is not NULL (room for max_stamps >= (1 + 3n) G
  * values), stamps_host[r * G + c] for CTA c: r = 0 its start; for phase i,
  * r = 1 + 3i when its first stage was ready (RMSNorm phase: input complete),
@@ -369,13 +370,15 @@ enum {
 int sd_model_set_timing(sd_model* m, int32_t enable);
 
 /* Timeline of the last timed call: for entry i, kind_host[i] (SD_K_*),
- * ms_host[i] (event-measured duration) and bytes_host[i] (algorithmic bytes of a GEMM: packed words,
- * escape list, row pointers, activations read and written; 0 for other
- * kinds).  Each SD_K_GEMM_CHAIN entry is followed by one entry per phase of
- * that launch with kind 100 + the phase's kind (SD_K_GEMM_O, SD_K_NORM, ...):
- * its time runs from the last CTA finishing the previous phase (the first CTA
- * starting, for the first phase) to the last CTA finishing this one, read from
- * the device clock (%globaltimer); these entries overlap their chain entry.
+ * ms_host[i] (event-measured duration) and bytes_host[i] (algorithmic bytes
+ * of a GEMM: packed words, escape tile index, activations read and written;
+ * 0 for other kinds).  Each traced launch (every SD_K_GEMM_CHAIN entry, and
+ * each lone GEMM of at most 128 rows) is followed by one entry per phase
+ * with kind 100 + the phase's kind (SD_K_GEMM_O, SD_K_NORM, ...): its time
+ * runs from the last CTA finishing the previous phase (the first CTA
+ * starting, for the first phase) to the last CTA finishing this one, read
+ * from the device clock (%globaltimer); these entries overlap their launch's
+ * entry.
  * Synchronises the device.  Returns the number of entries written (<= max),
  * or -1 with sd_last_error set. */
 int sd_model_timeline(sd_model* m, int32_t max, int32_t* kind_host, float* ms_host, double* bytes_host);

@@ -73,6 +73,15 @@ __device__ __forceinline__ void set_status(int* st, int code) {
 #define SD_TIMEOUT_AT(site) SD_ERR_TIMEOUT
 #endif
 
+// Add with release (this thread's writes, and those ordered before it by a
+// named barrier) and acquire (the writes released by earlier adders)
+// semantics at device scope; returns the old value.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -151,10 +151,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
 
   // --------------------------------------------------------- consumers --
   pdl_wait();
+  if (p.trace && threadIdx.x == 0) p.trace[blockIdx.x] = globaltimer();
   int slot = 0, cseg = 0;
   uint32_t phase = 0;
   consume_gemm<NT, AFFINE>(p, sx, sw, full, empty, red_v, red_i, flag, slot, phase, corr, corr_full, corr_empty,
-                           cseg, abort);
+                           cseg, abort, p.trace ? p.trace + G + blockIdx.x : nullptr, G);
+  if (p.trace) {
+    bar_sync(1, kNCW * 32);
+    if (threadIdx.x == 0) p.trace[3 * G + blockIdx.x] = globaltimer();
+  }
 }
 
 // ------------------------------------------------------------------ host --
@@ -164,6 +169,17 @@ int pad_rows(int M) { return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 
 static int nt_of(int M) { return M > 128 ? 16 : pad_rows(M) / 8; }
 
 int gemm_grid(int M) { return (nt_of(M) <= 4 ? 2 : 1) * num_sms(); }
+
+int gemm_launch_grid(const w12_tensor& W, int M, int epi) {
+  int grid = gemm_grid(M);
+  // few row blocks (q/k/v, O, down): a whole number of CTAs per row block,
+  // so that no CTA's range straddles two row blocks (a straddling CTA
+  // finishes two segments and trails the others); the argmax partials of
+  // the logits GEMM keep one slot per CTA of gemm_grid
+  const int nb = gemm_counters(W.N);
+  if (epi != EPI_LOGITS && nb * 4 <= grid) grid = nb * (grid / nb);
+  return grid;
+}
 
 size_t gemm_partial_floats(int M) { return (size_t)gemm_grid(M) * 2 * kRB * nt_of(M) * 128; }
 
@@ -287,11 +303,12 @@ int make_gemm_params(GemmParams* out, const w12_tensor& W, const uint16_t* x, in
 }
 
 int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
-                const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid) {
-  if (grid <= 0) grid = gemm_grid(M);
+                const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid, uint64_t* trace) {
+  if (grid <= 0) grid = gemm_launch_grid(W, M, epi.epi);
   GemmParams p;
   const int prc = make_gemm_params(&p, W, x, M, epi, ws, status);
   if (prc) return prc;
+  p.trace = M <= 128 ? trace : nullptr;
   if (ws.counters_len < p.NB) {
     set_error("gemm: workspace counters too small");
     return SD_ERR_WORKSPACE;

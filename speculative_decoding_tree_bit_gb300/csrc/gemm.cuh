@@ -54,6 +54,7 @@ struct GemmWorkspace {
 };
 
 int gemm_grid(int M);               // CTAs per launch for M rows (persistent: 1 or 2 per SM)
+int gemm_launch_grid(const w12_tensor& W, int M, int epi);  // the grid gemm_launch uses by default
 size_t gemm_partial_floats(int M);  // workspace floats for M rows
 int gemm_counters(int64_t N);       // counters for N rows
 int pad_rows(int M);                // rows of one launch's TMA box: 8, 16, 32, 64 or 128
@@ -68,9 +69,12 @@ int make_x_map(XMap* xm, const uint16_t* x, int rows_total, int64_t K, int box_r
 
 // y = epilogue(x W^T) for rows [0, M); M > 128 runs in launches of 128 rows.
 // grid: CTAs per launch, 0 = gemm_grid(M); the partial-sum workspace must
-// hold grid * 2 * 8 * (padded rows / 8) * 128 floats.
+// hold grid * 2 * 8 * (padded rows / 8) * 128 floats.  trace (optional, M <=
+// 128): [4][grid] device-clock stamps per CTA - start, first stage ready,
+// last stage consumed, finished.
 int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
-                const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid = 0);
+                const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid = 0,
+                uint64_t* trace = nullptr);
 
 // Descriptor of the packed words for the 2-D weight loads (one box = 8
 // strips x 1536 bytes).

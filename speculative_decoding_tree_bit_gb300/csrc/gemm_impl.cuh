@@ -48,6 +48,7 @@ struct GemmParams {
   int32_t* counters;
   GemmEpilogue e;
   int32_t* status;
+  uint64_t* trace;  // optional: [4][grid] device-clock stamps (start, first stage ready, last consumed, finished)
 };
 
 __device__ __forceinline__ uint32_t lut_exp(uint32_t c, const uint32_t* tab) {
@@ -402,11 +403,9 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
       // reads of the contributors' partials)
       bar_sync(1, kNCW * 32);
       if (threadIdx.x == 0) {
-        __threadfence();
         const int add = t1 - t0;
-        const int old = atomicAdd(&p.counters[b], add);
+        const int old = atomic_add_acq_rel(&p.counters[b], add);
         *flag = (old + add == KT) ? 1 : 0;
-        __threadfence();
       }
       bar_sync(1, kNCW * 32);
       if (!*flag) return;

@@ -220,7 +220,23 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
         const PendingOp& op = pend[i];
         if (op.d.type == PH_GEMM) {
           if ((rc = tbegin(op.kind, gbytes(*op.d.W, op.d.epi.epi)))) return rc;
-          if ((rc = gemm_launch(*op.d.W, op.d.x, *op.d.xm, rows, op.d.epi, m->gws, m->status, s, pdl))) return rc;
+          // timed steps record the launch's per-CTA stamps as a one-phase trace
+          uint64_t* trace = nullptr;
+          const int G = gemm_launch_grid(*op.d.W, rows, op.d.epi.epi);
+          if (m->timing && m->trace && rows <= 128 && trace_off + 4 * (size_t)G <= m->trace_cap) {
+            trace = m->trace + trace_off;
+            sd_model::ChainRec cr;
+            cr.entry = m->t_kind.size() - 1;
+            cr.off = trace_off;
+            cr.n = 1;
+            cr.G = G;
+            cr.kinds.push_back(op.kind);
+            cr.bytes.push_back(gbytes(*op.d.W, op.d.epi.epi));
+            m->t_chain.push_back(cr);
+            trace_off += 4 * (size_t)G;
+          }
+          if ((rc = gemm_launch(*op.d.W, op.d.x, *op.d.xm, rows, op.d.epi, m->gws, m->status, s, pdl, 0, trace)))
+            return rc;
           if ((rc = tend())) return rc;
           launches += rows > 128 ? 2 : 1;
         } else {
@@ -765,9 +781,10 @@ extern "C" int sd_model_set_timing(sd_model* m, int32_t enable) {
   }
   m->timing = enable != 0;
   if (m->timing && !m->trace) {
-    // stamps of every chain launch of one step: (layers + 2) launches of at
-    // most 1 + 3 x 6 rows x the largest grid (filled with zeros: a CTA
-    // without work in a phase leaves two of its stamps unwritten)
+    // stamps of every chain or GEMM launch of one step: at most (layers + 2)
+    // chains of 1 + 3 x 6 rows, or 4 GEMMs per layer + lm_head of 4 rows, x
+    // the largest grid (zero-filled: a CTA without work in a phase leaves
+    // two of its stamps unwritten)
     const size_t cap = (size_t)(m->cfg.n_layers + 2) * (1 + 3 * kChainMaxPhases) * gemm_grid(1);
     SD_CK(cudaMalloc(&m->trace, cap * sizeof(uint64_t)));
     SD_CK(cudaMemset(m->trace, 0, cap * sizeof(uint64_t)));
