@@ -260,6 +260,35 @@ def chain_phase_summary(model, launch):
     return res
 
 
+def overlapped_layer_trace(model, stream, step, layer):
+    """Device-clock stamps of one layer's GEMMs in an untimed-style step
+    (programmatic dependent launch, no events): per GEMM, the first CTA start,
+    the median first stage, the last stream end and the last CTA finish, in us
+    after the layer's first GEMM start."""
+    import numpy as np
+    import torch
+    model.set_timing(2)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+    torch.cuda.synchronize()
+    # traced launches: qkv of layer 0, then per layer attention, o, gate_up, down, next qkv
+    names = ["attention", "o", "gate_up", "down", "qkv_next"]
+    rows = []
+    t0 = None
+    for i in range(5):
+        st = model.chain_trace(1 + layer * 5 + i).astype(np.int64)
+        if t0 is None:
+            t0 = int(st[0].min())
+        rows.append({"kernel": names[i], "start": round((st[0].min() - t0) / 1e3, 2),
+                     "row1_med": round((np.median(st[1]) - t0) / 1e3, 2),
+                     "row2_max": round((st[2].max() - t0) / 1e3, 2),
+                     "end_max": round((st[3].max() - t0) / 1e3, 2)})
+    model.set_timing(False)
+    return {"overlapped_layer": layer, "rows": "gemm: start, first stage (median), last stream end, last finish; "
+            "attention: start, keys done (median), group ready (max), end", "kernels": rows}
+
+
 def gpu_arm(args, rank, world, dist):
     import numpy as np
     import torch
@@ -367,11 +396,14 @@ def gpu_arm(args, rank, world, dist):
     tl = model.timeline()
     chain_phases = None
     if args.timeline:
-        # the middle layer's launches (a chain, or its four GEMMs)
+        # the middle layer's launches (a chain, or its four GEMMs after its attention)
         per_layer = 1 if args.chain else 4
-        first = 1 + (shape.n_layers // 2) * per_layer if not args.chain else shape.n_layers // 2
+        first = 2 + (shape.n_layers // 2) * 5 if not args.chain else shape.n_layers // 2
         chain_phases = [chain_phase_summary(model, first + i) for i in range(per_layer)]
     model.set_timing(False)
+    overlap = None
+    if args.timeline and not args.chain:
+        overlap = overlapped_layer_trace(model, stream, step, shape.n_layers // 2)
 
     if dist is not None:
         t = torch.tensor([ms, ms_e2e], device=dev)
@@ -401,6 +433,8 @@ def gpu_arm(args, rank, world, dist):
                         for k, v in by_kind.items()}))
         if chain_phases:
             log(json.dumps(chain_phases))
+        if overlap:
+            log(json.dumps(overlap))
     value = world * M / (ms * 1e-3)
     res = {
         "metric": "tree_tokens_per_s", "value": value, "unit": "tree tokens/s",

@@ -339,8 +339,10 @@ int sd_model_set_graphs(sd_model* m, int32_t enable);
 int sd_model_set_chain(sd_model* m, int32_t enable);
 
 /* Raw device-clock stamps (%globaltimer, ns) of traced launch `launch` (0 =
- * the first) of the last timed step - every chain launch, and every lone
- * GEMM launch of at most 128 rows as a one-phase record: *n_phases = n, *n_ctas = G
+ * the first) of the last timed step - every chain launch, every lone GEMM
+ * launch of at most 128 rows and every attention launch as a one-phase
+ * record (attention rows: start, keys done, group's partials ready, end):
+ * *n_phases = n, *n_ctas = G
  * and, when stamps_host is not NULL (room for max_stamps >= (1 + 3n) G
  * values), stamps_host[r * G + c] for CTA c: r = 0 its start; for phase i,
  * r = 1 + 3i when its first stage was ready (RMSNorm phase: input complete),
@@ -368,6 +370,10 @@ enum {
  * steps are slower than untimed ones; use the numbers for the breakdown,
  * not the step time. */
 int sd_model_set_timing(sd_model* m, int32_t enable);
+/* (enable = 2: device-clock traces only - no events and no delay kernel,
+ * kernels launched directly with programmatic dependent launch as in an
+ * untimed step, so the traces show the overlapped schedule; the timeline
+ * then has no event-timed entries worth reading, use sd_model_chain_trace.) */
 
 /* Timeline of the last timed call: for entry i, kind_host[i] (SD_K_*),
  * ms_host[i] (event-measured duration) and bytes_host[i] (algorithmic bytes

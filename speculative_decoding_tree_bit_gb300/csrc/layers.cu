@@ -19,8 +19,8 @@ namespace sdv {
 __global__ void k_tree(const int32_t* __restrict__ tokens, const int32_t* __restrict__ parents,
                        const int32_t* __restrict__ cu, CacheView cv, int vocab, int max_positions, StepRows rows,
                        int32_t* status) {
+  pdl_launch();  // the next kernel may start streaming its (independent) weights now
   pdl_wait();
-  pdl_launch();
   __shared__ uint64_t anc[64];
   __shared__ int dep[64];
   __shared__ int okflag, ctx_s;
@@ -91,8 +91,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const uint16_t* __restrict__ sr
                                                  const uint16_t* __restrict__ embed, uint16_t* __restrict__ x_out,
                                                  const int32_t* __restrict__ row_req,
                                                  const int32_t* __restrict__ req_ok) {
+  pdl_launch();  // the next kernel may start streaming its (independent) weights now
   pdl_wait();
-  pdl_launch();
   const int m = blockIdx.x;
   const uint16_t* row;
   if (embed) {
@@ -175,9 +175,15 @@ struct AttnKernelArgs {
 };
 
 __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
+  pdl_launch();  // the next kernel may start streaming its (independent) weights now
   pdl_wait();
-  pdl_launch();
   const AttnArgs& a = ka.a;
+  const int64_t cta = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+  const int64_t ncta = (int64_t)gridDim.x * gridDim.y * gridDim.z;
+  auto stamp = [&](int row) {
+    if (a.trace && threadIdx.x == 0) a.trace[row * ncta + cta] = globaltimer();
+  };
+  stamp(0);
   extern __shared__ __align__(128) uint8_t smem_attn[];
   uint16_t* sK = reinterpret_cast<uint16_t*>(smem_attn);
   uint16_t* sV = sK + kAttnStages * kAttnTile * 128;
@@ -188,7 +194,12 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
   const int G = a.hq / a.hkv;
   const int node0 = a.cu[r], Mr = a.cu[r + 1] - node0;
   const int rows = G * Mr;
-  if (rc * 64 >= rows) return;  // no rows: no split of this chunk writes or merges anything
+  if (rc * 64 >= rows) {  // no rows: no split of this chunk writes or merges anything
+    stamp(1);
+    stamp(2);
+    stamp(3);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
   const int rt = rc * 4 + warp;
   const int ctx = a.ctx[r];
@@ -343,6 +354,7 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
     __syncthreads();
   }
   cp_async_wait<0>();
+  stamp(1);
 
   // this split's partial
   const int64_t gbase = (int64_t)(r * a.hkv + h) * (a.splits + 1);
@@ -388,37 +400,39 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
     __threadfence();
   }
   __syncthreads();
-  if (!s_last) return;
+  stamp(2);
+  if (!s_last) {
+    stamp(3);
+    return;
+  }
   // rows merged by this CTA
   const int rbeg0 = rc * 64, nrow0 = min(rows, rbeg0 + 64) - rbeg0;
   const int rbeg = ka.coop ? rbeg0 + sp * nrow0 / P : rbeg0;
   const int nrow = ka.coop ? rbeg0 + (sp + 1) * nrow0 / P - rbeg : nrow0;
-  // merge: split weights 2^(m_p - max) / L for every (row, split) into shared
-  // memory (one pass of independent loads), then each thread forms 4-wide
-  // slices of the output with its partial loads batched
-  float* wsm = reinterpret_cast<float*>(smem_attn);  // [64 rows][kMaxParts] (K/V ring no longer needed)
-  constexpr int kMaxParts = 33;
+  // merge: every (row, split) (max, sum) pair into shared memory with all
+  // loads in flight, then per row the split weights 2^(m_p - max) / L; then
+  // each thread forms 4-wide slices of the output with its partial loads
+  // batched
+  constexpr int kMaxParts = 65;
+  float* wsm = reinterpret_cast<float*>(smem_attn);                // [64 rows][kMaxParts] weights
+  float2* mlsm = reinterpret_cast<float2*>(wsm + 64 * kMaxParts);  // [64 rows][kMaxParts] (max, sum)
+  for (int e = threadIdx.x; e < nrow * P; e += 128) {
+    const int i = e / P, p = e - i * P;
+    mlsm[i * kMaxParts + p] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + ((gbase + p) * ka.rpg + rbeg + i) * 2));
+  }
+  __syncthreads();
   for (int i = threadIdx.x; i < nrow; i += 128) {
-    const int rho = rbeg + i;
-    // every split's (max, sum) in flight at once
-    float2 ml[kMaxParts];
-#pragma unroll
-    for (int p = 0; p < kMaxParts; p++)
-      ml[p] = p < P ? __ldcg(reinterpret_cast<const float2*>(a.part_ml + ((gbase + p) * ka.rpg + rho) * 2))
-                    : make_float2(-INFINITY, 0.f);
+    const float2* ml = mlsm + i * kMaxParts;
     float mx = -INFINITY;
-#pragma unroll
-    for (int p = 0; p < kMaxParts; p++) mx = fmaxf(mx, ml[p].x);
+    for (int p = 0; p < P; p++) mx = fmaxf(mx, ml[p].x);
     float L = 0.f;
-#pragma unroll
-    for (int p = 0; p < kMaxParts; p++) {
-      ml[p].x = ml[p].x == -INFINITY ? 0.f : exp2f(ml[p].x - mx);
-      L += ml[p].x * ml[p].y;
+    for (int p = 0; p < P; p++) {
+      const float w = ml[p].x == -INFINITY ? 0.f : exp2f(ml[p].x - mx);
+      wsm[i * kMaxParts + p] = w;
+      L += w * ml[p].y;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-    for (int p = 0; p < kMaxParts; p++)
-      if (p < P) wsm[i * kMaxParts + p] = ml[p].x * inv;
+    for (int p = 0; p < P; p++) wsm[i * kMaxParts + p] *= inv;
   }
   __syncthreads();
   // slice = (row, 4 dims): 32 slices per row; a slice's partials are loaded
@@ -457,6 +471,8 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
       gc[1] = 0;
     }
   }
+  __syncthreads();
+  stamp(3);
 }
 
 cudaError_t launch_attention(const AttnArgs& a, int rows_total, cudaStream_t s, bool pdl) {
@@ -490,8 +506,8 @@ __device__ __forceinline__ float phi(float x) { return x > 0.f ? x + 1.0f : expf
 constexpr int kRecSmem = (64 * 128 * 2 + 128 * 32 + 64 * 32 + 128 + 64 * 64 + 64) * 4;
 
 __global__ void __launch_bounds__(128) k_linrec(LinrecArgs a) {
+  pdl_launch();  // the next kernel may start streaming its (independent) weights now
   pdl_wait();
-  pdl_launch();
   extern __shared__ __align__(16) float smem_rec[];
   float* fq = smem_rec;       // [64][128]
   float* fk = fq + 64 * 128;  // [64][128]
@@ -562,8 +578,8 @@ cudaError_t launch_linrec(const LinrecArgs& a, cudaStream_t s, bool pdl) {
 // --------------------------------------------------- argmax + accept -----
 
 __global__ void k_accept(AcceptArgs a) {
+  pdl_launch();  // the next kernel may start streaming its (independent) weights now
   pdl_wait();
-  pdl_launch();
   __shared__ int am[64], par[64], dep[64], okn[64], pth[65];
   const int r = blockIdx.x;
   const int node0 = a.cu ? a.cu[r] : 0, Mr = a.cu ? a.cu[r + 1] - node0 : a.single_M;
@@ -631,8 +647,8 @@ cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s, bool pdl) {
 __global__ void __launch_bounds__(128) k_compact(CacheView cv, int hkv, const int32_t* __restrict__ ctx_snap,
                                                  const int32_t* __restrict__ path,
                                                  const int32_t* __restrict__ path_len) {
+  pdl_launch();  // the next kernel may start streaming its (independent) weights now
   pdl_wait();
-  pdl_launch();
   __shared__ uint4 bk[65][16], bv[65][16];
   const int r = blockIdx.x, la = blockIdx.y, h = blockIdx.z;
   const int P = path_len[r];
@@ -668,8 +684,8 @@ __global__ void __launch_bounds__(128) k_rec_commit(CacheView cv, int n_rec, int
                                                     const uint16_t* __restrict__ qkv_rec,
                                                     const int32_t* __restrict__ cu, const int32_t* __restrict__ path,
                                                     const int32_t* __restrict__ path_len) {
+  pdl_launch();  // the next kernel may start streaming its (independent) weights now
   pdl_wait();
-  pdl_launch();
   __shared__ float fk[65][128];
   __shared__ float vv[65][32];
   const int r = blockIdx.x / n_rec, lr = blockIdx.x % n_rec, h = blockIdx.y, cc = blockIdx.z;

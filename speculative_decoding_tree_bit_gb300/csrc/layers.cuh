@@ -55,6 +55,7 @@ struct AttnArgs {
   int32_t* tickets;        // [R][Hkv][row chunks][2]: zero between calls (each call resets its own)
   int32_t* status;         // a bounded wait that gave up records SD_ERR_TIMEOUT
   uint16_t* out;           // [rows][Hq*hd]
+  uint64_t* trace;         // optional [4][grid] device-clock stamps: start, keys done, group ready, end
 };
 int attn_rows_per_group(int hq, int hkv, int max_m);
 cudaError_t launch_attention(const AttnArgs& a, int rows_total, cudaStream_t s, bool pdl);

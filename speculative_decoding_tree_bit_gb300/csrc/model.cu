@@ -54,7 +54,8 @@ struct sd_model {
   bool use_chain = false;
   unsigned long long* chain_bar;  // grid-barrier words of the chain kernel (counter, base)
   // optional per-kernel timing
-  bool timing = false;
+  bool timing = false;   // events around every kernel group (+ device-clock traces)
+  bool tracing = false;  // device-clock traces only: launches as in untimed steps (no graph)
   std::vector<cudaEvent_t> events;  // 2 per entry
   std::vector<int32_t> t_kind;
   std::vector<double> t_bytes;
@@ -74,12 +75,13 @@ namespace sdv {
 
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Prefix splits per (request, kv head, row chunk): about one CTA per SM, so
-// that each split's key range (and its tensor-core latency chain) is short.
+// Prefix splits per (request, kv head, row chunk): about two CTAs per SM
+// (the tensor-core latency chains of one warp bound the kernel, so more
+// warps per SM and shorter key ranges per split pay for the larger merge).
 static int attn_splits(int R, int hkv, int chunks) {
   const int ctas = R * hkv * chunks;
-  const int s = (num_sms() + ctas - 1) / ctas - 1;
-  return std::max(1, std::min(32, s));
+  const int s = (2 * num_sms() + ctas - 1) / ctas - 1;
+  return std::max(1, std::min(64, s));
 }
 
 static int get_map(std::map<int, XMap>& cache, const uint16_t* buf, int rows_total, int64_t K, int M, XMap** out) {
@@ -199,7 +201,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
         uint64_t* trace = nullptr;
         const int G = chain_grid(rows);
         const size_t rows_tr = 1 + 3 * n;
-        if (m->timing && m->trace && trace_off + rows_tr * (size_t)G <= m->trace_cap) {
+        if ((m->timing || m->tracing) && m->trace && trace_off + rows_tr * (size_t)G <= m->trace_cap) {
           trace = m->trace + trace_off;
           sd_model::ChainRec cr;
           cr.entry = m->t_kind.size() - 1;
@@ -223,7 +225,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
           // timed steps record the launch's per-CTA stamps as a one-phase trace
           uint64_t* trace = nullptr;
           const int G = gemm_launch_grid(*op.d.W, rows, op.d.epi.epi);
-          if (m->timing && m->trace && rows <= 128 && trace_off + 4 * (size_t)G <= m->trace_cap) {
+          if ((m->timing || m->tracing) && m->trace && rows <= 128 && trace_off + 4 * (size_t)G <= m->trace_cap) {
             trace = m->trace + trace_off;
             sd_model::ChainRec cr;
             cr.entry = m->t_kind.size() - 1;
@@ -325,6 +327,22 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
       aa.status = m->status;
       aa.out = m->attn;
       if ((rc = tbegin(SD_K_ATTN, 0.0))) return rc;
+      {
+        // traced steps record the attention's per-CTA stamps as a one-phase trace
+        const int G = (splits + 1) * m->Hkv * chunks * io.R;
+        if ((m->timing || m->tracing) && m->trace && trace_off + 4 * (size_t)G <= m->trace_cap) {
+          aa.trace = m->trace + trace_off;
+          sd_model::ChainRec cr;
+          cr.entry = m->t_kind.size() - 1;
+          cr.off = trace_off;
+          cr.n = 1;
+          cr.G = G;
+          cr.kinds.push_back(SD_K_ATTN);
+          cr.bytes.push_back(0.0);
+          m->t_chain.push_back(cr);
+          trace_off += 4 * (size_t)G;
+        }
+      }
       const cudaError_t e = launch_attention(aa, rows, s, pdl);
       if (e != cudaSuccess) return cuda_fail(e, "attention");
       if ((rc = tend())) return rc;
@@ -415,7 +433,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
 // every pointer and size the kernels see, so a replay is the same launch
 // sequence; values behind the pointers are read at run time.
 static int launch_step(sd_model* m, const StepIO& io, cudaStream_t s, std::vector<uintptr_t> key) {
-  if (!m->use_graphs || m->timing || s == nullptr) return run_step(m, io, s);
+  if (!m->use_graphs || m->timing || m->tracing || s == nullptr) return run_step(m, io, s);
   key.push_back((uintptr_t)m->use_chain);
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   SD_CK(cudaStreamIsCapturing(s, &cs));
@@ -779,13 +797,14 @@ extern "C" int sd_model_set_timing(sd_model* m, int32_t enable) {
     set_error("sd_model_set_timing: null model");
     return SD_ERR_INVALID_ARG;
   }
-  m->timing = enable != 0;
-  if (m->timing && !m->trace) {
-    // stamps of every chain or GEMM launch of one step: at most (layers + 2)
-    // chains of 1 + 3 x 6 rows, or 4 GEMMs per layer + lm_head of 4 rows, x
-    // the largest grid (zero-filled: a CTA without work in a phase leaves
+  m->timing = enable == 1;
+  m->tracing = enable == 2;
+  if ((m->timing || m->tracing) && !m->trace) {
+    // stamps of every traced launch of one step: at most (layers + 2) chains
+    // of 1 + 3 x 6 rows, or per layer 4 GEMMs and the attention of 4 rows,
+    // x the largest grid (zero-filled: a CTA without work in a phase leaves
     // two of its stamps unwritten)
-    const size_t cap = (size_t)(m->cfg.n_layers + 2) * (1 + 3 * kChainMaxPhases) * gemm_grid(1);
+    const size_t cap = (size_t)(m->cfg.n_layers + 2) * (1 + 3 * kChainMaxPhases) * gemm_grid(1) * 2;
     SD_CK(cudaMalloc(&m->trace, cap * sizeof(uint64_t)));
     SD_CK(cudaMemset(m->trace, 0, cap * sizeof(uint64_t)));
     m->trace_cap = cap;

@@ -200,8 +200,9 @@ class Model:
         """Chained GEMM/RMSNorm launches (default on) or one kernel per op."""
         check(lib().sd_model_set_chain(self.handle, 1 if on else 0))
 
-    def set_timing(self, on: bool):
-        check(lib().sd_model_set_timing(self.handle, 1 if on else 0))
+    def set_timing(self, on):
+        """True / 1: event timing + traces; 2: device-clock traces only."""
+        check(lib().sd_model_set_timing(self.handle, int(on)))
 
     def timeline(self, max_entries: int = 4096):
         """[(kind name, ms, algorithmic bytes)] of the last timed call; the

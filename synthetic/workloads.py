@@ -78,6 +78,9 @@ SHAPES = {
     # small models for parity at sizes the oracle finishes in seconds; still
     # several GEMM tiles with ragged row blocks (V = 4000 = 31.25 * 128).
     "mini": _dense("mini", 2, 512, 1024, 4, 2, 4000, gamma_sigma=0.1),
+    # the 8B dimensions with 2 layers: profiling captures of one layer's
+    # kernels with a few GB on the device
+    "8b_2l": _dense("8b_2l", 2, 4096, 12288, 32, 8, 151936),
     "mini_hybrid": _hybrid("mini_hybrid", 4, 512, 1024, 4, 2, 4000, gamma_sigma=0.1),
 }
 
@@ -277,6 +280,7 @@ def decoder(shape_name: str, seed: int = 0, M: int = 16, max_depth: int = 8, ctx
 WORKLOADS = {
     "tiny": dict(kind="tiny"),
     "8b_m16": dict(kind="decoder", shape="8b", M=16, max_depth=8, ctx=2048, p=0.7),
+    "8b_2l_m16": dict(kind="decoder", shape="8b_2l", M=16, max_depth=8, ctx=2048, p=0.7),
     "27b_m8": dict(kind="decoder", shape="27b", M=8, max_depth=10, ctx=4096, p=0.7),
     "27b_m16": dict(kind="decoder", shape="27b", M=16, max_depth=10, ctx=4096, p=0.7),
     "27b_m32": dict(kind="decoder", shape="27b", M=32, max_depth=10, ctx=4096, p=0.7),
