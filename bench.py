@@ -30,6 +30,9 @@ sys.path.insert(0, ROOT)
 
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NOMINAL_BW_GBS = 8000.0       # the metric's "fraction of 8 TB/s"
+# DRAM bytes (read + write) of one k_w12_gemm gate/up launch, 8B shape,
+# M = 16, from an ncu --set full capture of that launch (the probe command)
+GATE_UP_TRAFFIC_8B = 151.687680e6 + 4.050944e6
 
 
 def peaks():
@@ -414,7 +417,16 @@ def gpu_arm(args, rank, world, dist):
     gemm = [(k, t, b) for k, t, b in tl if k.startswith("gemm")]  # chain launches and lone GEMMs (not their traces)
     g_ms = sum(t for _, t, _ in gemm)
     g_bytes = sum(b for _, _, b in gemm)
-    achieved = g_bytes / (g_ms * 1e-3) / 1e9 if g_ms > 0 else None
+    all_gemm_gbs = g_bytes / (g_ms * 1e-3) / 1e9 if g_ms > 0 else None
+    # the dominant kernel: k_w12_gemm on the gate/up shape (the largest GEMM of
+    # a layer), algorithmic bytes per launch / its mean event-timed launch
+    gu = [(t, b) for k, t, b in tl if k == "gemm_gate_up"]
+    gu_ms = sum(t for t, _ in gu) / len(gu) if gu else None
+    gu_bytes = gu[0][1] if gu else None
+    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9 if gu else all_gemm_gbs
+    # DRAM read + write of one gate/up launch from the ncu capture of this
+    # kernel, for the 8B shape only
+    traffic = GATE_UP_TRAFFIC_8B if (gu and shape.name == "8b" and M == 16) else None
     peak = pk["hbm_gbs"]
     step_bytes = model.packed_bytes + kv_bytes_per_step(shape, ctx, M)
     # the pages' per-kernel lower bound: max(FLOPs at 60% of dense peak, bytes at 90% of bandwidth)
@@ -452,10 +464,12 @@ def gpu_arm(args, rank, world, dist):
         "step_lower_bound_us": bound_s * 1e6,
         "frac_of_step_lower_bound": bound_s / (ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak if achieved else None, "traffic": None,
-                     "kernel": ("k_w12_gemm (all GEMM launches of a step, event-timed)" if not args.chain else
-                                "k_w12_chain + k_w12_gemm (all GEMM chain / GEMM launches of a step, event-timed; "
-                                "a chain's time includes its two RMSNorm phases)"),
+                     "frac": achieved / peak if achieved else None, "traffic": traffic,
+                     "kernel": ("k_w12_gemm, gate/up launches (algorithmic bytes per launch / mean event-timed "
+                                "launch; traffic from the committed ncu capture)" if gu else
+                                "k_w12_chain + k_w12_gemm (all GEMM chain / GEMM launches of a step, event-timed)"),
+                     "algorithmic_bytes_per_launch": gu_bytes, "launch_ms": gu_ms,
+                     "all_gemm_launches_gbs": all_gemm_gbs,
                      "peak_source": pk_src},
         "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in by_kind.items()},
         "e2e": {"value": world * M / (ms_e2e * 1e-3), "unit": "tree tokens/s", "h2d_bytes_per_step": h2d,
