@@ -303,32 +303,68 @@ def gpu_arm(args, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(local)
     spec = wl.make(args.workload, args.seed)
-    shape, M, ctx = spec.shape, spec.M, spec.ctx[0]
-    if spec.R != 1:
-        raise SystemExit("this bench drives single-request workloads")
+    shape, R = spec.shape, spec.R
+    ctx = max(spec.ctx)
     t0 = time.time()
     W = wl.SyntheticWeights(shape, args.seed)
-    model = Mdl.Model(shape, W, max_rows=M, max_requests=1, max_positions=ctx + M + 64)
-    model.set_chain(args.chain)
-    kv = Mdl.KVCache(shape, ctx + M + 16).fill(args.seed, ctx)
-    log(f"[rank {rank}] model built in {time.time() - t0:.1f}s, packed {model.packed_bytes / 1e9:.2f} GB")
-    td = spec.drafts[0]
-
-    def am_fn(tok, par):
-        _, am = model.forward(tok, par, kv, logits=False)
-        return am.cpu().numpy()
-
-    tokens = wl.copy_rule_tokens(td, am_fn)
     dev = torch.device("cuda", local)
-    tok_d = torch.from_numpy(tokens).to(dev)
-    par_d = torch.from_numpy(np.asarray(td.parents, np.int32)).to(dev)
-    out = model.outputs(M)
-    ctx0 = kv.ctx_len.clone()
     stream = torch.cuda.Stream(device=dev)
+    if R == 1:
+        M = spec.M
+        model = Mdl.Model(shape, W, max_rows=M, max_requests=1, max_positions=ctx + M + 64)
+        model.set_chain(args.chain)
+        kv = Mdl.KVCache(shape, ctx + M + 16).fill(args.seed, ctx)
+        log(f"[rank {rank}] model built in {time.time() - t0:.1f}s, packed {model.packed_bytes / 1e9:.2f} GB")
+        td = spec.drafts[0]
 
-    def step():
-        kv.ctx_len.copy_(ctx0, non_blocking=True)
-        model.verify(tok_d, par_d, kv, out=out, stream=stream)
+        def am_fn(tok, par):
+            _, am = model.forward(tok, par, kv, logits=False)
+            return am.cpu().numpy()
+
+        tokens = wl.copy_rule_tokens(td, am_fn)
+        parents = np.asarray(td.parents, np.int32)
+        tok_d = torch.from_numpy(tokens).to(dev)
+        par_d = torch.from_numpy(parents).to(dev)
+        out = model.outputs(M)
+        ctx0 = kv.ctx_len.clone()
+
+        def step():
+            kv.ctx_len.copy_(ctx0, non_blocking=True)
+            model.verify(tok_d, par_d, kv, out=out, stream=stream)
+    else:
+        # R requests over a paged cache, one batched verify per step
+        Mr = spec.M
+        M = R * Mr
+        model = Mdl.Model(shape, W, max_rows=M, max_requests=R, max_positions=ctx + Mr + 64)
+        table, n_pages = wl.page_tables(args.seed, spec.ctx, Mr, spec.page_size)
+        kv = Mdl.PagedKVCache(shape, table, n_pages, spec.page_size).fill(args.seed, spec.ctx)
+        log(f"[rank {rank}] model built in {time.time() - t0:.1f}s, packed {model.packed_bytes / 1e9:.2f} GB")
+        cu = np.cumsum([0] + [Mr] * R).astype(np.int32)
+        parents = np.concatenate([np.asarray(d.parents, np.int32) for d in spec.drafts])
+        par_d = torch.from_numpy(parents).to(dev)
+        ctx0 = kv.ctx_len.clone()
+        # copy-rule tokens by depth waves over the whole batch (a node's argmax
+        # depends on its root path only, final once its ancestors are)
+        tokens = np.concatenate([np.where(np.arange(Mr) == 0, d.root_token, d.rand_tok).astype(np.int32)
+                                 for d in spec.drafts])
+        dep = np.concatenate([wl.depths(np.asarray(d.parents)) for d in spec.drafts])
+        cop = np.concatenate([np.asarray(d.copy) for d in spec.drafts])
+        rnd = np.concatenate([np.asarray(d.rand_tok) for d in spec.drafts])
+        for wave in range(1, int(dep.max()) + 1):
+            kv.ctx_len.copy_(ctx0)
+            o = model.verify_batch(tokens, parents, cu, kv)
+            am = o["argmax"].cpu().numpy()
+            for r in range(R):
+                for i in range(1, Mr):
+                    g = cu[r] + i
+                    if dep[g] == wave:
+                        tokens[g] = am[cu[r] + parents[g]] if cop[g] else rnd[g]
+        tok_d = torch.from_numpy(tokens).to(dev)
+        out = model.outputs(M, R=R)
+
+        def step():
+            kv.ctx_len.copy_(ctx0, non_blocking=True)
+            model.verify_batch(tok_d, par_d, cu, kv, out=out, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -337,7 +373,7 @@ def gpu_arm(args, rank, world, dist):
     st = model.status()
     if st != 0:
         raise SystemExit(f"device status {st} after warm-up")
-    acc_len = int(out["accepted_len"][0])
+    acc_len = float(out["accepted_len"].float().mean())
     launches = model.last_launches()
 
     def barrier():
@@ -366,7 +402,7 @@ def gpu_arm(args, rank, world, dist):
 
     # ---- end to end through the public API with host buffers
     tok_h = torch.from_numpy(tokens).pin_memory()
-    par_h = torch.from_numpy(np.asarray(td.parents, np.int32)).pin_memory()
+    par_h = torch.from_numpy(parents).pin_memory()
     res_h = {k: torch.empty_like(out[k], device="cpu").pin_memory() for k in ("accepted_len", "accepted_tokens",
                                                                                  "bonus")}
 
@@ -398,14 +434,14 @@ def gpu_arm(args, rank, world, dist):
     torch.cuda.synchronize()
     tl = model.timeline()
     chain_phases = None
-    if args.timeline:
+    if args.timeline and M <= 128:
         # the middle layer's launches (a chain, or its four GEMMs after its attention)
         per_layer = 1 if args.chain else 4
         first = 2 + (shape.n_layers // 2) * 5 if not args.chain else shape.n_layers // 2
         chain_phases = [chain_phase_summary(model, first + i) for i in range(per_layer)]
     model.set_timing(False)
     overlap = None
-    if args.timeline and not args.chain:
+    if args.timeline and not args.chain and M <= 128 and shape.n_rec == 0:
         overlap = overlapped_layer_trace(model, stream, step, shape.n_layers // 2)
 
     if dist is not None:
@@ -428,12 +464,13 @@ def gpu_arm(args, rank, world, dist):
     # kernel, for the 8B shape only
     traffic = GATE_UP_TRAFFIC_8B if (gu and shape.name == "8b" and M == 16) else None
     peak = pk["hbm_gbs"]
-    step_bytes = model.packed_bytes + kv_bytes_per_step(shape, ctx, M)
+    ctx_sum = int(sum(spec.ctx))  # every request's prefix
+    step_bytes = model.packed_bytes + kv_bytes_per_step(shape, ctx_sum, M)
     # the pages' per-kernel lower bound: max(FLOPs at 60% of dense peak, bytes at 90% of bandwidth)
     flops = 2.0 * M * (shape.n_weights())
     P = pk["bf16_tflops"] * 1e12
     bound_s = sum(max(2.0 * M * (b / 1.5) / (0.6 * P), b / (0.9 * NOMINAL_BW_GBS * 1e9)) for _, _, b in gemm)
-    bound_s += kv_bytes_per_step(shape, ctx, M) / (0.9 * NOMINAL_BW_GBS * 1e9)
+    bound_s += kv_bytes_per_step(shape, ctx_sum, M) / (0.9 * NOMINAL_BW_GBS * 1e9)
     by_kind = {}
     for k, t, b in tl:
         a = by_kind.setdefault(k, [0, 0.0, 0.0])
@@ -454,7 +491,7 @@ def gpu_arm(args, rank, world, dist):
         "verify_step_us": ms * 1e3, "host_submit_us_per_step": t_host * 1e6, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "model": shape.name, "layers": shape.n_layers, "M": M,
-                   "gemm_chain": bool(args.chain),
+                   "requests": R, "gemm_chain": bool(args.chain),
                    "max_depth": spec.max_depth, "ctx": ctx, "p_copy": spec.p, "accepted_len": acc_len,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (packed weights %.1f GB)" % (model.packed_bytes / 1e9)},
@@ -477,8 +514,8 @@ def gpu_arm(args, rank, world, dist):
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        per_layer, t_lm, thr = oracle_sample(shape, args.seed, M, ctx, td.parents, tokens, n_layers=1)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and R == 1:
+        per_layer, t_lm, thr = oracle_sample(shape, args.seed, M, ctx, parents, tokens, n_layers=1)
         est = per_layer * shape.n_layers + t_lm
         res["cpu_baseline"] = {"value": M / est, "unit": "tree tokens/s", "cores": thr, "kind": "oracle",
                                "sample": f"oracle forward of layer 0 + lm_head/argmax (M={M}, ctx={ctx}); "
