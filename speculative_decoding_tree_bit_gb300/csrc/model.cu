@@ -77,11 +77,14 @@ static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Prefix splits per (request, kv head, row chunk): about two CTAs per SM
 // (the tensor-core latency chains of one warp bound the kernel, so more
-// warps per SM and shorter key ranges per split pay for the larger merge).
-static int attn_splits(int R, int hkv, int chunks) {
+// warps per SM and shorter key ranges per split pay for the larger merge),
+// and at least one split per 512 keys of the longest possible context (many
+// requests: otherwise each CTA walks a whole context).
+static int attn_splits(int R, int hkv, int chunks, int max_keys) {
   const int ctas = R * hkv * chunks;
-  const int s = (2 * num_sms() + ctas - 1) / ctas - 1;
-  return std::max(1, std::min(64, s));
+  const int by_sms = (2 * num_sms() + ctas - 1) / ctas - 1;
+  const int by_keys = (max_keys + 511) / 512;
+  return std::max(1, std::min(64, std::max(by_sms, by_keys)));
 }
 
 static int get_map(std::map<int, XMap>& cache, const uint16_t* buf, int rows_total, int64_t K, int M, XMap** out) {
@@ -273,7 +276,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
 
   const int rpg = attn_rows_per_group(m->Hq, m->Hkv, m->max_m);
   const int chunks = (rpg + 63) / 64;
-  int splits = attn_splits(io.R, m->Hkv, chunks);
+  int splits = attn_splits(io.R, m->Hkv, chunks, m->cfg.max_positions);
   while (splits > 1 && (size_t)io.R * (splits + 1) > m->attn_units) splits--;
   const int64_t layer_elems = (int64_t)io.cv.n_pages * m->Hkv * io.cv.page_size * m->hd;
 
@@ -589,7 +592,7 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
   const int rpg = attn_rows_per_group(m->Hq, m->Hkv, m->max_m);
   const int chunks = (rpg + 63) / 64;
   size_t units = 0;
-  for (int r = 1; r <= R; r++) units = std::max(units, (size_t)r * (attn_splits(r, m->Hkv, chunks) + 1));
+  for (int r = 1; r <= R; r++) units = std::max(units, (size_t)r * (attn_splits(r, m->Hkv, chunks, c.max_positions) + 1));
   m->attn_units = units;
   struct Item {
     void** p;
