@@ -163,6 +163,19 @@ int sd_w12_linear(const w12_tensor* W, const uint16_t* x, int32_t M, uint16_t* y
  * results; serialise them. */
 int sd_w12_linear_static(const w12_tensor* W, const uint16_t* x, int32_t M, uint16_t* y, void* stream);
 
+/* Rows per launch from which the fused W12 GEMMs (sd_w12_linear and every
+ * GEMM of the verify step) run on the tcgen05 tensor-core kernel: weights
+ * decoded into a shared-memory operand tile, escapes written over their
+ * slots, fp32 accumulators in tensor memory, up to 256 rows in one launch.
+ * Fewer rows run on the warp-level MMA kernel, which streams weights with
+ * less on-chip traffic while a launch is bandwidth-bound ("SpecPilot ...",
+ * batched results: the batched step crosses from the weight-bandwidth bound
+ * to the tensor-core bound).  Process-wide; applies to calls issued
+ * afterwards (a model re-captures its step graphs).  rows <= 0 restores the
+ * default, 129 (only launches of more than 128 rows).  Returns the value now
+ * in force.  Not thread-safe against concurrent GEMM calls. */
+int32_t sd_gemm_set_tc_min_rows(int32_t rows);
+
 /* ------------------------------------------------------ tree helpers -- */
 /* [TREE] Validate one draft tree (parents[0] == -1, 0 <= parents[i] < i,
  * M <= 64) and derive per node the ancestor bitmask anc[i] = anc[parent[i]]

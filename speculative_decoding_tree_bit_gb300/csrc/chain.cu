@@ -396,7 +396,7 @@ static int chain_blocks_per_sm() {
 }
 
 int chain_grid(int M) {
-  if (M < 1 || M > 128) return 0;
+  if (M < 1 || M > 128 || gemm_use_tc(M)) return 0;
   int nb = 0, want = 0;
   switch (pad_rows(M) / 8) {
     case 1: nb = chain_blocks_per_sm<1>(); want = chain_ctas_per_sm<1>(); break;

@@ -168,9 +168,22 @@ int pad_rows(int M) { return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 
 
 static int nt_of(int M) { return M > 128 ? 16 : pad_rows(M) / 8; }
 
-int gemm_grid(int M) { return (nt_of(M) <= 4 ? 2 : 1) * num_sms(); }
+// Default crossover of the two kernels (rows per launch).
+constexpr int kTcMinRowsDefault = 129;
+static int g_tc_min_rows = kTcMinRowsDefault;
+
+int gemm_tc_min_rows() { return g_tc_min_rows; }
+void gemm_set_tc_min_rows(int rows) { g_tc_min_rows = rows > 0 ? rows : kTcMinRowsDefault; }
+
+int gemm_grid(int M) { return gemm_use_tc(M) ? num_sms() : (nt_of(M) <= 4 ? 2 : 1) * num_sms(); }
 
 int gemm_launch_grid(const w12_tensor& W, int M, int epi) {
+  if (gemm_use_tc(M)) {
+    // few row blocks: a whole number of CTAs per block (no CTA's range
+    // straddles two blocks, every block has the same contributors)
+    const int nb = gemm_counters(W.N), sms = num_sms();
+    return (epi != EPI_LOGITS && nb * 2 <= sms) ? nb * (sms / nb) : sms;
+  }
   int grid = gemm_grid(M);
   // few row blocks (q/k/v, O, down): a whole number of CTAs per row block,
   // so that no CTA's range straddles two row blocks (a straddling CTA
@@ -181,7 +194,10 @@ int gemm_launch_grid(const w12_tensor& W, int M, int epi) {
   return grid;
 }
 
-size_t gemm_partial_floats(int M) { return (size_t)gemm_grid(M) * 2 * kRB * nt_of(M) * 128; }
+size_t gemm_partial_floats(int M) {
+  const size_t mma = (size_t)(nt_of(M) <= 4 ? 2 : 1) * num_sms() * 2 * kRB * nt_of(M) * 128;
+  return std::max(mma, gemm_tc_partial_floats(M));
+}
 
 int gemm_counters(int64_t N) { return (int)((N / 16 + kRB - 1) / kRB); }
 
@@ -204,7 +220,7 @@ int make_x_map(XMap* xm, const uint16_t* x, int rows_total, int64_t K, int box_r
     set_error("cuTensorMapEncodeTiled unavailable");
     return SD_ERR_CUDA;
   }
-  if ((reinterpret_cast<uintptr_t>(x) & 15) || K % 64 || box_rows < 8 || box_rows > 128 || rows_total < 1) {
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || K % 64 || box_rows < 8 || box_rows > 256 || rows_total < 1) {
     set_error("make_x_map: x must be 16-byte aligned, K % 64 == 0");
     return SD_ERR_INVALID_ARG;
   }
@@ -304,6 +320,7 @@ int make_gemm_params(GemmParams* out, const w12_tensor& W, const uint16_t* x, in
 
 int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
                 const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid, uint64_t* trace) {
+  if (gemm_use_tc(M)) return gemm_tc_launch(W, x, xm.rows_total, M, epi, ws, status, s, pdl);
   if (grid <= 0) grid = gemm_launch_grid(W, M, epi.epi);
   GemmParams p;
   const int prc = make_gemm_params(&p, W, x, M, epi, ws, status);
@@ -345,9 +362,14 @@ int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, c
 
 using namespace sdv;
 
+extern "C" int32_t sd_gemm_set_tc_min_rows(int32_t rows) {
+  gemm_set_tc_min_rows(rows);
+  return gemm_tc_min_rows();
+}
+
 extern "C" size_t sd_w12_linear_workspace(int64_t N, int64_t K, int32_t M) {
   (void)K;
-  const size_t pf = gemm_partial_floats(std::max(1, std::min<int>(M, 128)));
+  const size_t pf = gemm_partial_floats(std::max(1, std::min<int>(M, 256)));
   const size_t pbytes = (pf * sizeof(float) + 255) & ~size_t(255);
   return pbytes + (size_t)gemm_counters(N) * sizeof(int32_t) + 256;
 }
@@ -369,7 +391,7 @@ extern "C" int sd_w12_linear(const w12_tensor* W, const uint16_t* x, int32_t M, 
   cudaStream_t s = (cudaStream_t)stream;
   GemmWorkspace ws;
   ws.partial = reinterpret_cast<float*>(workspace);
-  ws.partial_floats = gemm_partial_floats(std::min<int>(M, 128));
+  ws.partial_floats = gemm_partial_floats(M);
   const size_t pbytes = (ws.partial_floats * sizeof(float) + 255) & ~size_t(255);
   ws.counters = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(workspace) + pbytes);
   ws.counters_len = gemm_counters(W->N);

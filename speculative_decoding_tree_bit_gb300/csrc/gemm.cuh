@@ -53,9 +53,20 @@ struct GemmWorkspace {
   int counters_len = 0;
 };
 
+// Launches of at least gemm_tc_min_rows() rows run on the tcgen05 kernel
+// (gemm_tc.cu, one CTA per SM, up to 256 rows in one launch); fewer rows run
+// on the warp-level MMA kernel (gemm.cu).
+int gemm_tc_min_rows();
+void gemm_set_tc_min_rows(int rows);  // <= 0: the default
+inline bool gemm_use_tc(int M) { return M >= gemm_tc_min_rows(); }
+int gemm_tc_rows(int M);               // MMA N side for M rows (multiple of 16, >= 32)
+size_t gemm_tc_partial_floats(int M);  // workspace floats of the tcgen05 kernel
+int gemm_tc_launch(const w12_tensor& W, const uint16_t* x, int rows_total, int M, const GemmEpilogue& epi,
+                   const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl);
+
 int gemm_grid(int M);               // CTAs per launch for M rows (persistent: 1 or 2 per SM)
 int gemm_launch_grid(const w12_tensor& W, int M, int epi);  // the grid gemm_launch uses by default
-size_t gemm_partial_floats(int M);  // workspace floats for M rows
+size_t gemm_partial_floats(int M);  // workspace floats for M rows (either kernel)
 int gemm_counters(int64_t N);       // counters for N rows
 int pad_rows(int M);                // rows of one launch's TMA box: 8, 16, 32, 64 or 128
 
@@ -67,11 +78,13 @@ struct XMap {
 };
 int make_x_map(XMap* xm, const uint16_t* x, int rows_total, int64_t K, int box_rows);
 
-// y = epilogue(x W^T) for rows [0, M); M > 128 runs in launches of 128 rows.
-// grid: CTAs per launch, 0 = gemm_grid(M); the partial-sum workspace must
-// hold grid * 2 * 8 * (padded rows / 8) * 128 floats.  trace (optional, M <=
-// 128): [4][grid] device-clock stamps per CTA - start, first stage ready,
-// last stage consumed, finished.
+// y = epilogue(x W^T) for rows [0, M).  With gemm_use_tc(M) one tcgen05
+// launch covers all rows (grid and trace are ignored, the x map is rebuilt
+// with a box of gemm_tc_rows(M) rows); otherwise M > 128 runs in launches of
+// 128 rows.  grid: CTAs per launch, 0 = gemm_grid(M); the partial-sum
+// workspace must hold grid * 2 * 8 * (padded rows / 8) * 128 floats.  trace
+// (optional, M <= 128): [4][grid] device-clock stamps per CTA - start, first
+// stage ready, last stage consumed, finished.
 int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
                 const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid = 0,
                 uint64_t* trace = nullptr);

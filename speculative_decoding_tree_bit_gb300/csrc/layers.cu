@@ -489,7 +489,7 @@ cudaError_t launch_attention(const AttnArgs& a, int rows_total, cudaStream_t s, 
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_attn, 128, kAttnSmem) != cudaSuccess) per_sm = 0;
   }
   const int rpg = attn_rows_per_group(a.hq, a.hkv, a.max_m);
-  const int chunks = (rpg + 63) / 64;
+  const int chunks = (attn_rows_per_group(a.hq, a.hkv, a.chunk_m > 0 ? a.chunk_m : a.max_m) + 63) / 64;
   const int64_t grid = (int64_t)(a.splits + 1) * a.hkv * chunks * a.R;
   const AttnKernelArgs ka{a, rpg, chunks, grid <= (int64_t)per_sm * num_sms() ? 1 : 0};
   return launch(k_attn, dim3(a.splits + 1, a.hkv * chunks, a.R), dim3(128), kAttnSmem, s, pdl, ka);

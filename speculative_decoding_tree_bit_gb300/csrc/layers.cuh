@@ -50,6 +50,7 @@ struct AttnArgs {
   const int32_t* row_req;  // [rows]
   const int32_t* req_ok;   // [R]: requests whose tree failed validation read no keys
   int R, max_m, splits;    // splits = prefix splits (the tree segment is one more)
+  int chunk_m;             // rows of the call's largest request (<= max_m; 0: max_m): sets the grid's row chunks
   float* part_o;           // [R][Hkv][splits+1][rows_per_group][hd]
   float* part_ml;          // [R][Hkv][splits+1][rows_per_group][2]
   int32_t* tickets;        // [R][Hkv][row chunks][2]: zero between calls (each call resets its own)

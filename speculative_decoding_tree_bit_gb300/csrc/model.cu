@@ -228,7 +228,8 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
           // timed steps record the launch's per-CTA stamps as a one-phase trace
           uint64_t* trace = nullptr;
           const int G = gemm_launch_grid(*op.d.W, rows, op.d.epi.epi);
-          if ((m->timing || m->tracing) && m->trace && rows <= 128 && trace_off + 4 * (size_t)G <= m->trace_cap) {
+          if ((m->timing || m->tracing) && m->trace && rows <= 128 && !gemm_use_tc(rows) &&
+              trace_off + 4 * (size_t)G <= m->trace_cap) {
             trace = m->trace + trace_off;
             sd_model::ChainRec cr;
             cr.entry = m->t_kind.size() - 1;
@@ -243,7 +244,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
           if ((rc = gemm_launch(*op.d.W, op.d.x, *op.d.xm, rows, op.d.epi, m->gws, m->status, s, pdl, 0, trace)))
             return rc;
           if ((rc = tend())) return rc;
-          launches += rows > 128 ? 2 : 1;
+          launches += (rows > 128 && !gemm_use_tc(rows)) ? 2 : 1;
         } else {
           if ((rc = tbegin(SD_K_NORM, 0.0))) return rc;
           const cudaError_t e = launch_rmsnorm(op.d.norm.src, op.d.norm.gamma, rows, op.d.norm.H, op.d.norm.eps,
@@ -274,8 +275,12 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   LK(SD_K_NORM, launch_rmsnorm(nullptr, m->layers[0].attn_norm, rows, m->H, m->cfg.rms_eps, m->xn, io.tokens, m->w.embed, m->x,
                     m->req, m->req_ok, s, pdl));
 
-  const int rpg = attn_rows_per_group(m->Hq, m->Hkv, m->max_m);
-  const int chunks = (rpg + 63) / 64;
+  // row chunks of the attention grid: the largest request of this call
+  int max_mr = 1;
+  for (int r = 0; r < io.R && r + 1 < (int)m->cu_host.size(); r++)
+    max_mr = std::max(max_mr, m->cu_host[r + 1] - m->cu_host[r]);
+  max_mr = std::min(max_mr, m->max_m);
+  const int chunks = (attn_rows_per_group(m->Hq, m->Hkv, max_mr) + 63) / 64;
   int splits = attn_splits(io.R, m->Hkv, chunks, m->cfg.max_positions);
   while (splits > 1 && (size_t)io.R * (splits + 1) > m->attn_units) splits--;
   const int64_t layer_elems = (int64_t)io.cv.n_pages * m->Hkv * io.cv.page_size * m->hd;
@@ -323,6 +328,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
       aa.req_ok = m->req_ok;
       aa.R = io.R;
       aa.max_m = m->max_m;
+      aa.chunk_m = max_mr;
       aa.splits = splits;
       aa.part_o = m->attn_o;
       aa.part_ml = m->attn_ml;
@@ -438,6 +444,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
 static int launch_step(sd_model* m, const StepIO& io, cudaStream_t s, std::vector<uintptr_t> key) {
   if (!m->use_graphs || m->timing || m->tracing || s == nullptr) return run_step(m, io, s);
   key.push_back((uintptr_t)m->use_chain);
+  key.push_back((uintptr_t)gemm_tc_min_rows());
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   SD_CK(cudaStreamIsCapturing(s, &cs));
   if (cs != cudaStreamCaptureStatusNone) return run_step(m, io, s);
@@ -592,7 +599,9 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
   const int rpg = attn_rows_per_group(m->Hq, m->Hkv, m->max_m);
   const int chunks = (rpg + 63) / 64;
   size_t units = 0;
-  for (int r = 1; r <= R; r++) units = std::max(units, (size_t)r * (attn_splits(r, m->Hkv, chunks, c.max_positions) + 1));
+  for (int ch = 1; ch <= chunks; ch++)
+    for (int r = 1; r <= R; r++)
+      units = std::max(units, (size_t)r * (attn_splits(r, m->Hkv, ch, c.max_positions) + 1));
   m->attn_units = units;
   struct Item {
     void** p;
@@ -624,8 +633,9 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
       {(void**)&m->attn_o, units * m->Hkv * rpg * 128 * 4},
       {(void**)&m->attn_ml, units * m->Hkv * rpg * 2 * 4},
       {(void**)&m->attn_tickets, (size_t)R * m->Hkv * chunks * 2 * 4},
-      {(void**)&m->amax_val, (size_t)gemm_grid(1) * MR * 4},
-      {(void**)&m->amax_idx, (size_t)gemm_grid(1) * MR * 4},
+      // one argmax partial per CTA of the widest GEMM grid (two per SM)
+      {(void**)&m->amax_val, (size_t)2 * num_sms() * MR * 4},
+      {(void**)&m->amax_idx, (size_t)2 * num_sms() * MR * 4},
       {(void**)&m->gws.partial, gemm_partial_floats(MR) * 4},
       {(void**)&m->gws.counters, (size_t)gemm_counters(max_n) * 4},
       {(void**)&m->chain_bar, 16},

@@ -113,6 +113,12 @@ def linear(p: Packed, x: torch.Tensor, ws: Workspace | None = None, stream=None)
     return y
 
 
+def set_tc_min_rows(rows: int) -> int:
+    """Rows per launch from which the W12 GEMMs run on the tcgen05 kernel
+    (process-wide; <= 0 restores the default).  Returns the value in force."""
+    return int(lib().sd_gemm_set_tc_min_rows(int(rows)))
+
+
 def row_map(kind: int, Hq: int, Hkv: int, inter: int, N: int) -> np.ndarray:
     out = np.empty(N, dtype=np.int32)
     check(lib().sd_model_row_map(kind, Hq, Hkv, 128, inter, out.ctypes.data, N))

@@ -288,7 +288,14 @@ WORKLOADS = {
     "hybrid_m16": dict(kind="decoder", shape="hybrid", M=16, max_depth=8, ctx=2048, p=0.7),
     "batched_r32": dict(kind="decoder", shape="8b", M=8, max_depth=7, R=32, chain_draft=True, p=0.6,
                         ctx_range=(1024, 4096), page_size=16),
+    # two-layer profiling case of the batched step
+    "8b_2l_r32": dict(kind="decoder", shape="8b_2l", M=8, max_depth=7, R=32, chain_draft=True, p=0.6,
+                      ctx_range=(1024, 4096), page_size=16),
 }
+# the batched step at fewer requests (M = 8R rows): the sweep over the
+# bandwidth-bound to tensor-bound crossover
+for _r in (1, 2, 4, 8, 16):
+    WORKLOADS[f"batched_r{_r}"] = dict(WORKLOADS["batched_r32"], R=_r)
 
 
 def make(name: str, seed: int = 0, **over):

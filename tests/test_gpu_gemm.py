@@ -88,3 +88,60 @@ def test_repeat_calls_are_deterministic_with_dirty_workspace(M):
     ws.buf.fill_(0xFF)
     b = M.linear(p, x, ws)
     assert torch.equal(a, b)
+
+
+# ------------------------------------------- tcgen05 kernel at any row count --
+
+@pytest.fixture()
+def tc_all(M):
+    """Every launch on the tcgen05 kernel (default: only launches of more
+    than 128 rows), restored afterwards."""
+    M.set_tc_min_rows(1)
+    yield M
+    M.set_tc_min_rows(0)
+
+
+@pytest.mark.parametrize("Mrows", [1, 5, 16, 17, 32, 48, 64, 100, 128])
+def test_tc_tiny_shape_row_counts(tc_all, Mrows):
+    t = wl.tiny()
+    _check(tc_all, t.W1, _x(Mrows, 1024))
+
+
+@pytest.mark.parametrize("N,K,Mrows", [(16, 64, 8), (48, 192, 16), (4000, 512, 40), (144, 1088, 3), (4000, 512, 64)])
+def test_tc_ragged_shapes(tc_all, N, K, Mrows):
+    W = synthetic.normal_bf16(synthetic.key(2, N * 7 + K), N * K, 0.02).reshape(N, K)
+    _check(tc_all, W, _x(Mrows, K, 1))
+
+
+def test_tc_escapes_and_general_table(tc_all):
+    t = wl.tiny()
+    p = _check(tc_all, t.Wlm, _x(24, 1024, 2))
+    assert p.meta.affine == 1 and p.n_escapes >= 4194
+    rng = np.random.default_rng(5)
+    exps = np.array([110, 112, 114, 116, 118, 120, 121, 122, 123, 124, 100, 102, 104, 106, 108, 90], np.uint32)
+    e = exps[rng.integers(0, exps.size, size=256 * 512)]
+    W = ((rng.integers(0, 2, size=e.size).astype(np.uint32) << 15) | (e << 7)
+         | rng.integers(0, 128, size=e.size).astype(np.uint32)).astype(np.uint16).reshape(256, 512)
+    p = _check(tc_all, W, _x(40, 512, 3))
+    assert p.meta.affine == 0 and p.n_escapes > 0
+
+
+@pytest.mark.parametrize("name,Mrows", [("w_down", 256), ("lm", 256), ("wq", 64)])
+def test_tc_full_size_8b(tc_all, name, Mrows):
+    sh = wl.SHAPES["8b"]
+    w = wl.SyntheticWeights(sh, 0)
+    W = w.lm_head() if name == "lm" else w.layer(0, name)
+    rows = np.sort(np.random.default_rng(0).choice(W.shape[0], 1024, replace=False))
+    _check(tc_all, W, _x(Mrows, W.shape[1], 4), rows=rows)
+
+
+def test_tc_repeat_calls_are_deterministic(tc_all):
+    t = wl.tiny()
+    p = tc_all.pack(tc_all.to_device_u16(t.W1))
+    x = tc_all.to_device_u16(_x(200, 1024, 9))
+    ws = tc_all.Workspace(int(tc_all.lib().sd_w12_linear_workspace(1024, 1024, 200)))
+    ws.buf.fill_(0x7F)
+    a = tc_all.linear(p, x, ws)
+    ws.buf.fill_(0xFF)
+    b = tc_all.linear(p, x, ws)
+    assert torch.equal(a, b)

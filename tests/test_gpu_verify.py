@@ -100,6 +100,18 @@ def test_tree_verify_matches_oracle(M, dec):
     _verify_case(M, shape, W, model, wl.draft(11, 0, 16, 8, 0.8, shape.V), 37)
 
 
+def test_tree_verify_on_tensor_core_gemms(M, dec):
+    """Every GEMM of the step (fused QKV/RoPE/KV write, residual, SiLU-mul,
+    logits + argmax epilogues) on the tcgen05 kernel."""
+    shape, W, model = dec
+    M.set_tc_min_rows(1)
+    try:
+        _verify_case(M, shape, W, model, wl.draft(11, 0, 16, 8, 0.8, shape.V), 37)
+        _verify_case(M, shape, W, model, wl.draft(12, 0, 64, 10, 0.7, shape.V), 130)
+    finally:
+        M.set_tc_min_rows(0)
+
+
 def test_wide_tree_64_nodes(M, dec):
     shape, W, model = dec
     _verify_case(M, shape, W, model, wl.draft(12, 0, 64, 10, 0.7, shape.V), 130)
@@ -146,6 +158,14 @@ def test_batched_paged_equals_oracle(M, dec):
         assert_accept(toks[r], drafts[r].parents, am[a:b], int(o["accepted_len"][r]), _np(o["accepted_tokens"][a:b]),
                       int(o["bonus"][r]), out.argmax[a:b])
         assert int(kv.ctx_len[r]) == ctxs[r] + int(o["accepted_len"][r]) + 1
+
+
+def test_batched_paged_on_tensor_core_gemms(M, dec):
+    M.set_tc_min_rows(1)
+    try:
+        test_batched_paged_equals_oracle(M, dec)
+    finally:
+        M.set_tc_min_rows(0)
 
 
 def test_bad_inputs_set_status_and_commit_nothing(M, dec):
