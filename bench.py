@@ -263,6 +263,28 @@ def chain_phase_summary(model, launch):
     return res
 
 
+def attention_trace_summary(model, record):
+    """Per-CTA device-clock stamps of one traced attention launch: start,
+    keys done, group ready and end (us after the first CTA start) as
+    percentiles over the CTAs with rows, and the CTA durations."""
+    import numpy as np
+    try:
+        st = model.chain_trace(record).astype(np.int64)
+    except Exception as e:
+        return {"error": str(e)}
+    t0 = int(st[0].min())
+    busy = st[1] > st[0]
+    out = {"attention_record": record, "ctas": int(st.shape[1]), "ctas_with_rows": int(busy.sum())}
+    for name, r in (("start", 0), ("keys_done", 1), ("group_ready", 2), ("end", 3)):
+        v = (st[r][busy] - t0) / 1e3
+        out[name] = [round(float(np.percentile(v, q)), 2) for q in (0, 10, 50, 90, 100)]
+    d = (st[3][busy] - st[0][busy]) / 1e3
+    k = (st[1][busy] - st[0][busy]) / 1e3
+    out["cta_us"] = [round(float(np.percentile(d, q)), 2) for q in (10, 50, 90, 100)]
+    out["cta_keys_us"] = [round(float(np.percentile(k, q)), 2) for q in (10, 50, 90, 100)]
+    return out
+
+
 def overlapped_layer_trace(model, stream, step, layer):
     """Device-clock stamps of one layer's GEMMs in an untimed-style step
     (programmatic dependent launch, no events): per GEMM, the first CTA start,
@@ -439,6 +461,9 @@ def gpu_arm(args, rank, world, dist):
         per_layer = 1 if args.chain else 4
         first = 2 + (shape.n_layers // 2) * 5 if not args.chain else shape.n_layers // 2
         chain_phases = [chain_phase_summary(model, first + i) for i in range(per_layer)]
+    elif args.timeline:
+        # launches of more than 128 rows record only the attention launches
+        chain_phases = [attention_trace_summary(model, shape.n_layers // 2)]
     model.set_timing(False)
     overlap = None
     if args.timeline and not args.chain and M <= 128 and shape.n_rec == 0:

@@ -166,6 +166,11 @@ constexpr int kAttnStages = 2;
 constexpr int kAttnSmem = kAttnStages * 2 * kAttnTile * 128 * 2;  // K and V tiles
 
 int attn_rows_per_group(int hq, int hkv, int max_m) { return (hq / hkv) * max_m; }
+int attn_key_split(int rows_per_group) { return rows_per_group <= 32 ? 2 : 1; }
+int attn_chunks(int rows_per_group) {
+  const int cr = 16 * (4 / attn_key_split(rows_per_group));
+  return (rows_per_group + cr - 1) / cr;
+}
 
 struct AttnKernelArgs {
   AttnArgs a;
@@ -174,7 +179,15 @@ struct AttnKernelArgs {
   int coop;    // 1: the whole grid is resident, splits merge together
 };
 
+// KS = 2 (groups of at most 32 rows, e.g. many requests with short trees):
+// the warps pair up on the same 16-row tile and each takes half of every
+// 64-key tile, so that all four warps work; a pair merges its two
+// online-softmax states in shared memory before the split's partial.
+template <int KS>
 __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
+  constexpr int kRowTiles = 4 / KS;       // 16-row tiles per chunk
+  constexpr int kChunkRows = 16 * kRowTiles;
+  constexpr int kNT = 8 / KS;             // 8-key n-tiles of a warp per 64-key tile
   pdl_launch();  // the next kernel may start streaming its (independent) weights now
   pdl_wait();
   const AttnArgs& a = ka.a;
@@ -194,14 +207,15 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
   const int G = a.hq / a.hkv;
   const int node0 = a.cu[r], Mr = a.cu[r + 1] - node0;
   const int rows = G * Mr;
-  if (rc * 64 >= rows) {  // no rows: no split of this chunk writes or merges anything
+  if (rc * kChunkRows >= rows) {  // no rows: no split of this chunk writes or merges anything
     stamp(1);
     stamp(2);
     stamp(3);
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-  const int rt = rc * 4 + warp;
+  const int rt = rc * kRowTiles + warp % kRowTiles;
+  const int kh = warp / kRowTiles;  // key half of every tile (KS = 2)
   const int ctx = a.ctx[r];
   const bool tree = sp == a.splits;
   int k0, k1;
@@ -214,7 +228,7 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
     k0 = (int)((int64_t)sp * ctx / a.splits);
     k1 = (int)((int64_t)(sp + 1) * ctx / a.splits);
   }
-  const bool has_rows = rt * 16 < rows;
+  bool has_rows = rt * 16 < rows;
   // this lane's two query rows
   const int rho0 = rt * 16 + g, rho1 = rho0 + 8;
   const bool v0 = rho0 < rows, v1 = rho1 < rows;
@@ -273,15 +287,16 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
     cp_async_wait<kAttnStages - 1>();
     __syncthreads();
     if (has_rows) {
-      float s[8][4];
+      float s[kNT][4];
 #pragma unroll
-      for (int i = 0; i < 8; i++) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+      for (int i = 0; i < kNT; i++) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
       const uint32_t kb = smem_u32(sK + buf * kAttnTile * 128);
+      const int key0 = kh * (kAttnTile / KS);  // this warp's first key of the tile
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) {
 #pragma unroll
-        for (int np = 0; np < 4; np++) {
-          const int key = np * 16 + (lane >> 4) * 8 + (lane & 7);
+        for (int np = 0; np < kNT / 2; np++) {
+          const int key = key0 + np * 16 + (lane >> 4) * 8 + (lane & 7);
           const int ch = 2 * kk + ((lane >> 3) & 1);
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kb + key * 256 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
@@ -289,10 +304,10 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
           mma_bf16(s[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
         }
       }
-      const int tb = k0 + tile * kAttnTile;
+      const int tb = k0 + tile * kAttnTile + key0;
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int nt = 0; nt < 8; nt++)
+      for (int nt = 0; nt < kNT; nt++)
 #pragma unroll
         for (int e = 0; e < 4; e++) {
           const int rr = e >> 1;
@@ -313,7 +328,7 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
         mrow[rr] = mn;
       }
 #pragma unroll
-      for (int nt = 0; nt < 8; nt++)
+      for (int nt = 0; nt < kNT; nt++)
 #pragma unroll
         for (int e = 0; e < 4; e++) {
           const int rr = e >> 1;
@@ -335,14 +350,14 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
       }
       const uint32_t vb = smem_u32(sV + buf * kAttnTile * 128);
 #pragma unroll
-      for (int k2 = 0; k2 < 4; k2++) {
+      for (int k2 = 0; k2 < kNT / 2; k2++) {
         const uint32_t pa0 = pack_bf16x2(s[2 * k2][0], s[2 * k2][1]);
         const uint32_t pa1 = pack_bf16x2(s[2 * k2][2], s[2 * k2][3]);
         const uint32_t pa2 = pack_bf16x2(s[2 * k2 + 1][0], s[2 * k2 + 1][1]);
         const uint32_t pa3 = pack_bf16x2(s[2 * k2 + 1][2], s[2 * k2 + 1][3]);
 #pragma unroll
         for (int dp = 0; dp < 8; dp++) {
-          const int key = k2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+          const int key = key0 + k2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
           const int ch = 2 * dp + (lane >> 4);
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(vb + key * 256 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
@@ -354,6 +369,41 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
     __syncthreads();
   }
   cp_async_wait<0>();
+  if constexpr (KS == 2) {
+    // the second warp of each pair hands its (max, sum, O) to the first
+    float* xs = reinterpret_cast<float*>(smem_attn);  // [2 row tiles][32 lanes][68]
+    float* mine = xs + ((warp & 1) * 32 + lane) * 68;
+    __syncthreads();  // every warp is done with the key tiles
+    if (kh == 1 && has_rows) {
+#pragma unroll
+      for (int dn = 0; dn < 16; dn++)
+        *reinterpret_cast<float4*>(mine + 4 * dn) = make_float4(o[dn][0], o[dn][1], o[dn][2], o[dn][3]);
+      *reinterpret_cast<float4*>(mine + 64) = make_float4(mrow[0], mrow[1], lrow[0], lrow[1]);
+    }
+    __syncthreads();
+    if (kh == 0 && has_rows) {
+      const float4 ml = *reinterpret_cast<const float4*>(mine + 64);
+      const float m1[2] = {ml.x, ml.y}, l1[2] = {ml.z, ml.w};
+      float a0[2], a1[2];
+#pragma unroll
+      for (int rr = 0; rr < 2; rr++) {
+        const float mn = fmaxf(mrow[rr], m1[rr]);
+        a0[rr] = mrow[rr] == -INFINITY ? 0.f : exp2f(mrow[rr] - mn);
+        a1[rr] = m1[rr] == -INFINITY ? 0.f : exp2f(m1[rr] - mn);
+        lrow[rr] = lrow[rr] * a0[rr] + l1[rr] * a1[rr];
+        mrow[rr] = mn;
+      }
+#pragma unroll
+      for (int dn = 0; dn < 16; dn++) {
+        const float4 v = *reinterpret_cast<const float4*>(mine + 4 * dn);
+        o[dn][0] = o[dn][0] * a0[0] + v.x * a1[0];
+        o[dn][1] = o[dn][1] * a0[0] + v.y * a1[0];
+        o[dn][2] = o[dn][2] * a0[1] + v.z * a1[1];
+        o[dn][3] = o[dn][3] * a0[1] + v.w * a1[1];
+      }
+    }
+    if (kh == 1) has_rows = false;  // the first warp of the pair writes the partial
+  }
   stamp(1);
 
   // this split's partial
@@ -406,7 +456,7 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
     return;
   }
   // rows merged by this CTA
-  const int rbeg0 = rc * 64, nrow0 = min(rows, rbeg0 + 64) - rbeg0;
+  const int rbeg0 = rc * kChunkRows, nrow0 = min(rows, rbeg0 + kChunkRows) - rbeg0;
   const int rbeg = ka.coop ? rbeg0 + sp * nrow0 / P : rbeg0;
   const int nrow = ka.coop ? rbeg0 + (sp + 1) * nrow0 / P - rbeg : nrow0;
   // merge: every (row, split) (max, sum) pair into shared memory with all
@@ -478,21 +528,25 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
 cudaError_t launch_attention(const AttnArgs& a, int rows_total, cudaStream_t s, bool pdl) {
   (void)rows_total;
   static bool attr = false;
+  static int per_sm[2] = {-1, -1};
   if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-    if (e != cudaSuccess) return e;
+    for (auto kern : {k_attn<1>, k_attn<2>}) {
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+      if (e != cudaSuccess) return e;
+      carveout_once(reinterpret_cast<const void*>(kern));
+    }
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[0], k_attn<1>, 128, kAttnSmem) != cudaSuccess) per_sm[0] = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[1], k_attn<2>, 128, kAttnSmem) != cudaSuccess) per_sm[1] = 0;
     attr = true;
   }
-  static int per_sm = -1;
-  if (per_sm < 0) {
-    carveout_once(reinterpret_cast<const void*>(k_attn));
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_attn, 128, kAttnSmem) != cudaSuccess) per_sm = 0;
-  }
   const int rpg = attn_rows_per_group(a.hq, a.hkv, a.max_m);
-  const int chunks = (attn_rows_per_group(a.hq, a.hkv, a.chunk_m > 0 ? a.chunk_m : a.max_m) + 63) / 64;
+  const int cm = attn_rows_per_group(a.hq, a.hkv, a.chunk_m > 0 ? a.chunk_m : a.max_m);
+  const int ks = attn_key_split(cm);
+  const int chunks = attn_chunks(cm);
   const int64_t grid = (int64_t)(a.splits + 1) * a.hkv * chunks * a.R;
-  const AttnKernelArgs ka{a, rpg, chunks, grid <= (int64_t)per_sm * num_sms() ? 1 : 0};
-  return launch(k_attn, dim3(a.splits + 1, a.hkv * chunks, a.R), dim3(128), kAttnSmem, s, pdl, ka);
+  const AttnKernelArgs ka{a, rpg, chunks, grid <= (int64_t)per_sm[ks - 1] * num_sms() ? 1 : 0};
+  return launch(ks == 2 ? k_attn<2> : k_attn<1>, dim3(a.splits + 1, a.hkv * chunks, a.R), dim3(128), kAttnSmem, s,
+                pdl, ka);
 }
 
 // ------------------------------------------------- linear recurrence -----

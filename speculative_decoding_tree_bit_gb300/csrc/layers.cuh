@@ -59,6 +59,11 @@ struct AttnArgs {
   uint64_t* trace;         // optional [4][grid] device-clock stamps: start, keys done, group ready, end
 };
 int attn_rows_per_group(int hq, int hkv, int max_m);
+// Key split of the attention kernel for groups of this many rows (2: pairs of
+// warps share a 16-row tile, each taking half of every key tile) and the
+// grid's row chunks per (request, kv head).
+int attn_key_split(int rows_per_group);
+int attn_chunks(int rows_per_group);
 cudaError_t launch_attention(const AttnArgs& a, int rows_total, cudaStream_t s, bool pdl);
 
 struct LinrecArgs {

@@ -280,7 +280,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   for (int r = 0; r < io.R && r + 1 < (int)m->cu_host.size(); r++)
     max_mr = std::max(max_mr, m->cu_host[r + 1] - m->cu_host[r]);
   max_mr = std::min(max_mr, m->max_m);
-  const int chunks = (attn_rows_per_group(m->Hq, m->Hkv, max_mr) + 63) / 64;
+  const int chunks = attn_chunks(attn_rows_per_group(m->Hq, m->Hkv, max_mr));
   int splits = attn_splits(io.R, m->Hkv, chunks, m->cfg.max_positions);
   while (splits > 1 && (size_t)io.R * (splits + 1) > m->attn_units) splits--;
   const int64_t layer_elems = (int64_t)io.cv.n_pages * m->Hkv * io.cv.page_size * m->hd;
@@ -597,7 +597,9 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
   // ---- workspace (one allocation)
   const int MR = m->max_rows, R = m->max_req;
   const int rpg = attn_rows_per_group(m->Hq, m->Hkv, m->max_m);
-  const int chunks = (rpg + 63) / 64;
+  // tickets are indexed by the grid's row chunk: size them for the most
+  // chunks any call can use (32-row chunks when groups are small)
+  const int chunks = std::max(attn_chunks(rpg), (rpg + 31) / 32);
   size_t units = 0;
   for (int ch = 1; ch <= chunks; ch++)
     for (int r = 1; r <= R; r++)
