@@ -22,7 +22,9 @@
 //    escaped weights (from the escape tile index) over their slots: the
 //    operand is the exact bf16 weight block.
 //  * Warp 1 (one thread) issues four K = 16 MMAs per k-tile and releases
-//    the rings with tcgen05.commit.
+//    the stage with one tcgen05.commit; it waits on one barrier per k-tile
+//    (each tcgen05 or mbarrier operation costs this single thread about a
+//    hundred cycles, so its per-k-tile instruction count sets the pace).
 //  * Warps 2..5 (one TMEM lane quarter each) read the accumulators
 //    (tcgen05.ld) and run the same fused epilogues as the skinny kernel.
 //  * Work = (row block, k-tile) units split evenly over one CTA per SM
@@ -53,7 +55,7 @@ struct TcParams {
   int acc_cols;    // TMEM columns between the two accumulator buffers
   int tmem_cols;   // TMEM columns allocated (power of two)
   uint32_t idesc;  // instruction descriptor
-  int SX, SA, SW;  // ring stages: activations, decoded weights, packed weights
+  int S, SW;       // ring stages: (activation + decoded weight) tiles, packed weights
   int off_a, off_w, off_bar, off_red, off_rows, smem;
 };
 
@@ -138,6 +140,7 @@ struct TcRows {
 // up (g, g + 8) for SiLU(gate) * up and the RoPE halves: the partner value
 // comes from lane + 8.  Every global load of a chunk is issued before its
 // stores (no load waits behind a store that might alias it).
+template <int EPI>
 __device__ __forceinline__ void tc_emit(const TcParams& P, int64_t n, int c0, const float (&v)[16], float* red_v,
                                         int* red_i, int quarter, const TcRows& rows) {
   const GemmParams& p = P.g;
@@ -146,7 +149,7 @@ __device__ __forceinline__ void tc_emit(const TcParams& P, int64_t n, int c0, co
   const bool valid_n = n < p.N;
   const int g = (int)(n & 15);
   const int mlim = p.M - c0;  // rows j < mlim are real
-  switch (E.epi) {
+  switch (EPI) {
     case EPI_LOGITS: {
 #pragma unroll
       for (int j = 0; j < 16; j++) {
@@ -262,7 +265,7 @@ __device__ __forceinline__ void tc_emit(const TcParams& P, int64_t n, int c0, co
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 
-template <bool AFFINE>
+template <bool AFFINE, int EPI>
 __global__ void __launch_bounds__(tc::kThreads, 1)
     k_w12_gemm_tc(const __grid_constant__ TcParams P, const __grid_constant__ CUtensorMap xmap,
                   const __grid_constant__ CUtensorMap wmap) {
@@ -274,14 +277,14 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   uint8_t* sw = smem + P.off_w;
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + P.off_bar);
   uint64_t* wempty = wfull + P.SW;
-  uint64_t* xfull = wempty + P.SW;
-  uint64_t* xempty = xfull + P.SX;
-  uint64_t* afull = xempty + P.SX;
-  uint64_t* aempty = afull + P.SA;
-  uint64_t* accfull = aempty + P.SA;
+  uint64_t* xfull = wempty + P.SW;   // activation tile landed (copy engine)
+  uint64_t* afull = xfull + P.S;     // decoded tile written and activation tile seen (8 decoder warps)
+  uint64_t* sempty = afull + P.S;    // the stage's MMAs are done (commit)
+  uint64_t* accfull = sempty + P.S;
   uint64_t* accempty = accfull + 2;
   uint64_t* mma_done = accempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* gbar = mma_done + 1;  // [2] finisher staging (bulk copies of partial slices)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbar + 2);
   int* flag = reinterpret_cast<int*>(tmem_slot + 1);
   volatile int* abort = flag + 1;
   float* red_v = reinterpret_cast<float*>(smem + P.off_red);
@@ -302,19 +305,18 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       mbar_init(&wfull[i], 1);
       mbar_init(&wempty[i], kRB);
     }
-    for (int i = 0; i < P.SX; i++) {
+    for (int i = 0; i < P.S; i++) {
       mbar_init(&xfull[i], 1);
-      mbar_init(&xempty[i], 1);
-    }
-    for (int i = 0; i < P.SA; i++) {
       mbar_init(&afull[i], kRB);
-      mbar_init(&aempty[i], 1);
+      mbar_init(&sempty[i], 1);
     }
     for (int i = 0; i < 2; i++) {
       mbar_init(&accfull[i], 1);
       mbar_init(&accempty[i], 4);
     }
     mbar_init(mma_done, 1);
+    mbar_init(&gbar[0], 1);
+    mbar_init(&gbar[1], 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -345,14 +347,14 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         uint32_t xph = 0, wph = 0;
         for (int64_t i = 0; i < n_units; i++) {
           const int64_t u = u0 + i;
-          if (i >= P.SX && !mbar_wait_or_abort(&xempty[xs], xph ^ 1u, abort)) {
+          if (i >= P.S && !mbar_wait_or_abort(&sempty[xs], xph ^ 1u, abort)) {
             set_status(p.status, SD_TIMEOUT_AT(21));
             break;
           }
           mbar_arrive_expect_tx(&xfull[xs], (uint32_t)XB);
           tma2d_g2s(sx + xs * XB, &xmap, (int)(u % KT) * 64, 0, &xfull[xs]);
           nx++;
-          if (++xs == P.SX) {
+          if (++xs == P.S) {
             xs = 0;
             xph ^= 1u;
           }
@@ -380,16 +382,17 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         const int64_t k = nw / P.SW + (s < nw % P.SW ? 1 : 0);
         if (!mbar_wait(&wfull[s], (uint32_t)((k - 1) & 1))) set_status(p.status, SD_TIMEOUT_AT(23));
       }
-      for (int s = 0; s < P.SX && s < nx; s++) {
-        const int64_t k = nx / P.SX + (s < nx % P.SX ? 1 : 0);
+      for (int s = 0; s < P.S && s < nx; s++) {
+        const int64_t k = nx / P.S + (s < nx % P.S ? 1 : 0);
         if (!mbar_wait(&xfull[s], (uint32_t)((k - 1) & 1))) set_status(p.status, SD_TIMEOUT_AT(24));
       }
     }
+    __syncwarp();  // the teardown barrier below wants every warp converged
   } else if (warp == tc::kMma) {
     // ---------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      int xs = 0, as = 0;
-      uint32_t xph = 0, aph = 0;
+      int st = 0;
+      uint32_t ph = 0;
       int64_t i = 0;
       int seg = 0;
       const uint32_t a0 = smem_u32(sa), x0 = smem_u32(sx);
@@ -400,29 +403,23 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         const int buf = seg & 1;
         if (seg >= 2 && !mbar_wait_or_abort(&accempty[buf], (uint32_t)(((seg >> 1) - 1) & 1), abort))
           set_status(p.status, SD_TIMEOUT_AT(25));
-        tc_fence_after();
+        tc_fence_after();  // the epilogue's reads of this buffer come first
         const uint32_t d = tmem + (uint32_t)(buf * P.acc_cols);
         for (int k = 0; k < len; k++) {
-          bool ok = mbar_wait_or_abort(&afull[as], aph, abort);
-          ok = mbar_wait_or_abort(&xfull[xs], xph, abort) && ok;
-          if (!ok) set_status(p.status, SD_TIMEOUT_AT(26));
-          tc_fence_after();
+          // one wait per k-tile: the decoders mark the stage ready once its
+          // activation tile has landed too
+          if (!mbar_wait_or_abort(&afull[st], ph, abort)) set_status(p.status, SD_TIMEOUT_AT(26));
           if (!*abort) {
-            const uint64_t da = sdesc_sw128(a0 + (uint32_t)(as * tc::kATile));
-            const uint64_t db = sdesc_sw128(x0 + (uint32_t)(xs * XB));
+            const uint64_t da = sdesc_sw128(a0 + (uint32_t)(st * tc::kATile));
+            const uint64_t db = sdesc_sw128(x0 + (uint32_t)(st * XB));
 #pragma unroll
             for (int kk = 0; kk < 4; kk++)  // K = 16 per MMA: +32 bytes inside the swizzle atom
               umma_bf16(d, da + 2 * kk, db + 2 * kk, P.idesc, (k | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(&aempty[as]);
-          umma_commit(&xempty[xs]);
-          if (++as == P.SA) {
-            as = 0;
-            aph ^= 1u;
-          }
-          if (++xs == P.SX) {
-            xs = 0;
-            xph ^= 1u;
+          umma_commit(&sempty[st]);
+          if (++st == P.S) {
+            st = 0;
+            ph ^= 1u;
           }
         }
         umma_commit(&accfull[buf]);
@@ -439,12 +436,12 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     const int quarter = warp & 3;  // TMEM lanes 32 * quarter .. + 31
     const int r = quarter * 32 + lane;
     pdl_wait();
-    if (p.e.epi == EPI_LOGITS)
+    if (EPI == EPI_LOGITS)
       for (int m = lane; m < P.MP; m += 32) {
         red_v[quarter * P.MP + m] = -INFINITY;
         red_i[quarter * P.MP + m] = 0x7FFFFFFF;
       }
-    if (p.e.epi == EPI_QKV) {
+    if (EPI == EPI_QKV) {
       const GemmEpilogue& E = p.e;
       for (int m = threadIdx.x - tc::kEpi0 * 32; m < p.M && m < P.MP; m += 128) {
         rows.pos[m] = E.rows.pos[m];
@@ -462,6 +459,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     const int mrows = P.MP < p.M ? P.MP : p.M;
     const int nch = (mrows + 15) / 16;
     const int first_b = n_units > 0 ? (int)(u0 / KT) : -1;
+    uint32_t stg_par = 0;  // bit b: parity of the next phase of staging barrier b
     int64_t i = 0;
     int seg = 0;
     while (i < n_units) {
@@ -478,7 +476,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         for (int c = 0; c < nch; c++) {
           float v[16];
           tmem_ld16(taddr + 16 * c, v);
-          tc_emit(P, n, 16 * c, v, red_v, red_i, quarter, rows);
+          tc_emit<EPI>(P, n, 16 * c, v, red_v, red_i, quarter, rows);
         }
         tc_fence_before();
         __syncwarp();
@@ -502,35 +500,102 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         if (*flag) {
           // contributors: the CTAs whose (non-empty) unit range meets block b,
           // summed in CTA order; this CTA's own share comes from TMEM (still
-          // held), the others' from their partials, two contributors' loads
-          // in flight at a time
+          // held)
           const int64_t c_first = (((int64_t)b * KT + 1) * G - 1) / p.U;
           const int64_t c_last = (((int64_t)(b + 1) * KT) * G - 1) / p.U;
-          for (int c = 0; c < nch; c++) {
-            float own[16], v[16];
-            tmem_ld16(taddr + 16 * c, own);
-#pragma unroll
-            for (int j = 0; j < 16; j++) v[j] = 0.f;
-            for (int64_t c0 = c_first; c0 <= c_last; c0 += 2) {
-              float w[2][16];
-              bool mine[2];
-#pragma unroll
-              for (int u = 0; u < 2; u++) {
-                const int64_t cc = c0 + u;
-                const int64_t cs = cc * p.U / G, ce = (cc + 1) * p.U / G;
-                mine[u] = cc == blockIdx.x;
-                const bool use = cc <= c_last && cs != ce && !mine[u];  // empty ranges wrote no partial
-                const int csid = (b != (int)(cs / KT)) ? 1 : 0;
-                const float* src = p.partial + ((int64_t)((use ? cc : 0) * 2 + csid) * P.MP + 16 * c) * 128 + r;
-#pragma unroll
-                for (int j = 0; j < 16; j++) w[u][j] = use ? __ldcg(src + j * 128) : 0.f;
+          auto other = [&](int64_t cc, int& csid) {  // a contributor whose partial is read
+            const int64_t cs = cc * p.U / G, ce = (cc + 1) * p.U / G;
+            csid = (b != (int)(cs / KT)) ? 1 : 0;
+            return cs != ce && cc != (int64_t)blockIdx.x;  // empty ranges wrote no partial
+          };
+          int n_oth = 0;
+          for (int64_t cc = c_first; cc <= c_last; cc++) {
+            int csid;
+            n_oth += other(cc, csid) ? 1 : 0;
+          }
+          // the CTA's last segment: the rings are idle (every copy consumed,
+          // every MMA complete), so one thread stages the others' partial
+          // slices there with bulk copies, two column groups in flight
+          int GC = 64;
+          while (GC > 16 && 2 * n_oth * GC * 512 > P.off_bar) GC >>= 1;
+          const bool staged = i + len == n_units && n_oth > 0 && 2 * n_oth * GC * 512 <= P.off_bar;
+          if (staged) {
+            float* stage = reinterpret_cast<float*>(smem);
+            const int ngroups = (nch * 16 + GC - 1) / GC;
+            auto issue = [&](int gi) {
+              if (threadIdx.x != tc::kEpi0 * 32) return;
+              const int cols = min(GC, P.MP - gi * GC);
+              fence_async_smem();  // earlier generic reads of the buffer come first
+              mbar_arrive_expect_tx(&gbar[gi & 1], (uint32_t)(n_oth * cols * 512));
+              int k = 0;
+              for (int64_t cc = c_first; cc <= c_last; cc++) {
+                int csid;
+                if (!other(cc, csid)) continue;
+                bulk_g2s(stage + (int64_t)((gi & 1) * n_oth + k) * GC * 128,
+                         p.partial + ((cc * 2 + csid) * P.MP + gi * GC) * 128, (uint32_t)(cols * 512), &gbar[gi & 1]);
+                k++;
               }
+            };
+            issue(0);
+            for (int gi = 0; gi < ngroups; gi++) {
+              if (gi + 1 < ngroups) {
+                bar_sync(2, 128);  // every thread is done with the buffer group gi + 1 reuses
+                issue(gi + 1);
+              }
+              if (!mbar_wait_or_abort(&gbar[gi & 1], (stg_par >> (gi & 1)) & 1u, abort))
+                set_status(p.status, SD_TIMEOUT_AT(31));
+              stg_par ^= 1u << (gi & 1);
+              const float* sb = stage + (int64_t)((gi & 1) * n_oth) * GC * 128 + r;
+              for (int cl = 0; cl < GC / 16; cl++) {
+                const int c = gi * (GC / 16) + cl;
+                if (c >= nch) break;
+                float own[16], v[16];
+                tmem_ld16(taddr + 16 * c, own);
 #pragma unroll
-              for (int u = 0; u < 2; u++)
+                for (int j = 0; j < 16; j++) v[j] = 0.f;
+                int k = 0;
+                for (int64_t cc = c_first; cc <= c_last; cc++) {
+                  int csid;
+                  if (cc == (int64_t)blockIdx.x) {
 #pragma unroll
-                for (int j = 0; j < 16; j++) v[j] += mine[u] ? own[j] : w[u][j];
+                    for (int j = 0; j < 16; j++) v[j] += own[j];
+                  } else if (other(cc, csid)) {
+                    const float* src = sb + (int64_t)k * GC * 128 + cl * 16 * 128;
+#pragma unroll
+                    for (int j = 0; j < 16; j++) v[j] += src[j * 128];
+                    k++;
+                  }
+                }
+                tc_emit<EPI>(P, n, 16 * c, v, red_v, red_i, quarter, rows);
+              }
             }
-            tc_emit(P, n, 16 * c, v, red_v, red_i, quarter, rows);
+          } else {
+            // two contributors' loads in flight at a time
+            for (int c = 0; c < nch; c++) {
+              float own[16], v[16];
+              tmem_ld16(taddr + 16 * c, own);
+#pragma unroll
+              for (int j = 0; j < 16; j++) v[j] = 0.f;
+              for (int64_t c0 = c_first; c0 <= c_last; c0 += 2) {
+                float w[2][16];
+                bool mine[2];
+#pragma unroll
+                for (int u = 0; u < 2; u++) {
+                  const int64_t cc = c0 + u;
+                  int csid = 0;
+                  mine[u] = cc == (int64_t)blockIdx.x;
+                  const bool use = cc <= c_last && other(cc, csid);
+                  const float* src = p.partial + ((int64_t)((use ? cc : 0) * 2 + csid) * P.MP + 16 * c) * 128 + r;
+#pragma unroll
+                  for (int j = 0; j < 16; j++) w[u][j] = use ? __ldcg(src + j * 128) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 2; u++)
+#pragma unroll
+                  for (int j = 0; j < 16; j++) v[j] += mine[u] ? own[j] : w[u][j];
+              }
+              tc_emit<EPI>(P, n, 16 * c, v, red_v, red_i, quarter, rows);
+            }
           }
           if (threadIdx.x == tc::kEpi0 * 32) p.counters[b] = 0;
         }
@@ -541,7 +606,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       seg++;
       i += len;
     }
-    if (p.e.epi == EPI_LOGITS) {
+    if (EPI == EPI_LOGITS) {
       bar_sync(2, 128);
       const int et = threadIdx.x - tc::kEpi0 * 32;
       for (int m = et; m < mrows; m += 128) {
@@ -616,7 +681,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         ws = 0;
         wph ^= 1u;
       }
-      if (i >= P.SA && !mbar_wait_or_abort(&aempty[as], aph ^ 1u, abort)) set_status(p.status, SD_TIMEOUT_AT(30));
+      if (i >= P.S && !mbar_wait_or_abort(&sempty[as], aph ^ 1u, abort)) set_status(p.status, SD_TIMEOUT_AT(30));
       uint8_t* dst = sa + as * tc::kATile;
 #pragma unroll
       for (int j = 0; j < 4; j++) {
@@ -639,9 +704,10 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       }
       // the tile is read by the tensor cores (async proxy)
       fence_async_smem();
+      if (!mbar_wait_or_abort(&xfull[as], aph, abort)) set_status(p.status, SD_TIMEOUT_AT(32));
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull[as]);
-      if (++as == P.SA) {
+      if (++as == P.S) {
         as = 0;
         aph ^= 1u;
       }
@@ -658,9 +724,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   }
 
   tc_fence_before();
+  __syncwarp();
   __syncthreads();
   if (warp == tc::kMma) {
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)P.tmem_cols);
   }
@@ -683,16 +749,17 @@ static int tc_setup(TcParams* P, int M) {
   P->tmem_cols = 2 * ac;
   P->idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(MP >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
   const int XB = MP * 128;
-  P->SX = 4;
-  P->SA = MP > 128 ? 2 : 3;
+  // stages of (activation tile, decoded tile): 3 of up to 48 KB, 4 for up to
+  // 128 rows; as many 12 KB packed-weight stages as fit
+  P->S = MP > 128 ? 3 : 4;
   const int bar_bytes = 512;
   const int red_bytes = 8 * MP * 4;
   const int rows_bytes = 12 * MP;
-  const int budget = tc::kSmemMax - 1024 - bar_bytes - red_bytes - rows_bytes - P->SX * XB - P->SA * tc::kATile;
+  const int budget = tc::kSmemMax - 1024 - bar_bytes - red_bytes - rows_bytes - P->S * (XB + tc::kATile);
   P->SW = std::min(8, budget / tc::kWTile);
   if (P->SW < 2) return SD_ERR_UNSUPPORTED;
-  P->off_a = P->SX * XB;
-  P->off_w = P->off_a + P->SA * tc::kATile;
+  P->off_a = P->S * XB;
+  P->off_w = P->off_a + P->S * tc::kATile;
   P->off_bar = P->off_w + P->SW * tc::kWTile;
   P->off_red = P->off_bar + bar_bytes;
   P->off_rows = P->off_red + red_bytes;
@@ -702,16 +769,31 @@ static int tc_setup(TcParams* P, int M) {
 
 size_t gemm_tc_partial_floats(int M) { return (size_t)num_sms() * 2 * gemm_tc_rows(std::min(M, 256)) * 128; }
 
-template <bool AFF>
+template <bool AFF, int EPI>
 static cudaError_t launch_tc(const TcParams& P, const CUtensorMap& xmap, const CUtensorMap& wmap, cudaStream_t s,
                              bool pdl, int grid) {
-  static int attr_set = 0;
-  if (attr_set < tc::kSmemMax) {
-    const cudaError_t e = cudaFuncSetAttribute(k_w12_gemm_tc<AFF>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemMax);
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k_w12_gemm_tc<AFF, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemMax);
     if (e != cudaSuccess) return e;
-    attr_set = tc::kSmemMax;
+    attr_set = true;
   }
-  return launch(k_w12_gemm_tc<AFF>, dim3(grid), dim3(tc::kThreads), (size_t)P.smem, s, pdl, P, xmap, wmap);
+  return launch(k_w12_gemm_tc<AFF, EPI>, dim3(grid), dim3(tc::kThreads), (size_t)P.smem, s, pdl, P, xmap, wmap);
+}
+
+// One kernel per (table kind, epilogue): no per-element dispatch, and each
+// keeps only its own epilogue's registers.
+template <bool AFF>
+static cudaError_t launch_tc_epi(const TcParams& P, const CUtensorMap& xmap, const CUtensorMap& wmap,
+                                 cudaStream_t s, bool pdl, int grid) {
+  switch (P.g.e.epi) {
+    case EPI_STORE: return launch_tc<AFF, EPI_STORE>(P, xmap, wmap, s, pdl, grid);
+    case EPI_RESID: return launch_tc<AFF, EPI_RESID>(P, xmap, wmap, s, pdl, grid);
+    case EPI_SILU: return launch_tc<AFF, EPI_SILU>(P, xmap, wmap, s, pdl, grid);
+    case EPI_QKV: return launch_tc<AFF, EPI_QKV>(P, xmap, wmap, s, pdl, grid);
+    default: return launch_tc<AFF, EPI_LOGITS>(P, xmap, wmap, s, pdl, grid);
+  }
 }
 
 int gemm_tc_launch(const w12_tensor& W, const uint16_t* x, int rows_total, int M, const GemmEpilogue& epi,
@@ -736,8 +818,8 @@ int gemm_tc_launch(const w12_tensor& W, const uint16_t* x, int rows_total, int M
   if ((rc = make_x_map(&xm, x, std::max(rows_total, M), W.K, P.MP))) return rc;
   CUtensorMap wmap;
   if ((rc = make_w_map(&wmap, W))) return rc;
-  const cudaError_t e = W.affine ? launch_tc<true>(P, xm.map, wmap, s, pdl, grid)
-                                 : launch_tc<false>(P, xm.map, wmap, s, pdl, grid);
+  const cudaError_t e = W.affine ? launch_tc_epi<true>(P, xm.map, wmap, s, pdl, grid)
+                                 : launch_tc_epi<false>(P, xm.map, wmap, s, pdl, grid);
   if (e != cudaSuccess) return cuda_fail(e, "k_w12_gemm_tc launch");
   return SD_OK;
 }
