@@ -22,9 +22,11 @@
 //    escaped weights (from the escape tile index) over their slots: the
 //    operand is the exact bf16 weight block.
 //  * Warp 1 (one thread) issues four K = 16 MMAs per k-tile and releases
-//    the stage with one tcgen05.commit; it waits on one barrier per k-tile
-//    (each tcgen05 or mbarrier operation costs this single thread about a
-//    hundred cycles, so its per-k-tile instruction count sets the pace).
+//    the stage with one tcgen05.commit.  An mbarrier wait costs its warp a
+//    round trip of over a hundred cycles even on a completed phase, so the
+//    MMA thread and the decoders probe the next k-tile's barriers with
+//    test_wait before the current k-tile's work and block only when a probe
+//    found a phase incomplete.
 //  * Warps 2..5 (one TMEM lane quarter each) read the accumulators
 //    (tcgen05.ld) and run the same fused epilogues as the skinny kernel.
 //  * Work = (row block, k-tile) units split evenly over one CTA per SM
@@ -393,6 +395,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     if (lane == 0) {
       int st = 0;
       uint32_t ph = 0;
+      bool ready = false;  // the current stage's probes found it complete
       int64_t i = 0;
       int seg = 0;
       const uint32_t a0 = smem_u32(sa), x0 = smem_u32(sx);
@@ -406,21 +409,33 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         tc_fence_after();  // the epilogue's reads of this buffer come first
         const uint32_t d = tmem + (uint32_t)(buf * P.acc_cols);
         for (int k = 0; k < len; k++) {
-          // one wait per k-tile: the decoders mark the stage ready once its
-          // activation tile has landed too
-          if (!mbar_wait_or_abort(&afull[st], ph, abort)) set_status(p.status, SD_TIMEOUT_AT(26));
-          if (!*abort) {
-            const uint64_t da = sdesc_sw128(a0 + (uint32_t)(st * tc::kATile));
-            const uint64_t db = sdesc_sw128(x0 + (uint32_t)(st * XB));
-#pragma unroll
-            for (int kk = 0; kk < 4; kk++)  // K = 16 per MMA: +32 bytes inside the swizzle atom
-              umma_bf16(d, da + 2 * kk, db + 2 * kk, P.idesc, (k | kk) != 0 ? 1u : 0u);
+          // the probes of this stage were issued a k-tile ago; block only if
+          // they found it incomplete
+          if (!ready) {
+            bool ok = mbar_wait_or_abort(&afull[st], ph, abort);
+            ok = mbar_wait_or_abort(&xfull[st], ph, abort) && ok;
+            if (!ok) set_status(p.status, SD_TIMEOUT_AT(26));
           }
-          umma_commit(&sempty[st]);
+          const int cur = st;
           if (++st == P.S) {
             st = 0;
             ph ^= 1u;
           }
+          // both probes go out before the MMAs (no branch on their results here)
+          bool pa = false, px = false;
+          if (i + k + 1 < n_units) {
+            pa = mbar_test_wait(&afull[st], ph);
+            px = mbar_test_wait(&xfull[st], ph);
+          }
+          if (!*abort) {
+            const uint64_t da = sdesc_sw128(a0 + (uint32_t)(cur * tc::kATile));
+            const uint64_t db = sdesc_sw128(x0 + (uint32_t)(cur * XB));
+#pragma unroll
+            for (int kk = 0; kk < 4; kk++)  // K = 16 per MMA: +32 bytes inside the swizzle atom
+              umma_bf16(d, da + 2 * kk, db + 2 * kk, P.idesc, (k | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&sempty[cur]);
+          ready = pa && px;
         }
         umma_commit(&accfull[buf]);
         seg++;
@@ -656,6 +671,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     }
     int ws = 0, as = 0;
     uint32_t wph = 0, aph = 0;
+    bool w_ok = false, s_ok = false;  // probes of the current k-tile's barriers found them complete
     const uint32_t off_lo = (uint32_t)((16 * d + g) * 128) + 4 * q, off_hi = off_lo + 8 * 128;
     for (int64_t i = 0; i < n_units; i++) {
       // entries of unit i + kEscAhead go in flight now
@@ -670,7 +686,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         fetch(kn, ent_n, base_n, cnt_n);
       }
       const uint32_t ent = q_ent[0], e_base = q_base[0], e_cnt = q_cnt[0];
-      if (!mbar_wait_or_abort(&wfull[ws], wph, abort)) set_status(p.status, SD_TIMEOUT_AT(29));
+      if (!w_ok && !mbar_wait_or_abort(&wfull[ws], wph, abort)) set_status(p.status, SD_TIMEOUT_AT(29));
       const uint8_t* src = sw + ws * tc::kWTile + d * kStripBytes + lane * 16;
       const uint4 W0 = *reinterpret_cast<const uint4*>(src);
       const uint4 W1 = *reinterpret_cast<const uint4*>(src + 512);
@@ -681,7 +697,15 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         ws = 0;
         wph ^= 1u;
       }
-      if (i >= P.S && !mbar_wait_or_abort(&sempty[as], aph ^ 1u, abort)) set_status(p.status, SD_TIMEOUT_AT(30));
+      if (i >= P.S && !s_ok && !mbar_wait_or_abort(&sempty[as], aph ^ 1u, abort))
+        set_status(p.status, SD_TIMEOUT_AT(30));
+      // probe the next k-tile's barriers now; the decode below hides the round trip
+      {
+        const int nas = as + 1 == P.S ? 0 : as + 1;
+        const uint32_t naph = as + 1 == P.S ? aph ^ 1u : aph;
+        w_ok = i + 1 < n_units && mbar_test_wait(&wfull[ws], wph);
+        s_ok = i + 1 < P.S || (i + 1 < n_units && mbar_test_wait(&sempty[nas], naph ^ 1u));
+      }
       uint8_t* dst = sa + as * tc::kATile;
 #pragma unroll
       for (int j = 0; j < 4; j++) {
@@ -704,7 +728,6 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       }
       // the tile is read by the tensor cores (async proxy)
       fence_async_smem();
-      if (!mbar_wait_or_abort(&xfull[as], aph, abort)) set_status(p.status, SD_TIMEOUT_AT(32));
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull[as]);
       if (++as == P.S) {
