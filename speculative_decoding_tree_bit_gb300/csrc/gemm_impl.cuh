@@ -85,13 +85,92 @@ __device__ __forceinline__ uint32_t comp(const uint4& v, int j) {
 }
 
 // Residuals may have been written earlier in the same launch by other CTAs
-// (chained phases): they are read with L1-bypassing loads.
+// (chained phases): they are read with L1-bypassing loads.  The residual and
+// QKV epilogues issue every load of the thread's rows before any store (the
+// output may alias the residual, so a load placed after a store would wait
+// for it: one memory round trip per element).
 template <int NT>
 __device__ __forceinline__ void epilogue(const GemmParams& p, int strip, int lane, float (&acc)[NT][4],
                                          float (&bestv)[NT][2], int (&besti)[NT][2]) {
   const int g = lane >> 2, q = lane & 3;
   const int64_t n_lo = (int64_t)strip * 16 + g;
   const GemmEpilogue& E = p.e;
+  if (E.epi == EPI_RESID) {
+    float r[NT][2][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int cc = 0; cc < 2; cc++) {
+        const int m = p.m0 + nt * 8 + 2 * q + cc;
+        const int64_t i0 = (int64_t)m * E.ldo + n_lo;
+        const bool ok = m < p.M;
+        r[nt][cc][0] = ok ? bf2f(__ldcg(E.resid + i0)) : 0.f;
+        r[nt][cc][1] = ok ? bf2f(__ldcg(E.resid + i0 + 8)) : 0.f;
+      }
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int cc = 0; cc < 2; cc++) {
+        const int m = p.m0 + nt * 8 + 2 * q + cc;
+        if (m >= p.M) continue;
+        const int64_t i0 = (int64_t)m * E.ldo + n_lo;
+        E.out[i0] = f2bf(r[nt][cc][0] + rbf(acc[nt][cc]));
+        E.out[i0 + 8] = f2bf(r[nt][cc][1] + rbf(acc[nt][2 + cc]));
+      }
+    return;
+  }
+  if (E.epi == EPI_QKV) {
+    const int64_t qrows = (int64_t)E.hq * 128, krows = (int64_t)E.hkv * 128;
+    const int64_t row0 = (int64_t)strip * 16;
+    const bool rope = row0 < qrows + krows;
+    const bool is_q = row0 < qrows;
+    const int64_t rr = rope ? (is_q ? row0 : row0 - qrows) : row0 - qrows - krows;
+    const int head = (int)(rr / 128);
+    const int d = rope ? (int)((rr % 128) / 16) * 8 + g : (int)(rr % 128) + g;
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) {
+      // the thread's two rows of this token tile: loads first, then stores
+      int pos[2], rq[2], slot[2];
+#pragma unroll
+      for (int cc = 0; cc < 2; cc++) {
+        const int m = p.m0 + nt * 8 + 2 * q + cc;
+        const bool ok = m < p.M;
+        pos[cc] = ok && rope ? E.rows.pos[m] : 0;
+        rq[cc] = ok && !is_q ? E.rows.req[m] : 0;
+        slot[cc] = ok && !is_q ? E.rows.slot[m] : 0;
+      }
+      float cs[2], sn[2];
+      int okr[2], page[2];
+#pragma unroll
+      for (int cc = 0; cc < 2; cc++) {
+        cs[cc] = rope ? E.rope_cos[(int64_t)pos[cc] * 64 + d] : 1.f;
+        sn[cc] = rope ? E.rope_sin[(int64_t)pos[cc] * 64 + d] : 0.f;
+        okr[cc] = is_q ? 1 : E.rows.req_ok[rq[cc]];
+        page[cc] = is_q ? 0 : E.cache.page_table[(int64_t)rq[cc] * E.cache.max_pages + slot[cc] / E.cache.page_size];
+      }
+#pragma unroll
+      for (int cc = 0; cc < 2; cc++) {
+        const int m = p.m0 + nt * 8 + 2 * q + cc;
+        if (m >= p.M || !okr[cc]) continue;
+        const float v_lo = acc[nt][cc], v_hi = acc[nt][2 + cc];
+        if (rope) {
+          const float x1 = rbf(v_lo), x2 = rbf(v_hi);
+          const uint16_t o1 = f2bf(x1 * cs[cc] - x2 * sn[cc]), o2 = f2bf(x2 * cs[cc] + x1 * sn[cc]);
+          uint16_t* dst = is_q ? E.q_out + ((int64_t)m * E.hq + head) * 128
+                               : E.cache.k + (((int64_t)page[cc] * E.cache.hkv + head) * E.cache.page_size +
+                                              slot[cc] % E.cache.page_size) * 128;
+          dst[d] = o1;
+          dst[d + 64] = o2;
+        } else {
+          uint16_t* dst = E.cache.v + (((int64_t)page[cc] * E.cache.hkv + head) * E.cache.page_size +
+                                       slot[cc] % E.cache.page_size) * 128;
+          dst[d] = f2bf(v_lo);
+          dst[d + 8] = f2bf(v_hi);
+        }
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int nt = 0; nt < NT; nt++)
 #pragma unroll
@@ -104,60 +183,10 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, int strip, int lan
           E.out[(int64_t)m * E.ldo + n_lo] = f2bf(v_lo);
           E.out[(int64_t)m * E.ldo + n_lo + 8] = f2bf(v_hi);
           break;
-        case EPI_RESID: {
-          const int64_t i0 = (int64_t)m * E.ldo + n_lo, i1 = i0 + 8;
-          const float r0 = bf2f(__ldcg(E.resid + i0)), r1 = bf2f(__ldcg(E.resid + i1));
-          E.out[i0] = f2bf(r0 + rbf(v_lo));
-          E.out[i1] = f2bf(r1 + rbf(v_hi));
-          break;
-        }
         case EPI_SILU: {
           const float gt = rbf(v_lo), up = rbf(v_hi);
           const float s = gt / (1.0f + expf(-gt));
           E.out[(int64_t)m * E.ldo + (int64_t)strip * 8 + g] = f2bf(s * up);
-          break;
-        }
-        case EPI_QKV: {
-          const int64_t qrows = (int64_t)E.hq * 128, krows = (int64_t)E.hkv * 128;
-          const int64_t row0 = (int64_t)strip * 16;
-          if (row0 < qrows + krows) {
-            const bool is_q = row0 < qrows;
-            const int64_t rr = is_q ? row0 : row0 - qrows;
-            const int head = (int)(rr / 128);
-            const int d = (int)((rr % 128) / 16) * 8 + g;
-            const float x1 = rbf(v_lo), x2 = rbf(v_hi);
-            const int pos = E.rows.pos[m];
-            const float c = E.rope_cos[(int64_t)pos * 64 + d], sn = E.rope_sin[(int64_t)pos * 64 + d];
-            const uint16_t o1 = f2bf(x1 * c - x2 * sn), o2 = f2bf(x2 * c + x1 * sn);
-            if (is_q) {
-              uint16_t* dst = E.q_out + ((int64_t)m * E.hq + head) * 128;
-              dst[d] = o1;
-              dst[d + 64] = o2;
-            } else {
-              const int r = E.rows.req[m];
-              if (E.rows.req_ok[r]) {
-                const int slot = E.rows.slot[m];
-                const int page = E.cache.page_table[(int64_t)r * E.cache.max_pages + slot / E.cache.page_size];
-                uint16_t* dst = E.cache.k + (((int64_t)page * E.cache.hkv + head) * E.cache.page_size +
-                                             slot % E.cache.page_size) * 128;
-                dst[d] = o1;
-                dst[d + 64] = o2;
-              }
-            }
-          } else {
-            const int64_t vr = row0 - qrows - krows;
-            const int head = (int)(vr / 128);
-            const int d = (int)(vr % 128) + g;
-            const int r = E.rows.req[m];
-            if (E.rows.req_ok[r]) {
-              const int slot = E.rows.slot[m];
-              const int page = E.cache.page_table[(int64_t)r * E.cache.max_pages + slot / E.cache.page_size];
-              uint16_t* dst = E.cache.v + (((int64_t)page * E.cache.hkv + head) * E.cache.page_size +
-                                           slot % E.cache.page_size) * 128;
-              dst[d] = f2bf(v_lo);
-              dst[d + 8] = f2bf(v_hi);
-            }
-          }
           break;
         }
         case EPI_LOGITS: {
