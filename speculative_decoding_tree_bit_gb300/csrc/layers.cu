@@ -485,32 +485,53 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
     for (int p = 0; p < P; p++) wsm[i * kMaxParts + p] *= inv;
   }
   __syncthreads();
-  // slice = (row, 4 dims): 32 slices per row; a slice's partials are loaded
-  // 16 splits at a time, all in flight before they are used
-  for (int sl = threadIdx.x; sl < nrow * 32; sl += 128) {
-    const int i = sl >> 5, d4 = sl & 31;
+  // slice = (row, 4 dims): 32 slices per row.  With few rows per CTA (the
+  // cooperative merge) the splits of a slice are dealt to nsub adjacent
+  // threads (split p to thread p % nsub), so that every thread's loads are in
+  // flight at once; the nsub partial sums are added with shuffles in a fixed
+  // order (deterministic).  Loads go 16 splits at a time.
+  const int nsub = nrow * 32 * 4 <= 128 ? 4 : nrow * 32 * 2 <= 128 ? 2 : 1;
+  const int nslices = nrow * 32;
+  for (int t0 = 0; t0 < nslices * nsub; t0 += 128) {
+    const int t = t0 + threadIdx.x;
+    const int sl = t / nsub, sub = t % nsub;
+    const bool live = sl < nslices;
+    const int i = live ? sl >> 5 : 0, d4 = sl & 31;
     const float4* src = reinterpret_cast<const float4*>(a.part_o + (gbase * ka.rpg + rbeg + i) * 128) + d4;
     const int64_t pstride = (int64_t)ka.rpg * 32;  // float4 per split
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p0 = 0; p0 < P; p0 += 16) {
+    for (int p0 = sub; p0 < P; p0 += 16 * nsub) {
       float4 v[16];
 #pragma unroll
-      for (int u = 0; u < 16; u++) v[u] = p0 + u < P ? __ldcg(src + (p0 + u) * pstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < 16; u++) {
+        const int pp = p0 + u * nsub;
+        v[u] = live && pp < P ? __ldcg(src + pp * pstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
       for (int u = 0; u < 16; u++) {
-        const float w = p0 + u < P ? wsm[i * kMaxParts + p0 + u] : 0.f;
+        const int pp = p0 + u * nsub;
+        const float w = live && pp < P ? wsm[i * kMaxParts + pp] : 0.f;
         acc.x = fmaf(w, v[u].x, acc.x);
         acc.y = fmaf(w, v[u].y, acc.y);
         acc.z = fmaf(w, v[u].z, acc.z);
         acc.w = fmaf(w, v[u].w, acc.w);
       }
     }
-    const int rho = rbeg + i;
-    const int node = rho % Mr, qh = h * G + rho / Mr;
-    uint2 o2;
-    o2.x = pack_bf16x2(acc.x, acc.y);
-    o2.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(a.out + (int64_t)(node0 + node) * a.hq * 128 + qh * 128 + d4 * 4) = o2;
+    // adjacent lanes hold the nsub shares of one slice (nsub divides 32)
+    for (int off = 1; off < nsub; off <<= 1) {
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+    }
+    if (live && sub == 0) {
+      const int rho = rbeg + i;
+      const int node = rho % Mr, qh = h * G + rho / Mr;
+      uint2 o2;
+      o2.x = pack_bf16x2(acc.x, acc.y);
+      o2.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(a.out + (int64_t)(node0 + node) * a.hq * 128 + qh * 128 + d4 * 4) = o2;
+    }
   }
   if (ka.coop) {
     // the last split to finish merging resets the group's counters (every
