@@ -184,19 +184,17 @@ struct AttnKernelArgs {
 // 64-key tile, so that all four warps work; a pair merges its two
 // online-softmax states in shared memory before the split's partial.
 template <int KS>
-__global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
+__global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
   constexpr int kRowTiles = 4 / KS;       // 16-row tiles per chunk
   constexpr int kChunkRows = 16 * kRowTiles;
   constexpr int kNT = 8 / KS;             // 8-key n-tiles of a warp per 64-key tile
   pdl_launch();  // the next kernel may start streaming its (independent) weights now
-  pdl_wait();
   const AttnArgs& a = ka.a;
   const int64_t cta = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
   const int64_t ncta = (int64_t)gridDim.x * gridDim.y * gridDim.z;
   auto stamp = [&](int row) {
     if (a.trace && threadIdx.x == 0) a.trace[row * ncta + cta] = globaltimer();
   };
-  stamp(0);
   extern __shared__ __align__(128) uint8_t smem_attn[];
   uint16_t* sK = reinterpret_cast<uint16_t*>(smem_attn);
   uint16_t* sV = sK + kAttnStages * kAttnTile * 128;
@@ -205,9 +203,11 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
   const int h = blockIdx.y % a.hkv, rc = blockIdx.y / a.hkv;
   const int r = blockIdx.z;
   const int G = a.hq / a.hkv;
+  // request offsets are host inputs: readable before the wait
   const int node0 = a.cu[r], Mr = a.cu[r + 1] - node0;
   const int rows = G * Mr;
   if (rc * kChunkRows >= rows) {  // no rows: no split of this chunk writes or merges anything
+    stamp(0);
     stamp(1);
     stamp(2);
     stamp(3);
@@ -216,25 +216,26 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
   const int rt = rc * kRowTiles + warp % kRowTiles;
   const int kh = warp / kRowTiles;  // key half of every tile (KS = 2)
-  const int ctx = a.ctx[r];
   const bool tree = sp == a.splits;
-  int k0, k1;
-  if (!a.req_ok[r]) {
-    k0 = k1 = 0;
-  } else if (tree) {
-    k0 = ctx;
-    k1 = ctx + Mr;
-  } else {
-    k0 = (int)((int64_t)sp * ctx / a.splits);
-    k1 = (int)((int64_t)(sp + 1) * ctx / a.splits);
-  }
+  const int cap = a.max_pages * a.page_size;
+  // a prefix split's keys: the committed prefix, which no kernel of the step
+  // writes before its commit, located through the host's page table and the
+  // context length as passed in; the first key tile is requested before the
+  // wait for the previous kernel
+  auto prefix_range = [&](int c, int& lo, int& hi) {
+    c = c < 0 ? 0 : (c > cap ? cap : c);
+    lo = (int)((int64_t)sp * c / a.splits);
+    hi = (int)((int64_t)(sp + 1) * c / a.splits);
+  };
+  int k0 = 0, k1 = 0;
+  const int ctx_pre = tree ? 0 : a.ctx_in[r];
+  if (!tree) prefix_range(ctx_pre, k0, k1);
   bool has_rows = rt * 16 < rows;
   // this lane's two query rows
   const int rho0 = rt * 16 + g, rho1 = rho0 + 8;
   const bool v0 = rho0 < rows, v1 = rho1 < rows;
   const int n0 = v0 ? rho0 % Mr : 0, n1 = v1 ? rho1 % Mr : 0;
   const int qh0 = h * G + (v0 ? rho0 / Mr : 0), qh1 = h * G + (v1 ? rho1 / Mr : 0);
-  const uint64_t anc0 = v0 ? a.anc[node0 + n0] : 0ull, anc1 = v1 ? a.anc[node0 + n1] : 0ull;
 
   const int64_t head_stride = (int64_t)a.page_size * 128;
   auto load_tile = [&](int tile, int buf) {
@@ -242,25 +243,49 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
     for (int c = threadIdx.x; c < kAttnTile * 16; c += 128) {
       const int kr = c >> 4, ch = c & 15;
       const int t = kb + kr;
-      const bool valid = t < k1;
+      bool valid = t < k1;
       int64_t off = 0;
       if (valid) {
+        // page ids may be read before the tree kernel validated them
         const int page = a.page_table[(int64_t)r * a.max_pages + t / a.page_size];
-        off = ((int64_t)page * a.hkv + h) * head_stride + (int64_t)(t % a.page_size) * 128 + ch * 8;
+        valid = page >= 0 && page < a.n_pages;
+        if (valid) off = ((int64_t)page * a.hkv + h) * head_stride + (int64_t)(t % a.page_size) * 128 + ch * 8;
       }
       const int so = (buf * kAttnTile + kr) * 128 + ((ch ^ (kr & 7)) * 8);
       cp_async16_zfill(sK + so, a.k_pool + off, valid);
       cp_async16_zfill(sV + so, a.v_pool + off, valid);
     }
   };
-  const int ntiles = (k1 - k0 + kAttnTile - 1) / kAttnTile;
+  static_assert(kAttnStages == 2, "one tile is requested ahead of the loop");
   // exactly kAttnStages - 1 groups before the loop and one per iteration, so
   // that waiting for all but the newest kAttnStages - 1 completes the tile
-#pragma unroll
-  for (int i = 0; i < kAttnStages - 1; i++) {
-    if (i < ntiles) load_tile(i, i);
-    cp_async_commit();
+  if (!tree && k1 > k0) load_tile(0, 0);
+  cp_async_commit();
+  pdl_wait();
+  stamp(0);
+  {
+    const int ctx = a.ctx[r];
+    int lo = 0, hi = 0;
+    if (!a.req_ok[r]) {
+      lo = hi = 0;
+    } else if (tree) {
+      lo = ctx;
+      hi = ctx + Mr;
+    } else {
+      prefix_range(ctx, lo, hi);
+    }
+    if (lo != k0 || hi != k1 || tree) {
+      // the tree split (its keys were just written), or a request whose range
+      // differs from the one requested early: start over
+      cp_async_wait<0>();
+      k0 = lo;
+      k1 = hi;
+      if (k1 > k0) load_tile(0, 0);
+      cp_async_commit();
+    }
   }
+  const uint64_t anc0 = v0 ? a.anc[node0 + n0] : 0ull, anc1 = v1 ? a.anc[node0 + n1] : 0ull;
+  const int ntiles = (k1 - k0 + kAttnTile - 1) / kAttnTile;
 
   uint32_t qa[8][4];
   {
@@ -313,7 +338,7 @@ __global__ void __launch_bounds__(128) k_attn(AttnKernelArgs ka) {
           const int rr = e >> 1;
           const int t = tb + nt * 8 + 2 * q + (e & 1);
           bool ok = t < k1 && (rr ? v1 : v0);
-          if (tree && ok) ok = ((rr ? anc1 : anc0) >> (t - ctx)) & 1ull;
+          if (tree && ok) ok = ((rr ? anc1 : anc0) >> (t - k0)) & 1ull;  // the tree split starts at ctx
           s[nt][e] = ok ? s[nt][e] * sl2 : -INFINITY;
           mx[rr] = fmaxf(mx[rr], s[nt][e]);
         }

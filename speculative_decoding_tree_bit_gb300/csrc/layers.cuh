@@ -44,8 +44,10 @@ struct AttnArgs {
   const uint16_t* v_pool;
   const int32_t* page_table;
   int32_t max_pages, page_size, hq, hkv;
+  int32_t n_pages;          // physical pages in the pool (page ids read before validation are checked)
   const int32_t* cu;       // [R+1]
   const int32_t* ctx;      // ctx_snap [R]
+  const int32_t* ctx_in;   // [R] the context lengths as passed in (not written before the step's commit)
   const uint64_t* anc;     // [rows]
   const int32_t* row_req;  // [rows]
   const int32_t* req_ok;   // [R]: requests whose tree failed validation read no keys

@@ -271,7 +271,10 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   if ((rc = get_map(m->map_act, m->act, m->max_rows, m->I, rows, &mc))) return rc;
 
   const StepRows sr{m->ctx_snap, m->req_ok, m->pos, m->slotv, m->req, m->depth, m->anc};
-  LK(SD_K_TREE, launch_tree(io.tokens, io.parents, m->cu, io.R, io.cv, m->V, m->cfg.max_positions, sr, m->status, s, pdl));
+  // the step's first kernel starts only after the previous step (its KV
+  // commit) is complete: later kernels of the step may read the committed
+  // prefix before their programmatic-launch wait
+  LK(SD_K_TREE, launch_tree(io.tokens, io.parents, m->cu, io.R, io.cv, m->V, m->cfg.max_positions, sr, m->status, s, false));
   LK(SD_K_NORM, launch_rmsnorm(nullptr, m->layers[0].attn_norm, rows, m->H, m->cfg.rms_eps, m->xn, io.tokens, m->w.embed, m->x,
                     m->req, m->req_ok, s, pdl));
 
@@ -323,6 +326,8 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
       aa.hkv = m->Hkv;
       aa.cu = m->cu;
       aa.ctx = m->ctx_snap;
+      aa.ctx_in = io.cv.ctx_len;
+      aa.n_pages = io.cv.n_pages;
       aa.anc = m->anc;
       aa.row_req = m->req;
       aa.req_ok = m->req_ok;
