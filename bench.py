@@ -461,6 +461,9 @@ def gpu_arm(args, rank, world, dist):
         per_layer = 1 if args.chain else 4
         first = 2 + (shape.n_layers // 2) * 5 if not args.chain else shape.n_layers // 2
         chain_phases = [chain_phase_summary(model, first + i) for i in range(per_layer)]
+        if not args.chain and shape.n_rec == 0:
+            # trace records: layer 0's q/k/v, then per layer attention, o, gate/up, down, next q/k/v
+            chain_phases.append(attention_trace_summary(model, 1 + (shape.n_layers // 2) * 5))
     elif args.timeline:
         # launches of more than 128 rows record only the attention launches
         chain_phases = [attention_trace_summary(model, shape.n_layers // 2)]

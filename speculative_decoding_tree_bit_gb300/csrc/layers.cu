@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
   uint16_t* sK = reinterpret_cast<uint16_t*>(smem_attn);
   uint16_t* sV = sK + kAttnStages * kAttnTile * 128;
   __shared__ int s_last;
+  __shared__ int s_tree_page[64];  // the tree split's page ids, read before the wait
   const int sp = blockIdx.x;
   const int h = blockIdx.y % a.hkv, rc = blockIdx.y / a.hkv;
   const int r = blockIdx.z;
@@ -228,8 +229,16 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
     hi = (int)((int64_t)(sp + 1) * c / a.splits);
   };
   int k0 = 0, k1 = 0;
-  const int ctx_pre = tree ? 0 : a.ctx_in[r];
-  if (!tree) prefix_range(ctx_pre, k0, k1);
+  const int ctx_pre = a.ctx_in[r];
+  if (!tree) {
+    prefix_range(ctx_pre, k0, k1);
+  } else if (threadIdx.x < 64) {
+    // the tree's own keys (slots ctx .. ctx + M - 1) are written by the q/k/v
+    // GEMM, so only their page ids can be looked up before the wait
+    const int t = ctx_pre + threadIdx.x;
+    s_tree_page[threadIdx.x] = ctx_pre >= 0 && t < cap ? a.page_table[(int64_t)r * a.max_pages + t / a.page_size] : -1;
+  }
+  bool spage = false;  // the tree tile takes its page ids from s_tree_page
   bool has_rows = rt * 16 < rows;
   // this lane's two query rows
   const int rho0 = rt * 16 + g, rho1 = rho0 + 8;
@@ -247,7 +256,7 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
       int64_t off = 0;
       if (valid) {
         // page ids may be read before the tree kernel validated them
-        const int page = a.page_table[(int64_t)r * a.max_pages + t / a.page_size];
+        const int page = spage ? s_tree_page[t - k0] : a.page_table[(int64_t)r * a.max_pages + t / a.page_size];
         valid = page >= 0 && page < a.n_pages;
         if (valid) off = ((int64_t)page * a.hkv + h) * head_stride + (int64_t)(t % a.page_size) * 128 + ch * 8;
       }
@@ -280,8 +289,11 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
       cp_async_wait<0>();
       k0 = lo;
       k1 = hi;
+      spage = tree && ctx == ctx_pre && hi - lo <= 64;
+      if (spage) __syncthreads();  // s_tree_page written by other threads
       if (k1 > k0) load_tile(0, 0);
       cp_async_commit();
+      spage = false;
     }
   }
   const uint64_t anc0 = v0 ? a.anc[node0 + n0] : 0ull, anc1 = v1 ? a.anc[node0 + n1] : 0ull;
@@ -496,18 +508,27 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
     mlsm[i * kMaxParts + p] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + ((gbase + p) * ka.rpg + rbeg + i) * 2));
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < nrow; i += 128) {
-    const float2* ml = mlsm + i * kMaxParts;
-    float mx = -INFINITY;
-    for (int p = 0; p < P; p++) mx = fmaxf(mx, ml[p].x);
-    float L = 0.f;
-    for (int p = 0; p < P; p++) {
-      const float w = ml[p].x == -INFINITY ? 0.f : exp2f(ml[p].x - mx);
-      wsm[i * kMaxParts + p] = w;
-      L += w * ml[p].y;
+  {
+    // one warp per row, lanes over the splits (butterfly reductions: a fixed
+    // order, deterministic)
+    const int wp = threadIdx.x >> 5, ln = threadIdx.x & 31;
+    for (int i = wp; i < nrow; i += 4) {
+      const float2* ml = mlsm + i * kMaxParts;
+      float mx = -INFINITY;
+      for (int p = ln; p < P; p += 32) mx = fmaxf(mx, ml[p].x);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      float L = 0.f;
+      for (int p = ln; p < P; p += 32) {
+        const float w = ml[p].x == -INFINITY ? 0.f : exp2f(ml[p].x - mx);
+        wsm[i * kMaxParts + p] = w;
+        L += w * ml[p].y;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (int p = ln; p < P; p += 32) wsm[i * kMaxParts + p] *= inv;
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int p = 0; p < P; p++) wsm[i * kMaxParts + p] *= inv;
   }
   __syncthreads();
   // slice = (row, 4 dims): 32 slices per row.  With few rows per CTA (the
