@@ -466,11 +466,12 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
   int32_t* gc = a.tickets + (((int64_t)r * a.hkv + h) * ka.chunks + rc) * 2;
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const int old = atomicAdd(gc, 1);
     if (ka.coop) {
-      // wait (bounded) for the group's other splits
-      int v = old + 1;
+      // a release add (this CTA's partial, ordered before it by the
+      // barrier, becomes visible with it; no value comes back), then wait
+      // (bounded) for the group's other splits
+      asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(gc) : "memory");
+      int v = 0;
       const uint64_t t0 = globaltimer();
       while (v < P) {
         if (globaltimer() - t0 > kWaitLimitNs) {
@@ -481,10 +482,12 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
       }
       s_last = 1;
     } else {
+      __threadfence();
+      const int old = atomicAdd(gc, 1);
       s_last = old == P - 1;
       if (s_last) *gc = 0;
+      __threadfence();
     }
-    __threadfence();
   }
   __syncthreads();
   stamp(2);
