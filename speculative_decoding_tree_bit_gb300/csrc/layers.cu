@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
   uint16_t* sK = reinterpret_cast<uint16_t*>(smem_attn);
   uint16_t* sV = sK + kAttnStages * kAttnTile * 128;
   __shared__ int s_last;
-  __shared__ int s_tree_page[64];  // the tree split's page ids, read before the wait
+  __shared__ int s_pg[64];  // page ids of the split's key range (pages pg0 .. pg0 + npg - 1), read before the wait
   const int sp = blockIdx.x;
   const int h = blockIdx.y % a.hkv, rc = blockIdx.y / a.hkv;
   const int r = blockIdx.z;
@@ -230,15 +230,26 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
   };
   int k0 = 0, k1 = 0;
   const int ctx_pre = a.ctx_in[r];
-  if (!tree) {
-    prefix_range(ctx_pre, k0, k1);
-  } else if (threadIdx.x < 64) {
-    // the tree's own keys (slots ctx .. ctx + M - 1) are written by the q/k/v
-    // GEMM, so only their page ids can be looked up before the wait
-    const int t = ctx_pre + threadIdx.x;
-    s_tree_page[threadIdx.x] = ctx_pre >= 0 && t < cap ? a.page_table[(int64_t)r * a.max_pages + t / a.page_size] : -1;
+  if (!tree) prefix_range(ctx_pre, k0, k1);
+  // the page ids of the split's keys are staged once, before the wait (the
+  // tree's own keys, slots ctx .. ctx + M - 1, are written by the q/k/v GEMM,
+  // but their page ids are known); a range of more than 64 pages looks its
+  // ids up per key
+  int pg0 = 0, npg = 0;
+  {
+    int lo = k0, hi = k1;
+    if (tree) {
+      lo = ctx_pre < 0 ? 0 : (ctx_pre > cap ? cap : ctx_pre);
+      hi = lo + Mr > cap ? cap : lo + Mr;
+    }
+    if (hi > lo) {
+      pg0 = lo / a.page_size;
+      npg = (hi - 1) / a.page_size - pg0 + 1;
+      if (npg > 64) npg = 0;
+    }
+    if (threadIdx.x < npg) s_pg[threadIdx.x] = a.page_table[(int64_t)r * a.max_pages + pg0 + threadIdx.x];
+    __syncthreads();
   }
-  bool spage = false;  // the tree tile takes its page ids from s_tree_page
   bool has_rows = rt * 16 < rows;
   // this lane's two query rows
   const int rho0 = rt * 16 + g, rho1 = rho0 + 8;
@@ -256,7 +267,8 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
       int64_t off = 0;
       if (valid) {
         // page ids may be read before the tree kernel validated them
-        const int page = spage ? s_tree_page[t - k0] : a.page_table[(int64_t)r * a.max_pages + t / a.page_size];
+        const int pi = t / a.page_size - pg0;
+        const int page = (pi >= 0 && pi < npg) ? s_pg[pi] : a.page_table[(int64_t)r * a.max_pages + t / a.page_size];
         valid = page >= 0 && page < a.n_pages;
         if (valid) off = ((int64_t)page * a.hkv + h) * head_stride + (int64_t)(t % a.page_size) * 128 + ch * 8;
       }
@@ -287,13 +299,11 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
       // the tree split (its keys were just written), or a request whose range
       // differs from the one requested early: start over
       cp_async_wait<0>();
+      if (!(tree && ctx == ctx_pre)) npg = 0;  // staged page ids belong to another range
       k0 = lo;
       k1 = hi;
-      spage = tree && ctx == ctx_pre && hi - lo <= 64;
-      if (spage) __syncthreads();  // s_tree_page written by other threads
       if (k1 > k0) load_tile(0, 0);
       cp_async_commit();
-      spage = false;
     }
   }
   const uint64_t anc0 = v0 ? a.anc[node0 + n0] : 0ull, anc1 = v1 ? a.anc[node0 + n1] : 0ull;
@@ -511,9 +521,24 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
     mlsm[i * kMaxParts + p] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + ((gbase + p) * ka.rpg + rbeg + i) * 2));
   }
   __syncthreads();
-  {
-    // one warp per row, lanes over the splits (butterfly reductions: a fixed
-    // order, deterministic)
+  if (P <= 16) {
+    // few splits (many requests): one thread per row
+    for (int i = threadIdx.x; i < nrow; i += 128) {
+      const float2* ml = mlsm + i * kMaxParts;
+      float mx = -INFINITY;
+      for (int p = 0; p < P; p++) mx = fmaxf(mx, ml[p].x);
+      float L = 0.f;
+      for (int p = 0; p < P; p++) {
+        const float w = ml[p].x == -INFINITY ? 0.f : exp2f(ml[p].x - mx);
+        wsm[i * kMaxParts + p] = w;
+        L += w * ml[p].y;
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (int p = 0; p < P; p++) wsm[i * kMaxParts + p] *= inv;
+    }
+  } else {
+    // many splits: one warp per row, lanes over the splits (butterfly
+    // reductions: a fixed order, deterministic)
     const int wp = threadIdx.x >> 5, ln = threadIdx.x & 31;
     for (int i = wp; i < nrow; i += 4) {
       const float2* ml = mlsm + i * kMaxParts;
