@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--nvtx", action="store_true", help="wrap the timed steps in the NVTX range 'sdv_step'")
     ap.add_argument("--probe", default=None, metavar="N,K,M",
                     help="time the fused W12 linear alone on an N x K tensor with M rows")
+    ap.add_argument("--tc-min-rows", type=int, default=0,
+                    help="rows per launch from which GEMMs run on the tcgen05 kernel (0: the library default)")
     return ap.parse_args()
 
 
@@ -71,6 +73,7 @@ def probe_arm(args):
     from speculative_decoding_tree_bit_gb300 import _build
     from speculative_decoding_tree_bit_gb300 import model as Mdl
     _build.build()
+    tc_rows = Mdl.set_tc_min_rows(args.tc_min_rows)
     N, K, M = (int(v) for v in args.probe.split(","))
     w = synthetic.normal_bf16(synthetic.key(args.seed, 4242), N * K, 0.02).reshape(N, K)
     p = Mdl.pack(Mdl.to_device_u16(w))
@@ -101,7 +104,7 @@ def probe_arm(args):
     del y
     nbytes = p.nbytes() + M * K * 2 + M * N * 2
     pk, src = peaks()
-    return {"probe": "sd_w12_linear", "N": N, "K": K, "M": M, "us_per_launch": us,
+    return {"probe": "sd_w12_linear", "N": N, "K": K, "M": M, "tc_min_rows": tc_rows, "us_per_launch": us,
             "GBps": nbytes / (us * 1e-6) / 1e9, "frac_of_peak": nbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"],
             "peak_source": src, "bytes": nbytes, "escapes": p.n_escapes}
 
@@ -324,6 +327,7 @@ def gpu_arm(args, rank, world, dist):
     _build.build()
     local = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(local)
+    tc_rows = Mdl.set_tc_min_rows(args.tc_min_rows)
     spec = wl.make(args.workload, args.seed)
     shape, R = spec.shape, spec.R
     ctx = max(spec.ctx)
@@ -519,7 +523,7 @@ def gpu_arm(args, rank, world, dist):
         "verify_step_us": ms * 1e3, "host_submit_us_per_step": t_host * 1e6, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "model": shape.name, "layers": shape.n_layers, "M": M,
-                   "requests": R, "gemm_chain": bool(args.chain),
+                   "requests": R, "gemm_chain": bool(args.chain), "tc_min_rows": tc_rows,
                    "max_depth": spec.max_depth, "ctx": ctx, "p_copy": spec.p, "accepted_len": acc_len,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (packed weights %.1f GB)" % (model.packed_bytes / 1e9)},

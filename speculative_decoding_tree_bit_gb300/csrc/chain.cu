@@ -199,7 +199,8 @@ __device__ __forceinline__ void chain_produce(const ChainArgs& a, uint8_t* sx, u
     const Phase& P = a.ph[p];
     if (P.type != PH_GEMM) continue;
     const GemmParams& g = P.g;
-    const int64_t u0 = (int64_t)blockIdx.x * g.U / G, u1 = (int64_t)(blockIdx.x + 1) * g.U / G;
+    int64_t u0, u1;
+    unit_range(g, u0, u1);
     if (u1 <= u0) continue;
     int b = (int)(u0 / g.KT), t = (int)(u0 % g.KT);
     for (int64_t i = u0; i < u1; i++) {
@@ -435,6 +436,9 @@ int chain_launch(const ChainPhaseDesc* ph, int n, int M, const GemmWorkspace& ws
       }
       int rc = make_gemm_params(&P.g, *ph[i].W, ph[i].x, M, ph[i].epi, ws, status);
       if (rc) return rc;
+      // the same partition of the units as the phase's own launch would use
+      // (same contributors per row block: the same bits)
+      P.g.G = gemm_launch_grid(*ph[i].W, M, ph[i].epi.epi);
       if (ws.counters_len < P.g.NB) {
         set_error("chain: workspace counters too small");
         return SD_ERR_WORKSPACE;

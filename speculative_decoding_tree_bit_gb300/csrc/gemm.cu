@@ -60,8 +60,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
   float* corr = reinterpret_cast<float*>(smem + C::OFF_CORR);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t G = gridDim.x;
-  const int64_t u0 = (int64_t)blockIdx.x * p.U / G, u1 = (int64_t)(blockIdx.x + 1) * p.U / G;
+  const int64_t G = gridDim.x;  // trace layout [4][grid]
+  int64_t u0, u1;
+  unit_range(p, u0, u1);
   const int KT = p.KT;
 
   if (threadIdx.x == 0) {
@@ -326,6 +327,7 @@ int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, c
   const int prc = make_gemm_params(&p, W, x, M, epi, ws, status);
   if (prc) return prc;
   p.trace = M <= 128 ? trace : nullptr;
+  p.G = grid;
   if (ws.counters_len < p.NB) {
     set_error("gemm: workspace counters too small");
     return SD_ERR_WORKSPACE;

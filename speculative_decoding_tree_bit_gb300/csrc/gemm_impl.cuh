@@ -49,7 +49,17 @@ struct GemmParams {
   GemmEpilogue e;
   int32_t* status;
   uint64_t* trace;  // optional: [4][grid] device-clock stamps (start, first stage ready, last consumed, finished)
+  int64_t G;        // CTAs sharing the units (<= the grid; 0: the grid); CTAs beyond it have no work
 };
+
+// This CTA's stream-K unit range [u0, u1) and the number of CTAs sharing
+// the units.
+__device__ __forceinline__ int64_t unit_ctas(const GemmParams& p) { return p.G > 0 ? p.G : (int64_t)gridDim.x; }
+__device__ __forceinline__ void unit_range(const GemmParams& p, int64_t& u0, int64_t& u1) {
+  const int64_t G = unit_ctas(p), c = blockIdx.x;
+  u0 = c < G ? c * p.U / G : p.U;
+  u1 = c < G ? (c + 1) * p.U / G : p.U;
+}
 
 __device__ __forceinline__ uint32_t lut_exp(uint32_t c, const uint32_t* tab) {
   const uint32_t lo = __byte_perm(tab[0], tab[1], c & 7);
@@ -256,8 +266,8 @@ __device__ __forceinline__ bool escape_segments(const GemmParams& p, const uint8
   using C = Cfg<NT>;
   constexpr int MP = C::MP;
   const int lane = threadIdx.x & 31;
-  const int64_t G = gridDim.x;
-  const int64_t u0 = (int64_t)blockIdx.x * p.U / G, u1 = (int64_t)(blockIdx.x + 1) * p.U / G;
+  int64_t u0, u1;
+  unit_range(p, u0, u1);
   if (u1 <= u0) return true;
   const int KT = p.KT;
   const int b_first = (int)(u0 / KT), b_last = (int)((u1 - 1) / KT);
@@ -364,8 +374,9 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
                                              uint64_t* corr_empty, int& cseg, volatile int* abort,
                                              uint64_t* stamps = nullptr, int64_t stride = 0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t G = gridDim.x;
-  const int64_t u0 = (int64_t)blockIdx.x * p.U / G, u1 = (int64_t)(blockIdx.x + 1) * p.U / G;
+  const int64_t G = unit_ctas(p);
+  int64_t u0, u1;
+  unit_range(p, u0, u1);
   const int KT = p.KT;
   // small tiles: even and odd sub-tiles feed separate accumulators so that
   // consecutive MMAs do not wait on each other; larger tiles have NT
