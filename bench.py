@@ -460,7 +460,7 @@ def gpu_arm(args, rank, world, dist):
     torch.cuda.synchronize()
     tl = model.timeline()
     chain_phases = None
-    if args.timeline and M <= 128:
+    if args.timeline and M < tc_rows:
         # the middle layer's launches (a chain, or its four GEMMs after its attention)
         per_layer = 1 if args.chain else 4
         first = 2 + (shape.n_layers // 2) * 5 if not args.chain else shape.n_layers // 2
@@ -469,11 +469,11 @@ def gpu_arm(args, rank, world, dist):
             # trace records: layer 0's q/k/v, then per layer attention, o, gate/up, down, next q/k/v
             chain_phases.append(attention_trace_summary(model, 1 + (shape.n_layers // 2) * 5))
     elif args.timeline:
-        # launches of more than 128 rows record only the attention launches
+        # tcgen05 GEMM launches are not traced: only the attention launches are
         chain_phases = [attention_trace_summary(model, shape.n_layers // 2)]
     model.set_timing(False)
     overlap = None
-    if args.timeline and not args.chain and M <= 128 and shape.n_rec == 0:
+    if args.timeline and not args.chain and M < tc_rows and shape.n_rec == 0:
         overlap = overlapped_layer_trace(model, stream, step, shape.n_layers // 2)
 
     if dist is not None:

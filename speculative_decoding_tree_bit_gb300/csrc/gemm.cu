@@ -169,8 +169,10 @@ int pad_rows(int M) { return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 
 
 static int nt_of(int M) { return M > 128 ? 16 : pad_rows(M) / 8; }
 
-// Default crossover of the two kernels (rows per launch).
-constexpr int kTcMinRowsDefault = 129;
+// Default crossover of the two kernels (rows per launch): the batched step
+// of the 8B-class decoder runs faster on the warp-level kernel at 64 rows
+// and on the tcgen05 kernel at 128.
+constexpr int kTcMinRowsDefault = 65;
 static int g_tc_min_rows = kTcMinRowsDefault;
 
 int gemm_tc_min_rows() { return g_tc_min_rows; }

@@ -95,7 +95,7 @@ def test_repeat_calls_are_deterministic_with_dirty_workspace(M):
 @pytest.fixture()
 def tc_all(M):
     """Every launch on the tcgen05 kernel (default: only launches of more
-    than 128 rows), restored afterwards."""
+    than 64 rows), restored afterwards."""
     M.set_tc_min_rows(1)
     yield M
     M.set_tc_min_rows(0)
