@@ -338,7 +338,8 @@ int sd_model_last_launches(sd_model* m);
 int sd_model_set_graphs(sd_model* m, int32_t enable);
 
 /* GEMM chaining (no counterpart in the pages: an execution choice of this
- * library).  With enable = 1 (default 0) and at most 128 rows per step,
+ * library).  With enable = 1 (default 0) and fewer rows per step than the
+ * tcgen05 threshold (sd_gemm_set_tc_min_rows; at most 128),
  * each run of GEMMs and RMSNorms between two attention / recurrence kernels
  * (O + residual, RMSNorm, gate/up + SiLU, down + residual, RMSNorm, the next
  * layer's q/k/v or the lm_head) is executed by one persistent kernel whose
@@ -353,7 +354,8 @@ int sd_model_set_chain(sd_model* m, int32_t enable);
 
 /* Raw device-clock stamps (%globaltimer, ns) of traced launch `launch` (0 =
  * the first) of the last timed step - every chain launch, every lone GEMM
- * launch of at most 128 rows and every attention launch as a one-phase
+ * launch on the warp-level kernel (fewer rows than the tcgen05 threshold)
+ * and every attention launch as a one-phase
  * record (attention rows: start, keys done, group's partials ready, end):
  * *n_phases = n, *n_ctas = G
  * and, when stamps_host is not NULL (room for max_stamps >= (1 + 3n) G
@@ -392,7 +394,7 @@ int sd_model_set_timing(sd_model* m, int32_t enable);
  * ms_host[i] (event-measured duration) and bytes_host[i] (algorithmic bytes
  * of a GEMM: packed words, escape tile index, activations read and written;
  * 0 for other kinds).  Each traced launch (every SD_K_GEMM_CHAIN entry, and
- * each lone GEMM of at most 128 rows) is followed by one entry per phase
+ * each lone warp-level GEMM) is followed by one entry per phase
  * with kind 100 + the phase's kind (SD_K_GEMM_O, SD_K_NORM, ...): its time
  * runs from the last CTA finishing the previous phase (the first CTA
  * starting, for the first phase) to the last CTA finishing this one, read
