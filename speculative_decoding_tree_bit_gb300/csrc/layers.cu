@@ -726,33 +726,48 @@ cudaError_t launch_linrec(const LinrecArgs& a, cudaStream_t s, bool pdl) {
 
 // --------------------------------------------------- argmax + accept -----
 
-__global__ void k_accept(AcceptArgs a) {
+__global__ void __launch_bounds__(512) k_accept(AcceptArgs a) {
   pdl_launch();  // the next kernel may start streaming its (independent) weights now
   pdl_wait();
   __shared__ int am[64], par[64], dep[64], okn[64], pth[65];
   const int r = blockIdx.x;
   const int node0 = a.cu ? a.cu[r] : 0, Mr = a.cu ? a.cu[r + 1] - node0 : a.single_M;
   const int i = threadIdx.x;
-  if (i < Mr && i < 64) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // per node: the argmax over the GEMM's per-CTA partials, one warp per node
+  // with the lanes over the partials (larger value, then smaller index: a
+  // total order, so the reduction order does not matter)
+  for (int n = warp; n < Mr && n < 64; n += 16) {
     int best;
     if (a.amax_val) {
       float v = -INFINITY;
       best = 0x7FFFFFFF;
-      for (int c = 0; c < a.n_part; c++) {
-        const float ov = a.amax_val[(int64_t)c * a.ld + node0 + i];
-        const int oi = a.amax_idx[(int64_t)c * a.ld + node0 + i];
+      for (int c = lane; c < a.n_part; c += 32) {
+        const float ov = a.amax_val[(int64_t)c * a.ld + node0 + n];
+        const int oi = a.amax_idx[(int64_t)c * a.ld + node0 + n];
+        if (ov > v || (ov == v && oi < best)) {
+          v = ov;
+          best = oi;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, best, off);
         if (ov > v || (ov == v && oi < best)) {
           v = ov;
           best = oi;
         }
       }
     } else {
-      best = a.argmax_in[node0 + i];
+      best = a.argmax_in[node0 + n];
     }
-    am[i] = best;
-    if (a.argmax_out) a.argmax_out[node0 + i] = best;
-    par[i] = a.parents[node0 + i];
+    if (lane == 0) {
+      am[n] = best;
+      if (a.argmax_out) a.argmax_out[node0 + n] = best;
+    }
   }
+  if (i < Mr && i < 64) par[i] = a.parents[node0 + i];
   __syncthreads();
   if (i != 0) return;
   bool valid = Mr >= 1 && Mr <= 64 && (a.req_ok ? a.req_ok[r] != 0 : true);
@@ -785,7 +800,7 @@ __global__ void k_accept(AcceptArgs a) {
 }
 
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s, bool pdl) {
-  return launch(k_accept, dim3(a.R), dim3(64), 0, s, pdl, a);
+  return launch(k_accept, dim3(a.R), dim3(512), 0, s, pdl, a);
 }
 
 // ------------------------------------------------------------- commit ----
