@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
       int64_t issued = 0;
       if (n > 0) {
         const int pre = (int)(n < C::S ? n : C::S);
-        int b = (int)(u0 / KT), t = (int)(u0 % KT);
+        int b = (int)udiv(u0, KT), t = (int)(u0 - (int64_t)b * KT);
         const int t_first = t;
         // one 2-D box per stage: 8 strips x 1536 bytes (ragged row blocks are
         // zero-filled by the copy engine and never read)

@@ -52,13 +52,21 @@ struct GemmParams {
   int64_t G;        // CTAs sharing the units (<= the grid; 0: the grid); CTAs beyond it have no work
 };
 
+// n / d for 0 <= n and 0 < d: one 32-bit division when both fit (a 64-bit
+// division is a long software sequence, and the unit bookkeeping of every
+// realistic shape fits in 32 bits).
+__device__ __forceinline__ int64_t udiv(int64_t n, int64_t d) {
+  if ((((uint64_t)n | (uint64_t)d) >> 32) == 0) return (int64_t)((uint32_t)n / (uint32_t)d);
+  return (int64_t)((uint64_t)n / (uint64_t)d);
+}
+
 // This CTA's stream-K unit range [u0, u1) and the number of CTAs sharing
 // the units.
 __device__ __forceinline__ int64_t unit_ctas(const GemmParams& p) { return p.G > 0 ? p.G : (int64_t)gridDim.x; }
 __device__ __forceinline__ void unit_range(const GemmParams& p, int64_t& u0, int64_t& u1) {
   const int64_t G = unit_ctas(p), c = blockIdx.x;
-  u0 = c < G ? c * p.U / G : p.U;
-  u1 = c < G ? (c + 1) * p.U / G : p.U;
+  u0 = c < G ? udiv(c * p.U, G) : p.U;
+  u1 = c < G ? udiv((c + 1) * p.U, G) : p.U;
 }
 
 __device__ __forceinline__ uint32_t lut_exp(uint32_t c, const uint32_t* tab) {
@@ -270,11 +278,11 @@ __device__ __forceinline__ bool escape_segments(const GemmParams& p, const uint8
   unit_range(p, u0, u1);
   if (u1 <= u0) return true;
   const int KT = p.KT;
-  const int b_first = (int)(u0 / KT), b_last = (int)((u1 - 1) / KT);
+  const int b_first = (int)udiv(u0, KT), b_last = (int)udiv(u1 - 1, KT);
   const bool any = p.tile_ptr != nullptr;
   const int mrows = min(MP, p.M - p.m0);
-  auto tbeg = [&](int b) { return b == b_first ? (int)(u0 % KT) : 0; };
-  auto tend = [&](int b) { return b == b_last ? (int)((u1 - 1) % KT) + 1 : KT; };
+  auto tbeg = [&](int b) { return b == b_first ? (int)(u0 - (int64_t)b_first * KT) : 0; };
+  auto tend = [&](int b) { return b == b_last ? (int)(u1 - 1 - (int64_t)b_last * KT) + 1 : KT; };
   bool ok = true;
   EscChunk cur{}, nxt{};
   int cb = b_first, ctc = tbeg(b_first), seg_b = -1;
@@ -392,7 +400,7 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
       bestv[nt][c] = -INFINITY;
       besti[nt][c] = 0x7FFFFFFF;
     }
-  const int first_b = u1 > u0 ? (int)(u0 / KT) : -1;
+  const int first_b = u1 > u0 ? (int)udiv(u0, KT) : -1;
 
   auto zero = [&]() {
 #pragma unroll
@@ -451,8 +459,8 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
       if (!*flag) return;
       zero();
       // contributors: the CTAs whose (non-empty) unit range meets row block b
-      const int64_t c_first = (((int64_t)b * KT + 1) * G - 1) / p.U;
-      const int64_t c_last = (((int64_t)(b + 1) * KT) * G - 1) / p.U;
+      const int64_t c_first = udiv(((int64_t)b * KT + 1) * G - 1, p.U);
+      const int64_t c_last = udiv(((int64_t)(b + 1) * KT) * G - 1, p.U);
       // partial slots of the contributors, read kBatch at a time with all
       // loads in flight before any is used (CTA order kept: deterministic)
       constexpr int kBatch = NT <= 2 ? 4 : 2;
@@ -462,9 +470,10 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
 #pragma unroll
         for (int u = 0; u < kBatch; u++) {
           const int64_t c = c0 + u;
-          const int64_t cs = c * p.U / G, ce = (c + 1) * p.U / G;
+          const int64_t cs = udiv(c * p.U, G), ce = udiv((c + 1) * p.U, G);
           use[u] = c <= c_last && cs != ce;  // empty ranges never wrote a partial
-          const float* src = partial_ptr(use[u] ? c : blockIdx.x, (use[u] && b != (int)(cs / KT)) ? 1 : 0);
+          // slot 1 when the contributor's range began in an earlier block
+          const float* src = partial_ptr(use[u] ? c : blockIdx.x, (use[u] && cs < (int64_t)b * KT) ? 1 : 0);
 #pragma unroll
           for (int nt = 0; nt < NT; nt++)
             v[u][nt] = use[u] ? __ldcg(reinterpret_cast<const float4*>(src + nt * 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -487,7 +496,7 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
   zero();
   int cur_b = -1, seg_t0 = 0;
   bool ok = true;
-  int b = u1 > u0 ? (int)(u0 / KT) : 0, t = u1 > u0 ? (int)(u0 % KT) : 0;
+  int b = u1 > u0 ? (int)udiv(u0, KT) : 0, t = u1 > u0 ? (int)(u0 - (int64_t)b * KT) : 0;
   for (int64_t n = u1 - u0; n > 0; --n) {
     if (b != cur_b) {
       if (cur_b >= 0) finish(cur_b, seg_t0, KT);
@@ -543,7 +552,7 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
     }
   }
   if (stamps && threadIdx.x == 0) stamps[stride] = globaltimer();
-  if (cur_b >= 0) finish(cur_b, seg_t0, (int)((u1 - 1) % KT) + 1);
+  if (cur_b >= 0) finish(cur_b, seg_t0, (int)(u1 - 1 - udiv(u1 - 1, KT) * KT) + 1);
 
   if (p.e.epi == EPI_LOGITS) {
 #pragma unroll

@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
-  const int64_t u0 = (int64_t)blockIdx.x * p.U / G, u1 = (int64_t)(blockIdx.x + 1) * p.U / G;
+  const int64_t u0 = udiv((int64_t)blockIdx.x * p.U, G), u1 = udiv((int64_t)(blockIdx.x + 1) * p.U, G);
   const int64_t n_units = u1 - u0;
   const int KT = p.KT;
   const int XB = P.MP * 128;
@@ -338,9 +338,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       if (n_units > 0) {
         const int pre = (int)min64(n_units, P.SW);
         for (int i = 0; i < pre; i++) {
-          const int64_t u = u0 + i;
+          const int64_t u = u0 + i, ub = udiv(u, KT);
           mbar_arrive_expect_tx(&wfull[i], tc::kWTile);
-          tma2d_g2s(sw + i * tc::kWTile, &wmap, (int)(u % KT) * 192, (int)(u / KT) * kRB, &wfull[i]);
+          tma2d_g2s(sw + i * tc::kWTile, &wmap, (int)(u - ub * KT) * 192, (int)ub * kRB, &wfull[i]);
         }
         nw = pre;
         pdl_wait();  // activations come from the previous kernel
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&xfull[xs], (uint32_t)XB);
-          tma2d_g2s(sx + xs * XB, &xmap, (int)(u % KT) * 64, 0, &xfull[xs]);
+          tma2d_g2s(sx + xs * XB, &xmap, (int)(u - udiv(u, KT) * KT) * 64, 0, &xfull[xs]);
           nx++;
           if (++xs == P.S) {
             xs = 0;
@@ -365,9 +365,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
               set_status(p.status, SD_TIMEOUT_AT(22));
               break;
             }
-            const int64_t uj = u0 + j;
+            const int64_t uj = u0 + j, ujb = udiv(uj, KT);
             mbar_arrive_expect_tx(&wfull[ws], tc::kWTile);
-            tma2d_g2s(sw + ws * tc::kWTile, &wmap, (int)(uj % KT) * 192, (int)(uj / KT) * kRB, &wfull[ws]);
+            tma2d_g2s(sw + ws * tc::kWTile, &wmap, (int)(uj - ujb * KT) * 192, (int)ujb * kRB, &wfull[ws]);
             nw++;
           }
           if (++ws == P.SW) {
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       const uint32_t a0 = smem_u32(sa), x0 = smem_u32(sx);
       while (i < n_units) {
         const int64_t u = u0 + i;
-        const int t0 = (int)(u % KT);
+        const int t0 = (int)(u - udiv(u, KT) * KT);
         const int len = (int)min64(KT - t0, n_units - i);
         const int buf = seg & 1;
         if (seg >= 2 && !mbar_wait_or_abort(&accempty[buf], (uint32_t)(((seg >> 1) - 1) & 1), abort))
@@ -472,13 +472,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     bar_sync(2, 128);
     const int mrows = P.MP < p.M ? P.MP : p.M;
     const int nch = (mrows + 15) / 16;
-    const int first_b = n_units > 0 ? (int)(u0 / KT) : -1;
+    const int first_b = n_units > 0 ? (int)udiv(u0, KT) : -1;
     uint32_t stg_par = 0;  // bit b: parity of the next phase of staging barrier b
     int64_t i = 0;
     int seg = 0;
     while (i < n_units) {
       const int64_t u = u0 + i;
-      const int b = (int)(u / KT), t0 = (int)(u % KT);
+      const int b = (int)udiv(u, KT), t0 = (int)(u - (int64_t)b * KT);
       const int len = (int)min64(KT - t0, n_units - i);
       const int buf = seg & 1;
       if (!mbar_wait_or_abort(&accfull[buf], (uint32_t)((seg >> 1) & 1), abort))
@@ -515,11 +515,11 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
           // contributors: the CTAs whose (non-empty) unit range meets block b,
           // summed in CTA order; this CTA's own share comes from TMEM (still
           // held)
-          const int64_t c_first = (((int64_t)b * KT + 1) * G - 1) / p.U;
-          const int64_t c_last = (((int64_t)(b + 1) * KT) * G - 1) / p.U;
+          const int64_t c_first = udiv(((int64_t)b * KT + 1) * G - 1, p.U);
+          const int64_t c_last = udiv(((int64_t)(b + 1) * KT) * G - 1, p.U);
           auto other = [&](int64_t cc, int& csid) {  // a contributor whose partial is read
-            const int64_t cs = cc * p.U / G, ce = (cc + 1) * p.U / G;
-            csid = (b != (int)(cs / KT)) ? 1 : 0;
+            const int64_t cs = udiv(cc * p.U, G), ce = udiv((cc + 1) * p.U, G);
+            csid = cs < (int64_t)b * KT ? 1 : 0;  // its range began in an earlier block
             return cs != ce && cc != (int64_t)blockIdx.x;  // empty ranges wrote no partial
           };
           int n_oth = 0;
