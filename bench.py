@@ -61,6 +61,8 @@ def parse():
                     help="time the fused W12 linear alone on an N x K tensor with M rows")
     ap.add_argument("--tc-min-rows", type=int, default=0,
                     help="rows per launch from which GEMMs run on the tcgen05 kernel (0: the library default)")
+    ap.add_argument("--attn-splits", type=int, default=0,
+                    help="prefix key splits of the step's attention per kv head and row chunk (0: automatic)")
     return ap.parse_args()
 
 
@@ -328,6 +330,7 @@ def gpu_arm(args, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(local)
     tc_rows = Mdl.set_tc_min_rows(args.tc_min_rows)
+    attn_splits = Mdl.set_attn_splits(args.attn_splits)
     spec = wl.make(args.workload, args.seed)
     shape, R = spec.shape, spec.R
     ctx = max(spec.ctx)
@@ -524,6 +527,7 @@ def gpu_arm(args, rank, world, dist):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "model": shape.name, "layers": shape.n_layers, "M": M,
                    "requests": R, "gemm_chain": bool(args.chain), "tc_min_rows": tc_rows,
+                   "attn_splits": attn_splits or "auto",
                    "max_depth": spec.max_depth, "ctx": ctx, "p_copy": spec.p, "accepted_len": acc_len,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (packed weights %.1f GB)" % (model.packed_bytes / 1e9)},

@@ -176,6 +176,18 @@ int sd_w12_linear_static(const w12_tensor* W, const uint16_t* x, int32_t M, uint
  * in force.  Not thread-safe against concurrent GEMM calls. */
 int32_t sd_gemm_set_tc_min_rows(int32_t rows);
 
+/* Prefix key splits per (request, kv head, 64-row chunk) of the verify
+ * step's attention ("SpecPilot ...", tree attention: the committed prefix
+ * is split over CTAs and the splits' softmax states are merged; the tree's
+ * own keys are one more split).  splits in 1..64 fixes the count (values
+ * above 64 are clamped; a smaller count may still be taken when the model's
+ * attention workspace holds fewer); splits <= 0 restores the automatic
+ * choice (about two CTAs per SM, at least one split per 512 keys of the
+ * context bound).  Process-wide; applies to steps issued afterwards (a
+ * model re-captures its step graphs).  Returns the value now in force (0:
+ * automatic).  Not thread-safe against concurrent steps. */
+int32_t sd_attn_set_splits(int32_t splits);
+
 /* ------------------------------------------------------ tree helpers -- */
 /* [TREE] Validate one draft tree (parents[0] == -1, 0 <= parents[i] < i,
  * M <= 64) and derive per node the ancestor bitmask anc[i] = anc[parent[i]]

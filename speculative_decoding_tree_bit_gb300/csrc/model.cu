@@ -80,7 +80,12 @@ static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 // warps per SM and shorter key ranges per split pay for the larger merge),
 // and at least one split per 512 keys of the longest possible context (many
 // requests: otherwise each CTA walks a whole context).
+// Prefix key splits per (request, kv head, row chunk): set by
+// sd_attn_set_splits (<= 0: chosen from the grid and the context bound).
+static int g_attn_splits = 0;
+
 static int attn_splits(int R, int hkv, int chunks, int max_keys) {
+  if (g_attn_splits > 0) return g_attn_splits;
   const int ctas = R * hkv * chunks;
   const int by_sms = (2 * num_sms() + ctas - 1) / ctas - 1;
   const int by_keys = (max_keys + 511) / 512;
@@ -450,6 +455,7 @@ static int launch_step(sd_model* m, const StepIO& io, cudaStream_t s, std::vecto
   if (!m->use_graphs || m->timing || m->tracing || s == nullptr) return run_step(m, io, s);
   key.push_back((uintptr_t)m->use_chain);
   key.push_back((uintptr_t)gemm_tc_min_rows());
+  key.push_back((uintptr_t)g_attn_splits);
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   SD_CK(cudaStreamIsCapturing(s, &cs));
   if (cs != cudaStreamCaptureStatusNone) return run_step(m, io, s);
@@ -682,6 +688,11 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
   }
   *out = m;
   return SD_OK;
+}
+
+extern "C" int32_t sd_attn_set_splits(int32_t splits) {
+  g_attn_splits = splits > 0 ? std::min(splits, 64) : 0;
+  return g_attn_splits;
 }
 
 extern "C" int sd_model_destroy(sd_model* m) {

@@ -119,6 +119,13 @@ def set_tc_min_rows(rows: int) -> int:
     return int(lib().sd_gemm_set_tc_min_rows(int(rows)))
 
 
+def set_attn_splits(splits: int) -> int:
+    """Prefix key splits of the step's attention per (request, kv head, row
+    chunk); <= 0 restores the automatic choice.  Returns the value in force
+    (0: automatic)."""
+    return int(lib().sd_attn_set_splits(int(splits)))
+
+
 def row_map(kind: int, Hq: int, Hkv: int, inter: int, N: int) -> np.ndarray:
     out = np.empty(N, dtype=np.int32)
     check(lib().sd_model_row_map(kind, Hq, Hkv, 128, inter, out.ctypes.data, N))

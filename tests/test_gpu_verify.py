@@ -112,6 +112,20 @@ def test_tree_verify_on_tensor_core_gemms(M, dec):
         M.set_tc_min_rows(0)
 
 
+@pytest.mark.parametrize("splits", [1, 3, 64])
+def test_tree_verify_with_fixed_attention_splits(M, dec, splits):
+    """One prefix split (no merge across CTAs), an odd count whose last
+    split is ragged, and the maximum (most splits empty at this context)."""
+    shape, W, model = dec
+    assert M.set_attn_splits(splits) == splits
+    try:
+        _verify_case(M, shape, W, model, wl.draft(14, 0, 16, 8, 0.8, shape.V), 200)
+        _verify_case(M, shape, W, model, wl.draft(15, 0, 5, 3, 0.7, shape.V), 61)
+        test_batched_paged_equals_oracle(M, dec)
+    finally:
+        assert M.set_attn_splits(0) == 0
+
+
 def test_wide_tree_64_nodes(M, dec):
     shape, W, model = dec
     _verify_case(M, shape, W, model, wl.draft(12, 0, 64, 10, 0.7, shape.V), 130)
