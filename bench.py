@@ -32,7 +32,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NOMINAL_BW_GBS = 8000.0       # the metric's "fraction of 8 TB/s"
 # DRAM bytes (read + write) of one k_w12_gemm gate/up launch, 8B shape,
 # M = 16, from an ncu --set full capture of that launch (the probe command)
-GATE_UP_TRAFFIC_8B = 151.682048e6 + 3.501056e6
+GATE_UP_TRAFFIC_8B = 151.707904e6 + 4.178176e6
 
 
 def peaks():
