@@ -92,6 +92,17 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const uint16_t* __restrict__ sr
                                                  const int32_t* __restrict__ row_req,
                                                  const int32_t* __restrict__ req_ok) {
   pdl_launch();  // the next kernel may start streaming its (independent) weights now
+  // up to kKeep 8-element chunks per thread stay in registers between the
+  // two passes (H <= 8192 at 256 threads); gamma is a weight, so it is read
+  // before the wait for the previous kernel
+  constexpr int kKeep = 4;
+  const int n8 = H / 8;
+  uint4 gk[kKeep], vk[kKeep];
+#pragma unroll
+  for (int it = 0; it < kKeep; it++) {
+    const int i = threadIdx.x + it * blockDim.x;
+    if (i < n8) gk[it] = reinterpret_cast<const uint4*>(gamma)[i];
+  }
   pdl_wait();
   const int m = blockIdx.x;
   const uint16_t* row;
@@ -102,10 +113,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const uint16_t* __restrict__ sr
   } else {
     row = src + (int64_t)m * H;
   }
-  const int n8 = H / 8;
   float ss = 0.f;
-  for (int i = threadIdx.x; i < n8; i += blockDim.x) {
-    const uint4 v = reinterpret_cast<const uint4*>(row)[i];
+  auto square_add = [&](const uint4& v, int i) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; j++) {
@@ -114,7 +123,19 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const uint16_t* __restrict__ sr
       ss = fmaf(hi, hi, ss);
     }
     if (x_out) reinterpret_cast<uint4*>(x_out + (int64_t)m * H)[i] = v;
+  };
+#pragma unroll
+  for (int it = 0; it < kKeep; it++) {
+    const int i = threadIdx.x + it * blockDim.x;
+    if (i < n8) vk[it] = reinterpret_cast<const uint4*>(row)[i];
   }
+#pragma unroll
+  for (int it = 0; it < kKeep; it++) {
+    const int i = threadIdx.x + it * blockDim.x;
+    if (i < n8) square_add(vk[it], i);
+  }
+  for (int i = threadIdx.x + kKeep * blockDim.x; i < n8; i += blockDim.x)
+    square_add(reinterpret_cast<const uint4*>(row)[i], i);
   __shared__ float red[8];
   for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
@@ -122,9 +143,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const uint16_t* __restrict__ sr
   float tot = 0.f;
   for (int i = 0; i < (int)(blockDim.x >> 5); i++) tot += red[i];
   const float rinv = 1.0f / sqrtf(tot / (float)H + eps);
-  for (int i = threadIdx.x; i < n8; i += blockDim.x) {
-    const uint4 v = reinterpret_cast<const uint4*>(row)[i];
-    const uint4 gm = reinterpret_cast<const uint4*>(gamma)[i];
+  auto scale_store = [&](const uint4& v, const uint4& gm, int i) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     const uint32_t gg[4] = {gm.x, gm.y, gm.z, gm.w};
     uint32_t o[4];
@@ -135,7 +154,14 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const uint16_t* __restrict__ sr
       o[j] = pack_bf16x2(lo, hi);
     }
     reinterpret_cast<uint4*>(xn + (int64_t)m * H)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  };
+#pragma unroll
+  for (int it = 0; it < kKeep; it++) {
+    const int i = threadIdx.x + it * blockDim.x;
+    if (i < n8) scale_store(vk[it], gk[it], i);
   }
+  for (int i = threadIdx.x + kKeep * blockDim.x; i < n8; i += blockDim.x)
+    scale_store(reinterpret_cast<const uint4*>(row)[i], reinterpret_cast<const uint4*>(gamma)[i], i);
 }
 
 cudaError_t launch_rmsnorm(const uint16_t* src, const uint16_t* gamma, int rows, int H, float eps, uint16_t* xn,
