@@ -20,6 +20,12 @@ Sources followed (page title, section):
     verification accepts tokens (``accept``).
   * "SpecPilot Uses Agentic Discovery ...", "Technical Mechanisms" -- a
     drafter proposes candidates, the target verifies them in parallel.
+  * "SpecPilot: AI Agent Framework ...", "(2) Best-first Tree Verification
+    for Hybrid Architectures" (candidates ranked by parent-conditioned
+    log-probability, highest cumulative path scores kept) and "(4) Three
+    Batch Optimization Mechanisms", Shared Node Budget (requests share one
+    node budget, given to the candidates of highest path probability) --
+    ``path_scores``, ``best_first_select``.
 The dense decoder itself (RMSNorm, RoPE, GQA, SwiGLU) is the synthetic
 architecture the workloads name; the pages do not define it.
 
@@ -518,3 +524,102 @@ def tiny_forward(W1, Wlm, act_bits):
     """Tiny verify model: y = bf16(a W1^T), logits = y Wlm^T (fp64)."""
     y = linear_bf16(act_bits, W1)
     return linear(y, Wlm)
+
+
+# ------------------------------------------------- best-first selection --
+
+SELECT_BAD_TREE = 5  # the library's SD_ERR_BAD_TREE
+
+
+@dataclass
+class Selection:
+    cu: np.ndarray       # int32 [R+1]: request r's selected nodes are cu[r] .. cu[r+1]-1
+    src: np.ndarray      # int32 [total]: global candidate index of each selected node
+    parents: np.ndarray  # int32 [total]: parent among the request's selected nodes (-1 at the root)
+    scores: np.ndarray   # float32 [total]: path score of each selected node
+    status: int          # 0, or SELECT_BAD_TREE when some request's input was invalid
+
+
+def path_scores(parents, logprob) -> np.ndarray:
+    """Path score of every candidate of one request ("(2) Best-first Tree
+    Verification ...": cumulative score of the parent-conditioned
+    log-probabilities along the root path).  The root scores 0; node i
+    scores its parent's score plus logprob[i], one fp32 addition per node
+    taken from the root down (the rounding the selection decides on)."""
+    parents = np.asarray(parents)
+    lp = np.asarray(logprob, dtype=np.float32)
+    s = np.zeros(len(parents), dtype=np.float32)
+    for i in range(1, len(parents)):
+        s[i] = np.float32(s[parents[i]]) + lp[i]
+    return s
+
+
+def select_request_valid(parents, logprob) -> bool:
+    """A request's candidates form a tree rooted at node 0 (parent[0] = -1,
+    0 <= parent[i] < i) and every non-root log-probability is <= 0 (NaN and
+    positive values are rejected)."""
+    n = len(parents)
+    if n < 1 or int(parents[0]) != -1:
+        return False
+    for i in range(1, n):
+        if not (0 <= int(parents[i]) < i):
+            return False
+        if not (float(logprob[i]) <= 0.0):
+            return False
+    return True
+
+
+def best_first_select(parents, logprob, cu, budget: int, cap: int) -> Selection:
+    """Best-first node selection under a shared node budget ("(4) Three
+    Batch Optimization Mechanisms", Shared Node Budget, with the ranking of
+    "(2) Best-first Tree Verification ...").  Every request keeps its root
+    (the node verification starts from).  The other candidates of all
+    requests are then taken one at a time in order of path score, highest
+    first, equal scores by lower request and then lower node index, passing
+    over a candidate whose request already holds `cap` nodes, until `budget`
+    nodes are held in total.  With log-probabilities <= 0 a node never
+    scores above its parent, so the kept nodes of a request form a tree.
+    Output per request in node-index order with parents renumbered.  A
+    request with invalid input keeps nothing and sets the status."""
+    parents = np.asarray(parents, dtype=np.int32)
+    logprob = np.asarray(logprob, dtype=np.float32)
+    cu = np.asarray(cu, dtype=np.int64)
+    R = len(cu) - 1
+    status = 0
+    scores = np.zeros(len(parents), dtype=np.float32)
+    order = []
+    for r in range(R):
+        a, b = int(cu[r]), int(cu[r + 1])
+        if not select_request_valid(parents[a:b], logprob[a:b]):
+            status = SELECT_BAD_TREE
+            continue
+        scores[a:b] = path_scores(parents[a:b], logprob[a:b])
+        for i in range(b - a):
+            g = a + i
+            # roots first; then score, highest first; then global index
+            order.append(((0 if i == 0 else 1), -float(scores[g]), g, r))
+    order.sort(key=lambda t: (t[0], t[1], t[2]))
+    taken = [[] for _ in range(R)]
+    total = 0
+    for _, _, g, r in order:
+        if total >= budget:
+            break
+        if len(taken[r]) >= cap:
+            continue
+        taken[r].append(g)
+        total += 1
+    out_cu = np.zeros(R + 1, dtype=np.int32)
+    src, par, sc = [], [], []
+    for r in range(R):
+        sel = sorted(taken[r])
+        local = {g: j for j, g in enumerate(sel)}
+        a = int(cu[r])
+        for g in sel:
+            src.append(g)
+            p = int(parents[g])
+            par.append(-1 if g == a else local[a + p])
+            sc.append(scores[g])
+        out_cu[r + 1] = out_cu[r] + len(sel)
+    return Selection(out_cu, np.array(src, dtype=np.int32), np.array(par, dtype=np.int32),
+                     np.array(sc, dtype=np.float32), status)
+

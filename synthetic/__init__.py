@@ -33,6 +33,9 @@ SID_EMBED = 10
 SID_LM_HEAD = 11
 SID_TINY_W1 = 12
 SID_ROOT_TOKEN = 13
+SID_CAND_TREE = 14
+SID_CAND_LP = 15
+SID_CAND_TOKEN = 16
 SID_LAYER_BASE = 1000  # + 16 * layer + weight slot
 
 

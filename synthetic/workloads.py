@@ -12,8 +12,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from . import (SID_ACT, SID_COINS, SID_CTX, SID_EMBED, SID_ESC, SID_GAMMA, SID_KV, SID_LM_HEAD, SID_PAGES,
-               SID_ROOT_TOKEN, SID_STATE, SID_TINY_W1, SID_TREE, chain, copy_coins, force_rare_exponents, key,
+from . import (SID_ACT, SID_CAND_LP, SID_CAND_TOKEN, SID_CAND_TREE, SID_COINS, SID_CTX, SID_EMBED, SID_ESC,
+               SID_GAMMA, SID_KV, SID_LM_HEAD, SID_PAGES, SID_ROOT_TOKEN, SID_STATE, SID_TINY_W1, SID_TREE, chain, copy_coins, force_rare_exponents, key,
                layer_key, normal_bf16, normal_f32, ones_bf16, permutation, tree, uniform_int)
 
 WEIGHT_SLOTS = {"wq": 0, "wk": 1, "wv": 2, "wo": 3, "w_gate": 4, "w_up": 5, "w_down": 6, "attn": 7, "mlp": 8}
@@ -184,6 +184,44 @@ def draft(seed: int, r: int, M: int, max_depth: int, p: float, V: int, shape_kin
     from . import lib
     root = int(lib().sg_u64(_rkey(seed, SID_ROOT_TOKEN, r), 0) % V)
     return TreeDraft(parents, cp, rt, root)
+
+
+@dataclass
+class Candidates:
+    """Draft candidate trees of R requests, concatenated: request r owns
+    entries cu[r] .. cu[r+1]-1; parents are local to the request (root first,
+    parent[i] < i); logprob[i] <= 0 is the draft log-probability of node i's
+    token given its parent (0 at the roots); tokens are the draft tokens."""
+    parents: np.ndarray
+    logprob: np.ndarray
+    tokens: np.ndarray
+    cu: np.ndarray
+
+
+def candidates(seed: int, R: int, n, max_depth: int, V: int, step: float = 0.0) -> Candidates:
+    """Synthetic candidate trees: n (an int, or one per request) nodes per
+    request in a random tree of depth <= max_depth; log-probabilities log(u)
+    with u uniform in (0, 1) (a drafter's softmax tail), rounded down to a
+    multiple of `step` when step > 0 (exact ties, zeros included)."""
+    ns = [int(n)] * R if np.isscalar(n) else [int(x) for x in n]
+    par, lp, tok = [], [], []
+    for r in range(R):
+        m = ns[r]
+        par.append(tree(_rkey(seed, SID_CAND_TREE, r), m, max_depth))
+        u = (uniform_int(_rkey(seed, SID_CAND_LP, r), m, 1, 1 << 24).astype(np.float64)) / float(1 << 24)
+        l = np.log(u)
+        if step > 0:
+            l = -np.floor(-l / step) * step
+            l = np.minimum(l, 0.0)
+        l = l.astype(np.float32)
+        if m:
+            l[0] = 0.0
+        lp.append(l)
+        tok.append(uniform_int(_rkey(seed, SID_CAND_TOKEN, r), m, 0, V).astype(np.int32))
+    cu = np.zeros(R + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(ns)
+    cat = lambda xs, dt: np.concatenate(xs).astype(dt) if xs else np.zeros(0, dt)
+    return Candidates(cat(par, np.int32), cat(lp, np.float32), cat(tok, np.int32), cu)
 
 
 def depths(parents) -> np.ndarray:
