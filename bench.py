@@ -61,9 +61,55 @@ def parse():
                     help="time the fused W12 linear alone on an N x K tensor with M rows")
     ap.add_argument("--tc-min-rows", type=int, default=0,
                     help="rows per launch from which GEMMs run on the tcgen05 kernel (0: the library default)")
+    ap.add_argument("--select", default=None, metavar="R,n,budget,cap",
+                    help="time the best-first node selection alone on R requests of n candidates")
     ap.add_argument("--attn-splits", type=int, default=0,
                     help="prefix key splits of the step's attention per kv head and row chunk (0: automatic)")
     return ap.parse_args()
+
+
+def select_arm(args):
+    """Best-first node selection under a shared node budget alone
+    (sd_best_first_select) on seeded synthetic candidate trees: per-call time
+    with CUDA events over graph replays; candidates per second."""
+    import numpy as np
+    import torch
+    from synthetic import workloads as wl
+    from speculative_decoding_tree_bit_gb300 import _build
+    from speculative_decoding_tree_bit_gb300 import model as Mdl
+    _build.build()
+    R, n, budget, cap = (int(v) for v in args.select.split(","))
+    c = wl.candidates(args.seed, R, n, 8, 32000)
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a.astype(dt))).cuda()
+    par, lp, cu, tok = dev(c.parents, np.int32), dev(c.logprob, np.float32), dev(c.cu, np.int32), dev(c.tokens, np.int32)
+    sel = Mdl.Selector(int(c.cu[-1]), R)
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            sel(par, lp, cu, budget, cap, tokens=tok, stream=stream, clear_status=False)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(args.steps):
+                sel(par, lp, cu, budget, cap, tokens=tok, stream=stream, clear_status=False)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    N = int(c.cu[-1])
+    kept = int(sel.out_cu[R].item())
+    status = int(sel.status.item())
+    # algorithmic bytes: candidates read (parent, log-prob, token), kept nodes written (src, parent, token, score)
+    nbytes = N * 12 + (R + 1) * 4 + kept * 16
+    return {"probe": "sd_best_first_select", "R": R, "n": n, "candidates": N, "budget": budget, "cap": cap,
+            "kept": kept, "status": status, "us_per_call": us, "candidates_per_s": N / (us * 1e-6),
+            "bound": "latency", "bytes": nbytes, "GBps": nbytes / (us * 1e-6) / 1e9,
+            "launches_per_call": 2, "memsets_per_call": 1}
 
 
 def probe_arm(args):
@@ -565,6 +611,9 @@ def main():
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     dist = None
+    if args.select:
+        print(json.dumps(select_arm(args)), flush=True)
+        return
     if args.probe:
         print(json.dumps(probe_arm(args)), flush=True)
         return

@@ -207,6 +207,49 @@ int sd_accept(const int32_t* tokens, const int32_t* parents, const int32_t* argm
               int32_t* accepted_len, int32_t* accepted_tokens, int32_t* bonus, int32_t* path, int32_t* status,
               void* stream);
 
+/* ------------------------------------------ best-first node selection -- */
+/* [SELECT] Best-first selection of the nodes one batched verify checks,
+ * under a node budget the requests share ("SpecPilot: AI Agent Framework
+ * Boosts Speculative Decoding 10.87x", "(2) Best-first Tree Verification
+ * for Hybrid Architectures": candidates ranked by parent-conditioned
+ * log-probability, highest cumulative path scores kept; "(4) Three Batch
+ * Optimization Mechanisms", Shared Node Budget).
+ *
+ * Input (device): R requests of drafted candidates, request r owning
+ * entries cu[r] .. cu[r+1]-1 (cu: int32 [R+1], cu[0] = 0, cu[R] = n_total,
+ * non-decreasing, 1..2048 candidates per request); parents: int32, local
+ * to the request (entry 0 is the root with parent -1, 0 <= parent[i] < i);
+ * logprob: fp32, the draft log-probability of node i given its parent
+ * (<= 0, -inf allowed; ignored at the root); tokens (optional): int32.
+ * Path score: 0 at the root, parent's score + logprob[i] (fp32, from the
+ * root down).  Every request keeps its root; the other candidates are taken
+ * in order of path score, highest first (equal scores: lower request, then
+ * lower node index), passing over a candidate whose request holds `cap`
+ * nodes (root included), until `budget` nodes are held in total.  Since a
+ * node never scores above its parent, each request keeps a tree.
+ *
+ * Output (device, caller-allocated): out_cu int32 [R+1] (request r's kept
+ * nodes are out_cu[r] .. out_cu[r+1]-1, in their original index order);
+ * out_src int32, out_parents int32 (renumbered within the request, -1 at the
+ * root), out_tokens int32 (optional, needs tokens), out_score fp32
+ * (optional), each with room for min(budget, n_total) entries.  out_cu,
+ * out_parents and the gathered tokens are the tokens / parents / cu of
+ * sd_verify_batch (its cu is read on the host: copy out_cu back).
+ *
+ * Limits: 1 <= R <= n_total <= 16384 (else SD_ERR_INVALID_ARG /
+ * SD_ERR_UNSUPPORTED), budget >= R and cap >= 1 (SD_ERR_INVALID_ARG).
+ * workspace: sd_select_workspace(n_total) bytes of device memory, any
+ * content.  *status (device int32, zeroed by the caller) becomes
+ * SD_ERR_BAD_TREE when a request's parents or log-probabilities are invalid
+ * (NaN, > 0): that request keeps nothing, the others are selected as if it
+ * were absent; an invalid cu array sets it and zeroes out_cu.  Asynchronous
+ * on `stream` (two kernels and a memset). */
+size_t sd_select_workspace(int32_t n_total);
+int sd_best_first_select(const int32_t* parents, const float* logprob, const int32_t* cu, int32_t R,
+                         int32_t n_total, int32_t budget, int32_t cap, const int32_t* tokens, int32_t* out_cu,
+                         int32_t* out_src, int32_t* out_parents, int32_t* out_tokens, float* out_score,
+                         int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
+
 /* -------------------------------------------------------- tiny verify -- */
 /* One linear layer and an lm_head: logits = (bf16(act W1^T)) Wlm^T, argmax
  * per node in fp32, then greedy acceptance over the tree.  act: bf16 [M][K];

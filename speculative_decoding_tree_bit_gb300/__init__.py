@@ -81,6 +81,9 @@ _SIGS = {
     "sd_attn_set_splits": (i32, [i32]),
     "sd_tree_info": (ctypes.c_int, [vp, i32, i32, vp, vp, vp, vp, vp]),
     "sd_accept": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]),
+    "sd_select_workspace": (ctypes.c_size_t, [i32]),
+    "sd_best_first_select": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                            ctypes.c_size_t, vp]),
     "sd_tiny_workspace": (ctypes.c_size_t, [i64, i64, i64, i32]),
     "sd_tiny_verify": (ctypes.c_int, [P(W12Tensor), P(W12Tensor), vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp,
                                       ctypes.c_size_t, vp]),

@@ -376,6 +376,45 @@ class PagedKVCache:
         return s
 
 
+class Selector:
+    """Best-first node selection under a shared node budget through the C
+    ABI (sd_best_first_select): owns the workspace and output buffers for up
+    to `max_total` candidates, so repeated calls allocate nothing."""
+
+    def __init__(self, max_total: int, max_requests: int, device="cuda"):
+        self.max_total, self.max_requests, self.device = int(max_total), int(max_requests), device
+        self.ws = Workspace(int(lib().sd_select_workspace(self.max_total)), device)
+        n, R = self.max_total, self.max_requests
+        self.out_cu = torch.zeros(R + 1, dtype=torch.int32, device=device)
+        self.out_src = torch.zeros(n, dtype=torch.int32, device=device)
+        self.out_parents = torch.zeros(n, dtype=torch.int32, device=device)
+        self.out_tokens = torch.zeros(n, dtype=torch.int32, device=device)
+        self.out_score = torch.zeros(n, dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def __call__(self, parents: torch.Tensor, logprob: torch.Tensor, cu: torch.Tensor, budget: int, cap: int,
+                 tokens: torch.Tensor | None = None, stream=None, clear_status: bool = True):
+        """parents / cu int32, logprob float32, tokens int32 (optional), all on
+        the device.  Returns views of the output buffers (valid until the next
+        call): cu [R+1], src, parents, tokens, score (each min(budget, n)
+        long; entries past cu[R] are unused) and status [1]."""
+        R, n = cu.numel() - 1, parents.numel()
+        if n > self.max_total or R > self.max_requests:
+            raise ValueError("more candidates or requests than the selector was made for")
+        if clear_status:
+            self.status.zero_()
+        k = min(int(budget), n)
+        check(lib().sd_best_first_select(parents.data_ptr(), logprob.data_ptr(), cu.data_ptr(), R, n, int(budget),
+                                         int(cap), _ptr(tokens), self.out_cu.data_ptr(), self.out_src.data_ptr(),
+                                         self.out_parents.data_ptr(),
+                                         self.out_tokens.data_ptr() if tokens is not None else 0,
+                                         self.out_score.data_ptr(), self.status.data_ptr(), self.ws.ptr,
+                                         self.ws.nbytes, stream_ptr(stream)))
+        return {"cu": self.out_cu[:R + 1], "src": self.out_src[:k], "parents": self.out_parents[:k],
+                "tokens": self.out_tokens[:k] if tokens is not None else None, "score": self.out_score[:k],
+                "status": self.status}
+
+
 def tiny_verify(W1: Packed, Wlm: Packed, act: torch.Tensor, tokens, parents, logits: bool = True, stream=None):
     """The tiny verify model through the C ABI; returns a dict of device tensors."""
     dev = act.device

@@ -71,5 +71,19 @@ def test_host_argument_checks(L):
     h = ctypes.c_void_p()
     assert L.sd_model_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == 2
     assert L.sd_accept(None, None, None, 4, None, None, None, None, None, None) == 1
+    # best-first selection: argument checks run before any device work
+    assert L.sd_select_workspace(0) == 0
+    assert L.sd_select_workspace(1000) == 20 * 1000 + 16
+    d = ctypes.c_void_p(16)
+    sel = lambda R, n, budget, cap, ws=1 << 20, tokens=d, out_tokens=d: L.sd_best_first_select(
+        d, d, d, R, n, budget, cap, tokens, d, d, d, out_tokens, None, d, d, ws, None)
+    assert sel(0, 4, 4, 1) == 1          # no request
+    assert sel(3, 2, 4, 1) == 1          # fewer candidates than requests
+    assert sel(3, 9, 2, 1) == 1          # budget below the number of roots
+    assert sel(3, 9, 4, 0) == 1          # cap below one
+    assert sel(3, 9, 4, 1, tokens=None) == 1  # gathered tokens without input tokens
+    assert sel(3, 16385, 4, 1) == 2      # more candidates than one call takes
+    assert sel(3, 9, 4, 1, ws=100) == 9  # workspace too small
+    assert L.sd_best_first_select(None, d, d, 1, 1, 1, 1, None, d, d, d, None, None, d, d, 1 << 20, None) == 1
     assert L.sd_tree_info(ctypes.c_void_p(16), 65, 0, ctypes.c_void_p(16), ctypes.c_void_p(16),
                           ctypes.c_void_p(16), None, None) == 2
