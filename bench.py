@@ -365,6 +365,23 @@ def overlapped_layer_trace(model, stream, step, layer):
             "attention: start, keys done (median), group ready (max), end", "kernels": rows}
 
 
+def slowest_rank(ms: float, ms_e2e: float, dist, device) -> tuple:
+    """The step times of the slowest replica (max over ranks): the job moves
+    at the pace of its slowest rank.  dist None: one process."""
+    if dist is None:
+        return ms, ms_e2e
+    import torch
+    t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0]), float(t[1])
+
+
+def job_throughput(world: int, rows_per_rank: int, ms: float) -> float:
+    """Tree tokens per second of the whole job: every rank verifies its own
+    rows each step (independent replicas, weak scaling)."""
+    return world * rows_per_rank / (ms * 1e-3)
+
+
 def gpu_arm(args, rank, world, dist):
     import numpy as np
     import torch
@@ -525,10 +542,7 @@ def gpu_arm(args, rank, world, dist):
     if args.timeline and not args.chain and M < tc_rows and shape.n_rec == 0:
         overlap = overlapped_layer_trace(model, stream, step, shape.n_layers // 2)
 
-    if dist is not None:
-        t = torch.tensor([ms, ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
+    ms, ms_e2e = slowest_rank(ms, ms_e2e, dist, dev)
 
     pk, pk_src = peaks()
     gemm = [(k, t, b) for k, t, b in tl if k.startswith("gemm")]  # chain launches and lone GEMMs (not their traces)
@@ -565,7 +579,7 @@ def gpu_arm(args, rank, world, dist):
             log(json.dumps(chain_phases))
         if overlap:
             log(json.dumps(overlap))
-    value = world * M / (ms * 1e-3)
+    value = job_throughput(world, M, ms)
     res = {
         "metric": "tree_tokens_per_s", "value": value, "unit": "tree tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -591,7 +605,7 @@ def gpu_arm(args, rank, world, dist):
                      "all_gemm_launches_gbs": all_gemm_gbs,
                      "peak_source": pk_src},
         "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in by_kind.items()},
-        "e2e": {"value": world * M / (ms_e2e * 1e-3), "unit": "tree tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(world, M, ms_e2e), "unit": "tree tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
