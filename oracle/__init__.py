@@ -20,6 +20,9 @@ Sources followed (page title, section):
     verification accepts tokens (``accept``).
   * "SpecPilot Uses Agentic Discovery ...", "Technical Mechanisms" -- a
     drafter proposes candidates, the target verifies them in parallel.
+  * same page, "(1) W12: Lossless 12-bit Weight Format", read literally: a
+    4-bit exponent OFFSET from a base chosen per output channel (``w12c_*``;
+    the per-tensor table above is the other reading).
   * "SpecPilot: AI Agent Framework ...", "(2) Best-first Tree Verification
     for Hybrid Architectures" (candidates ranked by parent-conditioned
     log-probability, highest cumulative path scores kept) and "(4) Three
@@ -622,4 +625,67 @@ def best_first_select(parents, logprob, cu, budget: int, cap: int) -> Selection:
         out_cu[r + 1] = out_cu[r] + len(sel)
     return Selection(out_cu, np.array(src, dtype=np.int32), np.array(par, dtype=np.int32),
                      np.array(sc, dtype=np.float32), status)
+
+
+# -------------------------------------------- W12, per-channel exponent base --
+
+@dataclass
+class W12C:
+    """Per-output-channel W12: row n stores each weight as sign, a 4-bit
+    offset of its exponent from the row's base, and the 7-bit mantissa;
+    offset 15 marks an escape whose original bf16 is in the side list."""
+    N: int
+    K: int
+    base: np.ndarray     # uint8 [N]: the row's base exponent
+    fields: np.ndarray   # uint16 [N][K]: sign << 11 | code << 7 | mantissa
+    esc_idx: np.ndarray  # uint32: n * K + k of every escape, ascending
+    esc_val: np.ndarray  # uint16: the escaped weights' bf16 bits
+
+    @property
+    def n_esc(self) -> int:
+        return int(self.esc_idx.size)
+
+
+def w12c_bases(W: np.ndarray) -> np.ndarray:
+    """Per output row, the base exponent b (0..241) whose window b .. b+14
+    holds the most of the row's exponents; ties go to the smaller b ("(1)
+    W12 ...": exponents concentrate within each output channel, so one
+    4-bit offset range per channel covers most of them)."""
+    W = np.asarray(W, dtype=np.uint16)
+    e = (W >> 7) & 0xFF
+    out = np.zeros(W.shape[0], dtype=np.uint8)
+    for n in range(W.shape[0]):
+        h = np.bincount(e[n], minlength=256).astype(np.int64)
+        c = np.concatenate([[0], np.cumsum(h)])
+        cover = c[15:257] - c[0:242]  # cover[b] = weights with exponent in b .. b+14
+        out[n] = int(np.argmax(cover))  # first maximum: the smaller base
+    return out
+
+
+def w12c_pack(W: np.ndarray, base: np.ndarray | None = None) -> W12C:
+    """Fields and escapes of W (bf16 bits [N][K]) under the per-row bases."""
+    W = np.asarray(W, dtype=np.uint16)
+    N, K = W.shape
+    if base is None:
+        base = w12c_bases(W)
+    base = np.asarray(base, dtype=np.uint8)
+    e = ((W >> 7) & 0xFF).astype(np.int32)
+    off = e - base.astype(np.int32)[:, None]
+    inside = (off >= 0) & (off <= 14)
+    code = np.where(inside, off, 15).astype(np.uint16)
+    fields = ((W >> 15) << 11) | (code << 7) | (W & 0x7F)
+    flat = np.flatnonzero(~inside.ravel()).astype(np.uint32)
+    return W12C(N, K, base.copy(), fields.astype(np.uint16), flat, W.ravel()[flat].copy())
+
+
+def w12c_unpack(p: W12C) -> np.ndarray:
+    """The bf16 bits back: exponent = base + code for codes 0..14, the side
+    list for code 15 (bit-exact restoration)."""
+    f = p.fields.astype(np.uint32)
+    code = (f >> 7) & 15
+    e = (p.base.astype(np.uint32)[:, None] + code) & 0xFF
+    W = (((f >> 11) & 1) << 15) | (e << 7) | (f & 0x7F)
+    W = W.astype(np.uint16).ravel()
+    W[p.esc_idx] = p.esc_val
+    return W.reshape(p.N, p.K)
 
