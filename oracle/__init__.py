@@ -20,6 +20,9 @@ Sources followed (page title, section):
     verification accepts tokens (``accept``).
   * "SpecPilot Uses Agentic Discovery ...", "Technical Mechanisms" -- a
     drafter proposes candidates, the target verifies them in parallel.
+  * same page, "(2) Best-first Tree Verification ...": Gated DeltaNet
+    layers follow each root path of the tree (``gdn_tree``, the published
+    gated delta rule).
   * same page, "(1) W12: Lossless 12-bit Weight Format", read literally: a
     4-bit exponent OFFSET from a base chosen per output channel (``w12c_*``;
     the per-tensor table above is the other reading).
@@ -345,6 +348,45 @@ def linrec_literal(q_bits, k_bits, v_bits, S0, z0, parents, eps):
         den = np.einsum("ha,ha->h", z[i], q[i]) + eps
         o[i] = num / den[:, None]
     return round_bf16(o), S, z
+
+
+def l2_normalise(x: np.ndarray) -> np.ndarray:
+    """x / ||x|| over the last axis (zero vectors stay zero)."""
+    n = np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
+    return np.where(n > 0, x / np.where(n > 0, n, 1.0), 0.0)
+
+
+def gdn_tree(q_bits, k_bits, v_bits, alpha, beta, S0, parents):
+    """Gated delta rule over a draft tree, literal per-node state ("(2)
+    Best-first Tree Verification for Hybrid Architectures": in Gated
+    DeltaNet layers the state is recomputed along each root path; the page
+    names the layer without writing its recurrence, which is the published
+    gated delta rule).
+
+    Per head, with q and k L2-normalised:
+      S_i = alpha_i (I - beta_i k_i k_i^T) S_parent(i) + beta_i k_i v_i^T
+      o_i = S_i^T q_i, rounded to bf16,
+    S0 the committed state before the root (row = key dim, column = value
+    dim).  q/k/v: bf16 [M][nh][hd]; alpha (gate, in (0, 1]) and beta
+    (write strength, in [0, 1]): [M][nh]; S0: [nh][hd][hd].  Returns
+    (o bits [M][nh][hd], S nodes [M][nh][hd][hd])."""
+    q = l2_normalise(bf16_to_f64(q_bits))
+    k = l2_normalise(bf16_to_f64(k_bits))
+    v = bf16_to_f64(v_bits)
+    a = np.asarray(alpha, dtype=np.float64)
+    b = np.asarray(beta, dtype=np.float64)
+    S0 = np.asarray(S0, dtype=np.float64)
+    M, nh, hd = q.shape
+    S = np.empty((M, nh, hd, hd))
+    o = np.empty((M, nh, hd))
+    for i in range(M):
+        Sp = S0 if parents[i] < 0 else S[parents[i]]
+        for h in range(nh):
+            kk = k[i, h]
+            # (I - beta k k^T) Sp = Sp - beta k (k^T Sp)
+            S[i, h] = a[i, h] * (Sp[h] - b[i, h] * np.outer(kk, kk @ Sp[h])) + b[i, h] * np.outer(kk, v[i, h])
+            o[i, h] = S[i, h].T @ q[i, h]
+    return round_bf16(o), S
 
 
 # -------------------------------------------------------- argmax / accept --
