@@ -20,6 +20,9 @@ Sources followed (page title, section):
     verification accepts tokens (``accept``).
   * "SpecPilot Uses Agentic Discovery ...", "Technical Mechanisms" -- a
     drafter proposes candidates, the target verifies them in parallel.
+  * same page, "(3) Two-Level Verification": a first round over the nested
+    8-bit weight view proposes a chain and accepts nothing, one exact round
+    decides (``w12_view8``, ``View8Weights``, ``two_level_verify``).
   * same page, "(2) Best-first Tree Verification ...": Gated DeltaNet
     layers follow each root path of the tree (``gdn_tree``, the published
     gated delta rule).
@@ -730,4 +733,67 @@ def w12c_unpack(p: W12C) -> np.ndarray:
     W = W.astype(np.uint16).ravel()
     W[p.esc_idx] = p.esc_val
     return W.reshape(p.N, p.K)
+
+
+# ------------------------------------------------- two-level verification --
+
+def w12_view8(W_bits) -> np.ndarray:
+    """The nested 8-bit view of W12 weights ("(3) Two-Level Verification":
+    the first round runs on W12's nested 8-bit weight view).  A weight's
+    12-bit field is sign, 4-bit exponent code and 7-bit mantissa; its high
+    byte keeps the sign, the code and the top 3 mantissa bits, so the view
+    is the weight with its 4 low mantissa bits cleared (an escaped weight
+    likewise, from the side list).  Truncates toward zero."""
+    return np.asarray(W_bits, dtype=np.uint16) & np.uint16(0xFFF0)
+
+
+class View8Weights:
+    """A model's W12-stored linear weights (q/k/v, O, gate/up, down,
+    lm_head) seen through the 8-bit view; the embedding and the norm
+    weights are not W12 tensors and stay as they are."""
+
+    def __init__(self, base):
+        self.base = base
+
+    def layer(self, l: int, name: str) -> np.ndarray:
+        return w12_view8(self.base.layer(l, name))
+
+    def lm_head(self) -> np.ndarray:
+        return w12_view8(self.base.lm_head())
+
+    def __getattr__(self, name):
+        return getattr(self.base, name)
+
+
+@dataclass
+class TwoLevel:
+    chain: np.ndarray    # int32: root token, the low-precision accepted path, its bonus token
+    low: Accept          # the low-precision walk over the draft tree (accepts nothing)
+    tokens: np.ndarray   # int32: the exact round's tree, the chain then the extension
+    parents: np.ndarray  # int32
+    exact: Accept        # the exact round's result: the only acceptance
+
+
+def two_level_verify(shape, weights, request: Request, extend) -> TwoLevel:
+    """Two-level verification ("(3) Two-Level Verification").  Round one
+    runs the request's draft tree with the 8-bit weight view and walks it
+    greedily: the path it would accept plus the token it would add form a
+    candidate chain; nothing is accepted and no state changes.  The drafter
+    then continues from the chain's end: ``extend(chain)`` returns (tokens,
+    parents) of new drafts, parents local to them with -1 meaning the
+    chain's last node.  One exact verification of the chain and the new
+    drafts decides what is accepted, so the result is what exact greedy
+    decoding would produce."""
+    low_out = forward(shape, View8Weights(weights), [request])
+    low = accept(request.tokens, request.parents, low_out.argmax)
+    chain = np.array([int(request.tokens[0])] + [int(t) for t in low.accepted_tokens] + [int(low.bonus)],
+                     dtype=np.int32)
+    ext_tok, ext_par = extend(chain)
+    ext_tok = np.asarray(ext_tok, dtype=np.int32)
+    ext_par = np.asarray(ext_par, dtype=np.int64)
+    n = len(chain)
+    tokens = np.concatenate([chain, ext_tok]).astype(np.int32)
+    parents = np.concatenate([np.arange(-1, n - 1), np.where(ext_par < 0, n - 1, ext_par + n)]).astype(np.int32)
+    out = forward(shape, weights, [Request(tokens, parents, request.ctx, request.layers)])
+    return TwoLevel(chain, low, tokens, parents, accept(tokens, parents, out.argmax))
 
