@@ -38,8 +38,8 @@ Sources followed (page title, section):
 The dense decoder itself (RMSNorm, RoPE, GQA, SwiGLU) is the synthetic
 architecture the workloads name; the pages do not define it.
 
-Readings where the pages are silent are listed in the design doc; the ones that
-change arithmetic are restated in the docstrings below.
+Where the pages are silent, each function's docstring states the reading it
+takes (the arithmetic, the order of operations, the tie rules).
 
 Parity pins for every function live in ``tests/test_oracle_*.py``.
 """
