@@ -71,6 +71,14 @@ def test_host_argument_checks(L):
     h = ctypes.c_void_p()
     assert L.sd_model_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == 2
     assert L.sd_accept(None, None, None, 4, None, None, None, None, None, None) == 1
+    # process-wide tuning knobs: host state only, clamped, <= 0 restores the default
+    assert L.sd_attn_set_splits(7) == 7
+    assert L.sd_attn_set_splits(1000) == 64
+    assert L.sd_attn_set_splits(-3) == 0
+    assert L.sd_attn_set_splits(0) == 0
+    assert L.sd_gemm_set_tc_min_rows(129) == 129
+    assert L.sd_gemm_set_tc_min_rows(0) == 65
+    assert L.sd_gemm_set_tc_min_rows(-1) == 65
     # best-first selection: argument checks run before any device work
     assert L.sd_select_workspace(0) == 0
     assert L.sd_select_workspace(1000) == 20 * 1000 + 16
