@@ -43,7 +43,9 @@ enum {
   SD_ERR_TIMEOUT = 6,      /* device: a bounded wait gave up */
   SD_ERR_CAPACITY = 7,     /* device: ctx + nodes exceeds the cache capacity / page table / RoPE table */
   SD_ERR_BAD_TOKEN = 8,    /* device: a token outside [0, vocab) */
-  SD_ERR_WORKSPACE = 9     /* caller workspace smaller than the size query returned */
+  SD_ERR_WORKSPACE = 9,    /* caller workspace smaller than the size query returned */
+  SD_ERR_IO = 10,          /* a file could not be opened or written */
+  SD_ERR_CORRUPT = 11      /* a file is not a W12 file of this version, or fails its checksums */
 };
 
 const char* sd_last_error(void);
@@ -206,6 +208,42 @@ int sd_tree_info(const int32_t* parents, int32_t M, int32_t ctx, uint64_t* anc, 
 int sd_accept(const int32_t* tokens, const int32_t* parents, const int32_t* argmax, int32_t M,
               int32_t* accepted_len, int32_t* accepted_tokens, int32_t* bonus, int32_t* path, int32_t* status,
               void* stream);
+
+/* ------------------------------------------------------- W12 on disk -- */
+/* A packed tensor in a file, so that weights are packed once ("SpecPilot:
+ * AI Agent Framework Boosts Speculative Decoding 10.87x", "(1) W12:
+ * Lossless 12-bit Weight Format").  Host memory only: the caller copies the
+ * arrays between the device and host buffers.  File (little-endian): a
+ * 224-byte header (magic "SDVW12F\n", version 1, N, K, n_escapes, the
+ * length of the escape tile index, the code table, n_table, affine, then
+ * offset / size / CRC-32 of each section, then the CRC-32 of the header's
+ * preceding bytes), followed by the sections at 16-byte aligned offsets:
+ * words (u32 [w12_words_count(N,K)]), esc_idx (u32 [n_escapes]), esc_val
+ * (u16 [n_escapes]), row_ptr (u32 [N+1]), tile_ptr (u32
+ * [w12_tile_ptr_count(N,K)]), tile_esc (u32 [n_escapes]).  CRC-32: IEEE
+ * 802.3 (reflected polynomial 0xEDB88320), as w12_crc32 computes it. */
+uint32_t w12_crc32(const void* data, size_t n);
+
+/* Write *t to path; t's array pointers are HOST pointers here (sizes as
+ * above; the escape arrays may be NULL when n_escapes == 0).  Errors:
+ * SD_ERR_INVALID_ARG (null pointer, shape outside N%16, K%64, N*K < 2^32),
+ * SD_ERR_IO (open or write failed; the file may be partial). */
+int w12_save(const char* path, const w12_tensor* t);
+
+/* Read and check path's header (magic, version, header CRC, section sizes
+ * against the shape): *meta gets N, K, the table, n_table, affine and
+ * n_escapes, *n_tile_ptr (optional) the tile index length, so the caller
+ * can size its buffers.  Errors: SD_ERR_INVALID_ARG, SD_ERR_IO (cannot
+ * open), SD_ERR_CORRUPT. */
+int w12_load_info(const char* path, w12_meta* meta, int64_t* n_tile_ptr);
+
+/* Read every section into caller-allocated HOST buffers (sizes from
+ * w12_load_info; the escape buffers may be NULL when there are no escapes),
+ * checking each section's CRC; fills *meta.  Errors: SD_ERR_INVALID_ARG,
+ * SD_ERR_IO, SD_ERR_CORRUPT (bad header, short file or checksum mismatch:
+ * the buffers' contents are then unspecified). */
+int w12_load(const char* path, uint32_t* words, uint32_t* esc_idx, uint16_t* esc_val, uint32_t* row_ptr,
+             uint32_t* tile_ptr, uint32_t* tile_esc, w12_meta* meta);
 
 /* ------------------------------------------ best-first node selection -- */
 /* [SELECT] Best-first selection of the nodes one batched verify checks,

@@ -17,7 +17,7 @@ from ._build import INCLUDE, LIB
 SD_OK = 0
 STATUS_NAMES = {0: "SD_OK", 1: "SD_ERR_INVALID_ARG", 2: "SD_ERR_UNSUPPORTED", 3: "SD_ERR_CUDA", 4: "SD_ERR_OOM",
                 5: "SD_ERR_BAD_TREE", 6: "SD_ERR_TIMEOUT", 7: "SD_ERR_CAPACITY", 8: "SD_ERR_BAD_TOKEN",
-                9: "SD_ERR_WORKSPACE"}
+                9: "SD_ERR_WORKSPACE", 10: "SD_ERR_IO", 11: "SD_ERR_CORRUPT"}
 
 
 class SdvError(RuntimeError):
@@ -81,6 +81,10 @@ _SIGS = {
     "sd_attn_set_splits": (i32, [i32]),
     "sd_tree_info": (ctypes.c_int, [vp, i32, i32, vp, vp, vp, vp, vp]),
     "sd_accept": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]),
+    "w12_crc32": (ctypes.c_uint32, [vp, ctypes.c_size_t]),
+    "w12_save": (ctypes.c_int, [ctypes.c_char_p, P(W12Tensor)]),
+    "w12_load_info": (ctypes.c_int, [ctypes.c_char_p, P(W12Meta), P(i64)]),
+    "w12_load": (ctypes.c_int, [ctypes.c_char_p, vp, vp, vp, vp, vp, vp, P(W12Meta)]),
     "sd_select_workspace": (ctypes.c_size_t, [i32]),
     "sd_best_first_select": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                             ctypes.c_size_t, vp]),

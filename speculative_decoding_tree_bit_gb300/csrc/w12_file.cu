@@ -1,0 +1,233 @@
+// Packed W12 tensors on disk, so that weights are packed once ("SpecPilot:
+// AI Agent Framework Boosts Speculative Decoding 10.87x", "(1) W12:
+// Lossless 12-bit Weight Format": the 12-bit codes and the sparse list of
+// out-of-range weights restore every weight exactly at load time).  Host
+// code only: the caller copies the arrays between device and host memory.
+//
+// File (little-endian): a fixed header, then six sections at 16-byte
+// aligned offsets: words, escape indices, escape values, row pointers, the
+// escape tile index (tile_ptr, tile_esc).  The header holds the shape, the
+// code table, the escape count, each section's offset, size and CRC-32,
+// and a CRC-32 of the header itself.  CRC-32 is the IEEE 802.3 checksum
+// (reflected polynomial 0xEDB88320, initial value and final xor 0xFFFFFFFF).
+
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "sdv.h"
+
+namespace sdv {
+namespace {
+
+constexpr char kMagic[8] = {'S', 'D', 'V', 'W', '1', '2', 'F', '\n'};
+constexpr uint32_t kVersion = 1;
+constexpr int kSections = 6;  // words, esc_idx, esc_val, row_ptr, tile_ptr, tile_esc
+
+struct Section {
+  uint64_t offset, bytes;
+  uint32_t crc, pad;
+};
+
+struct Header {
+  char magic[8];
+  uint32_t version, header_bytes;
+  int64_t N, K, n_escapes, n_tile_ptr;
+  uint8_t table[16];
+  int32_t n_table, affine;
+  Section sec[kSections];
+  uint32_t header_crc;  // over every byte before this field
+  uint32_t pad;
+};
+static_assert(sizeof(Header) == 8 + 8 + 32 + 16 + 8 + kSections * 24 + 8, "packed header layout");
+
+struct CrcTable {
+  uint32_t t[256];
+  CrcTable() {
+    for (uint32_t i = 0; i < 256; i++) {
+      uint32_t c = i;
+      for (int k = 0; k < 8; k++) c = (c & 1u) ? (0xEDB88320u ^ (c >> 1)) : (c >> 1);
+      t[i] = c;
+    }
+  }
+};
+
+uint32_t crc32_update(uint32_t crc, const void* data, size_t n) {
+  static const CrcTable tab;
+  const uint8_t* p = static_cast<const uint8_t*>(data);
+  uint32_t c = crc ^ 0xFFFFFFFFu;
+  for (size_t i = 0; i < n; i++) c = tab.t[(c ^ p[i]) & 0xFFu] ^ (c >> 8);
+  return c ^ 0xFFFFFFFFu;
+}
+
+bool shape_ok(int64_t N, int64_t K) {
+  return N > 0 && K > 0 && N % 16 == 0 && K % 64 == 0 && N * K < (int64_t(1) << 32);
+}
+
+// expected byte size of each section for a tensor of this shape
+void section_bytes(int64_t N, int64_t K, int64_t n_esc, int64_t n_tile_ptr, uint64_t out[kSections]) {
+  out[0] = (uint64_t)w12_words_count(N, K) * 4;
+  out[1] = (uint64_t)n_esc * 4;
+  out[2] = (uint64_t)n_esc * 2;
+  out[3] = (uint64_t)(N + 1) * 4;
+  out[4] = (uint64_t)n_tile_ptr * 4;
+  out[5] = (uint64_t)n_esc * 4;
+}
+
+struct File {
+  FILE* f = nullptr;
+  File(const char* path, const char* mode) : f(std::fopen(path, mode)) {}
+  ~File() {
+    if (f) std::fclose(f);
+  }
+};
+
+int read_header(FILE* f, Header& h, const char* who) {
+  if (std::fread(&h, sizeof h, 1, f) != 1) {
+    set_error(std::string(who) + ": short header");
+    return SD_ERR_CORRUPT;
+  }
+  if (std::memcmp(h.magic, kMagic, sizeof kMagic) != 0 || h.version != kVersion || h.header_bytes != sizeof h) {
+    set_error(std::string(who) + ": not a W12 file of this version");
+    return SD_ERR_CORRUPT;
+  }
+  if (crc32_update(0, &h, offsetof(Header, header_crc)) != h.header_crc) {
+    set_error(std::string(who) + ": header checksum mismatch");
+    return SD_ERR_CORRUPT;
+  }
+  uint64_t want[kSections];
+  if (!shape_ok(h.N, h.K) || h.n_escapes < 0 || h.n_escapes > h.N * h.K || h.n_table < 0 || h.n_table > 15 ||
+      h.n_tile_ptr != w12_tile_ptr_count(h.N, h.K)) {
+    set_error(std::string(who) + ": header fields out of range");
+    return SD_ERR_CORRUPT;
+  }
+  section_bytes(h.N, h.K, h.n_escapes, h.n_tile_ptr, want);
+  for (int s = 0; s < kSections; s++)
+    if (h.sec[s].bytes != want[s] || h.sec[s].offset % 16 != 0 || h.sec[s].offset < sizeof h) {
+      set_error(std::string(who) + ": section table inconsistent with the shape");
+      return SD_ERR_CORRUPT;
+    }
+  return SD_OK;
+}
+
+}  // namespace
+}  // namespace sdv
+
+using namespace sdv;
+
+extern "C" uint32_t w12_crc32(const void* data, size_t n) { return crc32_update(0, data, n); }
+
+extern "C" int w12_save(const char* path, const w12_tensor* t) {
+  if (!path || !t || !shape_ok(t->N, t->K) || t->n_escapes < 0 || t->n_table < 0 || t->n_table > 15 || !t->words ||
+      !t->row_ptr || !t->tile_ptr || (t->n_escapes > 0 && (!t->esc_idx || !t->esc_val || !t->tile_esc))) {
+    set_error("w12_save: bad argument");
+    return SD_ERR_INVALID_ARG;
+  }
+  Header h{};
+  std::memcpy(h.magic, kMagic, sizeof kMagic);
+  h.version = kVersion;
+  h.header_bytes = sizeof h;
+  h.N = t->N;
+  h.K = t->K;
+  h.n_escapes = t->n_escapes;
+  h.n_tile_ptr = w12_tile_ptr_count(t->N, t->K);
+  std::memcpy(h.table, t->table, 16);
+  h.n_table = t->n_table;
+  h.affine = t->affine;
+  const void* src[kSections] = {t->words, t->esc_idx, t->esc_val, t->row_ptr, t->tile_ptr, t->tile_esc};
+  uint64_t bytes[kSections];
+  section_bytes(h.N, h.K, h.n_escapes, h.n_tile_ptr, bytes);
+  uint64_t off = (sizeof h + 15) & ~uint64_t(15);
+  for (int s = 0; s < kSections; s++) {
+    h.sec[s].offset = off;
+    h.sec[s].bytes = bytes[s];
+    h.sec[s].crc = crc32_update(0, bytes[s] ? src[s] : "", bytes[s]);
+    off = (off + bytes[s] + 15) & ~uint64_t(15);
+  }
+  h.header_crc = crc32_update(0, &h, offsetof(Header, header_crc));
+  File f(path, "wb");
+  if (!f.f) {
+    set_error(std::string("w12_save: cannot open ") + path);
+    return SD_ERR_IO;
+  }
+  static const char zeros[16] = {};
+  bool ok = std::fwrite(&h, sizeof h, 1, f.f) == 1;
+  uint64_t at = sizeof h;
+  for (int s = 0; s < kSections && ok; s++) {
+    ok = std::fwrite(zeros, 1, h.sec[s].offset - at, f.f) == h.sec[s].offset - at;
+    if (ok && bytes[s]) ok = std::fwrite(src[s], 1, bytes[s], f.f) == bytes[s];
+    at = h.sec[s].offset + bytes[s];
+  }
+  ok = ok && std::fflush(f.f) == 0;
+  if (!ok) {
+    set_error(std::string("w12_save: write failed for ") + path);
+    return SD_ERR_IO;
+  }
+  return SD_OK;
+}
+
+extern "C" int w12_load_info(const char* path, w12_meta* meta, int64_t* n_tile_ptr) {
+  if (!path || !meta) {
+    set_error("w12_load_info: bad argument");
+    return SD_ERR_INVALID_ARG;
+  }
+  File f(path, "rb");
+  if (!f.f) {
+    set_error(std::string("w12_load_info: cannot open ") + path);
+    return SD_ERR_IO;
+  }
+  Header h;
+  const int rc = read_header(f.f, h, "w12_load_info");
+  if (rc) return rc;
+  meta->N = h.N;
+  meta->K = h.K;
+  std::memcpy(meta->table, h.table, 16);
+  meta->n_table = h.n_table;
+  meta->affine = h.affine;
+  meta->n_escapes = h.n_escapes;
+  if (n_tile_ptr) *n_tile_ptr = h.n_tile_ptr;
+  return SD_OK;
+}
+
+extern "C" int w12_load(const char* path, uint32_t* words, uint32_t* esc_idx, uint16_t* esc_val, uint32_t* row_ptr,
+                        uint32_t* tile_ptr, uint32_t* tile_esc, w12_meta* meta) {
+  if (!path || !words || !row_ptr || !tile_ptr || !meta) {
+    set_error("w12_load: bad argument");
+    return SD_ERR_INVALID_ARG;
+  }
+  File f(path, "rb");
+  if (!f.f) {
+    set_error(std::string("w12_load: cannot open ") + path);
+    return SD_ERR_IO;
+  }
+  Header h;
+  int rc = read_header(f.f, h, "w12_load");
+  if (rc) return rc;
+  if (h.n_escapes > 0 && (!esc_idx || !esc_val || !tile_esc)) {
+    set_error("w12_load: the file has escapes but no escape buffers were given");
+    return SD_ERR_INVALID_ARG;
+  }
+  void* dst[kSections] = {words, esc_idx, esc_val, row_ptr, tile_ptr, tile_esc};
+  for (int s = 0; s < kSections; s++) {
+    const uint64_t n = h.sec[s].bytes;
+    if (!n) continue;
+    if (std::fseek(f.f, (long)h.sec[s].offset, SEEK_SET) != 0 || std::fread(dst[s], 1, n, f.f) != n) {
+      set_error("w12_load: file shorter than its section table");
+      return SD_ERR_CORRUPT;
+    }
+    if (crc32_update(0, dst[s], n) != h.sec[s].crc) {
+      set_error("w12_load: section checksum mismatch");
+      return SD_ERR_CORRUPT;
+    }
+  }
+  meta->N = h.N;
+  meta->K = h.K;
+  std::memcpy(meta->table, h.table, 16);
+  meta->n_table = h.n_table;
+  meta->affine = h.affine;
+  meta->n_escapes = h.n_escapes;
+  return SD_OK;
+}

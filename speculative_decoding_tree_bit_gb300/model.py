@@ -92,6 +92,41 @@ def unpack(p: Packed, stream=None) -> torch.Tensor:
     return out
 
 
+def save(p: Packed, path: str) -> None:
+    """Write a packed tensor to a W12 file (w12_save): the arrays are copied
+    to host memory first."""
+    host = {k: getattr(p, k).cpu().numpy() for k in ("words", "esc_idx", "esc_val", "row_ptr", "tile_ptr", "tile_esc")}
+    t = p.struct()
+    t.words, t.esc_idx, t.esc_val = (host[k].ctypes.data for k in ("words", "esc_idx", "esc_val"))
+    t.row_ptr, t.tile_ptr, t.tile_esc = (host[k].ctypes.data for k in ("row_ptr", "tile_ptr", "tile_esc"))
+    check(lib().w12_save(str(path).encode(), ctypes.byref(t)))
+
+
+def load_host(path: str):
+    """Read a W12 file into host arrays (w12_load_info, w12_load): returns
+    (meta, dict of numpy arrays words, esc_idx, esc_val, row_ptr, tile_ptr,
+    tile_esc; the escape arrays have at least one element)."""
+    meta = W12Meta()
+    ntp = ctypes.c_int64()
+    check(lib().w12_load_info(str(path).encode(), ctypes.byref(meta), ctypes.byref(ntp)))
+    ne = max(int(meta.n_escapes), 1)
+    a = {"words": np.empty(int(lib().w12_words_count(meta.N, meta.K)), dtype=np.int32),
+         "esc_idx": np.empty(ne, dtype=np.int32), "esc_val": np.empty(ne, dtype=np.int16),
+         "row_ptr": np.empty(int(meta.N) + 1, dtype=np.int32), "tile_ptr": np.empty(int(ntp.value), dtype=np.int32),
+         "tile_esc": np.empty(ne, dtype=np.int32)}
+    check(lib().w12_load(str(path).encode(), *(a[k].ctypes.data for k in ("words", "esc_idx", "esc_val", "row_ptr",
+                                                                           "tile_ptr", "tile_esc")),
+                         ctypes.byref(meta)))
+    return meta, a
+
+
+def load(path: str, device="cuda") -> Packed:
+    """A packed tensor from a W12 file, its arrays copied to `device`."""
+    meta, a = load_host(path)
+    t = {k: torch.from_numpy(v).to(device) for k, v in a.items()}
+    return Packed(meta, t["words"], t["esc_idx"], t["esc_val"], t["row_ptr"], t["tile_ptr"], t["tile_esc"])
+
+
 class Workspace:
     """Caller-owned device scratch for the stand-alone entry points."""
 

@@ -1,0 +1,142 @@
+"""W12 tensors on disk (w12_save, w12_load_info, w12_load), host memory only,
+so no GPU: a packed tensor written and read back restores every weight bit
+for bit; each section's and the header's CRC-32 catch a changed byte; a
+short or foreign file is rejected; bad arguments return their codes."""
+import ctypes
+import struct
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+import speculative_decoding_tree_bit_gb300 as sdv
+from speculative_decoding_tree_bit_gb300 import _build
+
+SECTIONS = ("words", "esc_idx", "esc_val", "row_ptr", "tile_ptr", "tile_esc")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return sdv.lib()
+
+
+def _packed(N, K, seed, rare=0, no_escapes=False):
+    if no_escapes:
+        # every exponent in 110 .. 124: one 15-exponent table covers all
+        e = synthetic.uniform_int(synthetic.key(seed, 1), N * K, 110, 124).astype(np.uint16)  # bounds inclusive
+        m = synthetic.uniform_int(synthetic.key(seed, 2), N * K, 0, 255).astype(np.uint16)
+        W = ((m & 0x80) << 8 | (e << 7) | (m & 0x7F)).astype(np.uint16).reshape(N, K)
+    else:
+        W = synthetic.normal_bf16(synthetic.key(seed, 1), N * K, 0.02).reshape(N, K)
+    if rare:
+        synthetic.force_rare_exponents(synthetic.key(seed, 2), W, rare)
+    p = oracle.w12_pack(W)
+    return W, p
+
+
+def _tensor(L, p, seed):
+    """W12Tensor over host arrays: the oracle's words / escapes / row
+    pointers, and an arbitrary escape tile index of the right lengths (the
+    file stores it as given)."""
+    ntp = int(L.w12_tile_ptr_count(p.N, p.K))
+    a = {"words": np.ascontiguousarray(p.words, dtype=np.uint32),
+         "esc_idx": np.ascontiguousarray(p.esc_idx, dtype=np.uint32),
+         "esc_val": np.ascontiguousarray(p.esc_val, dtype=np.uint16),
+         "row_ptr": np.ascontiguousarray(p.row_ptr, dtype=np.uint32),
+         "tile_ptr": synthetic.uniform_int(synthetic.key(seed, 3), ntp, 0, 1 << 31).astype(np.uint32),
+         "tile_esc": synthetic.uniform_int(synthetic.key(seed, 4), p.n_esc, 0, 1 << 31).astype(np.uint32)}
+    t = sdv.W12Tensor()
+    t.N, t.K, t.n_escapes = p.N, p.K, p.n_esc
+    for k in SECTIONS:
+        setattr(t, k, a[k].ctypes.data if a[k].size else None)
+    tab = list(p.table)
+    for i, e in enumerate(tab):
+        t.table[i] = int(e)
+    t.n_table = len(tab)
+    t.affine = int(len(tab) > 0 and all(tab[c] == tab[0] + c for c in range(len(tab))) and tab[0] + 15 <= 254)
+    return t, a
+
+
+def _read(L, path):
+    meta = sdv.W12Meta()
+    ntp = ctypes.c_int64()
+    rc = L.w12_load_info(str(path).encode(), ctypes.byref(meta), ctypes.byref(ntp))
+    if rc:
+        return rc, None, None
+    ne = max(int(meta.n_escapes), 1)
+    b = {"words": np.zeros(int(L.w12_words_count(meta.N, meta.K)), np.uint32), "esc_idx": np.zeros(ne, np.uint32),
+         "esc_val": np.zeros(ne, np.uint16), "row_ptr": np.zeros(int(meta.N) + 1, np.uint32),
+         "tile_ptr": np.zeros(int(ntp.value), np.uint32), "tile_esc": np.zeros(ne, np.uint32)}
+    rc = L.w12_load(str(path).encode(), *(b[k].ctypes.data for k in SECTIONS), ctypes.byref(meta))
+    return rc, meta, b
+
+
+def test_crc32_is_the_ieee_checksum(L):
+    msg = b"123456789"
+    assert L.w12_crc32(msg, len(msg)) == 0xCBF43926  # the standard check value
+    data = synthetic.uniform_int(synthetic.key(7, 7), 10000, 0, 255).astype(np.uint8)
+    assert L.w12_crc32(data.ctypes.data, data.size) == zlib.crc32(data.tobytes())
+    assert L.w12_crc32(b"", 0) == 0
+
+
+@pytest.mark.parametrize("rare,no_escapes", [(0, True), (0, False), (40, False)])
+def test_round_trip_restores_every_weight(L, tmp_path, rare, no_escapes):
+    W, p = _packed(64, 192, 11 + rare, rare, no_escapes)
+    assert (p.n_esc == 0) if no_escapes else p.n_esc >= rare
+    t, a = _tensor(L, p, 5)
+    path = tmp_path / "w.w12"
+    assert L.w12_save(str(path).encode(), ctypes.byref(t)) == 0
+    rc, meta, b = _read(L, path)
+    assert rc == 0
+    assert (meta.N, meta.K, meta.n_escapes, meta.n_table, meta.affine) == (p.N, p.K, p.n_esc, t.n_table, t.affine)
+    assert list(meta.table[:meta.n_table]) == list(p.table)
+    for k in SECTIONS:
+        n = a[k].size
+        np.testing.assert_array_equal(b[k][:n], a[k])
+    back = oracle.W12(p.N, p.K, np.array(meta.table[:meta.n_table], np.uint8), b["words"],
+                      b["esc_idx"][:p.n_esc].copy(), b["esc_val"][:p.n_esc].copy(), b["row_ptr"])
+    np.testing.assert_array_equal(oracle.w12_unpack(back), W)
+
+
+def test_every_changed_byte_is_caught(L, tmp_path):
+    W, p = _packed(32, 128, 21, 12)
+    t, a = _tensor(L, p, 6)
+    path = tmp_path / "w.w12"
+    assert L.w12_save(str(path).encode(), ctypes.byref(t)) == 0
+    raw = bytearray(path.read_bytes())
+    # one byte inside each section, and bytes of the header
+    offs = [struct.unpack_from("<Q", raw, 72 + 24 * s)[0] for s in range(6)]
+    sizes = [struct.unpack_from("<Q", raw, 80 + 24 * s)[0] for s in range(6)]
+    for s in range(6):
+        assert sizes[s] > 0
+        bad = bytearray(raw)
+        bad[offs[s] + sizes[s] // 2] ^= 0x10
+        path.write_bytes(bad)
+        assert _read(L, path)[0] == 11
+    for pos in (0, 9, 20, 50, 100, 216):
+        bad = bytearray(raw)
+        bad[pos] ^= 0x01
+        path.write_bytes(bad)
+        assert _read(L, path)[0] == 11
+    path.write_bytes(raw[: len(raw) - 7])       # short file
+    assert _read(L, path)[0] == 11
+    path.write_bytes(raw[:100])                 # short header
+    assert _read(L, path)[0] == 11
+    path.write_bytes(raw)
+    assert _read(L, path)[0] == 0
+
+
+def test_bad_arguments_and_paths(L, tmp_path):
+    W, p = _packed(16, 64, 31)
+    t, a = _tensor(L, p, 8)
+    assert L.w12_save(None, ctypes.byref(t)) == 1
+    t.N = 24                                      # not a multiple of 16
+    assert L.w12_save(str(tmp_path / "x").encode(), ctypes.byref(t)) == 1
+    t.N = 16
+    assert L.w12_save(str(tmp_path).encode(), ctypes.byref(t)) == 10   # a directory
+    meta = sdv.W12Meta()
+    assert L.w12_load_info(str(tmp_path / "missing").encode(), ctypes.byref(meta), None) == 10
+    assert L.w12_load_info(str(tmp_path / "missing").encode(), None, None) == 1
