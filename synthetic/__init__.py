@@ -132,6 +132,7 @@ def copy_coins(k: int, M: int, p: float, V: int):
 
 
 def uniform_int(k: int, n: int, lo: int, hi: int) -> np.ndarray:
+    """n integers uniform in lo .. hi, both ends included."""
     out = np.empty(max(n, 1), dtype=np.int64)
     lib().sg_uniform_int(k, n, lo, hi, out.ctypes.data)
     return out[:n].copy()

@@ -201,8 +201,9 @@ class Candidates:
 def candidates(seed: int, R: int, n, max_depth: int, V: int, step: float = 0.0) -> Candidates:
     """Synthetic candidate trees: n (an int, or one per request) nodes per
     request in a random tree of depth <= max_depth; log-probabilities log(u)
-    with u uniform in (0, 1) (a drafter's softmax tail), rounded down to a
-    multiple of `step` when step > 0 (exact ties, zeros included)."""
+    with u uniform in (0, 1] (a drafter's softmax tail), rounded down to a
+    multiple of `step` when step > 0 (exact ties, zeros included); tokens
+    uniform in [0, V)."""
     ns = [int(n)] * R if np.isscalar(n) else [int(x) for x in n]
     par, lp, tok = [], [], []
     for r in range(R):
@@ -217,7 +218,7 @@ def candidates(seed: int, R: int, n, max_depth: int, V: int, step: float = 0.0) 
         if m:
             l[0] = 0.0
         lp.append(l)
-        tok.append(uniform_int(_rkey(seed, SID_CAND_TOKEN, r), m, 0, V).astype(np.int32))
+        tok.append(uniform_int(_rkey(seed, SID_CAND_TOKEN, r), m, 0, V - 1).astype(np.int32))  # bounds inclusive
     cu = np.zeros(R + 1, dtype=np.int32)
     cu[1:] = np.cumsum(ns)
     cat = lambda xs, dt: np.concatenate(xs).astype(dt) if xs else np.zeros(0, dt)

@@ -75,7 +75,7 @@ def _extend_with(shape, W, ctx, good: int, rng_key: int):
             t = int(oracle.forward(shape, W, [req]).argmax[-1])
             seq.append(t)
             out.append(t)
-        out += [int(x) for x in synthetic.uniform_int(rng_key, 2, 0, shape.V)]
+        out += [int(x) for x in synthetic.uniform_int(rng_key, 2, 0, shape.V - 1)]  # bounds inclusive
         return np.array(out, np.int32), np.arange(-1, len(out) - 1)
     return extend
 
