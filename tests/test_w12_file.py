@@ -140,3 +140,30 @@ def test_bad_arguments_and_paths(L, tmp_path):
     meta = sdv.W12Meta()
     assert L.w12_load_info(str(tmp_path / "missing").encode(), ctypes.byref(meta), None) == 10
     assert L.w12_load_info(str(tmp_path / "missing").encode(), None, None) == 1
+
+
+def test_python_save_and_load_round_trip(L, tmp_path):
+    # the binding's save / load on CPU tensors (the device copies are the only
+    # step the GPU path adds)
+    import torch
+    from speculative_decoding_tree_bit_gb300 import model as M
+    W, p = _packed(48, 128, 41, 9)
+    t, a = _tensor(L, p, 9)
+    meta = sdv.W12Meta()
+    meta.N, meta.K, meta.n_escapes, meta.n_table, meta.affine = p.N, p.K, p.n_esc, t.n_table, t.affine
+    for i in range(16):
+        meta.table[i] = t.table[i]
+    as_t = {k: torch.from_numpy(a[k].view(np.int32 if a[k].dtype == np.uint32 else np.int16).copy()) for k in SECTIONS}
+    packed = M.Packed(meta, as_t["words"], as_t["esc_idx"], as_t["esc_val"], as_t["row_ptr"], as_t["tile_ptr"],
+                      as_t["tile_esc"])
+    path = tmp_path / "p.w12"
+    M.save(packed, path)
+    m2, arrays = M.load_host(path)
+    assert (m2.N, m2.K, m2.n_escapes) == (p.N, p.K, p.n_esc)
+    for k in SECTIONS:
+        np.testing.assert_array_equal(arrays[k][:a[k].size].view(a[k].dtype), a[k])
+    back = M.load(path, device="cpu")
+    assert (back.N, back.K, back.n_escapes) == (p.N, p.K, p.n_esc)
+    np.testing.assert_array_equal(back.words.numpy().view(np.uint32), a["words"])
+    with pytest.raises(sdv.SdvError):
+        M.load_host(tmp_path / "missing.w12")
