@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -365,6 +366,26 @@ def overlapped_layer_trace(model, stream, step, layer):
             "attention: start, keys done (median), group ready (max), end", "kernels": rows}
 
 
+def step_distribution(times_ms) -> dict:
+    """Median, 10th / 90th percentiles and a 95% confidence interval of the
+    mean (normal approximation) of individually timed steps."""
+    import numpy as np
+    a = np.asarray(times_ms, dtype=np.float64)
+    n = int(a.size)
+    mean = float(a.mean())
+    half = 1.96 * float(a.std(ddof=1)) / math.sqrt(n) if n > 1 else 0.0
+    return {"n": n, "median_ms": float(np.median(a)), "p10_ms": float(np.percentile(a, 10)),
+            "p90_ms": float(np.percentile(a, 90)), "mean_ms": mean, "ci95_ms": [mean - half, mean + half]}
+
+
+def overhead_factor(step_ms: float, timeline) -> tuple:
+    """Step time over the sum of its kernels' serialised, event-timed
+    durations (phases nested in a chain launch, "chain.*", are not added
+    twice): below 1 where programmatic dependent launch overlaps kernels."""
+    total = sum(t for k, t, _ in timeline if not k.startswith("chain."))
+    return (step_ms / total if total > 0 else None), total
+
+
 def slowest_rank(ms: float, ms_e2e: float, dist, device) -> tuple:
     """The step times of the slowest replica (max over ranks): the job moves
     at the pace of its slowest rank.  dist None: one process."""
@@ -515,6 +536,21 @@ def gpu_arm(args, rank, world, dist):
         e1.record(stream)
     barrier()
     ms_e2e = e0.elapsed_time(e1) / args.steps
+
+    # ---- per-step distribution: each step between its own pair of events
+    # (after the timed region above; diagnostics only, never the value)
+    try:
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(max(args.steps, 50))]
+        with torch.cuda.stream(stream):
+            for a, b in pairs:
+                a.record(stream)
+                step()
+                b.record(stream)
+        torch.cuda.synchronize()
+        step_stats = step_distribution([a.elapsed_time(b) for a, b in pairs])
+    except Exception as ex:  # a failure here must not cost the bench line
+        step_stats = {"error": str(ex)[:200]}
     h2d = tok_h.numel() * 4 + par_h.numel() * 4 + 4
     d2h = sum(h.numel() * 4 for h in res_h.values())
 
@@ -580,6 +616,7 @@ def gpu_arm(args, rank, world, dist):
         if overlap:
             log(json.dumps(overlap))
     value = job_throughput(world, M, ms)
+    ovh, kernel_sum = overhead_factor(ms, tl)
     res = {
         "metric": "tree_tokens_per_s", "value": value, "unit": "tree tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -596,6 +633,8 @@ def gpu_arm(args, rank, world, dist):
         "step_bytes": step_bytes, "step_flops": flops,
         "step_lower_bound_us": bound_s * 1e6,
         "frac_of_step_lower_bound": bound_s / (ms * 1e-3),
+        "step_stats": step_stats,
+        "kernel_sum_ms": kernel_sum, "overhead_factor": ovh,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak if achieved else None, "traffic": traffic,
                      "kernel": ("k_w12_gemm, gate/up launches (algorithmic bytes per launch / mean event-timed "

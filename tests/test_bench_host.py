@@ -1,0 +1,25 @@
+"""Host-side arithmetic of the bench that needs no GPU: the per-step
+distribution (median, percentiles, confidence interval of the mean) and the
+overhead factor (step time over the sum of the kernels' serialised times)."""
+import math
+
+import pytest
+
+import bench
+
+
+def test_step_distribution_of_known_samples():
+    s = bench.step_distribution([4.0, 1.0, 3.0, 2.0, 5.0])
+    assert s["n"] == 5 and s["median_ms"] == 3.0 and s["mean_ms"] == 3.0
+    assert s["p10_ms"] == pytest.approx(1.4) and s["p90_ms"] == pytest.approx(4.6)  # linear interpolation
+    half = 1.96 * math.sqrt(2.5) / math.sqrt(5)  # sample variance of 1..5 is 2.5
+    assert s["ci95_ms"] == pytest.approx([3.0 - half, 3.0 + half])
+    one = bench.step_distribution([2.5])
+    assert one["ci95_ms"] == [2.5, 2.5] and one["median_ms"] == 2.5
+
+
+def test_overhead_factor_counts_top_level_launches_once():
+    tl = [("gemm_qkv", 1.0, 0.0), ("attention", 0.5, 0.0), ("chain.gemm_o", 0.3, 0.0), ("gemm_o", 0.5, 0.0)]
+    f, total = bench.overhead_factor(1.5, tl)
+    assert total == 2.0 and f == 0.75
+    assert bench.overhead_factor(1.0, []) == (None, 0)
