@@ -239,9 +239,13 @@ int w12_load_info(const char* path, w12_meta* meta, int64_t* n_tile_ptr);
 
 /* Read every section into caller-allocated HOST buffers (sizes from
  * w12_load_info; the escape buffers may be NULL when there are no escapes),
- * checking each section's CRC; fills *meta.  Errors: SD_ERR_INVALID_ARG,
- * SD_ERR_IO, SD_ERR_CORRUPT (bad header, short file or checksum mismatch:
- * the buffers' contents are then unspecified). */
+ * checking each section's CRC and that the arrays form a packed tensor
+ * (escape indices strictly increasing and below N*K, row_ptr counting the
+ * escapes before each row, the escape tile index the one the side list
+ * defines); fills *meta.  w12_save writes what it is given; this is where a
+ * file is checked.  Errors: SD_ERR_INVALID_ARG, SD_ERR_IO, SD_ERR_CORRUPT
+ * (bad header, short file, checksum mismatch or inconsistent arrays: the
+ * buffers' contents are then unspecified). */
 int w12_load(const char* path, uint32_t* words, uint32_t* esc_idx, uint16_t* esc_val, uint32_t* row_ptr,
              uint32_t* tile_ptr, uint32_t* tile_esc, w12_meta* meta);
 

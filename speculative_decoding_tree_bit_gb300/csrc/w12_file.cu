@@ -13,6 +13,7 @@
 
 #include <cstdint>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -111,6 +112,48 @@ int read_header(FILE* f, Header& h, const char* who) {
       return SD_ERR_CORRUPT;
     }
   return SD_OK;
+}
+
+// A file whose checksums pass may still hold arrays that do not form a
+// packed tensor (written from inconsistent buffers): the kernels index
+// memory with these values, so a loaded tensor must be one.  Checks, all
+// from the layout's definition: escape indices strictly increasing and
+// below N*K; row_ptr[n] = the number of escapes before row n; the escape
+// tile index exactly the one the side list defines (per 128-row block, the
+// block's escapes grouped by 64-column tile in side-list order, each entry
+// (bf16 << 16) | (row - 128 b) << 6 | (column - 64 t)).
+bool consistent(int64_t N, int64_t K, int64_t n_esc, const uint32_t* esc_idx, const uint16_t* esc_val,
+                const uint32_t* row_ptr, const uint32_t* tile_ptr, const uint32_t* tile_esc) {
+  const uint64_t NK = (uint64_t)N * (uint64_t)K;
+  for (int64_t e = 0; e < n_esc; e++)
+    if (esc_idx[e] >= NK || (e > 0 && esc_idx[e] <= esc_idx[e - 1])) return false;
+  int64_t e = 0;
+  for (int64_t n = 0; n <= N; n++) {
+    while (e < n_esc && (uint64_t)esc_idx[e] < (uint64_t)n * (uint64_t)K) e++;
+    if ((int64_t)row_ptr[n] != e) return false;
+  }
+  const int64_t KT = K / 64, NB = (N + 127) / 128;
+  std::vector<uint32_t> cursor((size_t)KT);
+  for (int64_t b = 0; b < NB; b++) {
+    const int64_t n0 = b * 128, n1 = n0 + 128 < N ? n0 + 128 : N;
+    const uint32_t e0 = row_ptr[n0], e1 = row_ptr[n1];
+    std::fill(cursor.begin(), cursor.end(), 0u);
+    for (uint32_t i = e0; i < e1; i++) cursor[(size_t)((esc_idx[i] % (uint64_t)K) / 64)]++;
+    uint32_t run = e0;
+    for (int64_t t = 0; t < KT; t++) {
+      if (tile_ptr[b * KT + t] != run) return false;
+      const uint32_t c = cursor[(size_t)t];
+      cursor[(size_t)t] = run;
+      run += c;
+    }
+    for (uint32_t i = e0; i < e1; i++) {
+      const uint64_t idx = esc_idx[i];
+      const uint32_t n = (uint32_t)(idx / (uint64_t)K), k = (uint32_t)(idx % (uint64_t)K);
+      const uint32_t want = ((uint32_t)esc_val[i] << 16) | ((n - (uint32_t)n0) << 6) | (k & 63u);
+      if (tile_esc[cursor[k / 64]++] != want) return false;
+    }
+  }
+  return (int64_t)tile_ptr[NB * KT] == n_esc;
 }
 
 }  // namespace
@@ -222,6 +265,10 @@ extern "C" int w12_load(const char* path, uint32_t* words, uint32_t* esc_idx, ui
       set_error("w12_load: section checksum mismatch");
       return SD_ERR_CORRUPT;
     }
+  }
+  if (!consistent(h.N, h.K, h.n_escapes, esc_idx, esc_val, row_ptr, tile_ptr, tile_esc)) {
+    set_error("w12_load: the arrays do not form a packed tensor (escape list, row pointers or tile index)");
+    return SD_ERR_CORRUPT;
   }
   meta->N = h.N;
   meta->K = h.K;

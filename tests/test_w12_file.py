@@ -37,17 +37,34 @@ def _packed(N, K, seed, rare=0, no_escapes=False):
     return W, p
 
 
+def _tile_index(N, K, esc_idx, esc_val):
+    """The escape tile index as the header defines it: per 128-row block and
+    64-column tile, the block's escapes in side-list order, each entry
+    (bf16 << 16) | (row - 128 b) << 6 | (column - 64 t)."""
+    KT, NB = K // 64, (N + 127) // 128
+    ptr, ent = [], []
+    for b in range(NB):
+        mine = [(int(i), int(v)) for i, v in zip(esc_idx, esc_val) if b * 128 <= int(i) // K < (b + 1) * 128]
+        for t in range(KT):
+            ptr.append(len(ent))
+            for i, v in mine:
+                n, k = divmod(i, K)
+                if k // 64 == t:
+                    ent.append((v << 16) | ((n - 128 * b) << 6) | (k & 63))
+    ptr.append(len(ent))
+    return np.array(ptr, np.uint32), np.array(ent, np.uint32)
+
+
 def _tensor(L, p, seed):
     """W12Tensor over host arrays: the oracle's words / escapes / row
-    pointers, and an arbitrary escape tile index of the right lengths (the
-    file stores it as given)."""
-    ntp = int(L.w12_tile_ptr_count(p.N, p.K))
+    pointers and the escape tile index they define."""
+    tp, te = _tile_index(p.N, p.K, p.esc_idx, p.esc_val)
+    assert tp.size == int(L.w12_tile_ptr_count(p.N, p.K))
     a = {"words": np.ascontiguousarray(p.words, dtype=np.uint32),
          "esc_idx": np.ascontiguousarray(p.esc_idx, dtype=np.uint32),
          "esc_val": np.ascontiguousarray(p.esc_val, dtype=np.uint16),
          "row_ptr": np.ascontiguousarray(p.row_ptr, dtype=np.uint32),
-         "tile_ptr": synthetic.uniform_int(synthetic.key(seed, 3), ntp, 0, 1 << 31).astype(np.uint32),
-         "tile_esc": synthetic.uniform_int(synthetic.key(seed, 4), p.n_esc, 0, 1 << 31).astype(np.uint32)}
+         "tile_ptr": tp, "tile_esc": te}
     t = sdv.W12Tensor()
     t.N, t.K, t.n_escapes = p.N, p.K, p.n_esc
     for k in SECTIONS:
@@ -167,3 +184,31 @@ def test_python_save_and_load_round_trip(L, tmp_path):
     np.testing.assert_array_equal(back.words.numpy().view(np.uint32), a["words"])
     with pytest.raises(sdv.SdvError):
         M.load_host(tmp_path / "missing.w12")
+
+
+@pytest.mark.parametrize("fault", ["esc_order", "esc_range", "row_ptr", "tile_ptr", "tile_entry", "tile_total"])
+def test_checksummed_but_inconsistent_arrays_are_rejected(L, tmp_path, fault):
+    # w12_save writes whatever it is given (with valid checksums); w12_load
+    # must still refuse arrays that are not a packed tensor
+    W, p = _packed(160, 128, 51, 30)  # two row blocks, the second ragged
+    t, a = _tensor(L, p, 10)
+    b = {k: v.copy() for k, v in a.items()}
+    if fault == "esc_order":
+        b["esc_idx"][[3, 4]] = b["esc_idx"][[4, 3]]
+    elif fault == "esc_range":
+        b["esc_idx"][-1] = p.N * p.K
+    elif fault == "row_ptr":
+        b["row_ptr"][5] += 1
+    elif fault == "tile_ptr":
+        b["tile_ptr"][1] += 1
+    elif fault == "tile_entry":
+        b["tile_esc"][2] ^= 1 << 13  # a row field past the block
+    else:
+        b["tile_ptr"][-1] -= 1
+    for k in SECTIONS:
+        setattr(t, k, b[k].ctypes.data if b[k].size else None)
+    path = tmp_path / "bad.w12"
+    assert L.w12_save(str(path).encode(), ctypes.byref(t)) == 0
+    assert _read(L, path)[0] == 11
+    assert b"packed tensor" in L.sd_last_error()
+
