@@ -209,6 +209,29 @@ int sd_accept(const int32_t* tokens, const int32_t* parents, const int32_t* argm
               int32_t* accepted_len, int32_t* accepted_tokens, int32_t* bonus, int32_t* path, int32_t* status,
               void* stream);
 
+/* ------------------------------------------ W12 with per-channel bases -- */
+/* Per-output-channel W12 ("SpecPilot: AI Agent Framework Boosts Speculative
+ * Decoding 10.87x", "(1) W12: Lossless 12-bit Weight Format", read
+ * literally: a 4-bit exponent offset within each output channel), offline
+ * host code.  Row n keeps base[n], the exponent starting the 15-exponent
+ * window that holds most of the row's weights (the smaller base on ties);
+ * a weight stores sign, e - base[n] (15: escaped, its bf16 in the side
+ * list) and the 7-bit mantissa, in the per-tensor format's word layout
+ * (escaped weights: code 15, sign and mantissa zero).  Host buffers: w
+ * bf16 [N][K]; base u8 [N]; words u32 [w12_words_count(N,K)]; esc_idx u32
+ * and esc_val u16 [esc_cap]; row_ptr u32 [N+1].  *n_escapes gets the
+ * number of escapes; SD_ERR_WORKSPACE (nothing written past the bases)
+ * when it exceeds esc_cap, so a call with esc_cap = 0 counts them.  Other
+ * errors: SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED (N%16, K%64, N*K < 2^32). */
+int w12c_pack_host(const uint16_t* w, int64_t N, int64_t K, uint8_t* base, uint32_t* words, uint32_t* esc_idx,
+                   uint16_t* esc_val, int64_t esc_cap, uint32_t* row_ptr, int64_t* n_escapes);
+
+/* The bf16 weights back from a per-channel packed tensor (host buffers, as
+ * w12c_pack_host writes them).  Errors: SD_ERR_INVALID_ARG,
+ * SD_ERR_UNSUPPORTED, SD_ERR_CORRUPT (an escape index >= N*K). */
+int w12c_unpack_host(const uint32_t* words, const uint8_t* base, int64_t N, int64_t K, const uint32_t* esc_idx,
+                     const uint16_t* esc_val, int64_t n_escapes, uint16_t* w);
+
 /* ------------------------------------------------------- W12 on disk -- */
 /* A packed tensor in a file, so that weights are packed once ("SpecPilot:
  * AI Agent Framework Boosts Speculative Decoding 10.87x", "(1) W12:
