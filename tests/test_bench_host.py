@@ -23,3 +23,15 @@ def test_overhead_factor_counts_top_level_launches_once():
     f, total = bench.overhead_factor(1.5, tl)
     assert total == 2.0 and f == 0.75
     assert bench.overhead_factor(1.0, []) == (None, 0)
+
+
+def test_kv_bytes_of_the_8b_step_match_the_stated_figure():
+    # 36 attention layers x 8 kv heads x (2048 prefix + 16 tree) keys x 128 dims x bf16 x (K and V): 0.30 GB
+    from synthetic import workloads as wl
+    b = bench.kv_bytes_per_step(wl.SHAPES["8b"], 2048, 16)
+    assert b == 36 * 8 * 2064 * 128 * 2 * 2
+    assert abs(b - 0.30e9) < 0.01e9
+
+
+def test_job_throughput_counts_every_rank():
+    assert bench.job_throughput(4, 16, 4.0) == pytest.approx(16000.0)
