@@ -232,6 +232,27 @@ int w12c_pack_host(const uint16_t* w, int64_t N, int64_t K, uint8_t* base, uint3
 int w12c_unpack_host(const uint32_t* words, const uint8_t* base, int64_t N, int64_t K, const uint32_t* esc_idx,
                      const uint16_t* esc_val, int64_t n_escapes, uint16_t* w);
 
+/* ------------------------------------------------ nested 8-bit plane -- */
+/* [2-LEVEL] The nested 8-bit view of W12 as its own plane ("SpecPilot: AI
+ * Agent Framework Boosts Speculative Decoding 10.87x", "(3) Two-Level
+ * Verification": the first round verifies with W12's nested 8-bit weight
+ * view): each weight's high byte of its 12-bit field, sign << 7 | code << 3
+ * | top 3 mantissa bits (escaped weights: code 15, sign and mantissa zero),
+ * 1 byte per weight, offline host code.  Layout: per 16-row strip and
+ * 64-column super-tile, u32 [2 planes][32 lanes][4 sub-tiles]; lane 4g + q,
+ * sub-tile j: plane 0 holds (row g, col c), (row g, c + 1), (row g + 8, c),
+ * (row g + 8, c + 1) in bytes 0..3, c = 16 j + 2 q; plane 1 the same at
+ * c + 8.  plane: u32 [N*K/4].  Pack from the bf16 weights w [N][K] and the
+ * tensor's code table (w12_pack_analyze's).  Unpack gives the view: each
+ * weight with its 4 low mantissa bits cleared (escaped weights from the
+ * side list, cleared the same way).  Errors: SD_ERR_INVALID_ARG,
+ * SD_ERR_UNSUPPORTED (N%16, K%64, N*K < 2^32), SD_ERR_CORRUPT (unpack: an
+ * escape index >= N*K). */
+int w12_plane8_pack_host(const uint16_t* w, int64_t N, int64_t K, const uint8_t* table, int32_t n_table,
+                         uint32_t* plane);
+int w12_plane8_unpack_host(const uint32_t* plane, int64_t N, int64_t K, const uint8_t* table, int32_t n_table,
+                           const uint32_t* esc_idx, const uint16_t* esc_val, int64_t n_escapes, uint16_t* w);
+
 /* ------------------------------------------------------- W12 on disk -- */
 /* A packed tensor in a file, so that weights are packed once ("SpecPilot:
  * AI Agent Framework Boosts Speculative Decoding 10.87x", "(1) W12:

@@ -81,6 +81,8 @@ _SIGS = {
     "sd_attn_set_splits": (i32, [i32]),
     "sd_tree_info": (ctypes.c_int, [vp, i32, i32, vp, vp, vp, vp, vp]),
     "sd_accept": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]),
+    "w12_plane8_pack_host": (ctypes.c_int, [vp, i64, i64, vp, i32, vp]),
+    "w12_plane8_unpack_host": (ctypes.c_int, [vp, i64, i64, vp, i32, vp, vp, i64, vp]),
     "w12c_pack_host": (ctypes.c_int, [vp, i64, i64, vp, vp, vp, vp, i64, vp, P(i64)]),
     "w12c_unpack_host": (ctypes.c_int, [vp, vp, i64, i64, vp, vp, i64, vp]),
     "w12_crc32": (ctypes.c_uint32, [vp, ctypes.c_size_t]),
