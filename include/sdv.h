@@ -2,7 +2,9 @@
  * sdv -- tree verification with lossless 12-bit weights on one GB300.
  *
  * C ABI of the library libsdv.so.  Every pointer is a DEVICE pointer unless
- * its name ends in _host.  Streams are passed as `void*` holding a
+ * its name ends in _host, or the function works in host memory only (the
+ * functions whose names end in _host, and the W12 file functions w12_save,
+ * w12_load_info and w12_load), as its comment states.  Streams are passed as `void*` holding a
  * cudaStream_t (NULL = legacy default stream).  Every function returns an
  * `int` status (SD_OK = 0); host-checkable argument errors are reported
  * synchronously, data errors found on the device (a bad parent array, a token
@@ -21,6 +23,8 @@
  *   [EXACT] first page, "(3) Two-Level Verification": only the exact target
  *          verification accepts tokens; second page "Core Idea", item 4
  *          (token forcing: outputs equal the stock greedy outputs).
+ *   [BATCH] first page, "(4) Three Batch Optimization Mechanisms", Shared
+ *          Node Budget (best-first node selection across a batch).
  */
 #ifndef SDV_H
 #define SDV_H
