@@ -10,8 +10,8 @@
 // with sign and mantissa zero, and the side list and row pointers are the
 // same as the per-tensor format's.  Offline (host) code.
 
-#include <cstdint>
 #include <algorithm>
+#include <cstdint>
 #include <cstring>
 #include <vector>
 

@@ -11,9 +11,10 @@
 // and a CRC-32 of the header itself.  CRC-32 is the IEEE 802.3 checksum
 // (reflected polynomial 0xEDB88320, initial value and final xor 0xFFFFFFFF).
 
+#include <algorithm>
+#include <cstddef>
 #include <cstdint>
 #include <cstdio>
-#include <algorithm>
 #include <cstring>
 #include <string>
 #include <vector>
