@@ -101,3 +101,42 @@ def test_siblings_do_not_see_each_other():
         chain = np.arange(-1, len(p) - 1, dtype=np.int32)
         _, Sc = oracle.gdn_tree(q[p], k[p], v[p], alpha[p], beta[p], S0, chain)
         np.testing.assert_array_equal(Sc[-1], S[i])
+
+
+def _wy_tree(parents, k, v, q, alpha, beta, S0):
+    """Every node of a tree at once, in WY form: with the strict-ancestor
+    mask A_ij (j a proper ancestor of i) and G_i the product of alpha over
+    i's root path, one unit-lower-triangular solve
+    T = I + A * (diag(beta) K K^T), W = T^-1 diag(beta) K, U = T^-1 diag(beta) (V / G),
+    then S_i = G_i [S0 - sum_{j in path(i)} k_j (w_j^T S0 - u_j^T)] and
+    o_i = G_i [S0^T q_i + sum_{j in path(i)} (k_j . q_i) (u_j - S0^T w_j)]."""
+    M = len(parents)
+    anc = np.zeros((M, M))
+    for i in range(M):
+        j = int(parents[i])
+        while j >= 0:
+            anc[i, j] = 1.0
+            j = int(parents[j])
+    path = anc + np.eye(M)
+    G = np.array([np.prod(alpha[np.nonzero(path[i])[0]]) for i in range(M)])
+    T = np.eye(M) + anc * (beta[:, None] * (k @ k.T))
+    W = np.linalg.solve(T, beta[:, None] * k)
+    U = np.linalg.solve(T, beta[:, None] * (v / G[:, None]))
+    D = U - W @ S0                                   # rows: u_j - S0^T w_j
+    o = G[:, None] * (q @ S0 + (path * (q @ k.T)) @ D)
+    S = np.stack([G[i] * (S0 + k.T @ (path[i][:, None] * D)) for i in range(M)])
+    return o, S
+
+
+def test_whole_tree_in_one_masked_wy_solve():
+    for seed in range(3):
+        M = 16
+        parents, q, k, v, alpha, beta, S0 = _inputs(20 + seed, M, 6)
+        o_bits, S = oracle.gdn_tree(q, k, v, alpha, beta, S0, parents)
+        kn = oracle.l2_normalise(oracle.bf16_to_f64(k))
+        qn = oracle.l2_normalise(oracle.bf16_to_f64(q))
+        vv = oracle.bf16_to_f64(v)
+        for h in range(NH):
+            o, Sw = _wy_tree(parents, kn[:, h], vv[:, h], qn[:, h], alpha[:, h], beta[:, h], S0[h])
+            np.testing.assert_allclose(Sw, S[:, h], rtol=1e-9, atol=1e-11)
+            np.testing.assert_allclose(oracle.bf16_to_f64(o_bits[:, h]), o, rtol=2.0 ** -8, atol=1e-6)
