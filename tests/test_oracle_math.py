@@ -226,3 +226,22 @@ def test_phi_is_elu_plus_one():
     x = np.linspace(-5, 5, 101)
     ref = torch.nn.functional.elu(torch.from_numpy(x)).numpy() + 1.0
     assert np.allclose(oracle.phi(x), ref, rtol=1e-15, atol=1e-15)
+
+
+def test_argmax_margin_by_hand():
+    L = np.array([[1.0, 3.0, 2.0, 3.0],      # tie at the top: the smaller index, margin 0
+                  [-5.0, -1.0, -2.0, -7.0],  # margin 1
+                  [0.5, 0.25, 0.125, 0.0]])  # first column wins, margin 0.25
+    idx, margin = oracle.argmax_margin(L)
+    assert list(idx) == [1, 1, 0]
+    assert list(margin) == [0.0, 1.0, 0.25]
+
+
+def test_residual_is_one_rounding_of_the_exact_sum():
+    # 1 + 2^-8 is not a bf16 (7 mantissa bits): ties to even gives 1; 1 + 3*2^-8 rounds up to 1 + 2^-6
+    one, e8 = np.uint16(0x3F80), np.uint16(0x3B80)  # 1.0 and 2^-8
+    three_e8 = np.uint16(0x3C40)                    # 3 * 2^-8 = 1.5 * 2^-7
+    assert int(oracle.residual(np.array([one]), np.array([e8]))[0]) == 0x3F80
+    assert int(oracle.residual(np.array([one]), np.array([three_e8]))[0]) == 0x3F82
+    # exact sums stay exact
+    assert int(oracle.residual(np.array([one]), np.array([one]))[0]) == 0x4000
