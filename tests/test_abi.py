@@ -95,3 +95,33 @@ def test_host_argument_checks(L):
     assert L.sd_best_first_select(None, d, d, 1, 1, 1, 1, None, d, d, d, None, None, d, d, 1 << 20, None) == 1
     assert L.sd_tree_info(ctypes.c_void_p(16), 65, 0, ctypes.c_void_p(16), ctypes.c_void_p(16),
                           ctypes.c_void_p(16), None, None) == 2
+
+
+def test_header_is_plain_c_and_links_from_c(L, tmp_path):
+    """include/sdv.h is a C header (C99, pedantic) and a C program linked
+    against the library calls it (host-only entry points: no GPU)."""
+    import os
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    inc = os.path.join(root, "include")
+    libdir = os.path.dirname(_build.build())
+    src = tmp_path / "use_sdv.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "sdv.h"\n'
+        'int main(void) {\n'
+        '  const char msg[] = "123456789";\n'
+        '  if (w12_crc32(msg, 9) != 0xCBF43926u) return 1;\n'
+        '  if (w12_words_count(16, 64) != 384) return 2;\n'
+        '  if (sd_select_workspace(10) != 216) return 3;\n'
+        '  if (sd_best_first_select(0, 0, 0, 1, 1, 1, 1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0) != SD_ERR_INVALID_ARG) return 4;\n'
+        '  printf("ok\\n");\n  return 0;\n}\n')
+    exe = tmp_path / "use_sdv"
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, str(src), "-L", libdir,
+                        "-lsdv", "-Wl,-rpath," + libdir, "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
