@@ -69,6 +69,21 @@ def parse():
     return ap.parse_args()
 
 
+def oracle_select_rate(c, budget: int, cap: int, reps: int = 3) -> dict:
+    """The oracle's best-first selection on the same candidates, timed on
+    the host (one Python thread): candidates per second, median of reps."""
+    import oracle
+    t = []
+    for _ in range(max(1, reps)):
+        t0 = time.perf_counter()
+        oracle.best_first_select(c.parents, c.logprob, c.cu, budget, cap)
+        t.append(time.perf_counter() - t0)
+    s = statistics.median(t)
+    n = int(c.cu[-1])
+    return {"value": n / s, "unit": "candidates/s", "cores": 1, "kind": "oracle",
+            "sample": f"the whole call ({n} candidates), median of {len(t)}", "s_per_call": s}
+
+
 def select_arm(args):
     """Best-first node selection under a shared node budget alone
     (sd_best_first_select) on seeded synthetic candidate trees: per-call time
@@ -107,10 +122,14 @@ def select_arm(args):
     status = int(sel.status.item())
     # algorithmic bytes: candidates read (parent, log-prob, token), kept nodes written (src, parent, token, score)
     nbytes = N * 12 + (R + 1) * 4 + kept * 16
+    try:
+        cpu = oracle_select_rate(c, budget, cap)
+    except Exception as ex:  # the oracle leg must not cost the GPU figure
+        cpu = {"error": str(ex)[:200]}
     return {"probe": "sd_best_first_select", "R": R, "n": n, "candidates": N, "budget": budget, "cap": cap,
             "kept": kept, "status": status, "us_per_call": us, "candidates_per_s": N / (us * 1e-6),
             "bound": "latency", "bytes": nbytes, "GBps": nbytes / (us * 1e-6) / 1e9,
-            "launches_per_call": 2, "memsets_per_call": 1}
+            "launches_per_call": 2, "memsets_per_call": 1, "cpu_baseline": cpu}
 
 
 def probe_arm(args):

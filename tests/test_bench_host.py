@@ -35,3 +35,11 @@ def test_kv_bytes_of_the_8b_step_match_the_stated_figure():
 
 def test_job_throughput_counts_every_rank():
     assert bench.job_throughput(4, 16, 4.0) == pytest.approx(16000.0)
+
+
+def test_oracle_selection_rate_on_the_probe_inputs():
+    from synthetic import workloads as wl
+    c = wl.candidates(0, 4, 64, 8, 32000)
+    r = bench.oracle_select_rate(c, 32, 16, reps=2)
+    assert r["kind"] == "oracle" and r["cores"] == 1 and r["unit"] == "candidates/s"
+    assert r["value"] == pytest.approx(256 / r["s_per_call"])
