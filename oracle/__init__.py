@@ -353,6 +353,13 @@ def linrec_literal(q_bits, k_bits, v_bits, S0, z0, parents, eps):
     return round_bf16(o), S, z
 
 
+def gdn_commit(S_nodes: np.ndarray, acc: "Accept") -> np.ndarray:
+    """The committed state after a verify over a gated-delta-rule tree: the
+    state of the deepest accepted node (the path root .. acc.last is what the
+    sequence now holds), [nh][hd][hd]."""
+    return S_nodes[acc.last].copy()
+
+
 def l2_normalise(x: np.ndarray) -> np.ndarray:
     """x / ||x|| over the last axis (zero vectors stay zero)."""
     n = np.sqrt(np.sum(x * x, axis=-1, keepdims=True))

@@ -140,3 +140,21 @@ def test_whole_tree_in_one_masked_wy_solve():
             o, Sw = _wy_tree(parents, kn[:, h], vv[:, h], qn[:, h], alpha[:, h], beta[:, h], S0[h])
             np.testing.assert_allclose(Sw, S[:, h], rtol=1e-9, atol=1e-11)
             np.testing.assert_allclose(oracle.bf16_to_f64(o_bits[:, h]), o, rtol=2.0 ** -8, atol=1e-6)
+
+
+def test_commit_is_the_accepted_path_run_as_a_chain():
+    # after acceptance the state is that of the deepest accepted node, the
+    # same as running the rule over the accepted path alone
+    parents, q, k, v, alpha, beta, S0 = _inputs(30, 12, 5)
+    _, S = oracle.gdn_tree(q, k, v, alpha, beta, S0, parents)
+    toks = np.arange(12, dtype=np.int32) + 100
+    am = np.zeros(12, dtype=np.int32)
+    leaf = 11
+    path = _path(parents, leaf)
+    for a, b in zip(path[:-1], path[1:]):  # the target agrees with the tokens along this path only
+        am[a] = toks[b]
+    acc = oracle.accept(toks, parents, am)
+    assert acc.last == leaf and acc.path == path
+    chain = np.arange(-1, len(path) - 1, dtype=np.int32)
+    _, Sc = oracle.gdn_tree(q[path], k[path], v[path], alpha[path], beta[path], S0, chain)
+    np.testing.assert_array_equal(oracle.gdn_commit(S, acc), Sc[-1])
