@@ -31,9 +31,9 @@ sys.path.insert(0, ROOT)
 
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NOMINAL_BW_GBS = 8000.0       # the metric's "fraction of 8 TB/s"
-# DRAM bytes (read + write) of one k_w12_gemm gate/up launch, 8B shape,
-# M = 16, from an ncu --set full capture of that launch (the probe command)
-GATE_UP_TRAFFIC_8B = 151.707904e6 + 4.178176e6
+# DRAM bytes (read + write) per launch of the dominant kernel, from ncu
+# captures (profiles/): none yet for the streamed launch
+STREAM_TRAFFIC = {}
 
 
 def peaks():
@@ -55,8 +55,6 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--timeline", action="store_true", help="print the per-kernel breakdown to stderr")
-    ap.add_argument("--chain", action="store_true",
-                    help="run each layer's GEMMs and RMSNorms as one persistent chain launch")
     ap.add_argument("--nvtx", action="store_true", help="wrap the timed steps in the NVTX range 'sdv_step'")
     ap.add_argument("--probe", default=None, metavar="N,K,M",
                     help="time the fused W12 linear alone on an N x K tensor with M rows")
@@ -304,87 +302,6 @@ def kv_bytes_per_step(shape, ctx, M):
     return attn + rec
 
 
-def chain_phase_summary(model, launch):
-    """Per phase of one chain launch: when the CTAs' first stage was ready,
-    their last stage consumed and the phase finished, in us after the previous
-    phase's last CTA finished (the first CTA's start for phase 0), as
-    [median, max] over the CTAs that had work."""
-    import numpy as np
-    try:
-        st = model.chain_trace(launch).astype(np.int64)
-    except Exception as e:  # no chain launch in the timed step
-        return {"error": str(e)}
-    n = (st.shape[0] - 1) // 3
-    prev = int(st[0].min())
-    out = [{"start": [round(float(np.median(st[0]) - prev) / 1e3, 2), round(float(st[0].max() - prev) / 1e3, 2)]}]
-    for p in range(n):
-        row = {}
-        for name, r in (("first_ready", 1 + 3 * p), ("last_consumed", 2 + 3 * p), ("finished", 3 + 3 * p)):
-            v = st[r][st[r] > 0]
-            row[name] = [round(float(np.median(v) - prev) / 1e3, 2), round(float(v.max() - prev) / 1e3, 2)] if v.size else None
-        out.append(row)
-        prev = int(st[3 + 3 * p].max())
-    res = {"chain_launch": launch, "phases_us_median_max": out}
-    if n == 1:
-        # spread of the stream end over the CTAs, and the slowest CTAs
-        lc = (st[2] - st[0].min()) / 1e3
-        res["last_consumed_pct"] = [round(float(np.percentile(lc, q)), 2) for q in (10, 50, 90, 99)]
-        res["slowest_ctas"] = [int(i) for i in np.argsort(lc)[-12:]]
-        res["fastest_ctas"] = [int(i) for i in np.argsort(lc)[:12]]
-    return res
-
-
-def attention_trace_summary(model, record):
-    """Per-CTA device-clock stamps of one traced attention launch: start,
-    keys done, group ready and end (us after the first CTA start) as
-    percentiles over the CTAs with rows, and the CTA durations."""
-    import numpy as np
-    try:
-        st = model.chain_trace(record).astype(np.int64)
-    except Exception as e:
-        return {"error": str(e)}
-    t0 = int(st[0].min())
-    busy = st[1] > st[0]
-    out = {"attention_record": record, "ctas": int(st.shape[1]), "ctas_with_rows": int(busy.sum())}
-    for name, r in (("start", 0), ("keys_done", 1), ("group_ready", 2), ("end", 3)):
-        v = (st[r][busy] - t0) / 1e3
-        out[name] = [round(float(np.percentile(v, q)), 2) for q in (0, 10, 50, 90, 100)]
-    d = (st[3][busy] - st[0][busy]) / 1e3
-    k = (st[1][busy] - st[0][busy]) / 1e3
-    out["cta_us"] = [round(float(np.percentile(d, q)), 2) for q in (10, 50, 90, 100)]
-    out["cta_keys_us"] = [round(float(np.percentile(k, q)), 2) for q in (10, 50, 90, 100)]
-    return out
-
-
-def overlapped_layer_trace(model, stream, step, layer):
-    """Device-clock stamps of one layer's GEMMs in an untimed-style step
-    (programmatic dependent launch, no events): per GEMM, the first CTA start,
-    the median first stage, the last stream end and the last CTA finish, in us
-    after the layer's first GEMM start."""
-    import numpy as np
-    import torch
-    model.set_timing(2)
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            step()
-    torch.cuda.synchronize()
-    # traced launches: qkv of layer 0, then per layer attention, o, gate_up, down, next qkv
-    names = ["attention", "o", "gate_up", "down", "qkv_next"]
-    rows = []
-    t0 = None
-    for i in range(5):
-        st = model.chain_trace(1 + layer * 5 + i).astype(np.int64)
-        if t0 is None:
-            t0 = int(st[0].min())
-        rows.append({"kernel": names[i], "start": round((st[0].min() - t0) / 1e3, 2),
-                     "row1_med": round((np.median(st[1]) - t0) / 1e3, 2),
-                     "row2_max": round((st[2].max() - t0) / 1e3, 2),
-                     "end_max": round((st[3].max() - t0) / 1e3, 2)})
-    model.set_timing(False)
-    return {"overlapped_layer": layer, "rows": "gemm: start, first stage (median), last stream end, last finish; "
-            "attention: start, keys done (median), group ready (max), end", "kernels": rows}
-
-
 def step_distribution(times_ms) -> dict:
     """Median, 10th / 90th percentiles and a 95% confidence interval of the
     mean (normal approximation) of individually timed steps."""
@@ -399,9 +316,8 @@ def step_distribution(times_ms) -> dict:
 
 def overhead_factor(step_ms: float, timeline) -> tuple:
     """Step time over the sum of its kernels' serialised, event-timed
-    durations (phases nested in a chain launch, "chain.*", are not added
-    twice): below 1 where programmatic dependent launch overlaps kernels."""
-    total = sum(t for k, t, _ in timeline if not k.startswith("chain."))
+    durations: below 1 where programmatic dependent launch overlaps kernels."""
+    total = sum(t for _, t, _ in timeline)
     return (step_ms / total if total > 0 else None), total
 
 
@@ -444,7 +360,6 @@ def gpu_arm(args, rank, world, dist):
     if R == 1:
         M = spec.M
         model = Mdl.Model(shape, W, max_rows=M, max_requests=1, max_positions=ctx + M + 64)
-        model.set_chain(args.chain)
         kv = Mdl.KVCache(shape, ctx + M + 16).fill(args.seed, ctx)
         log(f"[rank {rank}] model built in {time.time() - t0:.1f}s, packed {model.packed_bytes / 1e9:.2f} GB")
         td = spec.drafts[0]
@@ -580,39 +495,28 @@ def gpu_arm(args, rank, world, dist):
             step()
     torch.cuda.synchronize()
     tl = model.timeline()
-    chain_phases = None
-    if args.timeline and M < tc_rows:
-        # the middle layer's launches (a chain, or its four GEMMs after its attention)
-        per_layer = 1 if args.chain else 4
-        first = 2 + (shape.n_layers // 2) * 5 if not args.chain else shape.n_layers // 2
-        chain_phases = [chain_phase_summary(model, first + i) for i in range(per_layer)]
-        if not args.chain and shape.n_rec == 0:
-            # trace records: layer 0's q/k/v, then per layer attention, o, gate/up, down, next q/k/v
-            chain_phases.append(attention_trace_summary(model, 1 + (shape.n_layers // 2) * 5))
-    elif args.timeline:
-        # tcgen05 GEMM launches are not traced: only the attention launches are
-        chain_phases = [attention_trace_summary(model, shape.n_layers // 2)]
     model.set_timing(False)
-    overlap = None
-    if args.timeline and not args.chain and M < tc_rows and shape.n_rec == 0:
-        overlap = overlapped_layer_trace(model, stream, step, shape.n_layers // 2)
 
     ms, ms_e2e = slowest_rank(ms, ms_e2e, dist, dev)
 
     pk, pk_src = peaks()
-    gemm = [(k, t, b) for k, t, b in tl if k.startswith("gemm")]  # chain launches and lone GEMMs (not their traces)
+    gemm = [(k, t, b) for k, t, b in tl if k.startswith("gemm")]  # streamed launches or single GEMMs
     g_ms = sum(t for _, t, _ in gemm)
     g_bytes = sum(b for _, _, b in gemm)
     all_gemm_gbs = g_bytes / (g_ms * 1e-3) / 1e9 if g_ms > 0 else None
-    # the dominant kernel: k_w12_gemm on the gate/up shape (the largest GEMM of
-    # a layer), algorithmic bytes per launch / its mean event-timed launch
-    gu = [(t, b) for k, t, b in tl if k == "gemm_gate_up"]
-    gu_ms = sum(t for t, _ in gu) / len(gu) if gu else None
-    gu_bytes = gu[0][1] if gu else None
-    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9 if gu else all_gemm_gbs
-    # DRAM read + write of one gate/up launch from the ncu capture of this
-    # kernel, for the 8B shape only
-    traffic = GATE_UP_TRAFFIC_8B if (gu and shape.name == "8b" and M == 16) else None
+    # the dominant kernel: a layer's streamed launch (O, gate/up, down and the
+    # next q/k/v: the weights of a whole layer), or, on the tcgen05 path, the
+    # gate/up GEMM; algorithmic bytes per launch / its mean event-timed launch
+    dom_kind = "gemm_stream" if any(k == "gemm_stream" for k, _, _ in tl) else "gemm_gate_up"
+    dom = [(t, b) for k, t, b in tl if k == dom_kind]
+    if dom_kind == "gemm_stream":
+        # the per-layer launches (the first launch holds layer 0's q/k/v only)
+        big = max(b for _, b in dom)
+        dom = [(t, b) for t, b in dom if b > 0.5 * big]
+    dom_ms = sum(t for t, _ in dom) / len(dom) if dom else None
+    dom_bytes = sum(b for _, b in dom) / len(dom) if dom else None
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom else all_gemm_gbs
+    traffic = STREAM_TRAFFIC.get((shape.name, M, dom_kind))
     peak = pk["hbm_gbs"]
     ctx_sum = int(sum(spec.ctx))  # every request's prefix
     step_bytes = model.packed_bytes + kv_bytes_per_step(shape, ctx_sum, M)
@@ -630,10 +534,6 @@ def gpu_arm(args, rank, world, dist):
     if args.timeline:
         log(json.dumps({k: {"launches": v[0], "ms": round(v[1], 4), "GB/s": round(v[2] / v[1] / 1e6, 1) if v[2] else None}
                         for k, v in by_kind.items()}))
-        if chain_phases:
-            log(json.dumps(chain_phases))
-        if overlap:
-            log(json.dumps(overlap))
     value = job_throughput(world, M, ms)
     ovh, kernel_sum = overhead_factor(ms, tl)
     res = {
@@ -642,7 +542,7 @@ def gpu_arm(args, rank, world, dist):
         "verify_step_us": ms * 1e3, "host_submit_us_per_step": t_host * 1e6, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "model": shape.name, "layers": shape.n_layers, "M": M,
-                   "requests": R, "gemm_chain": bool(args.chain), "tc_min_rows": tc_rows,
+                   "requests": R, "tc_min_rows": tc_rows,
                    "attn_splits": attn_splits or "auto",
                    "max_depth": spec.max_depth, "ctx": ctx, "p_copy": spec.p, "accepted_len": acc_len,
                    "parallelism": "replicas" if world > 1 else "single",
@@ -656,10 +556,11 @@ def gpu_arm(args, rank, world, dist):
         "kernel_sum_ms": kernel_sum, "overhead_factor": ovh,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak if achieved else None, "traffic": traffic,
-                     "kernel": ("k_w12_gemm, gate/up launches (algorithmic bytes per launch / mean event-timed "
-                                "launch; traffic from the committed ncu capture)" if gu else
-                                "k_w12_chain + k_w12_gemm (all GEMM chain / GEMM launches of a step, event-timed)"),
-                     "algorithmic_bytes_per_launch": gu_bytes, "launch_ms": gu_ms,
+                     "kernel": ("k_w12_stream, the per-layer launches (O, gate/up, down, next q/k/v): algorithmic "
+                                "bytes per launch / mean event-timed launch" if dom_kind == "gemm_stream" else
+                                "k_w12_gemm_tc, gate/up launches (algorithmic bytes per launch / mean event-timed "
+                                "launch)"),
+                     "algorithmic_bytes_per_launch": dom_bytes, "launch_ms": dom_ms,
                      "all_gemm_launches_gbs": all_gemm_gbs,
                      "peak_source": pk_src},
         "kernels": {k: {"launches": v[0], "ms": v[1]} for k, v in by_kind.items()},

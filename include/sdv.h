@@ -254,6 +254,13 @@ int w12c_unpack_host(const uint32_t* words, const uint8_t* base, int64_t N, int6
  * escape index >= N*K). */
 int w12_plane8_pack_host(const uint16_t* w, int64_t N, int64_t K, const uint8_t* table, int32_t n_table,
                          uint32_t* plane);
+/* The same plane on the device: from the bf16 weights w [N][K] (device),
+ * with the code table of meta (w12_pack_analyze) and the optional row order
+ * row_src of w12_pack_encode, into plane (device,
+ * w12_plane8_words_count(N, K) u32, caller-allocated).  Asynchronous on
+ * `stream`.  Errors: SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED (shape). */
+int64_t w12_plane8_words_count(int64_t N, int64_t K);
+int w12_plane8_pack(const uint16_t* w, const int32_t* row_src, const w12_meta* meta, uint32_t* plane, void* stream);
 int w12_plane8_unpack_host(const uint32_t* plane, int64_t N, int64_t K, const uint8_t* table, int32_t n_table,
                            const uint32_t* esc_idx, const uint16_t* esc_val, int64_t n_escapes, uint16_t* w);
 
@@ -298,6 +305,46 @@ int w12_load(const char* path, uint32_t* words, uint32_t* esc_idx, uint16_t* esc
              uint32_t* tile_ptr, uint32_t* tile_esc, w12_meta* meta);
 
 /* ------------------------------------------ best-first node selection -- */
+/* Gated delta rule over draft trees, in WY form ("SpecPilot: AI Agent
+ * Framework Boosts Speculative Decoding 10.87x", "(2) Best-first Tree
+ * Verification for Hybrid Architectures": Gated DeltaNet layers recompute
+ * the state along each root path; a WY-form kernel evaluates many paths at
+ * once).  Per request and head, q and k L2-normalised (zero stays zero):
+ *   S_i = alpha_i (I - beta_i k_i k_i^T) S_parent(i) + beta_i k_i v_i^T,
+ *   o_i = S_i^T q_i   (bf16),
+ * S_root's parent state being the committed state S.  Evaluated for every
+ * node at once (one unit-lower-triangular solve over the tree's ancestor
+ * mask; S read once per request and head; no per-node state formed).
+ *
+ * Input (device): R requests, request r owning rows cu[r] .. cu[r+1]-1 (cu
+ * int32 [R+1] on the device, the same values in cu_host; 1..64 rows per
+ * request); q, k, v bf16 [rows][nh][128]; alpha (gate, in (0, 1]) and beta
+ * (write strength, in [0, 1]) fp32 [rows][nh]; parents int32 [rows], local
+ * to the request (root first with parent -1, 0 <= parent[i] < i); S fp32
+ * [R][nh][128][128] (row = key dimension), not modified.  The path products
+ * of alpha must stay in fp32's normal range.
+ * Output: out bf16 [rows][nh][128]; workspace (sd_gdn_workspace(rows, nh)
+ * bytes, 256-byte aligned, any content) receives what sd_gdn_commit needs.
+ * A request whose parent array is invalid sets *status (device int32) to
+ * SD_ERR_BAD_TREE and leaves its outputs unwritten.  Asynchronous on
+ * `stream`.  Errors: SD_ERR_INVALID_ARG (null pointer, bad cu_host),
+ * SD_ERR_UNSUPPORTED (a request outside 1..64 rows), SD_ERR_WORKSPACE. */
+size_t sd_gdn_workspace(int32_t rows, int32_t nh);
+int sd_gdn_tree_verify(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha, const float* beta,
+                       const int32_t* parents, const int32_t* cu, const int32_t* cu_host, int32_t R, int32_t nh,
+                       const float* S, uint16_t* out, void* workspace, size_t workspace_bytes, int32_t* status,
+                       void* stream);
+
+/* After acceptance: S of request r becomes the state of its node last[r]
+ * (device int32 [R], local index; the deepest accepted node), i.e. the rule
+ * run over that node's root path ("(3) Two-Level Verification": only the
+ * exact verification commits state).  Uses the workspace of the
+ * sd_gdn_tree_verify call on the same inputs, which must precede it on
+ * `stream`.  A request with last[r] outside its rows keeps its state.  S is
+ * updated in place. */
+int sd_gdn_commit(const int32_t* parents, const int32_t* cu, const int32_t* cu_host, int32_t R, int32_t nh,
+                  const int32_t* last, float* S, const void* workspace, size_t workspace_bytes, void* stream);
+
 /* [SELECT] Best-first selection of the nodes one batched verify checks,
  * under a node budget the requests share ("SpecPilot: AI Agent Framework
  * Boosts Speculative Decoding 10.87x", "(2) Best-first Tree Verification
@@ -455,6 +502,25 @@ int sd_verify_step(sd_model* m, const int32_t* tree_tokens, const int32_t* paren
 int sd_forward(sd_model* m, const int32_t* tree_tokens, const int32_t* parents, int32_t M, const sd_kv* kv,
                uint16_t* logits, int32_t* argmax, void* stream);
 
+/* Two-level verification ("SpecPilot: AI Agent Framework Boosts Speculative
+ * Decoding 10.87x", "(3) Two-Level Verification"): round one runs the draft
+ * tree on W12's nested 8-bit weight view, each weight with its 4 low
+ * mantissa bits cleared, streaming 1 byte per weight; it produces argmax
+ * (and logits) per node and accepts and commits nothing - its greedy walk
+ * (sd_accept) gives the candidate chain the drafter continues from, and
+ * one exact sd_verify_step of the chain and the new drafts decides.
+ * sd_model_set_view8 registers the planes (w12_plane8_pack of each W12
+ * tensor with the row order it was packed with; device, borrowed, 16-byte
+ * aligned): planes_host[4 l + 0..3] = layer l's qkv, o, gate_up, down, then
+ * planes_host[4 n_layers] = the lm_head's; n = 4 n_layers + 1.
+ * sd_forward_view8 is sd_forward over the view; it needs the streamed step
+ * (M below the tensor-core threshold, sd_gemm_set_tc_min_rows) and the
+ * registered planes, else SD_ERR_UNSUPPORTED.  The new K/V it writes to
+ * slots ctx + node are the view's (an exact step rewrites them). */
+int sd_model_set_view8(sd_model* m, const uint32_t* const* planes_host, int32_t n);
+int sd_forward_view8(sd_model* m, const int32_t* tree_tokens, const int32_t* parents, int32_t M, const sd_kv* kv,
+                     uint16_t* logits, int32_t* argmax, void* stream);
+
 /* Batched verify of R requests over a paged cache: request r owns nodes
  * [cu_nodes_host[r], cu_nodes_host[r+1]) of tokens/parents (parents local to
  * the request, <= 64 nodes each).  Every GEMM processes all rows at once;
@@ -465,13 +531,25 @@ int sd_verify_batch(sd_model* m, const int32_t* tokens, const int32_t* parents, 
                     int32_t* bonus, uint16_t* logits, int32_t* argmax, void* stream);
 
 /* Copy the device status word of the model's last calls (synchronises the
- * device) and clear it; after a non-zero status the GEMM chain's grid barrier
- * is also reset. */
+ * device) and clear it; after a non-zero status the counters of the
+ * streamed GEMM launches are also cleared (a launch that gave up on a wait
+ * may have left them set). */
 int sd_status(sd_model* m, int32_t* status_host);
 
 /* Number of kernels the last sd_verify_step / sd_forward / sd_verify_batch
  * call launched. */
 int sd_model_last_launches(sd_model* m);
+
+/* The final RMSNorm's output of the last sd_verify_step / sd_forward /
+ * sd_verify_batch call: the lm_head's input, bf16 [rows][hidden], rows in
+ * the call's row order ("(2) Best-first Tree Verification ...": every node
+ * is scored by the target's lm_head over this state).  Copied device to
+ * device into the caller's `out` on `stream`, ordered after the step when
+ * issued on the step's stream; valid until the next call on the model.
+ * rows must be 1..max_rows (SD_ERR_INVALID_ARG otherwise).  A test tap:
+ * with it, the argmax decision of a step can be checked against the lm_head
+ * applied to the very state the step scored. */
+int sd_model_final_hidden(sd_model* m, uint16_t* out, int32_t rows, void* stream);
 
 /* Step execution mode.  With enable = 1 (the default), a call on a
  * non-default stream that is not itself being captured is recorded once per
@@ -482,43 +560,13 @@ int sd_model_last_launches(sd_model* m);
  * stream and inside a caller's own stream capture). */
 int sd_model_set_graphs(sd_model* m, int32_t enable);
 
-/* GEMM chaining (no counterpart in the pages: an execution choice of this
- * library).  With enable = 1 (default 0) and fewer rows per step than the
- * tcgen05 threshold (sd_gemm_set_tc_min_rows; at most 128),
- * each run of GEMMs and RMSNorms between two attention / recurrence kernels
- * (O + residual, RMSNorm, gate/up + SiLU, down + residual, RMSNorm, the next
- * layer's q/k/v or the lm_head) is executed by one persistent kernel whose
- * phases are separated by grid barriers, so weight streaming continues across
- * phase boundaries.  enable = 0 launches every GEMM and RMSNorm as its own
- * kernel, chained by programmatic dependent launch (faster on GB300 for the
- * 8B-class step: a kernel's early CTAs start the next GEMM while its last
- * CTAs finish, which a grid barrier forbids).  Results are identical up to the order of fp32 additions inside
- * the GEMMs (none: both modes use the same partition and summation order).
- * Returns SD_OK or SD_ERR_INVALID_ARG for a null model. */
-int sd_model_set_chain(sd_model* m, int32_t enable);
-
-/* Raw device-clock stamps (%globaltimer, ns) of traced launch `launch` (0 =
- * the first) of the last timed step - every chain launch, every lone GEMM
- * launch on the warp-level kernel (fewer rows than the tcgen05 threshold)
- * and every attention launch as a one-phase
- * record (attention rows: start, keys done, group's partials ready, end):
- * *n_phases = n, *n_ctas = G
- * and, when stamps_host is not NULL (room for max_stamps >= (1 + 3n) G
- * values), stamps_host[r * G + c] for CTA c: r = 0 its start; for phase i,
- * r = 1 + 3i when its first stage was ready (RMSNorm phase: input complete),
- * r = 2 + 3i when its last stage was consumed (RMSNorm: rows written), r = 3 +
- * 3i when it finished the phase (0 = not written: no work in that phase).
- * Synchronises the device when copying.  SD_ERR_INVALID_ARG for a launch the
- * last timed step does not have or a short buffer. */
-int sd_model_chain_trace(sd_model* m, int32_t launch, int32_t* n_phases, int32_t* n_ctas, uint64_t* stamps_host,
-                         int64_t max_stamps);
-
-/* Kernel kinds reported by sd_model_timeline (SD_K_GEMM_CHAIN: one chain
- * launch; its bytes are those of the GEMMs it runs). */
+/* Kernel kinds reported by sd_model_timeline (SD_K_GEMM_STREAM: one
+ * streamed launch of several GEMMs; its bytes are those of the GEMMs it
+ * runs). */
 enum {
   SD_K_TREE = 0, SD_K_NORM = 1, SD_K_GEMM_QKV = 2, SD_K_ATTN = 3, SD_K_LINREC = 4, SD_K_GEMM_O = 5,
   SD_K_GEMM_GATE_UP = 6, SD_K_GEMM_DOWN = 7, SD_K_GEMM_LM_HEAD = 8, SD_K_ACCEPT = 9, SD_K_COMMIT = 10,
-  SD_K_GEMM_CHAIN = 11
+  SD_K_GEMM_STREAM = 11
 };
 
 /* Per-kernel timing of the following model calls: with enable = 1 every
@@ -530,23 +578,13 @@ enum {
  * steps are slower than untimed ones; use the numbers for the breakdown,
  * not the step time. */
 int sd_model_set_timing(sd_model* m, int32_t enable);
-/* (enable = 2: device-clock traces only - no events and no delay kernel,
- * kernels launched directly with programmatic dependent launch as in an
- * untimed step, so the traces show the overlapped schedule; the timeline
- * then has no event-timed entries worth reading, use sd_model_chain_trace.) */
 
 /* Timeline of the last timed call: for entry i, kind_host[i] (SD_K_*),
  * ms_host[i] (event-measured duration) and bytes_host[i] (algorithmic bytes
- * of a GEMM: packed words, escape tile index, activations read and written;
- * 0 for other kinds).  Each traced launch (every SD_K_GEMM_CHAIN entry, and
- * each lone warp-level GEMM) is followed by one entry per phase
- * with kind 100 + the phase's kind (SD_K_GEMM_O, SD_K_NORM, ...): its time
- * runs from the last CTA finishing the previous phase (the first CTA
- * starting, for the first phase) to the last CTA finishing this one, read
- * from the device clock (%globaltimer); these entries overlap their launch's
- * entry.
- * Synchronises the device.  Returns the number of entries written (<= max),
- * or -1 with sd_last_error set. */
+ * of the GEMMs of the launch: packed words, escape tile index, activations
+ * read and written; an RMSNorm's rows read and written; 0 for other
+ * kinds).  Synchronises the device.  Returns the number of entries written
+ * (<= max), or -1 with sd_last_error set. */
 int sd_model_timeline(sd_model* m, int32_t max, int32_t* kind_host, float* ms_host, double* bytes_host);
 
 #ifdef __cplusplus

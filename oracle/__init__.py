@@ -218,9 +218,23 @@ def linear(x: np.ndarray, W: np.ndarray) -> np.ndarray:
     return y
 
 
-def linear_bf16(x: np.ndarray, W: np.ndarray) -> np.ndarray:
+def linear_bf16(x: np.ndarray, W: np.ndarray, gemm=None) -> np.ndarray:
     """A GEMM kernel boundary: bf16(x W^T)."""
-    return round_bf16(linear(x, W))
+    return round_bf16((gemm or linear)(x, W))
+
+
+def linear_f32(x: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """y = x W^T with every product and sum in fp32 (the products of two bf16
+    values are exact in fp32; the summation order is numpy's).  Not part of
+    the definition: the fp32-accumulation twin of ``linear``, used to measure
+    how far an implementation that sums in fp32 (as the workloads' rule
+    allows) may move from the fp64 oracle through the bf16 rounding points
+    downstream."""
+    if x.dtype == np.uint16:
+        x = bf16_to_f64(x)
+    xf = np.asarray(x, dtype=np.float32)
+    Wf = bf16_to_f64(W).astype(np.float32)
+    return (xf @ Wf.T).astype(np.float64)
 
 
 # -------------------------------------------------------------- layers ----
@@ -473,7 +487,7 @@ class ForwardOut:
     infos: list                    # TreeInfo per request
 
 
-def forward(shape, weights, requests: list, n_layers: int | None = None) -> ForwardOut:
+def forward(shape, weights, requests: list, n_layers: int | None = None, gemm=None) -> ForwardOut:
     """One verify forward over the draft trees of all requests.
 
     Every GEMM sees the rows of all requests together (rows never interact);
@@ -481,7 +495,9 @@ def forward(shape, weights, requests: list, n_layers: int | None = None) -> Forw
       h = x + O(mix(RMSNorm(x)));  x' = h + down(silu(gate(n)) * up(n)), n = RMSNorm(h)
     with mix = tree attention (RoPE on q,k at position ctx + depth) or the
     tree linear recurrence.  Final RMSNorm then lm_head.  ``n_layers`` runs
-    only the first layers (a bounded sample for timing)."""
+    only the first layers (a bounded sample for timing); ``gemm`` replaces
+    ``linear`` in every GEMM (``linear_f32``: the fp32-accumulation twin)."""
+    gemm = gemm or linear
     hd, Hq, Hkv, eps = shape.hd, shape.Hq, shape.Hkv, shape.eps
     infos = [tree_info(r.parents) for r in requests]
     for inf in infos:
@@ -497,9 +513,9 @@ def forward(shape, weights, requests: list, n_layers: int | None = None) -> Forw
     for l, kind in enumerate(kinds):
         xn = rmsnorm(x, weights.norm(l, "attn"), eps)
         if kind == "attn":
-            q = linear_bf16(xn, weights.layer(l, "wq")).reshape(Mt, Hq, hd)
-            k = linear_bf16(xn, weights.layer(l, "wk")).reshape(Mt, Hkv, hd)
-            v = linear_bf16(xn, weights.layer(l, "wv")).reshape(Mt, Hkv, hd)
+            q = linear_bf16(xn, weights.layer(l, "wq"), gemm).reshape(Mt, Hq, hd)
+            k = linear_bf16(xn, weights.layer(l, "wk"), gemm).reshape(Mt, Hkv, hd)
+            v = linear_bf16(xn, weights.layer(l, "wv"), gemm).reshape(Mt, Hkv, hd)
             q = rope(q, pos, shape.rope_base)
             k = rope(k, pos, shape.rope_base)
             att = np.empty((Mt, Hq, hd), dtype=np.uint16)
@@ -510,25 +526,25 @@ def forward(shape, weights, requests: list, n_layers: int | None = None) -> Forw
             new_kv.append((k, v))
         else:
             nh = shape.H // hd
-            q = linear_bf16(xn, weights.layer(l, "wq")).reshape(Mt, nh, hd)
-            k = linear_bf16(xn, weights.layer(l, "wk")).reshape(Mt, nh, hd)
-            v = linear_bf16(xn, weights.layer(l, "wv")).reshape(Mt, nh, hd)
+            q = linear_bf16(xn, weights.layer(l, "wq"), gemm).reshape(Mt, nh, hd)
+            k = linear_bf16(xn, weights.layer(l, "wk"), gemm).reshape(Mt, nh, hd)
+            v = linear_bf16(xn, weights.layer(l, "wv"), gemm).reshape(Mt, nh, hd)
             att = np.empty((Mt, nh, hd), dtype=np.uint16)
             for r, req in enumerate(requests):
                 a, b = seg[r], seg[r + 1]
                 st = req.layers[l]
                 att[a:b], _, _ = linrec_literal(q[a:b], k[a:b], v[a:b], st.S, st.z, req.parents, shape.rec_eps)
             new_kv.append((k, v))
-        o = linear_bf16(att.reshape(Mt, -1), weights.layer(l, "wo"))
+        o = linear_bf16(att.reshape(Mt, -1), weights.layer(l, "wo"), gemm)
         h = residual(x, o)
         hn = rmsnorm(h, weights.norm(l, "mlp"), eps)
-        g = linear_bf16(hn, weights.layer(l, "w_gate"))
-        u = linear_bf16(hn, weights.layer(l, "w_up"))
+        g = linear_bf16(hn, weights.layer(l, "w_gate"), gemm)
+        u = linear_bf16(hn, weights.layer(l, "w_up"), gemm)
         a_ = silu_mul(g, u)
-        d = linear_bf16(a_, weights.layer(l, "w_down"))
+        d = linear_bf16(a_, weights.layer(l, "w_down"), gemm)
         x = residual(h, d)
     xf = rmsnorm(x, weights.final_norm(), eps)
-    logits = linear(xf, weights.lm_head())
+    logits = gemm(xf, weights.lm_head())
     idx, margin = argmax_margin(logits)
     return ForwardOut(logits, idx, margin, new_kv, infos)
 

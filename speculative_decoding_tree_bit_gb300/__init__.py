@@ -103,15 +103,22 @@ _SIGS = {
     "sd_verify_batch": (ctypes.c_int, [vp, vp, vp, vp, i32, P(PagedKV), vp, vp, vp, vp, vp, vp]),
     "sd_status": (ctypes.c_int, [vp, vp]),
     "sd_model_last_launches": (ctypes.c_int, [vp]),
+    "sd_model_final_hidden": (ctypes.c_int, [vp, vp, i32, vp]),
+    "sd_model_set_view8": (ctypes.c_int, [vp, vp, i32]),
+    "sd_forward_view8": (ctypes.c_int, [vp, vp, vp, i32, P(KV), vp, vp, vp]),
+    "w12_plane8_words_count": (i64, [i64, i64]),
+    "w12_plane8_pack": (ctypes.c_int, [vp, vp, P(W12Meta), vp, vp]),
+    "sd_gdn_workspace": (ctypes.c_size_t, [i32, i32]),
+    "sd_gdn_tree_verify": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, ctypes.c_size_t, vp,
+                                          vp]),
+    "sd_gdn_commit": (ctypes.c_int, [vp, vp, vp, i32, i32, vp, vp, vp, ctypes.c_size_t, vp]),
     "sd_model_set_timing": (ctypes.c_int, [vp, i32]),
     "sd_model_set_graphs": (ctypes.c_int, [vp, i32]),
-    "sd_model_set_chain": (ctypes.c_int, [vp, i32]),
-    "sd_model_chain_trace": (ctypes.c_int, [vp, i32, vp, vp, vp, ctypes.c_int64]),
     "sd_model_timeline": (ctypes.c_int, [vp, i32, vp, vp, vp]),
 }
 
 KERNEL_KINDS = ["tree", "rmsnorm", "gemm_qkv", "attention", "linrec", "gemm_o", "gemm_gate_up", "gemm_down",
-                "gemm_lm_head", "accept", "commit", "gemm_chain"]
+                "gemm_lm_head", "accept", "commit", "gemm_stream"]
 
 _lib = None
 _lock = threading.Lock()

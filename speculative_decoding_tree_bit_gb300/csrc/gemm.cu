@@ -33,6 +33,7 @@
 #include <mutex>
 
 #include "gemm_impl.cuh"
+#include "stream.cuh"
 
 namespace sdv {
 
@@ -270,6 +271,33 @@ int make_w_map(CUtensorMap* map, const w12_tensor& W) {
   return SD_OK;
 }
 
+// The 8-bit plane as a 2-D tensor of u64: [strips][K/64 * 128]; one box is
+// 128 u64 (one strip's 1024-byte super-tile) x 8 strips.
+int make_w8_map(CUtensorMap* map, const uint32_t* plane, int64_t N, int64_t K) {
+  auto fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled unavailable");
+    return SD_ERR_CUDA;
+  }
+  if (reinterpret_cast<uintptr_t>(plane) & 15) {
+    set_error("gemm: the 8-bit plane must be 16-byte aligned");
+    return SD_ERR_INVALID_ARG;
+  }
+  const int64_t KT = K / 64;
+  cuuint64_t dims[2] = {(cuuint64_t)KT * 128, (cuuint64_t)(N / 16)};
+  cuuint64_t strides[1] = {(cuuint64_t)KT * 1024};
+  cuuint32_t box[2] = {128, (cuuint32_t)kRB};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint32_t*>(plane), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (8-bit plane) failed: " + std::to_string((int)r));
+    return SD_ERR_CUDA;
+  }
+  return SD_OK;
+}
+
 template <int NT, bool AFF>
 static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, const CUtensorMap& wmap, cudaStream_t s,
                              bool pdl, int grid) {
@@ -371,11 +399,28 @@ extern "C" int32_t sd_gemm_set_tc_min_rows(int32_t rows) {
   return gemm_tc_min_rows();
 }
 
+static size_t al256b(size_t x) { return (x + 255) & ~size_t(255); }
+
+// One streamed phase (M <= 128 below the tensor-core threshold): scratch
+// = the site's state ints, then the split partials.
+static size_t linear_stream_bytes(int64_t N, int64_t K, int M, size_t* state_ints, size_t* part_floats) {
+  w12_tensor t{};
+  t.N = N;
+  t.K = K;
+  StreamPhaseDesc d;
+  d.W = &t;
+  *state_ints = stream_state_ints(&d, 1);
+  *part_floats = stream_partial_floats(&d, 1, M);
+  return al256b(*state_ints * sizeof(int32_t)) + al256b(*part_floats * sizeof(float));
+}
+
 extern "C" size_t sd_w12_linear_workspace(int64_t N, int64_t K, int32_t M) {
-  (void)K;
-  const size_t pf = gemm_partial_floats(std::max(1, std::min<int>(M, 256)));
-  const size_t pbytes = (pf * sizeof(float) + 255) & ~size_t(255);
-  return pbytes + (size_t)gemm_counters(N) * sizeof(int32_t) + 256;
+  const int m = std::max(1, std::min<int>(M, 256));
+  const size_t pf = gemm_partial_floats(m);
+  const size_t tc = al256b(pf * sizeof(float)) + (size_t)gemm_counters(N) * sizeof(int32_t) + 256;
+  size_t si = 0, sp = 0;
+  const size_t st = (m <= 128 && N > 0 && K > 0) ? linear_stream_bytes(N, K, m, &si, &sp) + 256 : 0;
+  return std::max(tc, st);
 }
 
 extern "C" int sd_w12_linear(const w12_tensor* W, const uint16_t* x, int32_t M, uint16_t* y, void* workspace,
@@ -393,6 +438,26 @@ extern "C" int sd_w12_linear(const w12_tensor* W, const uint16_t* x, int32_t M, 
     return SD_ERR_WORKSPACE;
   }
   cudaStream_t s = (cudaStream_t)stream;
+  GemmEpilogue e;
+  e.epi = EPI_STORE;
+  e.out = y;
+  e.ldo = (int)W->N;
+  if (M <= 128 && !gemm_use_tc(M)) {
+    size_t si = 0, sp = 0;
+    linear_stream_bytes(W->N, W->K, M, &si, &sp);
+    StreamWorkspace ws;
+    ws.state = reinterpret_cast<int32_t*>(workspace);
+    ws.state_ints = si;
+    ws.partial = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + al256b(si * sizeof(int32_t)));
+    ws.partial_floats = sp;
+    SD_CK(cudaMemsetAsync(ws.state, 0, si * sizeof(int32_t), s));
+    StreamPhaseDesc d;
+    d.W = W;
+    d.x = x;
+    d.x_rows = M;
+    d.epi = e;
+    return stream_launch(&d, 1, M, ws, nullptr, s, false);
+  }
   GemmWorkspace ws;
   ws.partial = reinterpret_cast<float*>(workspace);
   ws.partial_floats = gemm_partial_floats(M);
@@ -403,9 +468,5 @@ extern "C" int sd_w12_linear(const w12_tensor* W, const uint16_t* x, int32_t M, 
   XMap xm;
   const int rc = make_x_map(&xm, x, M, W->K, M > 128 ? 128 : pad_rows(M));
   if (rc) return rc;
-  GemmEpilogue e;
-  e.epi = EPI_STORE;
-  e.out = y;
-  e.ldo = (int)W->N;
   return gemm_launch(*W, x, xm, M, e, ws, nullptr, s, false);
 }

@@ -92,6 +92,8 @@ int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, c
 // Descriptor of the packed words for the 2-D weight loads (one box = 8
 // strips x 1536 bytes).
 int make_w_map(CUtensorMap* map, const w12_tensor& W);
+// Descriptor of a tensor's 8-bit plane (one box = 8 strips x 1024 bytes).
+int make_w8_map(CUtensorMap* map, const uint32_t* plane, int64_t N, int64_t K);
 
 struct GemmParams;
 int make_gemm_params(GemmParams* out, const w12_tensor& W, const uint16_t* x, int M, const GemmEpilogue& epi,

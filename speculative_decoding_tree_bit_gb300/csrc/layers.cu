@@ -421,21 +421,30 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
         o[dn][2] *= alpha[1];
         o[dn][3] *= alpha[1];
       }
+      // P enters the bf16 MMA as two terms, P = hi + lo (hi = bf16(P), lo =
+      // bf16(P - hi)): about 16 significant bits, so the product carries the
+      // fp32 softmax weights rather than their bf16 rounding (which would
+      // move the output by up to half a bf16 unit before its own rounding)
       const uint32_t vb = smem_u32(sV + buf * kAttnTile * 128);
 #pragma unroll
       for (int k2 = 0; k2 < kNT / 2; k2++) {
-        const uint32_t pa0 = pack_bf16x2(s[2 * k2][0], s[2 * k2][1]);
-        const uint32_t pa1 = pack_bf16x2(s[2 * k2][2], s[2 * k2][3]);
-        const uint32_t pa2 = pack_bf16x2(s[2 * k2 + 1][0], s[2 * k2 + 1][1]);
-        const uint32_t pa3 = pack_bf16x2(s[2 * k2 + 1][2], s[2 * k2 + 1][3]);
+        uint32_t ph[4], pl[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+          const float* sj = s[2 * k2 + (j >> 1)] + 2 * (j & 1);
+          ph[j] = pack_bf16x2(sj[0], sj[1]);
+          pl[j] = pack_bf16x2(sj[0] - bf2f(ph[j] & 0xFFFFu), sj[1] - bf2f(ph[j] >> 16));
+        }
 #pragma unroll
         for (int dp = 0; dp < 8; dp++) {
           const int key = key0 + k2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
           const int ch = 2 * dp + (lane >> 4);
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(vb + key * 256 + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
-          mma_bf16(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
-          mma_bf16(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
+          mma_bf16(o[2 * dp], ph[0], ph[1], ph[2], ph[3], b0, b1);
+          mma_bf16(o[2 * dp + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+          mma_bf16(o[2 * dp], pl[0], pl[1], pl[2], pl[3], b0, b1);
+          mma_bf16(o[2 * dp + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
         }
       }
     }

@@ -7,17 +7,19 @@
 // -> greedy acceptance -> K/V compaction / state commit.
 // Every kernel is launched with programmatic dependent launch, so a GEMM's
 // producer streams its weights while the previous kernel is still finishing.
-// With the chain enabled (up to 128 rows; off by default), each run of GEMMs
-// and RMSNorms between two attention (or recurrence) kernels - O, RMSNorm,
-// gate/up, down, RMSNorm, next q/k/v or lm_head - is one persistent launch.
+// Up to 128 rows (and below the tensor-core threshold) the GEMMs between two
+// attention (or recurrence) kernels - O, gate/up, down and the next layer's
+// q/k/v (or the lm_head) - run as one streamed launch with the RMSNorms
+// folded into them (stream.cu); above it, one tcgen05 GEMM launch per
+// linear with RMSNorm kernels between them.
 #include <algorithm>
 #include <cmath>
 #include <map>
 #include <vector>
 
-#include "chain.cuh"
 #include "gemm.cuh"
 #include "layers.cuh"
+#include "stream.cuh"
 
 struct sd_model {
   sd_model_config cfg;
@@ -51,24 +53,23 @@ struct sd_model {
   };
   std::vector<Graph> graphs;
   bool use_graphs = true;
-  bool use_chain = false;
-  unsigned long long* chain_bar;  // grid-barrier words of the chain kernel (counter, base)
+  // the tensors' nested 8-bit planes (borrowed): [layer][qkv, o, gate_up,
+  // down], then the lm_head; empty until sd_model_set_view8
+  std::vector<const uint32_t*> view8;
+  // streamed GEMM launches: per-site state (one site per launch of a step),
+  // shared partials, per-row-block sums of squares of the residual stream
+  int32_t* stream_state = nullptr;
+  size_t site_ints = 0;
+  int n_sites = 0;
+  float* stream_part = nullptr;
+  size_t stream_part_floats = 0;
+  float* ss_h = nullptr;  // [H/128][128]: of h (O's output)
+  float* ss_x = nullptr;  // [H/128][128]: of x (down's output)
   // optional per-kernel timing
-  bool timing = false;   // events around every kernel group (+ device-clock traces)
-  bool tracing = false;  // device-clock traces only: launches as in untimed steps (no graph)
+  bool timing = false;  // events around every kernel launch
   std::vector<cudaEvent_t> events;  // 2 per entry
   std::vector<int32_t> t_kind;
   std::vector<double> t_bytes;
-  // per-phase stamps of the chain launches of a timed step
-  uint64_t* trace = nullptr;
-  size_t trace_cap = 0;  // u64 entries
-  struct ChainRec {
-    size_t entry, off;
-    int n, G;
-    std::vector<int32_t> kinds;
-    std::vector<double> bytes;
-  };
-  std::vector<ChainRec> t_chain;
 };
 
 namespace sdv {
@@ -116,7 +117,18 @@ struct StepIO {
   uint16_t* logits;
   int32_t* argmax;
   bool commit;
+  bool view8;  // round one of two-level verification: the weights' 8-bit view
 };
+
+static double gemm_bytes(const w12_tensor& W, int rows, int epi) {
+  // packed words, escape tile index (entries and pointers), activations in,
+  // outputs (+ residual) out
+  double b = (double)W.N * W.K * 1.5 + (double)W.n_escapes * 4.0 + (double)w12_tile_ptr_count(W.N, W.K) * 4.0;
+  b += (double)rows * W.K * 2.0;
+  b += (double)rows * W.N * (epi == EPI_SILU ? 1.0 : 2.0);
+  if (epi == EPI_RESID) b += (double)rows * W.N * 2.0;
+  return b;
+}
 
 static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   const bool pdl = true;
@@ -125,9 +137,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   int rc;
   m->t_kind.clear();
   m->t_bytes.clear();
-  m->t_chain.clear();
-  size_t trace_off = 0;
-  // bracket one kernel group with events when timing is on
+  // bracket one launch with events when timing is on
   auto tbegin = [&](int kind, double bytes) -> int {
     if (!m->timing) return SD_OK;
     const size_t i = m->t_kind.size();
@@ -146,122 +156,61 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     SD_CK(cudaEventRecord(m->events[2 * (m->t_kind.size() - 1) + 1], s));
     return SD_OK;
   };
-  auto gbytes = [&](const w12_tensor& W, int epi) -> double {
-    // packed words, escape tile index (entries and pointers)
-    double b = (double)W.N * W.K * 1.5 + (double)W.n_escapes * 4.0 + (double)w12_tile_ptr_count(W.N, W.K) * 4.0;
-    b += (double)rows * W.K * 2.0;                                        // activations read
-    b += (double)rows * W.N * (epi == EPI_SILU ? 1.0 : 2.0);              // outputs written
-    if (epi == EPI_RESID) b += (double)rows * W.N * 2.0;                  // residual read
-    return b;
-  };
-#define LK(kind, expr)                                  \
+#define LK(kind, bytes, expr)                           \
   do {                                                  \
-    if ((rc = tbegin(kind, 0.0))) return rc;            \
+    if ((rc = tbegin(kind, bytes))) return rc;          \
     cudaError_t _e = (expr);                            \
     if (_e != cudaSuccess) return cuda_fail(_e, #expr); \
     if ((rc = tend())) return rc;                       \
     launches++;                                         \
   } while (0)
 
-  // GEMMs and RMSNorms are queued and launched at the next attention /
-  // recurrence / acceptance kernel: as chain launches, or one by one
-  struct PendingOp {
-    int kind;
-    ChainPhaseDesc d;
+  // streamed launches (rows <= 128 below the tensor-core threshold): the
+  // GEMMs between two attention / recurrence kernels in one launch with the
+  // RMSNorms folded in; otherwise one GEMM launch per linear and RMSNorm
+  // kernels between them
+  const bool streamed = rows <= 128 && !gemm_use_tc(rows);
+  if (io.view8 && (!streamed || m->view8.size() != (size_t)4 * m->cfg.n_layers + 1)) {
+    set_error("model: the 8-bit view needs sd_model_set_view8 and a streamed step (rows <= 128, below the "
+              "tensor-core threshold)");
+    return SD_ERR_UNSUPPORTED;
+  }
+  auto v8 = [&](int l, int k) -> const uint32_t* {
+    return io.view8 ? m->view8[l < 0 ? 4 * m->cfg.n_layers : 4 * l + k] : nullptr;
   };
-  std::vector<PendingOp> pend;
-  const bool chain = m->use_chain && rows <= 128 && chain_grid(rows) > 0;
-  auto add_gemm = [&](int kind, const w12_tensor& W, const uint16_t* x, const XMap* xm, const GemmEpilogue& e) {
-    PendingOp op{};
-    op.kind = kind;
-    op.d.type = PH_GEMM;
-    op.d.W = &W;
-    op.d.x = x;
-    op.d.xm = xm;
-    op.d.epi = e;
-    pend.push_back(op);
-  };
-  auto add_norm = [&](const uint16_t* src, const uint16_t* gamma, uint16_t* dst) {
-    PendingOp op{};
-    op.kind = SD_K_NORM;
-    op.d.type = PH_NORM;
-    op.d.norm.src = src;
-    op.d.norm.gamma = gamma;
-    op.d.norm.dst = dst;
-    op.d.norm.H = m->H;
-    op.d.norm.eps = m->cfg.rms_eps;
-    pend.push_back(op);
-  };
-  auto flush = [&]() -> int {
-    size_t i = 0;
-    while (i < pend.size()) {
-      size_t n = 1;
-      if (chain)
-        while (i + n < pend.size() && n < (size_t)kChainMaxPhases) n++;
-      if (n >= 2) {
-        std::vector<ChainPhaseDesc> d;
-        double bytes = 0.0;
-        for (size_t j = i; j < i + n; j++) {
-          d.push_back(pend[j].d);
-          if (pend[j].d.type == PH_GEMM) bytes += gbytes(*pend[j].d.W, pend[j].d.epi.epi);
-        }
-        if ((rc = tbegin(SD_K_GEMM_CHAIN, bytes))) return rc;
-        uint64_t* trace = nullptr;
-        const int G = chain_grid(rows);
-        const size_t rows_tr = 1 + 3 * n;
-        if ((m->timing || m->tracing) && m->trace && trace_off + rows_tr * (size_t)G <= m->trace_cap) {
-          trace = m->trace + trace_off;
-          sd_model::ChainRec cr;
-          cr.entry = m->t_kind.size() - 1;
-          cr.off = trace_off;
-          cr.n = (int)n;
-          cr.G = G;
-          for (size_t j = i; j < i + n; j++) {
-            cr.kinds.push_back(pend[j].kind);
-            cr.bytes.push_back(pend[j].d.type == PH_GEMM ? gbytes(*pend[j].d.W, pend[j].d.epi.epi) : 0.0);
-          }
-          m->t_chain.push_back(cr);
-          trace_off += rows_tr * (size_t)G;
-        }
-        if ((rc = chain_launch(d.data(), (int)n, rows, m->gws, m->chain_bar, m->status, s, pdl, trace))) return rc;
-        if ((rc = tend())) return rc;
-        launches++;
-      } else {
-        const PendingOp& op = pend[i];
-        if (op.d.type == PH_GEMM) {
-          if ((rc = tbegin(op.kind, gbytes(*op.d.W, op.d.epi.epi)))) return rc;
-          // timed steps record the launch's per-CTA stamps as a one-phase trace
-          uint64_t* trace = nullptr;
-          const int G = gemm_launch_grid(*op.d.W, rows, op.d.epi.epi);
-          if ((m->timing || m->tracing) && m->trace && rows <= 128 && !gemm_use_tc(rows) &&
-              trace_off + 4 * (size_t)G <= m->trace_cap) {
-            trace = m->trace + trace_off;
-            sd_model::ChainRec cr;
-            cr.entry = m->t_kind.size() - 1;
-            cr.off = trace_off;
-            cr.n = 1;
-            cr.G = G;
-            cr.kinds.push_back(op.kind);
-            cr.bytes.push_back(gbytes(*op.d.W, op.d.epi.epi));
-            m->t_chain.push_back(cr);
-            trace_off += 4 * (size_t)G;
-          }
-          if ((rc = gemm_launch(*op.d.W, op.d.x, *op.d.xm, rows, op.d.epi, m->gws, m->status, s, pdl, 0, trace)))
-            return rc;
-          if ((rc = tend())) return rc;
-          launches += (rows > 128 && !gemm_use_tc(rows)) ? 2 : 1;
-        } else {
-          if ((rc = tbegin(SD_K_NORM, 0.0))) return rc;
-          const cudaError_t e = launch_rmsnorm(op.d.norm.src, op.d.norm.gamma, rows, op.d.norm.H, op.d.norm.eps,
-                                               op.d.norm.dst, nullptr, nullptr, nullptr, nullptr, nullptr, s, pdl);
-          if (e != cudaSuccess) return cuda_fail(e, "rmsnorm");
-          if ((rc = tend())) return rc;
-          launches++;
-        }
-      }
-      i += n;
+  int site = 0;
+  std::vector<StreamPhaseDesc> ph;
+  auto flush_stream = [&]() -> int {
+    if (ph.empty()) return SD_OK;
+    if (site >= m->n_sites) {
+      set_error("model: more streamed launches than sites");
+      return SD_ERR_INVALID_ARG;
     }
-    pend.clear();
+    double bytes = 0.0;
+    for (auto& d : ph) bytes += gemm_bytes(*d.W, rows, d.epi.epi);
+    StreamWorkspace ws;
+    ws.state = m->stream_state + (size_t)site * m->site_ints;
+    ws.state_ints = m->site_ints;
+    ws.partial = m->stream_part;
+    ws.partial_floats = m->stream_part_floats;
+    if ((rc = tbegin(SD_K_GEMM_STREAM, bytes))) return rc;
+    if ((rc = stream_launch(ph.data(), (int)ph.size(), rows, ws, m->status, s, pdl))) return rc;
+    if ((rc = tend())) return rc;
+    launches++;
+    site++;
+    ph.clear();
+    return SD_OK;
+  };
+  auto gemm_one = [&](int kind, const w12_tensor& W, const uint16_t* x, const XMap* xm, const GemmEpilogue& e) -> int {
+    if ((rc = tbegin(kind, gemm_bytes(W, rows, e.epi)))) return rc;
+    if ((rc = gemm_launch(W, x, *xm, rows, e, m->gws, m->status, s, pdl))) return rc;
+    if ((rc = tend())) return rc;
+    launches += (rows > 128 && !gemm_use_tc(rows)) ? 2 : 1;
+    return SD_OK;
+  };
+  auto norm = [&](const uint16_t* src, const uint16_t* gamma, uint16_t* dst) -> int {
+    LK(SD_K_NORM, (double)rows * m->H * 4.0,
+       launch_rmsnorm(src, gamma, rows, m->H, m->cfg.rms_eps, dst, nullptr, nullptr, nullptr, nullptr, nullptr, s, pdl));
     return SD_OK;
   };
 
@@ -270,17 +219,21 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     const cudaError_t e = launch_delay(30000000ull, s);
     if (e != cudaSuccess) return cuda_fail(e, "delay");
   }
-  XMap *mx, *ma, *mc;
-  if ((rc = get_map(m->map_xn, m->xn, m->max_rows, m->H, rows, &mx))) return rc;
-  if ((rc = get_map(m->map_attn, m->attn, m->max_rows, (int64_t)m->Hq * m->hd, rows, &ma))) return rc;
-  if ((rc = get_map(m->map_act, m->act, m->max_rows, m->I, rows, &mc))) return rc;
+  XMap *mx = nullptr, *ma = nullptr, *mc = nullptr;
+  if (!streamed) {
+    if ((rc = get_map(m->map_xn, m->xn, m->max_rows, m->H, rows, &mx))) return rc;
+    if ((rc = get_map(m->map_attn, m->attn, m->max_rows, (int64_t)m->Hq * m->hd, rows, &ma))) return rc;
+    if ((rc = get_map(m->map_act, m->act, m->max_rows, m->I, rows, &mc))) return rc;
+  }
 
   const StepRows sr{m->ctx_snap, m->req_ok, m->pos, m->slotv, m->req, m->depth, m->anc};
   // the step's first kernel starts only after the previous step (its KV
   // commit) is complete: later kernels of the step may read the committed
   // prefix before their programmatic-launch wait
-  LK(SD_K_TREE, launch_tree(io.tokens, io.parents, m->cu, io.R, io.cv, m->V, m->cfg.max_positions, sr, m->status, s, false));
-  LK(SD_K_NORM, launch_rmsnorm(nullptr, m->layers[0].attn_norm, rows, m->H, m->cfg.rms_eps, m->xn, io.tokens, m->w.embed, m->x,
+  LK(SD_K_TREE, 0.0,
+     launch_tree(io.tokens, io.parents, m->cu, io.R, io.cv, m->V, m->cfg.max_positions, sr, m->status, s, false));
+  LK(SD_K_NORM, (double)rows * m->H * 4.0,
+     launch_rmsnorm(nullptr, m->layers[0].attn_norm, rows, m->H, m->cfg.rms_eps, m->xn, io.tokens, m->w.embed, m->x,
                     m->req, m->req_ok, s, pdl));
 
   // row chunks of the attention grid: the largest request of this call
@@ -293,12 +246,11 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   while (splits > 1 && (size_t)io.R * (splits + 1) > m->attn_units) splits--;
   const int64_t layer_elems = (int64_t)io.cv.n_pages * m->Hkv * io.cv.page_size * m->hd;
 
-  for (int l = 0; l < m->cfg.n_layers; l++) {
-    const sd_layer_weights& Lw = m->layers[l];
-    const bool is_attn = m->kind[l] == 0;
-    const int ls = m->slot[l];
+  // epilogue of layer l's q/k/v GEMM
+  auto qkv_epi = [&](int l) {
     GemmEpilogue eq;
-    if (is_attn) {
+    const int ls = m->slot[l];
+    if (m->kind[l] == 0) {
       eq.epi = EPI_QKV;
       eq.q_out = m->q;
       eq.hq = m->Hq;
@@ -317,8 +269,33 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
       eq.out = m->qkv_rec + (int64_t)ls * m->max_rows * 3 * m->H;
       eq.ldo = 3 * m->H;
     }
-    add_gemm(SD_K_GEMM_QKV, Lw.qkv, m->xn, mx, eq);
-    if ((rc = flush())) return rc;
+    return eq;
+  };
+  GemmEpilogue el;  // lm_head: logits + argmax partials
+  el.epi = EPI_LOGITS;
+  el.out = io.logits;
+  el.ldo = m->V;
+  el.amax_val = m->amax_val;
+  el.amax_idx = m->amax_idx;
+  el.ld_amax = m->max_rows;
+
+  if (streamed) {
+    StreamPhaseDesc d;
+    d.W = &m->layers[0].qkv;
+    d.view8 = v8(0, 0);
+    d.x = m->xn;
+    d.x_rows = m->max_rows;
+    d.epi = qkv_epi(0);
+    ph.push_back(d);
+    if ((rc = flush_stream())) return rc;
+  } else {
+    if ((rc = gemm_one(SD_K_GEMM_QKV, m->layers[0].qkv, m->xn, mx, qkv_epi(0)))) return rc;
+  }
+
+  for (int l = 0; l < m->cfg.n_layers; l++) {
+    const sd_layer_weights& Lw = m->layers[l];
+    const bool is_attn = m->kind[l] == 0;
+    const int ls = m->slot[l];
     if (is_attn) {
       AttnArgs aa{};
       aa.q = m->q;
@@ -345,27 +322,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
       aa.tickets = m->attn_tickets;
       aa.status = m->status;
       aa.out = m->attn;
-      if ((rc = tbegin(SD_K_ATTN, 0.0))) return rc;
-      {
-        // traced steps record the attention's per-CTA stamps as a one-phase trace
-        const int G = (splits + 1) * m->Hkv * chunks * io.R;
-        if ((m->timing || m->tracing) && m->trace && trace_off + 4 * (size_t)G <= m->trace_cap) {
-          aa.trace = m->trace + trace_off;
-          sd_model::ChainRec cr;
-          cr.entry = m->t_kind.size() - 1;
-          cr.off = trace_off;
-          cr.n = 1;
-          cr.G = G;
-          cr.kinds.push_back(SD_K_ATTN);
-          cr.bytes.push_back(0.0);
-          m->t_chain.push_back(cr);
-          trace_off += 4 * (size_t)G;
-        }
-      }
-      const cudaError_t e = launch_attention(aa, rows, s, pdl);
-      if (e != cudaSuccess) return cuda_fail(e, "attention");
-      if ((rc = tend())) return rc;
-      launches += 1;
+      LK(SD_K_ATTN, 0.0, launch_attention(aa, rows, s, pdl));
     } else {
       LinrecArgs la{};
       la.qkv = m->qkv_rec + (int64_t)ls * m->max_rows * 3 * m->H;
@@ -381,38 +338,72 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
       la.H = m->H;
       la.eps = m->cfg.rec_eps;
       la.out = m->attn;
-      LK(SD_K_LINREC, launch_linrec(la, s, pdl));
+      LK(SD_K_LINREC, 0.0, launch_linrec(la, s, pdl));
     }
     GemmEpilogue eo;  // h = x + O(attn)
     eo.epi = EPI_RESID;
     eo.out = m->h;
     eo.resid = m->x;
     eo.ldo = m->H;
-    add_gemm(SD_K_GEMM_O, Lw.o, m->attn, ma, eo);
-    add_norm(m->h, Lw.mlp_norm, m->xn);
-    GemmEpilogue eg;
+    GemmEpilogue eg;  // act = silu(gate) * up
     eg.epi = EPI_SILU;
     eg.out = m->act;
     eg.ldo = m->I;
-    add_gemm(SD_K_GEMM_GATE_UP, Lw.gate_up, m->xn, mx, eg);
     GemmEpilogue ed;  // x = h + down(act)
     ed.epi = EPI_RESID;
     ed.out = m->x;
     ed.resid = m->h;
     ed.ldo = m->H;
-    add_gemm(SD_K_GEMM_DOWN, Lw.down, m->act, mc, ed);
-    const uint16_t* gnext = l + 1 < m->cfg.n_layers ? m->layers[l + 1].attn_norm : m->w.final_norm;
-    add_norm(m->x, gnext, m->xn);
+    const bool last = l + 1 == m->cfg.n_layers;
+    const uint16_t* gnext = last ? m->w.final_norm : m->layers[l + 1].attn_norm;
+    if (streamed) {
+      StreamPhaseDesc o, g, d, n;
+      o.W = &Lw.o;
+      o.view8 = v8(l, 1);
+      o.x = m->attn;
+      o.x_rows = m->max_rows;
+      o.epi = eo;
+      o.out_ss = m->ss_h;
+      g.W = &Lw.gate_up;
+      g.view8 = v8(l, 2);
+      g.x = m->h;
+      g.x_rows = m->max_rows;
+      g.epi = eg;
+      g.dep = 0;
+      g.norm_gamma = Lw.mlp_norm;
+      g.norm_eps = m->cfg.rms_eps;
+      d.W = &Lw.down;
+      d.view8 = v8(l, 3);
+      d.x = m->act;
+      d.x_rows = m->max_rows;
+      d.epi = ed;
+      d.dep = 1;
+      d.dep_fine = 1;
+      d.out_ss = m->ss_x;
+      n.W = last ? &m->w.lm_head : &m->layers[l + 1].qkv;
+      n.view8 = last ? v8(-1, 0) : v8(l + 1, 0);
+      n.x = m->x;
+      n.x_rows = m->max_rows;
+      n.epi = last ? el : qkv_epi(l + 1);
+      n.dep = 2;
+      n.norm_gamma = gnext;
+      n.norm_eps = m->cfg.rms_eps;
+      n.norm_out = last ? m->xn : nullptr;  // the final hidden state (the lm_head's input), kept for the tap
+      ph = {o, g, d, n};
+      if ((rc = flush_stream())) return rc;
+    } else {
+      if ((rc = gemm_one(SD_K_GEMM_O, Lw.o, m->attn, ma, eo))) return rc;
+      if ((rc = norm(m->h, Lw.mlp_norm, m->xn))) return rc;
+      if ((rc = gemm_one(SD_K_GEMM_GATE_UP, Lw.gate_up, m->xn, mx, eg))) return rc;
+      if ((rc = gemm_one(SD_K_GEMM_DOWN, Lw.down, m->act, mc, ed))) return rc;
+      if ((rc = norm(m->x, gnext, m->xn))) return rc;
+      if (last) {
+        if ((rc = gemm_one(SD_K_GEMM_LM_HEAD, m->w.lm_head, m->xn, mx, el))) return rc;
+      } else {
+        if ((rc = gemm_one(SD_K_GEMM_QKV, m->layers[l + 1].qkv, m->xn, mx, qkv_epi(l + 1)))) return rc;
+      }
+    }
   }
-  GemmEpilogue el;
-  el.epi = EPI_LOGITS;
-  el.out = io.logits;
-  el.ldo = m->V;
-  el.amax_val = m->amax_val;
-  el.amax_idx = m->amax_idx;
-  el.ld_amax = m->max_rows;
-  add_gemm(SD_K_GEMM_LM_HEAD, m->w.lm_head, m->xn, mx, el);
-  if ((rc = flush())) return rc;
 
   AcceptArgs ac{};
   ac.tokens = io.tokens;
@@ -421,7 +412,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   ac.R = io.R;
   ac.amax_val = m->amax_val;
   ac.amax_idx = m->amax_idx;
-  ac.n_part = gemm_grid(rows);
+  ac.n_part = streamed ? stream_grid(rows) : gemm_grid(rows);
   ac.ld = m->max_rows;
   ac.req_ok = m->req_ok;
   ac.ctx_snap = m->ctx_snap;
@@ -433,11 +424,13 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   ac.path = m->path;
   ac.path_len = m->path_len;
   ac.status = m->status;
-  LK(SD_K_ACCEPT, launch_accept(ac, s, pdl));
+  LK(SD_K_ACCEPT, 0.0, launch_accept(ac, s, pdl));
   if (io.commit) {
-    if (m->n_attn) LK(SD_K_COMMIT, launch_compact(io.cv, m->n_attn, m->Hkv, io.R, m->ctx_snap, m->path, m->path_len, s, pdl));
+    if (m->n_attn)
+      LK(SD_K_COMMIT, 0.0, launch_compact(io.cv, m->n_attn, m->Hkv, io.R, m->ctx_snap, m->path, m->path_len, s, pdl));
     if (m->n_rec)
-      LK(SD_K_COMMIT, launch_rec_commit(io.cv, m->n_rec, m->nh_rec, m->H, io.R, m->max_rows, m->qkv_rec, m->cu, m->path,
+      LK(SD_K_COMMIT, 0.0,
+         launch_rec_commit(io.cv, m->n_rec, m->nh_rec, m->H, io.R, m->max_rows, m->qkv_rec, m->cu, m->path,
                            m->path_len, s, pdl));
   }
 #undef LK
@@ -452,8 +445,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
 // every pointer and size the kernels see, so a replay is the same launch
 // sequence; values behind the pointers are read at run time.
 static int launch_step(sd_model* m, const StepIO& io, cudaStream_t s, std::vector<uintptr_t> key) {
-  if (!m->use_graphs || m->timing || m->tracing || s == nullptr) return run_step(m, io, s);
-  key.push_back((uintptr_t)m->use_chain);
+  if (!m->use_graphs || m->timing || s == nullptr) return run_step(m, io, s);
   key.push_back((uintptr_t)gemm_tc_min_rows());
   key.push_back((uintptr_t)g_attn_splits);
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -494,7 +486,8 @@ static std::vector<uintptr_t> step_key(const StepIO& io, int M) {
   return {(uintptr_t)M, (uintptr_t)io.R, (uintptr_t)io.rows, u(io.tokens), u(io.parents), u(io.cv.k_pool),
           u(io.cv.v_pool), (uintptr_t)io.cv.n_pages, (uintptr_t)io.cv.page_size, u(io.cv.page_table),
           (uintptr_t)io.cv.max_pages, u(io.cv.S), u(io.cv.z), u(io.cv.ctx_len), u(io.accepted_len),
-          u(io.accepted_tokens), u(io.bonus), u(io.logits), u(io.argmax), (uintptr_t)io.commit};
+          u(io.accepted_tokens), u(io.bonus), u(io.logits), u(io.argmax), (uintptr_t)io.commit,
+          (uintptr_t)io.view8};
 }
 
 static int upload_cu(sd_model* m, const std::vector<int32_t>& cu, cudaStream_t s) {
@@ -616,6 +609,30 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
     for (int r = 1; r <= R; r++)
       units = std::max(units, (size_t)r * (attn_splits(r, m->Hkv, ch, c.max_positions) + 1));
   m->attn_units = units;
+  // streamed launches of a step: [q/k/v of layer 0], then per layer [O,
+  // gate/up, down, next q/k/v or lm_head]; scratch for the largest of them
+  // at any row count the model accepts
+  {
+    size_t ints = 0, floats = 0;
+    for (int l = -1; l < c.n_layers; l++) {
+      StreamPhaseDesc d[4];
+      int n = 0;
+      if (l < 0) {
+        d[n++].W = &m->layers[0].qkv;
+      } else {
+        d[n++].W = &m->layers[l].o;
+        d[n++].W = &m->layers[l].gate_up;
+        d[n++].W = &m->layers[l].down;
+        d[n++].W = l + 1 < c.n_layers ? &m->layers[l + 1].qkv : &m->w.lm_head;
+      }
+      ints = std::max(ints, stream_state_ints(d, n));
+      for (int rows = 1; rows <= std::min(MR, 128); rows *= 2) floats = std::max(floats, stream_partial_floats(d, n, rows));
+      floats = std::max(floats, stream_partial_floats(d, n, std::min(MR, 128)));
+    }
+    m->site_ints = (ints + 63) & ~size_t(63);
+    m->n_sites = c.n_layers + 1;
+    m->stream_part_floats = std::max<size_t>(floats, 4);
+  }
   struct Item {
     void** p;
     size_t bytes;
@@ -651,7 +668,10 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
       {(void**)&m->amax_idx, (size_t)2 * num_sms() * MR * 4},
       {(void**)&m->gws.partial, gemm_partial_floats(MR) * 4},
       {(void**)&m->gws.counters, (size_t)gemm_counters(max_n) * 4},
-      {(void**)&m->chain_bar, 16},
+      {(void**)&m->stream_state, (size_t)m->n_sites * m->site_ints * 4},
+      {(void**)&m->stream_part, m->stream_part_floats * 4},
+      {(void**)&m->ss_h, (size_t)(m->H / 128) * 128 * 4},
+      {(void**)&m->ss_x, (size_t)(m->H / 128) * 128 * 4},
   };
   size_t total = 0;
   for (auto& it : items) total = al256(total + it.bytes);
@@ -699,7 +719,6 @@ extern "C" int sd_model_destroy(sd_model* m) {
   if (!m) return SD_OK;
   for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);
   for (cudaEvent_t e : m->events) cudaEventDestroy(e);
-  if (m->trace) cudaFree(m->trace);
   cudaFree(m->arena);
   delete m;
   return SD_OK;
@@ -707,7 +726,7 @@ extern "C" int sd_model_destroy(sd_model* m) {
 
 static int single_step(sd_model* m, const int32_t* tokens, const int32_t* parents, int32_t M, const sd_kv* kv,
                        int32_t* accepted_len, int32_t* accepted_tokens, int32_t* bonus, uint16_t* logits,
-                       int32_t* argmax, bool commit, void* stream) {
+                       int32_t* argmax, bool commit, void* stream, bool view8 = false) {
   if (!m || !tokens || !parents || !kv || !kv->k || !kv->v || !kv->ctx_len || M < 1) {
     set_error("sd_verify_step: null argument");
     return SD_ERR_INVALID_ARG;
@@ -745,6 +764,7 @@ static int single_step(sd_model* m, const int32_t* tokens, const int32_t* parent
   io.logits = logits;
   io.argmax = argmax;
   io.commit = commit;
+  io.view8 = view8;
   return launch_step(m, io, s, step_key(io, M));
 }
 
@@ -758,6 +778,27 @@ extern "C" int sd_verify_step(sd_model* m, const int32_t* tree_tokens, const int
 extern "C" int sd_forward(sd_model* m, const int32_t* tree_tokens, const int32_t* parents, int32_t M, const sd_kv* kv,
                           uint16_t* logits, int32_t* argmax, void* stream) {
   return single_step(m, tree_tokens, parents, M, kv, nullptr, nullptr, nullptr, logits, argmax, false, stream);
+}
+
+extern "C" int sd_forward_view8(sd_model* m, const int32_t* tree_tokens, const int32_t* parents, int32_t M,
+                                const sd_kv* kv, uint16_t* logits, int32_t* argmax, void* stream) {
+  return single_step(m, tree_tokens, parents, M, kv, nullptr, nullptr, nullptr, logits, argmax, false, stream, true);
+}
+
+extern "C" int sd_model_set_view8(sd_model* m, const uint32_t* const* planes_host, int32_t n) {
+  if (!m || !planes_host || n != 4 * m->cfg.n_layers + 1) {
+    set_error("sd_model_set_view8: need 4 planes per layer (qkv, o, gate_up, down) and the lm_head's");
+    return SD_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < n; i++)
+    if (!planes_host[i] || (reinterpret_cast<uintptr_t>(planes_host[i]) & 15)) {
+      set_error("sd_model_set_view8: null or unaligned plane");
+      return SD_ERR_INVALID_ARG;
+    }
+  m->view8.assign(planes_host, planes_host + n);
+  for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);  // captured steps may hold the old planes
+  m->graphs.clear();
+  return SD_OK;
 }
 
 extern "C" int sd_verify_batch(sd_model* m, const int32_t* tokens, const int32_t* parents, const int32_t* cu_nodes_host,
@@ -815,31 +856,30 @@ extern "C" int sd_status(sd_model* m, int32_t* status_host) {
   SD_CK(cudaDeviceSynchronize());
   SD_CK(cudaMemcpy(status_host, m->status, 4, cudaMemcpyDeviceToHost));
   SD_CK(cudaMemset(m->status, 0, 4));
-  // a chain that gave up on a barrier may have left its arrival counter
-  // short of a multiple of the grid: start the next one from zero
-  if (*status_host != SD_OK) SD_CK(cudaMemset(m->chain_bar, 0, 16));
+  // a streamed launch that gave up on a wait may have left its unit
+  // counters, tickets or flags set: start the next step from zero
+  if (*status_host != SD_OK) SD_CK(cudaMemset(m->stream_state, 0, (size_t)m->n_sites * m->site_ints * 4));
   return SD_OK;
 }
 
 extern "C" int sd_model_last_launches(sd_model* m) { return m ? m->last_launches : 0; }
+
+extern "C" int sd_model_final_hidden(sd_model* m, uint16_t* out, int32_t rows, void* stream) {
+  if (!m || !out || rows < 1 || rows > m->max_rows) {
+    set_error("sd_model_final_hidden: bad argument (rows must be 1..max_rows)");
+    return SD_ERR_INVALID_ARG;
+  }
+  SD_CK(cudaMemcpyAsync(out, m->xn, (size_t)rows * m->H * sizeof(uint16_t), cudaMemcpyDeviceToDevice,
+                        (cudaStream_t)stream));
+  return SD_OK;
+}
 
 extern "C" int sd_model_set_timing(sd_model* m, int32_t enable) {
   if (!m) {
     set_error("sd_model_set_timing: null model");
     return SD_ERR_INVALID_ARG;
   }
-  m->timing = enable == 1;
-  m->tracing = enable == 2;
-  if ((m->timing || m->tracing) && !m->trace) {
-    // stamps of every traced launch of one step: at most (layers + 2) chains
-    // of 1 + 3 x 6 rows, or per layer 4 GEMMs and the attention of 4 rows,
-    // x the largest grid (zero-filled: a CTA without work in a phase leaves
-    // two of its stamps unwritten)
-    const size_t cap = (size_t)(m->cfg.n_layers + 2) * (1 + 3 * kChainMaxPhases) * gemm_grid(1) * 2;
-    SD_CK(cudaMalloc(&m->trace, cap * sizeof(uint64_t)));
-    SD_CK(cudaMemset(m->trace, 0, cap * sizeof(uint64_t)));
-    m->trace_cap = cap;
-  }
+  m->timing = enable != 0;
   return SD_OK;
 }
 
@@ -853,7 +893,6 @@ extern "C" int sd_model_timeline(sd_model* m, int32_t max, int32_t* kind_host, f
     return -1;
   }
   int n = 0;
-  size_t ci = 0;
   for (size_t i = 0; i < m->t_kind.size() && n < max; i++) {
     float ms = 0.f;
     if (cudaEventElapsedTime(&ms, m->events[2 * i], m->events[2 * i + 1]) != cudaSuccess) ms = -1.f;
@@ -861,65 +900,8 @@ extern "C" int sd_model_timeline(sd_model* m, int32_t max, int32_t* kind_host, f
     ms_host[n] = ms;
     bytes_host[n] = m->t_bytes[i];
     n++;
-    if (ci < m->t_chain.size() && m->t_chain[ci].entry == i) {
-      // the chain's phases from the device stamps: phase p lasts from the
-      // last CTA finishing phase p - 1 (the first CTA starting, for p = 0)
-      // to the last CTA finishing phase p
-      const sd_model::ChainRec& cr = m->t_chain[ci++];
-      std::vector<uint64_t> st((size_t)(1 + 3 * cr.n) * cr.G);
-      if (cudaMemcpy(st.data(), m->trace + cr.off, st.size() * sizeof(uint64_t), cudaMemcpyDeviceToHost) !=
-          cudaSuccess) {
-        set_error("sd_model_timeline: trace copy failed");
-        return -1;
-      }
-      uint64_t prev = ~0ull;
-      for (int c = 0; c < cr.G; c++) prev = std::min(prev, st[c]);
-      for (int p = 0; p < cr.n && n < max; p++) {
-        uint64_t end = 0;
-        for (int c = 0; c < cr.G; c++) end = std::max(end, st[(size_t)(3 + 3 * p) * cr.G + c]);
-        kind_host[n] = 100 + cr.kinds[p];
-        ms_host[n] = (float)((double)(end - prev) * 1e-6);
-        bytes_host[n] = cr.bytes[p];
-        n++;
-        prev = end;
-      }
-    }
   }
   return n;
-}
-
-extern "C" int sd_model_chain_trace(sd_model* m, int32_t launch, int32_t* n_phases, int32_t* n_ctas,
-                                    uint64_t* stamps_host, int64_t max_stamps) {
-  if (!m || !n_phases || !n_ctas || launch < 0) {
-    set_error("sd_model_chain_trace: bad argument");
-    return SD_ERR_INVALID_ARG;
-  }
-  if (launch >= (int)m->t_chain.size()) {
-    set_error("sd_model_chain_trace: no such chain launch in the last timed step");
-    return SD_ERR_INVALID_ARG;
-  }
-  const sd_model::ChainRec& cr = m->t_chain[launch];
-  *n_phases = cr.n;
-  *n_ctas = cr.G;
-  const size_t cnt = (size_t)(1 + 3 * cr.n) * cr.G;
-  if (stamps_host) {
-    if (max_stamps < (int64_t)cnt) {
-      set_error("sd_model_chain_trace: buffer too small");
-      return SD_ERR_INVALID_ARG;
-    }
-    SD_CK(cudaDeviceSynchronize());
-    SD_CK(cudaMemcpy(stamps_host, m->trace + cr.off, cnt * sizeof(uint64_t), cudaMemcpyDeviceToHost));
-  }
-  return SD_OK;
-}
-
-extern "C" int sd_model_set_chain(sd_model* m, int32_t enable) {
-  if (!m) {
-    set_error("sd_model_set_chain: null model");
-    return SD_ERR_INVALID_ARG;
-  }
-  m->use_chain = enable != 0;
-  return SD_OK;
 }
 
 extern "C" int sd_model_set_graphs(sd_model* m, int32_t enable) {

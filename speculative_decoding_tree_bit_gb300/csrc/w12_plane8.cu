@@ -12,14 +12,50 @@
 // and + 8): plane 0 holds the bytes of (row g, c), (row g, c + 1),
 // (row g + 8, c), (row g + 8, c + 1); plane 1 the same at column c + 8.  On
 // the contiguous-table path a byte b decodes to the bf16
-// ((b & 0x80) << 8) | (((b & 0x7F) << 4) + (table[0] << 7)).
+// ((b & 0x80) << 8) | (((b & 0x7F) << 4) + (table[0] << 7)).  The device
+// packer writes the same layout from the bf16 weights on the device.
 
+#include <algorithm>
 #include <cstdint>
 
 #include "common.cuh"
 #include "sdv.h"
 
 namespace sdv {
+
+struct Plane8Lut {
+  uint8_t code_of[256];  // exponent -> code (15: not in the table, escaped)
+};
+
+// One thread per (strip, super-tile, lane, sub-tile): the two words of that
+// lane's fragment bytes.
+__global__ void k_plane8_encode(const uint16_t* __restrict__ w, const int32_t* __restrict__ row_src, int64_t N,
+                                int64_t K, Plane8Lut lut, uint32_t* __restrict__ plane) {
+  const int64_t KT = K / 64;
+  const int64_t total = (N / 16) * KT * 128;
+  for (int64_t id = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; id < total; id += (int64_t)gridDim.x * blockDim.x) {
+    const int j = (int)(id & 3), lane = (int)((id >> 2) & 31);
+    const int64_t st = id >> 7;  // strip * KT + tile
+    const int64_t s = st / KT, t = st % KT;
+    const int g = lane >> 2, q = lane & 3;
+    const int64_t r0 = row_src ? row_src[s * 16 + g] : s * 16 + g;
+    const int64_t r1 = row_src ? row_src[s * 16 + g + 8] : s * 16 + g + 8;
+    const int64_t c = t * 64 + j * 16 + 2 * q;
+    auto byte_of = [&](uint32_t b) -> uint32_t {
+      const uint32_t code = lut.code_of[(b >> 7) & 0xFF];
+      if (code == 15) return 15u << 3;
+      return ((b >> 15) << 7) | (code << 3) | ((b >> 4) & 7u);
+    };
+#pragma unroll
+    for (int p = 0; p < 2; p++) {
+      const uint32_t a = *reinterpret_cast<const uint32_t*>(w + r0 * K + c + 8 * p);
+      const uint32_t b = *reinterpret_cast<const uint32_t*>(w + r1 * K + c + 8 * p);
+      plane[st * 256 + p * 128 + lane * 4 + j] =
+          byte_of(a & 0xFFFF) | (byte_of(a >> 16) << 8) | (byte_of(b & 0xFFFF) << 16) | (byte_of(b >> 16) << 24);
+    }
+  }
+}
+
 namespace {
 
 inline int64_t plane8_word(int64_t s, int64_t t, int64_t KT, int p, int lane, int j) {
@@ -68,6 +104,28 @@ extern "C" int w12_plane8_pack_host(const uint16_t* w, int64_t N, int64_t K, con
             plane[plane8_word(s, t, KT, p, lane, j)] = v;
           }
         }
+  return SD_OK;
+}
+
+extern "C" int64_t w12_plane8_words_count(int64_t N, int64_t K) { return N * K / 4; }
+
+extern "C" int w12_plane8_pack(const uint16_t* w, const int32_t* row_src, const w12_meta* meta, uint32_t* plane,
+                               void* stream) {
+  if (!w || !meta || !plane || meta->n_table < 0 || meta->n_table > 15) {
+    set_error("w12_plane8_pack: bad argument");
+    return SD_ERR_INVALID_ARG;
+  }
+  if (!plane8_shape_ok(meta->N, meta->K)) {
+    set_error("w12_plane8_pack: N % 16, K % 64 and N*K < 2^32 required");
+    return SD_ERR_UNSUPPORTED;
+  }
+  Plane8Lut lut;
+  for (int e = 0; e < 256; e++) lut.code_of[e] = 15;
+  for (int c = 0; c < meta->n_table; c++) lut.code_of[meta->table[c]] = (uint8_t)c;
+  const int64_t total = (meta->N / 16) * (meta->K / 64) * 128;
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, 65536);
+  k_plane8_encode<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(w, row_src, meta->N, meta->K, lut, plane);
+  SD_CK(cudaGetLastError());
   return SD_OK;
 }
 

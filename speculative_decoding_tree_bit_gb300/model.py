@@ -60,8 +60,9 @@ class Packed:
         return self.words.numel() * 4 + self.n_escapes * 4 + int(lib().w12_tile_ptr_count(self.N, self.K)) * 4
 
 
-def pack(w: torch.Tensor, row_src: np.ndarray | None = None, stream=None) -> Packed:
-    """Pack a bf16 device tensor [N][K] (int16/uint16/bfloat16 storage)."""
+def pack(w: torch.Tensor, row_src: np.ndarray | None = None, stream=None, view8: bool = False) -> Packed:
+    """Pack a bf16 device tensor [N][K] (int16/uint16/bfloat16 storage); with
+    view8 also its nested 8-bit plane (p.plane8, w12_plane8_pack)."""
     assert w.is_cuda and w.dim() == 2 and w.element_size() == 2 and w.is_contiguous()
     N, K = w.shape
     s = stream_ptr(stream)
@@ -81,6 +82,10 @@ def pack(w: torch.Tensor, row_src: np.ndarray | None = None, stream=None) -> Pac
     p.tile_esc = torch.empty(ne, dtype=torch.int32, device=dev)
     t = p.struct()
     check(lib().w12_pack_tile_index(ctypes.byref(t), p.tile_ptr.data_ptr(), p.tile_esc.data_ptr(), s))
+    p.plane8 = None
+    if view8:
+        p.plane8 = torch.empty(int(lib().w12_plane8_words_count(N, K)), dtype=torch.int32, device=dev)
+        check(lib().w12_plane8_pack(w.data_ptr(), _ptr(rs), ctypes.byref(meta), p.plane8.data_ptr(), s))
     torch.cuda.synchronize()
     return p
 
@@ -171,7 +176,7 @@ class Model:
     """A decoder whose linear weights are W12-packed on the device."""
 
     def __init__(self, shape, weights, max_rows: int = 64, max_requests: int = 1, max_positions: int = 4352,
-                 device: str = "cuda", progress=None):
+                 device: str = "cuda", progress=None, view8: bool = False):
         self.shape = shape
         self.device = device
         keep = []
@@ -182,13 +187,13 @@ class Model:
         self.layer_bytes = []
         for l, kind in enumerate(shape.layer_kinds):
             qkv = to_device_u16(np.concatenate([weights.layer(l, n) for n in ("wq", "wk", "wv")]), device)
-            p_qkv = pack(qkv, row_map(0, Hq, Hkv, I, qkv.shape[0]) if kind == "attn" else None)
+            p_qkv = pack(qkv, row_map(0, Hq, Hkv, I, qkv.shape[0]) if kind == "attn" else None, view8=view8)
             del qkv
-            p_o = pack(to_device_u16(weights.layer(l, "wo"), device))
+            p_o = pack(to_device_u16(weights.layer(l, "wo"), device), view8=view8)
             gu = to_device_u16(np.concatenate([weights.layer(l, "w_gate"), weights.layer(l, "w_up")]), device)
-            p_gu = pack(gu, row_map(1, Hq, Hkv, I, gu.shape[0]))
+            p_gu = pack(gu, row_map(1, Hq, Hkv, I, gu.shape[0]), view8=view8)
             del gu
-            p_d = pack(to_device_u16(weights.layer(l, "w_down"), device))
+            p_d = pack(to_device_u16(weights.layer(l, "w_down"), device), view8=view8)
             an = to_device_u16(weights.norm(l, "attn"), device)
             mn = to_device_u16(weights.norm(l, "mlp"), device)
             keep += [p_qkv, p_o, p_gu, p_d, an, mn]
@@ -201,7 +206,7 @@ class Model:
                 progress(l)
         self.embed = to_device_u16(weights.embedding(), device)
         self.final_norm = to_device_u16(weights.final_norm(), device)
-        self.lm_head = pack(to_device_u16(weights.lm_head(), device))
+        self.lm_head = pack(to_device_u16(weights.lm_head(), device), view8=view8)
         self.packed_bytes += self.lm_head.nbytes()
         keep += [self.embed, self.final_norm, self.lm_head]
         self._keep, self._layers = keep, layers
@@ -221,6 +226,11 @@ class Model:
         torch.cuda.synchronize()
         check(lib().sd_model_create(ctypes.byref(cfg), ctypes.byref(mw), ctypes.byref(h)))
         self.handle = h
+        if view8:
+            packed = [p for p in keep if isinstance(p, Packed)]  # per layer qkv, o, gate_up, down; then lm_head
+            planes = (ctypes.c_void_p * len(packed))(*[p.plane8.data_ptr() for p in packed])
+            self._planes = planes
+            check(lib().sd_model_set_view8(self.handle, planes, len(packed)))
 
     def close(self):
         if getattr(self, "handle", None):
@@ -241,20 +251,22 @@ class Model:
     def last_launches(self) -> int:
         return int(lib().sd_model_last_launches(self.handle))
 
+    def final_hidden(self, rows: int, stream=None) -> torch.Tensor:
+        """The last call's final RMSNorm output (the lm_head input), int16
+        bits [rows][hidden] (sd_model_final_hidden)."""
+        out = torch.empty((rows, self.shape.H), dtype=torch.int16, device=self.device)
+        check(lib().sd_model_final_hidden(self.handle, out.data_ptr(), rows, stream_ptr(stream)))
+        return out
+
     def set_graphs(self, on: bool):
         check(lib().sd_model_set_graphs(self.handle, 1 if on else 0))
 
-    def set_chain(self, on: bool):
-        """Chained GEMM/RMSNorm launches (default on) or one kernel per op."""
-        check(lib().sd_model_set_chain(self.handle, 1 if on else 0))
-
-    def set_timing(self, on):
-        """True / 1: event timing + traces; 2: device-clock traces only."""
-        check(lib().sd_model_set_timing(self.handle, int(on)))
+    def set_timing(self, on: bool):
+        """Event timing of every kernel launch of the following calls."""
+        check(lib().sd_model_set_timing(self.handle, 1 if on else 0))
 
     def timeline(self, max_entries: int = 4096):
-        """[(kind name, ms, algorithmic bytes)] of the last timed call; the
-        phases of a chain launch follow it as "chain.<kind>" entries."""
+        """[(kind name, ms, algorithmic bytes)] of the last timed call."""
         from . import KERNEL_KINDS
         k = np.zeros(max_entries, np.int32)
         ms = np.zeros(max_entries, np.float32)
@@ -262,19 +274,7 @@ class Model:
         n = lib().sd_model_timeline(self.handle, max_entries, k.ctypes.data, ms.ctypes.data, b.ctypes.data)
         if n < 0:
             check(3)
-        def name(x):
-            return "chain." + KERNEL_KINDS[x - 100] if x >= 100 else KERNEL_KINDS[x]
-        return [(name(int(k[i])), float(ms[i]), float(b[i])) for i in range(n)]
-
-    def chain_trace(self, launch: int):
-        """Device-clock stamps (ns) of chain launch `launch` of the last timed
-        step as an array [1 + 3 n_phases][n_ctas] (see sd_model_chain_trace)."""
-        n, g = ctypes.c_int32(), ctypes.c_int32()
-        check(lib().sd_model_chain_trace(self.handle, launch, ctypes.byref(n), ctypes.byref(g), None, 0))
-        buf = np.zeros((1 + 3 * n.value) * g.value, np.uint64)
-        check(lib().sd_model_chain_trace(self.handle, launch, ctypes.byref(n), ctypes.byref(g), buf.ctypes.data,
-                                         buf.size))
-        return buf.reshape(1 + 3 * n.value, g.value)
+        return [(KERNEL_KINDS[int(k[i])], float(ms[i]), float(b[i])) for i in range(n)]
 
     def outputs(self, M: int, logits: bool = False, R: int = 1):
         d = self.device
@@ -294,6 +294,18 @@ class Model:
         kvs = kv.struct()
         check(lib().sd_forward(self.handle, tok.data_ptr(), par.data_ptr(), M, ctypes.byref(kvs), _ptr(lg),
                                am.data_ptr(), stream_ptr(stream)))
+        return lg, am
+
+    def forward_view8(self, tokens, parents, kv: "KVCache", logits: bool = True, stream=None):
+        """Round one of two-level verification (sd_forward_view8): the
+        forward over the weights' 8-bit view; (logits or None, argmax)."""
+        tok, par = _i32(tokens, self.device), _i32(parents, self.device)
+        M = tok.numel()
+        lg = torch.empty((M, self.shape.V), dtype=torch.int16, device=self.device) if logits else None
+        am = torch.empty(M, dtype=torch.int32, device=self.device)
+        kvs = kv.struct()
+        check(lib().sd_forward_view8(self.handle, tok.data_ptr(), par.data_ptr(), M, ctypes.byref(kvs), _ptr(lg),
+                                     am.data_ptr(), stream_ptr(stream)))
         return lg, am
 
     def verify(self, tokens, parents, kv: "KVCache", logits: bool = False, out=None, stream=None):
@@ -470,3 +482,36 @@ def tiny_verify(W1: Packed, Wlm: Packed, act: torch.Tensor, tokens, parents, log
                                ws.nbytes, stream_ptr(stream)))
     o["_ws"] = ws
     return o
+
+
+class GdnLayer:
+    """Gated delta rule over draft trees through the C ABI (sd_gdn_tree_verify,
+    sd_gdn_commit); owns the workspace for up to `max_rows` rows."""
+
+    def __init__(self, max_rows: int, nh: int, device="cuda"):
+        self.nh, self.device = int(nh), device
+        self.ws = Workspace(int(lib().sd_gdn_workspace(int(max_rows), self.nh)), device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def verify(self, q, k, v, alpha, beta, parents, cu, S, stream=None) -> torch.Tensor:
+        """q, k, v int16 bits [rows][nh][128]; alpha, beta float32 [rows][nh];
+        parents int32 [rows]; cu host array [R+1]; S float32 [R][nh][128][128].
+        Returns o (int16 bf16 bits [rows][nh][128])."""
+        cu_h = np.ascontiguousarray(np.asarray(cu, dtype=np.int32))
+        cu_d = _i32(cu_h, self.device)
+        par = parents if isinstance(parents, torch.Tensor) else _i32(parents, self.device)
+        out = torch.empty_like(q)
+        self._cu = (cu_h, cu_d, par)
+        check(lib().sd_gdn_tree_verify(q.data_ptr(), k.data_ptr(), v.data_ptr(), alpha.data_ptr(), beta.data_ptr(),
+                                       par.data_ptr(), cu_d.data_ptr(), cu_h.ctypes.data, cu_h.size - 1, self.nh,
+                                       S.data_ptr(), out.data_ptr(), self.ws.ptr, self.ws.nbytes, self.status.data_ptr(),
+                                       stream_ptr(stream)))
+        return out
+
+    def commit(self, last, S, stream=None):
+        """S of each request becomes the state of its node last[r] (the
+        requests and parents of the preceding verify call)."""
+        cu_h, cu_d, par = self._cu
+        la = last if isinstance(last, torch.Tensor) else _i32(last, self.device)
+        check(lib().sd_gdn_commit(par.data_ptr(), cu_d.data_ptr(), cu_h.ctypes.data, cu_h.size - 1, self.nh,
+                                  la.data_ptr(), S.data_ptr(), self.ws.ptr, self.ws.nbytes, stream_ptr(stream)))

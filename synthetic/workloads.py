@@ -82,6 +82,10 @@ SHAPES = {
     # kernels with a few GB on the device
     "8b_2l": _dense("8b_2l", 2, 4096, 12288, 32, 8, 151936),
     "mini_hybrid": _hybrid("mini_hybrid", 4, 512, 1024, 4, 2, 4000, gamma_sigma=0.1),
+    # full layer dimensions with few layers: end-to-end parity against the
+    # oracle at the named models' widths, head groups and vocabulary
+    "27b_2l": _dense("27b_2l", 2, 5120, 21504, 40, 8, 151936),
+    "hybrid_4l": _hybrid("hybrid_4l", 4, 4096, 12288, 32, 8, 151936),
 }
 
 
@@ -232,23 +236,45 @@ def depths(parents) -> np.ndarray:
     return d
 
 
-def copy_rule_tokens(td: TreeDraft, argmax_fn) -> np.ndarray:
+def copy_rule_tokens(td: TreeDraft, argmax_fn, max_waves: int | None = None) -> np.ndarray:
     """Draft tokens by depth waves: node i at depth d copies the target's
     argmax at its parent when its coin says so, else takes its random token.
     ``argmax_fn(tokens_sub, parents_sub)`` must return the target argmax of
-    every node of the prefix-closed sub-tree it is given."""
-    parents = np.asarray(td.parents)
-    M = parents.size
-    d = depths(parents)
-    tok = np.zeros(M, dtype=np.int32)
-    tok[0] = td.root_token
-    for wave in range(1, int(d.max()) + 1 if M else 1):
-        sub = np.nonzero(d < wave)[0]
-        pos = {int(n): i for i, n in enumerate(sub)}
-        psub = np.array([-1 if parents[n] < 0 else pos[int(parents[n])] for n in sub], dtype=np.int32)
-        am = np.asarray(argmax_fn(tok[sub].copy(), psub))
-        for i in np.nonzero(d == wave)[0]:
-            tok[i] = am[pos[int(parents[i])]] if td.copy[i] else td.rand_tok[i]
+    every node of the prefix-closed sub-tree it is given.  With
+    ``max_waves`` only nodes down to that depth follow the rule (one target
+    pass per wave); deeper nodes take their random tokens."""
+    return copy_rule_tokens_batch([td], lambda subs: [argmax_fn(*subs[0])], max_waves)[0]
+
+
+def copy_rule_tokens_batch(tds, argmax_fn, max_waves: int | None = None) -> list:
+    """The copy rule for several requests at once: each wave makes one call
+    ``argmax_fn([(tokens_sub, parents_sub) per request])`` returning the
+    target argmax of every node of each sub-tree."""
+    parents = [np.asarray(td.parents) for td in tds]
+    d = [depths(p) for p in parents]
+    tok = []
+    for td, p, dd in zip(tds, parents, d):
+        t = np.zeros(p.size, dtype=np.int32)
+        t[0] = td.root_token
+        deep = np.nonzero(dd > (max_waves if max_waves is not None else p.size))[0]
+        t[deep] = td.rand_tok[deep]
+        tok.append(t)
+    last = max((int(dd.max()) for dd in d if dd.size), default=0)
+    if max_waves is not None:
+        last = min(last, max_waves)
+    for wave in range(1, last + 1):
+        subs, maps = [], []
+        for p, dd, t in zip(parents, d, tok):
+            sub = np.nonzero(dd < wave)[0]
+            pos = {int(n): i for i, n in enumerate(sub)}
+            psub = np.array([-1 if p[n] < 0 else pos[int(p[n])] for n in sub], dtype=np.int32)
+            subs.append((t[sub].copy(), psub))
+            maps.append(pos)
+        ams = argmax_fn(subs)
+        for td, p, dd, t, pos, am in zip(tds, parents, d, tok, maps, ams):
+            am = np.asarray(am)
+            for i in np.nonzero(dd == wave)[0]:
+                t[i] = am[pos[int(p[i])]] if td.copy[i] else td.rand_tok[i]
     return tok
 
 
@@ -360,3 +386,35 @@ def page_tables(seed: int, ctxs, M: int, page_size: int, slack_pages: int = 1):
         table[r, :n] = perm[o:o + n]
         o += n
     return table, total
+
+
+# ------------------------------------------------------- gated delta rule --
+
+@dataclass
+class GdnInputs:
+    """Inputs of one gated-delta-rule layer over the draft trees of R
+    requests: q, k, v bf16 [rows][nh][128], gates alpha in [alpha_lo, 1] and
+    write strengths beta in [0, 1] fp32 [rows][nh], parents local to each
+    request, cu [R+1], committed states S fp32 [R][nh][128][128]."""
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    alpha: np.ndarray
+    beta: np.ndarray
+    parents: np.ndarray
+    cu: np.ndarray
+    S: np.ndarray
+
+
+def gdn_inputs(seed: int, Ms, max_depth: int, nh: int, alpha_lo: float = 0.8, s_sigma: float = 0.01) -> GdnInputs:
+    R = len(Ms)
+    cu = np.zeros(R + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(Ms)
+    rows = int(cu[-1])
+    par = np.concatenate([tree(_rkey(seed, SID_TREE, r), int(m), max_depth) for r, m in enumerate(Ms)]).astype(np.int32)
+    q, k, v = (normal_bf16(key(seed, SID_ACT + j), rows * nh * 128, 1.0).reshape(rows, nh, 128) for j in range(3))
+    u = uniform_int(key(seed, SID_COINS), 2 * rows * nh, 0, (1 << 24) - 1).reshape(2, rows, nh) / float(1 << 24)
+    alpha = (alpha_lo + (1.0 - alpha_lo) * u[0]).astype(np.float32)
+    beta = u[1].astype(np.float32)
+    S = normal_f32(key(seed, SID_STATE), R * nh * 128 * 128, s_sigma).reshape(R, nh, 128, 128)
+    return GdnInputs(q, k, v, alpha, beta, par, cu, S)

@@ -23,11 +23,22 @@ def oracle_request(shape, seed, r, ctx, tokens, parents, cap=None):
     return oracle.Request(np.asarray(tokens, np.int32), np.asarray(parents, np.int32), ctx, layers)
 
 
-def oracle_copy_tokens(shape, W, seed, r, ctx, td):
-    """Copy-rule draft tokens by depth waves, the target argmax from the oracle."""
+def oracle_copy_tokens(shape, W, seed, r, ctx, td, max_waves=None):
+    """Copy-rule draft tokens by depth waves, the target argmax from the oracle
+    (down to depth ``max_waves`` when given, random tokens below)."""
     def am(tok, par):
         return oracle.forward(shape, W, [oracle_request(shape, seed, r, ctx, tok, par)]).argmax
-    return wl.copy_rule_tokens(td, am)
+    return wl.copy_rule_tokens(td, am, max_waves)
+
+
+def oracle_copy_tokens_batch(shape, W, seed, ctxs, tds, max_waves=None):
+    """The copy rule for a batch of requests, one oracle pass per wave."""
+    def am(subs):
+        reqs = [oracle_request(shape, seed, r, ctxs[r], t, p) for r, (t, p) in enumerate(subs)]
+        out = oracle.forward(shape, W, reqs)
+        seg = np.cumsum([0] + [len(t) for t, _ in subs])
+        return [out.argmax[seg[r]:seg[r + 1]] for r in range(len(subs))]
+    return wl.copy_rule_tokens_batch(tds, am, max_waves)
 
 
 def assert_close(gpu_bits, ref):
@@ -38,25 +49,33 @@ def assert_close(gpu_bits, ref):
     return float(err.max())
 
 
-# argmax positions that broke the strict 1e-3-margin rule but whose two
-# candidates are within the logit tolerance of each other: one upstream bf16
-# rounding on the other side of a boundary moves logits by ~1e-3..1e-2, so
-# both tokens are correct answers under the logit tolerance
-STRICT_FLIPS = []
+def row_errors(gpu_bits, ref):
+    """Per row: ||gpu - oracle||_2 / ||oracle||_2."""
+    got = oracle.bf16_to_f64(np.asarray(gpu_bits).view(np.uint16))
+    return np.linalg.norm(got - ref, axis=-1) / np.maximum(np.linalg.norm(ref, axis=-1), 1e-30)
 
 
-def assert_argmax(gpu_am, ref_am, margin, ref_logits):
-    """argmax must equal the oracle's except (a) where the oracle's top-2
-    margin is below MARGIN, or (b) where the GPU's pick has an oracle logit
-    within the logit tolerance of the oracle's top logit (the two tokens are
-    indistinguishable under the logit rule); (b) cases are recorded."""
+def assert_argmax(gpu_am, ref_am, margin, ref_logits=None):
+    """argmax must equal the oracle's at every position whose oracle top-2
+    margin (fp64 logits) is at least MARGIN.  With ``ref_logits`` (end-to-end
+    comparisons through several layers, where the bf16 rounding points carry
+    fp32-vs-fp64 differences forward; see test_oracle_sensitivity.py) a
+    position may also differ when the two tokens' oracle logits are within
+    the logit tolerance of each other; such positions must be few (at most
+    one, or 1% of the rows).  Returns the mask of positions that differ."""
     gpu_am, ref_am, margin = np.asarray(gpu_am), np.asarray(ref_am), np.asarray(margin)
     diff = gpu_am != ref_am
+    bad = []
+    tol_flips = []
     for i in np.nonzero(diff & (margin >= MARGIN))[0]:
-        top = ref_logits[i, ref_am[i]]
-        alt = ref_logits[i, gpu_am[i]]
-        assert top - alt <= ATOL + RTOL * abs(top), (i, int(gpu_am[i]), int(ref_am[i]), float(top - alt))
-        STRICT_FLIPS.append((int(i), float(margin[i]), float(top - alt)))
+        if ref_logits is not None:
+            top, alt = ref_logits[i, ref_am[i]], ref_logits[i, gpu_am[i]]
+            if top - alt <= ATOL + RTOL * abs(top):
+                tol_flips.append((int(i), float(margin[i]), float(top - alt)))
+                continue
+        bad.append((int(i), int(gpu_am[i]), int(ref_am[i]), float(margin[i])))
+    assert not bad, bad
+    assert len(tol_flips) <= max(1, gpu_am.size // 100), tol_flips
     return diff
 
 
@@ -87,3 +106,108 @@ def assert_accept(tokens, parents, gpu_am, acc_len, acc_tokens, bonus, ref_am=No
         a = oracle.accept(tokens, parents, ref_am)
         assert (a.accepted_len, a.bonus) == (acc_len, bonus)
     return path
+
+
+def sub_out(out, a, b):
+    """The oracle forward's rows a..b-1 (one request of a batch) as a
+    ForwardOut of their own."""
+    kv = [(k[a:b], v[a:b]) for k, v in out.new_kv]
+    return oracle.ForwardOut(out.logits[a:b], out.argmax[a:b], out.margin[a:b], kv, out.infos)
+
+
+def cache_rows(kv, r, la, n):
+    """Request r's K and V of attention layer la at positions 0..n-1 from a
+    contiguous or paged device cache, as bf16 bits [Hkv][n][128]."""
+    if hasattr(kv, "page_table_host"):
+        t = np.arange(n)
+        pages = kv.page_table_host[r, t // kv.page_size]
+        k = kv.k[la].cpu().numpy().view(np.uint16)[pages, :, t % kv.page_size, :].transpose(1, 0, 2)
+        v = kv.v[la].cpu().numpy().view(np.uint16)[pages, :, t % kv.page_size, :].transpose(1, 0, 2)
+        return k, v
+    return kv.k[la].cpu().numpy().view(np.uint16)[:, :n], kv.v[la].cpu().numpy().view(np.uint16)[:, :n]
+
+
+def rec_rows(kv, r, lr):
+    if hasattr(kv, "page_table_host"):
+        return kv.S[r, lr].cpu().numpy(), kv.z[r, lr].cpu().numpy()
+    return kv.S[lr].cpu().numpy(), kv.z[lr].cpu().numpy()
+
+
+def assert_global_close(gpu_bits_or_vals, ref, floor=0.0):
+    """||gpu - oracle||_F <= RTOL ||oracle||_F + floor over the whole array
+    (the rule's relative part over a tensor)."""
+    a = np.asarray(gpu_bits_or_vals)
+    got = oracle.bf16_to_f64(a.view(np.uint16)) if a.dtype in (np.uint16, np.int16) else a.astype(np.float64)
+    d = float(np.linalg.norm(got - ref))
+    assert d <= RTOL * float(np.linalg.norm(ref)) + floor, (d, float(np.linalg.norm(ref)))
+    return d / max(float(np.linalg.norm(ref)), 1e-30)
+
+
+def assert_committed(shape, req, out, path, ctx, kv, r, rule="elementwise"):
+    """The committed cache equals the oracle's commit of the path the GPU
+    accepted (root .. deepest accepted node, from the GPU's own argmax):
+    the prefix untouched, the path's K/V at positions ctx + depth and the
+    recurrent state.  rule "elementwise": K/V within the logit tolerance per
+    element, the state within the bound those tolerances give its sum (plus
+    fp32 summation); rule "global" (several layers at full widths, where
+    upstream fp32-vs-fp64 differences reach the deeper layers' K/V): per
+    layer, the K/V rows and the state's increment over S0 within RTOL in
+    Frobenius norm."""
+    acc = oracle.Accept(len(path) - 1, [int(req.tokens[j]) for j in path[1:]], -1, list(path), int(path[-1]))
+    st = oracle.commit(shape, [req], out, [acc])[0]
+    n = ctx + len(path)
+    la = lr = 0
+    for l, kind in enumerate(shape.layer_kinds):
+        if kind == "attn":
+            k, v = cache_rows(kv, r, la, n)
+            assert np.array_equal(k[:, :ctx], st.layers[l].k[:, :ctx])
+            assert np.array_equal(v[:, :ctx], st.layers[l].v[:, :ctx])
+            chk = assert_close if rule == "elementwise" else assert_global_close
+            chk(k[:, ctx:n], oracle.bf16_to_f64(st.layers[l].k[:, ctx:n]))
+            chk(v[:, ctx:n], oracle.bf16_to_f64(st.layers[l].v[:, ctx:n]))
+            la += 1
+        else:
+            S, z = rec_rows(kv, r, lr)
+            S0, z0 = req.layers[l].S, req.layers[l].z
+            if rule == "global":
+                assert_global_close(S - S0, st.layers[l].S - S0, 1e-6)
+                assert_global_close(z - z0, st.layers[l].z - z0, 1e-6)
+                lr += 1
+                continue
+            # S = S0 + sum over the path of phi(k) v^T from bf16 k, v: allow
+            # each k and v the cache rows' tolerance (|d| <= ATOL + RTOL |.|,
+            # and phi' <= 1), summed over the path's terms
+            kk, vv = out.new_kv[l]
+            kp = oracle.bf16_to_f64(kk[list(path)])
+            vp = oracle.bf16_to_f64(vv[list(path)])
+            fk = oracle.phi(kp)
+            dk, dv = ATOL + RTOL * np.abs(kp), ATOL + RTOL * np.abs(vp)
+            bS = np.einsum("phk,phv->hkv", dk, np.abs(vp) + dv) + np.einsum("phk,phv->hkv", fk, dv)
+            assert np.all(np.abs(S - st.layers[l].S) <= 1e-5 + 1e-6 * np.abs(st.layers[l].S) + bS)
+            assert np.all(np.abs(z - st.layers[l].z) <= 1e-5 + 1e-6 * np.abs(st.layers[l].z) + dk.sum(axis=0))
+            lr += 1
+
+
+def assert_commit_is_copy(model, M_, tokens, parents, kv_committed, ctx, path, fresh_kv):
+    """Compaction moves bits: the committed K/V at ctx + depth equal, bit
+    for bit, what a forward pass of the same step wrote for the path's
+    nodes at ctx + node (fresh_kv: a copy of the cache before the step)."""
+    model.forward(tokens, parents, fresh_kv, logits=False)
+    import torch
+    torch.cuda.synchronize()
+    for la in range(kv_committed.k.shape[0]):
+        for d, node in enumerate(path):
+            assert torch.equal(kv_committed.k[la, :, ctx + d], fresh_kv.k[la, :, ctx + node])
+            assert torch.equal(kv_committed.v[la, :, ctx + d], fresh_kv.v[la, :, ctx + node])
+
+
+def assert_final_hidden(model, o, lm_head, rows):
+    """The step's logits and argmax against the oracle's lm_head applied to
+    the step's own final hidden state (sd_model_final_hidden): one GEMM of
+    difference, so the element-wise logit tolerance and the strict margin
+    rule hold."""
+    xf = model.final_hidden(rows).cpu().numpy().view(np.uint16)
+    lg = oracle.linear(xf, lm_head)
+    am, margin = oracle.argmax_margin(lg)
+    assert_close(o["logits"].cpu().numpy(), lg)
+    assert_argmax(o["argmax"].cpu().numpy(), am, margin)

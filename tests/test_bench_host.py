@@ -18,8 +18,8 @@ def test_step_distribution_of_known_samples():
     assert one["ci95_ms"] == [2.5, 2.5] and one["median_ms"] == 2.5
 
 
-def test_overhead_factor_counts_top_level_launches_once():
-    tl = [("gemm_qkv", 1.0, 0.0), ("attention", 0.5, 0.0), ("chain.gemm_o", 0.3, 0.0), ("gemm_o", 0.5, 0.0)]
+def test_overhead_factor_over_the_serialised_launches():
+    tl = [("gemm_stream", 1.0, 0.0), ("attention", 0.5, 0.0), ("gemm_stream", 0.5, 0.0)]
     f, total = bench.overhead_factor(1.5, tl)
     assert total == 2.0 and f == 0.75
     assert bench.overhead_factor(1.0, []) == (None, 0)

@@ -1,0 +1,122 @@
+"""End-to-end verify against the oracle at the named models' layer widths.
+
+Few layers, full dimensions: the 8B-class decoder (GQA group 4, hidden 4096,
+intermediate 12288, the 151936-row lm_head inside the step, context 2048
+with the automatic attention split count), the ~27B-class decoder (group 5,
+hidden 5120, intermediate 21504, context 4096, a 64-node tree), the hybrid
+target (32-head recurrent layers beside a full-width attention layer) and
+the batched paged step (32 requests x 8-row chains, contexts in
+[1024, 4096], 256 rows on the tensor-core GEMM).  Logits within the
+rule's relative tolerance over the tensor (Frobenius norm; the element-wise
+bound is out of reach of any fp32-accumulating implementation at these
+widths, see test_oracle_sensitivity.py), and element-wise against the
+oracle's lm_head over the step's own final hidden state, where the argmax
+must also meet the strict margin rule; argmax end to end under the margin
+rule with the bounded logit-tolerance exemption; the accept walk and the
+context lengths exactly; the committed K/V and state per layer within the
+relative tolerance, and the compaction a bit-exact copy of the step's own
+K/V.
+
+Draft tokens follow the copy rule down to depth 2 or 3 (one oracle pass of
+the whole model per depth); deeper nodes take their random tokens, which
+changes no work of the step."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import workloads as wl
+from helpers import (assert_accept, assert_argmax, assert_commit_is_copy, assert_committed, assert_final_hidden,
+                     assert_global_close, row_errors,
+                     oracle_copy_tokens,
+                     oracle_copy_tokens_batch, oracle_request, sub_out)
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module")
+def M():
+    from speculative_decoding_tree_bit_gb300 import model
+    return model
+
+
+def _np(t):
+    return t.cpu().numpy()
+
+
+def _single(M, shape_name, m, max_depth, ctx, p, waves, seed=0):
+    shape = wl.SHAPES[shape_name]
+    W = wl.SyntheticWeights(shape, seed=seed, cache=True)
+    model = M.Model(shape, W, max_rows=64, max_requests=1, max_positions=ctx + 80)
+    try:
+        td = wl.draft(seed, 0, m, max_depth, p, shape.V)
+        tokens = oracle_copy_tokens(shape, W, seed, 0, ctx, td, max_waves=waves)
+        req = oracle_request(shape, seed, 0, ctx, tokens, td.parents, cap=ctx + 80)
+        out = oracle.forward(shape, W, [req])
+        kv = M.KVCache(shape, ctx + 80).fill(seed, ctx)
+        fresh = M.KVCache(shape, ctx + 80).fill(seed, ctx)
+        o = model.verify(tokens, td.parents, kv, logits=True)
+        torch.cuda.synchronize()
+        assert model.status() == 0
+        rel = assert_global_close(_np(o["logits"]), out.logits)
+        print(f"{shape_name}: logits relative error {rel:.2e} (largest row {row_errors(_np(o['logits']), out.logits).max():.2e})")
+        assert_final_hidden(model, o, W.lm_head(), m)
+        am = _np(o["argmax"])
+        assert_argmax(am, out.argmax, out.margin, out.logits)
+        path = assert_accept(tokens, td.parents, am, int(o["accepted_len"][0]), _np(o["accepted_tokens"]),
+                             int(o["bonus"][0]), out.argmax)
+        L = int(o["accepted_len"][0])
+        assert int(kv.ctx_len[0]) == ctx + L + 1
+        assert_committed(shape, req, out, path, ctx, kv, 0, rule="global")
+        assert_commit_is_copy(model, m, tokens, td.parents, kv, ctx, path, fresh)
+        return L
+    finally:
+        model.close()
+
+
+def test_8b_dims_two_layers_tree16_ctx2048(M):
+    _single(M, "8b_2l", 16, 8, 2048, 0.7, waves=3)
+
+
+def test_27b_dims_two_layers_tree64_ctx4096(M):
+    _single(M, "27b_2l", 64, 10, 4096, 0.7, waves=2)
+
+
+def test_hybrid_dims_four_layers_tree16(M):
+    _single(M, "hybrid_4l", 16, 8, 2048, 0.7, waves=3)
+
+
+def test_batched_8b_dims_two_layers_r32_paged(M):
+    """32 requests x 8-row chains (256 rows: the tensor-core GEMM), paged
+    cache of 16-slot pages in a random permutation, contexts U[1024, 4096]."""
+    seed = 0
+    shape = wl.SHAPES["8b_2l"]
+    wk = wl.make("batched_r32", seed)
+    W = wl.SyntheticWeights(shape, seed=seed, cache=True)
+    R, ctxs = wk.R, wk.ctx
+    model = M.Model(shape, W, max_rows=256, max_requests=R, max_positions=max(ctxs) + 80)
+    try:
+        toks = oracle_copy_tokens_batch(shape, W, seed, ctxs, wk.drafts, max_waves=2)
+        reqs = [oracle_request(shape, seed, r, ctxs[r], toks[r], wk.drafts[r].parents, cap=ctxs[r] + 32)
+                for r in range(R)]
+        out = oracle.forward(shape, W, reqs)
+        table, n_pages = wl.page_tables(seed, ctxs, wk.M, 16)
+        kv = M.PagedKVCache(shape, table, n_pages, 16).fill(seed, ctxs)
+        cu = np.cumsum([0] + [len(t) for t in toks])
+        o = model.verify_batch(np.concatenate(toks), np.concatenate([d.parents for d in wk.drafts]), cu, kv,
+                               logits=True)
+        torch.cuda.synchronize()
+        assert model.status() == 0
+        rel = assert_global_close(_np(o["logits"]), out.logits)
+        print(f"batched: logits relative error {rel:.2e} (largest row {row_errors(_np(o['logits']), out.logits).max():.2e})")
+        assert_final_hidden(model, o, W.lm_head(), int(cu[-1]))
+        am = _np(o["argmax"])
+        assert_argmax(am, out.argmax, out.margin, out.logits)
+        for r in range(R):
+            a, b = cu[r], cu[r + 1]
+            path = assert_accept(toks[r], wk.drafts[r].parents, am[a:b], int(o["accepted_len"][r]),
+                                 _np(o["accepted_tokens"][a:b]), int(o["bonus"][r]), out.argmax[a:b])
+            assert int(kv.ctx_len[r]) == ctxs[r] + int(o["accepted_len"][r]) + 1
+            assert_committed(shape, reqs[r], sub_out(out, a, b), path, ctxs[r], kv, r, rule="global")
+    finally:
+        model.close()
