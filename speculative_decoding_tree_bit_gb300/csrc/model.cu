@@ -63,8 +63,8 @@ struct sd_model {
   int n_sites = 0;
   float* stream_part = nullptr;
   size_t stream_part_floats = 0;
-  float* ss_h = nullptr;  // [H/128][128]: of h (O's output)
-  float* ss_x = nullptr;  // [H/128][128]: of x (down's output)
+  float* ss_h = nullptr;  // [H/128][9][128]: of h (O's output)
+  float* ss_x = nullptr;  // [H/128][9][128]: of x (down's output)
   // optional per-kernel timing
   bool timing = false;  // events around every kernel launch
   std::vector<cudaEvent_t> events;  // 2 per entry
@@ -670,8 +670,8 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
       {(void**)&m->gws.counters, (size_t)gemm_counters(max_n) * 4},
       {(void**)&m->stream_state, (size_t)m->n_sites * m->site_ints * 4},
       {(void**)&m->stream_part, m->stream_part_floats * 4},
-      {(void**)&m->ss_h, (size_t)(m->H / 128) * 128 * 4},
-      {(void**)&m->ss_x, (size_t)(m->H / 128) * 128 * 4},
+      {(void**)&m->ss_h, (size_t)(m->H / 128) * 9 * 128 * 4},
+      {(void**)&m->ss_x, (size_t)(m->H / 128) * 9 * 128 * 4},
   };
   size_t total = 0;
   for (auto& it : items) total = al256(total + it.bytes);

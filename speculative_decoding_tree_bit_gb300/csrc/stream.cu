@@ -51,6 +51,7 @@ constexpr int kSEsc = 9;        // escape-correction warp
 constexpr int kSNorm = 10;      // activation-tile warp (RMSNorm rewrite)
 constexpr int kSThreads = 11 * 32;
 constexpr int kSChunkTiles = 8;  // k-tiles per chunk of a split block (target)
+constexpr int kUq = 8;           // entries of the unit queue (producer -> escape warp)
 
 template <int NT>
 constexpr int s_ctas_per_sm() { return NT <= 4 ? 2 : 1; }
@@ -76,9 +77,9 @@ struct StreamPhase {
   int nss;
   uint16_t* norm_out;
   int dep, dep_fine;
-  float* out_ss;  // [NB][128]
+  float* out_ss;  // [NB][128] block sums, then [NB][8][128] strip sums
   float* part;    // split partials [(NB - nb_whole) * S][128 * MP]
-  int32_t* st;    // [0] next unit, [1] blocks done, [2, 2 + NB) tickets, [2 + NB, 2 + 2 NB) done flags
+  int32_t* st;    // [0] next unit, [1] blocks done, [2, 2 + 8 NB) strip tickets, then NB block counters, NB done flags
 };
 
 struct StreamArgs {
@@ -109,7 +110,8 @@ struct SCfg {
   static constexpr int OFF_RED_V = OFF_RINV + MP * 4;
   static constexpr int OFF_RED_I = OFF_RED_V + kSCons * MP * 4;
   static constexpr int OFF_PH = (OFF_RED_I + kSCons * MP * 4 + 15) & ~15;
-  static constexpr int OFF_CORR = (OFF_PH + (int)sizeof(StreamPhase) + 15) & ~15;
+  static constexpr int OFF_UQ = (OFF_PH + (int)sizeof(StreamPhase) + 15) & ~15;
+  static constexpr int OFF_CORR = (OFF_UQ + kUq * 20 + 15) & ~15;
   static constexpr int END = OFF_CORR + 128 * MP * 4;
   static constexpr int SMEM = 1024 + END;
 };
@@ -174,10 +176,19 @@ __device__ __forceinline__ int ld_acquire_s32(const int32_t* p) {
 __device__ __forceinline__ void fence_proxy_async_global_s() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // ------------------------------------------------------------ producer --
+// Lane 0 of the producer warp takes units (moving on through the phases),
+// announces each unit in a small queue (so the escape warp can prefetch its
+// escape index entries a unit ahead) and streams the units' weight tiles;
+// activation tiles are queued until what they read is complete.
+
+struct UnitQ {
+  int4 d[kUq];        // phase, row block, first tile, end tile
+  volatile int seq[kUq];  // the CTA's unit number held in the entry
+};
 
 template <int NT>
 __device__ __forceinline__ void s_produce(const StreamArgs& a, uint8_t* sx, uint8_t* sw, int4* info, uint64_t* full,
-                                          uint64_t* empty, volatile int* abort) {
+                                          uint64_t* empty, UnitQ* uq, volatile int* abort) {
   using C = SCfg<NT>;
   int slot = 0, round = 0;
   int64_t uses = 0;  // slot uses, the end marker included
@@ -201,7 +212,7 @@ __device__ __forceinline__ void s_produce(const StreamArgs& a, uint8_t* sx, uint
     const StreamPhase& Q = a.ph[P.dep];
     if (ld_acquire_s32(Q.st + 1) >= Q.NB) {
       all_ready[p] = true;
-    } else if (!P.dep_fine || ld_acquire_s32(Q.st + 2 + Q.NB + t) == 0) {
+    } else if (!P.dep_fine || ld_acquire_s32(Q.st + 2 + 9 * Q.NB + t) == 0) {
       return false;
     }
     fence_proxy_async_global_s();
@@ -239,40 +250,67 @@ __device__ __forceinline__ void s_produce(const StreamArgs& a, uint8_t* sx, uint
       round++;
     }
   };
-
-  for (int p = 0; p < a.n && ok; p++) {
-    const StreamPhase& P = a.ph[p];
-    int u = atomicAdd(P.st, 1);
-    while (u < P.U && ok) {
-      int b, c, t0, t1;
-      unit_of(P, u, b, c, t0, t1);
-      const int un = atomicAdd(P.st, 1);  // the next unit, taken while this one streams
-      for (int t = t0; t < t1; t++) {
-        if (!wait_slot()) {
-          ok = false;
-          break;
-        }
-        info[slot] = make_int4(p, b, t, (t == t0 ? 1 : 0) | (t == t1 - 1 ? 2 : 0) | ((c + 1) << 8) | (t1 << 16));
-        mbar_arrive_expect_tx(&full[slot], (P.view8 ? C::WB8 : C::WB) + C::XB);
-        tma2d_g2s(sw + slot * C::WB, &a.wmap[p], t * (P.view8 ? 128 : 192), b * kRB, &full[slot]);
-        const int qi = (qh + qn) % C::RING;
-        q_slot[qi] = slot;
-        q_p[qi] = p;
-        q_t[qi] = t;
-        qn++;
-        flush();
-        advance();
-      }
-      u = un;
+  // the next unit, moving on to the next phase when one runs out
+  auto grab = [&](int& p, int& u) -> bool {
+    while (p < a.n) {
+      u = atomicAdd(a.ph[p].st, 1);
+      if (u < a.ph[p].U) return true;
+      p++;
     }
+    return false;
+  };
+  auto publish = [&](int k, bool have, int p, int u) {
+    int4 d = make_int4(-1, 0, 0, 0);
+    if (have) {
+      int b, c, t0, t1;
+      unit_of(a.ph[p], u, b, c, t0, t1);
+      d = make_int4(p, b, t0, t1);
+    }
+    uq->d[k % kUq] = d;
+    __threadfence_block();
+    uq->seq[k % kUq] = k;
+  };
+
+  int p = 0, u = 0, k = 0;
+  bool have = grab(p, u);
+  publish(0, have, p, u);
+  while (have && ok) {
+    const StreamPhase& P = a.ph[p];
+    int b, c, t0, t1;
+    unit_of(P, u, b, c, t0, t1);
+    int pn = p, un = 0;
+    bool have_n = false;
+    for (int t = t0; t < t1; t++) {
+      if (!wait_slot()) {
+        ok = false;
+        break;
+      }
+      info[slot] = make_int4(p, b, t, (t == t0 ? 1 : 0) | (t == t1 - 1 ? 2 : 0) | ((c + 1) << 8) | (t1 << 16));
+      mbar_arrive_expect_tx(&full[slot], (P.view8 ? C::WB8 : C::WB) + C::XB);
+      tma2d_g2s(sw + slot * C::WB, &a.wmap[p], t * (P.view8 ? 128 : 192), b * kRB, &full[slot]);
+      const int qi = (qh + qn) % C::RING;
+      q_slot[qi] = slot;
+      q_p[qi] = p;
+      q_t[qi] = t;
+      qn++;
+      flush();
+      advance();
+      if (t == t0) {
+        // the next unit, announced while this one streams
+        have_n = grab(pn, un);
+        publish(k + 1, have_n, pn, un);
+      }
+    }
+    p = pn;
+    u = un;
+    have = have_n;
+    k++;
   }
   // end marker (plain arrival: no bytes)
   if (ok && wait_slot()) {
     info[slot] = make_int4(-1, 0, 0, 0);
     mbar_arrive(&full[slot]);
     advance();
-  } else {
-    ok = false;
   }
   {
     const uint64_t t0 = globaltimer();
@@ -324,15 +362,32 @@ __device__ __forceinline__ void s_norm(const StreamArgs& a, uint8_t* sx, const i
     const StreamPhase& P = a.ph[in.x];
     if (P.gamma) {
       if (in.x != cur) {
-        // 1/rms per token row from the producing phase's per-block sums
-        // (summed in block order); the acquire orders them after its flags
+        // 1/rms per token row from the producing phase's per-block sums of
+        // squares: lanes over the blocks, all loads in flight, then a fixed
+        // butterfly (the acquire orders them after the blocks' flags)
         const StreamPhase& Q = a.ph[P.dep];
         if (lane == 0) (void)ld_acquire_s32(Q.st + 1);
         __syncwarp();
-        for (int m = lane; m < MP; m += 32) {
-          float ss = 0.f;
-          for (int bq = 0; bq < P.nss; bq++) ss += __ldcg(P.in_ss + bq * 128 + m);
-          rinv[m] = 1.0f / sqrtf(ss / (float)P.K + P.eps);
+#pragma unroll 1
+        for (int m0 = 0; m0 < MP; m0 += 16) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; j++) v[j] = 0.f;
+          for (int bq = lane; bq < P.nss; bq += 32) {
+#pragma unroll
+            for (int j = 0; j < 16; j++) v[j] += __ldcg(P.in_ss + bq * 128 + m0 + j);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; j++) {
+#pragma unroll
+            for (int o = 16; o; o >>= 1) v[j] += __shfl_xor_sync(0xffffffffu, v[j], o);
+          }
+          if (lane < 16) {
+            float mine = v[0];
+#pragma unroll
+            for (int j = 1; j < 16; j++) mine = lane == j ? v[j] : mine;
+            rinv[m0 + lane] = 1.0f / sqrtf(mine / (float)P.K + P.eps);
+          }
         }
         __syncwarp();
       }
@@ -373,18 +428,45 @@ __device__ __forceinline__ void s_norm(const StreamArgs& a, uint8_t* sx, const i
 // Per unit, the corrections (w - slot) x[m][k] of the escapes of its rows
 // and k-tiles into corr[128 rows][MP], from the staged (normalised) tiles,
 // one escape at a time with the lanes over the token rows (fixed order).
+// The index entries of a unit (tile pointers of up to 32 tiles, the first
+// 128 entries) are loaded when the previous unit starts, from the unit
+// queue, so that they are in registers when the unit's tiles arrive.
+
+struct EscMeta {
+  int p = -1, b = 0, tc = 0, tend = 0;
+  uint32_t tpa = 0, tpb = 0, e_lo = 0;
+  uint32_t ent[4] = {0, 0, 0, 0};
+};
+
+__device__ __forceinline__ void esc_meta_load(const StreamPhase& P, int p, int b, int tc, int tend, EscMeta& m) {
+  const int lane = threadIdx.x & 31;
+  m.p = p;
+  m.b = b;
+  m.tc = tc;
+  m.tend = tend;
+  if (!P.tile_ptr) return;
+  const uint32_t* tp = P.tile_ptr + (int64_t)b * P.KT;
+  m.tpa = __ldg(tp + min(tc + lane, tend));
+  m.tpb = __ldg(tp + min(tc + lane + 1, tend));
+  m.e_lo = __shfl_sync(0xffffffffu, m.tpa, 0);
+  const uint32_t e_hi = __shfl_sync(0xffffffffu, m.tpb, min(31, tend - 1 - tc));
+#pragma unroll
+  for (int j = 0; j < 4; j++) {
+    const uint32_t e = m.e_lo + lane + 32 * j;
+    m.ent[j] = e < e_hi ? __ldg(P.tile_esc + e) : 0u;
+  }
+}
 
 template <int NT>
 __device__ __forceinline__ void s_escape(const StreamArgs& a, const uint8_t* sx, const int4* info, uint64_t* xrdy,
                                          uint64_t* empty, float* corr, uint64_t* corr_full, uint64_t* corr_empty,
-                                         volatile int* abort) {
+                                         const UnitQ* uq, volatile int* abort) {
   using C = SCfg<NT>;
   constexpr int MP = C::MP;
   const int lane = threadIdx.x & 31;
   const int mrows = min(MP, a.M);
-  int slot = 0, round = 0, eseg = 0;
-  int tc = -1;
-  uint32_t tpa = 0, tpb = 0, e_lo = 0, ent[4] = {0, 0, 0, 0};
+  int slot = 0, round = 0, eseg = 0, k = -1;
+  EscMeta cur, nxt;
   for (;;) {
     if (!mbar_wait_or_abort(&xrdy[slot], (uint32_t)round & 1u, abort)) {
       set_status(a.status, SD_TIMEOUT_AT(35));
@@ -395,6 +477,7 @@ __device__ __forceinline__ void s_escape(const StreamArgs& a, const uint8_t* sx,
     const StreamPhase& P = a.ph[in.x];
     const int b = in.y, t = in.z, tend = info_tend(in.w);
     if (in.w & 1) {
+      k++;
       if (!mbar_wait_or_abort(corr_empty, (uint32_t)(eseg & 1) ^ 1u, abort)) set_status(a.status, SD_TIMEOUT_AT(36));
 #pragma unroll
       for (int i = 0; i < 4; i++) {
@@ -402,32 +485,30 @@ __device__ __forceinline__ void s_escape(const StreamArgs& a, const uint8_t* sx,
 #pragma unroll
         for (int m = 0; m < MP; m += 4) *reinterpret_cast<float4*>(row + m) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      tc = -1;
+      if (nxt.p == in.x && nxt.b == b && nxt.tc == t && nxt.tend == tend) {
+        cur = nxt;
+      } else {
+        esc_meta_load(P, in.x, b, t, tend, cur);
+      }
+      nxt.p = -1;
+      // the next unit's entries, if it is announced already
+      const int j = (k + 1) % kUq;
+      if (uq->seq[j] == k + 1) {
+        __threadfence_block();
+        const int4 d = uq->d[j];
+        if (d.x >= 0) esc_meta_load(a.ph[d.x], d.x, d.y, d.z, d.w, nxt);
+      }
     }
     if (P.tile_ptr) {
-      if (tc < 0 || t - tc >= 32) {
-        // tile pointers of tiles tc .. tc + 31 of this block (lane i: tile
-        // tc + i's start and end) and the first 128 entries they cover
-        tc = t;
-        const uint32_t* tp = P.tile_ptr + (int64_t)b * P.KT;
-        tpa = __ldg(tp + min(tc + lane, tend));
-        tpb = __ldg(tp + min(tc + lane + 1, tend));
-        e_lo = __shfl_sync(0xffffffffu, tpa, 0);
-        const uint32_t e_hi = __shfl_sync(0xffffffffu, tpb, min(31, tend - 1 - tc));
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-          const uint32_t e = e_lo + lane + 32 * j;
-          ent[j] = e < e_hi ? __ldg(P.tile_esc + e) : 0u;
-        }
-      }
-      const uint32_t lo = __shfl_sync(0xffffffffu, tpa, t - tc);
-      const uint32_t hi = __shfl_sync(0xffffffffu, tpb, t - tc);
+      if (t - cur.tc >= 32) esc_meta_load(P, in.x, b, t, tend, cur);  // a unit of more than 32 tiles
+      const uint32_t lo = __shfl_sync(0xffffffffu, cur.tpa, t - cur.tc);
+      const uint32_t hi = __shfl_sync(0xffffffffu, cur.tpb, t - cur.tc);
       const uint8_t* xs = sx + slot * C::XB;
       for (uint32_t e = lo; e < hi; e++) {
-        const uint32_t idx = e - e_lo;
+        const uint32_t idx = e - cur.e_lo;
         uint32_t v;
         if (idx < 128) {
-          const uint32_t r = idx < 32 ? ent[0] : idx < 64 ? ent[1] : idx < 96 ? ent[2] : ent[3];
+          const uint32_t r = idx < 32 ? cur.ent[0] : idx < 64 ? cur.ent[1] : idx < 96 ? cur.ent[2] : cur.ent[3];
           v = __shfl_sync(0xffffffffu, r, idx & 31);
         } else {
           v = __ldg(P.tile_esc + e);
@@ -587,12 +668,64 @@ __device__ __forceinline__ void s_epilogue(const StreamPhase& P, int M, int stri
 }
 
 // ---------------------------------------------------------- consumers --
+// Each consumer warp owns one 16-row strip of the current row block and
+// finishes its strip on its own: a k-chunk of a split block leaves its fp32
+// partial in the chunk's slot and takes a per-strip ticket (its result is
+// looked at one stage later, so the warp does not wait for the atomic); the
+// warp whose ticket completes the strip sums the strip's slots in chunk
+// order (deterministic) and runs the strip's epilogue.  The strip
+// finishers of a block count in a per-block counter; the last one adds the
+// strips' sums of squares (residual epilogues) and publishes the block.
+
+template <int NT>
+__device__ __forceinline__ void s_strip_done(const StreamPhase& P, int b, int warp, int lane, float (&rs)[NT][2]) {
+  constexpr int MP = NT * 8;
+  if (P.out_ss) {
+    // the strip's sum of squares per token row (its 16 rows by shuffles)
+    float* dst = P.out_ss + (int64_t)P.NB * 128 + ((int64_t)b * 8 + warp) * 128;
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int cc = 0; cc < 2; cc++) {
+        float v = rs[nt][cc];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        if (lane < 4) __stcg(dst + nt * 8 + 2 * lane + cc, v);
+      }
+  }
+  __syncwarp();
+  int old = 0;
+  if (lane == 0) {
+    __threadfence();
+    old = atomicAdd(P.st + 2 + 8 * P.NB + b, 1);
+  }
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old + 1 != kRB) return;
+  // the block's last strip: the block sums (strips in order), then its flag
+  if (P.out_ss) {
+    __threadfence();
+    const float* src = P.out_ss + (int64_t)P.NB * 128 + (int64_t)b * 8 * 128;
+    for (int m = lane; m < MP; m += 32) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kRB; w++) v += __ldcg(src + w * 128 + m);
+      P.out_ss[(int64_t)b * 128 + m] = v;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    asm volatile("st.release.gpu.global.s32 [%0], 1;" ::"l"(P.st + 2 + 9 * P.NB + b) : "memory");
+    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(P.st + 1) : "memory");
+  }
+}
 
 template <int NT>
 __device__ __forceinline__ void s_consume(const StreamArgs& a, const uint8_t* sx, const uint8_t* sw, const int4* info,
                                           uint64_t* xrdy, uint64_t* empty, const float* corr, uint64_t* corr_full,
                                           uint64_t* corr_empty, StreamPhase* sph, float* red_v, int* red_i,
-                                          int* flag, uint64_t* cbar, volatile int* abort) {
+                                          uint64_t* cbar, volatile int* abort) {
   using C = SCfg<NT>;
   constexpr int MP = C::MP;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
@@ -617,10 +750,69 @@ __device__ __forceinline__ void s_consume(const StreamArgs& a, const uint8_t* sx
         if constexpr (kDual) acc2[nt][c] = 0.f;
       }
   };
+  // the strip region of a split block's chunk slot
+  auto slot_ptr = [&](const StreamPhase& P, int b, int c) {
+    return P.part + ((int64_t)(b - P.nb_whole) * P.S + c) * (128 * MP) + ((warp * NT) * 32 + lane) * 4;
+  };
+  // epilogue of this warp's strip of block b from its sums, then the
+  // block's bookkeeping
+  auto finish_strip = [&](const StreamPhase& P, int b, float (&sum)[NT][4]) {
+    float rs[NT][2];
+    const int strip = b * kRB + warp;
+    if (strip < P.NS) {
+      s_epilogue<NT>(P, a.M, strip, lane, sum, bestv, besti, rs);
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++) rs[nt][0] = rs[nt][1] = 0.f;
+    }
+    s_strip_done<NT>(P, b, warp, lane, rs);
+  };
+  // a pending ticket (split chunk): if it completed the strip, sum the
+  // strip's chunk slots in order and finish it
+  int pend_b = -1, pend_old = 0;
+  auto resolve = [&](const StreamPhase& P) {
+    if (pend_b < 0) return;
+    const int old = __shfl_sync(0xffffffffu, pend_old, 0);
+    const int b = pend_b;
+    pend_b = -1;
+    if (old + 1 != P.S) return;
+    float tot[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) tot[nt][0] = tot[nt][1] = tot[nt][2] = tot[nt][3] = 0.f;
+    constexpr int kB = NT <= 1 ? 8 : NT <= 2 ? 4 : 2;
+    for (int c0 = 0; c0 < P.S; c0 += kB) {
+      float4 v[kB][NT];
+#pragma unroll
+      for (int u = 0; u < kB; u++) {
+        const bool ld = c0 + u < P.S;
+        const float* src = slot_ptr(P, b, ld ? c0 + u : 0);
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+          v[u][nt] = ld ? __ldcg(reinterpret_cast<const float4*>(src + nt * 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kB; u++) {
+        if (c0 + u >= P.S) continue;
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+          tot[nt][0] += v[u][nt].x;
+          tot[nt][1] += v[u][nt].y;
+          tot[nt][2] += v[u][nt].z;
+          tot[nt][3] += v[u][nt].w;
+        }
+      }
+    }
+    finish_strip(P, b, tot);  // acc may already hold the next unit's sums
+  };
+
   pdl_wait();  // residuals and cache positions come from earlier kernels
   int slot = 0, round = 0, cseg = 0, cur = -1;
+  bool fresh = true;  // acc holds nothing of the current unit yet
   zero();
   for (;;) {
+    // a pending ticket is settled before any wait that is not already over:
+    // the next tile may read the very block that ticket completes
+    if (pend_b >= 0 && !mbar_test_wait(&xrdy[slot], (uint32_t)round & 1u)) resolve(*sph);
     if (!mbar_wait_or_abort(&xrdy[slot], (uint32_t)round & 1u, abort)) {
       set_status(a.status, SD_TIMEOUT_AT(37));
       break;
@@ -628,7 +820,9 @@ __device__ __forceinline__ void s_consume(const StreamArgs& a, const uint8_t* sx
     const int4 in = info[slot];
     if (in.x < 0) break;
     if (in.x != cur) {
-      // the phase's descriptor in shared memory (uniform loads in the hot loop)
+      // a pending ticket belongs to the old phase: settle it first; then the
+      // phase's descriptor in shared memory (uniform loads in the hot loop)
+      if (cur >= 0) resolve(*sph);
       if (!cons_sync(cbar, cph, abort)) break;
       const uint32_t* src = reinterpret_cast<const uint32_t*>(&a.ph[in.x]);
       uint32_t* dst = reinterpret_cast<uint32_t*>(sph);
@@ -638,7 +832,8 @@ __device__ __forceinline__ void s_consume(const StreamArgs& a, const uint8_t* sx
     }
     const StreamPhase& P = *sph;
     const int b = in.y;
-    if (in.w & 1) zero();
+    if ((in.w & 1) && !fresh) zero();
+    fresh = false;
     const int strip = b * kRB + warp;
     if (strip < P.NS) {
       const bool v8 = P.view8 != 0;
@@ -682,6 +877,8 @@ __device__ __forceinline__ void s_consume(const StreamArgs& a, const uint8_t* sx
       slot = 0;
       round++;
     }
+    // the ticket of the previous unit has had a stage's time to come back
+    resolve(P);
     if (!(in.w & 2)) continue;
 
     // ------------------------------------------------ unit finished --
@@ -706,92 +903,25 @@ __device__ __forceinline__ void s_consume(const StreamArgs& a, const uint8_t* sx
     if (lane == 0) mbar_arrive(corr_empty);
     cseg++;
     const int chunk = info_chunk(in.w);
-    if (chunk >= 0) {
-      // a k-chunk of a split block: partial to its slot, ticket; the last
-      // chunk to arrive sums the slots in chunk order and finishes
-      const int64_t slot_floats = 128 * MP;
-      const int64_t sb = (int64_t)(b - P.nb_whole) * P.S;
-      float* mine = P.part + (sb + chunk) * slot_floats + ((warp * NT) * 32 + lane) * 4;
+    if (chunk < 0) {
+      finish_strip(P, b, acc);  // a whole block: no partial, no ticket
+    } else {
+      float* mine = slot_ptr(P, b, chunk);
 #pragma unroll
       for (int nt = 0; nt < NT; nt++)
         __stcg(reinterpret_cast<float4*>(mine + nt * 128),
                make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]));
-      if (!cons_sync(cbar, cph, abort)) break;
-      if (tid == 0) {
-        const int old = atomic_add_acq_rel(P.st + 2 + b, 1);
-        *flag = old + 1 == P.S ? 1 : 0;
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        pend_old = atomicAdd(P.st + 2 + b * kRB + warp, 1);
       }
-      if (!cons_sync(cbar, cph, abort)) break;
-      if (!*flag) continue;
-      float tot[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; nt++) tot[nt][0] = tot[nt][1] = tot[nt][2] = tot[nt][3] = 0.f;
-      constexpr int kB = NT <= 1 ? 8 : NT <= 2 ? 4 : 2;
-      for (int c0 = 0; c0 < P.S; c0 += kB) {
-        float4 v[kB][NT];
-#pragma unroll
-        for (int u = 0; u < kB; u++) {
-          const int cc = c0 + u;
-          const bool ld = cc < P.S && cc != chunk;
-          const float* src = P.part + (sb + (ld ? cc : chunk)) * slot_floats + ((warp * NT) * 32 + lane) * 4;
-#pragma unroll
-          for (int nt = 0; nt < NT; nt++)
-            v[u][nt] = ld ? __ldcg(reinterpret_cast<const float4*>(src + nt * 128))
-                          : make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-        }
-#pragma unroll
-        for (int u = 0; u < kB; u++) {
-          if (c0 + u >= P.S) continue;
-#pragma unroll
-          for (int nt = 0; nt < NT; nt++) {
-            tot[nt][0] += v[u][nt].x;
-            tot[nt][1] += v[u][nt].y;
-            tot[nt][2] += v[u][nt].z;
-            tot[nt][3] += v[u][nt].w;
-          }
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-        for (int c = 0; c < 4; c++) acc[nt][c] = tot[nt][c];
+      pend_b = b;
     }
-    // epilogue of block b, then its completion flag
-    float rs[NT][2];
-    if (strip < P.NS) {
-      s_epilogue<NT>(P, a.M, strip, lane, acc, bestv, besti, rs);
-    } else {
-#pragma unroll
-      for (int nt = 0; nt < NT; nt++) rs[nt][0] = rs[nt][1] = 0.f;
-    }
-    if (P.out_ss) {
-      // sums of squares of the block's outputs per token row: over the
-      // warp's 16 rows by shuffles, then over the 8 warps in order
-#pragma unroll
-      for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-        for (int cc = 0; cc < 2; cc++) {
-          float v = rs[nt][cc];
-          v += __shfl_xor_sync(0xffffffffu, v, 4);
-          v += __shfl_xor_sync(0xffffffffu, v, 8);
-          v += __shfl_xor_sync(0xffffffffu, v, 16);
-          if (lane < 4) red_v[warp * MP + nt * 8 + 2 * lane + cc] = v;
-        }
-      if (!cons_sync(cbar, cph, abort)) break;
-      if (tid < MP) {
-        float s = 0.f;
-        for (int w = 0; w < kSCons; w++) s += red_v[w * MP + tid];
-        P.out_ss[(int64_t)b * 128 + tid] = s;
-      }
-    }
-    // every epilogue store (and red_v read) of the block before its flag
-    if (!cons_sync(cbar, cph, abort)) break;
-    if (tid == 0) {
-      __threadfence();
-      asm volatile("st.release.gpu.global.s32 [%0], 1;" ::"l"(P.st + 2 + P.NB + b) : "memory");
-      asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(P.st + 1) : "memory");
-    }
+    zero();
+    fresh = true;
   }
+  if (cur >= 0) resolve(*sph);
 
   // per-CTA argmax partial of a logits phase (every CTA writes one)
   bool logits = false;
@@ -864,6 +994,7 @@ __global__ void __launch_bounds__(kSThreads, s_ctas_per_sm<NT>()) k_w12_stream(c
   float* red_v = reinterpret_cast<float*>(smem + C::OFF_RED_V);
   int* red_i = reinterpret_cast<int*>(smem + C::OFF_RED_I);
   StreamPhase* sph = reinterpret_cast<StreamPhase*>(smem + C::OFF_PH);
+  UnitQ* uq = reinterpret_cast<UnitQ*>(smem + C::OFF_UQ);
   float* corr = reinterpret_cast<float*>(smem + C::OFF_CORR);
 
   const int warp = threadIdx.x >> 5;
@@ -879,19 +1010,20 @@ __global__ void __launch_bounds__(kSThreads, s_ctas_per_sm<NT>()) k_w12_stream(c
     flag[0] = 0;
     flag[1] = 0;
     flag[2] = 0;
+    for (int i = 0; i < kUq; i++) uq->seq[i] = -1;
     fence_mbar_init();
   }
   __syncthreads();
   pdl_launch();
 
   if (warp == kSProd) {
-    if ((threadIdx.x & 31) == 0) s_produce<NT>(a, sx, sw, info, full, empty, abort);
+    if ((threadIdx.x & 31) == 0) s_produce<NT>(a, sx, sw, info, full, empty, uq, abort);
   } else if (warp == kSNorm) {
     s_norm<NT>(a, sx, info, full, xrdy, rinv, abort);
   } else if (warp == kSEsc) {
-    s_escape<NT>(a, sx, info, xrdy, empty, corr, corr_full, corr_empty, abort);
+    s_escape<NT>(a, sx, info, xrdy, empty, corr, corr_full, corr_empty, uq, abort);
   } else {
-    s_consume<NT>(a, sx, sw, info, xrdy, empty, corr, corr_full, corr_empty, sph, red_v, red_i, flag, cbar, abort);
+    s_consume<NT>(a, sx, sw, info, xrdy, empty, corr, corr_full, corr_empty, sph, red_v, red_i, cbar, abort);
   }
   __syncthreads();
   // the last CTA to get here clears the site's counters, tickets and flags
@@ -918,12 +1050,12 @@ static int blocks_of(const w12_tensor& W) { return (int)((W.N / 16 + kRB - 1) / 
 
 size_t stream_state_ints(const StreamPhaseDesc* ph, int n) {
   size_t s = 1;
-  for (int i = 0; i < n; i++) s += 2 + 2 * (size_t)blocks_of(*ph[i].W);
+  for (int i = 0; i < n; i++) s += 2 + 10 * (size_t)blocks_of(*ph[i].W);
   return s;
 }
 
 size_t stream_state_ints_bound(int64_t n_max) {
-  return 1 + (size_t)kStreamMaxPhases * (2 + 2 * (size_t)((n_max / 16 + kRB - 1) / kRB));
+  return 1 + (size_t)kStreamMaxPhases * (2 + 10 * (size_t)((n_max / 16 + kRB - 1) / kRB));
 }
 
 struct SplitPlan {
@@ -1047,7 +1179,7 @@ int stream_launch(const StreamPhaseDesc* ph, int n, int M, const StreamWorkspace
     P.dep_fine = d.dep_fine;
     P.out_ss = d.out_ss;
     P.st = ws.state + st_off;
-    st_off += 2 + 2 * (size_t)P.NB;
+    st_off += 2 + 10 * (size_t)P.NB;
     P.part = ws.partial + part_off;
     part_off += (size_t)sp.nb_split * sp.S * 128 * MP;
     XMap xm;

@@ -31,7 +31,8 @@ struct StreamPhaseDesc {
   float norm_eps = 0.f;
   uint16_t* norm_out = nullptr;  // optional: the normalised activations, bf16 [M][K]
   // EPI_RESID: per row block b and token row m, the sum of squares of the
-  // block's bf16 outputs, out_ss[b * 128 + m] (feeds a later phase's norm)
+  // block's bf16 outputs, out_ss[b * 128 + m] (feeds a later phase's norm);
+  // room for 9 * NB * 128 floats (the strips' sums follow the blocks')
   float* out_ss = nullptr;
 };
 

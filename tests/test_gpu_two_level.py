@@ -64,7 +64,7 @@ def test_device_plane_equals_host_plane(M, rare, perm):
 def test_round_one_matches_the_oracle_view(M, mdl):
     shape, W, model = mdl
     ctx = 60
-    td = wl.draft(91, 0, 24, 6, 0.8, shape.V)
+    td = wl.draft(91, 0, 16, 6, 0.8, shape.V)
     tokens = oracle_copy_tokens(shape, W, 3, 0, ctx, td)
     req = oracle_request(shape, 3, 0, ctx, tokens, td.parents, cap=ctx + 80)
     low = oracle.forward(shape, oracle.View8Weights(W), [req])
@@ -96,7 +96,7 @@ def _extension(chain):
 def test_two_level_verification_matches_the_oracle(M, mdl):
     from speculative_decoding_tree_bit_gb300 import check, lib
     shape, W, model = mdl
-    for seed, (m, depth, ctx) in enumerate([(16, 6, 40), (32, 8, 90), (9, 4, 130)]):
+    for seed, (m, depth, ctx) in enumerate([(16, 6, 40), (12, 8, 90), (9, 4, 130)]):
         td = wl.draft(100 + seed, 0, m, depth, 0.8, shape.V)
         tokens = oracle_copy_tokens(shape, W, 3, 0, ctx, td)
         req = oracle_request(shape, 3, 0, ctx, tokens, td.parents, cap=ctx + 80)
