@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--timeline", action="store_true", help="print the per-kernel breakdown to stderr")
+    ap.add_argument("--fused", action="store_true",
+                    help="skinny steps: the linears between two attention kernels as one launch")
     ap.add_argument("--nvtx", action="store_true", help="wrap the timed steps in the NVTX range 'sdv_step'")
     ap.add_argument("--probe", default=None, metavar="N,K,M",
                     help="time the fused W12 linear alone on an N x K tensor with M rows")
@@ -360,6 +362,7 @@ def gpu_arm(args, rank, world, dist):
     if R == 1:
         M = spec.M
         model = Mdl.Model(shape, W, max_rows=M, max_requests=1, max_positions=ctx + M + 64)
+        model.set_fused(args.fused)
         kv = Mdl.KVCache(shape, ctx + M + 16).fill(args.seed, ctx)
         log(f"[rank {rank}] model built in {time.time() - t0:.1f}s, packed {model.packed_bytes / 1e9:.2f} GB")
         td = spec.drafts[0]
@@ -368,7 +371,7 @@ def gpu_arm(args, rank, world, dist):
             _, am = model.forward(tok, par, kv, logits=False)
             return am.cpu().numpy()
 
-        tokens = wl.copy_rule_tokens(td, am_fn)
+        tokens = wl.copy_rule_tokens(td, am_fn, full_tree=True)
         parents = np.asarray(td.parents, np.int32)
         tok_d = torch.from_numpy(tokens).to(dev)
         par_d = torch.from_numpy(parents).to(dev)
@@ -383,6 +386,7 @@ def gpu_arm(args, rank, world, dist):
         Mr = spec.M
         M = R * Mr
         model = Mdl.Model(shape, W, max_rows=M, max_requests=R, max_positions=ctx + Mr + 64)
+        model.set_fused(args.fused)
         table, n_pages = wl.page_tables(args.seed, spec.ctx, Mr, spec.page_size)
         kv = Mdl.PagedKVCache(shape, table, n_pages, spec.page_size).fill(args.seed, spec.ctx)
         log(f"[rank {rank}] model built in {time.time() - t0:.1f}s, packed {model.packed_bytes / 1e9:.2f} GB")
@@ -543,7 +547,7 @@ def gpu_arm(args, rank, world, dist):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "model": shape.name, "layers": shape.n_layers, "M": M,
                    "requests": R, "tc_min_rows": tc_rows,
-                   "attn_splits": attn_splits or "auto",
+                   "attn_splits": attn_splits or "auto", "schedule": "fused" if args.fused else "per-linear",
                    "max_depth": spec.max_depth, "ctx": ctx, "p_copy": spec.p, "accepted_len": acc_len,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (packed weights %.1f GB)" % (model.packed_bytes / 1e9)},
@@ -558,8 +562,8 @@ def gpu_arm(args, rank, world, dist):
                      "frac": achieved / peak if achieved else None, "traffic": traffic,
                      "kernel": ("k_w12_stream, the per-layer launches (O, gate/up, down, next q/k/v): algorithmic "
                                 "bytes per launch / mean event-timed launch" if dom_kind == "gemm_stream" else
-                                "k_w12_gemm_tc, gate/up launches (algorithmic bytes per launch / mean event-timed "
-                                "launch)"),
+                                "%s, gate/up launches (algorithmic bytes per launch / mean event-timed launch)" %
+                                ("k_w12_stream" if M <= 64 and M < tc_rows else "k_w12_gemm_tc")),
                      "algorithmic_bytes_per_launch": dom_bytes, "launch_ms": dom_ms,
                      "all_gemm_launches_gbs": all_gemm_gbs,
                      "peak_source": pk_src},

@@ -55,6 +55,38 @@ enum {
 const char* sd_last_error(void);
 const char* sd_version(void);
 
+/* Test hook for the device-side bounded waits: every wait of the library's
+ * kernels on an mbarrier or a device flag gives up after 2 s, records
+ * SD_ERR_TIMEOUT in the caller's status word and lets the kernel return, so
+ * that a stuck pipeline never hangs the GPU.  This launches one small kernel
+ * that waits, with those same helpers, on something nothing completes
+ * (which = 0: an mbarrier nobody arrives at, waited by two warps sharing an
+ * abort flag; which = 1: a device flag nobody sets, polled with acquire
+ * loads) for limit_ns nanoseconds (clamped to [1 us, 2 s]), then sets
+ * *status (device int32, caller-owned, not cleared here) to SD_ERR_TIMEOUT.
+ * Errors: SD_ERR_INVALID_ARG, SD_ERR_CUDA (launch). */
+int sd_debug_bounded_wait(int32_t* status, int64_t limit_ns, int32_t which, void* stream);
+
+/* Event log of the streamed W12 GEMM launches (diagnostics: where a launch
+ * of several GEMMs spends its time).  While a buffer is set (device memory,
+ * 16-byte aligned, zeroed by the caller), each streamed launch takes the
+ * next sd_stream_grid(M) * 64 records of 16 bytes, in launch order, until
+ * the buffer is full (later launches log nothing).  Records of CTA c:
+ * [c * 64, c * 64 + 32) from its producer, [c * 64 + 32, c * 64 + 64) from
+ * its consumers, unused ones left zero; each is {device clock in ns, tag},
+ * tag = kind | phase << 8 | row block << 16 | k-tile << 40 with kind 1
+ * producer start, 2 first weight tile of a segment issued, 3 its first
+ * activation tile issued (what it reads is complete), 4 the segment's first
+ * stage ready at the consumers, 5 the segment finished (k-tile field 1: the
+ * block's epilogue ran here, 0: a partial was left for another CTA), 6 the
+ * consumers done.  buf null or bytes 0 turns the log off.  Process-wide; not
+ * thread-safe against concurrent launches.  sd_stream_trace_launches: the
+ * launches logged since the buffer was set; sd_stream_grid: CTAs of a
+ * streamed launch of M rows (0 outside 1..64). */
+int sd_stream_set_trace(uint64_t* buf, int64_t bytes);
+int32_t sd_stream_trace_launches(void);
+int32_t sd_stream_grid(int32_t M);
+
 /* ---------------------------------------------------------------- W12 -- */
 /* [W12] Each bf16 weight is stored in 12 bits: sign, 7-bit mantissa and a
  * 4-bit code into a per-tensor table of the 15 most frequent exponents
@@ -153,6 +185,19 @@ size_t sd_w12_linear_workspace(int64_t N, int64_t K, int32_t M);
 int sd_w12_linear(const w12_tensor* W, const uint16_t* x, int32_t M, uint16_t* y, void* workspace,
                   size_t workspace_bytes, void* stream);
 
+/* The same linear on the weight-streaming kernel (the kernel of the fused
+ * schedule and of the 8-bit view of two-level verification), 1 <= M <= 64.
+ * plane8: null for the exact 12-bit weights, or W's nested 8-bit plane
+ * (w12_plane8_pack; N*K/4 u32, 16-byte aligned), in which case the call
+ * multiplies by the 8-bit view of W (each weight with its 4 low mantissa
+ * bits cleared, escapes likewise) while streaming 1 byte per weight.
+ * workspace: sd_w12_linear_stream_workspace(N, K, M) bytes, 256-byte
+ * aligned, no initialisation needed.  Errors: SD_ERR_INVALID_ARG,
+ * SD_ERR_UNSUPPORTED (shape, M), SD_ERR_WORKSPACE, SD_ERR_CUDA. */
+size_t sd_w12_linear_stream_workspace(int64_t N, int64_t K, int32_t M);
+int sd_w12_linear_stream(const w12_tensor* W, const uint32_t* plane8, const uint16_t* x, int32_t M, uint16_t* y,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
 /* The same linear for callers that cannot allocate device memory: a host
  * framework that owns all device memory through its own pool, a real-time
  * thread that must not take cudaMalloc's implicit synchronisation, a plug-in
@@ -161,9 +206,13 @@ int sd_w12_linear(const w12_tensor* W, const uint16_t* x, int32_t M, uint16_t* y
  * scratch lives in a static device array inside the library (about 9.5 MiB
  * that every GPU loading the library holds until the process exits), so the
  * call allocates nothing; the caller passes only W, x and y.
- * Limits: 1 <= M <= 64 and N <= 262144, else SD_ERR_UNSUPPORTED.
- * The first call on a device looks up the array's device address (with that
- * device current), so make that first call before any stream capture.
+ * Limits: 1 <= M <= 64 and N <= 262144, and M below the tensor-core
+ * threshold (sd_gemm_set_tc_min_rows: the static scratch serves the
+ * warp-level kernel only), else SD_ERR_UNSUPPORTED.  The launch takes the
+ * grid sd_w12_linear's warp-level path takes (up to 1216 CTAs x 8-row tiles).
+ * Each call looks up the array's address in the current context (a context
+ * made after cudaDeviceReset gets its own); inside a stream capture use
+ * cudaStreamCaptureModeRelaxed, which allows that lookup.
  * Every call on a device shares the one array: calls that can overlap on the
  * GPU (different streams without ordering between them) race and give wrong
  * results; serialise them. */
@@ -514,7 +563,7 @@ int sd_forward(sd_model* m, const int32_t* tree_tokens, const int32_t* parents, 
  * aligned): planes_host[4 l + 0..3] = layer l's qkv, o, gate_up, down, then
  * planes_host[4 n_layers] = the lm_head's; n = 4 n_layers + 1.
  * sd_forward_view8 is sd_forward over the view; it needs the streamed step
- * (M below the tensor-core threshold, sd_gemm_set_tc_min_rows) and the
+ * (M <= 64 and below the tensor-core threshold, sd_gemm_set_tc_min_rows) and the
  * registered planes, else SD_ERR_UNSUPPORTED.  The new K/V it writes to
  * slots ctx + node are the view's (an exact step rewrites them). */
 int sd_model_set_view8(sd_model* m, const uint32_t* const* planes_host, int32_t n);
@@ -559,6 +608,17 @@ int sd_model_final_hidden(sd_model* m, uint16_t* out, int32_t rows, void* stream
  * kernels directly every call (also the behaviour on the legacy default
  * stream and inside a caller's own stream capture). */
 int sd_model_set_graphs(sd_model* m, int32_t enable);
+
+/* Schedule of skinny steps (rows <= 64, below the tensor-core threshold):
+ * enable = 0 (the default) launches the warp-level W12 GEMM once per linear
+ * with an RMSNorm kernel before gate/up and before the next q/k/v;
+ * enable = 1 runs, on the weight-streaming kernel (sd_w12_linear_stream),
+ * the linears between two attention (or recurrence)
+ * kernels - O, gate/up, down and the next layer's q/k/v or the lm_head - as
+ * one launch of four dependent GEMMs with the RMSNorms folded in (each
+ * activation tile waits only for the blocks it reads).  Both give the same
+ * results up to the order of fp32 split-K sums; drops captured graphs. */
+int sd_model_set_fused(sd_model* m, int32_t enable);
 
 /* Kernel kinds reported by sd_model_timeline (SD_K_GEMM_STREAM: one
  * streamed launch of several GEMMs; its bytes are those of the GEMMs it

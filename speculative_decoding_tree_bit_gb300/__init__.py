@@ -68,6 +68,10 @@ P = ctypes.POINTER
 _SIGS = {
     "sd_last_error": (ctypes.c_char_p, []),
     "sd_version": (ctypes.c_char_p, []),
+    "sd_debug_bounded_wait": (ctypes.c_int, [vp, i64, i32, vp]),
+    "sd_stream_set_trace": (ctypes.c_int, [vp, i64]),
+    "sd_stream_trace_launches": (i32, []),
+    "sd_stream_grid": (i32, [i32]),
     "w12_words_count": (i64, [i64, i64]),
     "w12_pack_analyze": (ctypes.c_int, [vp, i64, i64, P(W12Meta), vp]),
     "w12_pack_encode": (ctypes.c_int, [vp, vp, P(W12Meta), vp, vp, vp, vp, vp]),
@@ -77,6 +81,8 @@ _SIGS = {
     "sd_w12_linear_workspace": (ctypes.c_size_t, [i64, i64, i32]),
     "sd_w12_linear": (ctypes.c_int, [P(W12Tensor), vp, i32, vp, vp, ctypes.c_size_t, vp]),
     "sd_w12_linear_static": (ctypes.c_int, [P(W12Tensor), vp, i32, vp, vp]),
+    "sd_w12_linear_stream_workspace": (ctypes.c_size_t, [i64, i64, i32]),
+    "sd_w12_linear_stream": (ctypes.c_int, [P(W12Tensor), vp, vp, i32, vp, vp, ctypes.c_size_t, vp]),
     "sd_gemm_set_tc_min_rows": (i32, [i32]),
     "sd_attn_set_splits": (i32, [i32]),
     "sd_tree_info": (ctypes.c_int, [vp, i32, i32, vp, vp, vp, vp, vp]),
@@ -105,6 +111,7 @@ _SIGS = {
     "sd_model_last_launches": (ctypes.c_int, [vp]),
     "sd_model_final_hidden": (ctypes.c_int, [vp, vp, i32, vp]),
     "sd_model_set_view8": (ctypes.c_int, [vp, vp, i32]),
+    "sd_model_set_fused": (ctypes.c_int, [vp, i32]),
     "sd_forward_view8": (ctypes.c_int, [vp, vp, vp, i32, P(KV), vp, vp, vp]),
     "w12_plane8_words_count": (i64, [i64, i64]),
     "w12_plane8_pack": (ctypes.c_int, [vp, vp, P(W12Meta), vp, vp]),

@@ -63,9 +63,57 @@ __global__ void k_tree_single(const int32_t* __restrict__ parents, int M, int ct
   }
 }
 
+// The bounded waits' give-up path, exercised on purpose: one CTA waits with
+// the library's own helpers on something nothing completes - an mbarrier
+// nobody arrives at (which = 0: two warps, the first to give up aborts the
+// other, as in the GEMM pipelines) or a device flag nobody sets (which = 1:
+// the acquire poll of the streamed GEMM's dependency waits) - and reports
+// SD_ERR_TIMEOUT in *status once limit_ns has passed.
+static __device__ int g_never_set;
+
+__global__ void k_debug_wait(int32_t* status, uint64_t limit_ns, int which) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  if (which == 0) {
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_or_abort(&bar, 0, &abort, limit_ns);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok && lane == 0) set_status(status, SD_ERR_TIMEOUT);
+  } else if (threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+      int v;
+      asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(&g_never_set) : "memory");
+      if (v != 0) break;
+      if (globaltimer() - t0 > limit_ns) {
+        set_status(status, SD_ERR_TIMEOUT);
+        break;
+      }
+    }
+  }
+}
+
 }  // namespace sdv
 
 using namespace sdv;
+
+extern "C" int sd_debug_bounded_wait(int32_t* status, int64_t limit_ns, int32_t which, void* stream) {
+  if (!status || (which != 0 && which != 1)) {
+    set_error("sd_debug_bounded_wait: bad argument");
+    return SD_ERR_INVALID_ARG;
+  }
+  const uint64_t lim = (uint64_t)std::min<int64_t>(std::max<int64_t>(limit_ns, 1000), (int64_t)kWaitLimitNs);
+  k_debug_wait<<<1, 64, 0, (cudaStream_t)stream>>>(status, lim, which);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SD_OK : cuda_fail(e, "k_debug_wait launch");
+}
 
 extern "C" const char* sd_last_error(void) { return g_last_error.c_str(); }
 extern "C" const char* sd_version(void) { return "sdv 0.1 (sm_103a)"; }

@@ -401,26 +401,11 @@ extern "C" int32_t sd_gemm_set_tc_min_rows(int32_t rows) {
 
 static size_t al256b(size_t x) { return (x + 255) & ~size_t(255); }
 
-// One streamed phase (M <= 128 below the tensor-core threshold): scratch
-// = the site's state ints, then the split partials.
-static size_t linear_stream_bytes(int64_t N, int64_t K, int M, size_t* state_ints, size_t* part_floats) {
-  w12_tensor t{};
-  t.N = N;
-  t.K = K;
-  StreamPhaseDesc d;
-  d.W = &t;
-  *state_ints = stream_state_ints(&d, 1);
-  *part_floats = stream_partial_floats(&d, 1, M);
-  return al256b(*state_ints * sizeof(int32_t)) + al256b(*part_floats * sizeof(float));
-}
-
 extern "C" size_t sd_w12_linear_workspace(int64_t N, int64_t K, int32_t M) {
+  (void)K;
   const int m = std::max(1, std::min<int>(M, 256));
   const size_t pf = gemm_partial_floats(m);
-  const size_t tc = al256b(pf * sizeof(float)) + (size_t)gemm_counters(N) * sizeof(int32_t) + 256;
-  size_t si = 0, sp = 0;
-  const size_t st = (m <= 128 && N > 0 && K > 0) ? linear_stream_bytes(N, K, m, &si, &sp) + 256 : 0;
-  return std::max(tc, st);
+  return al256b(pf * sizeof(float)) + (size_t)gemm_counters(N) * sizeof(int32_t) + 256;
 }
 
 extern "C" int sd_w12_linear(const w12_tensor* W, const uint16_t* x, int32_t M, uint16_t* y, void* workspace,
@@ -442,22 +427,6 @@ extern "C" int sd_w12_linear(const w12_tensor* W, const uint16_t* x, int32_t M, 
   e.epi = EPI_STORE;
   e.out = y;
   e.ldo = (int)W->N;
-  if (M <= 128 && !gemm_use_tc(M)) {
-    size_t si = 0, sp = 0;
-    linear_stream_bytes(W->N, W->K, M, &si, &sp);
-    StreamWorkspace ws;
-    ws.state = reinterpret_cast<int32_t*>(workspace);
-    ws.state_ints = si;
-    ws.partial = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + al256b(si * sizeof(int32_t)));
-    ws.partial_floats = sp;
-    SD_CK(cudaMemsetAsync(ws.state, 0, si * sizeof(int32_t), s));
-    StreamPhaseDesc d;
-    d.W = W;
-    d.x = x;
-    d.x_rows = M;
-    d.epi = e;
-    return stream_launch(&d, 1, M, ws, nullptr, s, false);
-  }
   GemmWorkspace ws;
   ws.partial = reinterpret_cast<float*>(workspace);
   ws.partial_floats = gemm_partial_floats(M);

@@ -7,11 +7,14 @@
 // -> greedy acceptance -> K/V compaction / state commit.
 // Every kernel is launched with programmatic dependent launch, so a GEMM's
 // producer streams its weights while the previous kernel is still finishing.
-// Up to 128 rows (and below the tensor-core threshold) the GEMMs between two
-// attention (or recurrence) kernels - O, gate/up, down and the next layer's
-// q/k/v (or the lm_head) - run as one streamed launch with the RMSNorms
-// folded into them (stream.cu); above it, one tcgen05 GEMM launch per
-// linear with RMSNorm kernels between them.
+// Each linear is one GEMM launch with RMSNorm kernels between them: the
+// warp-level kernel (gemm.cu) up to 64 rows below the tensor-core
+// threshold, the tcgen05 kernel (gemm_tc.cu) above.  The 8-bit view of
+// two-level verification streams its planes through the weight-streaming
+// kernel (stream.cu); with the fused schedule (sd_model_set_fused) the GEMMs
+// between two attention (or recurrence) kernels - O, gate/up, down and the
+// next layer's q/k/v (or the lm_head) - run as one launch of that kernel
+// with the RMSNorms folded into it.
 #include <algorithm>
 #include <cmath>
 #include <map>
@@ -63,10 +66,11 @@ struct sd_model {
   int n_sites = 0;
   float* stream_part = nullptr;
   size_t stream_part_floats = 0;
-  float* ss_h = nullptr;  // [H/128][9][128]: of h (O's output)
-  float* ss_x = nullptr;  // [H/128][9][128]: of x (down's output)
+  float* ss_h = nullptr;  // [H/128][128]: of h (O's output)
+  float* ss_x = nullptr;  // [H/128][128]: of x (down's output)
   // optional per-kernel timing
   bool timing = false;  // events around every kernel launch
+  bool fused = false;   // skinny steps: O..next q/k/v as one streamed launch
   std::vector<cudaEvent_t> events;  // 2 per entry
   std::vector<int32_t> t_kind;
   std::vector<double> t_bytes;
@@ -165,13 +169,16 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     launches++;                                         \
   } while (0)
 
-  // streamed launches (rows <= 128 below the tensor-core threshold): the
-  // GEMMs between two attention / recurrence kernels in one launch with the
-  // RMSNorms folded in; otherwise one GEMM launch per linear and RMSNorm
-  // kernels between them
-  const bool streamed = rows <= 128 && !gemm_use_tc(rows);
-  if (io.view8 && (!streamed || m->view8.size() != (size_t)4 * m->cfg.n_layers + 1)) {
-    set_error("model: the 8-bit view needs sd_model_set_view8 and a streamed step (rows <= 128, below the "
+  // one launch per linear with RMSNorm kernels between them: the warp-level
+  // kernel for skinny steps (rows <= 64 below the tensor-core threshold), the
+  // tcgen05 kernel above; the 8-bit view streams its planes through the
+  // weight-streaming kernel; fused (skinny steps): the GEMMs between two
+  // attention / recurrence kernels as one launch of that kernel with the
+  // RMSNorms folded in
+  const bool skinny = rows <= kStreamMaxRows && !gemm_use_tc(rows);
+  const bool fused = skinny && m->fused;
+  if (io.view8 && (!skinny || m->view8.size() != (size_t)4 * m->cfg.n_layers + 1)) {
+    set_error("model: the 8-bit view needs sd_model_set_view8 and a streamed step (rows <= 64, below the "
               "tensor-core threshold)");
     return SD_ERR_UNSUPPORTED;
   }
@@ -180,7 +187,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   };
   int site = 0;
   std::vector<StreamPhaseDesc> ph;
-  auto flush_stream = [&]() -> int {
+  auto flush_stream = [&](int kind) -> int {
     if (ph.empty()) return SD_OK;
     if (site >= m->n_sites) {
       set_error("model: more streamed launches than sites");
@@ -193,7 +200,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     ws.state_ints = m->site_ints;
     ws.partial = m->stream_part;
     ws.partial_floats = m->stream_part_floats;
-    if ((rc = tbegin(SD_K_GEMM_STREAM, bytes))) return rc;
+    if ((rc = tbegin(kind, bytes))) return rc;
     if ((rc = stream_launch(ph.data(), (int)ph.size(), rows, ws, m->status, s, pdl))) return rc;
     if ((rc = tend())) return rc;
     launches++;
@@ -201,7 +208,25 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     ph.clear();
     return SD_OK;
   };
-  auto gemm_one = [&](int kind, const w12_tensor& W, const uint16_t* x, const XMap* xm, const GemmEpilogue& e) -> int {
+  // one linear: the 8-bit view (plane) and the fused schedule's first q/k/v
+  // on the streaming kernel; else the warp-level kernel (skinny steps) or
+  // the tcgen05 kernel
+  auto gemm_one = [&](int kind, const w12_tensor& W, const uint16_t* x, const XMap* xm, const GemmEpilogue& e,
+                      const uint32_t* plane) -> int {
+    if (plane || fused) {
+      StreamPhaseDesc d;
+      d.W = &W;
+      d.view8 = plane;
+      d.x = x;
+      d.x_rows = m->max_rows;
+      d.epi = e;
+      ph = {d};
+      return flush_stream(kind);
+    }
+    if (!xm) {
+      set_error("model: no activation tensor map for a GEMM launch");
+      return SD_ERR_INVALID_ARG;
+    }
     if ((rc = tbegin(kind, gemm_bytes(W, rows, e.epi)))) return rc;
     if ((rc = gemm_launch(W, x, *xm, rows, e, m->gws, m->status, s, pdl))) return rc;
     if ((rc = tend())) return rc;
@@ -220,7 +245,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     if (e != cudaSuccess) return cuda_fail(e, "delay");
   }
   XMap *mx = nullptr, *ma = nullptr, *mc = nullptr;
-  if (!streamed) {
+  if (!fused && !io.view8) {
     if ((rc = get_map(m->map_xn, m->xn, m->max_rows, m->H, rows, &mx))) return rc;
     if ((rc = get_map(m->map_attn, m->attn, m->max_rows, (int64_t)m->Hq * m->hd, rows, &ma))) return rc;
     if ((rc = get_map(m->map_act, m->act, m->max_rows, m->I, rows, &mc))) return rc;
@@ -279,18 +304,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   el.amax_idx = m->amax_idx;
   el.ld_amax = m->max_rows;
 
-  if (streamed) {
-    StreamPhaseDesc d;
-    d.W = &m->layers[0].qkv;
-    d.view8 = v8(0, 0);
-    d.x = m->xn;
-    d.x_rows = m->max_rows;
-    d.epi = qkv_epi(0);
-    ph.push_back(d);
-    if ((rc = flush_stream())) return rc;
-  } else {
-    if ((rc = gemm_one(SD_K_GEMM_QKV, m->layers[0].qkv, m->xn, mx, qkv_epi(0)))) return rc;
-  }
+  if ((rc = gemm_one(SD_K_GEMM_QKV, m->layers[0].qkv, m->xn, mx, qkv_epi(0), v8(0, 0)))) return rc;
 
   for (int l = 0; l < m->cfg.n_layers; l++) {
     const sd_layer_weights& Lw = m->layers[l];
@@ -356,7 +370,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     ed.ldo = m->H;
     const bool last = l + 1 == m->cfg.n_layers;
     const uint16_t* gnext = last ? m->w.final_norm : m->layers[l + 1].attn_norm;
-    if (streamed) {
+    if (fused) {
       StreamPhaseDesc o, g, d, n;
       o.W = &Lw.o;
       o.view8 = v8(l, 1);
@@ -390,17 +404,17 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
       n.norm_eps = m->cfg.rms_eps;
       n.norm_out = last ? m->xn : nullptr;  // the final hidden state (the lm_head's input), kept for the tap
       ph = {o, g, d, n};
-      if ((rc = flush_stream())) return rc;
+      if ((rc = flush_stream(SD_K_GEMM_STREAM))) return rc;
     } else {
-      if ((rc = gemm_one(SD_K_GEMM_O, Lw.o, m->attn, ma, eo))) return rc;
+      if ((rc = gemm_one(SD_K_GEMM_O, Lw.o, m->attn, ma, eo, v8(l, 1)))) return rc;
       if ((rc = norm(m->h, Lw.mlp_norm, m->xn))) return rc;
-      if ((rc = gemm_one(SD_K_GEMM_GATE_UP, Lw.gate_up, m->xn, mx, eg))) return rc;
-      if ((rc = gemm_one(SD_K_GEMM_DOWN, Lw.down, m->act, mc, ed))) return rc;
+      if ((rc = gemm_one(SD_K_GEMM_GATE_UP, Lw.gate_up, m->xn, mx, eg, v8(l, 2)))) return rc;
+      if ((rc = gemm_one(SD_K_GEMM_DOWN, Lw.down, m->act, mc, ed, v8(l, 3)))) return rc;
       if ((rc = norm(m->x, gnext, m->xn))) return rc;
       if (last) {
-        if ((rc = gemm_one(SD_K_GEMM_LM_HEAD, m->w.lm_head, m->xn, mx, el))) return rc;
+        if ((rc = gemm_one(SD_K_GEMM_LM_HEAD, m->w.lm_head, m->xn, mx, el, v8(-1, 0)))) return rc;
       } else {
-        if ((rc = gemm_one(SD_K_GEMM_QKV, m->layers[l + 1].qkv, m->xn, mx, qkv_epi(l + 1)))) return rc;
+        if ((rc = gemm_one(SD_K_GEMM_QKV, m->layers[l + 1].qkv, m->xn, mx, qkv_epi(l + 1), v8(l + 1, 0)))) return rc;
       }
     }
   }
@@ -412,7 +426,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   ac.R = io.R;
   ac.amax_val = m->amax_val;
   ac.amax_idx = m->amax_idx;
-  ac.n_part = streamed ? stream_grid(rows) : gemm_grid(rows);
+  ac.n_part = (fused || io.view8) ? stream_grid(rows) : gemm_grid(rows);  // the lm_head's argmax partials
   ac.ld = m->max_rows;
   ac.req_ok = m->req_ok;
   ac.ctx_snap = m->ctx_snap;
@@ -609,9 +623,9 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
     for (int r = 1; r <= R; r++)
       units = std::max(units, (size_t)r * (attn_splits(r, m->Hkv, ch, c.max_positions) + 1));
   m->attn_units = units;
-  // streamed launches of a step: [q/k/v of layer 0], then per layer [O,
-  // gate/up, down, next q/k/v or lm_head]; scratch for the largest of them
-  // at any row count the model accepts
+  // streamed launches of a step: one per linear, or (fused) [q/k/v of
+  // layer 0], then per layer [O, gate/up, down, next q/k/v or lm_head];
+  // scratch for the largest of them at any row count the model accepts
   {
     size_t ints = 0, floats = 0;
     for (int l = -1; l < c.n_layers; l++) {
@@ -626,11 +640,12 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
         d[n++].W = l + 1 < c.n_layers ? &m->layers[l + 1].qkv : &m->w.lm_head;
       }
       ints = std::max(ints, stream_state_ints(d, n));
-      for (int rows = 1; rows <= std::min(MR, 128); rows *= 2) floats = std::max(floats, stream_partial_floats(d, n, rows));
-      floats = std::max(floats, stream_partial_floats(d, n, std::min(MR, 128)));
+      for (int rows = 1; rows <= std::min(MR, kStreamMaxRows); rows *= 2)
+        floats = std::max(floats, stream_partial_floats(d, n, rows));
+      floats = std::max(floats, stream_partial_floats(d, n, std::min(MR, kStreamMaxRows)));
     }
     m->site_ints = (ints + 63) & ~size_t(63);
-    m->n_sites = c.n_layers + 1;
+    m->n_sites = 4 * c.n_layers + 1;  // one per linear (the fused schedule uses n_layers + 1)
     m->stream_part_floats = std::max<size_t>(floats, 4);
   }
   struct Item {
@@ -670,8 +685,8 @@ extern "C" int sd_model_create(const sd_model_config* cfg, const sd_model_weight
       {(void**)&m->gws.counters, (size_t)gemm_counters(max_n) * 4},
       {(void**)&m->stream_state, (size_t)m->n_sites * m->site_ints * 4},
       {(void**)&m->stream_part, m->stream_part_floats * 4},
-      {(void**)&m->ss_h, (size_t)(m->H / 128) * 9 * 128 * 4},
-      {(void**)&m->ss_x, (size_t)(m->H / 128) * 9 * 128 * 4},
+      {(void**)&m->ss_h, (size_t)((m->H + 127) / 128) * 128 * 4},
+      {(void**)&m->ss_x, (size_t)((m->H + 127) / 128) * 128 * 4},
   };
   size_t total = 0;
   for (auto& it : items) total = al256(total + it.bytes);
@@ -871,6 +886,19 @@ extern "C" int sd_model_final_hidden(sd_model* m, uint16_t* out, int32_t rows, v
   }
   SD_CK(cudaMemcpyAsync(out, m->xn, (size_t)rows * m->H * sizeof(uint16_t), cudaMemcpyDeviceToDevice,
                         (cudaStream_t)stream));
+  return SD_OK;
+}
+
+extern "C" int sd_model_set_fused(sd_model* m, int32_t enable) {
+  if (!m) {
+    set_error("sd_model_set_fused: null model");
+    return SD_ERR_INVALID_ARG;
+  }
+  if ((enable != 0) != m->fused) {
+    for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);  // captured steps follow the old schedule
+    m->graphs.clear();
+  }
+  m->fused = enable != 0;
   return SD_OK;
 }
 

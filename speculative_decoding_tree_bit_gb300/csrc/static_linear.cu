@@ -15,45 +15,35 @@
 namespace sdv {
 
 // Limits of the static scratch (every GPU that loads the library holds it
-// until the process exits: 152 CTAs x 2 partial slots x 8 warps x 8 token
-// tiles x 128 floats = 9.5 MiB, plus one ticket per 128 output rows).
+// until the process exits: 1216 CTA-tiles x 2 partial slots x 8 warps x 8
+// rows x 128 floats = 9.5 MiB, plus one ticket per 128 output rows).  A
+// launch of G CTAs over NT token tiles of 8 needs G * NT <= 1216: 152 CTAs
+// at 64 rows, 304 at 32 rows or fewer, as sd_w12_linear uses on 152 SMs.
 constexpr int kStaticMaxRows = 64;           // M <= 64 (8 token tiles of 8)
-constexpr int kStaticMaxCtas = 152;          // CTAs per launch
+constexpr int kStaticCtaTiles = 1216;        // CTAs x token tiles per launch
 constexpr int64_t kStaticMaxN = 1 << 18;     // output rows
-constexpr size_t kStaticPartialFloats = (size_t)kStaticMaxCtas * 2 * 8 * (kStaticMaxRows / 8) * 128;
+constexpr size_t kStaticPartialFloats = (size_t)kStaticCtaTiles * 2 * 8 * 128;
 constexpr int kStaticCounters = (int)(kStaticMaxN / 128);
 
 static __device__ __align__(256) float g_static_partial[kStaticPartialFloats];
 static __device__ __align__(256) int32_t g_static_counters[kStaticCounters];
 
-// Device addresses of the arrays, looked up once per device (the names are
-// host-side stand-ins in host code, never valid device pointers).
+// Device addresses of the arrays in the current context (the names are
+// host-side stand-ins in host code, never valid device pointers).  Looked
+// up on every call, so that a new context (after cudaDeviceReset, or on
+// another device) gets its own addresses.
 struct StaticScratch {
   float* partial = nullptr;
   int32_t* counters = nullptr;
 };
 
 static int static_scratch(StaticScratch* out) {
-  static std::mutex mu;
-  static StaticScratch table[64];
-  static bool ready[64] = {false};
-  int dev = 0;
-  SD_CK(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= 64) {
-    set_error("sd_w12_linear_static: device index out of range");
-    return SD_ERR_UNSUPPORTED;
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ready[dev]) {
-    void* p = nullptr;
-    void* c = nullptr;
-    SD_CK(cudaGetSymbolAddress(&p, g_static_partial));
-    SD_CK(cudaGetSymbolAddress(&c, g_static_counters));
-    table[dev].partial = static_cast<float*>(p);
-    table[dev].counters = static_cast<int32_t*>(c);
-    ready[dev] = true;
-  }
-  *out = table[dev];
+  void* p = nullptr;
+  void* c = nullptr;
+  SD_CK(cudaGetSymbolAddress(&p, g_static_partial));
+  SD_CK(cudaGetSymbolAddress(&c, g_static_counters));
+  out->partial = static_cast<float*>(p);
+  out->counters = static_cast<int32_t*>(c);
   return SD_OK;
 }
 
@@ -75,6 +65,11 @@ extern "C" int sd_w12_linear_static(const w12_tensor* W, const uint16_t* x, int3
               "use sd_w12_linear with a workspace for larger calls");
     return SD_ERR_UNSUPPORTED;
   }
+  if (gemm_use_tc(M)) {
+    set_error("sd_w12_linear_static: M is at or above the tensor-core threshold (sd_gemm_set_tc_min_rows); "
+              "the static scratch serves the warp-level kernel only");
+    return SD_ERR_UNSUPPORTED;
+  }
   StaticScratch sc;
   int rc = static_scratch(&sc);
   if (rc) return rc;
@@ -94,6 +89,9 @@ extern "C" int sd_w12_linear_static(const w12_tensor* W, const uint16_t* x, int3
   e.epi = EPI_STORE;
   e.out = y;
   e.ldo = (int)W->N;
-  const int grid = gemm_grid(M) < kStaticMaxCtas ? gemm_grid(M) : kStaticMaxCtas;
+  // the grid sd_w12_linear's warp-level path takes, within the scratch
+  const int nt = pad_rows(M) / 8;
+  int grid = gemm_launch_grid(*W, M, EPI_STORE);
+  if (grid * nt > kStaticCtaTiles) grid = kStaticCtaTiles / nt;
   return gemm_launch(*W, x, xm, M, e, ws, nullptr, s, false, grid);
 }

@@ -6,6 +6,7 @@
 namespace sdv {
 
 constexpr int kStreamMaxPhases = 4;
+constexpr int kStreamMaxRows = 64;  // rows of one streamed launch (up to 8 token tiles)
 
 // One GEMM of a streamed launch, as the host describes it.
 struct StreamPhaseDesc {
@@ -32,7 +33,7 @@ struct StreamPhaseDesc {
   uint16_t* norm_out = nullptr;  // optional: the normalised activations, bf16 [M][K]
   // EPI_RESID: per row block b and token row m, the sum of squares of the
   // block's bf16 outputs, out_ss[b * 128 + m] (feeds a later phase's norm);
-  // room for 9 * NB * 128 floats (the strips' sums follow the blocks')
+  // room for NB * 128 floats
   float* out_ss = nullptr;
 };
 
@@ -57,13 +58,16 @@ size_t stream_partial_floats(const StreamPhaseDesc* ph, int n, int M);
 size_t stream_state_ints_bound(int64_t n_max);
 size_t stream_partial_floats_bound(int64_t n_max, int64_t k_max, int M);
 
-// y = epilogue(x W^T) for every phase, rows [0, M) (M <= 128), in one
-// persistent launch: each CTA takes (row block, k-chunk) units of each phase
-// in turn from a shared counter while its producer streams their weights;
-// activation tiles wait only for the blocks of earlier phases they read.
-// split_blocks (0: the default) caps how many row blocks of a phase are
-// split into k-chunks (the others are one unit each).
+// y = epilogue(x W^T) for every phase, rows [0, M) (M <= 64), in one
+// persistent launch: each CTA takes a contiguous share of each phase's
+// (row block, k-tile) tiles in turn (stream-K) while its producer streams
+// their weights; activation tiles wait only for the blocks of earlier
+// phases they read.
 int stream_launch(const StreamPhaseDesc* ph, int n, int M, const StreamWorkspace& ws, int32_t* status,
-                  cudaStream_t s, bool pdl, int split_blocks = 0);
+                  cudaStream_t s, bool pdl);
+
+// Event log of streamed launches (diagnostics; see sd_stream_set_trace).
+int stream_set_trace(uint64_t* buf, size_t bytes);
+int stream_trace_launches();
 
 }  // namespace sdv

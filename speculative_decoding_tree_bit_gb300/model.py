@@ -153,6 +153,21 @@ def linear(p: Packed, x: torch.Tensor, ws: Workspace | None = None, stream=None)
     return y
 
 
+def linear_stream(p: Packed, x: torch.Tensor, plane8: torch.Tensor | None = None, ws: Workspace | None = None,
+                  stream=None) -> torch.Tensor:
+    """y = bf16(x W^T) on the weight-streaming kernel (M <= 64); with plane8
+    (the tensor's nested 8-bit plane) the product with the 8-bit view."""
+    M = x.shape[0]
+    need = int(lib().sd_w12_linear_stream_workspace(p.N, p.K, M))
+    if ws is None or ws.nbytes < need:
+        ws = Workspace(need, x.device)
+    y = torch.empty((M, p.N), dtype=torch.int16, device=x.device)
+    t = p.struct()
+    check(lib().sd_w12_linear_stream(ctypes.byref(t), None if plane8 is None else plane8.data_ptr(), x.data_ptr(), M,
+                                     y.data_ptr(), ws.ptr, ws.nbytes, stream_ptr(stream)))
+    return y
+
+
 def set_tc_min_rows(rows: int) -> int:
     """Rows per launch from which the W12 GEMMs run on the tcgen05 kernel
     (process-wide; <= 0 restores the default).  Returns the value in force."""
@@ -260,6 +275,11 @@ class Model:
 
     def set_graphs(self, on: bool):
         check(lib().sd_model_set_graphs(self.handle, 1 if on else 0))
+
+    def set_fused(self, on: bool):
+        """Skinny steps: the linears between two attention kernels as one
+        launch with the RMSNorms folded in (on) or one launch per linear."""
+        check(lib().sd_model_set_fused(self.handle, 1 if on else 0))
 
     def set_timing(self, on: bool):
         """Event timing of every kernel launch of the following calls."""

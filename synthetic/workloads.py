@@ -236,20 +236,25 @@ def depths(parents) -> np.ndarray:
     return d
 
 
-def copy_rule_tokens(td: TreeDraft, argmax_fn, max_waves: int | None = None) -> np.ndarray:
+def copy_rule_tokens(td: TreeDraft, argmax_fn, max_waves: int | None = None, full_tree: bool = False) -> np.ndarray:
     """Draft tokens by depth waves: node i at depth d copies the target's
     argmax at its parent when its coin says so, else takes its random token.
     ``argmax_fn(tokens_sub, parents_sub)`` must return the target argmax of
     every node of the prefix-closed sub-tree it is given.  With
     ``max_waves`` only nodes down to that depth follow the rule (one target
-    pass per wave); deeper nodes take their random tokens."""
-    return copy_rule_tokens_batch([td], lambda subs: [argmax_fn(*subs[0])], max_waves)[0]
+    pass per wave); deeper nodes take their random tokens.  full_tree: every
+    wave passes the whole tree (nodes not yet decided hold their random
+    tokens; a node's argmax depends on its root path only), so each node
+    keeps the row it has in the final tree - for a target whose fp32
+    rounding, and so an argmax at a near tie, may depend on the row."""
+    return copy_rule_tokens_batch([td], lambda subs: [argmax_fn(*subs[0])], max_waves, full_tree)[0]
 
 
-def copy_rule_tokens_batch(tds, argmax_fn, max_waves: int | None = None) -> list:
+def copy_rule_tokens_batch(tds, argmax_fn, max_waves: int | None = None, full_tree: bool = False) -> list:
     """The copy rule for several requests at once: each wave makes one call
     ``argmax_fn([(tokens_sub, parents_sub) per request])`` returning the
-    target argmax of every node of each sub-tree."""
+    target argmax of every node of each sub-tree (of each whole tree with
+    full_tree)."""
     parents = [np.asarray(td.parents) for td in tds]
     d = [depths(p) for p in parents]
     tok = []
@@ -258,6 +263,9 @@ def copy_rule_tokens_batch(tds, argmax_fn, max_waves: int | None = None) -> list
         t[0] = td.root_token
         deep = np.nonzero(dd > (max_waves if max_waves is not None else p.size))[0]
         t[deep] = td.rand_tok[deep]
+        if full_tree:
+            later = np.nonzero(dd >= 1)[0]
+            t[later] = td.rand_tok[later]
         tok.append(t)
     last = max((int(dd.max()) for dd in d if dd.size), default=0)
     if max_waves is not None:
@@ -265,7 +273,7 @@ def copy_rule_tokens_batch(tds, argmax_fn, max_waves: int | None = None) -> list
     for wave in range(1, last + 1):
         subs, maps = [], []
         for p, dd, t in zip(parents, d, tok):
-            sub = np.nonzero(dd < wave)[0]
+            sub = np.arange(p.size) if full_tree else np.nonzero(dd < wave)[0]
             pos = {int(n): i for i, n in enumerate(sub)}
             psub = np.array([-1 if p[n] < 0 else pos[int(p[n])] for n in sub], dtype=np.int32)
             subs.append((t[sub].copy(), psub))

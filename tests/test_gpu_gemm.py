@@ -1,4 +1,6 @@
-"""Fused W12-decode GEMM (sd_w12_linear) vs the oracle's fp64 linear.
+"""Fused W12-decode GEMMs (sd_w12_linear: warp-level and tcgen05 kernels;
+sd_w12_linear_stream: the weight-streaming kernel, 12-bit weights or the
+nested 8-bit view) vs the oracle's fp64 linear.
 
 Tolerance: |gpu - oracle| <= 2e-2 + 1e-2 |oracle| per element (the rule for
 bf16 outputs with fp32 accumulation); in addition almost every element must
@@ -26,9 +28,9 @@ def _x(Mrows, K, seed=0):
     return synthetic.normal_bf16(synthetic.key(seed, 77 + Mrows), Mrows * K, 1.0).reshape(Mrows, K)
 
 
-def _check(M, W, x, rows=None, exact_frac=0.99, p=None):
+def _check(M, W, x, rows=None, exact_frac=0.99, p=None, lin=None):
     p = p or M.pack(M.to_device_u16(W))
-    y = M.linear(p, M.to_device_u16(x)).cpu().numpy().view(np.uint16)
+    y = (lin or M.linear)(p, M.to_device_u16(x)).cpu().numpy().view(np.uint16)
     if rows is not None:
         W, y = W[rows], y[:, rows]
     ref = oracle.linear(x, W)
@@ -145,3 +147,63 @@ def test_tc_repeat_calls_are_deterministic(tc_all):
     ws.buf.fill_(0xFF)
     b = tc_all.linear(p, x, ws)
     assert torch.equal(a, b)
+
+
+# ------------------------------------ weight-streaming kernel (M <= 64) --
+
+@pytest.mark.parametrize("Mrows", [1, 5, 8, 13, 16, 17, 32, 48, 64])
+def test_stream_tiny_shape_row_counts(M, Mrows):
+    t = wl.tiny()
+    _check(M, t.W1, _x(Mrows, 1024), lin=M.linear_stream)
+
+
+@pytest.mark.parametrize("N,K,Mrows", [(16, 64, 8), (48, 192, 16), (4000, 512, 8), (512, 512, 8), (1024, 4096, 16),
+                                       (144, 1088, 3), (4000, 512, 64)])
+def test_stream_ragged_shapes(M, N, K, Mrows):
+    W = synthetic.normal_bf16(synthetic.key(2, N * 7 + K), N * K, 0.02).reshape(N, K)
+    _check(M, W, _x(Mrows, K, 1), lin=M.linear_stream)
+
+
+def test_stream_escapes_and_general_table(M):
+    t = wl.tiny()
+    p = _check(M, t.Wlm, _x(8, 1024, 2), lin=M.linear_stream)
+    assert p.meta.affine == 1 and p.n_escapes >= 4194
+    rng = np.random.default_rng(5)
+    exps = np.array([110, 112, 114, 116, 118, 120, 121, 122, 123, 124, 100, 102, 104, 106, 108, 90], np.uint32)
+    e = exps[rng.integers(0, exps.size, size=256 * 512)]
+    W = ((rng.integers(0, 2, size=e.size).astype(np.uint32) << 15) | (e << 7)
+         | rng.integers(0, 128, size=e.size).astype(np.uint32)).astype(np.uint16).reshape(256, 512)
+    p = _check(M, W, _x(16, 512, 3), lin=M.linear_stream)
+    assert p.meta.affine == 0 and p.n_escapes > 0
+
+
+@pytest.mark.parametrize("name,Mrows", [("wq", 16), ("w_down", 16), ("lm", 16), ("lm", 64)])
+def test_stream_full_size_8b(M, name, Mrows):
+    sh = wl.SHAPES["8b"]
+    w = wl.SyntheticWeights(sh, 0)
+    W = w.lm_head() if name == "lm" else w.layer(0, name)
+    rows = np.sort(np.random.default_rng(0).choice(W.shape[0], 1024, replace=False))
+    _check(M, W, _x(Mrows, W.shape[1], 4), rows=rows, lin=M.linear_stream)
+
+
+@pytest.mark.parametrize("Mrows", [1, 16, 40, 64])
+def test_stream_view8_matches_the_oracle_view(M, Mrows):
+    """Streaming the nested 8-bit plane multiplies by the 8-bit view of W
+    (oracle.w12_view8), escapes included."""
+    t = wl.tiny()
+    W = t.Wlm
+    p = M.pack(M.to_device_u16(W), view8=True)
+    x = _x(Mrows, W.shape[1], 6)
+    y = M.linear_stream(p, M.to_device_u16(x), p.plane8).cpu().numpy().view(np.uint16)
+    ref = oracle.linear(x, oracle.w12_view8(W))
+    got = oracle.bf16_to_f64(y)
+    assert np.all(np.abs(got - ref) <= ATOL + RTOL * np.abs(ref))
+    assert np.mean(oracle.round_bf16(ref) == y) >= 0.99
+
+
+def test_stream_rejects_rows_beyond_64(M):
+    t = wl.tiny()
+    p = M.pack(M.to_device_u16(t.W1))
+    from speculative_decoding_tree_bit_gb300 import SdvError
+    with pytest.raises(SdvError):
+        M.linear_stream(p, M.to_device_u16(_x(65, 1024)))

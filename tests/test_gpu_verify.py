@@ -101,6 +101,21 @@ def test_tree_verify_on_tensor_core_gemms(M, dec):
         M.set_tc_min_rows(0)
 
 
+def test_tree_verify_on_the_fused_schedule(M, dec):
+    """The linears between two attention (or recurrence) kernels as one
+    launch of four dependent GEMMs with the RMSNorms folded in: trees of 1,
+    16 and 64 nodes, and a batch of paged requests."""
+    shape, W, model = dec
+    model.set_fused(True)
+    try:
+        _verify_case(M, shape, W, model, wl.draft(11, 0, 16, 8, 0.8, shape.V), 37)
+        _verify_case(M, shape, W, model, wl.draft(12, 0, 64, 10, 0.7, shape.V), 130)
+        assert _verify_case(M, shape, W, model, wl.draft(13, 0, 1, 1, 0.7, shape.V), 300) == 0
+        test_batched_paged_equals_oracle(M, dec)
+    finally:
+        model.set_fused(False)
+
+
 @pytest.mark.parametrize("splits", [1, 3, 64])
 def test_tree_verify_with_fixed_attention_splits(M, dec, splits):
     """One prefix split (no merge across CTAs), an odd count whose last
@@ -218,12 +233,22 @@ def test_graph_capture_and_replay_match_direct_launches(M, dec):
             assert torch.equal(r[k], results[0][k]), k
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("n", [5, 16, 64])
-def test_repeated_steps_give_identical_bits(M, dec, n):
-    """The streamed GEMMs hand units out dynamically (which CTA computes what
-    changes from run to run) but sum split blocks in chunk order: every run
-    gives the same bits."""
+def test_repeated_steps_give_identical_bits(M, dec, n, fused):
+    """The streamed GEMMs' split row blocks are finished by whichever
+    contributor arrives last (it changes from run to run), which sums the
+    partials in CTA order: every run gives the same bits, on both
+    schedules."""
     shape, W, model = dec
+    model.set_fused(fused)
+    try:
+        _repeat(M, shape, W, model, n)
+    finally:
+        model.set_fused(False)
+
+
+def _repeat(M, shape, W, model, n):
     ctx = 45
     td = wl.draft(40 + n, 0, n, 6, 0.8, shape.V)
     tok = np.random.default_rng(n).integers(0, shape.V, n).astype(np.int32)

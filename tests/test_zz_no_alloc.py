@@ -15,7 +15,7 @@ import torch
 import oracle
 import synthetic
 from synthetic import workloads as wl
-from helpers import ATOL, RTOL
+from helpers import ATOL, RTOL, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -36,6 +36,42 @@ def test_static_linear_matches_workspace_linear_twice():
             got = y.cpu().numpy().view(np.uint16)
             a, b = oracle.bf16_to_f64(got), oracle.bf16_to_f64(ref)
             assert np.all(np.abs(a - b) <= ATOL + RTOL * np.abs(b))
+
+
+@pytest.mark.parametrize("Mrows", [1, 5, 33, 64])
+def test_static_linear_matches_the_oracle(Mrows):
+    """Element by element against oracle.linear (fp64 sums of the decoded
+    weights), for escapes included: rare exponents are forced into W."""
+    from speculative_decoding_tree_bit_gb300 import check, lib, stream_ptr
+    from speculative_decoding_tree_bit_gb300 import model as M
+    N, K = 384, 1536
+    W = synthetic.normal_bf16(synthetic.key(61, Mrows), N * K, 0.02).reshape(N, K)
+    synthetic.force_rare_exponents(synthetic.key(62, Mrows), W, 30)
+    p = M.pack(M.to_device_u16(W))
+    assert p.meta.n_escapes > 0
+    st = p.struct()
+    x = synthetic.normal_bf16(synthetic.key(63, Mrows), Mrows * K, 1.0).reshape(Mrows, K)
+    y = torch.empty((Mrows, N), dtype=torch.int16, device="cuda")
+    check(lib().sd_w12_linear_static(ctypes.byref(st), M.to_device_u16(x).data_ptr(), Mrows, y.data_ptr(),
+                                     stream_ptr()))
+    torch.cuda.synchronize()
+    assert_close(y.cpu().numpy().view(np.uint16), oracle.linear(x, W))
+
+
+def test_static_linear_refuses_the_tensor_core_range():
+    from speculative_decoding_tree_bit_gb300 import lib
+    from speculative_decoding_tree_bit_gb300 import model as M
+    t = wl.tiny()
+    p = M.pack(M.to_device_u16(t.W1))
+    st = p.struct()
+    x = torch.zeros((16, t.W1.shape[1]), dtype=torch.int16, device="cuda")
+    y = torch.empty((16, t.W1.shape[0]), dtype=torch.int16, device="cuda")
+    assert M.set_tc_min_rows(16) == 16
+    try:
+        assert lib().sd_w12_linear_static(ctypes.byref(st), x.data_ptr(), 16, y.data_ptr(), None) == 2
+        assert b"tensor-core threshold" in lib().sd_last_error()
+    finally:
+        M.set_tc_min_rows(0)
 
 
 def test_static_linear_rejects_sizes_beyond_its_scratch():
