@@ -563,7 +563,8 @@ def gpu_arm(args, rank, world, dist):
                      "kernel": ("k_w12_stream, the per-layer launches (O, gate/up, down, next q/k/v): algorithmic "
                                 "bytes per launch / mean event-timed launch" if dom_kind == "gemm_stream" else
                                 "%s, gate/up launches (algorithmic bytes per launch / mean event-timed launch)" %
-                                ("k_w12_stream" if M <= 64 and M < tc_rows else "k_w12_gemm_tc")),
+                                ("k_w12_stream" if args.fused else "k_w12_gemm") if M <= 64 and M < tc_rows else
+                                "k_w12_gemm_tc"),
                      "algorithmic_bytes_per_launch": dom_bytes, "launch_ms": dom_ms,
                      "all_gemm_launches_gbs": all_gemm_gbs,
                      "peak_source": pk_src},

@@ -84,6 +84,15 @@ int sd_debug_bounded_wait(int32_t* status, int64_t limit_ns, int32_t which, void
  * launches logged since the buffer was set; sd_stream_grid: CTAs of a
  * streamed launch of M rows (0 outside 1..64). */
 int sd_stream_set_trace(uint64_t* buf, int64_t bytes);
+
+/* Device-clock stamps of the verify step's attention launches (diagnostics):
+ * while a buffer is set (device memory, zeroed by the caller), each launch
+ * takes the next 4 x grid u64 of it in launch order until it is full: for
+ * CTA c (x fastest, then y, z of the launch grid) at [i * grid + c] the time
+ * in ns after its wait for the previous kernel (i = 0), after its keys
+ * (1), once its split group is ready to merge (2), at its end (3).  buf
+ * null or bytes 0 turns the log off; process-wide. */
+int sd_attn_set_trace(uint64_t* buf, int64_t bytes);
 int32_t sd_stream_trace_launches(void);
 int32_t sd_stream_grid(int32_t M);
 

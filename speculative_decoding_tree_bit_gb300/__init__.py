@@ -70,6 +70,7 @@ _SIGS = {
     "sd_version": (ctypes.c_char_p, []),
     "sd_debug_bounded_wait": (ctypes.c_int, [vp, i64, i32, vp]),
     "sd_stream_set_trace": (ctypes.c_int, [vp, i64]),
+    "sd_attn_set_trace": (ctypes.c_int, [vp, i64]),
     "sd_stream_trace_launches": (i32, []),
     "sd_stream_grid": (i32, [i32]),
     "w12_words_count": (i64, [i64, i64]),

@@ -10,6 +10,8 @@
 // the target scores all tree nodes in one pass; each node must see exactly
 // its root path, and a recurrent state has to follow each root path.
 // "(3) Two-Level Verification": only the exact verification accepts tokens.
+#include <mutex>
+
 #include "layers.cuh"
 
 namespace sdv {
@@ -187,6 +189,14 @@ cudaError_t launch_rmsnorm(const uint16_t* src, const uint16_t* gamma, int rows,
 // 1/P share of the rows; otherwise the last split to finish merges them all.
 // The group counters return to zero for the next call.
 
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32: a few ulp,
+// subnormal results flushed to zero); softmax weights of the main loop only
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 constexpr int kAttnTile = 64;
 constexpr int kAttnStages = 2;
 constexpr int kAttnSmem = kAttnStages * 2 * kAttnTile * 128 * 2;  // K and V tiles
@@ -210,7 +220,7 @@ struct AttnKernelArgs {
 // 64-key tile, so that all four warps work; a pair merges its two
 // online-softmax states in shared memory before the split's partial.
 template <int KS>
-__global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
+__global__ void __launch_bounds__(128, 2) k_attn(AttnKernelArgs ka) {
   constexpr int kRowTiles = 4 / KS;       // 16-row tiles per chunk
   constexpr int kChunkRows = 16 * kRowTiles;
   constexpr int kNT = 8 / KS;             // 8-key n-tiles of a warp per 64-key tile
@@ -310,10 +320,27 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
   cp_async_commit();
   pdl_wait();
   stamp(0);
+  // everything the split reads from earlier kernels, requested at once: the
+  // context and the request flag (tree kernel), the rows' ancestor masks,
+  // the query fragments (q/k/v GEMM)
+  const int ctx_now = a.ctx[r], ok_now = a.req_ok[r];
+  const uint64_t anc0 = v0 ? a.anc[node0 + n0] : 0ull, anc1 = v1 ? a.anc[node0 + n1] : 0ull;
+  uint32_t qa[8][4];
   {
-    const int ctx = a.ctx[r];
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q + ((int64_t)(node0 + n0) * a.hq + qh0) * 128);
+    const uint32_t* q1 = reinterpret_cast<const uint32_t*>(a.q + ((int64_t)(node0 + n1) * a.hq + qh1) * 128);
+#pragma unroll
+    for (int kk = 0; kk < 8; kk++) {
+      qa[kk][0] = v0 ? q0[(16 * kk + 2 * q) / 2] : 0u;
+      qa[kk][1] = v1 ? q1[(16 * kk + 2 * q) / 2] : 0u;
+      qa[kk][2] = v0 ? q0[(16 * kk + 8 + 2 * q) / 2] : 0u;
+      qa[kk][3] = v1 ? q1[(16 * kk + 8 + 2 * q) / 2] : 0u;
+    }
+  }
+  {
+    const int ctx = ctx_now;
     int lo = 0, hi = 0;
-    if (!a.req_ok[r]) {
+    if (!ok_now) {
       lo = hi = 0;
     } else if (tree) {
       lo = ctx;
@@ -332,21 +359,8 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
       cp_async_commit();
     }
   }
-  const uint64_t anc0 = v0 ? a.anc[node0 + n0] : 0ull, anc1 = v1 ? a.anc[node0 + n1] : 0ull;
   const int ntiles = (k1 - k0 + kAttnTile - 1) / kAttnTile;
 
-  uint32_t qa[8][4];
-  {
-    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q + ((int64_t)(node0 + n0) * a.hq + qh0) * 128);
-    const uint32_t* q1 = reinterpret_cast<const uint32_t*>(a.q + ((int64_t)(node0 + n1) * a.hq + qh1) * 128);
-#pragma unroll
-    for (int kk = 0; kk < 8; kk++) {
-      qa[kk][0] = v0 ? q0[(16 * kk + 2 * q) / 2] : 0u;
-      qa[kk][1] = v1 ? q1[(16 * kk + 2 * q) / 2] : 0u;
-      qa[kk][2] = v0 ? q0[(16 * kk + 8 + 2 * q) / 2] : 0u;
-      qa[kk][3] = v1 ? q1[(16 * kk + 8 + 2 * q) / 2] : 0u;
-    }
-  }
   float o[16][4];
 #pragma unroll
   for (int i = 0; i < 16; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -397,7 +411,7 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
         mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
         const float mn = fmaxf(mrow[rr], mx[rr]);
         ms[rr] = mn == -INFINITY ? 0.f : mn;
-        alpha[rr] = exp2f(mrow[rr] - ms[rr]);
+        alpha[rr] = ex2_fast(mrow[rr] - ms[rr]);
         mrow[rr] = mn;
       }
 #pragma unroll
@@ -405,7 +419,7 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
 #pragma unroll
         for (int e = 0; e < 4; e++) {
           const int rr = e >> 1;
-          s[nt][e] = exp2f(s[nt][e] - ms[rr]);
+          s[nt][e] = ex2_fast(s[nt][e] - ms[rr]);
           sum[rr] += s[nt][e];
         }
 #pragma unroll
@@ -655,8 +669,23 @@ __global__ void __launch_bounds__(128, 3) k_attn(AttnKernelArgs ka) {
   stamp(3);
 }
 
-cudaError_t launch_attention(const AttnArgs& a, int rows_total, cudaStream_t s, bool pdl) {
+// Device-clock stamps of attention launches (diagnostics; sd_attn_set_trace):
+// each launch while a buffer is set takes the next 4 x grid stamps.
+static std::mutex g_attn_trace_mu;
+static uint64_t* g_attn_trace = nullptr;
+static size_t g_attn_trace_cap = 0, g_attn_trace_used = 0;
+
+int attn_set_trace(uint64_t* buf, size_t n) {
+  std::lock_guard<std::mutex> lock(g_attn_trace_mu);
+  g_attn_trace = buf;
+  g_attn_trace_cap = buf ? n : 0;
+  g_attn_trace_used = 0;
+  return SD_OK;
+}
+
+cudaError_t launch_attention(const AttnArgs& a_in, int rows_total, cudaStream_t s, bool pdl) {
   (void)rows_total;
+  AttnArgs a = a_in;
   static bool attr = false;
   static int per_sm[2] = {-1, -1};
   if (!attr) {
@@ -674,6 +703,13 @@ cudaError_t launch_attention(const AttnArgs& a, int rows_total, cudaStream_t s, 
   const int ks = attn_key_split(cm);
   const int chunks = attn_chunks(cm);
   const int64_t grid = (int64_t)(a.splits + 1) * a.hkv * chunks * a.R;
+  {
+    std::lock_guard<std::mutex> lock(g_attn_trace_mu);
+    if (g_attn_trace && g_attn_trace_used + 4 * (size_t)grid <= g_attn_trace_cap) {
+      a.trace = g_attn_trace + g_attn_trace_used;
+      g_attn_trace_used += 4 * (size_t)grid;
+    }
+  }
   const AttnKernelArgs ka{a, rpg, chunks, grid <= (int64_t)per_sm[ks - 1] * num_sms() ? 1 : 0};
   return launch(ks == 2 ? k_attn<2> : k_attn<1>, dim3(a.splits + 1, a.hkv * chunks, a.R), dim3(128), kAttnSmem, s,
                 pdl, ka);
@@ -938,3 +974,11 @@ __global__ void k_delay(uint64_t ns) {
 cudaError_t launch_delay(uint64_t ns, cudaStream_t s) { return launch(k_delay, dim3(1), dim3(1), 0, s, false, ns); }
 
 }  // namespace sdv
+
+extern "C" int sd_attn_set_trace(uint64_t* buf, int64_t bytes) {
+  if (bytes < 0) {
+    sdv::set_error("sd_attn_set_trace: bad argument");
+    return SD_ERR_INVALID_ARG;
+  }
+  return sdv::attn_set_trace(bytes > 0 ? buf : nullptr, (size_t)bytes / 8);
+}
