@@ -55,27 +55,31 @@ def row_errors(gpu_bits, ref):
     return np.linalg.norm(got - ref, axis=-1) / np.maximum(np.linalg.norm(ref, axis=-1), 1e-30)
 
 
-def assert_argmax(gpu_am, ref_am, margin, ref_logits=None):
+def assert_argmax(gpu_am, ref_am, margin, tap_am=None):
     """argmax must equal the oracle's at every position whose oracle top-2
-    margin (fp64 logits) is at least MARGIN.  With ``ref_logits`` (end-to-end
-    comparisons through several layers, where the bf16 rounding points carry
-    fp32-vs-fp64 differences forward; see test_oracle_sensitivity.py) a
-    position may also differ when the two tokens' oracle logits are within
-    the logit tolerance of each other; such positions must be few (at most
-    one, or 1% of the rows).  Returns the mask of positions that differ."""
+    margin (fp64 logits) is at least MARGIN.
+
+    End to end through several layers the two sides' bf16 rounding points
+    carry fp32-vs-fp64 differences forward, so the final hidden states
+    differ in a few bf16 units (within the logit tolerance; the oracle's own
+    fp32 twin shows the same, test_oracle_sensitivity.py).  ``tap_am`` is the
+    oracle's fp64 lm_head + argmax over the GPU step's own final hidden state
+    (assert_final_hidden, which holds the strict rule).  A position at
+    margin >= MARGIN may differ only where tap_am shows that the GPU's own
+    hidden state selects the GPU's token: the difference arose upstream of
+    the lm_head and argmax, never in them.  Such positions must be few (at
+    most one, or 1% of the rows).  Returns the mask of positions that
+    differ."""
     gpu_am, ref_am, margin = np.asarray(gpu_am), np.asarray(ref_am), np.asarray(margin)
     diff = gpu_am != ref_am
-    bad = []
-    tol_flips = []
+    bad, upstream = [], []
     for i in np.nonzero(diff & (margin >= MARGIN))[0]:
-        if ref_logits is not None:
-            top, alt = ref_logits[i, ref_am[i]], ref_logits[i, gpu_am[i]]
-            if top - alt <= ATOL + RTOL * abs(top):
-                tol_flips.append((int(i), float(margin[i]), float(top - alt)))
-                continue
+        if tap_am is not None and int(np.asarray(tap_am)[i]) == int(gpu_am[i]):
+            upstream.append((int(i), float(margin[i])))
+            continue
         bad.append((int(i), int(gpu_am[i]), int(ref_am[i]), float(margin[i])))
     assert not bad, bad
-    assert len(tol_flips) <= max(1, gpu_am.size // 100), tol_flips
+    assert len(upstream) <= max(1, gpu_am.size // 100), upstream
     return diff
 
 
@@ -211,3 +215,4 @@ def assert_final_hidden(model, o, lm_head, rows):
     am, margin = oracle.argmax_margin(lg)
     assert_close(o["logits"].cpu().numpy(), lg)
     assert_argmax(o["argmax"].cpu().numpy(), am, margin)
+    return am

@@ -67,9 +67,9 @@ def _single(M, shape_name, m, max_depth, ctx, p, waves, seed=0):
         floor = float(np.linalg.norm(twin.logits - out.logits))
         rel = assert_global_close(_np(o["logits"]), out.logits, floor=floor)
         print(f"{shape_name}: logits relative error {rel:.2e} (largest row {row_errors(_np(o['logits']), out.logits).max():.2e})")
-        assert_final_hidden(model, o, W.lm_head(), m)
+        tap = assert_final_hidden(model, o, W.lm_head(), m)
         am = _np(o["argmax"])
-        assert_argmax(am, out.argmax, out.margin, out.logits)
+        assert_argmax(am, out.argmax, out.margin, tap_am=tap)
         path = assert_accept(tokens, td.parents, am, int(o["accepted_len"][0]), _np(o["accepted_tokens"]),
                              int(o["bonus"][0]), out.argmax)
         L = int(o["accepted_len"][0])
@@ -114,15 +114,11 @@ def test_batched_8b_dims_two_layers_r32_paged(M):
                                logits=True)
         torch.cuda.synchronize()
         assert model.status() == 0
-        # the model's own amplification of fp32 rounding: the oracle's fp32
-        # twin (same steps, fp32 GEMM sums) deviates from it by this much
-        twin = oracle.forward(shape, W, [req], gemm=oracle.linear_f32)
-        floor = float(np.linalg.norm(twin.logits - out.logits))
-        rel = assert_global_close(_np(o["logits"]), out.logits, floor=floor)
+        rel = assert_global_close(_np(o["logits"]), out.logits)
         print(f"batched: logits relative error {rel:.2e} (largest row {row_errors(_np(o['logits']), out.logits).max():.2e})")
-        assert_final_hidden(model, o, W.lm_head(), int(cu[-1]))
+        tap = assert_final_hidden(model, o, W.lm_head(), int(cu[-1]))
         am = _np(o["argmax"])
-        assert_argmax(am, out.argmax, out.margin, out.logits)
+        assert_argmax(am, out.argmax, out.margin, tap_am=tap)
         for r in range(R):
             a, b = cu[r], cu[r + 1]
             path = assert_accept(toks[r], wk.drafts[r].parents, am[a:b], int(o["accepted_len"][r]),

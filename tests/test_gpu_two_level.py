@@ -19,7 +19,8 @@ import torch
 import oracle
 import synthetic
 from synthetic import workloads as wl
-from helpers import (assert_accept, assert_argmax, assert_close, oracle_copy_tokens, oracle_request)
+from helpers import (assert_accept, assert_argmax, assert_close, assert_final_hidden, oracle_copy_tokens,
+                     oracle_request)
 
 pytestmark = pytest.mark.gpu
 
@@ -74,15 +75,24 @@ def test_round_one_matches_the_oracle_view(M, mdl):
     torch.cuda.synchronize()
     assert model.status() == 0 and int(kv.ctx_len[0]) == ctx  # nothing committed
     assert_close(_np(lg), low.logits)
-    assert_argmax(_np(am), low.argmax, low.margin, low.logits)
     # the lm_head over the step's own final hidden state, through the view
-    xf = model.final_hidden(len(tokens)).cpu().numpy().view(np.uint16)
-    lg_h = oracle.linear(xf, oracle.w12_view8(W.lm_head()))
-    am_h, margin_h = oracle.argmax_margin(lg_h)
-    assert_close(_np(lg), lg_h)
-    assert_argmax(_np(am), am_h, margin_h)
+    am_h = _view8_tap(model, W, len(tokens), lg, am)
+    assert_argmax(_np(am), low.argmax, low.margin, tap_am=am_h)
     # the view really differs from the exact weights (else the test shows nothing)
     assert np.abs(low.logits - exact.logits).max() > 1e-3
+
+
+def _view8_tap(model, W, rows, lg, am):
+    """The oracle's lm_head (through the 8-bit view) over the step's own
+    final hidden state: element-wise logits and the strict argmax rule;
+    returns that argmax."""
+    xf = model.final_hidden(rows).cpu().numpy().view(np.uint16)
+    lg_h = oracle.linear(xf, oracle.w12_view8(W.lm_head()))
+    am_h, margin_h = oracle.argmax_margin(lg_h)
+    if lg is not None:
+        assert_close(_np(lg), lg_h)
+    assert_argmax(_np(am), am_h, margin_h)
+    return am_h
 
 
 def _extension(chain):
@@ -107,7 +117,7 @@ def test_two_level_verification_matches_the_oracle(M, mdl):
         torch.cuda.synchronize()
         assert int(kv.ctx_len[0]) == ctx
         low = oracle.forward(shape, oracle.View8Weights(W), [req])
-        assert_argmax(_np(am), low.argmax, low.margin, low.logits)
+        assert_argmax(_np(am), low.argmax, low.margin, tap_am=_view8_tap(model, W, m, None, am))
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, dtype=np.int32))).cuda()
         tok_d, par_d = dev(tokens), dev(td.parents)
         L, acc, bonus, st = (torch.zeros(n, dtype=torch.int32, device="cuda") for n in (1, m, 1, 1))
@@ -127,8 +137,9 @@ def test_two_level_verification_matches_the_oracle(M, mdl):
         assert model.status() == 0
         exact = oracle.forward(shape, W, [oracle_request(shape, 3, 0, ctx, tok2, par2, cap=ctx + 80)])
         assert_close(_np(o["logits"]), exact.logits)
+        tap = assert_final_hidden(model, o, W.lm_head(), len(tok2))
         am2 = _np(o["argmax"])
-        assert_argmax(am2, exact.argmax, exact.margin, exact.logits)
+        assert_argmax(am2, exact.argmax, exact.margin, tap_am=tap)
         assert_accept(tok2, par2, am2, int(o["accepted_len"][0]), _np(o["accepted_tokens"]), int(o["bonus"][0]),
                       exact.argmax)
         if np.array_equal(chain, ref.chain) and np.array_equal(am2, exact.argmax):

@@ -73,9 +73,9 @@ def _verify_case(M, shape, W, model, td, ctx, seed=3):
     torch.cuda.synchronize()
     assert model.status() == 0
     assert_close(_np(o["logits"]), out.logits)
-    assert_final_hidden(model, o, W.lm_head(), len(tokens))
+    tap = assert_final_hidden(model, o, W.lm_head(), len(tokens))
     am = _np(o["argmax"])
-    assert_argmax(am, out.argmax, out.margin, out.logits)
+    assert_argmax(am, out.argmax, out.margin, tap_am=tap)
     path = assert_accept(tokens, td.parents, am, int(o["accepted_len"][0]), _np(o["accepted_tokens"]),
                          int(o["bonus"][0]), out.argmax)
     L = int(o["accepted_len"][0])
@@ -169,9 +169,9 @@ def test_batched_paged_equals_oracle(M, dec):
     torch.cuda.synchronize()
     assert model.status() == 0
     assert_close(_np(o["logits"]), out.logits)
-    assert_final_hidden(model, o, W.lm_head(), int(cu[-1]))
+    tap = assert_final_hidden(model, o, W.lm_head(), int(cu[-1]))
     am = _np(o["argmax"])
-    assert_argmax(am, out.argmax, out.margin, out.logits)
+    assert_argmax(am, out.argmax, out.margin, tap_am=tap)
     for r in range(3):
         a, b = cu[r], cu[r + 1]
         path = assert_accept(toks[r], drafts[r].parents, am[a:b], int(o["accepted_len"][r]),
