@@ -60,6 +60,10 @@ def parse():
     ap.add_argument("--nvtx", action="store_true", help="wrap the timed steps in the NVTX range 'sdv_step'")
     ap.add_argument("--probe", default=None, metavar="N,K,M",
                     help="time the fused W12 linear alone on an N x K tensor with M rows")
+    ap.add_argument("--probe-kernel", default="gemm", choices=["gemm", "stream"],
+                    help="--probe: sd_w12_linear (warp-level / tcgen05) or sd_w12_linear_stream")
+    ap.add_argument("--gdn", default=None, metavar="R,nh,M",
+                    help="time the gated-delta-rule tree kernel alone: R requests of M-node trees, nh heads")
     ap.add_argument("--tc-min-rows", type=int, default=0,
                     help="rows per launch from which GEMMs run on the tcgen05 kernel (0: the library default)")
     ap.add_argument("--select", default=None, metavar="R,n,budget,cap",
@@ -146,20 +150,30 @@ def probe_arm(args):
     w = synthetic.normal_bf16(synthetic.key(args.seed, 4242), N * K, 0.02).reshape(N, K)
     p = Mdl.pack(Mdl.to_device_u16(w))
     del w
+    # copies of the packed tensor that together exceed L2, cycled by the
+    # launches, so that every launch streams its weights from HBM
+    n_copies = max(1, -(-256 * 2 ** 20 // p.nbytes()))
+    packs = [p] + [p.copy() for _ in range(n_copies - 1)]
     x = Mdl.to_device_u16(synthetic.normal_bf16(synthetic.key(args.seed, 4243), M * K, 1.0).reshape(M, K))
     import speculative_decoding_tree_bit_gb300 as sdv
-    ws = Mdl.Workspace(int(sdv.lib().sd_w12_linear_workspace(N, K, M)))
-    y = Mdl.linear(p, x, ws)
+    stream_kernel = args.probe_kernel == "stream"
+    need = (sdv.lib().sd_w12_linear_stream_workspace(N, K, M) if stream_kernel else
+            sdv.lib().sd_w12_linear_workspace(N, K, M))
+    ws = Mdl.Workspace(int(need))
+    lin = (lambda q, stream=None: Mdl.linear_stream(q, x, ws=ws, stream=stream)) if stream_kernel else \
+        (lambda q, stream=None: Mdl.linear(q, x, ws, stream=stream))
+    y = lin(p)
     stream = torch.cuda.Stream()
     # the launches are replayed from a CUDA graph: no host time between them
     g = torch.cuda.CUDAGraph()
+    n_launch = args.steps * n_copies
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            Mdl.linear(p, x, ws, stream=stream)
+        for i in range(max(args.warmup, n_copies)):
+            lin(packs[i % n_copies], stream=stream)
         stream.synchronize()
         with torch.cuda.graph(g, stream=stream):
-            for _ in range(args.steps):
-                Mdl.linear(p, x, ws, stream=stream)
+            for i in range(n_launch):
+                lin(packs[i % n_copies], stream=stream)
     torch.cuda.synchronize()
     g.replay()
     torch.cuda.synchronize()
@@ -168,13 +182,80 @@ def probe_arm(args):
     g.replay()
     e1.record()
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    us = e0.elapsed_time(e1) * 1e3 / n_launch
     del y
     nbytes = p.nbytes() + M * K * 2 + M * N * 2
     pk, src = peaks()
-    return {"probe": "sd_w12_linear", "N": N, "K": K, "M": M, "tc_min_rows": tc_rows, "us_per_launch": us,
+    return {"probe": "sd_w12_linear_stream" if stream_kernel else "sd_w12_linear", "N": N, "K": K, "M": M,
+            "tc_min_rows": tc_rows, "us_per_launch": us,
             "GBps": nbytes / (us * 1e-6) / 1e9, "frac_of_peak": nbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"],
-            "peak_source": src, "bytes": nbytes, "escapes": p.n_escapes}
+            "peak_source": src, "bytes": nbytes, "escapes": p.n_escapes,
+            "l2": f"{n_copies} copies of the packed tensor cycled ({n_copies * p.nbytes() / 2**20:.0f} MiB)"}
+
+
+def gdn_arm(args):
+    """The gated-delta-rule tree kernel (sd_gdn_tree_verify) alone, then with
+    the commit (sd_gdn_commit): per-launch time with CUDA events over graph
+    replays, against the bytes it must move - each request's fp32 state S0
+    [nh][128][128] read once (and written once by the commit), q/k/v in,
+    o out, alpha/beta - as a fraction of the measured copy bandwidth."""
+    import numpy as np
+    import torch
+    from speculative_decoding_tree_bit_gb300 import _build
+    from speculative_decoding_tree_bit_gb300 import model as Mdl
+    from synthetic import workloads as wl
+    _build.build()
+    R, nh, M = (int(v) for v in args.gdn.split(","))
+    # several input sets whose states together exceed L2, cycled by the replays
+    per_set = R * nh * 128 * 128 * 4
+    n_sets = max(1, -(-256 * 2 ** 20 // per_set))
+    sets = []
+    for i in range(n_sets):
+        g = wl.gdn_inputs(args.seed + i, [M] * R, 8, nh)
+        dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a).view(dt)).cuda()
+        sets.append(dict(q=dev(g.q, np.int16), k=dev(g.k, np.int16), v=dev(g.v, np.int16),
+                         alpha=torch.from_numpy(g.alpha).cuda(), beta=torch.from_numpy(g.beta).cuda(),
+                         par=torch.from_numpy(g.parents.astype(np.int32)).cuda(), cu=g.cu,
+                         cu_dev=torch.from_numpy(g.cu.astype(np.int32)).cuda(),
+                         S=torch.from_numpy(g.S).cuda(), last=torch.full((R,), M - 1, dtype=torch.int32).cuda()))
+    layer = Mdl.GdnLayer(R * M, nh)
+    rows = R * M
+    io_bytes = rows * nh * 128 * 2 * 4 + rows * nh * 4 * 2 + rows * 4
+    res = {"probe": "gdn_tree", "R": R, "nh": nh, "M": M, "l2": f"{n_sets} input sets cycled ({n_sets * per_set / 2**20:.0f} MiB of states)"}
+    pk, src = peaks()
+    for with_commit in (False, True):
+        stream = torch.cuda.Stream()
+        g_ = torch.cuda.CUDAGraph()
+
+        def one(i):
+            d = sets[i % n_sets]
+            layer.verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["par"], d["cu"], d["S"], stream=stream,
+                         cu_dev=d["cu_dev"])
+            if with_commit:
+                layer.commit(d["last"], d["S"], stream=stream)
+        with torch.cuda.stream(stream):
+            for i in range(max(args.warmup, n_sets)):
+                one(i)
+            stream.synchronize()
+            with torch.cuda.graph(g_, stream=stream):
+                for i in range(args.steps * n_sets):
+                    one(i)
+        torch.cuda.synchronize()
+        g_.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g_.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (args.steps * n_sets)
+        nbytes = per_set * (2 if with_commit else 1) + io_bytes
+        key = "verify_commit" if with_commit else "verify"
+        res[key] = {"us_per_call": us, "bytes": nbytes, "GBps": nbytes / (us * 1e-6) / 1e9,
+                    "frac_of_peak": nbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"]}
+    res["status"] = int(layer.status.item())
+    res["peak_source"] = src
+    return res
 
 
 def log(*a):
@@ -594,6 +675,9 @@ def main():
         return
     if args.probe:
         print(json.dumps(probe_arm(args)), flush=True)
+        return
+    if args.gdn:
+        print(json.dumps(gdn_arm(args)), flush=True)
         return
     if args.impl == "reference":
         if rank == 0:

@@ -215,10 +215,10 @@ int sd_w12_linear_stream(const w12_tensor* W, const uint32_t* plane8, const uint
  * scratch lives in a static device array inside the library (about 9.5 MiB
  * that every GPU loading the library holds until the process exits), so the
  * call allocates nothing; the caller passes only W, x and y.
- * Limits: 1 <= M <= 64 and N <= 262144, and M below the tensor-core
- * threshold (sd_gemm_set_tc_min_rows: the static scratch serves the
- * warp-level kernel only), else SD_ERR_UNSUPPORTED.  The launch takes the
- * grid sd_w12_linear's warp-level path takes (up to 1216 CTAs x 8-row tiles).
+ * Limits: 1 <= M <= 64 and N <= 262144, else SD_ERR_UNSUPPORTED.  The
+ * call always runs the warp-level kernel (the static scratch is sized for
+ * it), whatever sd_gemm_set_tc_min_rows says, with the grid sd_w12_linear
+ * gives that kernel (up to 1216 CTAs x 8-row tiles).
  * Each call looks up the array's address in the current context (a context
  * made after cudaDeviceReset gets its own); inside a stream capture use
  * cudaStreamCaptureModeRelaxed, which allows that lookup.
@@ -236,8 +236,9 @@ int sd_w12_linear_static(const w12_tensor* W, const uint16_t* x, int32_t M, uint
  * batched results: the batched step crosses from the weight-bandwidth bound
  * to the tensor-core bound).  Process-wide; applies to calls issued
  * afterwards (a model re-captures its step graphs).  rows <= 0 restores the
- * default, 65 (launches of more than 64 rows).  Returns the value now
- * in force.  Not thread-safe against concurrent GEMM calls. */
+ * default, 33 (the measured crossover: the warp-level kernel is faster up to
+ * 32 rows).  Returns the value now in force.  Not thread-safe against
+ * concurrent GEMM calls. */
 int32_t sd_gemm_set_tc_min_rows(int32_t rows);
 
 /* Prefix key splits per (request, kv head, 64-row chunk) of the verify
@@ -571,9 +572,9 @@ int sd_forward(sd_model* m, const int32_t* tree_tokens, const int32_t* parents, 
  * tensor with the row order it was packed with; device, borrowed, 16-byte
  * aligned): planes_host[4 l + 0..3] = layer l's qkv, o, gate_up, down, then
  * planes_host[4 n_layers] = the lm_head's; n = 4 n_layers + 1.
- * sd_forward_view8 is sd_forward over the view; it needs the streamed step
- * (M <= 64 and below the tensor-core threshold, sd_gemm_set_tc_min_rows) and the
- * registered planes, else SD_ERR_UNSUPPORTED.  The new K/V it writes to
+ * sd_forward_view8 is sd_forward over the view (every linear on the
+ * weight-streaming kernel); it needs M <= 64 and the registered planes,
+ * else SD_ERR_UNSUPPORTED.  The new K/V it writes to
  * slots ctx + node are the view's (an exact step rewrites them). */
 int sd_model_set_view8(sd_model* m, const uint32_t* const* planes_host, int32_t n);
 int sd_forward_view8(sd_model* m, const int32_t* tree_tokens, const int32_t* parents, int32_t M, const sd_kv* kv,

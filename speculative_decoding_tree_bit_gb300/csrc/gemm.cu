@@ -170,16 +170,30 @@ int pad_rows(int M) { return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 
 
 static int nt_of(int M) { return M > 128 ? 16 : pad_rows(M) / 8; }
 
-// Default crossover of the two kernels (rows per launch): the batched step
-// of the 8B-class decoder runs faster on the warp-level kernel at 64 rows
-// and on the tcgen05 kernel at 128.
-constexpr int kTcMinRowsDefault = 65;
+// Default crossover of the two kernels (rows per launch), measured on the
+// 8B-class gate/up GEMM (24576 x 4096, event-timed launches on GB300): the
+// warp-level kernel takes 43 / 54 us at 16 / 32 rows (tcgen05: 66 / 67),
+// the tcgen05 kernel 68 / 70 us at 48 / 64 rows (warp-level: 72 / 72).
+constexpr int kTcMinRowsDefault = 33;
 static int g_tc_min_rows = kTcMinRowsDefault;
 
 int gemm_tc_min_rows() { return g_tc_min_rows; }
 void gemm_set_tc_min_rows(int rows) { g_tc_min_rows = rows > 0 ? rows : kTcMinRowsDefault; }
 
-int gemm_grid(int M) { return gemm_use_tc(M) ? num_sms() : (nt_of(M) <= 4 ? 2 : 1) * num_sms(); }
+static int warp_grid(int M) { return (nt_of(M) <= 4 ? 2 : 1) * num_sms(); }
+
+int gemm_grid(int M) { return gemm_use_tc(M) ? num_sms() : warp_grid(M); }
+
+int gemm_warp_launch_grid(const w12_tensor& W, int M, int epi) {
+  int grid = warp_grid(M);
+  // few row blocks (q/k/v, O, down): a whole number of CTAs per row block,
+  // so that no CTA's range straddles two row blocks (a straddling CTA
+  // finishes two segments and trails the others); the argmax partials of
+  // the logits GEMM keep one slot per CTA of gemm_grid
+  const int nb = gemm_counters(W.N);
+  if (epi != EPI_LOGITS && nb * 4 <= grid) grid = nb * (grid / nb);
+  return grid;
+}
 
 int gemm_launch_grid(const w12_tensor& W, int M, int epi) {
   if (gemm_use_tc(M)) {
@@ -188,14 +202,7 @@ int gemm_launch_grid(const w12_tensor& W, int M, int epi) {
     const int nb = gemm_counters(W.N), sms = num_sms();
     return (epi != EPI_LOGITS && nb * 2 <= sms) ? nb * (sms / nb) : sms;
   }
-  int grid = gemm_grid(M);
-  // few row blocks (q/k/v, O, down): a whole number of CTAs per row block,
-  // so that no CTA's range straddles two row blocks (a straddling CTA
-  // finishes two segments and trails the others); the argmax partials of
-  // the logits GEMM keep one slot per CTA of gemm_grid
-  const int nb = gemm_counters(W.N);
-  if (epi != EPI_LOGITS && nb * 4 <= grid) grid = nb * (grid / nb);
-  return grid;
+  return gemm_warp_launch_grid(W, M, epi);
 }
 
 size_t gemm_partial_floats(int M) {
@@ -352,7 +359,12 @@ int make_gemm_params(GemmParams* out, const w12_tensor& W, const uint16_t* x, in
 int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
                 const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid, uint64_t* trace) {
   if (gemm_use_tc(M)) return gemm_tc_launch(W, x, xm.rows_total, M, epi, ws, status, s, pdl);
-  if (grid <= 0) grid = gemm_launch_grid(W, M, epi.epi);
+  return gemm_warp_launch(W, x, xm, M, epi, ws, status, s, pdl, grid, trace);
+}
+
+int gemm_warp_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
+                     const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid, uint64_t* trace) {
+  if (grid <= 0) grid = gemm_warp_launch_grid(W, M, epi.epi);
   GemmParams p;
   const int prc = make_gemm_params(&p, W, x, M, epi, ws, status);
   if (prc) return prc;

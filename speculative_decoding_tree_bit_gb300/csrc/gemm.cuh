@@ -88,6 +88,12 @@ int make_x_map(XMap* xm, const uint16_t* x, int rows_total, int64_t K, int box_r
 int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
                 const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid = 0,
                 uint64_t* trace = nullptr);
+// The same on the warp-level kernel whatever the row count (M <= 64 in one
+// launch), with its own default grid.
+int gemm_warp_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
+                     const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid = 0,
+                     uint64_t* trace = nullptr);
+int gemm_warp_launch_grid(const w12_tensor& W, int M, int epi);
 
 // Descriptor of the packed words for the 2-D weight loads (one box = 8
 // strips x 1536 bytes).

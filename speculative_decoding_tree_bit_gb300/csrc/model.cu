@@ -177,9 +177,8 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   // RMSNorms folded in
   const bool skinny = rows <= kStreamMaxRows && !gemm_use_tc(rows);
   const bool fused = skinny && m->fused;
-  if (io.view8 && (!skinny || m->view8.size() != (size_t)4 * m->cfg.n_layers + 1)) {
-    set_error("model: the 8-bit view needs sd_model_set_view8 and a streamed step (rows <= 64, below the "
-              "tensor-core threshold)");
+  if (io.view8 && (rows > kStreamMaxRows || m->view8.size() != (size_t)4 * m->cfg.n_layers + 1)) {
+    set_error("model: the 8-bit view needs sd_model_set_view8 and at most 64 rows");
     return SD_ERR_UNSUPPORTED;
   }
   auto v8 = [&](int l, int k) -> const uint32_t* {

@@ -65,11 +65,6 @@ extern "C" int sd_w12_linear_static(const w12_tensor* W, const uint16_t* x, int3
               "use sd_w12_linear with a workspace for larger calls");
     return SD_ERR_UNSUPPORTED;
   }
-  if (gemm_use_tc(M)) {
-    set_error("sd_w12_linear_static: M is at or above the tensor-core threshold (sd_gemm_set_tc_min_rows); "
-              "the static scratch serves the warp-level kernel only");
-    return SD_ERR_UNSUPPORTED;
-  }
   StaticScratch sc;
   int rc = static_scratch(&sc);
   if (rc) return rc;
@@ -89,9 +84,10 @@ extern "C" int sd_w12_linear_static(const w12_tensor* W, const uint16_t* x, int3
   e.epi = EPI_STORE;
   e.out = y;
   e.ldo = (int)W->N;
-  // the grid sd_w12_linear's warp-level path takes, within the scratch
+  // the warp-level kernel whatever the tensor-core threshold (the static
+  // scratch is sized for it), with the grid sd_w12_linear gives it
   const int nt = pad_rows(M) / 8;
-  int grid = gemm_launch_grid(*W, M, EPI_STORE);
+  int grid = gemm_warp_launch_grid(*W, M, EPI_STORE);
   if (grid * nt > kStaticCtaTiles) grid = kStaticCtaTiles / nt;
-  return gemm_launch(*W, x, xm, M, e, ws, nullptr, s, false, grid);
+  return gemm_warp_launch(*W, x, xm, M, e, ws, nullptr, s, false, grid);
 }

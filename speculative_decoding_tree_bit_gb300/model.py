@@ -55,6 +55,15 @@ class Packed:
         t.affine = self.meta.affine
         return t
 
+    def copy(self) -> "Packed":
+        """A copy in new device buffers (same meta); the 8-bit plane too."""
+        cl = lambda t: None if t is None else t.clone()
+        q = Packed(self.meta, cl(self.words), cl(self.esc_idx), cl(self.esc_val), cl(self.row_ptr), cl(self.tile_ptr),
+                   cl(self.tile_esc))
+        if getattr(self, "plane8", None) is not None:
+            q.plane8 = self.plane8.clone()
+        return q
+
     def nbytes(self) -> int:
         """Bytes a GEMM streams: the packed words plus the escape tile index."""
         return self.words.numel() * 4 + self.n_escapes * 4 + int(lib().w12_tile_ptr_count(self.N, self.K)) * 4
@@ -513,12 +522,13 @@ class GdnLayer:
         self.ws = Workspace(int(lib().sd_gdn_workspace(int(max_rows), self.nh)), device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
-    def verify(self, q, k, v, alpha, beta, parents, cu, S, stream=None) -> torch.Tensor:
+    def verify(self, q, k, v, alpha, beta, parents, cu, S, stream=None, cu_dev=None) -> torch.Tensor:
         """q, k, v int16 bits [rows][nh][128]; alpha, beta float32 [rows][nh];
-        parents int32 [rows]; cu host array [R+1]; S float32 [R][nh][128][128].
-        Returns o (int16 bf16 bits [rows][nh][128])."""
+        parents int32 [rows]; cu host array [R+1] (cu_dev: the same on the
+        device, e.g. for a call inside a stream capture); S float32
+        [R][nh][128][128].  Returns o (int16 bf16 bits [rows][nh][128])."""
         cu_h = np.ascontiguousarray(np.asarray(cu, dtype=np.int32))
-        cu_d = _i32(cu_h, self.device)
+        cu_d = cu_dev if cu_dev is not None else _i32(cu_h, self.device)
         par = parents if isinstance(parents, torch.Tensor) else _i32(parents, self.device)
         out = torch.empty_like(q)
         self._cu = (cu_h, cu_d, par)

@@ -107,6 +107,7 @@ def test_tree_verify_on_the_fused_schedule(M, dec):
     16 and 64 nodes, and a batch of paged requests."""
     shape, W, model = dec
     model.set_fused(True)
+    M.set_tc_min_rows(65)  # every step of at most 64 rows on the fused schedule
     try:
         _verify_case(M, shape, W, model, wl.draft(11, 0, 16, 8, 0.8, shape.V), 37)
         _verify_case(M, shape, W, model, wl.draft(12, 0, 64, 10, 0.7, shape.V), 130)
@@ -114,6 +115,7 @@ def test_tree_verify_on_the_fused_schedule(M, dec):
         test_batched_paged_equals_oracle(M, dec)
     finally:
         model.set_fused(False)
+        M.set_tc_min_rows(0)
 
 
 @pytest.mark.parametrize("splits", [1, 3, 64])
@@ -242,10 +244,12 @@ def test_repeated_steps_give_identical_bits(M, dec, n, fused):
     schedules."""
     shape, W, model = dec
     model.set_fused(fused)
+    M.set_tc_min_rows(65)
     try:
         _repeat(M, shape, W, model, n)
     finally:
         model.set_fused(False)
+        M.set_tc_min_rows(0)
 
 
 def _repeat(M, shape, W, model, n):

@@ -58,20 +58,25 @@ def test_static_linear_matches_the_oracle(Mrows):
     assert_close(y.cpu().numpy().view(np.uint16), oracle.linear(x, W))
 
 
-def test_static_linear_refuses_the_tensor_core_range():
-    from speculative_decoding_tree_bit_gb300 import lib
+def test_static_linear_ignores_the_tensor_core_threshold():
+    """The static scratch is sized for the warp-level kernel, which the call
+    runs whatever sd_gemm_set_tc_min_rows says."""
+    from speculative_decoding_tree_bit_gb300 import check, lib, stream_ptr
     from speculative_decoding_tree_bit_gb300 import model as M
-    t = wl.tiny()
-    p = M.pack(M.to_device_u16(t.W1))
+    N, K, Mrows = 256, 1024, 48
+    W = synthetic.normal_bf16(synthetic.key(64, 0), N * K, 0.02).reshape(N, K)
+    p = M.pack(M.to_device_u16(W))
     st = p.struct()
-    x = torch.zeros((16, t.W1.shape[1]), dtype=torch.int16, device="cuda")
-    y = torch.empty((16, t.W1.shape[0]), dtype=torch.int16, device="cuda")
+    x = synthetic.normal_bf16(synthetic.key(65, 0), Mrows * K, 1.0).reshape(Mrows, K)
+    y = torch.empty((Mrows, N), dtype=torch.int16, device="cuda")
     assert M.set_tc_min_rows(16) == 16
     try:
-        assert lib().sd_w12_linear_static(ctypes.byref(st), x.data_ptr(), 16, y.data_ptr(), None) == 2
-        assert b"tensor-core threshold" in lib().sd_last_error()
+        check(lib().sd_w12_linear_static(ctypes.byref(st), M.to_device_u16(x).data_ptr(), Mrows, y.data_ptr(),
+                                         stream_ptr()))
+        torch.cuda.synchronize()
     finally:
         M.set_tc_min_rows(0)
+    assert_close(y.cpu().numpy().view(np.uint16), oracle.linear(x, W))
 
 
 def test_static_linear_rejects_sizes_beyond_its_scratch():
