@@ -64,13 +64,13 @@ struct GdnSmem {
   int ok;
 };
 
-// Validates one request's parent array into s.anc / s.par (thread 0).
-__device__ __forceinline__ bool gdn_tree_ok(const int32_t* parents, int node0, int M, GdnSmem& s) {
+// Validates one request's parent array (staged in s.par) into s.anc
+// (thread 0; no global loads on its serial chain).
+__device__ __forceinline__ bool gdn_tree_ok(int M, GdnSmem& s) {
   if (M < 1 || M > kGdnMaxM) return false;
   for (int i = 0; i < M; i++) {
-    const int p = parents[node0 + i];
+    const int p = s.par[i];
     if (i == 0 ? p != -1 : (p < 0 || p >= i)) return false;
-    s.par[i] = p;
     s.anc[i] = (i ? s.anc[p] : 0ull) | (1ull << i);
   }
   return true;
@@ -92,8 +92,15 @@ __global__ void __launch_bounds__(kGdnThreads, 1) k_gdn_tree(GdnArgs a) {
         __ldcg(reinterpret_cast<const float4*>(S0 + (int64_t)row * kGdnHd + cc * kGdnCols) + c4);
   }
   const int node0 = a.cu[r], M = a.cu[r + 1] - node0;
+  // the parents and gates of the request, all loads at once (the serial
+  // chains below then run on shared memory)
+  for (int i = tid; i < M && i < kGdnMaxM; i += kGdnThreads) {
+    s.par[i] = a.parents[node0 + i];
+    s.g[i] = a.alpha[(int64_t)(node0 + i) * nh + h];
+  }
+  __syncthreads();
   if (tid == 0) {
-    s.ok = gdn_tree_ok(a.parents, node0, M, s) ? 1 : 0;
+    s.ok = gdn_tree_ok(M, s) ? 1 : 0;
     if (!s.ok) set_status(a.status, SD_ERR_BAD_TREE);
   }
   __syncthreads();
@@ -123,12 +130,16 @@ __global__ void __launch_bounds__(kGdnThreads, 1) k_gdn_tree(GdnArgs a) {
     }
     if (lane == 0) s.b[i] = a.beta[(int64_t)(node0 + i) * nh + h];
   }
+  // this CTA's value columns of every node, staged in u (the solve below
+  // overwrites each row with its result)
+  for (int e = tid; e < M * kGdnCols; e += kGdnThreads) {
+    const int i = e / kGdnCols, c = e % kGdnCols;
+    s.u[i][c] = bf2f(a.v[((int64_t)(node0 + i) * nh + h) * kGdnHd + cc * kGdnCols + c]);
+  }
   if (tid == 0) {
-    // path products of the gates, root first (G_i = alpha_i G_parent)
-    for (int i = 0; i < M; i++) {
-      const float al = a.alpha[(int64_t)(node0 + i) * nh + h];
-      s.g[i] = i ? al * s.g[s.par[i]] : al;
-    }
+    // path products of the gates, root first (G_i = alpha_i G_parent), in
+    // place over the staged gates (parents precede children)
+    for (int i = 1; i < M; i++) s.g[i] = s.g[i] * s.g[s.par[i]];
   }
   __syncthreads();
   // dot products along root paths: t (strict ancestors, scaled by beta_i)
@@ -173,8 +184,7 @@ __global__ void __launch_bounds__(kGdnThreads, 1) k_gdn_tree(GdnArgs a) {
       s.w[i][tid] = acc;
     } else if (tid < kGdnHd + kGdnCols) {
       const int c = tid - kGdnHd;
-      const float vv = bf2f(a.v[((int64_t)(node0 + i) * nh + h) * kGdnHd + cc * kGdnCols + c]);
-      float acc = s.b[i] * (vv / s.g[i]);
+      float acc = s.b[i] * (s.u[i][c] / s.g[i]);
       uint64_t m = strict;
       while (m) {
         const int j = __ffsll((long long)m) - 1;
@@ -232,10 +242,15 @@ __global__ void __launch_bounds__(kGdnThreads) k_gdn_commit(const int32_t* __res
   pdl_launch();
   pdl_wait();
   __shared__ int path[kGdnMaxM];
+  __shared__ int par_s[kGdnMaxM];
   __shared__ int n_path;
   __shared__ float kp[kGdnMaxM][kGdnCommitRows];
   const int rb = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
   const int node0 = cu[r], M = cu[r + 1] - node0;
+  // the request's parents, all loads at once; the walk then runs on shared
+  // memory
+  for (int i = threadIdx.x; i < M && i < kGdnMaxM; i += blockDim.x) par_s[i] = parents[node0 + i];
+  __syncthreads();
   if (threadIdx.x == 0) {
     int n = 0;
     int j = last[r];
@@ -243,7 +258,7 @@ __global__ void __launch_bounds__(kGdnThreads) k_gdn_commit(const int32_t* __res
       int tmp[kGdnMaxM];
       while (j >= 0 && n < kGdnMaxM) {
         tmp[n++] = j;
-        const int p = parents[node0 + j];
+        const int p = par_s[j];
         j = (p < j) ? p : -1;  // parents precede children (validated by the verify kernel)
       }
       for (int i = 0; i < n; i++) path[i] = tmp[n - 1 - i];
