@@ -341,7 +341,17 @@ def oracle_sample(shape, seed, M, ctx, parents, tokens, n_layers=1, reps=1):
     oracle.linear(x, W.lm_head())
     t_lm = time.perf_counter() - t0
     per_layer = max(1e-9, (statistics.median(t_full) - t_lm) / n_layers)
-    return per_layer, t_lm, os.cpu_count()
+    return per_layer, t_lm, oracle_threads()
+
+
+def oracle_threads() -> int:
+    """Threads the oracle's OpenMP loops use: OMP_NUM_THREADS when set (read
+    when the library loads), else every host core."""
+    try:
+        n = int(os.environ.get("OMP_NUM_THREADS", "0").split(",")[0])
+    except ValueError:
+        n = 0
+    return n if n > 0 else os.cpu_count()
 
 
 def reference_arm(args):
