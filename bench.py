@@ -60,8 +60,10 @@ def parse():
     ap.add_argument("--nvtx", action="store_true", help="wrap the timed steps in the NVTX range 'sdv_step'")
     ap.add_argument("--probe", default=None, metavar="N,K,M",
                     help="time the fused W12 linear alone on an N x K tensor with M rows")
-    ap.add_argument("--probe-kernel", default="gemm", choices=["gemm", "stream"],
-                    help="--probe: sd_w12_linear (warp-level / tcgen05) or sd_w12_linear_stream")
+    ap.add_argument("--probe-kernel", default="gemm", choices=["gemm", "stream", "view8", "stream_view8"],
+                    help="--probe: sd_w12_linear (warp-level / tcgen05), sd_w12_linear_stream, "
+                         "sd_w12_linear_view8 (the nested 8-bit plane, 1 byte per weight), or the streaming "
+                         "kernel over the plane")
     ap.add_argument("--gdn", default=None, metavar="R,nh,M",
                     help="time the gated-delta-rule tree kernel alone: R requests of M-node trees, nh heads")
     ap.add_argument("--tc-min-rows", type=int, default=0,
@@ -148,20 +150,27 @@ def probe_arm(args):
     tc_rows = Mdl.set_tc_min_rows(args.tc_min_rows)
     N, K, M = (int(v) for v in args.probe.split(","))
     w = synthetic.normal_bf16(synthetic.key(args.seed, 4242), N * K, 0.02).reshape(N, K)
-    p = Mdl.pack(Mdl.to_device_u16(w))
+    view8 = args.probe_kernel in ("view8", "stream_view8")
+    p = Mdl.pack(Mdl.to_device_u16(w), view8=view8)
     del w
+    wbytes = (p.plane8.numel() * p.plane8.element_size() + p.nbytes() - p.words.numel() * 4) if view8 else p.nbytes()
     # copies of the packed tensor that together exceed L2, cycled by the
     # launches, so that every launch streams its weights from HBM
-    n_copies = max(1, -(-256 * 2 ** 20 // p.nbytes()))
+    n_copies = max(1, -(-256 * 2 ** 20 // wbytes))
     packs = [p] + [p.copy() for _ in range(n_copies - 1)]
     x = Mdl.to_device_u16(synthetic.normal_bf16(synthetic.key(args.seed, 4243), M * K, 1.0).reshape(M, K))
     import speculative_decoding_tree_bit_gb300 as sdv
-    stream_kernel = args.probe_kernel == "stream"
-    need = (sdv.lib().sd_w12_linear_stream_workspace(N, K, M) if stream_kernel else
-            sdv.lib().sd_w12_linear_workspace(N, K, M))
+    kind = args.probe_kernel
+    need = {"gemm": sdv.lib().sd_w12_linear_workspace, "view8": sdv.lib().sd_w12_linear_view8_workspace,
+            "stream": sdv.lib().sd_w12_linear_stream_workspace,
+            "stream_view8": sdv.lib().sd_w12_linear_stream_workspace}[kind](N, K, M)
     ws = Mdl.Workspace(int(need))
-    lin = (lambda q, stream=None: Mdl.linear_stream(q, x, ws=ws, stream=stream)) if stream_kernel else \
-        (lambda q, stream=None: Mdl.linear(q, x, ws, stream=stream))
+    if kind == "gemm":
+        lin = lambda q, stream=None: Mdl.linear(q, x, ws, stream=stream)
+    elif kind == "view8":
+        lin = lambda q, stream=None: Mdl.linear_view8(q, x, q.plane8, ws=ws, stream=stream)
+    else:
+        lin = lambda q, stream=None: Mdl.linear_stream(q, x, q.plane8 if view8 else None, ws=ws, stream=stream)
     y = lin(p)
     stream = torch.cuda.Stream()
     # the launches are replayed from a CUDA graph: no host time between them
@@ -184,13 +193,15 @@ def probe_arm(args):
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / n_launch
     del y
-    nbytes = p.nbytes() + M * K * 2 + M * N * 2
+    nbytes = wbytes + M * K * 2 + M * N * 2
     pk, src = peaks()
-    return {"probe": "sd_w12_linear_stream" if stream_kernel else "sd_w12_linear", "N": N, "K": K, "M": M,
+    name = {"gemm": "sd_w12_linear", "stream": "sd_w12_linear_stream", "view8": "sd_w12_linear_view8",
+            "stream_view8": "sd_w12_linear_stream (8-bit view)"}
+    return {"probe": name[args.probe_kernel], "N": N, "K": K, "M": M,
             "tc_min_rows": tc_rows, "us_per_launch": us,
             "GBps": nbytes / (us * 1e-6) / 1e9, "frac_of_peak": nbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"],
             "peak_source": src, "bytes": nbytes, "escapes": p.n_escapes,
-            "l2": f"{n_copies} copies of the packed tensor cycled ({n_copies * p.nbytes() / 2**20:.0f} MiB)"}
+            "l2": f"{n_copies} copies of the packed tensor cycled ({n_copies * wbytes / 2**20:.0f} MiB)"}
 
 
 def gdn_arm(args):

@@ -207,6 +207,18 @@ size_t sd_w12_linear_stream_workspace(int64_t N, int64_t K, int32_t M);
 int sd_w12_linear_stream(const w12_tensor* W, const uint32_t* plane8, const uint16_t* x, int32_t M, uint16_t* y,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/* The product with the nested 8-bit view of W ("SpecPilot ...", "(3)
+ * Two-Level Verification": round one of two-level verification), streaming
+ * W's 8-bit plane at 1 byte per weight (plane8: w12_plane8_pack, 16-byte
+ * aligned), 1 <= M <= 64: the warp-level kernel in its 8-bit decode mode
+ * for a contiguous exponent table, the weight-streaming kernel otherwise.
+ * workspace: sd_w12_linear_view8_workspace(N, K, M) bytes, 256-byte
+ * aligned.  Errors: SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED,
+ * SD_ERR_WORKSPACE, SD_ERR_CUDA. */
+size_t sd_w12_linear_view8_workspace(int64_t N, int64_t K, int32_t M);
+int sd_w12_linear_view8(const w12_tensor* W, const uint32_t* plane8, const uint16_t* x, int32_t M, uint16_t* y,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
 /* The same linear for callers that cannot allocate device memory: a host
  * framework that owns all device memory through its own pool, a real-time
  * thread that must not take cudaMalloc's implicit synchronisation, a plug-in

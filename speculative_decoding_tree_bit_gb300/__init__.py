@@ -83,6 +83,8 @@ _SIGS = {
     "sd_w12_linear": (ctypes.c_int, [P(W12Tensor), vp, i32, vp, vp, ctypes.c_size_t, vp]),
     "sd_w12_linear_static": (ctypes.c_int, [P(W12Tensor), vp, i32, vp, vp]),
     "sd_w12_linear_stream_workspace": (ctypes.c_size_t, [i64, i64, i32]),
+    "sd_w12_linear_view8_workspace": (ctypes.c_size_t, [i64, i64, i32]),
+    "sd_w12_linear_view8": (ctypes.c_int, [P(W12Tensor), vp, vp, i32, vp, vp, ctypes.c_size_t, vp]),
     "sd_w12_linear_stream": (ctypes.c_int, [P(W12Tensor), vp, vp, i32, vp, vp, ctypes.c_size_t, vp]),
     "sd_gemm_set_tc_min_rows": (i32, [i32]),
     "sd_attn_set_splits": (i32, [i32]),

@@ -41,11 +41,11 @@ namespace sdv {
 template <int NT>
 constexpr int ctas_per_sm() { return NT <= 4 ? 2 : 1; }
 
-template <int NT, bool AFFINE>
+template <int NT, bool AFFINE, bool V8 = false>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
     k_w12_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap xmap,
                const __grid_constant__ CUtensorMap wmap) {
-  using C = Cfg<NT>;
+  using C = Cfg<NT, V8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sx = smem;
@@ -91,8 +91,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
         // one 2-D box per stage: 8 strips x 1536 bytes (ragged row blocks are
         // zero-filled by the copy engine and never read)
         auto issue_weights = [&](int slot, int bb, int tt) {
+          // 8 strips x 1536 bytes, or 8 strips x 1024 bytes of the 8-bit plane
           mbar_arrive_expect_tx(&full[slot], C::WB + C::XB);
-          tma2d_g2s(sw + slot * C::WB, &wmap, tt * 192, bb * kRB, &full[slot]);
+          tma2d_g2s(sw + slot * C::WB, &wmap, tt * (V8 ? 128 : 192), bb * kRB, &full[slot]);
         };
         for (int i = 0; i < pre; i++) {
           issue_weights(i, b, t);
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
     // -------------------------------------------------- escape warp --
     int eseg = 0, eslot = 0;
     uint32_t ephase = 0;
-    escape_segments<NT>(p, sx, full, empty, eslot, ephase, corr, corr_full, corr_empty, eseg, abort);
+    escape_segments<NT, V8>(p, sx, full, empty, eslot, ephase, corr, corr_full, corr_empty, eseg, abort);
     return;
   }
 
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
   if (p.trace && threadIdx.x == 0) p.trace[blockIdx.x] = globaltimer();
   int slot = 0, cseg = 0;
   uint32_t phase = 0;
-  consume_gemm<NT, AFFINE>(p, sx, sw, full, empty, red_v, red_i, flag, slot, phase, corr, corr_full, corr_empty,
+  consume_gemm<NT, AFFINE, V8>(p, sx, sw, full, empty, red_v, red_i, flag, slot, phase, corr, corr_full, corr_empty,
                            cseg, abort, p.trace ? p.trace + G + blockIdx.x : nullptr, G);
   if (p.trace) {
     bar_sync(1, kNCW * 32);
@@ -181,6 +182,7 @@ int gemm_tc_min_rows() { return g_tc_min_rows; }
 void gemm_set_tc_min_rows(int rows) { g_tc_min_rows = rows > 0 ? rows : kTcMinRowsDefault; }
 
 static int warp_grid(int M) { return (nt_of(M) <= 4 ? 2 : 1) * num_sms(); }
+int gemm_warp_grid(int M) { return warp_grid(M); }
 
 int gemm_grid(int M) { return gemm_use_tc(M) ? num_sms() : warp_grid(M); }
 
@@ -305,17 +307,17 @@ int make_w8_map(CUtensorMap* map, const uint32_t* plane, int64_t N, int64_t K) {
   return SD_OK;
 }
 
-template <int NT, bool AFF>
+template <int NT, bool AFF, bool V8 = false>
 static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, const CUtensorMap& wmap, cudaStream_t s,
                              bool pdl, int grid) {
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e =
-        cudaFuncSetAttribute(k_w12_gemm<NT, AFF>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NT>::SMEM);
+        cudaFuncSetAttribute(k_w12_gemm<NT, AFF, V8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NT, V8>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch(k_w12_gemm<NT, AFF>, dim3(grid), dim3(kThreads), Cfg<NT>::SMEM, s, pdl, p, map, wmap);
+  return launch(k_w12_gemm<NT, AFF, V8>, dim3(grid), dim3(kThreads), Cfg<NT, V8>::SMEM, s, pdl, p, map, wmap);
 }
 
 int make_gemm_params(GemmParams* out, const w12_tensor& W, const uint16_t* x, int M, const GemmEpilogue& epi,
@@ -340,6 +342,8 @@ int make_gemm_params(GemmParams* out, const w12_tensor& W, const uint16_t* x, in
   for (int i = 0; i < 4; i++)
     p.tab[i] = t16[4 * i] | (t16[4 * i + 1] << 8) | (t16[4 * i + 2] << 16) | ((uint32_t)t16[4 * i + 3] << 24);
   p.esc_slot = W.affine ? ldexpf(1.0f, (int)base + 15 - 127) : 0.0f;
+  p.view8 = 0;
+  p.esc_mask = 0xFFFFu;
   if (W.n_escapes > 0 && (!W.tile_ptr || !W.tile_esc)) {
     set_error("gemm: the tensor has escapes but no escape tile index (w12_pack_tile_index)");
     return SD_ERR_INVALID_ARG;
@@ -363,11 +367,20 @@ int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, c
 }
 
 int gemm_warp_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
-                     const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid, uint64_t* trace) {
+                     const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid, uint64_t* trace,
+                     const uint32_t* plane8) {
   if (grid <= 0) grid = gemm_warp_launch_grid(W, M, epi.epi);
   GemmParams p;
   const int prc = make_gemm_params(&p, W, x, M, epi, ws, status);
   if (prc) return prc;
+  if (plane8 && (!W.affine || M > 64)) {
+    set_error("gemm: the 8-bit view runs on the warp-level kernel for a contiguous exponent table and M <= 64");
+    return SD_ERR_UNSUPPORTED;
+  }
+  if (plane8) {
+    p.view8 = 1;
+    p.esc_mask = 0xFFF0u;
+  }
   p.trace = M <= 128 ? trace : nullptr;
   p.G = grid;
   if (ws.counters_len < p.NB) {
@@ -385,8 +398,19 @@ int gemm_warp_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int
   }
   const bool aff = W.affine != 0;
   CUtensorMap wmap;
-  const int wrc = make_w_map(&wmap, W);
+  const int wrc = plane8 ? make_w8_map(&wmap, plane8, W.N, W.K) : make_w_map(&wmap, W);
   if (wrc) return wrc;
+  if (plane8) {
+    cudaError_t e;
+    switch (NT) {
+      case 1: e = launch_nt<1, true, true>(p, xm.map, wmap, s, pdl, grid); break;
+      case 2: e = launch_nt<2, true, true>(p, xm.map, wmap, s, pdl, grid); break;
+      case 4: e = launch_nt<4, true, true>(p, xm.map, wmap, s, pdl, grid); break;
+      default: e = launch_nt<8, true, true>(p, xm.map, wmap, s, pdl, grid); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "k_w12_gemm (8-bit view) launch");
+    return SD_OK;
+  }
   for (int m0 = 0; m0 < M; m0 += 128) {
     p.m0 = m0;
     cudaError_t e;
@@ -450,4 +474,43 @@ extern "C" int sd_w12_linear(const w12_tensor* W, const uint16_t* x, int32_t M, 
   const int rc = make_x_map(&xm, x, M, W->K, M > 128 ? 128 : pad_rows(M));
   if (rc) return rc;
   return gemm_launch(*W, x, xm, M, e, ws, nullptr, s, false);
+}
+
+extern "C" size_t sd_w12_linear_view8_workspace(int64_t N, int64_t K, int32_t M) {
+  return std::max(sd_w12_linear_workspace(N, K, M), sd_w12_linear_stream_workspace(N, K, M));
+}
+
+extern "C" int sd_w12_linear_view8(const w12_tensor* W, const uint32_t* plane8, const uint16_t* x, int32_t M,
+                                   uint16_t* y, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!W || !plane8 || !x || !y || !workspace || M < 1) {
+    set_error("sd_w12_linear_view8: bad argument");
+    return SD_ERR_INVALID_ARG;
+  }
+  if (M > 64 || W->N % 16 || W->K % 64) {
+    set_error("sd_w12_linear_view8: need 1 <= M <= 64, N % 16 == 0 and K % 64 == 0");
+    return SD_ERR_UNSUPPORTED;
+  }
+  if (workspace_bytes < sd_w12_linear_view8_workspace(W->N, W->K, M) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255) || (reinterpret_cast<uintptr_t>(plane8) & 15)) {
+    set_error("sd_w12_linear_view8: workspace too small or misaligned (256 bytes), or plane8 not 16-byte aligned");
+    return SD_ERR_WORKSPACE;
+  }
+  if (!W->affine)  // a general exponent table: the streaming kernel decodes it
+    return sd_w12_linear_stream(W, plane8, x, M, y, workspace, workspace_bytes, stream);
+  cudaStream_t s = (cudaStream_t)stream;
+  GemmEpilogue e;
+  e.epi = EPI_STORE;
+  e.out = y;
+  e.ldo = (int)W->N;
+  GemmWorkspace ws;
+  ws.partial = reinterpret_cast<float*>(workspace);
+  ws.partial_floats = gemm_partial_floats(M);
+  const size_t pbytes = (ws.partial_floats * sizeof(float) + 255) & ~size_t(255);
+  ws.counters = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(workspace) + pbytes);
+  ws.counters_len = gemm_counters(W->N);
+  SD_CK(cudaMemsetAsync(ws.counters, 0, (size_t)ws.counters_len * sizeof(int32_t), s));
+  XMap xm;
+  const int rc = make_x_map(&xm, x, M, W->K, pad_rows(M));
+  if (rc) return rc;
+  return gemm_warp_launch(*W, x, xm, M, e, ws, nullptr, s, false, 0, nullptr, plane8);
 }

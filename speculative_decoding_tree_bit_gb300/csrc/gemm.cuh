@@ -89,11 +89,14 @@ int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, c
                 const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid = 0,
                 uint64_t* trace = nullptr);
 // The same on the warp-level kernel whatever the row count (M <= 64 in one
-// launch), with its own default grid.
+// launch), with its own default grid.  plane8 (W's nested 8-bit plane, W
+// with a contiguous exponent table, M <= 64): the product with the 8-bit
+// view, streaming the plane at 1 byte per weight.
 int gemm_warp_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
                      const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid = 0,
-                     uint64_t* trace = nullptr);
+                     uint64_t* trace = nullptr, const uint32_t* plane8 = nullptr);
 int gemm_warp_launch_grid(const w12_tensor& W, int M, int epi);
+int gemm_warp_grid(int M);  // CTAs of a warp-level launch of M rows
 
 // Descriptor of the packed words for the 2-D weight loads (one box = 8
 // strips x 1536 bytes).

@@ -14,12 +14,15 @@ constexpr int kThreads = (kNCW + 2) * 32;
 constexpr int kStripBytes = 1536;  // one strip x one super-tile (16 x 64 x 12 bit)
 
 // Shared-memory layout of the GEMM kernels (after 1024-byte alignment).
-template <int NT>
+// V8: the weights are the nested 8-bit plane (1024 bytes per strip and
+// super-tile instead of 1536), the freed shared memory goes to more stages.
+template <int NT, bool V8 = false>
 struct Cfg {
   static constexpr int MP = NT * 8;    // padded rows (tokens) per launch
   static constexpr int XB = MP * 128;  // x tile bytes per stage (64 columns of bf16)
-  static constexpr int WB = kRB * kStripBytes;
-  static constexpr int S = NT <= 1 ? 8 : NT <= 2 ? 7 : NT <= 8 ? 5 : 4;  // ring stages
+  static constexpr int WB = kRB * (V8 ? 1024 : kStripBytes);
+  static constexpr int S = V8 ? (NT <= 1 ? 11 : NT <= 2 ? 10 : NT <= 4 ? 7 : NT <= 8 ? 6 : 4)
+                              : (NT <= 1 ? 8 : NT <= 2 ? 7 : NT <= 8 ? 5 : 4);  // ring stages
   static constexpr int OFF_W = S * XB;
   static constexpr int OFF_FULL = OFF_W + S * WB;
   static constexpr int OFF_EMPTY = OFF_FULL + S * 8;
@@ -50,6 +53,8 @@ struct GemmParams {
   int32_t* status;
   uint64_t* trace;  // optional: [4][grid] device-clock stamps (start, first stage ready, last consumed, finished)
   int64_t G;        // CTAs sharing the units (<= the grid; 0: the grid); CTAs beyond it have no work
+  int view8;         // the weights are the nested 8-bit plane (1 KB per strip and super-tile)
+  uint32_t esc_mask;  // applied to an escape's bf16 bits: 0xFFFF, or 0xFFF0 for the 8-bit view
 };
 
 // n / d for 0 <= n and 0 < d: one 32-bit division when both fit (a 64-bit
@@ -96,6 +101,25 @@ __device__ __forceinline__ void decode(uint32_t w0, uint32_t w1, uint32_t w2, ui
     a2 = general_pair(w2 & 0x87FF87FFu, tab);
     a3 = general_pair((X & 0x07FF07FFu) | ((X << 4) & 0x80008000u), tab);
   }
+}
+
+// Two bytes of the nested 8-bit plane (bits 0..7 and 16..23: sign << 7 |
+// code << 3 | top mantissa bits) -> their bf16 view, as a bf16x2 fragment
+// register.
+__device__ __forceinline__ uint32_t view8_pair(uint32_t v, bool aff, uint32_t base2, const uint32_t* tab) {
+  if (aff) return (((v & 0x007F007Fu) << 4) + base2) | ((v & 0x00800080u) << 8);
+  const uint32_t e0 = lut_exp((v >> 3) & 15, tab), e1 = lut_exp((v >> 19) & 15, tab);
+  return ((v & 0x00070007u) << 4) | (e0 << 7) | (e1 << 23) | ((v & 0x00800080u) << 8);
+}
+
+// A fragment of one sub-tile from its two plane words: p0 holds (row g,
+// k), (g, k + 1), (g + 8, k), (g + 8, k + 1), p1 the same at k + 8.
+__device__ __forceinline__ void decode_view8(uint32_t p0, uint32_t p1, bool aff, uint32_t base2, const uint32_t* tab,
+                                             uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+  a0 = view8_pair(__byte_perm(p0, 0, 0x4140), aff, base2, tab);
+  a1 = view8_pair(__byte_perm(p0, 0, 0x4342), aff, base2, tab);
+  a2 = view8_pair(__byte_perm(p1, 0, 0x4140), aff, base2, tab);
+  a3 = view8_pair(__byte_perm(p1, 0, 0x4342), aff, base2, tab);
 }
 
 __device__ __forceinline__ uint32_t comp(const uint4& v, int j) {
@@ -266,12 +290,12 @@ __device__ __forceinline__ void esc_chunk_entries(const GemmParams& p, int tc, i
 // The escape warp's work for one GEMM; slot / phase follow the ring exactly
 // as the consumers do (it arrives on every stage's empty barrier).  eseg
 // counts the tiles produced.  Returns false on a failed wait (status set).
-template <int NT>
+template <int NT, bool V8 = false>
 __device__ __forceinline__ bool escape_segments(const GemmParams& p, const uint8_t* sx, uint64_t* full,
                                                 uint64_t* empty, int& slot, uint32_t& phase, float* corr,
                                                 uint64_t* corr_full, uint64_t* corr_empty, int& eseg,
                                                 volatile int* abort) {
-  using C = Cfg<NT>;
+  using C = Cfg<NT, V8>;
   constexpr int MP = C::MP;
   const int lane = threadIdx.x & 31;
   int64_t u0, u1;
@@ -336,7 +360,7 @@ __device__ __forceinline__ bool escape_segments(const GemmParams& p, const uint8
             v = __ldg(p.tile_esc + e);  // a chunk with more than 128 escapes
           }
           const int row = (v >> 6) & 127, kk = v & 63;
-          const float w = bf2f(v >> 16);
+          const float w = bf2f((v >> 16) & p.esc_mask);
           float* cr = corr + row * MP;
           for (int m = lane; m < mrows; m += 32) {
             const float xv = bf2f(
@@ -375,7 +399,7 @@ __device__ __forceinline__ bool escape_segments(const GemmParams& p, const uint8
 // Escape corrections of each segment come from the escape warp's tile (cseg
 // counts the tiles taken).  After a failed wait (status set) the warps run
 // on with stale data, so all of them keep meeting at the named barriers.
-template <int NT, bool AFFINE>
+template <int NT, bool AFFINE, bool V8 = false>
 __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, uint8_t* sw, uint64_t* full,
                                              uint64_t* empty, float* red_v, int* red_i, int* flag, int& slot,
                                              uint32_t& phase, const float* corr, uint64_t* corr_full,
@@ -426,7 +450,7 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
     // this segment's escape corrections
     if (!mbar_wait_or_abort(corr_full, (uint32_t)(cseg & 1), abort)) set_status(p.status, SD_TIMEOUT_AT(4));
     {
-      constexpr int MP = Cfg<NT>::MP;
+      constexpr int MP = Cfg<NT, V8>::MP;
       const int g = lane >> 2, q = lane & 3;
       const float* c0 = corr + (warp * 16 + g) * MP;
 #pragma unroll
@@ -511,15 +535,19 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
     if (stamps && threadIdx.x == 0 && n == u1 - u0) stamps[0] = globaltimer();
     const int strip = b * kRB + warp;
     if (strip < p.NS) {
-      const uint8_t* wsm = sw + slot * Cfg<NT>::WB + warp * kStripBytes;
+      const uint8_t* wsm = sw + slot * Cfg<NT, V8>::WB + warp * (V8 ? 1024 : kStripBytes);
       const uint4 W0 = *reinterpret_cast<const uint4*>(wsm + lane * 16);
       const uint4 W1 = *reinterpret_cast<const uint4*>(wsm + 512 + lane * 16);
-      const uint4 W2 = *reinterpret_cast<const uint4*>(wsm + 1024 + lane * 16);
-      const uint32_t xb = smem_u32(sx + slot * Cfg<NT>::XB);
+      uint4 W2 = W1;
+      if (!V8) W2 = *reinterpret_cast<const uint4*>(wsm + 1024 + lane * 16);
+      const uint32_t xb = smem_u32(sx + slot * Cfg<NT, V8>::XB);
 #pragma unroll
       for (int j = 0; j < 4; j++) {
         uint32_t a0, a1, a2, a3;
-        decode<AFFINE>(comp(W0, j), comp(W1, j), comp(W2, j), p.base2, p.tab, a0, a1, a2, a3);
+        if constexpr (V8)
+          decode_view8(comp(W0, j), comp(W1, j), AFFINE, p.base2, p.tab, a0, a1, a2, a3);
+        else
+          decode<AFFINE>(comp(W0, j), comp(W1, j), comp(W2, j), p.base2, p.tab, a0, a1, a2, a3);
         const int kchunk = 2 * j + ((lane >> 3) & 1);
         // even and odd sub-tiles accumulate into separate sets (shorter MMA chains)
         float(*A)[4] = (kDual && (j & 1)) ? acc2 : acc;
@@ -542,7 +570,7 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
-    if (++slot == Cfg<NT>::S) {
+    if (++slot == Cfg<NT, V8>::S) {
       slot = 0;
       phase ^= 1u;
     }
@@ -571,18 +599,18 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
           }
         }
         if (lane < 4) {
-          red_v[warp * Cfg<NT>::MP + nt * 8 + 2 * lane + c] = v;
-          red_i[warp * Cfg<NT>::MP + nt * 8 + 2 * lane + c] = i;
+          red_v[warp * Cfg<NT, V8>::MP + nt * 8 + 2 * lane + c] = v;
+          red_i[warp * Cfg<NT, V8>::MP + nt * 8 + 2 * lane + c] = i;
         }
       }
     bar_sync(1, kNCW * 32);
-    if (threadIdx.x < Cfg<NT>::MP) {
+    if (threadIdx.x < Cfg<NT, V8>::MP) {
       const int ml = threadIdx.x;
       float v = -INFINITY;
       int i = 0x7FFFFFFF;
       for (int w = 0; w < kNCW; w++) {
-        const float ov = red_v[w * Cfg<NT>::MP + ml];
-        const int oi = red_i[w * Cfg<NT>::MP + ml];
+        const float ov = red_v[w * Cfg<NT, V8>::MP + ml];
+        const int oi = red_i[w * Cfg<NT, V8>::MP + ml];
         if (ov > v || (ov == v && oi < i)) {
           v = ov;
           i = oi;

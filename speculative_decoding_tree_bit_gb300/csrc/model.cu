@@ -207,12 +207,24 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     ph.clear();
     return SD_OK;
   };
-  // one linear: the 8-bit view (plane) and the fused schedule's first q/k/v
-  // on the streaming kernel; else the warp-level kernel (skinny steps) or
-  // the tcgen05 kernel
+  // one linear: the 8-bit view (plane) on the warp-level kernel in its
+  // 8-bit mode (a contiguous exponent table; else the streaming kernel), the
+  // fused schedule's first q/k/v on the streaming kernel; else the
+  // warp-level kernel (skinny steps) or the tcgen05 kernel.  lm_part: the
+  // argmax partials the lm_head launch leaves (one per CTA of its grid)
+  int lm_part = gemm_grid(rows);
   auto gemm_one = [&](int kind, const w12_tensor& W, const uint16_t* x, const XMap* xm, const GemmEpilogue& e,
                       const uint32_t* plane) -> int {
+    if (plane && !fused && W.affine && xm) {
+      if ((rc = tbegin(kind, gemm_bytes(W, rows, e.epi) * (1.0 / 1.5)))) return rc;
+      if ((rc = gemm_warp_launch(W, x, *xm, rows, e, m->gws, m->status, s, pdl, 0, nullptr, plane))) return rc;
+      if ((rc = tend())) return rc;
+      launches++;
+      if (kind == SD_K_GEMM_LM_HEAD) lm_part = gemm_warp_grid(rows);
+      return SD_OK;
+    }
     if (plane || fused) {
+      if (kind == SD_K_GEMM_LM_HEAD) lm_part = stream_grid(rows);
       StreamPhaseDesc d;
       d.W = &W;
       d.view8 = plane;
@@ -244,7 +256,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     if (e != cudaSuccess) return cuda_fail(e, "delay");
   }
   XMap *mx = nullptr, *ma = nullptr, *mc = nullptr;
-  if (!fused && !io.view8) {
+  if (!fused) {
     if ((rc = get_map(m->map_xn, m->xn, m->max_rows, m->H, rows, &mx))) return rc;
     if ((rc = get_map(m->map_attn, m->attn, m->max_rows, (int64_t)m->Hq * m->hd, rows, &ma))) return rc;
     if ((rc = get_map(m->map_act, m->act, m->max_rows, m->I, rows, &mc))) return rc;
@@ -425,7 +437,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
   ac.R = io.R;
   ac.amax_val = m->amax_val;
   ac.amax_idx = m->amax_idx;
-  ac.n_part = (fused || io.view8) ? stream_grid(rows) : gemm_grid(rows);  // the lm_head's argmax partials
+  ac.n_part = fused ? stream_grid(rows) : lm_part;  // the lm_head's argmax partials
   ac.ld = m->max_rows;
   ac.req_ok = m->req_ok;
   ac.ctx_snap = m->ctx_snap;

@@ -171,24 +171,6 @@ __device__ __forceinline__ void cta_range(const StreamPhase& P, int64_t c, int64
   u1 = c < P.G ? sdiv((c + 1) * P.U, P.G) : P.U;
 }
 
-// Two bytes of the 8-bit plane (bits 0..7 and 16..23: sign << 7 | code << 3
-// | top mantissa bits) -> their bf16 view, as a bf16x2 fragment register.
-__device__ __forceinline__ uint32_t view8_pair(uint32_t v, bool aff, uint32_t base2, const uint32_t* tab) {
-  if (aff) return (((v & 0x007F007Fu) << 4) + base2) | ((v & 0x00800080u) << 8);
-  const uint32_t e0 = lut_exp((v >> 3) & 15, tab), e1 = lut_exp((v >> 19) & 15, tab);
-  return ((v & 0x00070007u) << 4) | (e0 << 7) | (e1 << 23) | ((v & 0x00800080u) << 8);
-}
-
-// A fragment of one sub-tile from its two plane words: p0 holds (row g,
-// k), (g, k + 1), (g + 8, k), (g + 8, k + 1), p1 the same at k + 8.
-__device__ __forceinline__ void decode_view8(uint32_t p0, uint32_t p1, bool aff, uint32_t base2, const uint32_t* tab,
-                                             uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-  a0 = view8_pair(__byte_perm(p0, 0, 0x4140), aff, base2, tab);
-  a1 = view8_pair(__byte_perm(p0, 0, 0x4342), aff, base2, tab);
-  a2 = view8_pair(__byte_perm(p1, 0, 0x4140), aff, base2, tab);
-  a3 = view8_pair(__byte_perm(p1, 0, 0x4342), aff, base2, tab);
-}
-
 __device__ __forceinline__ int ld_acquire_s32(const int32_t* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

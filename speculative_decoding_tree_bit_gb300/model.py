@@ -177,6 +177,21 @@ def linear_stream(p: Packed, x: torch.Tensor, plane8: torch.Tensor | None = None
     return y
 
 
+def linear_view8(p: Packed, x: torch.Tensor, plane8: torch.Tensor, ws: Workspace | None = None,
+                 stream=None) -> torch.Tensor:
+    """y = bf16(x V^T), V the nested 8-bit view of W (sd_w12_linear_view8,
+    M <= 64), streaming the plane at 1 byte per weight."""
+    M = x.shape[0]
+    need = int(lib().sd_w12_linear_view8_workspace(p.N, p.K, M))
+    if ws is None or ws.nbytes < need:
+        ws = Workspace(need, x.device)
+    y = torch.empty((M, p.N), dtype=torch.int16, device=x.device)
+    t = p.struct()
+    check(lib().sd_w12_linear_view8(ctypes.byref(t), plane8.data_ptr(), x.data_ptr(), M, y.data_ptr(), ws.ptr,
+                                    ws.nbytes, stream_ptr(stream)))
+    return y
+
+
 def set_tc_min_rows(rows: int) -> int:
     """Rows per launch from which the W12 GEMMs run on the tcgen05 kernel
     (process-wide; <= 0 restores the default).  Returns the value in force."""

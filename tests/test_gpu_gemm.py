@@ -207,3 +207,23 @@ def test_stream_rejects_rows_beyond_64(M):
     from speculative_decoding_tree_bit_gb300 import SdvError
     with pytest.raises(SdvError):
         M.linear_stream(p, M.to_device_u16(_x(65, 1024)))
+
+
+@pytest.mark.parametrize("Mrows", [1, 16, 40, 64])
+def test_view8_linear_matches_the_oracle_view(M, Mrows):
+    """sd_w12_linear_view8: the warp-level kernel in its 8-bit decode mode
+    (contiguous table) and the streaming kernel (general table) multiply by
+    oracle.w12_view8(W), escapes included."""
+    rng = np.random.default_rng(9)
+    exps = np.array([110, 112, 114, 116, 118, 120, 121, 122, 123, 124, 100, 102, 104, 106, 108, 90], np.uint32)
+    e = exps[rng.integers(0, exps.size, size=256 * 512)]
+    Wg = ((rng.integers(0, 2, size=e.size).astype(np.uint32) << 15) | (e << 7)
+          | rng.integers(0, 128, size=e.size).astype(np.uint32)).astype(np.uint16).reshape(256, 512)
+    for W in (wl.tiny().Wlm, Wg):
+        p = M.pack(M.to_device_u16(W), view8=True)
+        x = _x(Mrows, W.shape[1], 7)
+        y = M.linear_view8(p, M.to_device_u16(x), p.plane8).cpu().numpy().view(np.uint16)
+        ref = oracle.linear(x, oracle.w12_view8(W))
+        got = oracle.bf16_to_f64(y)
+        assert np.all(np.abs(got - ref) <= ATOL + RTOL * np.abs(ref))
+        assert np.mean(oracle.round_bf16(ref) == y) >= 0.99
