@@ -60,6 +60,10 @@ def parse():
     ap.add_argument("--nvtx", action="store_true", help="wrap the timed steps in the NVTX range 'sdv_step'")
     ap.add_argument("--probe", default=None, metavar="N,K,M",
                     help="time the fused W12 linear alone on an N x K tensor with M rows")
+    ap.add_argument("--probe-weights", default="normal", choices=["normal", "scaled"],
+                    help="--probe: i.i.d. N(0, 0.02) weights, or rows of different norms (wl.row_scaled)")
+    ap.add_argument("--probe-format", default="tensor", choices=["tensor", "channel"],
+                    help="--probe: per-tensor exponent table or per-channel bases (pack_channel)")
     ap.add_argument("--probe-kernel", default="gemm", choices=["gemm", "stream", "view8", "stream_view8"],
                     help="--probe: sd_w12_linear (warp-level / tcgen05), sd_w12_linear_stream, "
                          "sd_w12_linear_view8 (the nested 8-bit plane, 1 byte per weight), or the streaming "
@@ -149,9 +153,12 @@ def probe_arm(args):
     _build.build()
     tc_rows = Mdl.set_tc_min_rows(args.tc_min_rows)
     N, K, M = (int(v) for v in args.probe.split(","))
-    w = synthetic.normal_bf16(synthetic.key(args.seed, 4242), N * K, 0.02).reshape(N, K)
+    from synthetic import workloads as wl
+    w = (wl.row_scaled(args.seed + 4242, N, K) if args.probe_weights == "scaled" else
+         synthetic.normal_bf16(synthetic.key(args.seed, 4242), N * K, 0.02).reshape(N, K))
     view8 = args.probe_kernel in ("view8", "stream_view8")
-    p = Mdl.pack(Mdl.to_device_u16(w), view8=view8)
+    p = (Mdl.pack_channel(Mdl.to_device_u16(w)) if args.probe_format == "channel" else
+         Mdl.pack(Mdl.to_device_u16(w), view8=view8))
     del w
     wbytes = (p.plane8.numel() * p.plane8.element_size() + p.nbytes() - p.words.numel() * 4) if view8 else p.nbytes()
     # copies of the packed tensor that together exceed L2, cycled by the
@@ -200,7 +207,8 @@ def probe_arm(args):
     return {"probe": name[args.probe_kernel], "N": N, "K": K, "M": M,
             "tc_min_rows": tc_rows, "us_per_launch": us,
             "GBps": nbytes / (us * 1e-6) / 1e9, "frac_of_peak": nbytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"],
-            "peak_source": src, "bytes": nbytes, "escapes": p.n_escapes,
+            "peak_source": src, "bytes": nbytes, "escapes": p.n_escapes, "weights": args.probe_weights,
+            "format": args.probe_format,
             "l2": f"{n_copies} copies of the packed tensor cycled ({n_copies * wbytes / 2**20:.0f} MiB)"}
 
 

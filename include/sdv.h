@@ -137,6 +137,11 @@ typedef struct {
   uint8_t table[16];
   int32_t n_table;
   int32_t affine;
+  /* device [N] or null.  Non-null: a per-channel tensor (w12c_pack_*): row n
+   * decodes code c < 15 as exponent row_base[n] + c and table / n_table are
+   * unused; affine = 1 when every base is at most 239 (the GEMM decodes
+   * such tensors; others pack, unpack and round-trip but do not multiply). */
+  const uint8_t* row_base;
 } w12_tensor;
 
 /* Number of u32 words of a packed N x K tensor (N*K*3/8). */
@@ -184,7 +189,8 @@ int w12_pack_tile_index(const w12_tensor* t, uint32_t* tile_ptr, uint32_t* tile_
 /* [W12] y[m][n] = bf16( sum_k x[m][k] * W[n][k] ), fp32 accumulation, with
  * the weights decoded in registers straight from the packed words (they
  * cross HBM once, 1.5 bytes each) and the escapes added from the escape tile
- * index (W->tile_ptr / tile_esc must be set).
+ * index (W->tile_ptr / tile_esc must be set).  A per-channel tensor
+ * (W->row_base set, affine) runs on the warp-level kernel, M <= 64.
  * x: bf16 [M][K] row-major, 16-byte aligned; y: bf16 [M][N] row-major.
  * 1 <= M <= 256.  workspace: caller-owned device scratch of
  * sd_w12_linear_workspace(N, K, M) bytes, 256-byte aligned; it needs no
@@ -285,6 +291,21 @@ int sd_accept(const int32_t* tokens, const int32_t* parents, const int32_t* argm
               void* stream);
 
 /* ------------------------------------------ W12 with per-channel bases -- */
+/* Device packer of the per-channel format (the format of w12c_pack_host,
+ * bit for bit; words in the per-tensor layout).  w: bf16 [N][K] device;
+ * row_src (device [N] or null): packed row n takes source row row_src[n]
+ * (the fused tensors' row orders).  w12c_pack_analyze writes each packed
+ * row's base (device uint8 [N]) and the side list's CSR row pointers
+ * (device u32 [N+1]), fills meta (n_escapes; affine = 1 when every base is
+ * at most 239; n_table 0) and synchronises `stream`.  w12c_pack_encode then
+ * writes the words (w12_words_count) and the side list (esc_idx / esc_val
+ * [meta->n_escapes], flat index order).  Errors: SD_ERR_INVALID_ARG,
+ * SD_ERR_UNSUPPORTED (N % 16, K % 64, N*K < 2^32), SD_ERR_CUDA. */
+int w12c_pack_analyze(const uint16_t* w, const int32_t* row_src, int64_t N, int64_t K, uint8_t* base,
+                      uint32_t* row_ptr, w12_meta* meta, void* stream);
+int w12c_pack_encode(const uint16_t* w, const int32_t* row_src, int64_t N, int64_t K, const uint8_t* base,
+                     const uint32_t* row_ptr, uint32_t* words, uint32_t* esc_idx, uint16_t* esc_val, void* stream);
+
 /* Per-output-channel W12 ("SpecPilot: AI Agent Framework Boosts Speculative
  * Decoding 10.87x", "(1) W12: Lossless 12-bit Weight Format", read
  * literally: a 4-bit exponent offset within each output channel), offline
@@ -353,7 +374,8 @@ uint32_t w12_crc32(const void* data, size_t n);
 /* Write *t to path; t's array pointers are HOST pointers here (sizes as
  * above; the escape arrays may be NULL when n_escapes == 0).  Errors:
  * SD_ERR_INVALID_ARG (null pointer, shape outside N%16, K%64, N*K < 2^32),
- * SD_ERR_IO (open or write failed; the file may be partial). */
+ * SD_ERR_UNSUPPORTED (a per-channel tensor: the file holds per-tensor
+ * tables only), SD_ERR_IO (open or write failed; the file may be partial). */
 int w12_save(const char* path, const w12_tensor* t);
 
 /* Read and check path's header (magic, version, header CRC, section sizes

@@ -36,7 +36,7 @@ class W12Meta(ctypes.Structure):
 class W12Tensor(ctypes.Structure):
     _fields_ = [("N", i64), ("K", i64), ("words", vp), ("esc_idx", vp), ("esc_val", vp), ("row_ptr", vp),
                 ("tile_ptr", vp), ("tile_esc", vp), ("n_escapes", i64), ("table", u8 * 16), ("n_table", i32),
-                ("affine", i32)]
+                ("affine", i32), ("row_base", vp)]
 
 
 class ModelConfig(ctypes.Structure):
@@ -93,6 +93,8 @@ _SIGS = {
     "w12_plane8_pack_host": (ctypes.c_int, [vp, i64, i64, vp, i32, vp]),
     "w12_plane8_unpack_host": (ctypes.c_int, [vp, i64, i64, vp, i32, vp, vp, i64, vp]),
     "w12c_pack_host": (ctypes.c_int, [vp, i64, i64, vp, vp, vp, vp, i64, vp, P(i64)]),
+    "w12c_pack_analyze": (ctypes.c_int, [vp, vp, i64, i64, vp, vp, P(W12Meta), vp]),
+    "w12c_pack_encode": (ctypes.c_int, [vp, vp, i64, i64, vp, vp, vp, vp, vp, vp]),
     "w12c_unpack_host": (ctypes.c_int, [vp, vp, i64, i64, vp, vp, i64, vp]),
     "w12_crc32": (ctypes.c_uint32, [vp, ctypes.c_size_t]),
     "w12_save": (ctypes.c_int, [ctypes.c_char_p, P(W12Tensor)]),

@@ -41,7 +41,7 @@ namespace sdv {
 template <int NT>
 constexpr int ctas_per_sm() { return NT <= 4 ? 2 : 1; }
 
-template <int NT, bool AFFINE, bool V8 = false>
+template <int NT, bool AFFINE, bool V8 = false, bool CH = false>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
     k_w12_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap xmap,
                const __grid_constant__ CUtensorMap wmap) {
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<NT>())
   if (p.trace && threadIdx.x == 0) p.trace[blockIdx.x] = globaltimer();
   int slot = 0, cseg = 0;
   uint32_t phase = 0;
-  consume_gemm<NT, AFFINE, V8>(p, sx, sw, full, empty, red_v, red_i, flag, slot, phase, corr, corr_full, corr_empty,
+  consume_gemm<NT, AFFINE, V8, CH>(p, sx, sw, full, empty, red_v, red_i, flag, slot, phase, corr, corr_full, corr_empty,
                            cseg, abort, p.trace ? p.trace + G + blockIdx.x : nullptr, G);
   if (p.trace) {
     bar_sync(1, kNCW * 32);
@@ -307,17 +307,17 @@ int make_w8_map(CUtensorMap* map, const uint32_t* plane, int64_t N, int64_t K) {
   return SD_OK;
 }
 
-template <int NT, bool AFF, bool V8 = false>
+template <int NT, bool AFF, bool V8 = false, bool CH = false>
 static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, const CUtensorMap& wmap, cudaStream_t s,
                              bool pdl, int grid) {
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(k_w12_gemm<NT, AFF, V8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NT, V8>::SMEM);
+    const cudaError_t e = cudaFuncSetAttribute(k_w12_gemm<NT, AFF, V8, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               Cfg<NT, V8>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch(k_w12_gemm<NT, AFF, V8>, dim3(grid), dim3(kThreads), Cfg<NT, V8>::SMEM, s, pdl, p, map, wmap);
+  return launch(k_w12_gemm<NT, AFF, V8, CH>, dim3(grid), dim3(kThreads), Cfg<NT, V8>::SMEM, s, pdl, p, map, wmap);
 }
 
 int make_gemm_params(GemmParams* out, const w12_tensor& W, const uint16_t* x, int M, const GemmEpilogue& epi,
@@ -344,6 +344,7 @@ int make_gemm_params(GemmParams* out, const w12_tensor& W, const uint16_t* x, in
   p.esc_slot = W.affine ? ldexpf(1.0f, (int)base + 15 - 127) : 0.0f;
   p.view8 = 0;
   p.esc_mask = 0xFFFFu;
+  p.row_base = W.row_base;
   if (W.n_escapes > 0 && (!W.tile_ptr || !W.tile_esc)) {
     set_error("gemm: the tensor has escapes but no escape tile index (w12_pack_tile_index)");
     return SD_ERR_INVALID_ARG;
@@ -362,7 +363,8 @@ int make_gemm_params(GemmParams* out, const w12_tensor& W, const uint16_t* x, in
 
 int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
                 const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid, uint64_t* trace) {
-  if (gemm_use_tc(M)) return gemm_tc_launch(W, x, xm.rows_total, M, epi, ws, status, s, pdl);
+  // a per-channel tensor has the warp-level kernel's decode only
+  if (gemm_use_tc(M) && !W.row_base) return gemm_tc_launch(W, x, xm.rows_total, M, epi, ws, status, s, pdl);
   return gemm_warp_launch(W, x, xm, M, epi, ws, status, s, pdl, grid, trace);
 }
 
@@ -400,6 +402,23 @@ int gemm_warp_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int
   CUtensorMap wmap;
   const int wrc = plane8 ? make_w8_map(&wmap, plane8, W.N, W.K) : make_w_map(&wmap, W);
   if (wrc) return wrc;
+  if (W.row_base) {
+    // a per-channel tensor: the warp-level kernel's per-row decode (M <= 64,
+    // every base at most 239)
+    if (!W.affine || M > 64 || plane8) {
+      set_error("gemm: a per-channel tensor multiplies on the warp-level kernel (M <= 64, bases <= 239, no 8-bit view)");
+      return SD_ERR_UNSUPPORTED;
+    }
+    cudaError_t e;
+    switch (NT) {
+      case 1: e = launch_nt<1, true, false, true>(p, xm.map, wmap, s, pdl, grid); break;
+      case 2: e = launch_nt<2, true, false, true>(p, xm.map, wmap, s, pdl, grid); break;
+      case 4: e = launch_nt<4, true, false, true>(p, xm.map, wmap, s, pdl, grid); break;
+      default: e = launch_nt<8, true, false, true>(p, xm.map, wmap, s, pdl, grid); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "k_w12_gemm (per-channel) launch");
+    return SD_OK;
+  }
   if (plane8) {
     cudaError_t e;
     switch (NT) {

@@ -55,6 +55,7 @@ struct GemmParams {
   int64_t G;        // CTAs sharing the units (<= the grid; 0: the grid); CTAs beyond it have no work
   int view8;         // the weights are the nested 8-bit plane (1 KB per strip and super-tile)
   uint32_t esc_mask;  // applied to an escape's bf16 bits: 0xFFFF, or 0xFFF0 for the 8-bit view
+  const uint8_t* row_base;  // per-channel bases [N] (null: the tensor's table)
 };
 
 // n / d for 0 <= n and 0 < d: one 32-bit division when both fit (a 64-bit
@@ -120,6 +121,17 @@ __device__ __forceinline__ void decode_view8(uint32_t p0, uint32_t p1, bool aff,
   a1 = view8_pair(__byte_perm(p0, 0, 0x4342), aff, base2, tab);
   a2 = view8_pair(__byte_perm(p1, 0, 0x4140), aff, base2, tab);
   a3 = view8_pair(__byte_perm(p1, 0, 0x4342), aff, base2, tab);
+}
+
+// Per-channel decode (contiguous window per row): a0 and a2 hold row g of
+// the strip, a1 and a3 row g + 8, so each takes its own row's base.
+__device__ __forceinline__ void decode_rows(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t b2lo, uint32_t b2hi,
+                                            uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+  const uint32_t X = ((w0 >> 11) & 0x000F000Fu) | ((w1 >> 7) & 0x00F000F0u) | ((w2 >> 3) & 0x0F000F00u);
+  a0 = (w0 & 0x87FF87FFu) + b2lo;
+  a1 = (w1 & 0x87FF87FFu) + b2hi;
+  a2 = (w2 & 0x87FF87FFu) + b2lo;
+  a3 = ((X & 0x07FF07FFu) + b2hi) | ((X << 4) & 0x80008000u);
 }
 
 __device__ __forceinline__ uint32_t comp(const uint4& v, int j) {
@@ -361,12 +373,16 @@ __device__ __forceinline__ bool escape_segments(const GemmParams& p, const uint8
           }
           const int row = (v >> 6) & 127, kk = v & 63;
           const float w = bf2f((v >> 16) & p.esc_mask);
+          // the value the slot decodes to: 2^(base + 15 - 127), per row for
+          // a per-channel tensor
+          const float slot_v = p.row_base ? __uint_as_float((uint32_t)(p.row_base[(int64_t)cb * 128 + row] + 15) << 23)
+                                          : p.esc_slot;
           float* cr = corr + row * MP;
           for (int m = lane; m < mrows; m += 32) {
             const float xv = bf2f(
                 *reinterpret_cast<const uint16_t*>(xs + m * 128 + (((kk >> 3) ^ (m & 7)) << 4) + (kk & 7) * 2));
             const float a = fmaf(w, xv, cr[m]);
-            cr[m] = fmaf(-p.esc_slot, xv, a);
+            cr[m] = fmaf(-slot_v, xv, a);
           }
         }
       }
@@ -399,7 +415,7 @@ __device__ __forceinline__ bool escape_segments(const GemmParams& p, const uint8
 // Escape corrections of each segment come from the escape warp's tile (cseg
 // counts the tiles taken).  After a failed wait (status set) the warps run
 // on with stale data, so all of them keep meeting at the named barriers.
-template <int NT, bool AFFINE, bool V8 = false>
+template <int NT, bool AFFINE, bool V8 = false, bool CH = false>
 __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, uint8_t* sw, uint64_t* full,
                                              uint64_t* empty, float* red_v, int* red_i, int* flag, int& slot,
                                              uint32_t& phase, const float* corr, uint64_t* corr_full,
@@ -519,6 +535,7 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
 
   zero();
   int cur_b = -1, seg_t0 = 0;
+  uint32_t b2lo = 0, b2hi = 0;  // per-channel bases of the lane's rows (CH)
   bool ok = true;
   int b = u1 > u0 ? (int)udiv(u0, KT) : 0, t = u1 > u0 ? (int)(u0 - (int64_t)b * KT) : 0;
   for (int64_t n = u1 - u0; n > 0; --n) {
@@ -527,6 +544,14 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
       cur_b = b;
       seg_t0 = t;
       zero();
+      if constexpr (CH) {
+        // the bases of this lane's two rows of its strip, shifted into both
+        // halves' exponent fields
+        const int64_t r0 = (int64_t)(b * kRB + warp) * 16 + (lane >> 2);
+        const uint32_t blo = r0 < p.N ? p.row_base[r0] : 0u, bhi = r0 + 8 < p.N ? p.row_base[r0 + 8] : 0u;
+        b2lo = (blo << 7) | (blo << 23);
+        b2hi = (bhi << 7) | (bhi << 23);
+      }
     }
     if (!mbar_wait_or_abort(&full[slot], phase, abort)) {
       set_status(p.status, SD_TIMEOUT_AT(5));
@@ -546,6 +571,8 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
         uint32_t a0, a1, a2, a3;
         if constexpr (V8)
           decode_view8(comp(W0, j), comp(W1, j), AFFINE, p.base2, p.tab, a0, a1, a2, a3);
+        else if constexpr (CH)
+          decode_rows(comp(W0, j), comp(W1, j), comp(W2, j), b2lo, b2hi, a0, a1, a2, a3);
         else
           decode<AFFINE>(comp(W0, j), comp(W1, j), comp(W2, j), p.base2, p.tab, a0, a1, a2, a3);
         const int kchunk = 2 * j + ((lane >> 3) & 1);

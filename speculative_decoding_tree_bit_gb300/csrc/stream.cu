@@ -119,6 +119,10 @@ int stream_launch(const StreamPhaseDesc* ph, int n, int M, const StreamWorkspace
       set_error("stream: the tensor has escapes but no escape tile index (w12_pack_tile_index)");
       return SD_ERR_INVALID_ARG;
     }
+    if (W.row_base) {
+      set_error("stream: per-channel tensors multiply on the warp-level kernel (sd_w12_linear)");
+      return SD_ERR_UNSUPPORTED;
+    }
     if (d.dep >= i || d.dep < -1 || (d.dep_fine && d.dep < 0)) {
       set_error("stream: a phase may depend on an earlier phase only");
       return SD_ERR_INVALID_ARG;

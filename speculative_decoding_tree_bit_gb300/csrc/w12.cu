@@ -270,7 +270,7 @@ struct TableArg {
 };
 
 __global__ void k_unpack(const uint32_t* __restrict__ words, int64_t N, int64_t K, TableArg tab,
-                         uint16_t* __restrict__ out) {
+                         const uint8_t* __restrict__ row_base, uint16_t* __restrict__ out) {
   const int64_t KT = K / 64;
   const int64_t total = (N / 16) * KT * 128;
   for (int64_t id = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; id < total; id += (int64_t)gridDim.x * blockDim.x) {
@@ -298,7 +298,7 @@ __global__ void k_unpack(const uint32_t* __restrict__ words, int64_t N, int64_t 
               (((W[2] >> (11 + 16 * h)) & 0xF) << 8);
         }
         const uint32_t code = (f >> 7) & 15;
-        const uint32_t e = code == 15 ? 0u : tab.t[code];
+        const uint32_t e = code == 15 ? 0u : row_base ? (row_base[rows[p]] + code) & 0xFF : tab.t[code];
         const uint32_t b = ((f >> 11) << 15) | (e << 7) | (f & 0x7F);
         pairbits |= b << (16 * h);
       }
@@ -429,7 +429,8 @@ extern "C" int w12_unpack(const w12_tensor* t, uint16_t* w_out, void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
   TableArg tab;
   for (int i = 0; i < 16; i++) tab.t[i] = i < t->n_table ? t->table[i] : 0;
-  k_unpack<<<grid_for((t->N / 16) * (t->K / 64) * 128, 256), 256, 0, s>>>(t->words, t->N, t->K, tab, w_out);
+  k_unpack<<<grid_for((t->N / 16) * (t->K / 64) * 128, 256), 256, 0, s>>>(t->words, t->N, t->K, tab, t->row_base,
+                                                                           w_out);
   SD_CK(cudaGetLastError());
   if (t->n_escapes > 0) {
     k_scatter_escapes<<<grid_for(t->n_escapes, 256), 256, 0, s>>>(t->esc_idx, t->esc_val, t->n_escapes, w_out);

@@ -170,6 +170,10 @@ extern "C" int w12_save(const char* path, const w12_tensor* t) {
     set_error("w12_save: bad argument");
     return SD_ERR_INVALID_ARG;
   }
+  if (t->row_base) {
+    set_error("w12_save: the file format holds per-tensor tables only (not a per-channel tensor)");
+    return SD_ERR_UNSUPPORTED;
+  }
   Header h{};
   std::memcpy(h.magic, kMagic, sizeof kMagic);
   h.version = kVersion;

@@ -53,6 +53,7 @@ class Packed:
         t.table = self.meta.table
         t.n_table = self.meta.n_table
         t.affine = self.meta.affine
+        t.row_base = _ptr(getattr(self, "row_base", None))
         return t
 
     def copy(self) -> "Packed":
@@ -60,6 +61,8 @@ class Packed:
         cl = lambda t: None if t is None else t.clone()
         q = Packed(self.meta, cl(self.words), cl(self.esc_idx), cl(self.esc_val), cl(self.row_ptr), cl(self.tile_ptr),
                    cl(self.tile_esc))
+        if getattr(self, "row_base", None) is not None:
+            q.row_base = self.row_base.clone()
         if getattr(self, "plane8", None) is not None:
             q.plane8 = self.plane8.clone()
         return q
@@ -95,6 +98,37 @@ def pack(w: torch.Tensor, row_src: np.ndarray | None = None, stream=None, view8:
     if view8:
         p.plane8 = torch.empty(int(lib().w12_plane8_words_count(N, K)), dtype=torch.int32, device=dev)
         check(lib().w12_plane8_pack(w.data_ptr(), _ptr(rs), ctypes.byref(meta), p.plane8.data_ptr(), s))
+    torch.cuda.synchronize()
+    return p
+
+
+def pack_channel(w: torch.Tensor, row_src: np.ndarray | None = None, stream=None) -> Packed:
+    """Pack a bf16 device tensor [N][K] in the per-channel format
+    (w12c_pack_analyze / w12c_pack_encode): a base exponent per output row
+    (p.row_base), the per-tensor word layout, the same side list."""
+    assert w.is_cuda and w.dim() == 2 and w.element_size() == 2 and w.is_contiguous()
+    N, K = w.shape
+    s = stream_ptr(stream)
+    dev = w.device
+    rs = None if row_src is None else _i32(row_src, dev)
+    base = torch.empty(N, dtype=torch.uint8, device=dev)
+    row_ptr = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    meta = W12Meta()
+    check(lib().w12c_pack_analyze(w.data_ptr(), _ptr(rs), N, K, base.data_ptr(), row_ptr.data_ptr(),
+                                  ctypes.byref(meta), s))
+    words = torch.empty(int(lib().w12_words_count(N, K)), dtype=torch.int32, device=dev)
+    ne = max(int(meta.n_escapes), 1)
+    esc_idx = torch.empty(ne, dtype=torch.int32, device=dev)
+    esc_val = torch.empty(ne, dtype=torch.int16, device=dev)
+    check(lib().w12c_pack_encode(w.data_ptr(), _ptr(rs), N, K, base.data_ptr(), row_ptr.data_ptr(), words.data_ptr(),
+                                 esc_idx.data_ptr(), esc_val.data_ptr(), s))
+    p = Packed(meta, words, esc_idx, esc_val, row_ptr)
+    p.row_base = base
+    p.tile_ptr = torch.empty(int(lib().w12_tile_ptr_count(N, K)), dtype=torch.int32, device=dev)
+    p.tile_esc = torch.empty(ne, dtype=torch.int32, device=dev)
+    t = p.struct()
+    check(lib().w12_pack_tile_index(ctypes.byref(t), p.tile_ptr.data_ptr(), p.tile_esc.data_ptr(), s))
+    p.plane8 = None
     torch.cuda.synchronize()
     return p
 

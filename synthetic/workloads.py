@@ -414,6 +414,18 @@ class GdnInputs:
     S: np.ndarray
 
 
+def row_scaled(seed: int, N: int, K: int, spread: float = 2.0) -> np.ndarray:
+    """bf16 bits [N][K]: row n ~ N(0, (0.02 * 2^u_n)^2), u_n uniform in
+    [-spread, spread] (output channels of different norms, the case a
+    per-channel exponent base is for)."""
+    u = uniform_int(key(seed, 2), N, 0, 1 << 20) / float(1 << 20) * 2 * spread - spread
+    W = np.empty((N, K), dtype=np.uint16)
+    k = key(seed, 3)
+    for n in range(N):
+        normal_bf16(k, K, 0.02 * 2.0 ** u[n], offset=n * K, out=W[n])
+    return W
+
+
 def gdn_inputs(seed: int, Ms, max_depth: int, nh: int, alpha_lo: float = 0.8, s_sigma: float = 0.01) -> GdnInputs:
     R = len(Ms)
     cu = np.zeros(R + 1, dtype=np.int32)
