@@ -259,6 +259,20 @@ int sd_w12_linear_static(const w12_tensor* W, const uint16_t* x, int32_t M, uint
  * concurrent GEMM calls. */
 int32_t sd_gemm_set_tc_min_rows(int32_t rows);
 
+/* Finish of row blocks split over a whole number k (2..16) of CTAs in the
+ * warp-level GEMM (q/k/v, O, down and other GEMMs with few row blocks): with
+ * enable = 1 the k CTAs of a block run as one thread-block
+ * cluster, stage their fp32 partials in shared memory and the first of them
+ * sums the others' through distributed shared memory in CTA order before
+ * the epilogue; with 0 (the default) they leave the partials in the
+ * workspace and the last to finish sums them (an acq_rel ticket, measured
+ * faster on GB300 at every shape tried).  The sums are the same up
+ * to the sign of an all-zero sum.  A cluster size the GPU cannot schedule
+ * falls back to the workspace path.  enable < 0 only queries.  Returns the
+ * setting in force.  Process-wide; not thread-safe against concurrent GEMM
+ * calls; a model re-captures its step graphs. */
+int32_t sd_gemm_set_cluster_finish(int32_t enable);
+
 /* Prefix key splits per (request, kv head, 64-row chunk) of the verify
  * step's attention ("SpecPilot ...", tree attention: the committed prefix
  * is split over CTAs and the splits' softmax states are merged; the tree's

@@ -56,6 +56,10 @@ struct GemmParams {
   int view8;         // the weights are the nested 8-bit plane (1 KB per strip and super-tile)
   uint32_t esc_mask;  // applied to an escape's bf16 bits: 0xFFFF, or 0xFFF0 for the 8-bit view
   const uint8_t* row_base;  // per-channel bases [N] (null: the tensor's table)
+  // > 1: the launch is in clusters of cluster_k CTAs, one cluster per row
+  // block, each CTA one k-range of it; the block is finished through
+  // distributed shared memory instead of partials in global memory
+  int cluster_k;
 };
 
 // n / d for 0 <= n and 0 < d: one 32-bit division when both fit (a 64-bit
@@ -480,7 +484,42 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
     __syncwarp();
     if (lane == 0) mbar_arrive(corr_empty);
     cseg++;
-    if (!(t0 == 0 && t1 == KT)) {
+    if (!(t0 == 0 && t1 == KT) && p.cluster_k > 1) {
+      // the cluster's CTAs are the block's contributors, in CTA order: each
+      // stages its partial in its own shared memory (the weight ring is idle
+      // once the segment's last stage is consumed), the leader (rank 0, the
+      // first contributor) adds the others' through distributed shared
+      // memory in rank order - the sum the global path forms - and runs the
+      // epilogue; the second barrier keeps every CTA's shared memory alive
+      // until the leader has read it.  The staging area overlaps the first
+      // ring slot, which another consumer warp may still be reading for its
+      // last stage: every consumer warp is past its last stage first.
+      bar_sync(1, kNCW * 32);
+      float* stage = reinterpret_cast<float*>(sw) + ((warp * NT) * 32 + lane) * 4;
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+        *reinterpret_cast<float4*>(stage + nt * 128) = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+      cluster_sync_all();
+      const bool leader = cluster_rank() == 0;
+      if (leader) {
+        const uint32_t mine = smem_u32(stage);
+        for (int r = 1; r < p.cluster_k; r++) {
+          const uint32_t remote = cluster_map(mine, (uint32_t)r);
+          float4 v[NT];
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++) v[nt] = ld_cluster_f4(remote + nt * 128 * 4);
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++) {
+            acc[nt][0] += v[nt].x;
+            acc[nt][1] += v[nt].y;
+            acc[nt][2] += v[nt].z;
+            acc[nt][3] += v[nt].w;
+          }
+        }
+      }
+      cluster_sync_all();
+      if (!leader) return;
+    } else if (!(t0 == 0 && t1 == KT)) {
       const int slot_id = (b == first_b) ? 0 : 1;
       float* dst = partial_ptr(blockIdx.x, slot_id);
 #pragma unroll

@@ -80,6 +80,42 @@ def test_full_size_8b(M, name, Mrows):
     _check(M, W, _x(Mrows, W.shape[1], 4), rows=rows)
 
 
+@pytest.fixture()
+def cluster_finish(M):
+    """Split row blocks finished through thread-block clusters (default:
+    workspace partials and a ticket), restored afterwards."""
+    M.set_cluster_finish(True)
+    yield M
+    M.set_cluster_finish(False)
+
+
+@pytest.mark.parametrize("name,Mrows", [("wq", 16), ("wo", 1), ("wo", 8), ("w_down", 16), ("w_down", 32)])
+def test_cluster_finish_8b(cluster_finish, name, Mrows):
+    """The cluster finish sums the same partials in the same order as the
+    ticket path: bit-identical outputs, and within tolerance of the oracle on
+    sampled rows.  down (224 k-tiles over 9 CTAs per block) wraps the weight
+    ring, so a CTA's last stages sit in the slot the partials are staged in."""
+    M = cluster_finish
+    sh = wl.SHAPES["8b"]
+    W = wl.SyntheticWeights(sh, 0).layer(0, name)
+    x = _x(Mrows, W.shape[1], 6)
+    p = M.pack(M.to_device_u16(W))
+    xd = M.to_device_u16(x)
+    y_cl = M.linear(p, xd).cpu()
+    M.set_cluster_finish(False)
+    y_ws = M.linear(p, xd).cpu()
+    M.set_cluster_finish(True)
+    assert torch.equal(y_cl, y_ws)
+    rows = np.sort(np.random.default_rng(1).choice(W.shape[0], 512, replace=False))
+    _check(M, W, x, rows=rows, p=p)
+
+
+@pytest.mark.parametrize("N,K,Mrows", [(4000, 512, 64), (2048, 1024, 8), (1024, 4096, 3)])
+def test_cluster_finish_ragged(cluster_finish, N, K, Mrows):
+    W = synthetic.normal_bf16(synthetic.key(3, N * 5 + K), N * K, 0.02).reshape(N, K)
+    _check(cluster_finish, W, _x(Mrows, K, 2))
+
+
 def test_repeat_calls_are_deterministic_with_dirty_workspace(M):
     t = wl.tiny()
     p = M.pack(M.to_device_u16(t.W1))
