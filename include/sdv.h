@@ -273,6 +273,19 @@ int32_t sd_gemm_set_tc_min_rows(int32_t rows);
  * calls; a model re-captures its step graphs. */
 int32_t sd_gemm_set_cluster_finish(int32_t enable);
 
+/* Finish of row blocks split over a whole number k (2..16) of CTAs in the
+ * warp-level GEMM (q/k/v, O, down: the launches with few row blocks), when
+ * the cluster finish is off: with enable = 1 the GEMM's CTAs
+ * leave their fp32 partials in the workspace and return, and a second
+ * kernel on the same stream (one warp per 16-row strip) sums them in CTA
+ * order and runs the epilogue - every contributor's partial in flight at
+ * once, no ticket; with 0 (the default: the extra kernel boundary measured
+ * slower on GB300) the last CTA of a block to finish sums them inside the
+ * GEMM (an acq_rel ticket).  The sums are identical.  enable < 0 only
+ * queries.  Returns the setting in force.  Process-wide; not thread-safe
+ * against concurrent GEMM calls; a model re-captures its step graphs. */
+int32_t sd_gemm_set_deferred_finish(int32_t enable);
+
 /* Prefix key splits per (request, kv head, 64-row chunk) of the verify
  * step's attention ("SpecPilot ...", tree attention: the committed prefix
  * is split over CTAs and the splits' softmax states are merged; the tree's

@@ -194,12 +194,19 @@ void gemm_set_tc_min_rows(int rows) { g_tc_min_rows = rows > 0 ? rows : kTcMinRo
 
 static int warp_grid(int M) { return (nt_of(M) <= 4 ? 2 : 1) * num_sms(); }
 
+// Row blocks split over a whole number of CTAs may finish in a separate
+// kernel (sd_gemm_set_deferred_finish); off by default: the extra kernel
+// boundary measured slower than the in-kernel finisher (8B-class step 4.75
+// vs 4.29 ms at 16 rows).
+static bool g_defer_finish = false;
+
 // Row blocks split over a whole number of CTAs may finish through a
 // thread-block cluster (sd_gemm_set_cluster_finish); off by default: the
 // cluster launch measured slower than the workspace ticket at every shape
 // (O 24.0 vs 20.7 us, down 41.9 vs 32.8 us at 16 rows).
 static bool g_cluster_finish = false;
 int gemm_warp_grid(int M) { return warp_grid(M); }
+int gemm_finish_mode() { return (g_cluster_finish ? 2 : 0) | (g_defer_finish ? 1 : 0); }
 
 int gemm_grid(int M) { return gemm_use_tc(M) ? num_sms() : warp_grid(M); }
 
@@ -368,6 +375,76 @@ static int cluster_for(const GemmParams& p, int grid) {
   return k;
 }
 
+// Split-K finish of a deferred launch (GemmParams::defer): one warp per
+// 16-row strip sums the fragments the row block's contributors left in their
+// partial slots, in CTA order and in the in-kernel finisher's grouping (the
+// same sums, up to nothing), and runs the epilogue.  Every contributor's
+// loads are in flight at once (one round trip where the in-kernel finisher
+// takes one per batch, after its release / acquire ticket).  It follows the
+// GEMM on the stream; under programmatic dependent launch it starts early
+// and waits for the GEMM's completion.
+template <int NT>
+__global__ void __launch_bounds__(128) k_gemm_finish(const __grid_constant__ GemmParams p) {
+  pdl_launch();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x >> 1;
+  const int w = (blockIdx.x & 1) * 4 + warp;  // strip within the block
+  const int strip = b * kRB + w;
+  pdl_wait();
+  if (strip >= p.NS) return;
+  const int64_t G = unit_ctas(p);
+  const int KT = p.KT;
+  const int64_t c_first = udiv(((int64_t)b * KT + 1) * G - 1, p.U);
+  const int64_t c_last = udiv(((int64_t)(b + 1) * KT) * G - 1, p.U);
+  constexpr int kLoad = NT <= 2 ? 16 : NT <= 4 ? 8 : 4;  // contributors in flight (a launch has at most 16)
+  constexpr int kB = finish_batch(NT);
+  static_assert(kLoad % kB == 0, "loads cover whole batches");
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+    for (int c = 0; c < 4; c++) acc[nt][c] = 0.f;
+  for (int64_t c0 = c_first; c0 <= c_last; c0 += kLoad) {
+    float4 v[kLoad][NT];
+#pragma unroll
+    for (int u = 0; u < kLoad; u++) {
+      const int64_t c = c0 + u;
+      const int64_t cs = udiv(c * p.U, G), ce = udiv((c + 1) * p.U, G);
+      const bool use = c <= c_last && cs != ce;
+      const int64_t sid = use && cs < (int64_t)b * KT ? 1 : 0;  // the range began in an earlier block
+      const float* src = p.partial + (((use ? c : 0) * 2 + sid) * kRB + w) * NT * 128 + lane * 4;
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+        v[u][nt] = use ? __ldcg(reinterpret_cast<const float4*>(src + nt * 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // the in-kernel finisher's batches start at c_first in steps of kB and
+    // add every slot of a batch (+0 past the last contributor)
+#pragma unroll
+    for (int u = 0; u < kLoad; u++) {
+      if (c0 + (u / kB) * kB > c_last) break;  // a batch the finisher never starts
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++) {
+        acc[nt][0] += v[u][nt].x;
+        acc[nt][1] += v[u][nt].y;
+        acc[nt][2] += v[u][nt].z;
+        acc[nt][3] += v[u][nt].w;
+      }
+    }
+  }
+  float bestv[NT][2];
+  int besti[NT][2];
+  epilogue<NT>(p, strip, lane, acc, bestv, besti);
+}
+
+// A deferred finish for this launch: split row blocks with a whole number
+// (2..16) of CTAs each (no CTA's range meets two blocks), the argmax
+// epilogue excepted (its partials are per CTA), one row tile.
+static bool defer_for(int NB, int M, int epi, int grid) {
+  if (!g_defer_finish || g_cluster_finish || epi == EPI_LOGITS || M > 128 || grid % NB) return false;
+  const int k = grid / NB;
+  return k >= 2 && k <= 16;
+}
+
 template <int NT, bool AFF, bool V8 = false, bool CH = false>
 static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, const CUtensorMap& wmap, cudaStream_t s,
                              bool pdl, int grid) {
@@ -383,7 +460,17 @@ static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, const 
   if (q.cluster_k > 1)
     return launch_cluster(k_w12_gemm<NT, AFF, V8, CH>, dim3(grid), dim3(kThreads), Cfg<NT, V8>::SMEM, s, pdl,
                           q.cluster_k, q, map, wmap);
-  return launch(k_w12_gemm<NT, AFF, V8, CH>, dim3(grid), dim3(kThreads), Cfg<NT, V8>::SMEM, s, pdl, q, map, wmap);
+  q.defer = defer_for(q.NB, q.M, q.e.epi, grid) ? 1 : 0;
+  const cudaError_t e =
+      launch(k_w12_gemm<NT, AFF, V8, CH>, dim3(grid), dim3(kThreads), Cfg<NT, V8>::SMEM, s, pdl, q, map, wmap);
+  if (e != cudaSuccess || !q.defer) return e;
+  return launch(k_gemm_finish<NT>, dim3(2 * q.NB), dim3(128), 0, s, pdl, q);
+}
+
+int gemm_kernel_count(const w12_tensor& W, int M, int epi, int grid) {
+  if (gemm_use_tc(M) && !W.row_base) return 1;
+  if (grid <= 0) grid = gemm_warp_launch_grid(W, M, epi);
+  return (M + 127) / 128 + (defer_for(gemm_counters(W.N), M, epi, grid) ? 1 : 0);
 }
 
 
@@ -414,6 +501,7 @@ int make_gemm_params(GemmParams* out, const w12_tensor& W, const uint16_t* x, in
   p.esc_mask = 0xFFFFu;
   p.row_base = W.row_base;
   p.cluster_k = 0;
+  p.defer = 0;
   if (W.n_escapes > 0 && (!W.tile_ptr || !W.tile_esc)) {
     set_error("gemm: the tensor has escapes but no escape tile index (w12_pack_tile_index)");
     return SD_ERR_INVALID_ARG;
@@ -517,6 +605,11 @@ int gemm_warp_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int
 }  // namespace sdv
 
 using namespace sdv;
+
+extern "C" int32_t sd_gemm_set_deferred_finish(int32_t enable) {
+  if (enable >= 0) g_defer_finish = enable != 0;
+  return g_defer_finish ? 1 : 0;
+}
 
 extern "C" int32_t sd_gemm_set_cluster_finish(int32_t enable) {
   if (enable >= 0) g_cluster_finish = enable != 0;

@@ -85,6 +85,12 @@ int make_x_map(XMap* xm, const uint16_t* x, int rows_total, int64_t K, int box_r
 // workspace must hold grid * 2 * 8 * (padded rows / 8) * 128 floats.  trace
 // (optional, M <= 128): [4][grid] device-clock stamps per CTA - start, first
 // stage ready, last stage consumed, finished.
+// The process-wide split-K finish settings (cluster << 1 | deferred): part of
+// a captured step's identity.
+int gemm_finish_mode();
+// Kernels gemm_launch (grid <= 0: its default grid) issues for one call: the
+// GEMM's row tiles and, for a deferred split-K finish, the finish kernel.
+int gemm_kernel_count(const w12_tensor& W, int M, int epi, int grid = 0);
 int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
                 const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid = 0,
                 uint64_t* trace = nullptr);

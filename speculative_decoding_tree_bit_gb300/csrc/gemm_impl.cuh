@@ -60,7 +60,14 @@ struct GemmParams {
   // block, each CTA one k-range of it; the block is finished through
   // distributed shared memory instead of partials in global memory
   int cluster_k;
+  // 1: split row blocks leave their partials and return; k_gemm_finish,
+  // launched after the GEMM, sums them and runs the epilogue
+  int defer;
 };
+
+// Contributors whose partials the in-kernel finisher loads at a time (empty
+// slots of a batch add +0); the deferred finish adds in the same grouping.
+__host__ __device__ constexpr int finish_batch(int NT) { return NT <= 2 ? 4 : 2; }
 
 // n / d for 0 <= n and 0 < d: one 32-bit division when both fit (a 64-bit
 // division is a long software sequence, and the unit bookkeeping of every
@@ -525,6 +532,7 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
 #pragma unroll
       for (int nt = 0; nt < NT; nt++)
         __stcg(reinterpret_cast<float4*>(dst + nt * 128), make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]));
+      if (p.defer) return;  // the finish kernel sums the block's partials
       // the named barrier orders every thread's partial before thread 0's
       // device-scope fence and ticket (and the ticket before the others'
       // reads of the contributors' partials)
@@ -542,7 +550,7 @@ __device__ __forceinline__ bool consume_gemm(const GemmParams& p, uint8_t* sx, u
       const int64_t c_last = udiv(((int64_t)(b + 1) * KT) * G - 1, p.U);
       // partial slots of the contributors, read kBatch at a time with all
       // loads in flight before any is used (CTA order kept: deterministic)
-      constexpr int kBatch = NT <= 2 ? 4 : 2;
+      constexpr int kBatch = finish_batch(NT);
       for (int64_t c0 = c_first; c0 <= c_last; c0 += kBatch) {
         float4 v[kBatch][NT];
         bool use[kBatch];

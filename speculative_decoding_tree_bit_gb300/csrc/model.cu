@@ -219,7 +219,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
       if ((rc = tbegin(kind, gemm_bytes(W, rows, e.epi) * (1.0 / 1.5)))) return rc;
       if ((rc = gemm_warp_launch(W, x, *xm, rows, e, m->gws, m->status, s, pdl, 0, nullptr, plane))) return rc;
       if ((rc = tend())) return rc;
-      launches++;
+      launches += gemm_kernel_count(W, rows, e.epi, gemm_warp_launch_grid(W, rows, e.epi));
       if (kind == SD_K_GEMM_LM_HEAD) lm_part = gemm_warp_grid(rows);
       return SD_OK;
     }
@@ -241,7 +241,7 @@ static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
     if ((rc = tbegin(kind, gemm_bytes(W, rows, e.epi)))) return rc;
     if ((rc = gemm_launch(W, x, *xm, rows, e, m->gws, m->status, s, pdl))) return rc;
     if ((rc = tend())) return rc;
-    launches += (rows > 128 && !gemm_use_tc(rows)) ? 2 : 1;
+    launches += gemm_kernel_count(W, rows, e.epi);
     return SD_OK;
   };
   auto norm = [&](const uint16_t* src, const uint16_t* gamma, uint16_t* dst) -> int {
@@ -473,6 +473,7 @@ static int launch_step(sd_model* m, const StepIO& io, cudaStream_t s, std::vecto
   if (!m->use_graphs || m->timing || s == nullptr) return run_step(m, io, s);
   key.push_back((uintptr_t)gemm_tc_min_rows());
   key.push_back((uintptr_t)g_attn_splits);
+  key.push_back((uintptr_t)gemm_finish_mode());
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   SD_CK(cudaStreamIsCapturing(s, &cs));
   if (cs != cudaStreamCaptureStatusNone) return run_step(m, io, s);

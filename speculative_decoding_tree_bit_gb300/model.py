@@ -226,6 +226,13 @@ def linear_view8(p: Packed, x: torch.Tensor, plane8: torch.Tensor, ws: Workspace
     return y
 
 
+def set_deferred_finish(on: bool | None) -> bool:
+    """Split row blocks of the warp-level GEMM finished by a separate kernel
+    after the GEMM (True) or by their last contributor inside it (False, the
+    default); None only queries.  Returns the setting in force."""
+    return bool(lib().sd_gemm_set_deferred_finish(-1 if on is None else (1 if on else 0)))
+
+
 def set_cluster_finish(on: bool | None) -> bool:
     """Split row blocks of the warp-level GEMM finished through thread-block
     clusters (True) or partials in the workspace (False, the default);

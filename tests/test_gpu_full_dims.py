@@ -127,3 +127,39 @@ def test_batched_8b_dims_two_layers_r32_paged(M):
             assert_committed(shape, reqs[r], sub_out(out, a, b), path, ctxs[r], kv, r, rule="global")
     finally:
         model.close()
+
+
+@pytest.mark.parametrize("mode", ["deferred", "cluster"])
+def test_split_finish_modes_give_identical_steps(M, mode):
+    """The 8B-class decoder (full dimensions, two layers) verified with the
+    row blocks of q/k/v, O and down finished by the separate finish kernel
+    or through thread-block clusters: the same step bits as the default
+    in-kernel finisher (logits, accepted path, committed keys and values),
+    with the step graphs re-captured for each setting."""
+    shape = wl.SHAPES["8b_2l"]
+    W = wl.SyntheticWeights(shape, seed=5, cache=True)
+    td = wl.draft(21, 0, 16, 8, 0.8, shape.V)
+    tok_d = torch.from_numpy(np.asarray(td.rand_tok, np.int32)).cuda()
+    par_d = torch.from_numpy(np.asarray(td.parents, np.int32)).cuda()
+    ctx = 300
+    model = M.Model(shape, W, max_rows=16, max_requests=1, max_positions=ctx + 64)
+    setter = M.set_deferred_finish if mode == "deferred" else M.set_cluster_finish
+    stream = torch.cuda.Stream()
+    try:
+        outs = []
+        for on in (False, True, False):
+            setter(on)
+            kv = M.KVCache(shape, ctx + 32).fill(5, ctx)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                o = model.verify(tok_d, par_d, kv, logits=True, stream=stream)
+            torch.cuda.synchronize()
+            assert model.status() == 0
+            outs.append((o["logits"].cpu(), o["argmax"].cpu(), int(o["accepted_len"][0]),
+                         [kv.k.cpu(), kv.v.cpu(), kv.ctx_len.cpu()]))
+        for a, b in ((outs[0], outs[1]), (outs[0], outs[2])):
+            assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and a[2] == b[2]
+            assert all(torch.equal(x, y) for x, y in zip(a[3], b[3]))
+    finally:
+        setter(False)
+        model.close()

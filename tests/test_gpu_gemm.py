@@ -81,6 +81,57 @@ def test_full_size_8b(M, name, Mrows):
 
 
 @pytest.fixture()
+def deferred(M):
+    """Split row blocks finished by the separate finish kernel (default: the
+    in-kernel finisher), restored afterwards."""
+    M.set_deferred_finish(True)
+    yield M
+    M.set_deferred_finish(False)
+
+
+@pytest.mark.parametrize("name,Mrows", [("wq", 16), ("wo", 1), ("wo", 8), ("w_down", 16), ("w_down", 4),
+                                        ("w_down", 32)])
+def test_deferred_finish_8b(deferred, name, Mrows):
+    """The deferred finish kernel sums the partials in the in-kernel
+    finisher's order and grouping: bit-identical outputs, and within
+    tolerance of the oracle on sampled rows."""
+    M = deferred
+    sh = wl.SHAPES["8b"]
+    W = wl.SyntheticWeights(sh, 0).layer(0, name)
+    x = _x(Mrows, W.shape[1], 7)
+    p = M.pack(M.to_device_u16(W))
+    xd = M.to_device_u16(x)
+    assert M.set_deferred_finish(None)
+    y_def = M.linear(p, xd).cpu()
+    M.set_deferred_finish(False)
+    try:
+        y_in = M.linear(p, xd).cpu()
+    finally:
+        M.set_deferred_finish(True)
+    assert torch.equal(y_def, y_in)
+    rows = np.sort(np.random.default_rng(2).choice(W.shape[0], 512, replace=False))
+    _check(M, W, x, rows=rows, p=p)
+
+
+@pytest.mark.parametrize("N,K,Mrows", [(3008, 1024, 8), (4000, 512, 1), (2448, 4096, 16), (3008, 2048, 3),
+                                        (4000, 512, 32)])
+def test_deferred_finish_ragged(deferred, N, K, Mrows):
+    """Ragged last row blocks (strips past N; 9 to 15 CTAs per block, the
+    deferred layout)."""
+    M = deferred
+    W = synthetic.normal_bf16(synthetic.key(4, N * 3 + K), N * K, 0.02).reshape(N, K)
+    x = _x(Mrows, K, 5)
+    p = _check(M, W, x)
+    y_def = M.linear(p, M.to_device_u16(x)).cpu()
+    M.set_deferred_finish(False)
+    try:
+        y_in = M.linear(p, M.to_device_u16(x)).cpu()
+    finally:
+        M.set_deferred_finish(True)
+    assert torch.equal(y_def, y_in)
+
+
+@pytest.fixture()
 def cluster_finish(M):
     """Split row blocks finished through thread-block clusters (default:
     workspace partials and a ticket), restored afterwards."""
