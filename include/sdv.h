@@ -254,8 +254,8 @@ int sd_w12_linear_static(const w12_tensor* W, const uint16_t* x, int32_t M, uint
  * batched results: the batched step crosses from the weight-bandwidth bound
  * to the tensor-core bound).  Process-wide; applies to calls issued
  * afterwards (a model re-captures its step graphs).  rows <= 0 restores the
- * default, 33 (the measured crossover: the warp-level kernel is faster up to
- * 32 rows).  Returns the value now in force.  Not thread-safe against
+ * default, 65 (the measured crossover in whole verify steps: the warp-level
+ * kernel is faster up to 64 rows).  Returns the value now in force.  Not thread-safe against
  * concurrent GEMM calls. */
 int32_t sd_gemm_set_tc_min_rows(int32_t rows);
 

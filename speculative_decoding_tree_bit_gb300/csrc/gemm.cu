@@ -182,11 +182,14 @@ int pad_rows(int M) { return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 
 
 static int nt_of(int M) { return M > 128 ? 16 : pad_rows(M) / 8; }
 
-// Default crossover of the two kernels (rows per launch), measured on the
-// 8B-class gate/up GEMM (24576 x 4096, event-timed launches on GB300): the
-// warp-level kernel takes 43 / 54 us at 16 / 32 rows (tcgen05: 66 / 67),
-// the tcgen05 kernel 68 / 70 us at 48 / 64 rows (warp-level: 72 / 72).
-constexpr int kTcMinRowsDefault = 33;
+// Default crossover of the two kernels (rows per launch), measured on whole
+// verify steps on GB300 (graph replay, programmatic dependent launch): at
+// 64 rows the warp-level kernel takes the 27B-class step in 23.7 ms
+// (tcgen05: 26.8) and the 8B-class batched step of 8 requests in 8.2 ms
+// (tcgen05: 9.2); at 128 rows the tcgen05 kernel wins (12.5 vs 16.0 ms).
+// A lone gate/up launch (no neighbours to overlap) favours tcgen05 from 48
+// rows, by 2-6%.
+constexpr int kTcMinRowsDefault = 65;
 static int g_tc_min_rows = kTcMinRowsDefault;
 
 int gemm_tc_min_rows() { return g_tc_min_rows; }

@@ -77,8 +77,8 @@ def test_host_argument_checks(L):
     assert L.sd_attn_set_splits(-3) == 0
     assert L.sd_attn_set_splits(0) == 0
     assert L.sd_gemm_set_tc_min_rows(129) == 129
-    assert L.sd_gemm_set_tc_min_rows(0) == 33
-    assert L.sd_gemm_set_tc_min_rows(-1) == 33
+    assert L.sd_gemm_set_tc_min_rows(0) == 65
+    assert L.sd_gemm_set_tc_min_rows(-1) == 65
     # best-first selection: argument checks run before any device work
     assert L.sd_select_workspace(0) == 0
     assert L.sd_select_workspace(1000) == 20 * 1000 + 16
