@@ -495,9 +495,18 @@ def gpu_arm(args, rank, world, dist):
         par_d = torch.from_numpy(parents).to(dev)
         out = model.outputs(M)
         ctx0 = kv.ctx_len.clone()
+        # a recurrent layer's commit replaces its state in place: each step
+        # restores it (device copies inside the timed region) so that every
+        # step verifies the same tree from the same root state
+        S0 = kv.S.clone() if shape.n_rec else None
+        z0 = kv.z.clone() if shape.n_rec else None
+        restore_bytes = 0 if S0 is None else 2 * (S0.numel() * 4 + z0.numel() * 4)
 
         def step():
             kv.ctx_len.copy_(ctx0, non_blocking=True)
+            if S0 is not None:
+                kv.S.copy_(S0, non_blocking=True)
+                kv.z.copy_(z0, non_blocking=True)
             model.verify(tok_d, par_d, kv, out=out, stream=stream)
     else:
         # R requests over a paged cache, one batched verify per step
@@ -512,6 +521,9 @@ def gpu_arm(args, rank, world, dist):
         parents = np.concatenate([np.asarray(d.parents, np.int32) for d in spec.drafts])
         par_d = torch.from_numpy(parents).to(dev)
         ctx0 = kv.ctx_len.clone()
+        S0 = kv.S.clone() if shape.n_rec else None  # as above: each step from the same root states
+        z0 = kv.z.clone() if shape.n_rec else None
+        restore_bytes = 0 if S0 is None else 2 * (S0.numel() * 4 + z0.numel() * 4)
         # copy-rule tokens by depth waves over the whole batch (a node's argmax
         # depends on its root path only, final once its ancestors are)
         tokens = np.concatenate([np.where(np.arange(Mr) == 0, d.root_token, d.rand_tok).astype(np.int32)
@@ -521,6 +533,9 @@ def gpu_arm(args, rank, world, dist):
         rnd = np.concatenate([np.asarray(d.rand_tok) for d in spec.drafts])
         for wave in range(1, int(dep.max()) + 1):
             kv.ctx_len.copy_(ctx0)
+            if S0 is not None:
+                kv.S.copy_(S0)
+                kv.z.copy_(z0)
             o = model.verify_batch(tokens, parents, cu, kv)
             am = o["argmax"].cpu().numpy()
             for r in range(R):
@@ -533,6 +548,9 @@ def gpu_arm(args, rank, world, dist):
 
         def step():
             kv.ctx_len.copy_(ctx0, non_blocking=True)
+            if S0 is not None:
+                kv.S.copy_(S0, non_blocking=True)
+                kv.z.copy_(z0, non_blocking=True)
             model.verify_batch(tok_d, par_d, cu, kv, out=out, stream=stream)
 
     with torch.cuda.stream(stream):
@@ -669,6 +687,7 @@ def gpu_arm(args, rank, world, dist):
                    "split_finish": ("cluster" if args.cluster_finish else
                                     "deferred kernel" if args.deferred_finish else "workspace"),
                    "max_depth": spec.max_depth, "ctx": ctx, "p_copy": spec.p, "accepted_len": acc_len,
+                   "state_restore_bytes_per_step": restore_bytes,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (packed weights %.1f GB)" % (model.packed_bytes / 1e9)},
         "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
