@@ -1,5 +1,6 @@
-// Device building blocks of the fused W12 GEMM shared by the per-GEMM kernel
-// (gemm.cu) and the persistent GEMM-chain kernel (chain.cu).
+// Device building blocks of the warp-level fused W12 GEMM (gemm.cu): the
+// shared-memory layout, the decodes, the epilogues, the escape warp and the
+// consumers' main loop and split-K finish.
 #pragma once
 
 #include "gemm.cuh"
