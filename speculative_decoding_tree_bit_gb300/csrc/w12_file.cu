@@ -106,6 +106,17 @@ int read_header(FILE* f, Header& h, const char* who) {
     set_error(std::string(who) + ": header fields out of range");
     return SD_ERR_CORRUPT;
   }
+  // the decode the kernels take follows this flag: it must be the packer's
+  // reading of the stored table (1: empty, or contiguous with its last code
+  // below the escape exponent; else 0)
+  int aff = 1;
+  for (int c = 0; c < h.n_table; c++)
+    if (h.table[c] != h.table[0] + c) aff = 0;
+  if (h.n_table > 0 && h.table[0] + 15 > 254) aff = 0;
+  if (h.affine != aff) {
+    set_error(std::string(who) + ": header fields out of range (affine flag does not match the table)");
+    return SD_ERR_CORRUPT;
+  }
   section_bytes(h.N, h.K, h.n_escapes, h.n_tile_ptr, want);
   for (int s = 0; s < kSections; s++)
     if (h.sec[s].bytes != want[s] || h.sec[s].offset % 16 != 0 || h.sec[s].offset < sizeof h) {

@@ -73,7 +73,9 @@ def _tensor(L, p, seed):
     for i, e in enumerate(tab):
         t.table[i] = int(e)
     t.n_table = len(tab)
-    t.affine = int(len(tab) > 0 and all(tab[c] == tab[0] + c for c in range(len(tab))) and tab[0] + 15 <= 254)
+    # the packer's reading: an empty table, or a contiguous one whose last code
+    # stays below the escape exponent
+    t.affine = int(len(tab) == 0 or (all(tab[c] == tab[0] + c for c in range(len(tab))) and tab[0] + 15 <= 254))
     return t, a
 
 
@@ -212,3 +214,20 @@ def test_checksummed_but_inconsistent_arrays_are_rejected(L, tmp_path, fault):
     assert _read(L, path)[0] == 11
     assert b"packed tensor" in L.sd_last_error()
 
+
+
+@pytest.mark.parametrize("affine", ["flipped", 7])
+def test_affine_flag_must_match_the_table(L, tmp_path, affine):
+    # the kernels pick their decode from this flag: a checksummed header whose
+    # flag is not the packer's reading of its own table is refused
+    W, p = _packed(160, 128, 52, 30)
+    t, a = _tensor(L, p, 11)
+    good = int(t.affine)
+    t.affine = (1 - good) if affine == "flipped" else affine
+    path = tmp_path / "aff.w12"
+    assert L.w12_save(str(path).encode(), ctypes.byref(t)) == 0
+    assert _read(L, path)[0] == 11
+    assert b"affine" in L.sd_last_error()
+    t.affine = good
+    assert L.w12_save(str(path).encode(), ctypes.byref(t)) == 0
+    assert _read(L, path)[0] == 0
