@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--timeline", action="store_true", help="print the per-kernel breakdown to stderr")
+    ap.add_argument("--no-strip", action="store_true",
+                    help="skinny O / down launches on the warp-level split-K kernel instead of the strip-parallel one")
     ap.add_argument("--deferred-finish", action="store_true",
                     help="split row blocks finished by a separate kernel after the GEMM")
     ap.add_argument("--cluster-finish", action="store_true",
@@ -158,6 +160,7 @@ def probe_arm(args):
     tc_rows = Mdl.set_tc_min_rows(args.tc_min_rows)
     Mdl.set_cluster_finish(args.cluster_finish)
     Mdl.set_deferred_finish(args.deferred_finish)
+    Mdl.set_strip(not args.no_strip)
     N, K, M = (int(v) for v in args.probe.split(","))
     from synthetic import workloads as wl
     w = (wl.row_scaled(args.seed + 4242, N, K) if args.probe_weights == "scaled" else
@@ -469,6 +472,7 @@ def gpu_arm(args, rank, world, dist):
     tc_rows = Mdl.set_tc_min_rows(args.tc_min_rows)
     Mdl.set_cluster_finish(args.cluster_finish)
     Mdl.set_deferred_finish(args.deferred_finish)
+    Mdl.set_strip(not args.no_strip)
     attn_splits = Mdl.set_attn_splits(args.attn_splits)
     spec = wl.make(args.workload, args.seed)
     shape, R = spec.shape, spec.R
@@ -684,6 +688,7 @@ def gpu_arm(args, rank, world, dist):
         "config": {"workload": args.workload, "model": shape.name, "layers": shape.n_layers, "M": M,
                    "requests": R, "tc_min_rows": tc_rows,
                    "attn_splits": attn_splits or "auto", "schedule": "fused" if args.fused else "per-linear",
+                   "strip_kernel": not args.no_strip,
                    "split_finish": ("cluster" if args.cluster_finish else
                                     "deferred kernel" if args.deferred_finish else "workspace"),
                    "max_depth": spec.max_depth, "ctx": ctx, "p_copy": spec.p, "accepted_len": acc_len,

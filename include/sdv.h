@@ -286,6 +286,20 @@ int32_t sd_gemm_set_cluster_finish(int32_t enable);
  * against concurrent GEMM calls; a model re-captures its step graphs. */
 int32_t sd_gemm_set_deferred_finish(int32_t enable);
 
+/* Strip-parallel W12 GEMM for skinny launches ("SpecPilot ...", "(1) W12";
+ * the O and down projections of the 8B-class decoder): with enable = 1 (the
+ * default) a launch of at most 16 rows whose 16-row strips fit one wave of
+ * two CTAs per SM (N / 16 <= 2 x SMs), without the argmax epilogue, runs one
+ * CTA per strip over the whole k range - the 8 consumer warps take
+ * alternate 64-column tiles and sum their fp32 partials in shared memory in
+ * warp order, the strip's escape corrections come from the side list - so
+ * no partial crosses CTAs (no split-K finisher); 0 sends such launches to
+ * the warp-level kernel's split-K path.  Results equal up to the order of
+ * fp32 sums.  enable < 0 only queries.  Returns the setting in force.
+ * Process-wide; not thread-safe against concurrent GEMM calls; a model
+ * re-captures its step graphs. */
+int32_t sd_gemm_set_strip(int32_t enable);
+
 /* Prefix key splits per (request, kv head, 64-row chunk) of the verify
  * step's attention ("SpecPilot ...", tree attention: the committed prefix
  * is split over CTAs and the splits' softmax states are merged; the tree's

@@ -89,6 +89,7 @@ _SIGS = {
     "sd_gemm_set_tc_min_rows": (i32, [i32]),
     "sd_gemm_set_cluster_finish": (i32, [i32]),
     "sd_gemm_set_deferred_finish": (i32, [i32]),
+    "sd_gemm_set_strip": (i32, [i32]),
     "sd_attn_set_splits": (i32, [i32]),
     "sd_tree_info": (ctypes.c_int, [vp, i32, i32, vp, vp, vp, vp, vp]),
     "sd_accept": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]),

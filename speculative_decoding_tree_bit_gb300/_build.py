@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsdv.so")
-SOURCES = ["w12.cu", "gemm.cu", "gemm_tc.cu", "stream.cu", "stream_a12.cu", "stream_a8.cu", "stream_any.cu", "layers.cu", "api.cu", "model.cu", "static_linear.cu", "select.cu", "w12_file.cu", "w12_channel.cu", "w12_plane8.cu", "gdn.cu"]
+SOURCES = ["w12.cu", "gemm.cu", "gemm_tc.cu", "gemm_strip.cu", "stream.cu", "stream_a12.cu", "stream_a8.cu", "stream_any.cu", "layers.cu", "api.cu", "model.cu", "static_linear.cu", "select.cu", "w12_file.cu", "w12_channel.cu", "w12_plane8.cu", "gdn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -209,7 +209,9 @@ static bool g_defer_finish = false;
 // (O 24.0 vs 20.7 us, down 41.9 vs 32.8 us at 16 rows).
 static bool g_cluster_finish = false;
 int gemm_warp_grid(int M) { return warp_grid(M); }
-int gemm_finish_mode() { return (g_cluster_finish ? 2 : 0) | (g_defer_finish ? 1 : 0); }
+int gemm_finish_mode() {
+  return (g_cluster_finish ? 2 : 0) | (g_defer_finish ? 1 : 0) | (gemm_strip_eligible_setting() ? 4 : 0);
+}
 
 int gemm_grid(int M) { return gemm_use_tc(M) ? num_sms() : warp_grid(M); }
 
@@ -472,6 +474,7 @@ static cudaError_t launch_nt(const GemmParams& p, const CUtensorMap& map, const 
 
 int gemm_kernel_count(const w12_tensor& W, int M, int epi, int grid) {
   if (gemm_use_tc(M) && !W.row_base) return 1;
+  if (grid <= 0 && gemm_strip_eligible(W, M, epi)) return 1;
   if (grid <= 0) grid = gemm_warp_launch_grid(W, M, epi);
   return (M + 127) / 128 + (defer_for(gemm_counters(W.N), M, epi, grid) ? 1 : 0);
 }
@@ -525,6 +528,8 @@ int gemm_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, c
                 const GemmWorkspace& ws, int32_t* status, cudaStream_t s, bool pdl, int grid, uint64_t* trace) {
   // a per-channel tensor has the warp-level kernel's decode only
   if (gemm_use_tc(M) && !W.row_base) return gemm_tc_launch(W, x, xm.rows_total, M, epi, ws, status, s, pdl);
+  if (grid <= 0 && !trace && gemm_strip_eligible(W, M, epi.epi))
+    return gemm_strip_launch(W, x, xm, M, epi, status, s, pdl);
   return gemm_warp_launch(W, x, xm, M, epi, ws, status, s, pdl, grid, trace);
 }
 

@@ -85,6 +85,15 @@ int make_x_map(XMap* xm, const uint16_t* x, int rows_total, int64_t K, int box_r
 // workspace must hold grid * 2 * 8 * (padded rows / 8) * 128 floats.  trace
 // (optional, M <= 128): [4][grid] device-clock stamps per CTA - start, first
 // stage ready, last stage consumed, finished.
+// Strip-parallel kernel (gemm_strip.cu): one CTA per 16-row strip over the
+// whole k range, no split-K across CTAs; for skinny launches (M <= 16) whose
+// strips fit one wave (the O and down projections).  gemm_launch takes it at
+// its default grid when eligible (sd_gemm_set_strip).
+bool gemm_strip_eligible(const w12_tensor& W, int M, int epi);
+bool gemm_strip_eligible_setting();  // sd_gemm_set_strip
+int gemm_strip_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, int M, const GemmEpilogue& epi,
+                      int32_t* status, cudaStream_t s, bool pdl);
+
 // The process-wide split-K finish settings (cluster << 1 | deferred): part of
 // a captured step's identity.
 int gemm_finish_mode();

@@ -226,6 +226,13 @@ def linear_view8(p: Packed, x: torch.Tensor, plane8: torch.Tensor, ws: Workspace
     return y
 
 
+def set_strip(on: bool | None) -> bool:
+    """Skinny launches whose 16-row strips fit one wave on the strip-parallel
+    kernel (True, the default: no split-K across CTAs) or on the warp-level
+    kernel (False); None only queries.  Returns the setting in force."""
+    return bool(lib().sd_gemm_set_strip(-1 if on is None else (1 if on else 0)))
+
+
 def set_deferred_finish(on: bool | None) -> bool:
     """Split row blocks of the warp-level GEMM finished by a separate kernel
     after the GEMM (True) or by their last contributor inside it (False, the

@@ -80,13 +80,63 @@ def test_full_size_8b(M, name, Mrows):
     _check(M, W, _x(Mrows, W.shape[1], 4), rows=rows)
 
 
+# ------------------------------------------- strip-parallel kernel (M <= 16) --
+
+@pytest.mark.parametrize("N,K,Mrows", [(4096, 4096, 16), (4096, 12288, 16), (4096, 4096, 1), (4000, 4160, 8),
+                                        (2000, 448, 13), (160, 64, 16), (4864, 1024, 9)])
+def test_strip_kernel_matches_oracle(M, N, K, Mrows):
+    """One CTA per 16-row strip over the whole k range: ragged last strips of
+    a block (N = 4000, 2000, 160), k-tile counts not a multiple of the 8
+    consumer warps (65, 7, 1), one wave at the limit (4864 rows = 304
+    strips); the same rows against the split-K kernel within the tolerance."""
+    assert M.set_strip(None)
+    W = synthetic.normal_bf16(synthetic.key(6, N * 7 + K), N * K, 0.02).reshape(N, K)
+    x = _x(Mrows, K, 8)
+    p = _check(M, W, x)
+    y_strip = oracle.bf16_to_f64(M.linear(p, M.to_device_u16(x)).cpu().numpy().view(np.uint16))
+    M.set_strip(False)
+    try:
+        y_split = oracle.bf16_to_f64(M.linear(p, M.to_device_u16(x)).cpu().numpy().view(np.uint16))
+    finally:
+        M.set_strip(True)
+    assert np.all(np.abs(y_strip - y_split) <= 2 * (ATOL + RTOL * np.abs(y_split)))
+
+
+@pytest.mark.parametrize("rare", [0, 400, 5000])
+def test_strip_kernel_escapes(M, rare):
+    """Escapes by the strip's run of the side list: none, a few per strip,
+    and more than 32 per strip (several index chunks)."""
+    N, K = 1024, 2048
+    W = synthetic.normal_bf16(synthetic.key(7, rare), N * K, 0.02).reshape(N, K)
+    if rare:
+        synthetic.force_rare_exponents(synthetic.key(7, rare + 1), W, rare)
+    p = _check(M, W, _x(16, K, 9))
+    if rare > 1000:
+        assert p.n_escapes > 32 * (N // 16)
+
+
+def test_strip_kernel_general_table(M):
+    """A non-contiguous exponent table (the table decode; escaped weights
+    decode to zero) on the strip kernel."""
+    rng = np.random.default_rng(11)
+    exps = np.array([110, 112, 114, 116, 118, 120, 121, 122, 123, 124, 100, 102, 104, 106, 108, 90], np.uint32)
+    e = exps[rng.integers(0, exps.size, size=512 * 1024)]
+    W = ((rng.integers(0, 2, size=e.size).astype(np.uint32) << 15) | (e << 7)
+         | rng.integers(0, 128, size=e.size).astype(np.uint32)).astype(np.uint16).reshape(512, 1024)
+    p = _check(M, W, _x(16, 1024, 4))
+    assert p.meta.affine == 0 and p.n_escapes > 0
+
+
 @pytest.fixture()
 def deferred(M):
     """Split row blocks finished by the separate finish kernel (default: the
-    in-kernel finisher), restored afterwards."""
+    in-kernel finisher), restored afterwards; the strip-parallel kernel off
+    (it takes these launches otherwise)."""
     M.set_deferred_finish(True)
+    M.set_strip(False)
     yield M
     M.set_deferred_finish(False)
+    M.set_strip(True)
 
 
 @pytest.mark.parametrize("name,Mrows", [("wq", 16), ("wo", 1), ("wo", 8), ("w_down", 16), ("w_down", 4),
@@ -134,10 +184,13 @@ def test_deferred_finish_ragged(deferred, N, K, Mrows):
 @pytest.fixture()
 def cluster_finish(M):
     """Split row blocks finished through thread-block clusters (default:
-    workspace partials and a ticket), restored afterwards."""
+    workspace partials and a ticket), restored afterwards; the strip-parallel
+    kernel off (it takes these launches otherwise)."""
     M.set_cluster_finish(True)
+    M.set_strip(False)
     yield M
     M.set_cluster_finish(False)
+    M.set_strip(True)
 
 
 @pytest.mark.parametrize("name,Mrows", [("wq", 16), ("wo", 1), ("wo", 8), ("w_down", 16), ("w_down", 32)])
