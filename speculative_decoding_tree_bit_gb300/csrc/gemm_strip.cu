@@ -1,5 +1,6 @@
-// Strip-parallel W12 GEMM for skinny launches with few row blocks (the O and
-// down projections: N = 4096 is 256 strips of 16 rows).
+// Strip-parallel W12 GEMM for skinny launches with a short k range and few
+// row blocks (the O and q/k/v projections: N = 4096 is 256 strips of 16
+// rows, 6144 is 384).
 //
 // "SpecPilot: AI Agent Framework Boosts Speculative Decoding 10.87x for
 // Qwen3.8-27B", "(1) W12" (decode fused into the GEMM) and "Phase 0:
@@ -8,18 +9,19 @@
 // 128-row block, and the last CTA of a block sums the others' fp32 partials
 // from global memory before the epilogue - a chain of an acq_rel ticket and
 // dependent round trips that ends the launch 8-10 us after the other CTAs.
-// Here a CTA owns one 16-row strip and the whole k range, so nothing is
-// summed across CTAs:
+// Here a CTA owns SPC (1 or 2) 16-row strips and the whole k range, so
+// nothing is summed across CTAs:
 //
-//  * Stage = 8 consecutive 64-column tiles of the strip: its packed words
-//    are one contiguous 12 KB run (one bulk copy) and the 8 activation tiles
-//    come by the 2-D TMA map of the warp-level kernel (64 columns x padded
-//    rows, 128-byte swizzle).
-//  * Consumer warp w decodes and multiplies tile w of every stage - the
-//    warp-level kernel's decode and mma.sync code unchanged - so the 8 warps
-//    hold fp32 partials over disjoint k ranges; at the end they are summed in
-//    shared memory in warp order (deterministic) by warp 0, which runs the
-//    epilogue.
+//  * Stage = KG = 8 / SPC consecutive 64-column tiles of each strip: each
+//    strip's packed words are one contiguous run (a bulk copy), 12 KB per
+//    stage in all, and the KG activation tiles, shared by the strips, come
+//    by the 2-D TMA map of the warp-level kernel (64 columns x padded rows,
+//    128-byte swizzle).
+//  * Consumer warp w takes strip w / KG and tile w % KG of every stage - the
+//    warp-level kernel's decode and mma.sync code unchanged - so the KG
+//    warps of a strip hold fp32 partials over disjoint k ranges; at the end
+//    the first of them sums them in shared memory in warp order
+//    (deterministic) and runs the epilogue.
 //  * Escapes: the strip's escapes are one contiguous run of the row-major
 //    side list.  The escape warp forms their correction sum (w - slot) x[m][k]
 //    per (row, m) from the activations in global memory (L2) while the
@@ -37,32 +39,36 @@ struct StripEsc {
   const uint16_t* esc_val;  // bf16 bits
 };
 
-template <int NT>
+template <int NT, int SPC>
 struct SCfgStrip {
   static constexpr int MP = NT * 8;
-  static constexpr int XB = MP * 128;       // one activation tile (64 columns)
-  static constexpr int XS = kNCW * XB;      // a stage's 8 activation tiles
-  static constexpr int WB = kNCW * kStripBytes;  // a stage's 8 weight tiles of the strip
-  static constexpr int S = NT <= 1 ? 4 : 3;  // stages (two CTAs per SM)
+  static constexpr int KG = kNCW / SPC;          // tiles per strip per stage (k-groups)
+  static constexpr int XB = MP * 128;            // one activation tile (64 columns)
+  static constexpr int XS = KG * XB;             // a stage's activation tiles
+  static constexpr int WB = kNCW * kStripBytes;  // a stage's weight tiles (SPC strips x KG tiles)
+  // stages: as many as two CTAs per SM allow
+  static constexpr int S = SPC == 1 ? (NT <= 1 ? 4 : 3) : (NT <= 1 ? 6 : 5);
   static constexpr int OFF_W = S * XS;
   static constexpr int OFF_FULL = OFF_W + S * WB;
   static constexpr int OFF_EMPTY = OFF_FULL + S * 8;
   static constexpr int OFF_CBAR = OFF_EMPTY + S * 8;   // corrections ready
   static constexpr int OFF_FLAG = OFF_CBAR + 8;        // abort flag
-  static constexpr int OFF_CORR = (OFF_FLAG + 8 + 15) & ~15;  // [16 rows][MP] fp32
-  static constexpr int END = OFF_CORR + 16 * MP * 4;
+  static constexpr int OFF_CORR = (OFF_FLAG + 8 + 15) & ~15;  // [16 SPC rows][MP] fp32
+  static constexpr int END = OFF_CORR + 16 * SPC * MP * 4;
   static constexpr int SMEM = 1024 + END;
   static_assert(kNCW * NT * 128 * 4 <= S * WB, "the reduction buffer fits the weight ring");
+  static_assert(2 * (SMEM + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
 // Escapes per batch whose activation loads are in flight together.
 constexpr int kStripEscBatch = 8;
 
-template <int NT, bool AFFINE>
+template <int NT, int SPC, bool AFFINE>
 __global__ void __launch_bounds__(kThreads, 2)
     k_w12_gemm_strip(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap xmap,
                      const __grid_constant__ StripEsc es) {
-  using C = SCfgStrip<NT>;
+  using C = SCfgStrip<NT, SPC>;
+  constexpr int KG = C::KG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sx = smem;
@@ -74,10 +80,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* corr = reinterpret_cast<float*>(smem + C::OFF_CORR);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int strip = blockIdx.x;
+  const int s0 = blockIdx.x * SPC;                       // the CTA's first strip
+  const int nsp = min(SPC, (int)p.NS - s0);              // its strips (the last CTA may have fewer)
   const int KT = p.KT;
-  const int NJ = (KT + kNCW - 1) / kNCW;  // stages
-  auto tiles_of = [&](int j) { return min(kNCW, KT - j * kNCW); };
+  const int NJ = (KT + KG - 1) / KG;  // stages
+  auto tiles_of = [&](int j) { return min(KG, KT - j * KG); };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::S; i++) {
@@ -95,17 +102,18 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------- producer --
-    if (lane == 0 && strip < p.NS) {
-      const uint32_t* wsrc = p.words + (int64_t)strip * KT * (kStripBytes / 4);
+    if (lane == 0 && nsp > 0) {
       auto issue_w = [&](int slot, int j) {
         const int nk = tiles_of(j);
-        mbar_arrive_expect_tx(&full[slot], (uint32_t)(nk * (kStripBytes + C::XB)));
-        bulk_g2s(sw + slot * C::WB, wsrc + (int64_t)j * kNCW * (kStripBytes / 4), (uint32_t)(nk * kStripBytes),
-                 &full[slot]);
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)(nk * (nsp * kStripBytes + C::XB)));
+        for (int si = 0; si < nsp; si++)
+          bulk_g2s(sw + slot * C::WB + si * KG * kStripBytes,
+                   p.words + ((int64_t)(s0 + si) * KT + (int64_t)j * KG) * (kStripBytes / 4),
+                   (uint32_t)(nk * kStripBytes), &full[slot]);
       };
       auto issue_x = [&](int slot, int j) {
         const int nk = tiles_of(j);
-        for (int t = 0; t < nk; t++) tma2d_g2s(sx + slot * C::XS + t * C::XB, &xmap, (j * kNCW + t) * 64, p.m0, &full[slot]);
+        for (int t = 0; t < nk; t++) tma2d_g2s(sx + slot * C::XS + t * C::XB, &xmap, (j * KG + t) * 64, p.m0, &full[slot]);
       };
       const int pre = NJ < C::S ? NJ : C::S;
       for (int j = 0; j < pre; j++) issue_w(j, j);
@@ -141,13 +149,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == kEscapeWarp) {
     // ------------------------------------------------- escape warp --
-    // corr[r][m] = sum over the strip's escapes (row 16 strip + r, column k,
+    // corr[r][m] = sum over the strips' escapes (row 16 s0 + r, column k,
     // weight w) of (w - slot) x[m][k], in side-list order; lanes over m
     const int mrows = min(C::MP, p.M - p.m0);
-    for (int i = lane; i < 16 * C::MP; i += 32) corr[i] = 0.f;
-    if (p.tile_ptr != nullptr && strip < p.NS) {  // the tensor has escapes
-      const int64_t n0 = (int64_t)strip * 16;
-      const int64_t n1 = n0 + 16 < p.N ? n0 + 16 : p.N;
+    for (int i = lane; i < 16 * SPC * C::MP; i += 32) corr[i] = 0.f;
+    if (p.tile_ptr != nullptr && nsp > 0) {  // the tensor has escapes
+      const int64_t n0 = (int64_t)s0 * 16;
+      const int64_t n1 = n0 + 16 * nsp < p.N ? n0 + 16 * nsp : p.N;
       const uint32_t e0 = __ldg(es.row_ptr + n0), e1 = __ldg(es.row_ptr + n1);
       pdl_wait();  // the activations come from the previous kernel
       const float slot_v = p.esc_slot;
@@ -203,12 +211,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint32_t phase = 0;
   for (int j = 0; j < NJ; j++) {
     if (!mbar_wait_or_abort(&full[slot], phase, abort)) set_status(p.status, SD_TIMEOUT_AT(42));
-    if (strip < p.NS && j * kNCW + warp < KT) {
+    if (warp / KG < nsp && j * KG + warp % KG < KT) {
       const uint8_t* wsm = sw + slot * C::WB + warp * kStripBytes;
       const uint4 W0 = *reinterpret_cast<const uint4*>(wsm + lane * 16);
       const uint4 W1 = *reinterpret_cast<const uint4*>(wsm + 512 + lane * 16);
       const uint4 W2 = *reinterpret_cast<const uint4*>(wsm + 1024 + lane * 16);
-      const uint32_t xb = smem_u32(sx + slot * C::XS + warp * C::XB);
+      const uint32_t xb = smem_u32(sx + slot * C::XS + (warp % KG) * C::XB);
 #pragma unroll
       for (int jj = 0; jj < 4; jj++) {
         uint32_t a0, a1, a2, a3;
@@ -246,8 +254,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int c = 0; c < 4; c++) acc[nt][c] += acc2[nt][c];
   }
-  // the 8 warps' partials meet in the weight ring, idle once every consumer
-  // warp is past its last stage
+  // the KG warps' partials of a strip meet in the weight ring, idle once
+  // every consumer warp is past its last stage
   bar_sync(1, kNCW * 32);
   float* red = reinterpret_cast<float*>(sw);
 #pragma unroll
@@ -255,14 +263,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     *reinterpret_cast<float4*>(red + ((warp * NT + nt) * 32 + lane) * 4) =
         make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
   bar_sync(1, kNCW * 32);
-  if (warp != 0 || strip >= p.NS) return;
+  const int sidx = warp / KG;  // the warp's strip in the CTA
+  if (warp % KG != 0 || sidx >= nsp) return;
+  const int strip = s0 + sidx;
   float sum[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; nt++)
 #pragma unroll
     for (int c = 0; c < 4; c++) sum[nt][c] = 0.f;
 #pragma unroll
-  for (int w = 0; w < kNCW; w++)
+  for (int w = warp; w < warp + KG; w++)
 #pragma unroll
     for (int nt = 0; nt < NT; nt++) {
       const float4 v = *reinterpret_cast<const float4*>(red + ((w * NT + nt) * 32 + lane) * 4);
@@ -278,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int nt = 0; nt < NT; nt++)
 #pragma unroll
       for (int cc = 0; cc < 2; cc++) {
-        sum[nt][cc] += corr[g * C::MP + nt * 8 + 2 * q + cc];
-        sum[nt][2 + cc] += corr[(g + 8) * C::MP + nt * 8 + 2 * q + cc];
+        sum[nt][cc] += corr[(sidx * 16 + g) * C::MP + nt * 8 + 2 * q + cc];
+        sum[nt][2 + cc] += corr[(sidx * 16 + g + 8) * C::MP + nt * 8 + 2 * q + cc];
       }
   }
   float bestv[NT][2];
@@ -287,18 +297,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   epilogue<NT>(p, strip, lane, sum, bestv, besti);
 }
 
-template <int NT, bool AFF>
+template <int NT, int SPC, bool AFF>
 static cudaError_t launch_strip(const GemmParams& p, const CUtensorMap& xmap, const StripEsc& es, cudaStream_t s,
                                 bool pdl) {
+  using C = SCfgStrip<NT, SPC>;
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(k_w12_gemm_strip<NT, AFF>, cudaFuncAttributeMaxDynamicSharedMemorySize, SCfgStrip<NT>::SMEM);
+    const cudaError_t e = cudaFuncSetAttribute(k_w12_gemm_strip<NT, SPC, AFF>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch(k_w12_gemm_strip<NT, AFF>, dim3((unsigned)p.NS), dim3(kThreads), SCfgStrip<NT>::SMEM, s, pdl, p, xmap,
-                es);
+  return launch(k_w12_gemm_strip<NT, SPC, AFF>, dim3((unsigned)((p.NS + SPC - 1) / SPC)), dim3(kThreads), C::SMEM, s,
+                pdl, p, xmap, es);
 }
 
 static bool g_strip_gemm = true;
@@ -314,7 +325,7 @@ bool gemm_strip_eligible(const w12_tensor& W, int M, int epi) {
   // one wave of two CTAs per SM; the argmax epilogue keeps its per-CTA
   // partials on the warp-level kernel
   return g_strip_gemm && M >= 1 && M <= 16 && epi != EPI_LOGITS && !W.row_base && W.N % 16 == 0 && W.K % 64 == 0 &&
-         W.K <= g_strip_max_k && W.N / 16 <= 2 * (int64_t)num_sms() &&
+         W.K <= g_strip_max_k && W.N / 16 <= 4 * (int64_t)num_sms() &&
          (W.n_escapes == 0 || (W.row_ptr && W.esc_idx && W.esc_val));
 }
 
@@ -330,11 +341,16 @@ int gemm_strip_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, in
     return SD_ERR_INVALID_ARG;
   }
   StripEsc es{W.row_ptr, W.esc_idx, W.esc_val};
+  // one strip per CTA while the strips fit one wave of two CTAs per SM, else
+  // two (the 8B-class q/k/v: 384 strips; the 27B-class O: 320)
+  const bool two = p.NS > 2 * (int64_t)num_sms();
   cudaError_t e;
   if (NT == 1)
-    e = W.affine ? launch_strip<1, true>(p, xm.map, es, s, pdl) : launch_strip<1, false>(p, xm.map, es, s, pdl);
+    e = two ? (W.affine ? launch_strip<1, 2, true>(p, xm.map, es, s, pdl) : launch_strip<1, 2, false>(p, xm.map, es, s, pdl))
+            : (W.affine ? launch_strip<1, 1, true>(p, xm.map, es, s, pdl) : launch_strip<1, 1, false>(p, xm.map, es, s, pdl));
   else
-    e = W.affine ? launch_strip<2, true>(p, xm.map, es, s, pdl) : launch_strip<2, false>(p, xm.map, es, s, pdl);
+    e = two ? (W.affine ? launch_strip<2, 2, true>(p, xm.map, es, s, pdl) : launch_strip<2, 2, false>(p, xm.map, es, s, pdl))
+            : (W.affine ? launch_strip<2, 1, true>(p, xm.map, es, s, pdl) : launch_strip<2, 1, false>(p, xm.map, es, s, pdl));
   if (e != cudaSuccess) return cuda_fail(e, "k_w12_gemm_strip launch");
   return SD_OK;
 }
