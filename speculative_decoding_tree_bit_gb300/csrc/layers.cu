@@ -723,15 +723,19 @@ cudaError_t launch_attention(const AttnArgs& a_in, int rows_total, cudaStream_t 
 
 __device__ __forceinline__ float phi(float x) { return x > 0.f ? x + 1.0f : expf(x); }
 
-constexpr int kRecSmem = (64 * 128 * 2 + 128 * 32 + 64 * 32 + 128 + 64 * 64 + 64) * 4;
+// phi(q), phi(k) rows padded to 129 floats: the tree dot products read
+// element d of many rows at once, which a 128-float stride puts in one bank
+// (measured: no change in the hybrid step; the kernel is bound elsewhere)
+constexpr int kRecFS = 129;
+constexpr int kRecSmem = (64 * kRecFS * 2 + 128 * 32 + 64 * 32 + 128 + 64 * 64 + 64) * 4;
 
 __global__ void __launch_bounds__(128) k_linrec(LinrecArgs a) {
   pdl_launch();  // the next kernel may start streaming its (independent) weights now
   pdl_wait();
   extern __shared__ __align__(16) float smem_rec[];
-  float* fq = smem_rec;       // [64][128]
-  float* fk = fq + 64 * 128;  // [64][128]
-  float* sS = fk + 64 * 128;  // [128][32]
+  float* fq = smem_rec;          // [64][kRecFS]
+  float* fk = fq + 64 * kRecFS;  // [64][kRecFS]
+  float* sS = fk + 64 * kRecFS;  // [128][32]
   float* sv = sS + 128 * 32;  // [64][32]
   float* sz = sv + 64 * 32;   // [128]
   float* dots = sz + 128;     // [64][64]
@@ -742,8 +746,8 @@ __global__ void __launch_bounds__(128) k_linrec(LinrecArgs a) {
   for (int idx = threadIdx.x; idx < Mr * 128; idx += blockDim.x) {
     const int i = idx >> 7, d = idx & 127;
     const uint16_t* row = a.qkv + (int64_t)(node0 + i) * H3;
-    fq[i * 128 + d] = phi(bf2f(row[h * 128 + d]));
-    fk[i * 128 + d] = phi(bf2f(row[a.H + h * 128 + d]));
+    fq[i * kRecFS + d] = phi(bf2f(row[h * 128 + d]));
+    fk[i * kRecFS + d] = phi(bf2f(row[a.H + h * 128 + d]));
   }
   for (int idx = threadIdx.x; idx < Mr * 32; idx += blockDim.x) {
     const int i = idx >> 5, c = idx & 31;
@@ -761,20 +765,20 @@ __global__ void __launch_bounds__(128) k_linrec(LinrecArgs a) {
     const int i = idx / Mr, j = idx % Mr;
     float dt = 0.f;
     if ((a.anc[node0 + i] >> j) & 1ull) {
-      for (int d = 0; d < 128; d++) dt = fmaf(fk[j * 128 + d], fq[i * 128 + d], dt);
+      for (int d = 0; d < 128; d++) dt = fmaf(fk[j * kRecFS + d], fq[i * kRecFS + d], dt);
     }
     dots[i * 64 + j] = dt;
   }
   for (int i = threadIdx.x; i < Mr; i += blockDim.x) {
     float t = 0.f;
-    for (int d = 0; d < 128; d++) t = fmaf(sz[d], fq[i * 128 + d], t);
+    for (int d = 0; d < 128; d++) t = fmaf(sz[d], fq[i * kRecFS + d], t);
     zq[i] = t;
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < Mr * 32; idx += blockDim.x) {
     const int i = idx >> 5, c = idx & 31;
     float num = 0.f;
-    for (int k = 0; k < 128; k++) num = fmaf(fq[i * 128 + k], sS[k * 32 + c], num);
+    for (int k = 0; k < 128; k++) num = fmaf(fq[i * kRecFS + k], sS[k * 32 + c], num);
     float den = zq[i];
     for (int j = 0; j < Mr; j++) {
       const float w = dots[i * 64 + j];
@@ -941,13 +945,23 @@ __global__ void __launch_bounds__(128) k_rec_commit(CacheView cv, int n_rec, int
   __syncthreads();
   float* S = cv.S + (((int64_t)r * n_rec + lr) * nh + h) * 128 * 128;
   float* z = cv.z + (((int64_t)r * n_rec + lr) * nh + h) * 128;
-  const int k = threadIdx.x;
-  for (int c = 0; c < 32; c++) {
-    float add = 0.f;
-    for (int p = 0; p < P; p++) add = fmaf(fk[p][k], vv[p][c], add);
-    S[k * 128 + cc * 32 + c] += add;
+  // lanes over the chunk's 32 columns (one 128-byte row segment per warp
+  // access), warps over the rows, 8 rows' loads in flight at a time
+  const int warp = threadIdx.x >> 5, c = threadIdx.x & 31;
+  constexpr int kRows = 8;
+  for (int k0 = warp * kRows; k0 < 128; k0 += 4 * kRows) {
+    float cur[kRows];
+#pragma unroll
+    for (int u = 0; u < kRows; u++) cur[u] = S[(k0 + u) * 128 + cc * 32 + c];
+#pragma unroll
+    for (int u = 0; u < kRows; u++) {
+      float add = 0.f;
+      for (int p = 0; p < P; p++) add = fmaf(fk[p][k0 + u], vv[p][c], add);
+      S[(k0 + u) * 128 + cc * 32 + c] = cur[u] + add;
+    }
   }
   if (cc == 0) {
+    const int k = threadIdx.x;
     float add = 0.f;
     for (int p = 0; p < P; p++) add += fk[p][k];
     z[k] += add;
