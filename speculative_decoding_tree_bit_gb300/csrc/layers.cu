@@ -725,9 +725,8 @@ __device__ __forceinline__ float phi(float x) { return x > 0.f ? x + 1.0f : expf
 
 // phi(q), phi(k) rows padded to 129 floats: the tree dot products read
 // element d of many rows at once, which a 128-float stride puts in one bank
-// (measured: no change in the hybrid step; the kernel is bound elsewhere)
 constexpr int kRecFS = 129;
-constexpr int kRecSmem = (64 * kRecFS * 2 + 128 * 32 + 64 * 32 + 128 + 64 * 64 + 64) * 4;
+constexpr int kRecSmem = (64 * kRecFS * 2 + 128 * 32 + 64 * 32 + 128 + 64 * 64 + 64) * 4 + 64 * 8;
 
 __global__ void __launch_bounds__(128) k_linrec(LinrecArgs a) {
   pdl_launch();  // the next kernel may start streaming its (independent) weights now
@@ -741,30 +740,65 @@ __global__ void __launch_bounds__(128) k_linrec(LinrecArgs a) {
   float* dots = sz + 128;     // [64][64]
   float* zq = dots + 64 * 64; // [64]
   const int cc = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
+  uint64_t* sanc = reinterpret_cast<uint64_t*>(zq + 64);  // [64] ancestor masks
   const int node0 = a.cu[r], Mr = min(a.cu[r + 1] - node0, 64);
   const int64_t H3 = (int64_t)a.H * 3;
-  for (int idx = threadIdx.x; idx < Mr * 128; idx += blockDim.x) {
-    const int i = idx >> 7, d = idx & 127;
-    const uint16_t* row = a.qkv + (int64_t)(node0 + i) * H3;
-    fq[i * kRecFS + d] = phi(bf2f(row[h * 128 + d]));
-    fk[i * kRecFS + d] = phi(bf2f(row[a.H + h * 128 + d]));
+  // staging: every thread's global loads of a batch are in flight before
+  // any is stored (a load-store loop waits one L2 round trip per element)
+  constexpr int kB = 8;
+  for (int base = 0; base < Mr * 128; base += kB * 128) {
+    uint16_t lq[kB], lk[kB];
+#pragma unroll
+    for (int u = 0; u < kB; u++) {
+      const int idx = base + u * 128 + threadIdx.x;
+      const int i = idx >> 7, d = idx & 127;
+      const uint16_t* row = a.qkv + (int64_t)(node0 + i) * H3;
+      lq[u] = idx < Mr * 128 ? row[h * 128 + d] : (uint16_t)0;
+      lk[u] = idx < Mr * 128 ? row[a.H + h * 128 + d] : (uint16_t)0;
+    }
+#pragma unroll
+    for (int u = 0; u < kB; u++) {
+      const int idx = base + u * 128 + threadIdx.x;
+      if (idx >= Mr * 128) break;
+      const int i = idx >> 7, d = idx & 127;
+      fq[i * kRecFS + d] = phi(bf2f(lq[u]));
+      fk[i * kRecFS + d] = phi(bf2f(lk[u]));
+    }
   }
-  for (int idx = threadIdx.x; idx < Mr * 32; idx += blockDim.x) {
-    const int i = idx >> 5, c = idx & 31;
-    sv[i * 32 + c] = bf2f(a.qkv[(int64_t)(node0 + i) * H3 + 2 * a.H + h * 128 + cc * 32 + c]);
+  for (int base = 0; base < Mr * 32; base += kB * 128) {
+    uint16_t lv[kB];
+#pragma unroll
+    for (int u = 0; u < kB; u++) {
+      const int idx = base + u * 128 + threadIdx.x;
+      const int i = idx >> 5, c = idx & 31;
+      lv[u] = idx < Mr * 32 ? a.qkv[(int64_t)(node0 + i) * H3 + 2 * a.H + h * 128 + cc * 32 + c] : (uint16_t)0;
+    }
+#pragma unroll
+    for (int u = 0; u < kB; u++) {
+      const int idx = base + u * 128 + threadIdx.x;
+      if (idx >= Mr * 32) break;
+      sv[(idx >> 5) * 32 + (idx & 31)] = bf2f(lv[u]);
+    }
   }
   const float* Sg = a.S + r * a.req_stride_S + (int64_t)h * 128 * 128;
   const float* zg = a.z + r * a.req_stride_z + (int64_t)h * 128;
-  for (int idx = threadIdx.x; idx < 128 * 32; idx += blockDim.x) {
-    const int k = idx >> 5, c = idx & 31;
-    sS[k * 32 + c] = Sg[k * 128 + cc * 32 + c];
+  for (int base = 0; base < 128 * 32; base += 16 * 128) {
+    float ls[16];
+#pragma unroll
+    for (int u = 0; u < 16; u++) {
+      const int idx = base + u * 128 + threadIdx.x;
+      ls[u] = Sg[(idx >> 5) * 128 + cc * 32 + (idx & 31)];
+    }
+#pragma unroll
+    for (int u = 0; u < 16; u++) sS[base + u * 128 + threadIdx.x] = ls[u];
   }
   for (int k = threadIdx.x; k < 128; k += blockDim.x) sz[k] = zg[k];
+  for (int i = threadIdx.x; i < Mr; i += blockDim.x) sanc[i] = a.anc[node0 + i];
   __syncthreads();
   for (int idx = threadIdx.x; idx < Mr * Mr; idx += blockDim.x) {
     const int i = idx / Mr, j = idx % Mr;
     float dt = 0.f;
-    if ((a.anc[node0 + i] >> j) & 1ull) {
+    if ((sanc[i] >> j) & 1ull) {
       for (int d = 0; d < 128; d++) dt = fmaf(fk[j * kRecFS + d], fq[i * kRecFS + d], dt);
     }
     dots[i * 64 + j] = dt;

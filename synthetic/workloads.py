@@ -359,6 +359,8 @@ WORKLOADS = {
     "27b_m32": dict(kind="decoder", shape="27b", M=32, max_depth=10, ctx=4096, p=0.7),
     "27b_m64": dict(kind="decoder", shape="27b", M=64, max_depth=10, ctx=4096, p=0.7),
     "hybrid_m16": dict(kind="decoder", shape="hybrid", M=16, max_depth=8, ctx=2048, p=0.7),
+    # four-layer profiling case of the hybrid step (3 recurrent + 1 attention)
+    "hybrid_4l_m16": dict(kind="decoder", shape="hybrid_4l", M=16, max_depth=8, ctx=2048, p=0.7),
     "batched_r32": dict(kind="decoder", shape="8b", M=8, max_depth=7, R=32, chain_draft=True, p=0.6,
                         ctx_range=(1024, 4096), page_size=16),
     # two-layer profiling case of the batched step
