@@ -86,10 +86,21 @@ __global__ void __launch_bounds__(kGdnThreads, 1) k_gdn_tree(GdnArgs a) {
   const int nh = a.nh;
   pdl_wait();  // q, k, v, the gates and the state may come from the previous kernel
   const float* S0 = a.S + ((int64_t)r * nh + h) * kGdnHd * kGdnHd;
-  for (int e = tid; e < kGdnHd * kGdnCols / 4; e += kGdnThreads) {
-    const int row = e / (kGdnCols / 4), c4 = e % (kGdnCols / 4);
-    *reinterpret_cast<float4*>(&s.s0[row][4 * c4]) =
-        __ldcg(reinterpret_cast<const float4*>(S0 + (int64_t)row * kGdnHd + cc * kGdnCols) + c4);
+  {
+    // the state tile: every thread's loads in flight before its stores
+    constexpr int kIt = kGdnHd * kGdnCols / 4 / kGdnThreads;
+    static_assert(kIt * kGdnThreads * 4 == kGdnHd * kGdnCols, "whole float4 per thread");
+    float4 v[kIt];
+#pragma unroll
+    for (int u = 0; u < kIt; u++) {
+      const int e = tid + u * kGdnThreads, row = e / (kGdnCols / 4), c4 = e % (kGdnCols / 4);
+      v[u] = __ldcg(reinterpret_cast<const float4*>(S0 + (int64_t)row * kGdnHd + cc * kGdnCols) + c4);
+    }
+#pragma unroll
+    for (int u = 0; u < kIt; u++) {
+      const int e = tid + u * kGdnThreads, row = e / (kGdnCols / 4), c4 = e % (kGdnCols / 4);
+      *reinterpret_cast<float4*>(&s.s0[row][4 * c4]) = v[u];
+    }
   }
   const int node0 = a.cu[r], M = a.cu[r + 1] - node0;
   // the parents and gates of the request, all loads at once (the serial
@@ -106,35 +117,59 @@ __global__ void __launch_bounds__(kGdnThreads, 1) k_gdn_tree(GdnArgs a) {
   __syncthreads();
   if (!s.ok) return;
 
-  // normalised q and k (x / ||x||, zero stays zero), one warp per node
-  for (int i = warp; i < M; i += kWarps) {
-    const int64_t row = ((int64_t)(node0 + i) * nh + h) * kGdnHd;
-    float qv[4], kv[4], sq = 0.f, sk = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-      qv[j] = bf2f(a.q[row + lane + 32 * j]);
-      kv[j] = bf2f(a.k[row + lane + 32 * j]);
-      sq = fmaf(qv[j], qv[j], sq);
-      sk = fmaf(kv[j], kv[j], sk);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      sk += __shfl_xor_sync(0xffffffffu, sk, o);
-    }
-    const float nq = sqrtf(sq), nk = sqrtf(sk);
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-      s.qn[i][lane + 32 * j] = nq > 0.f ? qv[j] / nq : 0.f;
-      s.kn[i][lane + 32 * j] = nk > 0.f ? kv[j] / nk : 0.f;
-    }
-    if (lane == 0) s.b[i] = a.beta[(int64_t)(node0 + i) * nh + h];
-  }
   // this CTA's value columns of every node, staged in u (the solve below
-  // overwrites each row with its result)
-  for (int e = tid; e < M * kGdnCols; e += kGdnThreads) {
-    const int i = e / kGdnCols, c = e % kGdnCols;
-    s.u[i][c] = bf2f(a.v[((int64_t)(node0 + i) * nh + h) * kGdnHd + cc * kGdnCols + c]);
+  // overwrites each row with its result); loads before stores
+  {
+    constexpr int kIt = kGdnMaxM * kGdnCols / kGdnThreads;
+    uint16_t vv[kIt];
+#pragma unroll
+    for (int u = 0; u < kIt; u++) {
+      const int e = tid + u * kGdnThreads, i = e / kGdnCols, c = e % kGdnCols;
+      vv[u] = i < M ? a.v[((int64_t)(node0 + i) * nh + h) * kGdnHd + cc * kGdnCols + c] : (uint16_t)0;
+    }
+#pragma unroll
+    for (int u = 0; u < kIt; u++) {
+      const int e = tid + u * kGdnThreads, i = e / kGdnCols, c = e % kGdnCols;
+      if (i < M) s.u[i][c] = bf2f(vv[u]);
+    }
+  }
+  // normalised q and k (x / ||x||, zero stays zero), one warp per node, a
+  // warp's two nodes' loads in flight together
+  for (int i0 = warp; i0 < M; i0 += 2 * kWarps) {
+    float qv[2][4], kv[2][4];
+#pragma unroll
+    for (int t = 0; t < 2; t++) {
+      const int i = i0 + t * kWarps;
+      const int64_t row = ((int64_t)(node0 + (i < M ? i : i0)) * nh + h) * kGdnHd;
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        qv[t][j] = bf2f(a.q[row + lane + 32 * j]);
+        kv[t][j] = bf2f(a.k[row + lane + 32 * j]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 2; t++) {
+      const int i = i0 + t * kWarps;
+      if (i >= M) break;
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        sq = fmaf(qv[t][j], qv[t][j], sq);
+        sk = fmaf(kv[t][j], kv[t][j], sk);
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+      }
+      const float nq = sqrtf(sq), nk = sqrtf(sk);
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        s.qn[i][lane + 32 * j] = nq > 0.f ? qv[t][j] / nq : 0.f;
+        s.kn[i][lane + 32 * j] = nk > 0.f ? kv[t][j] / nk : 0.f;
+      }
+      if (lane == 0) s.b[i] = a.beta[(int64_t)(node0 + i) * nh + h];
+    }
   }
   if (tid == 0) {
     // path products of the gates, root first (G_i = alpha_i G_parent), in
@@ -275,12 +310,29 @@ __global__ void __launch_bounds__(kGdnThreads) k_gdn_commit(const int32_t* __res
   __syncthreads();
   const float G = ws_g[(int64_t)(node0 + path[P - 1]) * nh + h];
   float* Sh = S + ((int64_t)r * nh + h) * kGdnHd * kGdnHd;
-  for (int e = threadIdx.x; e < kGdnCommitRows * kGdnHd; e += blockDim.x) {
-    const int x = e / kGdnHd, c = e % kGdnHd;
-    float acc = Sh[(int64_t)(rb * kGdnCommitRows + x) * kGdnHd + c];
-    for (int pi = 0; pi < P; pi++)
-      acc = fmaf(kp[pi][x], ws_d[((int64_t)(node0 + path[pi]) * nh + h) * kGdnHd + c], acc);
-    Sh[(int64_t)(rb * kGdnCommitRows + x) * kGdnHd + c] = G * acc;
+  // the thread's state elements: all loads before the first store (a store
+  // to S could alias a later load of it, so one element at a time would wait
+  // one round trip each)
+  constexpr int kIt = kGdnCommitRows * kGdnHd / kGdnThreads;
+  static_assert(kIt * kGdnThreads == kGdnCommitRows * kGdnHd, "whole elements per thread");
+  float acc[kIt];
+#pragma unroll
+  for (int u = 0; u < kIt; u++) {
+    const int e = threadIdx.x + u * kGdnThreads, x = e / kGdnHd, c = e % kGdnHd;
+    acc[u] = Sh[(int64_t)(rb * kGdnCommitRows + x) * kGdnHd + c];
+  }
+  for (int pi = 0; pi < P; pi++) {
+    const float* dp = ws_d + ((int64_t)(node0 + path[pi]) * nh + h) * kGdnHd;
+#pragma unroll
+    for (int u = 0; u < kIt; u++) {
+      const int e = threadIdx.x + u * kGdnThreads, x = e / kGdnHd, c = e % kGdnHd;
+      acc[u] = fmaf(kp[pi][x], dp[c], acc[u]);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kIt; u++) {
+    const int e = threadIdx.x + u * kGdnThreads, x = e / kGdnHd, c = e % kGdnHd;
+    Sh[(int64_t)(rb * kGdnCommitRows + x) * kGdnHd + c] = G * acc[u];
   }
 }
 
