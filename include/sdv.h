@@ -718,10 +718,10 @@ enum {
  * kernel group of a step is bracketed by CUDA events on the call's stream and
  * the step is launched directly (no graph) behind a 30 ms busy-wait kernel,
  * so that the host has queued the whole step before the GPU reaches it and
- * host launch gaps do not enter the times.  The events serialise kernels that
- * would otherwise overlap through programmatic dependent launch, so timed
- * steps are slower than untimed ones; use the numbers for the breakdown,
- * not the step time. */
+ * host launch gaps do not enter the times.  The kernels launch without
+ * programmatic dependent launch in this mode, each alone between its events,
+ * so timed steps are slower than untimed ones; use the numbers for the
+ * breakdown, not the step time. */
 int sd_model_set_timing(sd_model* m, int32_t enable);
 
 /* Timeline of the last timed call: for entry i, kind_host[i] (SD_K_*),

@@ -136,7 +136,11 @@ static double gemm_bytes(const w12_tensor& W, int rows, int epi) {
 }
 
 static int run_step(sd_model* m, const StepIO& io, cudaStream_t s) {
-  const bool pdl = true;
+  // programmatic dependent launch between the step's kernels, except in the
+  // per-kernel timing pass: there each kernel runs alone between its events
+  // (with the attribute a kernel could start inside its predecessor's
+  // bracket, and its own time would depend on its neighbours)
+  const bool pdl = !m->timing;
   int launches = 0;
   const int rows = io.rows;
   int rc;
