@@ -726,9 +726,15 @@ __device__ __forceinline__ float phi(float x) { return x > 0.f ? x + 1.0f : expf
 // phi(q), phi(k) rows padded to 129 floats: the tree dot products read
 // element d of many rows at once, which a 128-float stride puts in one bank
 constexpr int kRecFS = 129;
+// 16 warps: the output phase's per-thread chains (128 + tree terms each) are
+// its critical path at one CTA per (32 value columns, head, request); at 16
+// nodes every thread then owns one output (hybrid step, 24 recurrent layers:
+// 0.432 / 0.343 / 0.328 ms of recurrence at 4 / 8 / 16 warps)
+constexpr int kRecThreads = 512;
+constexpr int kSIt = 128 * 32 / kRecThreads;  // state-tile elements per thread
 constexpr int kRecSmem = (64 * kRecFS * 2 + 128 * 32 + 64 * 32 + 128 + 64 * 64 + 64) * 4 + 64 * 8;
 
-__global__ void __launch_bounds__(128) k_linrec(LinrecArgs a) {
+__global__ void __launch_bounds__(kRecThreads) k_linrec(LinrecArgs a) {
   pdl_launch();  // the next kernel may start streaming its (independent) weights now
   pdl_wait();
   extern __shared__ __align__(16) float smem_rec[];
@@ -746,11 +752,11 @@ __global__ void __launch_bounds__(128) k_linrec(LinrecArgs a) {
   // staging: every thread's global loads of a batch are in flight before
   // any is stored (a load-store loop waits one L2 round trip per element)
   constexpr int kB = 8;
-  for (int base = 0; base < Mr * 128; base += kB * 128) {
+  for (int base = 0; base < Mr * 128; base += kB * kRecThreads) {
     uint16_t lq[kB], lk[kB];
 #pragma unroll
     for (int u = 0; u < kB; u++) {
-      const int idx = base + u * 128 + threadIdx.x;
+      const int idx = base + u * kRecThreads + threadIdx.x;
       const int i = idx >> 7, d = idx & 127;
       const uint16_t* row = a.qkv + (int64_t)(node0 + i) * H3;
       lq[u] = idx < Mr * 128 ? row[h * 128 + d] : (uint16_t)0;
@@ -758,39 +764,39 @@ __global__ void __launch_bounds__(128) k_linrec(LinrecArgs a) {
     }
 #pragma unroll
     for (int u = 0; u < kB; u++) {
-      const int idx = base + u * 128 + threadIdx.x;
+      const int idx = base + u * kRecThreads + threadIdx.x;
       if (idx >= Mr * 128) break;
       const int i = idx >> 7, d = idx & 127;
       fq[i * kRecFS + d] = phi(bf2f(lq[u]));
       fk[i * kRecFS + d] = phi(bf2f(lk[u]));
     }
   }
-  for (int base = 0; base < Mr * 32; base += kB * 128) {
+  for (int base = 0; base < Mr * 32; base += kB * kRecThreads) {
     uint16_t lv[kB];
 #pragma unroll
     for (int u = 0; u < kB; u++) {
-      const int idx = base + u * 128 + threadIdx.x;
+      const int idx = base + u * kRecThreads + threadIdx.x;
       const int i = idx >> 5, c = idx & 31;
       lv[u] = idx < Mr * 32 ? a.qkv[(int64_t)(node0 + i) * H3 + 2 * a.H + h * 128 + cc * 32 + c] : (uint16_t)0;
     }
 #pragma unroll
     for (int u = 0; u < kB; u++) {
-      const int idx = base + u * 128 + threadIdx.x;
+      const int idx = base + u * kRecThreads + threadIdx.x;
       if (idx >= Mr * 32) break;
       sv[(idx >> 5) * 32 + (idx & 31)] = bf2f(lv[u]);
     }
   }
   const float* Sg = a.S + r * a.req_stride_S + (int64_t)h * 128 * 128;
   const float* zg = a.z + r * a.req_stride_z + (int64_t)h * 128;
-  for (int base = 0; base < 128 * 32; base += 16 * 128) {
-    float ls[16];
+  for (int base = 0; base < 128 * 32; base += kSIt * kRecThreads) {
+    float ls[kSIt];
 #pragma unroll
-    for (int u = 0; u < 16; u++) {
-      const int idx = base + u * 128 + threadIdx.x;
+    for (int u = 0; u < kSIt; u++) {
+      const int idx = base + u * kRecThreads + threadIdx.x;
       ls[u] = Sg[(idx >> 5) * 128 + cc * 32 + (idx & 31)];
     }
 #pragma unroll
-    for (int u = 0; u < 16; u++) sS[base + u * 128 + threadIdx.x] = ls[u];
+    for (int u = 0; u < kSIt; u++) sS[base + u * kRecThreads + threadIdx.x] = ls[u];
   }
   for (int k = threadIdx.x; k < 128; k += blockDim.x) sz[k] = zg[k];
   for (int i = threadIdx.x; i < Mr; i += blockDim.x) sanc[i] = a.anc[node0 + i];
@@ -830,7 +836,7 @@ cudaError_t launch_linrec(const LinrecArgs& a, cudaStream_t s, bool pdl) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch(k_linrec, dim3(4, a.nh, a.R), dim3(128), kRecSmem, s, pdl, a);
+  return launch(k_linrec, dim3(4, a.nh, a.R), dim3(kRecThreads), kRecSmem, s, pdl, a);
 }
 
 // --------------------------------------------------- argmax + accept -----
