@@ -28,7 +28,12 @@ namespace sdv {
 
 constexpr int kGdnMaxM = 64;
 constexpr int kGdnCols = 32;       // value columns per CTA
-constexpr int kGdnThreads = 256;
+// 16 warps in the verify kernel: its output phases give each thread one
+// (node, column) chain at 16 nodes (1 x 16: 16.8 -> 15.2 us, 8 x 16: 108.5
+// -> 98.4 us against 8 warps); 8 warps in the commit (at 32 x 8 its 16-warp
+// form measured slower)
+constexpr int kGdnThreads = 512;
+constexpr int kGdnCommitThreads = 256;
 constexpr int kGdnHd = 128;
 
 struct GdnArgs {
@@ -268,7 +273,7 @@ __global__ void __launch_bounds__(kGdnThreads, 1) k_gdn_tree(GdnArgs a) {
 // (a rejected tree) keeps its state.
 constexpr int kGdnCommitRows = 16;
 
-__global__ void __launch_bounds__(kGdnThreads) k_gdn_commit(const int32_t* __restrict__ parents,
+__global__ void __launch_bounds__(kGdnCommitThreads) k_gdn_commit(const int32_t* __restrict__ parents,
                                                             const int32_t* __restrict__ cu, int nh,
                                                             const int32_t* __restrict__ last, float* S,
                                                             const float* __restrict__ ws_d,
@@ -313,25 +318,25 @@ __global__ void __launch_bounds__(kGdnThreads) k_gdn_commit(const int32_t* __res
   // the thread's state elements: all loads before the first store (a store
   // to S could alias a later load of it, so one element at a time would wait
   // one round trip each)
-  constexpr int kIt = kGdnCommitRows * kGdnHd / kGdnThreads;
-  static_assert(kIt * kGdnThreads == kGdnCommitRows * kGdnHd, "whole elements per thread");
+  constexpr int kIt = kGdnCommitRows * kGdnHd / kGdnCommitThreads;
+  static_assert(kIt * kGdnCommitThreads == kGdnCommitRows * kGdnHd, "whole elements per thread");
   float acc[kIt];
 #pragma unroll
   for (int u = 0; u < kIt; u++) {
-    const int e = threadIdx.x + u * kGdnThreads, x = e / kGdnHd, c = e % kGdnHd;
+    const int e = threadIdx.x + u * kGdnCommitThreads, x = e / kGdnHd, c = e % kGdnHd;
     acc[u] = Sh[(int64_t)(rb * kGdnCommitRows + x) * kGdnHd + c];
   }
   for (int pi = 0; pi < P; pi++) {
     const float* dp = ws_d + ((int64_t)(node0 + path[pi]) * nh + h) * kGdnHd;
 #pragma unroll
     for (int u = 0; u < kIt; u++) {
-      const int e = threadIdx.x + u * kGdnThreads, x = e / kGdnHd, c = e % kGdnHd;
+      const int e = threadIdx.x + u * kGdnCommitThreads, x = e / kGdnHd, c = e % kGdnHd;
       acc[u] = fmaf(kp[pi][x], dp[c], acc[u]);
     }
   }
 #pragma unroll
   for (int u = 0; u < kIt; u++) {
-    const int e = threadIdx.x + u * kGdnThreads, x = e / kGdnHd, c = e % kGdnHd;
+    const int e = threadIdx.x + u * kGdnCommitThreads, x = e / kGdnHd, c = e % kGdnHd;
     Sh[(int64_t)(rb * kGdnCommitRows + x) * kGdnHd + c] = G * acc[u];
   }
 }
@@ -416,7 +421,7 @@ extern "C" int sd_gdn_commit(const int32_t* parents, const int32_t* cu, const in
     return SD_ERR_WORKSPACE;
   }
   const float* ws = reinterpret_cast<const float*>(workspace);
-  SD_CK(launch(k_gdn_commit, dim3(kGdnHd / kGdnCommitRows, nh, R), dim3(kGdnThreads), 0, (cudaStream_t)stream, true,
+  SD_CK(launch(k_gdn_commit, dim3(kGdnHd / kGdnCommitRows, nh, R), dim3(kGdnCommitThreads), 0, (cudaStream_t)stream, true,
                parents, cu, nh, last, S, ws, ws + (size_t)rows * nh * kGdnHd, ws + (size_t)rows * nh * kGdnHd * 2));
   return SD_OK;
 }
