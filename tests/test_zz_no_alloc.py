@@ -58,6 +58,24 @@ def test_static_linear_matches_the_oracle(Mrows):
     assert_close(y.cpu().numpy().view(np.uint16), oracle.linear(x, W))
 
 
+def test_static_linear_at_the_lm_head_height():
+    """N = 151936 output rows (the lm_head's vocabulary; 1187 row blocks,
+    far more than CTAs): sampled rows against oracle.linear."""
+    from speculative_decoding_tree_bit_gb300 import check, lib, stream_ptr
+    from speculative_decoding_tree_bit_gb300 import model as M
+    N, K, Mrows = 151936, 1024, 16
+    W = synthetic.normal_bf16(synthetic.key(66, 0), N * K, 0.02).reshape(N, K)
+    p = M.pack(M.to_device_u16(W))
+    st = p.struct()
+    x = synthetic.normal_bf16(synthetic.key(67, 0), Mrows * K, 1.0).reshape(Mrows, K)
+    y = torch.empty((Mrows, N), dtype=torch.int16, device="cuda")
+    check(lib().sd_w12_linear_static(ctypes.byref(st), M.to_device_u16(x).data_ptr(), Mrows, y.data_ptr(),
+                                     stream_ptr()))
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(3).choice(N, 1024, replace=False))
+    assert_close(y.cpu().numpy().view(np.uint16)[:, rows], oracle.linear(x, W[rows]))
+
+
 def test_static_linear_ignores_the_tensor_core_threshold():
     """The static scratch is sized for the warp-level kernel, which the call
     runs whatever sd_gemm_set_tc_min_rows says."""
