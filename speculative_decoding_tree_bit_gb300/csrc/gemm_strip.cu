@@ -5,8 +5,8 @@
 // "SpecPilot: AI Agent Framework Boosts Speculative Decoding 10.87x for
 // Qwen3.8-27B", "(1) W12" (decode fused into the GEMM) and "Phase 0:
 // Bottleneck Analysis" (the step is a stream of weight bytes): the
-// warp-level kernel splits such GEMMs over the k dimension across 9 CTAs per
-// 128-row block, and the last CTA of a block sums the others' fp32 partials
+// warp-level kernel splits such GEMMs over the k dimension across 6-9 CTAs
+// per 128-row block, and the last CTA of a block sums the others' fp32 partials
 // from global memory before the epilogue - a chain of an acq_rel ticket and
 // dependent round trips that ends the launch 8-10 us after the other CTAs.
 // Here a CTA owns SPC (1 or 2) 16-row strips and the whole k range, so
@@ -22,10 +22,11 @@
 //    warps of a strip hold fp32 partials over disjoint k ranges; at the end
 //    the first of them sums them in shared memory in warp order
 //    (deterministic) and runs the epilogue.
-//  * Escapes: the strip's escapes are one contiguous run of the row-major
-//    side list.  The escape warp forms their correction sum (w - slot) x[m][k]
-//    per (row, m) from the activations in global memory (L2) while the
-//    consumers stream, in side-list order, and hands it to warp 0 once.
+//  * Escapes: the CTA's strips' escapes are one contiguous run of the
+//    row-major side list.  The escape warp forms their correction sum
+//    (w - slot) x[m][k] per (row, m) from the activations in global memory
+//    (L2) while the consumers stream, in side-list order, and hands it once
+//    to the first warp of each strip.
 // Results equal the warp-level kernel's up to the order of fp32 sums.
 #include <cudaTypedefs.h>
 
@@ -321,9 +322,10 @@ static int64_t g_strip_max_k = 4096;
 bool gemm_strip_eligible_setting() { return g_strip_gemm; }
 
 bool gemm_strip_eligible(const w12_tensor& W, int M, int epi) {
-  // skinny launches (at most 16 rows) of the 12-bit words whose strips fit
-  // one wave of two CTAs per SM; the argmax epilogue keeps its per-CTA
-  // partials on the warp-level kernel
+  // skinny launches (at most 16 rows, k range at most g_strip_max_k) of the
+  // 12-bit words whose strips fit one wave of two CTAs per SM at one or two
+  // strips per CTA; the argmax epilogue keeps its per-CTA partials on the
+  // warp-level kernel
   return g_strip_gemm && M >= 1 && M <= 16 && epi != EPI_LOGITS && !W.row_base && W.N % 16 == 0 && W.K % 64 == 0 &&
          W.K <= g_strip_max_k && W.N / 16 <= 4 * (int64_t)num_sms() &&
          (W.n_escapes == 0 || (W.row_ptr && W.esc_idx && W.esc_val));
@@ -342,7 +344,7 @@ int gemm_strip_launch(const w12_tensor& W, const uint16_t* x, const XMap& xm, in
   }
   StripEsc es{W.row_ptr, W.esc_idx, W.esc_val};
   // one strip per CTA while the strips fit one wave of two CTAs per SM, else
-  // two (the 8B-class q/k/v: 384 strips; the 27B-class O: 320)
+  // two (the 8B-class q/k/v: 384 strips on 192 CTAs)
   const bool two = p.NS > 2 * (int64_t)num_sms();
   cudaError_t e;
   if (NT == 1)
