@@ -79,6 +79,16 @@ def test_host_argument_checks(L):
     assert L.sd_gemm_set_tc_min_rows(129) == 129
     assert L.sd_gemm_set_tc_min_rows(0) == 65
     assert L.sd_gemm_set_tc_min_rows(-1) == 65
+    # the skinny GEMM's paths: strip-parallel on, deferred and cluster
+    # finishes off by default; < 0 only queries
+    assert L.sd_gemm_set_strip(-1) == 1
+    assert L.sd_gemm_set_deferred_finish(-1) == 0
+    assert L.sd_gemm_set_cluster_finish(-1) == 0
+    for setter, default in ((L.sd_gemm_set_strip, 1), (L.sd_gemm_set_deferred_finish, 0),
+                            (L.sd_gemm_set_cluster_finish, 0)):
+        assert setter(1 - default) == 1 - default
+        assert setter(-1) == 1 - default
+        assert setter(default) == default
     # best-first selection: argument checks run before any device work
     assert L.sd_select_workspace(0) == 0
     assert L.sd_select_workspace(1000) == 20 * 1000 + 16
