@@ -219,8 +219,13 @@ struct AttnKernelArgs {
 // the warps pair up on the same 16-row tile and each takes half of every
 // 64-key tile, so that all four warps work; a pair merges its two
 // online-softmax states in shared memory before the split's partial.
-template <int KS>
-__global__ void __launch_bounds__(128, 2) k_attn(AttnKernelArgs ka) {
+// MINB: CTAs per SM the registers are budgeted for.  KS = 1 needs its 255
+// registers (two); KS = 2 holds half the scores per warp and also compiles
+// for three without spills, which pays for grids beyond one wave of three
+// per SM (16 and 32 requests of 8-row chains: 13.2 -> 12.8 and 19.55 ->
+// 19.0 ms per step) but not below (8 requests: 8.80 -> 8.98 ms)
+template <int KS, int MINB = 2>
+__global__ void __launch_bounds__(128, MINB) k_attn(AttnKernelArgs ka) {
   constexpr int kRowTiles = 4 / KS;       // 16-row tiles per chunk
   constexpr int kChunkRows = 16 * kRowTiles;
   constexpr int kNT = 8 / KS;             // 8-key n-tiles of a warp per 64-key tile
@@ -687,15 +692,17 @@ cudaError_t launch_attention(const AttnArgs& a_in, int rows_total, cudaStream_t 
   (void)rows_total;
   AttnArgs a = a_in;
   static bool attr = false;
-  static int per_sm[2] = {-1, -1};
+  static int per_sm[3] = {-1, -1, -1};  // k_attn<1>, k_attn<2>, k_attn<2, 3>
   if (!attr) {
-    for (auto kern : {k_attn<1>, k_attn<2>}) {
+    for (auto kern : {k_attn<1>, k_attn<2>, k_attn<2, 3>}) {
       const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
       if (e != cudaSuccess) return e;
       carveout_once(reinterpret_cast<const void*>(kern));
     }
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[0], k_attn<1>, 128, kAttnSmem) != cudaSuccess) per_sm[0] = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[1], k_attn<2>, 128, kAttnSmem) != cudaSuccess) per_sm[1] = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[2], k_attn<2, 3>, 128, kAttnSmem) != cudaSuccess)
+      per_sm[2] = 0;
     attr = true;
   }
   const int rpg = attn_rows_per_group(a.hq, a.hkv, a.max_m);
@@ -710,9 +717,14 @@ cudaError_t launch_attention(const AttnArgs& a_in, int rows_total, cudaStream_t 
       g_attn_trace_used += 4 * (size_t)grid;
     }
   }
-  const AttnKernelArgs ka{a, rpg, chunks, grid <= (int64_t)per_sm[ks - 1] * num_sms() ? 1 : 0};
-  return launch(ks == 2 ? k_attn<2> : k_attn<1>, dim3(a.splits + 1, a.hkv * chunks, a.R), dim3(128), kAttnSmem, s,
-                pdl, ka);
+  // the key-split kernel budgeted for three CTAs per SM once the grid is
+  // more than one wave of three
+  const int var = ks == 1 ? 0 : (per_sm[2] >= 3 && grid > (int64_t)per_sm[2] * num_sms()) ? 2 : 1;
+  const AttnKernelArgs ka{a, rpg, chunks, grid <= (int64_t)per_sm[var] * num_sms() ? 1 : 0};
+  const dim3 g3(a.splits + 1, a.hkv * chunks, a.R);
+  if (var == 0) return launch(k_attn<1>, g3, dim3(128), kAttnSmem, s, pdl, ka);
+  if (var == 1) return launch(k_attn<2>, g3, dim3(128), kAttnSmem, s, pdl, ka);
+  return launch(k_attn<2, 3>, g3, dim3(128), kAttnSmem, s, pdl, ka);
 }
 
 // ------------------------------------------------- linear recurrence -----
