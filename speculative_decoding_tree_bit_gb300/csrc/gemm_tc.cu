@@ -49,6 +49,7 @@ constexpr int kThreads = (kDec0 + kRB) * 32;
 constexpr int kATile = 128 * 128;             // decoded block: 128 rows x 64 bf16
 constexpr int kWTile = kRB * kStripBytes;     // packed block: 8 strips x 1536 bytes
 constexpr int kSmemMax = 227 * 1024;
+constexpr int kMaxCon = 512;  // CTAs of a launch (bounds a finisher's list of contributors)
 }  // namespace tc
 
 struct TcParams {
@@ -58,7 +59,7 @@ struct TcParams {
   int tmem_cols;   // TMEM columns allocated (power of two)
   uint32_t idesc;  // instruction descriptor
   int S, SW;       // ring stages: (activation + decoded weight) tiles, packed weights
-  int off_a, off_w, off_bar, off_red, off_rows, smem;
+  int off_a, off_w, off_bar, off_red, off_rows, off_con, smem;
 };
 
 // ------------------------------------------------------- tcgen05 helpers --
@@ -293,6 +294,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   TcRows rows;
   rows.kv_off = reinterpret_cast<long long*>(smem + P.off_rows);
   rows.pos = reinterpret_cast<int*>(rows.kv_off + P.MP);
+  int* con = reinterpret_cast<int*>(smem + P.off_con);  // finisher: the others' partial slices
+  int* con_cnt = con + tc::kMaxCon;                      // [4] per-warp counts, [4] this CTA's place
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
@@ -517,16 +520,33 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
           // held)
           const int64_t c_first = udiv(((int64_t)b * KT + 1) * G - 1, p.U);
           const int64_t c_last = udiv(((int64_t)(b + 1) * KT) * G - 1, p.U);
-          auto other = [&](int64_t cc, int& csid) {  // a contributor whose partial is read
-            const int64_t cs = udiv(cc * p.U, G), ce = udiv((cc + 1) * p.U, G);
-            csid = cs < (int64_t)b * KT ? 1 : 0;  // its range began in an earlier block
-            return cs != ce && cc != (int64_t)blockIdx.x;  // empty ranges wrote no partial
-          };
+          // the others' partial slices in CTA order, con[0 .. n_oth), and
+          // k_self, how many of them precede this CTA: listed once by the 128
+          // epilogue threads (a contributor each), so that the loops below
+          // divide nothing
+          const int et = threadIdx.x - tc::kEpi0 * 32, ew = et >> 5;
           int n_oth = 0;
-          for (int64_t cc = c_first; cc <= c_last; cc++) {
-            int csid;
-            n_oth += other(cc, csid) ? 1 : 0;
+          for (int64_t w = c_first; w <= c_last; w += 128) {
+            const int64_t cc = w + et;
+            bool o = false;
+            int64_t cs = 0;
+            if (cc <= c_last) {
+              cs = udiv(cc * p.U, G);
+              o = cs != udiv((cc + 1) * p.U, G) && cc != (int64_t)blockIdx.x;  // empty ranges wrote no partial
+            }
+            const uint32_t om = __ballot_sync(0xffffffffu, o);
+            if (lane == 0) con_cnt[ew] = __popc(om);
+            bar_sync(2, 128);
+            int at = n_oth + __popc(om & ((1u << lane) - 1u));
+            for (int q = 0; q < ew; q++) at += con_cnt[q];
+            // a range that began in an earlier block left this block's share
+            // in its second slice
+            if (o) con[at] = (int)(cc * 2 + (cs < (int64_t)b * KT ? 1 : 0));
+            if (cc == (int64_t)blockIdx.x) con_cnt[4] = at;
+            n_oth += con_cnt[0] + con_cnt[1] + con_cnt[2] + con_cnt[3];
+            bar_sync(2, 128);
           }
+          const int k_self = con_cnt[4];
           // the CTA's last segment: the rings are idle (every copy consumed,
           // every MMA complete), so one thread stages the others' partial
           // slices there with bulk copies, two column groups in flight
@@ -541,14 +561,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
               const int cols = min(GC, P.MP - gi * GC);
               fence_async_smem();  // earlier generic reads of the buffer come first
               mbar_arrive_expect_tx(&gbar[gi & 1], (uint32_t)(n_oth * cols * 512));
-              int k = 0;
-              for (int64_t cc = c_first; cc <= c_last; cc++) {
-                int csid;
-                if (!other(cc, csid)) continue;
+              for (int k = 0; k < n_oth; k++)
                 bulk_g2s(stage + (int64_t)((gi & 1) * n_oth + k) * GC * 128,
-                         p.partial + ((cc * 2 + csid) * P.MP + gi * GC) * 128, (uint32_t)(cols * 512), &gbar[gi & 1]);
-                k++;
-              }
+                         p.partial + ((int64_t)con[k] * P.MP + gi * GC) * 128, (uint32_t)(cols * 512), &gbar[gi & 1]);
             };
             issue(0);
             for (int gi = 0; gi < ngroups; gi++) {
@@ -567,19 +582,17 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
                 tmem_ld16(taddr + 16 * c, own);
 #pragma unroll
                 for (int j = 0; j < 16; j++) v[j] = 0.f;
-                int k = 0;
-                for (int64_t cc = c_first; cc <= c_last; cc++) {
-                  int csid;
-                  if (cc == (int64_t)blockIdx.x) {
+                for (int k = 0; k < n_oth; k++) {
+                  if (k == k_self)
 #pragma unroll
                     for (int j = 0; j < 16; j++) v[j] += own[j];
-                  } else if (other(cc, csid)) {
-                    const float* src = sb + (int64_t)k * GC * 128 + cl * 16 * 128;
+                  const float* src = sb + (int64_t)k * GC * 128 + cl * 16 * 128;
 #pragma unroll
-                    for (int j = 0; j < 16; j++) v[j] += src[j * 128];
-                    k++;
-                  }
+                  for (int j = 0; j < 16; j++) v[j] += src[j * 128];
                 }
+                if (k_self == n_oth)
+#pragma unroll
+                  for (int j = 0; j < 16; j++) v[j] += own[j];
                 tc_emit<EPI>(P, n, 16 * c, v, red_v, red_i, quarter, rows);
               }
             }
@@ -590,24 +603,28 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
               tmem_ld16(taddr + 16 * c, own);
 #pragma unroll
               for (int j = 0; j < 16; j++) v[j] = 0.f;
-              for (int64_t c0 = c_first; c0 <= c_last; c0 += 2) {
+              for (int k0 = 0; k0 < n_oth; k0 += 2) {
                 float w[2][16];
-                bool mine[2];
 #pragma unroll
                 for (int u = 0; u < 2; u++) {
-                  const int64_t cc = c0 + u;
-                  int csid = 0;
-                  mine[u] = cc == (int64_t)blockIdx.x;
-                  const bool use = cc <= c_last && other(cc, csid);
-                  const float* src = p.partial + ((int64_t)((use ? cc : 0) * 2 + csid) * P.MP + 16 * c) * 128 + r;
+                  const bool use = k0 + u < n_oth;
+                  const float* src = p.partial + ((int64_t)(use ? con[k0 + u] : 0) * P.MP + 16 * c) * 128 + r;
 #pragma unroll
                   for (int j = 0; j < 16; j++) w[u][j] = use ? __ldcg(src + j * 128) : 0.f;
                 }
 #pragma unroll
-                for (int u = 0; u < 2; u++)
+                for (int u = 0; u < 2; u++) {
+                  if (k0 + u >= n_oth) break;
+                  if (k0 + u == k_self)
 #pragma unroll
-                  for (int j = 0; j < 16; j++) v[j] += mine[u] ? own[j] : w[u][j];
+                    for (int j = 0; j < 16; j++) v[j] += own[j];
+#pragma unroll
+                  for (int j = 0; j < 16; j++) v[j] += w[u][j];
+                }
               }
+              if (k_self == n_oth)
+#pragma unroll
+                for (int j = 0; j < 16; j++) v[j] += own[j];
               tc_emit<EPI>(P, n, 16 * c, v, red_v, red_i, quarter, rows);
             }
           }
@@ -777,7 +794,9 @@ static int tc_setup(TcParams* P, int M) {
   const int bar_bytes = 512;
   const int red_bytes = 8 * MP * 4;
   const int rows_bytes = 12 * MP;
-  const int budget = tc::kSmemMax - 1024 - bar_bytes - red_bytes - rows_bytes - P->S * (XB + tc::kATile);
+  const int con_bytes = 4 * (tc::kMaxCon + 8);
+  const int budget =
+      tc::kSmemMax - 1024 - bar_bytes - red_bytes - rows_bytes - con_bytes - P->S * (XB + tc::kATile);
   P->SW = std::min(8, budget / tc::kWTile);
   if (P->SW < 2) return SD_ERR_UNSUPPORTED;
   P->off_a = P->S * XB;
@@ -785,7 +804,8 @@ static int tc_setup(TcParams* P, int M) {
   P->off_bar = P->off_w + P->SW * tc::kWTile;
   P->off_red = P->off_bar + bar_bytes;
   P->off_rows = P->off_red + red_bytes;
-  P->smem = 1024 + P->off_rows + rows_bytes;
+  P->off_con = P->off_rows + rows_bytes;
+  P->smem = 1024 + P->off_con + con_bytes;
   return SD_OK;
 }
 
@@ -832,6 +852,10 @@ int gemm_tc_launch(const w12_tensor& W, const uint16_t* x, int rows_total, int M
     return SD_ERR_WORKSPACE;
   }
   const int grid = gemm_launch_grid(W, M, epi.epi);
+  if (grid > tc::kMaxCon) {
+    set_error("gemm: more CTAs than the tensor-core finisher lists");
+    return SD_ERR_UNSUPPORTED;
+  }
   if (ws.partial_floats < (size_t)grid * 2 * P.MP * 128) {
     set_error("gemm: workspace too small");
     return SD_ERR_WORKSPACE;
