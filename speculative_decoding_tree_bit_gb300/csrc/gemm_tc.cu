@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   rows.kv_off = reinterpret_cast<long long*>(smem + P.off_rows);
   rows.pos = reinterpret_cast<int*>(rows.kv_off + P.MP);
   int* con = reinterpret_cast<int*>(smem + P.off_con);  // finisher: the others' partial slices
-  int* con_cnt = con + tc::kMaxCon;                      // [4] per-warp counts, [4] this CTA's place
+  int* con_cnt = con + tc::kMaxCon;                      // [0..3] per-warp counts, [4] this CTA's place
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
